@@ -1,0 +1,295 @@
+/*
+ * kda_oracle.c -- plain, slow, single-threaded CPU oracle for the speculative
+ * verify walk through one Kimi-Delta-Attention (KDA) layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the CPU
+ * baseline leg of the benchmark call it; the CUDA library never does.  It
+ * shares no code, header, table or helper with the CUDA path.
+ *
+ * Precision: inputs and stored state are f32 (the pages keep the KDA state as
+ * f32: one glm5_next KDA state is 64 heads x 128 x 128 f32, glm_spec.rs module
+ * doc, ROLLBACK).  Every arithmetic step here runs in double and is rounded to
+ * f32 only where a result is stored (state, conv ring, output rows).  bf16 raw
+ * rows are widened exactly by a 16-bit left shift (dflash.rs, bf16_to_f32).
+ *
+ * What is computed, per (session, layer), for one head h and rows t = 0..T-1:
+ *   short conv (width 4, depthwise, causal) over the raw q, k, v rows, with the
+ *     3-slot ring of the previous raw inputs supplying x[t-3..t-1] for early rows,
+ *     then SiLU:  y = a * sigmoid(a),  a = w0 x[t-3] + w1 x[t-2] + w2 x[t-1] + w3 x[t]
+ *   L2 normalisation of q and k:  x_hat = y / sqrt(sum y^2 + 1e-6)
+ *   gates:  g = -5 * sigmoid(raw_g) per key channel (gate_lower_bound -5.0 in the
+ *     linear_attn_config of the mini fixture, glm5_spec_ppn_gate.rs);
+ *     beta = sigmoid(raw_beta) per head
+ *   gated delta rule on S [d_k = 128][d_v = 128]:
+ *     S' = diag(exp g) S ;  u = S'^T k_hat ;  w = beta (v - u) ;
+ *     S  = S' + k_hat w^T ;  o = S^T q_hat / sqrt(128)
+ *   ring <- the last 3 of [ring, x_0 .. x_{T-1}]            (per stream)
+ * The recurrence is sequential in t, one row at a time (glm_spec.rs module doc,
+ * VERIFY-ROW BATCHING: the in-kernel T-loop is the chained t=1 program).
+ *
+ * Greedy accept (glm_spec.rs, glm5_spec_round step 4; dflash.rs,
+ * dspark_accept_prefix): vam[r] = first index of the row maximum, j = the first
+ * r < K with drafts[r] != vam[r] (else K), bonus = vam[j]; a NaN row yields a
+ * sentinel that is refused loudly (the guard_vocab_token convention).
+ *
+ * Rollback (glm_spec.rs, glm5_verify_rollback and the KDA arm of
+ * glm5_rollback_layer): keep must lie in 1..T; keep == T leaves the state as it
+ * is; otherwise state and ring are rebuilt from the pre-round snapshot by running
+ * rows 0..keep-1 again.
+ *
+ * Layouts of one (session, layer) unit, all row-major:
+ *   raw rows q, k, v, g   [T][H][128]   (f32 or bf16 bits)
+ *   raw beta              [T][H]
+ *   conv_w                [H][3 stream: q,k,v][128][4 taps]  (tap 3 = current row)
+ *   ring                  [H][3 stream][3 slot][128]         (slot 0 = oldest)
+ *   state                 [H][128 d_k][128 d_v]
+ *   out                   [T][H][128]
+ */
+#include "kda_oracle.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define D KDAO_D
+
+/* bf16 -> f32: the 16 stored bits become the high half of an f32. */
+static double widen(const void *base, int dtype, size_t idx)
+{
+    if (dtype == KDAO_BF16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[idx];
+}
+
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+
+/* ---------------------------------------------------------------------------
+ * Activations: conv + SiLU, L2 norm, gates, ring re-roll.
+ * ------------------------------------------------------------------------- */
+int kdao_prepare(int H, int T, int dtype,
+                 const void *xq, const void *xk, const void *xv,
+                 const void *xg, const void *xb,
+                 const float *conv_w, const float *ring_in,
+                 double *q_hat, double *k_hat, double *v_out,
+                 double *g_out, double *beta_out, float *ring_out)
+{
+    if (H < 0 || T < 1 || (dtype != KDAO_F32 && dtype != KDAO_BF16))
+        return KDAO_EINVAL;
+    const void *raw[3] = {xq, xk, xv};
+    /* hist[s][n][c]: n = 0..2 the ring slots (oldest first), n = 3 + t raw row t */
+    double *hist = (double *)malloc(sizeof(double) * 3 * (size_t)(T + 3) * D);
+    double *y = (double *)malloc(sizeof(double) * 3 * (size_t)T * D);
+    if (!hist || !y) {
+        free(hist);
+        free(y);
+        return KDAO_ENOMEM;
+    }
+    for (int h = 0; h < H; ++h) {
+        for (int s = 0; s < 3; ++s) {
+            for (int n = 0; n < 3; ++n)
+                for (int c = 0; c < D; ++c)
+                    hist[((size_t)s * (T + 3) + n) * D + c] =
+                        ring_in[(((size_t)h * 3 + s) * 3 + n) * D + c];
+            for (int t = 0; t < T; ++t)
+                for (int c = 0; c < D; ++c)
+                    hist[((size_t)s * (T + 3) + 3 + t) * D + c] =
+                        widen(raw[s], dtype, ((size_t)t * H + h) * D + c);
+        }
+        /* depthwise causal conv, width 4, then SiLU */
+        for (int s = 0; s < 3; ++s)
+            for (int t = 0; t < T; ++t)
+                for (int c = 0; c < D; ++c) {
+                    const float *w = conv_w + (((size_t)h * 3 + s) * D + c) * 4;
+                    const double *x = hist + ((size_t)s * (T + 3) + t) * D + c;
+                    double a = (double)w[0] * x[0] + (double)w[1] * x[D] +
+                               (double)w[2] * x[2 * D] + (double)w[3] * x[3 * D];
+                    y[((size_t)s * T + t) * D + c] = a * sigmoid(a);
+                }
+        for (int t = 0; t < T; ++t) {
+            size_t row = ((size_t)t * H + h) * D;
+            /* L2 normalisation of q (s = 0) and k (s = 1) */
+            for (int s = 0; s < 2; ++s) {
+                const double *ys = y + ((size_t)s * T + t) * D;
+                double ss = 0.0;
+                for (int c = 0; c < D; ++c)
+                    ss += ys[c] * ys[c];
+                double r = 1.0 / sqrt(ss + KDAO_L2_EPS);
+                double *dst = (s == 0) ? q_hat : k_hat;
+                for (int c = 0; c < D; ++c)
+                    dst[row + c] = ys[c] * r;
+            }
+            for (int c = 0; c < D; ++c)
+                v_out[row + c] = y[((size_t)2 * T + t) * D + c];
+            /* forget gate per key channel, write strength per head */
+            for (int c = 0; c < D; ++c)
+                g_out[row + c] = KDAO_GATE_LOWER_BOUND * sigmoid(widen(xg, dtype, row + c));
+            beta_out[(size_t)t * H + h] = sigmoid(widen(xb, dtype, (size_t)t * H + h));
+        }
+        /* ring <- the last three raw inputs of each stream */
+        if (ring_out)
+            for (int s = 0; s < 3; ++s)
+                for (int n = 0; n < 3; ++n)
+                    for (int c = 0; c < D; ++c)
+                        ring_out[(((size_t)h * 3 + s) * 3 + n) * D + c] =
+                            (float)hist[((size_t)s * (T + 3) + T + n) * D + c];
+    }
+    free(hist);
+    free(y);
+    return KDAO_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * The gated delta rule, row by row, on post-activation inputs.
+ * S is [H][d_k][d_v] in double, updated in place; out [T][H][d_v] may be NULL.
+ * ------------------------------------------------------------------------- */
+int kdao_core(int H, int T, const double *q_hat, const double *k_hat,
+              const double *v, const double *g, const double *beta,
+              double *S, double *out)
+{
+    if (H < 0 || T < 0)
+        return KDAO_EINVAL;
+    const double scale = 1.0 / sqrt((double)D);
+    double u[D], w[D];
+    for (int t = 0; t < T; ++t) {
+        for (int h = 0; h < H; ++h) {
+            size_t row = ((size_t)t * H + h) * D;
+            const double *q = q_hat + row, *k = k_hat + row, *vv = v + row, *gg = g + row;
+            double b = beta[(size_t)t * H + h];
+            double *Sh = S + (size_t)h * D * D;
+            /* S' = diag(exp g) S : row i of S (key channel i) decays by exp(g_i) */
+            for (int i = 0; i < D; ++i) {
+                double d = exp(gg[i]);
+                for (int j = 0; j < D; ++j)
+                    Sh[i * D + j] *= d;
+            }
+            /* u = S'^T k */
+            for (int j = 0; j < D; ++j) {
+                double acc = 0.0;
+                for (int i = 0; i < D; ++i)
+                    acc += Sh[i * D + j] * k[i];
+                u[j] = acc;
+            }
+            /* w = beta (v - u) */
+            for (int j = 0; j < D; ++j)
+                w[j] = b * (vv[j] - u[j]);
+            /* S = S' + k w^T */
+            for (int i = 0; i < D; ++i)
+                for (int j = 0; j < D; ++j)
+                    Sh[i * D + j] += k[i] * w[j];
+            /* o = S^T q / sqrt(d_k) */
+            if (out)
+                for (int j = 0; j < D; ++j) {
+                    double acc = 0.0;
+                    for (int i = 0; i < D; ++i)
+                        acc += Sh[i * D + j] * q[i];
+                    out[row + j] = acc * scale;
+                }
+        }
+    }
+    return KDAO_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * One verify launch for one (session, layer): T rows from state_in/ring_in.
+ * state_out / ring_out receive the state after row T-1 (f32); out the T rows.
+ * ------------------------------------------------------------------------- */
+int kdao_verify(int H, int T, int dtype,
+                const void *xq, const void *xk, const void *xv,
+                const void *xg, const void *xb,
+                const float *conv_w, const float *ring_in, const float *state_in,
+                float *ring_out, float *state_out, float *out)
+{
+    if (H < 0 || T < 1 || T > KDAO_TMAX)
+        return KDAO_EINVAL;
+    size_t nrow = (size_t)T * H * D, nst = (size_t)H * D * D;
+    double *q = (double *)malloc(sizeof(double) * nrow + 1);
+    double *k = (double *)malloc(sizeof(double) * nrow + 1);
+    double *v = (double *)malloc(sizeof(double) * nrow + 1);
+    double *g = (double *)malloc(sizeof(double) * nrow + 1);
+    double *b = (double *)malloc(sizeof(double) * (size_t)T * H + 1);
+    double *S = (double *)malloc(sizeof(double) * nst + 1);
+    double *o = (double *)malloc(sizeof(double) * nrow + 1);
+    int rc = KDAO_ENOMEM;
+    if (q && k && v && g && b && S && o) {
+        rc = kdao_prepare(H, T, dtype, xq, xk, xv, xg, xb, conv_w, ring_in, q, k, v, g, b,
+                          ring_out);
+        if (rc == KDAO_OK) {
+            for (size_t n = 0; n < nst; ++n)
+                S[n] = (double)state_in[n];
+            rc = kdao_core(H, T, q, k, v, g, b, S, o);
+        }
+        if (rc == KDAO_OK) {
+            for (size_t n = 0; n < nst; ++n)
+                state_out[n] = (float)S[n];
+            if (out)
+                for (size_t n = 0; n < nrow; ++n)
+                    out[n] = (float)o[n];
+        }
+    }
+    free(q);
+    free(k);
+    free(v);
+    free(g);
+    free(b);
+    free(S);
+    free(o);
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * Accept-j rollback for one (session, layer).  T is the row count of the round
+ * the snapshots belong to; the raw rows are that round's [T][H][128] rows.
+ * ------------------------------------------------------------------------- */
+int kdao_rollback(int H, int T, int keep, int dtype,
+                  const void *xq, const void *xk, const void *xv,
+                  const void *xg, const void *xb, const float *conv_w,
+                  const float *ring_snap, const float *state_snap,
+                  const float *ring_cur, const float *state_cur,
+                  float *ring_out, float *state_out)
+{
+    if (keep < 1 || keep > T)
+        return KDAO_EINVAL;
+    if (keep == T) {
+        /* the resident state is the state after the last kept row */
+        memmove(state_out, state_cur, sizeof(float) * (size_t)H * D * D);
+        memmove(ring_out, ring_cur, sizeof(float) * (size_t)H * 3 * 3 * D);
+        return KDAO_OK;
+    }
+    return kdao_verify(H, keep, dtype, xq, xk, xv, xg, xb, conv_w, ring_snap, state_snap,
+                       ring_out, state_out, NULL);
+}
+
+/* ---------------------------------------------------------------------------
+ * Greedy accept for one session: logits [T][V], drafts [T-1].
+ * ------------------------------------------------------------------------- */
+int kdao_accept(int T, int V, int dtype, const void *logits, const int *drafts,
+                int *vam, int *j_out, int *bonus_out)
+{
+    if (T < 1 || V < 1 || (dtype != KDAO_F32 && dtype != KDAO_BF16))
+        return KDAO_EINVAL;
+    for (int r = 0; r < T; ++r) {
+        int best = 0, nan_row = 0;
+        double bv = widen(logits, dtype, (size_t)r * V);
+        for (int c = 0; c < V; ++c) {
+            double x = widen(logits, dtype, (size_t)r * V + c);
+            if (isnan(x))
+                nan_row = 1;
+            else if (isnan(bv) || x > bv) {
+                bv = x;
+                best = c;
+            }
+        }
+        vam[r] = nan_row ? KDAO_SENTINEL : best;
+    }
+    int K = T - 1, j = 0;
+    while (j < K && vam[j] != KDAO_SENTINEL && drafts[j] == vam[j])
+        ++j;
+    *j_out = j;
+    *bonus_out = vam[j];
+    return vam[j] == KDAO_SENTINEL ? KDAO_ENAN : KDAO_OK;
+}

@@ -1,0 +1,434 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``pin_*`` takes a loaded oracle and raises AssertionError when it is wrong.
+The checks are closed forms, invariants, special cases that reduce to library
+routines, brute force on tiny inputs in an independent formulation (the matrix
+form of the recurrence, ``np.correlate`` for the conv, sorting for the argmax),
+and the values printed on the pages (``tests/golden``).  The mutation test runs
+every pin against deliberately broken copies of the oracle and requires each
+copy to fail at least one of them.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+from scipy.special import expit
+
+D = 128
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+# ---------------------------------------------------------------------------
+# independent helpers (numpy / scipy, no oracle code)
+# ---------------------------------------------------------------------------
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+def _unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _post_inputs(rng, T, H, g_lo=-5.0):
+    q = _unit(rng.standard_normal((T, H, D)))
+    k = _unit(rng.standard_normal((T, H, D)))
+    v = rng.standard_normal((T, H, D))
+    g = rng.uniform(g_lo, 0.0, (T, H, D))
+    beta = rng.uniform(0.05, 0.95, (T, H))
+    S = 0.01 * rng.standard_normal((H, D, D))
+    return q, k, v, g, beta, S
+
+
+def matrix_form(q, k, v, g, beta, S0):
+    """S_t = (I - beta k k^T) diag(exp g) S_{t-1} + beta k v^T ; o_t = S_t^T q / sqrt(128)."""
+    T, H = q.shape[0], q.shape[1]
+    S = S0.copy()
+    out = np.empty((T, H, D))
+    eye = np.eye(D)
+    for t in range(T):
+        for h in range(H):
+            kk = k[t, h][:, None]
+            A = (eye - beta[t, h] * kk @ kk.T) @ np.diag(np.exp(g[t, h]))
+            S[h] = A @ S[h] + beta[t, h] * kk @ v[t, h][None, :]
+            out[t, h] = S[h].T @ q[t, h] / math.sqrt(D)
+    return S, out
+
+
+def silu(x):
+    return x * expit(x)
+
+
+def _raw_inputs(rng, T, H):
+    xq, xk, xv, xg = (rng.standard_normal((T, H, D)).astype(np.float32) for _ in range(4))
+    xb = rng.standard_normal((T, H)).astype(np.float32)
+    conv_w = rng.uniform(-0.5, 0.5, (H, 3, D, 4)).astype(np.float32)
+    ring = (0.1 * rng.standard_normal((H, 3, 3, D))).astype(np.float32)
+    state = (0.01 * rng.standard_normal((H, D, D))).astype(np.float32)
+    return xq, xk, xv, xg, xb, conv_w, ring, state
+
+
+def brute_verify(xq, xk, xv, xg, xb, conv_w, ring, state):
+    """The whole verify of one unit from library routines, in float64."""
+    T, H = xq.shape[0], xq.shape[1]
+    raw = [xq.astype(np.float64), xk.astype(np.float64), xv.astype(np.float64)]
+    y = np.empty((3, T, H, D))
+    for s in range(3):
+        for h in range(H):
+            for c in range(D):
+                seq = np.concatenate([ring[h, s, :, c].astype(np.float64), raw[s][:, h, c]])
+                # correlate(seq, w, 'valid')[t] = sum_m seq[t+m] w[m]: tap 3 meets row t
+                y[s, :, h, c] = silu(np.correlate(seq, conv_w[h, s, c].astype(np.float64), "valid"))
+    q = y[0] / np.sqrt((y[0] ** 2).sum(-1, keepdims=True) + 1e-6)
+    k = y[1] / np.sqrt((y[1] ** 2).sum(-1, keepdims=True) + 1e-6)
+    g = -5.0 * expit(xg.astype(np.float64))
+    beta = expit(xb.astype(np.float64))
+    S, out = matrix_form(q, k, y[2], g, beta, state.astype(np.float64))
+    ring_out = np.empty_like(ring)
+    for s in range(3):
+        seq = np.concatenate([ring[:, s].transpose(1, 0, 2), raw[s].astype(np.float32)], axis=0)
+        ring_out[:, s] = seq[-3:].transpose(1, 0, 2)
+    return S, out, ring_out
+
+
+def _close(a, b, rtol, atol, what):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    err = np.abs(a - b) - (atol + rtol * np.abs(b))
+    assert np.all(err <= 0), f"{what}: max excess {err.max():.3e}"
+
+
+# ---------------------------------------------------------------------------
+# the recurrence (core entry)
+# ---------------------------------------------------------------------------
+def pin_core_matrix_form(orc):
+    """Brute force in the matrix form, tiny inputs, several heads and rows."""
+    rng = _rng(11)
+    for T, H in ((1, 1), (5, 2), (8, 1)):
+        q, k, v, g, beta, S0 = _post_inputs(rng, T, H)
+        S, out = orc.core(q, k, v, g, beta, S0)
+        Sb, outb = matrix_form(q, k, v, g, beta, S0)
+        _close(S, Sb, 1e-12, 1e-14, "state vs matrix form")
+        _close(out, outb, 1e-11, 1e-14, "out vs matrix form")
+
+
+def pin_core_closed_form_first_write(orc):
+    """From S = 0 one row gives S = beta k v^T and o = beta (q.k) v / sqrt(128)."""
+    rng = _rng(12)
+    q, k, v, g, beta, _ = _post_inputs(rng, 1, 3)
+    S, out = orc.core(q, k, v, g, beta, np.zeros((3, D, D)))
+    for h in range(3):
+        _close(S[h], beta[0, h] * np.outer(k[0, h], v[0, h]), 1e-13, 1e-15, "S closed form")
+        o = beta[0, h] * float(q[0, h] @ k[0, h]) * v[0, h] / math.sqrt(D)
+        _close(out[0, h], o, 1e-12, 1e-15, "o closed form")
+
+
+def pin_core_identity(orc):
+    """beta = 0 and g = 0 leave S unchanged, bit for bit."""
+    rng = _rng(13)
+    q, k, v, _, _, S0 = _post_inputs(rng, 6, 2)
+    S, _ = orc.core(q, k, v, np.zeros_like(q), np.zeros((6, 2)), S0)
+    assert np.array_equal(S, S0), "beta=0, g=0 must leave the state unchanged"
+
+
+def pin_core_orthonormal_writes(orc):
+    """g = 0, beta = 1 and orthonormal keys: afterwards S^T k_t = v_t for every row t."""
+    rng = _rng(14)
+    T = 7
+    basis, _ = np.linalg.qr(rng.standard_normal((D, D)))
+    k = basis[:, :T].T.reshape(T, 1, D)
+    q = _unit(rng.standard_normal((T, 1, D)))
+    v = rng.standard_normal((T, 1, D))
+    S0 = 0.01 * rng.standard_normal((1, D, D))
+    S, _ = orc.core(q, k, v, np.zeros((T, 1, D)), np.ones((T, 1)), S0)
+    for t in range(T):
+        _close(S[0].T @ k[t, 0], v[t, 0], 1e-12, 1e-12, f"read back row {t}")
+    # the part of S orthogonal to every written key is untouched
+    P = np.eye(D) - k[:, 0].T @ k[:, 0]
+    _close(P @ S[0], P @ S0[0], 1e-12, 1e-14, "orthogonal complement")
+
+
+def pin_core_decay_only(orc):
+    """beta = 0: S_T = diag(exp(sum_t g_t)) S_0 and o_t = S_t^T q_t / sqrt(128)."""
+    rng = _rng(15)
+    q, k, v, g, _, S0 = _post_inputs(rng, 5, 2)
+    S, out = orc.core(q, k, v, g, np.zeros((5, 2)), S0)
+    for h in range(2):
+        _close(S[h], np.exp(g[:, h].sum(0))[:, None] * S0[h], 1e-13, 1e-16, "pure decay")
+        St = S0[h].copy()
+        for t in range(5):
+            St = np.exp(g[t, h])[:, None] * St
+            _close(out[t, h], St.T @ q[t, h] / math.sqrt(D), 1e-12, 1e-16, "decay-only output")
+
+
+# ---------------------------------------------------------------------------
+# activations (prepare entry)
+# ---------------------------------------------------------------------------
+def _taps(H, tap):
+    w = np.zeros((H, 3, D, 4), np.float32)
+    w[..., tap] = 1.0
+    return w
+
+
+def pin_prepare_current_tap(orc):
+    """Weights [0,0,0,1]: the conv is the identity, so v = SiLU(x) and q, k are SiLU(x)/norm."""
+    rng = _rng(21)
+    xq, xk, xv, xg, xb, _, ring, _ = _raw_inputs(rng, 4, 2)
+    q, k, v, g, b, _ = orc.prepare(xq, xk, xv, xg, xb, _taps(2, 3), ring)
+    _close(v, silu(xv.astype(np.float64)), 1e-15, 1e-300, "v = SiLU(x)")
+    for got, x in ((q, xq), (k, xk)):
+        y = silu(x.astype(np.float64))
+        n = (y ** 2).sum(-1, keepdims=True)
+        _close((got ** 2).sum(-1, keepdims=True), n / (n + 1e-6), 1e-14, 0, "|x_hat|^2 = n/(n+eps)")
+        _close(got * np.linalg.norm(y, axis=-1, keepdims=True), y * np.sqrt(n / (n + 1e-6)),
+               1e-13, 1e-15, "x_hat parallel to SiLU(x)")
+
+
+def pin_prepare_shifted_taps(orc):
+    """Weights with one tap m pick x[t-3+m]: the ring supplies the rows before row 0, oldest first."""
+    rng = _rng(22)
+    T, H = 5, 2
+    xq, xk, xv, xg, xb, _, ring, _ = _raw_inputs(rng, T, H)
+    for m in range(3):
+        _, _, v, _, _, _ = orc.prepare(xq, xk, xv, xg, xb, _taps(H, m), ring)
+        seq = np.concatenate([ring[:, 2].transpose(1, 0, 2), xv], axis=0)  # [3+T][H][D]
+        _close(v, silu(seq[m:m + T].astype(np.float64)), 1e-15, 1e-300, f"tap {m}")
+
+
+def pin_prepare_vs_correlate(orc):
+    """Random weights: the conv equals np.correlate over [ring, rows]."""
+    rng = _rng(23)
+    T, H = 6, 2
+    xq, xk, xv, xg, xb, conv_w, ring, _ = _raw_inputs(rng, T, H)
+    _, _, v, _, _, _ = orc.prepare(xq, xk, xv, xg, xb, conv_w, ring)
+    for h in range(H):
+        for c in (0, 17, 127):
+            seq = np.concatenate([ring[h, 2, :, c], xv[:, h, c]]).astype(np.float64)
+            a = np.correlate(seq, conv_w[h, 2, c].astype(np.float64), "valid")
+            _close(v[:, h, c], silu(a), 1e-14, 1e-16, "conv vs correlate")
+
+
+def pin_prepare_gates(orc):
+    """g = -5 sigmoid(raw): raw 0 -> -2.5, raw -inf -> 0 (no decay), raw +inf -> -5; beta likewise."""
+    T, H = 3, 2
+    z = np.zeros((T, H, D), np.float32)
+    xg = np.zeros((T, H, D), np.float32)
+    xg[1] = -np.inf
+    xg[2] = np.inf
+    xb = np.array([[0.0, -np.inf], [np.inf, 0.0], [2.0, -2.0]], np.float32)
+    _, _, _, g, b, _ = orc.prepare(z, z, z, xg, xb, _taps(H, 3), np.zeros((H, 3, 3, D), np.float32))
+    assert np.all(g[0] == -2.5) and np.all(g[1] == 0.0) and np.all(g[2] == -5.0), "gate specials"
+    _close(b, [[0.5, 0.0], [1.0, 0.5], [expit(2.0), expit(-2.0)]], 1e-15, 0, "beta = sigmoid")
+    rng = _rng(24)
+    xg = rng.standard_normal((T, H, D)).astype(np.float32)
+    _, _, _, g, _, _ = orc.prepare(z, z, z, xg, xb, _taps(H, 3), np.zeros((H, 3, 3, D), np.float32))
+    _close(g, -5.0 * expit(xg.astype(np.float64)), 1e-15, 0, "g = -5 expit")
+
+
+def pin_prepare_ring_reroll(orc):
+    """ring_out = the last 3 raw inputs of [ring, x_0..x_{T-1}] per stream, for T = 1, 2, 3, 7."""
+    rng = _rng(25)
+    H = 2
+    for T in (1, 2, 3, 7):
+        xq, xk, xv, xg, xb, conv_w, ring, _ = _raw_inputs(rng, T, H)
+        *_, ring_out = orc.prepare(xq, xk, xv, xg, xb, conv_w, ring)
+        for s, x in enumerate((xq, xk, xv)):
+            seq = np.concatenate([ring[:, s].transpose(1, 0, 2), x], axis=0)
+            assert np.array_equal(ring_out[:, s], seq[-3:].transpose(1, 0, 2)), f"ring T={T} s={s}"
+
+
+def _golden_bf16():
+    rows = []
+    with open(os.path.join(GOLDEN, "bf16_widen.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                bits, val = line.split()
+                rows.append((int(bits, 16), float(val)))
+    return rows
+
+
+def pin_bf16_widening(orc):
+    """bf16 rows widen exactly (tests/golden/bf16_widen.txt); checked through v = SiLU(x)."""
+    rows = _golden_bf16()
+    bits = np.array([b for b, _ in rows], np.uint16)
+    vals = np.array([v for _, v in rows], np.float64)
+    H = 1
+    xv = np.zeros((1, H, D), np.uint16)
+    xv[0, 0, : len(bits)] = bits
+    z = np.zeros((1, H, D), np.uint16)
+    _, _, v, _, _, _ = orc.prepare(z, z, xv, z, np.zeros((1, H), np.uint16), _taps(H, 3),
+                                   np.zeros((H, 3, 3, D), np.float32))
+    got = v[0, 0, : len(bits)]
+    fin = np.isfinite(vals)
+    assert np.array_equal(got[fin], silu(vals[fin])), "bf16 widening"
+    assert np.isinf(got[~fin]).all()
+    # (the sign of a zero does not survive the conv sum 0 + (-0) = +0, so -0.0 is
+    # checked by value only here; the accept pins compare -0.0 with +0.0 directly)
+
+
+# ---------------------------------------------------------------------------
+# the whole verify, rollback
+# ---------------------------------------------------------------------------
+def pin_verify_brute_force(orc):
+    """The full unit verify equals the library-routine brute force (conv, SiLU, norm, gates, matrix form)."""
+    rng = _rng(31)
+    for T, H in ((1, 1), (4, 2), (8, 1)):
+        args = _raw_inputs(rng, T, H)
+        st, ring_out, out = orc.verify(*args)
+        Sb, outb, ringb = brute_verify(*args)
+        _close(st, Sb, 2e-7, 1e-9, "verify state")
+        _close(out, outb, 2e-6, 1e-9, "verify out")
+        assert np.array_equal(ring_out, ringb), "verify ring"
+
+
+def pin_verify_chained_rows(orc):
+    """Running rows one launch at a time (f32 state between) stays within f32 rounding of one launch."""
+    rng = _rng(32)
+    T, H = 6, 2
+    xq, xk, xv, xg, xb, conv_w, ring, state = _raw_inputs(rng, T, H)
+    st_all, ring_all, out_all = orc.verify(xq, xk, xv, xg, xb, conv_w, ring, state)
+    st, rg = state, ring
+    for t in range(T):
+        sl = slice(t, t + 1)
+        st, rg, out = orc.verify(xq[sl], xk[sl], xv[sl], xg[sl], xb[sl], conv_w, rg, st)
+        _close(out[0], out_all[t], 1e-5, 1e-8, f"row {t} output")
+    _close(st, st_all, 1e-5, 1e-8, "chained state")
+    assert np.array_equal(rg, ring_all), "chained ring"
+
+
+def pin_rollback(orc):
+    """keep == T keeps the resident state; keep < T equals a fresh run of rows 0..keep-1; bad keep refused."""
+    import oracle
+    rng = _rng(33)
+    T, H = 5, 2
+    xq, xk, xv, xg, xb, conv_w, ring, state = _raw_inputs(rng, T, H)
+    st_T, ring_T, _ = orc.verify(xq, xk, xv, xg, xb, conv_w, ring, state)
+    for keep in range(1, T + 1):
+        st, rg = orc.rollback(keep, xq, xk, xv, xg, xb, conv_w, ring, state, ring_T, st_T)
+        if keep == T:
+            assert np.array_equal(st, st_T) and np.array_equal(rg, ring_T), "keep == T"
+        else:
+            sl = slice(0, keep)
+            st_k, ring_k, _ = orc.verify(xq[sl], xk[sl], xv[sl], xg[sl], xb[sl], conv_w, ring, state)
+            assert np.array_equal(st, st_k) and np.array_equal(rg, ring_k), f"keep={keep}"
+            # and the rollback really moved the state off the post-row-T value
+            assert not np.array_equal(st, st_T)
+    for bad in (0, T + 1):
+        try:
+            orc.rollback(bad, xq, xk, xv, xg, xb, conv_w, ring, state, ring_T, st_T)
+        except oracle.OracleError as e:
+            assert e.rc == oracle.EINVAL
+        else:
+            raise AssertionError(f"keep={bad} accepted")
+
+
+# ---------------------------------------------------------------------------
+# greedy accept
+# ---------------------------------------------------------------------------
+def _planted_logits(vam, V, rng):
+    x = rng.uniform(-3.0, 3.0, (len(vam), V)).astype(np.float32)
+    for r, a in enumerate(vam):
+        x[r, a] = 10.0
+    return x
+
+
+def _golden_harvest():
+    out = []
+    with open(os.path.join(GOLDEN, "accept_harvest_fixture.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                name, T, vam, drafts, j, bonus = line.split()
+                out.append((name, int(T), [int(x) for x in vam.split(",")],
+                            [int(x) for x in drafts.split(",")], int(j), int(bonus)))
+    return out
+
+
+def pin_accept_page_fixture(orc):
+    """The harvest-alignment fixture printed on the pages: aligned -> full block, misaligned -> 0."""
+    rng = _rng(41)
+    for name, T, vam, drafts, j_exp, bonus_exp in _golden_harvest():
+        x = _planted_logits(vam, 1024, rng)
+        j, bonus, got_vam, rc = orc.accept(x, drafts)
+        assert rc == 0 and list(got_vam) == vam, name
+        assert (j, bonus) == (j_exp, bonus_exp), f"{name}: {(j, bonus)} != {(j_exp, bonus_exp)}"
+
+
+def _first_argmax_by_sort(row):
+    order = sorted(range(len(row)), key=lambda c: (-row[c], c))
+    return order[0]
+
+
+def _accept_brute(logits, drafts):
+    vam = [_first_argmax_by_sort(list(r)) for r in logits]
+    K = len(drafts)
+    j = max(m for m in range(K + 1) if all(drafts[r] == vam[r] for r in range(m)))
+    return j, vam[j], vam
+
+
+def pin_accept_brute_force(orc):
+    """Tiny vocabularies with many ties, every draft combination: j, bonus, vam as brute force gives."""
+    rng = _rng(42)
+    V = 3
+    for trial in range(30):
+        T = 1 + trial % 4
+        x = rng.integers(0, 3, (T, V)).astype(np.float32)  # values in {0,1,2}: ties everywhere
+        for code in range(V ** (T - 1)):
+            drafts = [(code // V ** r) % V for r in range(T - 1)]
+            j, bonus, vam, rc = orc.accept(x, np.array(drafts, np.int32))
+            jb, bb, vb = _accept_brute(x, drafts)
+            assert rc == 0 and (j, bonus) == (jb, bb) and list(vam) == vb, (x, drafts)
+
+
+def pin_accept_nan(orc):
+    """A NaN in a consulted row is refused (sentinel bonus); a NaN in a row past j is not consulted."""
+    import oracle
+    rng = _rng(43)
+    vam = [5, 6, 7, 8]
+    x = _planted_logits(vam, 16, rng)
+    x_bad = x.copy()
+    x_bad[2, 3] = np.nan
+    # drafts match rows 0 and 1, so the walk reaches the NaN row 2
+    j, bonus, got, rc = orc.accept(x_bad, np.array([5, 6, 7], np.int32))
+    assert rc == oracle.ENAN and j == 2 and bonus == oracle.SENTINEL and got[2] == oracle.SENTINEL
+    # drafts mismatch at row 0: row 2 is never consulted
+    j, bonus, got, rc = orc.accept(x_bad, np.array([4, 6, 7], np.int32))
+    assert rc == 0 and (j, bonus) == (0, 5)
+
+
+def pin_accept_ties(orc):
+    """Equal maxima: the lowest index wins, for f32 and bf16 rows and for -0.0 against +0.0."""
+    x = np.array([[1.0, 3.0, 3.0, 2.0], [-0.0, 0.0, -1.0, -0.0], [-np.inf, -np.inf, -np.inf, -np.inf]],
+                 np.float32)
+    _, _, vam, rc = orc.accept(x, np.array([9, 9], np.int32))
+    assert rc == 0 and list(vam) == [1, 0, 0], vam
+    bits = (np.ascontiguousarray(x).view(np.uint32) >> 16).astype(np.uint16)
+    _, _, vam, rc = orc.accept(bits, np.array([9, 9], np.int32))
+    assert rc == 0 and list(vam) == [1, 0, 0], vam
+    # a bf16 row whose values differ only below bf16 precision in f32 would tie; bf16 decides
+    y = np.array([[0x3F80, 0x3F81, 0x3F81, 0x3F80]], np.uint16)
+    _, bonus, vam, _ = orc.accept(y, np.zeros(0, np.int32))
+    assert vam[0] == 1 and bonus == 1
+
+
+PINS = [
+    pin_core_matrix_form,
+    pin_core_closed_form_first_write,
+    pin_core_identity,
+    pin_core_orthonormal_writes,
+    pin_core_decay_only,
+    pin_prepare_current_tap,
+    pin_prepare_shifted_taps,
+    pin_prepare_vs_correlate,
+    pin_prepare_gates,
+    pin_prepare_ring_reroll,
+    pin_bf16_widening,
+    pin_verify_brute_force,
+    pin_verify_chained_rows,
+    pin_rollback,
+    pin_accept_page_fixture,
+    pin_accept_brute_force,
+    pin_accept_nan,
+    pin_accept_ties,
+]

@@ -1,0 +1,89 @@
+"""Every plausible mistake planted in the oracle must fail at least one pin.
+
+Each mutation is a one-spot textual change of ``oracle/kda_oracle.c`` (a dropped
+term, a wrong sign or index, a transposed operand, an off-by-one), compiled into
+a throw-away library on the CPU.  The pins run in a child process so that a
+mutation that crashes counts as caught without taking pytest down.
+"""
+import json
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(ROOT, "oracle", "kda_oracle.c")
+
+MUTATIONS = {
+    "no_decay": ("Sh[i * D + j] *= d;", "Sh[i * D + j] *= 1.0;"),
+    "delta_sign": ("w[j] = b * (vv[j] - u[j]);", "w[j] = b * (vv[j] + u[j]);"),
+    "no_beta": ("w[j] = b * (vv[j] - u[j]);", "w[j] = (vv[j] - u[j]);"),
+    "u_transposed": ("acc += Sh[i * D + j] * k[i];", "acc += Sh[j * D + i] * k[i];"),
+    "o_transposed": ("acc += Sh[i * D + j] * q[i];", "acc += Sh[j * D + i] * q[i];"),
+    "o_uses_k": ("acc += Sh[i * D + j] * q[i];", "acc += Sh[i * D + j] * k[i];"),
+    "no_scale": ("out[row + j] = acc * scale;", "out[row + j] = acc;"),
+    "update_uses_q": ("Sh[i * D + j] += k[i] * w[j];", "Sh[i * D + j] += q[i] * w[j];"),
+    "ring_order": ("ring_in[(((size_t)h * 3 + s) * 3 + n) * D + c];",
+                   "ring_in[(((size_t)h * 3 + s) * 3 + (2 - n)) * D + c];"),
+    "tap_swap": ("(double)w[0] * x[0]", "(double)w[3] * x[0]"),
+    "no_silu": ("y[((size_t)s * T + t) * D + c] = a * sigmoid(a);",
+                "y[((size_t)s * T + t) * D + c] = a;"),
+    "no_l2norm": ("dst[row + c] = ys[c] * r;", "dst[row + c] = ys[c];"),
+    "l2_eps": ("sqrt(ss + KDAO_L2_EPS)", "sqrt(ss + 1e-2)"),
+    "gate_bound": ("KDAO_GATE_LOWER_BOUND * sigmoid(widen(xg", "sigmoid(widen(xg"),
+    "beta_raw": ("sigmoid(widen(xb, dtype, (size_t)t * H + h))", "widen(xb, dtype, (size_t)t * H + h)"),
+    "ring_reroll": ("hist[((size_t)s * (T + 3) + T + n) * D + c]",
+                    "hist[((size_t)s * (T + 3) + T - 1 + n) * D + c]"),
+    "bf16_shift": ("<< 16;", "<< 15;"),
+    "argmax_last_tie": ("x > bv", "x >= bv"),
+    "j_off_by_one": ("*j_out = j;", "*j_out = j + (j < K);"),
+    "bonus_prev_row": ("*bonus_out = vam[j];", "*bonus_out = vam[j > 0 ? j - 1 : 0];"),
+    "nan_ignored": ("nan_row = 1;", "nan_row = 0;"),
+    "rollback_keep_early": ("if (keep == T) {", "if (keep >= T - 1) {"),
+    "rollback_from_current": ("ring_snap, state_snap,\n                       ring_out, state_out, NULL);",
+                              "ring_cur, state_cur,\n                       ring_out, state_out, NULL);"),
+}
+
+
+def _run_pins(lib_path):
+    code = (
+        "import sys, json; sys.path[:0] = [%r, %r]\n"
+        "import oracle, oracle_pins\n"
+        "orc = oracle.Oracle(%r)\n"
+        "failed = []\n"
+        "for p in oracle_pins.PINS:\n"
+        "    try:\n"
+        "        p(orc)\n"
+        "    except Exception as e:\n"
+        "        failed.append(p.__name__)\n"
+        "print(json.dumps(failed))\n" % (ROOT, HERE, lib_path)
+    )
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        return ["<crashed>"]
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def test_unmutated_oracle_passes_every_pin():
+    import oracle
+    with tempfile.TemporaryDirectory() as d:
+        lib = oracle.build(os.path.join(d, "lib.so"))
+        assert _run_pins(lib) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name):
+    import oracle
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation site for {name} no longer in the oracle"
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "kda_oracle.c")
+        with open(path, "w") as f:
+            f.write(src.replace(old, new, 1))
+        lib = oracle.build(os.path.join(d, "lib.so"), source=path)
+        failed = _run_pins(lib)
+    assert failed, f"mutation {name} passed every pin"
