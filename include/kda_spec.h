@@ -1,0 +1,179 @@
+/*
+ * kda_spec.h -- C ABI of the GB300 (sm_103a) speculative-verify walk through a
+ * Kimi-Delta-Attention (KDA) linear-attention layer.
+ *
+ * One verify round of K drafted tokens runs T = K+1 rows of a session through
+ *   1. a depthwise causal short conv of width 4 with SiLU over the q, k, v raw
+ *      rows, fed by a ring of the last 3 raw inputs,
+ *   2. L2 normalisation of q and k, the forget gate g = -5 sigmoid(raw_g) per key
+ *      channel and the write strength beta = sigmoid(raw_beta) per head,
+ *   3. the gated delta rule on a resident f32 state S [d_k=128][d_v=128] per head:
+ *        S' = diag(exp g) S;  u = S'^T k;  S = S' + beta k (v - u)^T;
+ *        o = S^T q / sqrt(128)
+ *      sequentially over the T rows inside one launch,
+ * followed by greedy acceptance and accept-j rollback (snapshot + replay).
+ * Passages (memra-engine docs.rs pages):
+ *   glm_spec.rs 0.123.0, module doc "VERIFY-ROW BATCHING" (one launch per layer
+ *     per round, T-loop inside the kernel, bit-identical to chained t=1 steps)
+ *   glm_spec.rs, module doc "ROLLBACK" and the Glm5VerifyCkpt doc (one state
+ *     snapshot per layer per round taken before row 0, stolen scan inputs,
+ *     replay of rows 0..keep-1; 64 heads x 128 x 128 f32 = 4 MiB per layer)
+ *   glm_spec.rs, glm5_verify_rollback / glm5_rollback_layer (keep = j+1 in 1..t;
+ *     keep == t keeps the resident state)
+ *   glm_spec.rs, glm5_spec_round step 4 (device argmax per verify row, lowest index
+ *     wins; j = first mismatch; bonus = vam[j]) and guard_vocab_token (NaN rows)
+ *   glm5_spec_ppn_gate.rs, mini fixture linear_attn_config (head_dim 128,
+ *     short_conv_kernel_size 4, gate_lower_bound -5.0)
+ *   glm_spec.rs, glm5_verify_rows (t <= 15: the decode-exact cap)
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     keeps none of them past the call except through the kda_stash it fills.
+ *   - Every call is asynchronous on `stream` and never synchronises.
+ *   - The library allocates no memory.  spec_accept takes caller scratch.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns KDA_EINVAL and enqueues nothing.  The reason is kept
+ *     per thread for kda_last_error().
+ *   - Conditions found on the device (a NaN row at the accept point, a device
+ *     keep outside 1..T) are OR-ed as KDA_ST_* bits into the caller's device int
+ *     `dev_status` (may be NULL); the caller reads it after synchronising.
+ *   - Pointers to float / 16-byte vectors must be 16-byte aligned.
+ */
+#ifndef KDA_SPEC_H
+#define KDA_SPEC_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_DK 128       /* key channels per head   (head_dim 128)            */
+#define KDA_DV 128       /* value channels per head                          */
+#define KDA_TMAX 15      /* rows per verify round: K <= 14 drafts            */
+#define KDA_CONV_W 4     /* short_conv_kernel_size                           */
+#define KDA_RING 3       /* ring slots: the last conv_w - 1 raw inputs       */
+#define KDA_HOST_KEEP_MAX 2048 /* sessions per kda_rollback with host keep  */
+
+/* return codes */
+#define KDA_OK 0
+#define KDA_EINVAL 1   /* bad argument; nothing was launched                 */
+#define KDA_ENAN 2     /* reserved for host-side reports of KDA_ST_NAN       */
+#define KDA_ECUDA 3    /* a CUDA launch or attribute call failed             */
+#define KDA_ETIMEOUT 4 /* reserved: no kernel here waits on another one      */
+
+/* bits OR-ed into *dev_status by kernels */
+#define KDA_ST_NAN 0x1      /* spec_accept: row j (the bonus row) holds a NaN */
+#define KDA_ST_BADKEEP 0x2  /* kda_rollback: a device keep outside 1..T       */
+
+/* element types of raw rows and logits */
+#define KDA_F32 0
+#define KDA_BF16 1
+
+/* where kda_rollback finds keep[] */
+#define KDA_MEM_HOST 0
+#define KDA_MEM_DEVICE 1
+
+/* Problem sizes.  L layers x B sessions x H heads, each an independent unit;
+ * dk and dv must be 128; dtype is the element type of the raw rows. */
+typedef struct kda_dims {
+    int L, B, H;
+    int dk, dv;
+    int dtype; /* KDA_F32 or KDA_BF16 */
+} kda_dims;
+
+/* Resident per-layer state, updated in place by kda_verify_scan / kda_rollback.
+ *   state     f32 [L][B][H][dk][dv]           S, d_v contiguous
+ *   conv_ring f32 [L][B][H][3 stream][3 slot][dk]  raw q,k,v inputs of the last 3
+ *             rows; slot 0 the oldest.  Streams in the order q, k, v.
+ *   conv_w    f32 [L][H][3 stream][dk][4 tap]  tap 3 multiplies the current row,
+ *             tap 0 the row three back. */
+typedef struct kda_layer_state {
+    float *state;
+    float *conv_ring;
+    const float *conv_w;
+} kda_layer_state;
+
+/* Raw (pre-conv, pre-activation) rows of one round, element type dims.dtype:
+ *   q, k, v, g [L][B][T][H][128];  beta [L][B][T][H]. */
+typedef struct kda_rows {
+    const void *q, *k, *v, *g, *beta;
+} kda_rows;
+
+/* Rollback material of one round (the KDA fields of the pages' verify
+ * checkpoint).  The caller allocates state_snap (same shape as state) and
+ * ring_snap (same shape as conv_ring); kda_verify_scan writes the pre-round state
+ * and ring into them as it first reads them, and records `rows` and `T`.  The
+ * stash holds the raw rows by pointer ("stolen", zero copies): they must stay
+ * alive and unchanged until kda_rollback has run or the round is committed. */
+typedef struct kda_stash {
+    float *state_snap;
+    float *ring_snap;
+    kda_rows rows; /* filled by kda_verify_scan */
+    int T;         /* filled by kda_verify_scan */
+} kda_stash;
+
+/*
+ * kda_verify_scan -- one verify round over every (layer, session, head) unit.
+ * Rows 0..T-1 of `rows` pass through conv + SiLU, normalisation, gates and the
+ * gated delta rule in one launch; state and conv_ring advance by T rows in place.
+ *   out   f32 [L][B][T][H][dv] the attention outputs o_t, or NULL.
+ *   stash NULL (no snapshot: a plain decode step), or a stash whose state_snap and
+ *         ring_snap are non-NULL; they receive the pre-round state and ring.
+ * T must lie in 1..KDA_TMAX.  With T = 1 this is exactly the chained per-row step:
+ * running rows one call at a time gives bit-identical state, ring and outputs to
+ * one call with all T rows.
+ */
+int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
+                    int T, float *out, kda_stash *stash, cudaStream_t stream);
+
+/*
+ * kda_rollback -- accept-j rollback of the round recorded in `stash`.
+ * keep[b] (= accepted drafts + 1, the anchor row is always kept) selects, per
+ * session b, the state after row keep-1:
+ *   keep == stash->T : nothing to do (the resident state is that state);
+ *   keep <  stash->T : state <- replay of rows 0..keep-1 from state_snap, conv_ring
+ *                      <- the ring after those rows, both bit-identical to a
+ *                      kda_verify_scan of those rows from the snapshot.
+ * keep_mem = KDA_MEM_HOST: keep is a host array [B], validated (1..T, B <=
+ *   KDA_HOST_KEEP_MAX) before launch.
+ * keep_mem = KDA_MEM_DEVICE: keep is a device array [B] (e.g. spec_accept's
+ *   keep_out); a session whose keep is outside 1..T is left untouched and sets
+ *   KDA_ST_BADKEEP in *dev_status.
+ */
+int kda_rollback(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash,
+                 const int *keep, int keep_mem, int *dev_status, cudaStream_t stream);
+
+/* Bytes of device scratch spec_accept needs for B sessions of T rows of V logits. */
+size_t spec_accept_scratch_bytes(int B, int T, int V);
+
+/*
+ * spec_accept -- greedy acceptance for B sessions.
+ *   logits [B][T][V] (KDA_F32 or KDA_BF16, logit_dtype), drafts int32 [B][T-1]
+ *   (drafts[b][r] is the token drafted for the position that row r predicts).
+ * Per session: vam[r] = index of the maximum of row r, the lowest index winning
+ * ties (bf16 compared after exact widening); a row holding a NaN has no argmax.
+ * j = the first r < T-1 with drafts[r] != vam[r] (or a NaN row), else T-1;
+ * bonus = vam[j]; keep = j + 1.
+ * Outputs (device int32 [B], each may be NULL): j_out, bonus_out, keep_out.  If
+ * row j holds a NaN, bonus is -1 and KDA_ST_NAN is set in *dev_status.
+ * scratch: device memory of at least spec_accept_scratch_bytes(B, T, V) bytes,
+ * 16-byte aligned; its contents need no initialisation.
+ */
+int spec_accept(const void *logits, int logit_dtype, int B, int T, int V, const int *drafts,
+                int *j_out, int *bonus_out, int *keep_out, int *dev_status, void *scratch,
+                size_t scratch_bytes, cudaStream_t stream);
+
+/* Static description of a return code, and the calling thread's last error text. */
+const char *kda_error_string(int code);
+const char *kda_last_error(void);
+
+/* Library version, for the binding's load check. */
+int kda_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_SPEC_H */

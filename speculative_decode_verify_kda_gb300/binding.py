@@ -1,0 +1,248 @@
+"""Thin ctypes binding of the C ABI in include/kda_spec.h.
+
+Argument marshalling only: torch tensors are checked for device, dtype, shape and
+contiguity, their data pointers and the current CUDA stream go to the library,
+and every step of the path runs in the library's kernels.  There is no fallback:
+if the compiled library is missing, loading it raises.
+
+Names follow the C ABI: ``kda_verify_scan``, ``kda_rollback``, ``spec_accept``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib")
+LIB_PATH = os.path.join(LIB_DIR, "libkda_spec.so")
+
+D = 128
+TMAX = 15
+HOST_KEEP_MAX = 2048
+OK, EINVAL, ENAN, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
+ST_NAN, ST_BADKEEP = 0x1, 0x2
+F32, BF16 = 0, 1
+MEM_HOST, MEM_DEVICE = 0, 1
+
+# every symbol the header declares (checked by the CPU test of the library load)
+EXPORTS = ("kda_verify_scan", "kda_rollback", "spec_accept_scratch_bytes", "spec_accept",
+           "kda_error_string", "kda_last_error", "kda_abi_version")
+
+
+class KdaDims(ctypes.Structure):
+    _fields_ = [("L", ctypes.c_int), ("B", ctypes.c_int), ("H", ctypes.c_int),
+                ("dk", ctypes.c_int), ("dv", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class KdaLayerState(ctypes.Structure):
+    _fields_ = [("state", ctypes.c_void_p), ("conv_ring", ctypes.c_void_p), ("conv_w", ctypes.c_void_p)]
+
+
+class KdaRows(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
+
+
+class KdaStashC(ctypes.Structure):
+    _fields_ = [("state_snap", ctypes.c_void_p), ("ring_snap", ctypes.c_void_p),
+                ("rows", KdaRows), ("T", ctypes.c_int)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, fn: str, rc: int, msg: str):
+        super().__init__(f"{fn} failed ({rc}): {msg}")
+        self.rc = rc
+
+
+_lib = None
+
+
+def lib(path: str | None = None):
+    """Load the compiled library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library {p} is missing: run __graft_entry__.build() "
+                           "(or python -m speculative_decode_verify_kda_gb300.build) first")
+    L = ctypes.CDLL(p)
+    vp, ci, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    L.kda_verify_scan.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                  ctypes.POINTER(KdaRows), ci, vp, ctypes.POINTER(KdaStashC), vp]
+    L.kda_verify_scan.restype = ci
+    L.kda_rollback.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                               ctypes.POINTER(KdaStashC), vp, ci, vp, vp]
+    L.kda_rollback.restype = ci
+    L.spec_accept_scratch_bytes.argtypes = [ci, ci, ci]
+    L.spec_accept_scratch_bytes.restype = sz
+    L.spec_accept.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_accept.restype = ci
+    L.kda_error_string.argtypes = [ci]
+    L.kda_error_string.restype = ctypes.c_char_p
+    L.kda_last_error.argtypes = []
+    L.kda_last_error.restype = ctypes.c_char_p
+    L.kda_abi_version.argtypes = []
+    L.kda_abi_version.restype = ci
+    if path is None:
+        _lib = L
+    return L
+
+
+def _check(fn: str, rc: int):
+    if rc != OK:
+        raise KdaError(fn, rc, lib().kda_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _row_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"raw rows must be float32 or bfloat16, got {t.dtype}")
+
+
+class LayerState:
+    """Resident state of L layers x B sessions x H heads (device tensors).
+
+    state [L][B][H][128][128] f32, conv_ring [L][B][H][3][3][128] f32,
+    conv_w [L][H][3][128][4] f32.
+    """
+
+    def __init__(self, state: torch.Tensor, conv_ring: torch.Tensor, conv_w: torch.Tensor):
+        L, B, H = state.shape[:3]
+        self.L, self.B, self.H = int(L), int(B), int(H)
+        self.state = _dev(state, "state", torch.float32, (L, B, H, D, D))
+        self.conv_ring = _dev(conv_ring, "conv_ring", torch.float32, (L, B, H, 3, 3, D))
+        self.conv_w = _dev(conv_w, "conv_w", torch.float32, (L, H, 3, D, 4))
+
+    def c(self) -> KdaLayerState:
+        return KdaLayerState(self.state.data_ptr(), self.conv_ring.data_ptr(), self.conv_w.data_ptr())
+
+    def dims(self, dtype: int) -> KdaDims:
+        return KdaDims(self.L, self.B, self.H, D, D, dtype)
+
+
+class Stash:
+    """Rollback material of one verify round: snapshots (owned here) + the raw rows.
+
+    The raw-row tensors are referenced, not copied, and stay alive with the stash.
+    """
+
+    def __init__(self, st: LayerState):
+        self.state_snap = torch.empty_like(st.state)
+        self.ring_snap = torch.empty_like(st.conv_ring)
+        self.c = KdaStashC(self.state_snap.data_ptr(), self.ring_snap.data_ptr(), KdaRows(), 0)
+        self.rows = None
+        self.dtype = None
+
+    @property
+    def T(self) -> int:
+        return int(self.c.T)
+
+
+def _rows(st: LayerState, q, k, v, g, beta, T: int | None = None):
+    dt = q.dtype
+    if T is None:
+        T = int(q.shape[2])
+    shp = (st.L, st.B, T, st.H, D)
+    tensors = [_dev(q, "q", dt, shp), _dev(k, "k", dt, shp), _dev(v, "v", dt, shp),
+               _dev(g, "g", dt, shp), _dev(beta, "beta", dt, shp[:4])]
+    return KdaRows(*(x.data_ptr() for x in tensors)), tensors, _row_dtype(q), T
+
+
+def kda_verify_scan(st: LayerState, q, k, v, g, beta, out: torch.Tensor | None = None,
+                    stash: Stash | None = None, stream=None) -> Stash | None:
+    """One verify round of T = q.shape[2] rows for every (layer, session, head).
+
+    q, k, v, g: [L][B][T][H][128], beta [L][B][T][H] (float32 or bfloat16, raw rows);
+    out: None or f32 [L][B][T][H][128].  state and conv_ring advance in place.
+    With a stash, its snapshots receive the pre-round state and ring.
+    """
+    rows, tensors, dt, T = _rows(st, q, k, v, g, beta)
+    if out is not None:
+        _dev(out, "out", torch.float32, (st.L, st.B, T, st.H, D))
+    dims, cst = st.dims(dt), st.c()
+    rc = lib().kda_verify_scan(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(rows), T,
+                               _ptr(out), ctypes.byref(stash.c) if stash is not None else None,
+                               ctypes.c_void_p(_stream(stream)))
+    _check("kda_verify_scan", rc)
+    if stash is not None:
+        stash.rows, stash.dtype = tensors, dt
+    return stash
+
+
+def kda_rollback(st: LayerState, stash: Stash, keep, dev_status: torch.Tensor | None = None,
+                 stream=None) -> None:
+    """Accept-j rollback.  keep: host sequence of B ints, or a device int32 tensor [B]."""
+    if stash.rows is None:
+        raise ValueError("stash holds no verify round")
+    dims, cst = st.dims(stash.dtype), st.c()
+    if isinstance(keep, torch.Tensor) and keep.is_cuda:
+        _dev(keep, "keep", torch.int32, (st.B,))
+        kp, mem = ctypes.c_void_p(keep.data_ptr()), MEM_DEVICE
+        hold = keep
+    else:
+        hold = (ctypes.c_int * max(st.B, 1))(*[int(x) for x in keep])
+        if len(list(keep)) != st.B:
+            raise ValueError(f"keep must have {st.B} entries")
+        kp, mem = ctypes.cast(hold, ctypes.c_void_p), MEM_HOST
+    if dev_status is not None:
+        _dev(dev_status, "dev_status", torch.int32)
+    rc = lib().kda_rollback(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(stash.c), kp, mem,
+                            _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+    del hold
+    _check("kda_rollback", rc)
+
+
+def spec_accept_scratch_bytes(B: int, T: int, V: int) -> int:
+    return int(lib().spec_accept_scratch_bytes(B, T, V))
+
+
+def spec_accept(logits: torch.Tensor, drafts: torch.Tensor, j_out=None, bonus_out=None, keep_out=None,
+                dev_status=None, scratch: torch.Tensor | None = None, stream=None):
+    """Greedy accept for B sessions: logits [B][T][V] (f32/bf16), drafts int32 [B][T-1].
+
+    Returns (j_out, bonus_out, keep_out) device int32 tensors [B] (allocated here
+    by torch when not given).
+    """
+    _dev(logits, "logits")
+    B, T, V = (int(x) for x in logits.shape)
+    _dev(drafts, "drafts", torch.int32, (B, T - 1))
+    dev = logits.device
+    j_out = torch.empty(B, dtype=torch.int32, device=dev) if j_out is None else j_out
+    bonus_out = torch.empty(B, dtype=torch.int32, device=dev) if bonus_out is None else bonus_out
+    keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
+    need = spec_accept_scratch_bytes(B, T, V)
+    if scratch is None:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib().spec_accept(_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out),
+                           _ptr(bonus_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch),
+                           scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
+    _check("spec_accept", rc)
+    return j_out, bonus_out, keep_out

@@ -1,0 +1,228 @@
+// spec_accept.cu -- greedy acceptance over the verify logits (sm_103a).
+//
+// glm_spec.rs (memra-engine 0.123.0), glm5_spec_round step 4: one device argmax
+// per verify row with the lowest index winning ties, one small readback, then
+// j = the first row whose draft differs from the row's argmax (else K) and the
+// bonus token vam[j]; keep = j + 1 (the anchor row is always committed).  A row
+// holding a NaN has no argmax; reaching it refuses loudly (guard_vocab_token).
+//
+// Two launches, no inter-CTA waiting:
+//   1. accept_partial_kernel: grid (B*T rows, VS slices of the vocabulary); each
+//      CTA reduces its slice to (max, lowest index of the max, NaN seen) and
+//      writes that triple to the caller's scratch.
+//   2. accept_final_kernel: one warp per session; lane r folds the VS triples of
+//      row r in slice order, then a ballot over the mismatch predicate gives j.
+// The selection is a total order on (value, -index), so the reduction order
+// never changes the result.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr int ACC_THREADS = 256;
+constexpr int SLICE = 4096;  // logits per CTA of the first pass
+constexpr int MAX_VS = 64;
+
+struct Partial {
+    float v;
+    int idx;
+    int nan;
+    int pad;
+};
+
+__host__ __device__ inline int slices_for(int V)
+{
+    int vs = (V + SLICE - 1) / SLICE;
+    return vs < 1 ? 1 : (vs > MAX_VS ? MAX_VS : vs);
+}
+
+__device__ __forceinline__ void take(float &bv, int &bi, float v, int i)
+{
+    if (v > bv || (v == bv && i < bi)) {
+        bv = v;
+        bi = i;
+    }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(ACC_THREADS) accept_partial_kernel(const void *__restrict__ logits, int V,
+                                                                      int vs, int chunk, Partial *__restrict__ part)
+{
+    const long long row = blockIdx.x;
+    const int s = blockIdx.y;
+    const int begin = s * chunk;
+    const int end = min(V, begin + chunk);
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    int nan = 0;
+    if (BF16) {
+        const uint16_t *x = static_cast<const uint16_t *>(logits) + row * V;
+        const bool vec = (V % 8 == 0) && (chunk % 8 == 0);
+        if (vec) {
+            const uint4 *x8 = reinterpret_cast<const uint4 *>(x);
+            for (int c8 = begin / 8 + threadIdx.x; c8 < end / 8; c8 += ACC_THREADS) {
+                const uint4 r = x8[c8];
+                const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const float lo = __uint_as_float(w[m] << 16), hi = __uint_as_float(w[m] & 0xffff0000u);
+                    nan |= (lo != lo) | (hi != hi);
+                    take(bv, bi, lo, 8 * c8 + 2 * m);
+                    take(bv, bi, hi, 8 * c8 + 2 * m + 1);
+                }
+            }
+        } else {
+            for (int c = begin + threadIdx.x; c < end; c += ACC_THREADS) {
+                const float v = __uint_as_float(static_cast<uint32_t>(x[c]) << 16);
+                nan |= (v != v);
+                take(bv, bi, v, c);
+            }
+        }
+    } else {
+        const float *x = static_cast<const float *>(logits) + row * V;
+        const bool vec = (V % 4 == 0) && (chunk % 4 == 0);
+        if (vec) {
+            const float4 *x4 = reinterpret_cast<const float4 *>(x);
+            for (int c4 = begin / 4 + threadIdx.x; c4 < end / 4; c4 += ACC_THREADS) {
+                const float4 r = x4[c4];
+                nan |= (r.x != r.x) | (r.y != r.y) | (r.z != r.z) | (r.w != r.w);
+                take(bv, bi, r.x, 4 * c4);
+                take(bv, bi, r.y, 4 * c4 + 1);
+                take(bv, bi, r.z, 4 * c4 + 2);
+                take(bv, bi, r.w, 4 * c4 + 3);
+            }
+        } else {
+            for (int c = begin + threadIdx.x; c < end; c += ACC_THREADS) {
+                const float v = x[c];
+                nan |= (v != v);
+                take(bv, bi, v, c);
+            }
+        }
+    }
+    // NaN never wins `take` (every comparison with NaN is false)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        nan |= __shfl_xor_sync(0xffffffffu, nan, off);
+        take(bv, bi, ov, oi);
+    }
+    __shared__ float sv[ACC_THREADS / 32];
+    __shared__ int si[ACC_THREADS / 32], sn[ACC_THREADS / 32];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (lane == 0) {
+        sv[wid] = bv;
+        si[wid] = bi;
+        sn[wid] = nan;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < ACC_THREADS / 32; ++w) {
+            take(bv, bi, sv[w], si[w]);
+            nan |= sn[w];
+        }
+        Partial pt;
+        pt.v = bv;
+        pt.idx = bi;
+        pt.nan = nan;
+        pt.pad = 0;
+        part[row * vs + s] = pt;
+    }
+}
+
+__global__ void accept_final_kernel(const Partial *__restrict__ part, int B, int T, int vs,
+                                    const int *__restrict__ drafts, int *j_out, int *bonus_out, int *keep_out,
+                                    int *status)
+{
+    const int warps = blockDim.x / 32;
+    const int b = blockIdx.x * warps + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (b >= B)
+        return;
+    const int K = T - 1;
+    int vam = -1;
+    if (lane < T) {
+        const Partial *pr = part + (static_cast<long long>(b) * T + lane) * vs;
+        float bv = -INFINITY;
+        int bi = 0x7fffffff, nan = 0;
+        for (int s = 0; s < vs; ++s) {
+            const Partial q = pr[s];
+            nan |= q.nan;
+            take(bv, bi, q.v, q.idx);
+        }
+        vam = nan ? -1 : bi;
+    }
+    const bool miss = lane < K && (vam < 0 || drafts[static_cast<long long>(b) * K + lane] != vam);
+    const unsigned mask = __ballot_sync(0xffffffffu, miss);
+    const int j = mask ? __ffs(mask) - 1 : K;
+    const int bonus = __shfl_sync(0xffffffffu, vam, j);
+    if (lane == 0) {
+        if (j_out)
+            j_out[b] = j;
+        if (bonus_out)
+            bonus_out[b] = bonus;
+        if (keep_out)
+            keep_out[b] = j + 1;
+        if (bonus < 0 && status)
+            atomicOr(status, KDA_ST_NAN);
+    }
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" size_t spec_accept_scratch_bytes(int B, int T, int V)
+{
+    if (B <= 0 || T <= 0 || V <= 0)
+        return 0;
+    return static_cast<size_t>(B) * T * slices_for(V) * sizeof(Partial);
+}
+
+extern "C" int spec_accept(const void *logits, int logit_dtype, int B, int T, int V, const int *drafts,
+                           int *j_out, int *bonus_out, int *keep_out, int *dev_status, void *scratch,
+                           size_t scratch_bytes, cudaStream_t stream)
+{
+    if (B < 0)
+        return fail(KDA_EINVAL, "B must be >= 0");
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
+    if (V < 1)
+        return fail(KDA_EINVAL, "V must be >= 1");
+    if (logit_dtype != KDA_F32 && logit_dtype != KDA_BF16)
+        return fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
+    if (B == 0)
+        return ok();
+    if (!logits || (T > 1 && !drafts))
+        return fail(KDA_EINVAL, "logits and drafts must not be NULL");
+    if (!aligned16(logits))
+        return fail(KDA_EINVAL, "logits must be 16-byte aligned");
+    const size_t need = spec_accept_scratch_bytes(B, T, V);
+    if (!scratch || scratch_bytes < need || !aligned16(scratch))
+        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " +
+                                    std::to_string(need) + " bytes");
+    if (static_cast<long long>(B) * T > 0x7fffffffLL)
+        return fail(KDA_EINVAL, "B*T exceeds the grid limit");
+    const int vs = slices_for(V);
+    int chunk = (V + vs - 1) / vs;
+    chunk = (chunk + 7) / 8 * 8;
+    Partial *part = static_cast<Partial *>(scratch);
+    dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
+    if (logit_dtype == KDA_BF16)
+        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+    else
+        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+    int rc = check_launch("accept_partial_kernel");
+    if (rc)
+        return rc;
+    const int warps = 4;
+    accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
+                                                                            bonus_out, keep_out, dev_status);
+    return check_launch("accept_final_kernel");
+}

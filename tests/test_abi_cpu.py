@@ -1,0 +1,132 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every symbol
+include/kda_spec.h declares, and rejects invalid calls on the host (KDA_EINVAL)
+before anything touches a device.  No call here reaches a launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from libs import ROOT, ensure_built
+
+from speculative_decode_verify_kda_gb300 import binding as kb
+
+HEADER = os.path.join(ROOT, "include", "kda_spec.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    ensure_built()
+    return kb.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^(?:int|size_t|const char \*)\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert set(names) == set(kb.EXPORTS), names
+    for n in names:
+        assert hasattr(L, n), n
+    assert L.kda_abi_version() == 1
+    assert L.kda_error_string(kb.EINVAL) == b"invalid argument"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def _state(H=64, B=1, L_=1, dtype=kb.BF16, dk=128):
+    return (kb.KdaDims(L_, B, H, dk, 128, dtype), kb.KdaLayerState(FAKE, FAKE, FAKE),
+            kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE))
+
+
+@pytest.mark.parametrize("case", ["T0", "T16", "dk64", "dtype", "null_state", "null_rows", "misaligned",
+                                  "snap_alias", "snap_null", "negB"])
+def test_verify_rejects_on_host(L, case):
+    dims, st, rows = _state()
+    T, stash = 8, None
+    if case == "T0":
+        T = 0
+    elif case == "T16":
+        T = 16
+    elif case == "dk64":
+        dims.dk = 64
+    elif case == "dtype":
+        dims.dtype = 7
+    elif case == "null_state":
+        st.state = None
+    elif case == "null_rows":
+        rows.v = None
+    elif case == "misaligned":
+        rows.q = FAKE + 2
+    elif case == "snap_alias":
+        stash = kb.KdaStashC(FAKE, FAKE + 0x100, kb.KdaRows(), 0)
+    elif case == "snap_null":
+        stash = kb.KdaStashC(None, FAKE, kb.KdaRows(), 0)
+    elif case == "negB":
+        dims.B = -1
+    rc = L.kda_verify_scan(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), T, None,
+                           ctypes.byref(stash) if stash is not None else None, None)
+    assert rc == kb.EINVAL
+    assert L.kda_last_error()  # a reason is recorded
+
+
+@pytest.mark.parametrize("keep", [[0], [9], [-1]])
+def test_rollback_rejects_bad_host_keep(L, keep):
+    dims, st, rows = _state()
+    stash = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, rows, 8)
+    arr = (ctypes.c_int * 1)(*keep)
+    rc = L.kda_rollback(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash),
+                        ctypes.cast(arr, ctypes.c_void_p), kb.MEM_HOST, None, None)
+    assert rc == kb.EINVAL
+    assert b"outside 1..8" in L.kda_last_error()
+
+
+def test_rollback_full_accept_host_keep_is_a_no_op(L):
+    # keep == T for every session: nothing to restore, nothing launched, OK
+    dims, st, rows = _state(B=3)
+    stash = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, rows, 8)
+    arr = (ctypes.c_int * 3)(8, 8, 8)
+    assert L.kda_rollback(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash),
+                          ctypes.cast(arr, ctypes.c_void_p), kb.MEM_HOST, None, None) == kb.OK
+
+
+def test_rollback_rejects_missing_round_and_bad_mode(L):
+    dims, st, rows = _state()
+    arr = (ctypes.c_int * 1)(1)
+    empty = kb.KdaStashC(FAKE, FAKE, rows, 0)
+    assert L.kda_rollback(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(empty),
+                          ctypes.cast(arr, ctypes.c_void_p), kb.MEM_HOST, None, None) == kb.EINVAL
+    stash = kb.KdaStashC(FAKE, FAKE, rows, 4)
+    assert L.kda_rollback(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash),
+                          ctypes.cast(arr, ctypes.c_void_p), 5, None, None) == kb.EINVAL
+    big = kb.KdaDims(1, kb.HOST_KEEP_MAX + 1, 64, 128, 128, kb.BF16)
+    arr2 = (ctypes.c_int * (kb.HOST_KEEP_MAX + 1))(*([1] * (kb.HOST_KEEP_MAX + 1)))
+    assert L.kda_rollback(ctypes.byref(big), ctypes.byref(st), ctypes.byref(stash),
+                          ctypes.cast(arr2, ctypes.c_void_p), kb.MEM_HOST, None, None) == kb.EINVAL
+
+
+def test_accept_rejects_on_host(L):
+    need = L.spec_accept_scratch_bytes(2, 8, 32768)
+    assert need == 2 * 8 * 8 * 16
+    args = dict(logits=FAKE, dt=kb.BF16, B=2, T=8, V=32768, drafts=FAKE)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return L.spec_accept(a["logits"], a["dt"], a["B"], a["T"], a["V"], a["drafts"], None, None, None,
+                             None, kw.get("scratch", FAKE), kw.get("nbytes", need), None)
+    assert call(T=16) == kb.EINVAL
+    assert call(T=0) == kb.EINVAL
+    assert call(V=0) == kb.EINVAL
+    assert call(dt=3) == kb.EINVAL
+    assert call(nbytes=need - 1) == kb.EINVAL
+    assert call(scratch=None) == kb.EINVAL
+    assert call(logits=FAKE + 4) == kb.EINVAL
+    assert call(B=0) == kb.OK  # nothing to do
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="missing"):
+        kb.lib(str(tmp_path / "libkda_spec.so"))
