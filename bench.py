@@ -1,0 +1,445 @@
+"""Benchmark: KDA speculative-verify rounds on one GB300 (or N replicas).
+
+A step is one verify round of the whole hot path on resident inputs:
+  kda_verify_scan  (conv + activations + gated delta rule over T rows, fused
+                    state snapshot)  ->  spec_accept (device argmax per row,
+                    first mismatch, keep = j+1)  ->  kda_rollback (device keep;
+                    replay of rows 0..keep-1 from the snapshot where keep < T).
+Default workload: the 34-layer KDA stack of one session, 64 heads x 128x128 f32
+state per layer, K = 7 drafts (T = 8), 64 seeded rounds cycled, accept j drawn
+per round.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "KDA verify rows/s (T=K+1, 64 heads) and achieved HBM GB/s vs 8 TB/s roofline"
+UNIT = "verify rows/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOAD_TEXT = {
+    "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
+               "64 seeded rounds cycled, accept j ~ U{0..7}, logits [8][32768] bf16",
+    "stress64x34": "64 sessions x 34 layers x 64 heads x 128x128 f32 state, K=14 (T=15), skewed accept, "
+                   "16 rounds cycled",
+    "batched32": "32 sessions x 1 layer x 64 heads, K=14 (T=15), 16 rounds cycled",
+    "layer64": "one 64-head KDA layer, K=7 (T=8), 1 session",
+    "tiny": "1 layer, 1 head, K=7, f32 rows, V=32",
+}
+
+
+# ---------------------------------------------------------------------------
+# byte accounting (algorithmic bytes: every tensor element moved once)
+# ---------------------------------------------------------------------------
+def verify_bytes(w) -> int:
+    es = 2 if w.bf16 else 4
+    D = 128
+    per_head = 3 * D * D * 4 + 3 * 9 * D * 4  # S read + snapshot write + S write; ring read/write/snapshot
+    rows = w.T * w.H * (4 * D + 1) * es
+    out = w.T * w.H * D * 4
+    return w.L * w.B * (w.H * per_head + rows + out) + w.L * w.H * 3 * D * 4 * 4
+
+
+def rollback_bytes(w, keeps) -> int:
+    es = 2 if w.bf16 else 4
+    D = 128
+    n = 0
+    for k in keeps:
+        if k < w.T:
+            n += w.L * (w.H * (2 * D * D * 4 + 2 * 9 * D * 4) + k * w.H * (4 * D + 1) * es)
+    if n:
+        n += w.L * w.H * 3 * D * 4 * 4
+    return n
+
+
+def accept_bytes(w) -> int:
+    return w.B * w.T * w.V * (2 if w.bf16 else 4) + w.B * (w.T - 1) * 4 + 3 * w.B * 4
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (the reference arm and the cpu_baseline key)
+# ---------------------------------------------------------------------------
+class OracleArm:
+    """The CPU oracle, as it stands, on one (layer, session) unit of the workload.
+
+    Inputs for a few rounds are drawn once (untimed); each call runs accept +
+    verify + rollback of one round on a slice of the unit's heads (heads are
+    independent) and returns the oracle's own time.  State carries across rounds.
+    """
+
+    def __init__(self, w, n_rounds: int = 4):
+        import oracle
+        from speculative_decode_verify_kda_gb300 import synth
+        self.orc = oracle.load()
+        self.w = w
+        l, b = 0, 0
+        self.state = synth.unit_state(w, l, b)
+        self.ring = synth.unit_ring(w, l, b)
+        self.cw = synth.layer_conv_w(w, l)
+        self.rounds = []
+        for r in range(min(n_rounds, w.rounds)):
+            d = synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V)[b]
+            self.rounds.append((synth.unit_rows(w, r, l, b), synth.logits(w, r, sessions=[b])[0], d))
+        self.r = 0
+        self.h0 = 0
+
+    def step(self, n_heads: int):
+        """One round of accept + verify + rollback on the next n_heads heads."""
+        rows, lg, d = self.rounds[self.r % len(self.rounds)]
+        hs = slice(self.h0, min(self.w.H, self.h0 + n_heads))
+        args = tuple(np.ascontiguousarray(rows[n][:, hs]) for n in ("q", "k", "v", "g", "beta"))
+        s, rg, cw = (np.ascontiguousarray(a[hs]) for a in (self.state, self.ring, self.cw))
+        t0 = time.perf_counter()
+        j, _, _, _ = self.orc.accept(lg, d)
+        t1 = time.perf_counter()
+        st_T, ring_T, _ = self.orc.verify(*args, cw, rg, s)
+        st_k, ring_k = self.orc.rollback(j + 1, *args, cw, rg, s, ring_T, st_T)
+        t2 = time.perf_counter()
+        self.state[hs], self.ring[hs] = st_k, ring_k
+        done = hs.stop - hs.start
+        self.h0 = hs.stop
+        if self.h0 >= self.w.H:
+            self.h0 = 0
+            self.r += 1
+        return t2 - t1, t1 - t0, done
+
+    def rows_per_s(self, scan_s_per_head: float, accept_s: float) -> float:
+        w = self.w
+        round_s = scan_s_per_head * w.H * w.L * w.B + accept_s * w.B
+        return w.B * w.T / round_s
+
+
+def oracle_baseline(w, budget_s: float):
+    """cpu_baseline: whole unit-rounds of the oracle for about budget_s seconds."""
+    arm = OracleArm(w)
+    t_scan = t_acc = 0.0
+    heads = rounds = 0
+    while t_scan + t_acc < budget_s or rounds == 0:
+        ts, ta, n = arm.step(w.H)
+        t_scan, t_acc, heads, rounds = t_scan + ts, t_acc + ta, heads + n, rounds + 1
+    val = arm.rows_per_s(t_scan / heads, t_acc / rounds)
+    desc = (f"{rounds} rounds of one (layer, session) unit of {w.name} ({w.H} heads, T={w.T}: accept + "
+            f"verify + rollback), {t_scan + t_acc:.1f} s of single-threaded oracle time, extrapolated "
+            f"linearly to {w.L} layers x {w.B} sessions per round")
+    return {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from speculative_decode_verify_kda_gb300 import binding as kb
+    from speculative_decode_verify_kda_gb300 import synth, synth_gpu
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = synth.WORKLOADS[args.workload]
+    R = min(w.rounds, args.rounds) if args.rounds else w.rounds
+
+    st = kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev))
+    stash = kb.Stash(st)
+    rows = [synth_gpu.rows(w, r, dev) for r in range(R)]
+    logits = [synth_gpu.logits(w, r, dev) for r in range(R)]
+    drafts, jt = zip(*[synth_gpu.drafts(w, r, dev) for r in range(R)])
+    out = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev)
+    j_out = torch.empty(w.B, dtype=torch.int32, device=dev)
+    bonus_out = torch.empty_like(j_out)
+    keep_out = torch.empty_like(j_out)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scratch = torch.empty(max(kb.spec_accept_scratch_bytes(w.B, w.T, w.V), 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    plans = [kb.RoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+                          scratch, stream) for r in range(R)]
+
+    def step(r, ev=None):
+        p = plans[r]
+        if ev is None:
+            p()
+            return
+        ev[0].record(stream)
+        p.verify()
+        ev[1].record(stream)
+        p.accept()
+        ev[2].record(stream)
+        p.rollback()
+        ev[3].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i % R)
+    barrier()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t_wall = time.perf_counter()
+        e0.record(stream)
+        for i in range(K):
+            step((args.warmup + i) % R, evs[i])
+        e1.record(stream)
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    total_ms = e0.elapsed_time(e1)
+    verify_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    accept_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    roll_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    st_word = int(status.item())
+    if st_word:
+        raise RuntimeError(f"device status {st_word:#x} after the timed steps")
+    ms_step = total_ms / K
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    keeps_all = [[j + 1 for j in jt[(args.warmup + i) % R]] for i in range(K)]
+    vb = verify_bytes(w)
+    step_bytes = [vb + accept_bytes(w) + rollback_bytes(w, k) for k in keeps_all]
+    verify_avg_ms = sum(verify_ms) / K
+    peak, peak_kind = measured_peak()
+    achieved = vb / (verify_avg_ms * 1e-3) / 1e9
+
+    res = {
+        "rows_per_s": world * w.B * w.T / (ms_step * 1e-3),
+        "ms_per_step": ms_step,
+        "verify_ms": verify_avg_ms,
+        "accept_ms": sum(accept_ms) / K,
+        "rollback_ms": sum(roll_ms) / K,
+        "wall_s": t_wall,
+        "verify_bytes": vb,
+        "step_gbs": sum(step_bytes) / (total_ms * 1e-3) / 1e9,
+        "achieved": achieved,
+        "peak": peak,
+        "peak_kind": peak_kind,
+        "clocks": clk.summary(),
+        "launches_per_step": 4,
+    }
+
+    # e2e: host buffers through the public API, copies inside the timed region
+    if not args.no_e2e:
+        HR = min(R, 4)
+        host_rows = [{n: t.cpu().pin_memory() for n, t in rows[r].items()} for r in range(HR)]
+        host_logits = [logits[r].cpu().pin_memory() for r in range(HR)]
+        host_drafts = [drafts[r].cpu().pin_memory() for r in range(HR)]
+        dev_rows = {n: torch.empty_like(t) for n, t in rows[0].items()}
+        dev_logits = torch.empty_like(logits[0])
+        dev_drafts = torch.empty_like(drafts[0])
+        host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_rows[0].values()) + \
+            host_logits[0].numel() * host_logits[0].element_size() + host_drafts[0].numel() * 4
+        d2h = host_res.numel() * 4
+        Ke = max(1, min(args.e2e_steps, K))
+
+        eplan = kb.RoundPlan(st, dev_rows, out, stash, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
+                             status, scratch, stream)
+
+        def e2e_step(r):
+            for n in dev_rows:
+                dev_rows[n].copy_(host_rows[r][n], non_blocking=True)
+            dev_logits.copy_(host_logits[r], non_blocking=True)
+            dev_drafts.copy_(host_drafts[r], non_blocking=True)
+            eplan()
+            host_res[0].copy_(j_out, non_blocking=True)
+            host_res[1].copy_(bonus_out, non_blocking=True)
+            stream.synchronize()  # the host needs j and the bonus before the next round
+
+        for i in range(3):
+            e2e_step(i % HR)
+        barrier()
+        t0 = time.perf_counter()
+        for i in range(Ke):
+            e2e_step(i % HR)
+        barrier()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        res["e2e"] = {"value": world * w.B * w.T / (e2e_ms * 1e-3), "unit": UNIT,
+                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                      "ms_per_step": e2e_ms, "steps": Ke}
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=6000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="stack34", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--rounds", type=int, default=0, help="distinct input rounds kept resident (0: all)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from speculative_decode_verify_kda_gb300 import synth
+    w = synth.WORKLOADS[args.workload]
+    config = {"workload": args.workload, "description": WORKLOAD_TEXT[args.workload],
+              "L": w.L, "B": w.B, "H": w.H, "T": w.T, "V": w.V, "rows_dtype": "bf16" if w.bf16 else "f32",
+              "state_dtype": "f32", "l2": "no flush: >= 0.8 GB moved per step, larger than the 129 MB L2",
+              "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        arm = OracleArm(w)
+        ts, ta, n = arm.step(w.H)  # calibration: one whole unit-round
+        per_head = ts / n
+        budget = min(0.5, 90.0 / (args.steps + args.warmup))
+        hps = int(max(1, min(w.H, budget // max(per_head, 1e-9))))
+        t_scan = t_acc = 0.0
+        heads = rounds = 0
+        for i in range(args.warmup + args.steps):
+            ts, ta, n = arm.step(hps)
+            if i >= args.warmup:
+                t_scan += ts
+                heads += n
+                t_acc += ta * n / w.H  # one accept per round, spread over the round's heads
+        val = arm.rows_per_s(t_scan / heads, t_acc / heads * w.H)
+        sample = (f"{args.steps} steps of {hps} heads each of one (layer, session) unit of {args.workload} "
+                  f"(accept + verify + rollback, single-threaded oracle), extrapolated linearly to "
+                  f"{w.H} heads x {w.L} layers x {w.B} sessions per round")
+        line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.B * w.T / val * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded counter-based draws)", "config": config,
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+                "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_gpu(args, rank, world, local_rank)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = oracle_baseline(w, args.cpu_budget)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    frac = res["achieved"] / res["peak"]
+    line = {
+        "metric": METRIC, "value": res["rows_per_s"], "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based draws; bf16 raw rows)",
+        "config": config,
+        "roofline": {"bound": "hbm", "kernel": "kda_scan_kernel (verify)", "achieved": res["achieved"],
+                     "peak": res["peak"], "unit": "GB/s", "frac": frac,
+                     "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
+                     "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
+                     "bytes_per_launch": res["verify_bytes"], "traffic": None},
+        "verify_ms": res["verify_ms"], "accept_ms": res["accept_ms"], "rollback_ms": res["rollback_ms"],
+        "step_achieved_gbs": res["step_gbs"],
+        "gpu_launches": res["launches_per_step"] * args.steps,
+        "clocks": res["clocks"],
+        "cpu_baseline": cpu,
+        "e2e": res.get("e2e"),
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -246,3 +246,59 @@ def spec_accept(logits: torch.Tensor, drafts: torch.Tensor, j_out=None, bonus_ou
                            scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
     _check("spec_accept", rc)
     return j_out, bonus_out, keep_out
+
+
+class RoundPlan:
+    """Pre-marshalled arguments of one verify round, for calling it many times.
+
+    Holds the ctypes argument tuples of kda_verify_scan, spec_accept and
+    kda_rollback (device keep from spec_accept's keep_out) for fixed tensors, so
+    each call is one foreign call with no per-call marshalling.  The tensors are
+    referenced and must keep their storage while the plan is used.
+    """
+
+    def __init__(self, st: LayerState, rows: dict, out, stash: Stash, logits, drafts, j_out, bonus_out,
+                 keep_out, dev_status, scratch, stream=None):
+        L = lib()
+        self._keep = (st, rows, out, stash, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch)
+        crows, tensors, dt, T = _rows(st, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
+        B, Tl, V = (int(x) for x in logits.shape)
+        if Tl != T or B != st.B:
+            raise ValueError("logits must be [B][T][V] of the round")
+        _dev(drafts, "drafts", torch.int32, (B, T - 1))
+        for name, t in (("j_out", j_out), ("bonus_out", bonus_out), ("keep_out", keep_out)):
+            _dev(t, name, torch.int32, (B,))
+        if out is not None:
+            _dev(out, "out", torch.float32, (st.L, st.B, T, st.H, D))
+        self.dims, self.cst, self.crows = st.dims(dt), st.c(), crows
+        s = ctypes.c_void_p(_stream(stream))
+        self._verify = (ctypes.byref(self.dims), ctypes.byref(self.cst), ctypes.byref(self.crows), T,
+                        _ptr(out), ctypes.byref(stash.c), s)
+        nbytes = scratch.numel() * scratch.element_size()
+        self._accept = (_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out), _ptr(bonus_out),
+                        _ptr(keep_out), _ptr(dev_status), _ptr(scratch), nbytes, s)
+        self._rollback = (ctypes.byref(self.dims), ctypes.byref(self.cst), ctypes.byref(stash.c),
+                          _ptr(keep_out), MEM_DEVICE, _ptr(dev_status), s)
+        self._stash, self._tensors, self._dt = stash, tensors, dt
+        self._L = L
+
+    def verify(self):
+        rc = self._L.kda_verify_scan(*self._verify)
+        if rc:
+            _check("kda_verify_scan", rc)
+        self._stash.rows, self._stash.dtype = self._tensors, self._dt
+
+    def accept(self):
+        rc = self._L.spec_accept(*self._accept)
+        if rc:
+            _check("spec_accept", rc)
+
+    def rollback(self):
+        rc = self._L.kda_rollback(*self._rollback)
+        if rc:
+            _check("kda_rollback", rc)
+
+    def __call__(self):
+        self.verify()
+        self.accept()
+        self.rollback()

@@ -392,6 +392,8 @@ int check_common(const kda_dims *dims, const kda_layer_state *st)
         return fail(KDA_EINVAL, "dk and dv must both be 128");
     if (dims->dtype != KDA_F32 && dims->dtype != KDA_BF16)
         return fail(KDA_EINVAL, "dtype must be KDA_F32 or KDA_BF16");
+    if (static_cast<long long>(dims->L) * dims->B * dims->H == 0)
+        return KDA_OK;  // an empty problem touches no memory; pointers may be NULL
     if (!st->state || !st->conv_ring || !st->conv_w)
         return fail(KDA_EINVAL, "state, conv_ring and conv_w must not be NULL");
     if (!aligned16(st->state) || !aligned16(st->conv_ring) || !aligned16(st->conv_w))
@@ -422,10 +424,17 @@ extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, 
     int rc = check_common(dims, st);
     if (rc)
         return rc;
-    if ((rc = check_rows(rows, dims->dtype)))
-        return rc;
     if (T < 1 || T > KDA_TMAX)
         return fail(KDA_EINVAL, "T must lie in 1..15 (K <= 14 drafts per round), got " + std::to_string(T));
+    if (static_cast<long long>(dims->L) * dims->B * dims->H == 0) {
+        if (stash) {
+            stash->rows = rows ? *rows : kda_rows{};
+            stash->T = T;
+        }
+        return ok();
+    }
+    if ((rc = check_rows(rows, dims->dtype)))
+        return rc;
     if (out && (reinterpret_cast<uintptr_t>(out) & 3u))
         return fail(KDA_EINVAL, "out must be 4-byte aligned");
     if (stash) {
@@ -470,11 +479,13 @@ extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, con
         return fail(KDA_EINVAL, "stash must not be NULL");
     if (stash->T < 1 || stash->T > KDA_TMAX)
         return fail(KDA_EINVAL, "stash->T is not a verify round's row count (run kda_verify_scan first)");
+    if (static_cast<long long>(dims->L) * dims->B * dims->H == 0)
+        return ok();
     if (!stash->state_snap || !stash->ring_snap || !aligned16(stash->state_snap) || !aligned16(stash->ring_snap))
         return fail(KDA_EINVAL, "stash snapshots must be non-NULL and 16-byte aligned");
     if ((rc = check_rows(&stash->rows, dims->dtype)))
         return rc;
-    if (!keep && dims->B > 0)
+    if (!keep)
         return fail(KDA_EINVAL, "keep must not be NULL");
     ScanParams p{};
     if (keep_mem == KDA_MEM_HOST) {

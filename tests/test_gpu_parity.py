@@ -198,11 +198,18 @@ def test_shapes_and_edges(orc, H, T):
 
 
 def test_empty_problem_is_a_no_op():
+    """L*B*H = 0: verify and rollback succeed without touching memory (torch gives NULL pointers)."""
     st = kb.LayerState(torch.zeros((0, 1, 64, 128, 128), device="cuda"), torch.zeros((0, 1, 64, 3, 3, 128), device="cuda"),
                        torch.zeros((0, 64, 3, 128, 4), device="cuda"))
     z = torch.zeros((0, 1, 8, 64, 128), dtype=torch.bfloat16, device="cuda")
-    kb.kda_verify_scan(st, z, z, z, z, torch.zeros((0, 1, 8, 64), dtype=torch.bfloat16, device="cuda"))
+    stash = kb.Stash(st)
+    kb.kda_verify_scan(st, z, z, z, z, torch.zeros((0, 1, 8, 64), dtype=torch.bfloat16, device="cuda"), stash=stash)
+    assert stash.T == 8
+    kb.kda_rollback(st, stash, [3])
+    j, bonus, keep = kb.spec_accept(torch.zeros((0, 4, 100), device="cuda"),
+                                    torch.zeros((0, 3), dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
+    assert j.numel() == 0
 
 
 # ---------------------------------------------------------------------------
