@@ -165,6 +165,28 @@ int spec_accept(const void *logits, int logit_dtype, int B, int T, int V, const 
                 int *j_out, int *bonus_out, int *keep_out, int *dev_status, void *scratch,
                 size_t scratch_bytes, cudaStream_t stream);
 
+/*
+ * spec_accept_noalloc -- spec_accept without caller scratch.  The pages have no
+ * counterpart: this entry point exists for callers of this library that cannot
+ * allocate device memory when they accept a round, for example a serving loop
+ * whose device memory is all handed out up front by a fixed arena, or a host
+ * path that must not call cudaMalloc / cudaFree because those calls can
+ * synchronise the device.
+ * Arguments and results are those of spec_accept.  The partial results live in
+ * one fixed device array of KDA_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library holds until the process exits.  Calls whose
+ * spec_accept_scratch_bytes(B, T, V) exceeds it return KDA_EINVAL and launch
+ * nothing.  The first call on a device looks up the array's device address with
+ * that device current; make that first call before any stream capture.  The
+ * array keeps the last call's contents; nothing in it needs to start at zero.
+ * All calls share the one array, so calls that overlap on the GPU (for instance
+ * on two streams at once) race; order them on one stream or with events.
+ * The library calls no allocation routine for this entry point.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+int spec_accept_noalloc(const void *logits, int logit_dtype, int B, int T, int V, const int *drafts,
+                        int *j_out, int *bonus_out, int *keep_out, int *dev_status, cudaStream_t stream);
+
 /* Static description of a return code, and the calling thread's last error text. */
 const char *kda_error_string(int code);
 const char *kda_last_error(void);

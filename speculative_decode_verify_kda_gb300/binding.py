@@ -27,7 +27,7 @@ MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "spec_accept_scratch_bytes", "spec_accept",
-           "kda_error_string", "kda_last_error", "kda_abi_version")
+           "spec_accept_noalloc", "kda_error_string", "kda_last_error", "kda_abi_version")
 
 
 class KdaDims(ctypes.Structure):

@@ -226,3 +226,94 @@ extern "C" int spec_accept(const void *logits, int logit_dtype, int B, int T, in
                                                                             bonus_out, keep_out, dev_status);
     return check_launch("accept_final_kernel");
 }
+
+// ---------------------------------------------------------------------------
+// spec_accept_noalloc: the same two passes, with the per-slice partial results
+// kept in a fixed array that lives in the library's device image instead of
+// caller scratch.  For callers that cannot allocate device memory at the point
+// where they accept a round (see the declaration in kda_spec.h).
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace kda {
+namespace {
+
+constexpr size_t NOALLOC_SCRATCH = KDA_NOALLOC_SCRATCH_BYTES;
+constexpr int MAX_DEVICES = 64;
+
+// One copy per device that loads the library, held until the process exits.
+static __device__ __align__(256) unsigned char g_accept_scratch[NOALLOC_SCRATCH];
+
+std::mutex g_scratch_mutex;
+void *g_scratch_addr[MAX_DEVICES] = {};
+
+// Device address of g_accept_scratch on the current device.  On the host the
+// symbol is only a stand-in, so its address is looked up once per device (with
+// that device current) and cached.
+int noalloc_scratch(void **addr)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(KDA_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= MAX_DEVICES)
+        return fail(KDA_EINVAL, "device ordinal beyond the no-allocation table");
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_accept_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(KDA_ECUDA, std::string("cudaGetSymbolAddress(accept scratch): ") + cudaGetErrorString(e));
+        g_scratch_addr[dev] = p;
+    }
+    *addr = g_scratch_addr[dev];
+    return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int spec_accept_noalloc(const void *logits, int logit_dtype, int B, int T, int V, const int *drafts,
+                                   int *j_out, int *bonus_out, int *keep_out, int *dev_status, cudaStream_t stream)
+{
+    if (B < 0)
+        return fail(KDA_EINVAL, "B must be >= 0");
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
+    if (V < 1)
+        return fail(KDA_EINVAL, "V must be >= 1");
+    if (logit_dtype != KDA_F32 && logit_dtype != KDA_BF16)
+        return fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
+    if (B == 0)
+        return ok();
+    if (!logits || (T > 1 && !drafts))
+        return fail(KDA_EINVAL, "logits and drafts must not be NULL");
+    if (!aligned16(logits))
+        return fail(KDA_EINVAL, "logits must be 16-byte aligned");
+    const size_t need = spec_accept_scratch_bytes(B, T, V);
+    if (need > NOALLOC_SCRATCH)
+        return fail(KDA_EINVAL, "spec_accept_noalloc: B=" + std::to_string(B) + ", T=" + std::to_string(T) +
+                                    ", V=" + std::to_string(V) + " needs " + std::to_string(need) +
+                                    " bytes of scratch, above its fixed " + std::to_string(NOALLOC_SCRATCH) +
+                                    "; call spec_accept with caller scratch instead");
+    void *scratch = nullptr;
+    int rc = noalloc_scratch(&scratch);
+    if (rc)
+        return rc;
+    const int vs = slices_for(V);
+    int chunk = (V + vs - 1) / vs;
+    chunk = (chunk + 7) / 8 * 8;
+    Partial *part = static_cast<Partial *>(scratch);
+    dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
+    if (logit_dtype == KDA_BF16)
+        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+    else
+        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+    rc = check_launch("accept_partial_kernel");
+    if (rc)
+        return rc;
+    const int warps = 4;
+    accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
+                                                                            bonus_out, keep_out, dev_status);
+    return check_launch("accept_final_kernel");
+}
