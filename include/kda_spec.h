@@ -61,11 +61,13 @@ extern "C" {
 #define KDA_EINVAL 1   /* bad argument; nothing was launched                 */
 #define KDA_ENAN 2     /* reserved for host-side reports of KDA_ST_NAN       */
 #define KDA_ECUDA 3    /* a CUDA launch or attribute call failed             */
-#define KDA_ETIMEOUT 4 /* reserved: no kernel here waits on another one      */
+#define KDA_ETIMEOUT 4 /* reserved for host-side reports of KDA_ST_TIMEOUT   */
 
 /* bits OR-ed into *dev_status by kernels */
 #define KDA_ST_NAN 0x1      /* spec_accept: row j (the bonus row) holds a NaN */
 #define KDA_ST_BADKEEP 0x2  /* kda_rollback: a device keep outside 1..T       */
+#define KDA_ST_TIMEOUT 0x4  /* a bulk copy into shared memory did not arrive in
+                               time (bounded wait); the CTA stopped early       */
 
 /* element types of raw rows and logits */
 #define KDA_F32 0

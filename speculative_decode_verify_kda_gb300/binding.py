@@ -21,7 +21,7 @@ D = 128
 TMAX = 15
 HOST_KEEP_MAX = 2048
 OK, EINVAL, ENAN, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
-ST_NAN, ST_BADKEEP = 0x1, 0x2
+ST_NAN, ST_BADKEEP, ST_TIMEOUT = 0x1, 0x2, 0x4
 F32, BF16 = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 
