@@ -96,9 +96,11 @@ struct Layout {
     __host__ __device__ size_t total() const { return bar() + 16; }
 };
 
+// sigmoid through the fast exp2 / reciprocal intrinsics: relative error ~1e-6, far
+// inside the 1e-4 parity bar, and a short dependency chain for the prologue
 __device__ __forceinline__ float sigmoidf_(float z)
 {
-    return __frcp_rn(__fadd_rn(1.0f, expf(-z)));
+    return __fdividef(1.0f, __fadd_rn(1.0f, __expf(-z)));
 }
 
 __device__ __forceinline__ float load_scalar(const void *base, int bf16, size_t idx)
@@ -131,9 +133,9 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar)
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
@@ -241,40 +243,31 @@ __device__ void prefetch_state(const ScanParams &p, const Layout &lay, unsigned 
                   16384, bar);
 }
 
-// Warp 0 fills the rest of the stage with unit u's raw rows, ring and conv weights.
+// All threads fill the rest of the stage with unit u's raw rows (16-byte cp.async,
+// spread over the CTA) and thread 32 adds the ring and conv weights as two bulk
+// copies.  The input mbarrier completes once every thread's cp.async has landed
+// (NT no-increment arrivals) and the bulk bytes have arrived (one expect_tx arrival).
 __device__ void prefetch_inputs(const ScanParams &p, const Layout &lay, unsigned char *smem, uint32_t bar,
-                                int u, int lane)
+                                int u, int tid)
 {
     const Unit x = unit_of(p, u);
-    const int rbytes = D * lay.es;
-    const uint32_t total = 4 * x.T * rbytes + 9 * D * 4 + 3 * D * 16;
-    if (lane == 0)
-        mbar_expect_tx(bar, total);
-    __syncwarp();
+    const int rbytes = D * lay.es, cpr = rbytes / 16, per_stream = x.T * cpr;
     const void *xs[4] = {p.xq, p.xk, p.xv, p.xg};
-    const int ncopy = 4 * x.T + 2;
-    for (int c = lane; c < ncopy; c += 32) {
-        if (c < 4 * x.T) {
-            const int s = c / x.T, t = c % x.T;
-            const char *src = static_cast<const char *>(xs[s]) +
-                              ((static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h) * static_cast<size_t>(rbytes);
-            bulk_load(smem_addr(smem + lay.stage_rows() + static_cast<size_t>(s * lay.tcap + t) * rbytes), src,
-                      rbytes, bar);
-        } else if (c == 4 * x.T) {
-            bulk_load(smem_addr(smem + lay.stage_ring()), p.ring_in + static_cast<size_t>(u) * 9 * D, 9 * D * 4, bar);
-        } else {
-            bulk_load(smem_addr(smem + lay.stage_w()), p.conv_w + (static_cast<size_t>(x.l) * p.H + x.h) * 3 * D * 4,
-                      3 * D * 16, bar);
-        }
+    for (int c = tid; c < 4 * per_stream; c += NT) {
+        const int s = c / per_stream, rem = c - s * per_stream, t = rem / cpr, q = rem - t * cpr;
+        const char *src = static_cast<const char *>(xs[s]) +
+                          ((static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h) * static_cast<size_t>(rbytes) + 16 * q;
+        const uint32_t dst = smem_addr(smem + lay.stage_rows() + static_cast<size_t>(s * lay.tcap + t) * rbytes + 16 * q);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
     }
-}
-
-__device__ __forceinline__ float load_beta(const ScanParams &p, int u, int lane)
-{
-    const Unit x = unit_of(p, u);
-    if (lane >= x.T)
-        return 0.f;
-    return load_scalar(p.xb, p.bf16, (static_cast<size_t>(x.lb) * p.T_rows + lane) * p.H + x.h);
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+    if (tid == 32) {  // not thread 0, which tends the state stage
+        fence_proxy_async();  // the prologue's generic reads of the stage come first
+        mbar_expect_tx(bar, 9 * D * 4 + 3 * D * 16);
+        bulk_load(smem_addr(smem + lay.stage_ring()), p.ring_in + static_cast<size_t>(u) * 9 * D, 9 * D * 4, bar);
+        bulk_load(smem_addr(smem + lay.stage_w()), p.conv_w + (static_cast<size_t>(x.l) * p.H + x.h) * 3 * D * 4,
+                  3 * D * 16, bar);
+    }
 }
 
 // four consecutive channels of stream s at extended index n (0..2 ring slots, 3+t row t)
@@ -291,7 +284,7 @@ __device__ __forceinline__ float4 fetch4(const Layout &lay, const unsigned char 
 }
 
 // Persistent: each CTA walks units blockIdx.x, +gridDim.x, ...; while it scans
-// one unit out of registers, the bulk copies of its next unit are in flight.
+// one unit out of registers, the copies of its next unit are in flight.
 __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__ ScanParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -310,18 +303,16 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
     float *skq = reinterpret_cast<float *>(smem + lay.kq());
 
     if (tid == 0) {
-        mbar_init(bar_state);
-        mbar_init(bar_in);
+        mbar_init(bar_state, 1);
+        mbar_init(bar_in, NT + 1);
     }
     __syncthreads();
-
     int u = next_live(p, blockIdx.x, n);
-    if (u < n && wi == 0) {
-        if (lane == 0)
+    if (u < n) {
+        if (tid == 0)
             prefetch_state(p, lay, smem, bar_state, u);
-        prefetch_inputs(p, lay, smem, bar_in, u, lane);
+        prefetch_inputs(p, lay, smem, bar_in, u, tid);
     }
-    float beta_raw = (u < n && wi == 0) ? load_beta(p, u, lane) : 0.f;
     uint32_t parity_state = 0, parity_in = 0;
 
     while (u < n) {
@@ -343,7 +334,21 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
         {
             const float4 *cw = reinterpret_cast<const float4 *>(smem + lay.stage_w());
             const int c0 = 4 * lane;
+            // conv ring after the round (last 3 of [ring, rows]) and its snapshot; issued
+            // first, they depend on nothing computed here
+            float4 *rout = reinterpret_cast<float4 *>(p.ring_out + static_cast<size_t>(u) * 9 * D);
+            float4 *rsnap = p.ring_snap ? reinterpret_cast<float4 *>(p.ring_snap + static_cast<size_t>(u) * 9 * D)
+                                        : nullptr;
+            for (int idx = tid; idx < 9 * D / 4; idx += NT) {
+                const int s = idx / 96, slot = (idx % 96) / 32, c4 = idx % 32;
+                rout[idx] = fetch4(lay, smem, s, T + slot, 4 * c4);
+                if (rsnap)
+                    rsnap[idx] = fetch4(lay, smem, s, slot, 4 * c4);
+            }
             for (int t = wi; t < T; t += NW) {
+                // the row's beta load goes out first; its latency hides behind the conv
+                const float rb = lane == 0 ? load_scalar(p.xb, p.bf16, (static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h)
+                                           : 0.f;
                 float y[3][4];
 #pragma unroll
                 for (int s = 0; s < 3; ++s) {
@@ -380,29 +385,18 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
                 float dv[4];
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc)
-                    dv[cc] = expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(rgv[cc])));
+                    dv[cc] = __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(rgv[cc])));
                 float *vt = vec + t * 4 * D + c0;
                 *reinterpret_cast<float4 *>(vt) = make_float4(dv[0], dv[1], dv[2], dv[3]);
                 *reinterpret_cast<float4 *>(vt + D) = make_float4(kh[0], kh[1], kh[2], kh[3]);
                 *reinterpret_cast<float4 *>(vt + 2 * D) = make_float4(qh[0], qh[1], qh[2], qh[3]);
                 *reinterpret_cast<float4 *>(vt + 3 * D) = make_float4(y[2][0], y[2][1], y[2][2], y[2][3]);
-                if (lane == 0)
+                if (lane == 0) {
                     skq[t] = kq;
-            }
-            if (wi == 0 && lane < T)
-                sbeta[lane] = sigmoidf_(beta_raw);
-            // conv ring after the round (last 3 of [ring, rows]) and its snapshot
-            float4 *rout = reinterpret_cast<float4 *>(p.ring_out + static_cast<size_t>(u) * 9 * D);
-            float4 *rsnap = p.ring_snap ? reinterpret_cast<float4 *>(p.ring_snap + static_cast<size_t>(u) * 9 * D)
-                                        : nullptr;
-            for (int idx = tid; idx < 9 * D / 4; idx += NT) {
-                const int s = idx / 96, slot = (idx % 96) / 32, c4 = idx % 32;
-                rout[idx] = fetch4(lay, smem, s, T + slot, 4 * c4);
-                if (rsnap)
-                    rsnap[idx] = fetch4(lay, smem, s, slot, 4 * c4);
+                    sbeta[t] = sigmoidf_(rb);
+                }
             }
         }
-
         // ---- state: stage -> registers ---------------------------------------------
         arrived = mbar_wait(bar_state, parity_state);
         if (__syncthreads_or(!arrived)) {
@@ -414,6 +408,14 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
             return;
         }
         parity_state ^= 1u;
+        if (tid == 0 && p.s_snap) {
+            // the pre-round state leaves as a bulk store straight from the stage; the stage
+            // holds only what the bulk load wrote, so no proxy fence is needed before it
+            for (int c = 0; c < 4; ++c)
+                bulk_store(p.s_snap + static_cast<size_t>(u) * D * D + c * 4096,
+                           smem_addr(smem + lay.stage_state() + c * 16384), 16384);
+            bulk_commit();
+        }
         float2 S[8][4];  // S[rp][c] = (S[16rg + 2rp][jbase + c], S[16rg + 2rp + 1][jbase + c])
         {
             const float *Ss = reinterpret_cast<const float *>(smem + lay.stage_state());
@@ -430,33 +432,19 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
         }
         __syncthreads();  // every generic read of the stage is done; vec, beta, k.q are written
 
-        // ---- snapshot out of the stage, refill the stage with the next unit ----------
-        // The pre-round state leaves as a bulk store straight from the stage while this
-        // unit scans; the next unit's state is fetched once that store has read the stage.
+        // ---- refill the stage with the next unit while this one scans ----------------
         const int un = next_live(p, u + gridDim.x, n);
-        bool state_due = un < n;  // the next unit's state fetch is still to be issued
-        if (wi == 0) {
-            if (lane == 0) {
+        // the next unit's state fetch waits until the snapshot store has read the stage
+        bool state_due = un < n;
+        if (state_due && !p.s_snap) {
+            if (tid == 0) {
                 fence_proxy_async();
-                if (p.s_snap) {
-                    for (int c = 0; c < 4; ++c)
-                        bulk_store(p.s_snap + static_cast<size_t>(u) * D * D + c * 4096,
-                                   smem_addr(smem + lay.stage_state() + c * 16384), 16384);
-                    bulk_commit();
-                } else if (state_due) {
-                    prefetch_state(p, lay, smem, bar_state, un);
-                }
+                prefetch_state(p, lay, smem, bar_state, un);
             }
-            if (!p.s_snap)
-                state_due = false;
-            if (un < n) {
-                fence_proxy_async();
-                prefetch_inputs(p, lay, smem, bar_in, un, lane);
-            }
-            beta_raw = un < n ? load_beta(p, un, lane) : 0.f;
-        } else if (!p.s_snap) {
             state_due = false;
         }
+        if (un < n)
+            prefetch_inputs(p, lay, smem, bar_in, un, tid);
 
         // ---- the T-row gated delta rule -----------------------------------------
         float *outp = p.out ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum : nullptr;
@@ -562,6 +550,7 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
 struct DeviceInfo {
     int sms = 0;
     int smem_set = 0;
+    int per_sm[2][KDA_TMAX + 1] = {};  // CTAs per SM by (raw element size 2/4, rows)
 };
 
 int launch_scan(const ScanParams &p, int tcap, cudaStream_t stream)
@@ -593,10 +582,14 @@ int launch_scan(const ScanParams &p, int tcap, cudaStream_t stream)
             return fail(KDA_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
         di.smem_set = static_cast<int>(most);
     }
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_scan_kernel, NT, smem);
-    if (e != cudaSuccess || per_sm < 1)
-        return fail(KDA_ECUDA, "kda_scan_kernel does not fit on an SM");
+    int &per_sm = di.per_sm[p.bf16 ? 0 : 1][tcap];
+    if (per_sm == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_scan_kernel, NT, smem);
+        if (e != cudaSuccess || per_sm < 1) {
+            per_sm = 0;
+            return fail(KDA_ECUDA, "kda_scan_kernel does not fit on an SM");
+        }
+    }
     const long long grid = std::min<long long>(units, static_cast<long long>(di.sms) * per_sm);
     kda_scan_kernel<<<static_cast<unsigned>(grid), NT, smem, stream>>>(p);
     return check_launch("kda_scan_kernel");
