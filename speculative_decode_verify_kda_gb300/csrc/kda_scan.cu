@@ -1,29 +1,41 @@
 // kda_scan.cu -- the fused KDA verify walk (short conv, activations, gated delta
 // rule) for sm_103a, and the accept-j rollback that replays it.
 //
-// One persistent kernel serves both.  A unit is one (layer, session, head): its
-// 128 x 128 f32 state, the raw rows of its T drafted positions, its conv ring and
-// conv weights.  Each CTA (8 warps, 2 per SM) walks units blockIdx.x, +gridDim.x,
-// ... and keeps one unit's state in registers for its whole T-row loop, so the 64
-// KiB state of a head crosses HBM once in and once out per round.
+// A unit is one (layer, session, head): its 128 x 128 f32 state, the raw rows of
+// its T drafted positions, its conv ring and conv weights.  One persistent CTA per
+// SM walks the units blockIdx.x, +gridDim.x, ... with three kinds of warps that
+// hand work to each other through mbarriers in shared memory:
 //
-// Memory pipeline per CTA (bulk copies = the 1D TMA, counted by mbarriers):
-//   - the next unit's raw rows, ring and weights are bulk-loaded into a stage as
-//     soon as the current unit's prologue has consumed them;
-//   - the current unit's pre-round state leaves the stage as a bulk store to the
-//     snapshot (the fused snapshot write) while the unit scans, after which the
-//     next unit's state is bulk-loaded into the stage;
-//   - the scanned state is stored from registers.
-// Every wait on an mbarrier is bounded; a wait that runs out sets KDA_ST_TIMEOUT,
-// lets the copies in flight land and ends the CTA.
+//   copy warp (1)      TMA: the unit's state arrives as four 2D tensor copies
+//                      (32 columns x 128 rows each, 128-byte swizzle) into one of
+//                      two state slots, two units ahead; as soon as it lands it
+//                      leaves again as four tensor stores to the snapshot (the
+//                      fused snapshot write).  The unit's raw q, k, v, g rows are
+//                      staged with 1D bulk copies one unit ahead.
+//   prologue warps (4) one per stream (q, k, v, g), one unit ahead of the scan:
+//                      width-4 causal conv + SiLU of q, k, v (mini fixture
+//                      linear_attn_config of glm5_spec_ppn_gate.rs:
+//                      short_conv_kernel_size 4, head_dim 128, gate_lower_bound
+//                      -5.0) sliding along the rows in registers, the L2 norms of
+//                      q and k, k.q, the forget gate d = exp(-5 sigmoid(raw_g))
+//                      and beta = sigmoid(raw_beta), written as the round's scan
+//                      inputs into one of two shared buffers; they also re-roll
+//                      the conv ring (and snapshot it).
+//   scan warps (8)     hold the unit's state in registers for its whole T-row
+//                      loop and write it back once: each 64 KiB head state
+//                      crosses HBM once in and once out per round, plus the
+//                      snapshot copy.
 //
-// Register tile: lane 4 rg + cg of warp wi holds key rows 16 rg .. 16 rg + 15 of
-// value columns 16 wi + 4 cg .. +3, with row pairs packed into float2 so each
+// Register tile: lane 4 rg + cg of scan warp wi holds key rows rg + 8 r (r < 16)
+// of value columns 16 wi + 4 cg .. +3, row pairs packed into float2 so each
 // element operation is one lane of a packed f32x2 instruction (__fmul2_rn,
-// __ffma2_rn).  Per row t (glm_spec.rs module doc, VERIFY-ROW BATCHING: the
-// recurrence stays sequential inside one launch, the in-kernel T-loop being the
-// chained t=1 program):
-//   S' = d_t (.) S               d = exp(g), g = -5 sigmoid(raw_g)
+// __ffma2_rn).  Rows rg + 8 r share their 128-byte swizzle phase.  The scan
+// inputs of a row hold each row group's d, k and q contiguously, so a quarter
+// warp reads two broadcast addresses per load.
+// Per row t (glm_spec.rs module doc, VERIFY-ROW BATCHING: the recurrence stays
+// sequential inside one launch, the in-kernel T-loop being the chained t=1
+// program):
+//   S' = d_t (.) S               d = exp(g)
 //   u  = S'^T k,  e = S'^T q     one register sweep, then a 3-step shuffle
 //                                reduce-scatter over the 8 row groups
 //   w  = beta (v - u)
@@ -33,16 +45,20 @@
 // not depend on T or on the unit, so T rows in one launch and T launches of one
 // row give the same bits, and so do a rollback replay and a fresh verify.
 //
-// Prologue per unit: one warp per row computes the width-4 causal conv + SiLU of
-// q, k, v (mini fixture linear_attn_config of glm5_spec_ppn_gate.rs:
-// short_conv_kernel_size 4, head_dim 128, gate_lower_bound -5.0), the L2 norms
-// of q and k, k.q, the gates and beta, with one fixed reduction tree per row,
-// into shared memory that the T-loop reads as broadcast float4 loads.
+// Rollback runs the same kernel from the snapshot over rows 0..keep-1 of the
+// stashed raw rows (the conv re-runs inside the replay), with outputs and the
+// snapshot store switched off.
+// Every wait on an mbarrier is bounded.  A wait that runs out sets
+// KDA_ST_TIMEOUT and a shared abort flag that ends every warp of the CTA; the
+// copy warp first lets its copies in flight land.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <string>
 
 #include "kda_internal.h"
@@ -51,57 +67,72 @@ namespace kda {
 namespace {
 
 constexpr int D = 128;
-constexpr int NW = 8;           // warps per CTA
-constexpr int NT = NW * 32;     // threads per CTA
+constexpr int NSCAN = 8;                   // scan warps
+constexpr int NPRO = 4;                    // prologue warps: q, k, v, g
+constexpr int WCOPY = NSCAN + NPRO;        // the copy warp
+constexpr int NT = (NSCAN + NPRO + 1) * 32;
+constexpr int GRP = 52;                    // floats per row group of a scan-input row: d, k, q (16 each), pad
+constexpr int SI_V = 8 * GRP;              // offset of v (natural order) in a scan-input row
+constexpr int SI_ROW = SI_V + D;           // floats per scan-input row
 constexpr float L2_EPS = 1e-6f;
 constexpr float GATE_LOWER_BOUND = -5.0f;
 constexpr float OUT_SCALE = 0.0883883476483184405501f;  // 1 / sqrt(128)
+constexpr uint64_t WAIT_NS = 1000000000ull;  // an mbarrier wait gives up after one second
+
+// mbarriers: state slots full/empty, scan-input buffers full/empty, raw-row stages
+// full/empty, and the prologue warps' own rendezvous before k.q
+enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, B_STG_EMPTY = 10, B_PRO = 12,
+       NBARS = 13 };
 
 enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2 };
 
 struct ScanParams {
-    const float *s_in;   // [L][B][H][D][D]
-    float *s_out;
-    float *s_snap;       // nullable: receives s_in of each unit
+    CUtensorMap tm_in;     // state read: [units * 128 rows][128] f32, box 32 x 128, 128B swizzle
+    CUtensorMap tm_snap;   // snapshot write, same geometry (unused without s_snap)
+    float *s_out;          // [L][B][H][D][D]
+    float *s_snap;         // nullable: receives the state read through tm_in
     const float *ring_in;  // [L][B][H][3][3][D]
     float *ring_out;
-    float *ring_snap;    // nullable: receives ring_in of each unit
-    const float *conv_w; // [L][H][3][D][4]
+    float *ring_snap;      // nullable: receives ring_in of each unit
+    const float *conv_w;   // [L][H][3][D][4]
     const void *xq, *xk, *xv, *xg, *xb;  // [L][B][T_rows][H][D], xb [L][B][T_rows][H]
-    float *out;          // nullable: [L][B][T_rows][H][D]
-    const int *keep_dev; // KEEP_DEVICE: [B]
-    int *status;         // nullable device status word
+    float *out;            // nullable: [L][B][T_rows][H][D]
+    const int *keep_dev;   // KEEP_DEVICE: [B]
+    int *status;           // nullable device status word
     int L, B, H;
-    int T_rows;          // row count of the raw-row tensors
-    int T_run;           // rows to run for KEEP_NONE
+    int T_rows;            // row count of the raw-row tensors
+    int T_run;             // rows to run for KEEP_NONE
+    int tcap;              // most rows any unit runs (sizes the buffers)
+    int nstg;              // raw-row stages: 2 where shared memory allows, else 1
     int bf16;
     int keep_mode;
     unsigned char keep_host[KDA_HOST_KEEP_MAX];
 };
 
-constexpr int MAX_POLLS = 1 << 24;  // mbarrier polls (with back-off, a few seconds) before giving up
-
-// Shared memory of a CTA whose units run at most `tcap` rows; `es` is the raw-row
-// element size.  The stage holds the NEXT unit's inputs, filled by bulk copies.
+// Shared memory, from a 1024-byte aligned base (the 128-byte swizzle repeats
+// every 1024 bytes): two 64 KiB state slots, two scan-input buffers of tcap rows,
+// their {beta, k.q} scalars, nstg raw-row stages [4 streams][tcap][128], the
+// mbarriers and the abort flag.
 struct Layout {
-    int tcap, es;
-    __host__ __device__ size_t stage_state() const { return 0; }                       // [128][128] f32
-    __host__ __device__ size_t stage_rows() const { return (size_t)D * D * 4; }         // [4: q,k,v,g][tcap][128]
-    __host__ __device__ size_t stage_ring() const { return stage_rows() + (size_t)4 * tcap * D * es; }  // [3][3][128]
-    __host__ __device__ size_t stage_w() const { return stage_ring() + (size_t)9 * D * 4; }   // [3][128] x 4 taps
-    __host__ __device__ size_t vec() const { return stage_w() + (size_t)3 * D * 16; }         // [tcap][4][128] f32
-    __host__ __device__ size_t beta() const { return vec() + (size_t)tcap * 4 * D * 4; }      // [16] f32
-    __host__ __device__ size_t kq() const { return beta() + 64; }                             // [16] f32
-    __host__ __device__ size_t bar() const { return kq() + 64; }  // mbarriers: [0] state stage, [1] the rest
-    __host__ __device__ size_t total() const { return bar() + 16; }
+    int tcap, es, nstg;
+    __host__ __device__ size_t slot(int s) const { return static_cast<size_t>(s) * D * D * 4; }
+    __host__ __device__ size_t si(int b) const { return slot(2) + static_cast<size_t>(b) * tcap * SI_ROW * 4; }
+    __host__ __device__ size_t sc(int b) const { return si(2) + static_cast<size_t>(b) * 16 * 8; }
+    __host__ __device__ size_t row_bytes() const { return static_cast<size_t>(D) * es; }
+    __host__ __device__ size_t stg(int b) const { return sc(2) + static_cast<size_t>(b) * 4 * tcap * row_bytes(); }
+    __host__ __device__ size_t bars() const { return stg(nstg); }
+    __host__ __device__ size_t flag() const { return bars() + NBARS * 8; }
+    __host__ __device__ size_t total() const { return flag() + 16 + 1024; }  // + alignment slack
 };
 
 // sigmoid through the fast exp2 / reciprocal intrinsics: relative error ~1e-6, far
-// inside the 1e-4 parity bar, and a short dependency chain for the prologue
+// inside the 1e-4 parity bar, and a short dependency chain
 __device__ __forceinline__ float sigmoidf_(float z)
 {
     return __fdividef(1.0f, __fadd_rn(1.0f, __expf(-z)));
 }
+
+__device__ __forceinline__ float silu(float a) { return __fmul_rn(a, sigmoidf_(a)); }
 
 __device__ __forceinline__ float load_scalar(const void *base, int bf16, size_t idx)
 {
@@ -125,9 +156,7 @@ __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, f
     return __fmaf_rn(w.w, x3, __fmaf_rn(w.z, x2, __fmaf_rn(w.y, x1, __fmul_rn(w.x, x0))));
 }
 
-__device__ __forceinline__ float silu(float a) { return __fmul_rn(a, sigmoidf_(a)); }
-
-// ---- bulk copies and the mbarrier that counts their bytes -------------------
+// ---- TMA, bulk copies and mbarriers ------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -136,7 +165,11 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
@@ -144,17 +177,34 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// 1D bulk copy global -> shared, counted in bytes by `bar`
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
 {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
-// bulk store of shared memory to global memory, tracked by bulk groups
-__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+// 2D tensor copy global -> shared of the box at (x, y), counted in bytes by `bar`
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y, uint32_t bar)
 {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+// 2D tensor copy shared -> global of the box at (x, y), tracked by bulk groups
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, int x, int y, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -167,27 +217,65 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+// Shared control block of a CTA: mbarrier base address, abort flag, status word.
+struct Ctl {
+    uint32_t bars;
+    volatile int *abort;
+    int *status;
+    __device__ uint32_t bar(int i) const { return bars + 8u * i; }
+};
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
 {
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}" : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
-// Bounded wait for the phase with `parity`; false after MAX_POLLS polls.
-__device__ bool mbar_wait(uint32_t bar, uint32_t parity)
+// Bounded warp-wide wait for the phase of barrier `i` with `parity`.  Every lane
+// acquires the phase itself; the warp leaves together.  False once the CTA is
+// aborting, or after WAIT_NS of waiting (which starts the abort).
+__device__ bool warp_wait(const Ctl &c, int i, uint32_t parity)
 {
-    for (int i = 0; i < MAX_POLLS; ++i) {
-        if (mbar_try(bar, parity))
+    const uint32_t a = c.bar(i);
+    if (__all_sync(0xffffffffu, mbar_try(a, parity)))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (__all_sync(0xffffffffu, mbar_try(a, parity)))
             return true;
-        if (i >= 1024)
-            __nanosleep(64);
+        if ((n & 15) == 0) {
+            if (__any_sync(0xffffffffu, *c.abort != 0))
+                return false;
+            if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > WAIT_NS))
+                break;
+        }
+        if (n >= 64)
+            __nanosleep(128);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        if (c.status)
+            atomicOr(c.status, KDA_ST_TIMEOUT);
+        *c.abort = 1;
     }
     return false;
 }
 
-// ---- units --------------------------------------------------------------------
+// The same bounded wait for one thread that must not leave early (copies in flight).
+__device__ bool drain_wait(uint32_t a, uint32_t parity)
+{
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 0;; ++n) {
+        if (mbar_try(a, parity))
+            return true;
+        if ((n & 15) == 0 && globaltimer_ns() - t0 > WAIT_NS)
+            return false;
+        if (n >= 64)
+            __nanosleep(128);
+    }
+}
+
+// ---- units --------------------------------------------------------------------------
 struct Unit {
     int h, b, l, T;
     long long lb;  // l * B + b
@@ -212,7 +300,7 @@ __device__ __forceinline__ int unit_rows(const ScanParams &p, int b)
 __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
 {
     Unit x;
-    x.h = static_cast<int>(u % p.H);
+    x.h = u % p.H;
     x.lb = u / p.H;
     x.b = static_cast<int>(x.lb % p.B);
     x.l = static_cast<int>(x.lb / p.B);
@@ -220,272 +308,403 @@ __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
     return x;
 }
 
-// the first unit at or after u (stepping by the grid) that has rows to run
-__device__ int next_live(const ScanParams &p, int u, int n)
+// The first unit at or after u (stepping by the grid) that has rows to run.  Every
+// warp walks the same sequence; only the copy warp's lane 0 reports bad keeps.
+__device__ int next_live(const ScanParams &p, int u, int n, bool report)
 {
     for (; u < n; u += gridDim.x) {
-        const int T = unit_rows(p, static_cast<int>((u / p.H) % p.B));
+        const int T = unit_rows(p, (u / p.H) % p.B);
         if (T > 0)
             return u;
-        if (T < 0 && p.status && threadIdx.x == 0)
+        if (T < 0 && report && p.status)
             atomicOr(p.status, KDA_ST_BADKEEP);  // the session is left untouched
     }
     return n;
 }
 
-// One thread fills the state stage with unit u's 64 KiB state.
-__device__ void prefetch_state(const ScanParams &p, const Layout &lay, unsigned char *smem, uint32_t bar,
-                               int u)
+// ---- copy warp ----------------------------------------------------------------------
+// Unit u's 64 KiB state into a slot: four boxes of 32 columns x 128 rows (lane 0).
+__device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, uint32_t bar, int u)
 {
     mbar_expect_tx(bar, D * D * 4);
-    for (int c = 0; c < 4; ++c)
-        bulk_load(smem_addr(smem + lay.stage_state() + c * 16384), p.s_in + static_cast<size_t>(u) * D * D + c * 4096,
-                  16384, bar);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        tma_load_2d(slot + b * 16384, &p.tm_in, 32 * b, u * D, bar);
 }
 
-// All threads fill the rest of the stage with unit u's raw rows (16-byte cp.async,
-// spread over the CTA) and thread 32 adds the ring and conv weights as two bulk
-// copies.  The input mbarrier completes once every thread's cp.async has landed
-// (NT no-increment arrivals) and the bulk bytes have arrived (one expect_tx arrival).
-__device__ void prefetch_inputs(const ScanParams &p, const Layout &lay, unsigned char *smem, uint32_t bar,
-                                int u, int tid)
+// Unit u's raw q, k, v, g rows into the stage, one bulk copy per (stream, row),
+// spread over the warp; lane 0 arms the barrier with the byte count first.
+__device__ void issue_stage(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, int u, int lane)
 {
     const Unit x = unit_of(p, u);
-    const int rbytes = D * lay.es, cpr = rbytes / 16, per_stream = x.T * cpr;
-    const void *xs[4] = {p.xq, p.xk, p.xv, p.xg};
-    for (int c = tid; c < 4 * per_stream; c += NT) {
-        const int s = c / per_stream, rem = c - s * per_stream, t = rem / cpr, q = rem - t * cpr;
-        const char *src = static_cast<const char *>(xs[s]) +
-                          ((static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h) * static_cast<size_t>(rbytes) + 16 * q;
-        const uint32_t dst = smem_addr(smem + lay.stage_rows() + static_cast<size_t>(s * lay.tcap + t) * rbytes + 16 * q);
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-    }
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-    if (tid == 32) {  // not thread 0, which tends the state stage
-        fence_proxy_async();  // the prologue's generic reads of the stage come first
-        mbar_expect_tx(bar, 9 * D * 4 + 3 * D * 16);
-        bulk_load(smem_addr(smem + lay.stage_ring()), p.ring_in + static_cast<size_t>(u) * 9 * D, 9 * D * 4, bar);
-        bulk_load(smem_addr(smem + lay.stage_w()), p.conv_w + (static_cast<size_t>(x.l) * p.H + x.h) * 3 * D * 4,
-                  3 * D * 16, bar);
+    const uint32_t rb = static_cast<uint32_t>(lay.row_bytes());
+    if (lane == 0)
+        mbar_expect_tx(bar, 4u * x.T * rb);
+    __syncwarp();
+    fence_proxy_async();  // the prologue's generic reads of the stage come first
+    for (int i = lane; i < 4 * x.T; i += 32) {
+        const int s = i / x.T, t = i - s * x.T;
+        const void *base = s == 0 ? p.xq : s == 1 ? p.xk : s == 2 ? p.xv : p.xg;
+        const char *src = static_cast<const char *>(base) +
+                          ((static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h) * rb;
+        bulk_load(stg + (s * lay.tcap + t) * rb, src, rb, bar);
     }
 }
 
-// four consecutive channels of stream s at extended index n (0..2 ring slots, 3+t row t)
-__device__ __forceinline__ float4 fetch4(const Layout &lay, const unsigned char *smem, int s, int n, int c0)
+// The copy warp runs two units ahead of the scan for states and nstg units ahead
+// of the prologue for raw rows, and sends each state on to the snapshot as soon
+// as it has landed.  Unit k uses state slot k % 2 and raw-row stage k % nstg.
+__device__ void copy_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
-    if (n < 3)
-        return *reinterpret_cast<const float4 *>(smem + lay.stage_ring() + ((s * 3 + n) * D + c0) * 4);
-    const unsigned char *r = smem + lay.stage_rows() + (static_cast<size_t>(s * lay.tcap + n - 3) * D + c0) * lay.es;
+    const int lane = threadIdx.x & 31;
+    const uint32_t slot0 = smem_addr(sm + lay.slot(0)), stg0 = smem_addr(sm + lay.stg(0));
+    const uint32_t stage_bytes = static_cast<uint32_t>(lay.stg(1) - lay.stg(0));
+    constexpr uint32_t SLOT = D * D * 4;
+    // copies in flight, for the drain on abort: state slot s / stage b and the
+    // parity of the phase that will count them
+    bool pend0 = false, pend1 = false, pstg0 = false, pstg1 = false;
+    uint32_t par0 = 0, par1 = 0, spar0 = 0, spar1 = 0;
+    int uk = next_live(p, blockIdx.x, n, lane == 0);
+    int u1 = uk < n ? next_live(p, uk + gridDim.x, n, lane == 0) : n;
+    int u2 = u1 < n ? next_live(p, u1 + gridDim.x, n, lane == 0) : n;
+    if (uk < n) {
+        if (lane == 0)
+            issue_state(p, slot0, c.bar(B_STATE_FULL), uk);
+        pend0 = true;
+        issue_stage(p, lay, stg0, c.bar(B_STG_FULL), uk, lane);
+        pstg0 = true;
+    }
+    if (u1 < n) {
+        if (lane == 0)
+            issue_state(p, slot0 + SLOT, c.bar(B_STATE_FULL + 1), u1);
+        pend1 = true;
+        if (lay.nstg == 2) {
+            issue_stage(p, lay, stg0 + stage_bytes, c.bar(B_STG_FULL + 1), u1, lane);
+            pstg1 = true;
+        }
+    }
+    bool aborted = false;
+    for (int k = 0; uk < n; ++k) {
+        const int s = k & 1;
+        const uint32_t ph = (k >> 1) & 1;
+        // unit k's state has landed: the fused snapshot leaves straight from the slot
+        if (!warp_wait(c, B_STATE_FULL + s, ph)) {
+            aborted = true;
+            break;
+        }
+        (s ? pend1 : pend0) = false;
+        if (p.s_snap && lane == 0) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                tma_store_2d(&p.tm_snap, 32 * b, uk * D, slot0 + s * SLOT + b * 16384);
+            bulk_commit();
+        }
+        // the prologue is done with unit k's raw rows: stage unit k + nstg's there
+        const int b = lay.nstg == 2 ? s : 0;
+        const int m = lay.nstg == 2 ? k >> 1 : k;  // uses of stage b before unit k
+        if (!warp_wait(c, B_STG_EMPTY + b, m & 1)) {
+            aborted = true;
+            break;
+        }
+        (b ? pstg1 : pstg0) = false;
+        const int ustg = lay.nstg == 2 ? u2 : u1;
+        if (ustg < n) {
+            issue_stage(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + b), ustg, lane);
+            (b ? pstg1 : pstg0) = true;
+            (b ? spar1 : spar0) = (m + 1) & 1;
+        }
+        // the scan warps hold unit k in registers and the snapshot store has read
+        // the slot: load unit k+2 into it
+        if (u2 < n) {
+            if (!warp_wait(c, B_STATE_EMPTY + s, ph)) {
+                aborted = true;
+                break;
+            }
+            if (lane == 0) {
+                bulk_wait_read();
+                fence_proxy_async();
+                issue_state(p, slot0 + s * SLOT, c.bar(B_STATE_FULL + s), u2);
+            }
+            (s ? pend1 : pend0) = true;
+            (s ? par1 : par0) = ((k + 2) >> 1) & 1;
+        }
+        uk = u1;
+        u1 = u2;
+        u2 = u2 < n ? next_live(p, u2 + gridDim.x, n, lane == 0) : n;
+    }
+    if (lane == 0) {
+        if (aborted) {  // copies still in flight must land before the CTA leaves
+            if (pend0)
+                drain_wait(c.bar(B_STATE_FULL), par0);
+            if (pend1)
+                drain_wait(c.bar(B_STATE_FULL + 1), par1);
+            if (pstg0)
+                drain_wait(c.bar(B_STG_FULL), spar0);
+            if (pstg1)
+                drain_wait(c.bar(B_STG_FULL + 1), spar1);
+        }
+        bulk_wait_all();  // the snapshot stores leave before the CTA's shared memory does
+    }
+}
+
+// ---- prologue warps -----------------------------------------------------------------
+// What a prologue lane loads for a unit before it needs it: for q, k, v the conv
+// weights and ring slots of its 4 channels, for g the raw beta of row `lane`.
+struct Pre {
+    float4 w[4];     // w[m]: the 4 taps of channel 4 lane + m
+    float4 ring[3];  // ring slot 0 (oldest) .. 2 of channels 4 lane .. +3
+    float beta;
+};
+
+__device__ __forceinline__ void load_pre(const ScanParams &p, int u, int pw, int lane, Pre &pr)
+{
+    const Unit x = unit_of(p, u);
+    if (pw < 3) {
+        const float4 *w = reinterpret_cast<const float4 *>(p.conv_w) +
+                          ((static_cast<size_t>(x.l) * p.H + x.h) * 3 + pw) * D + 4 * lane;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            pr.w[m] = w[m];
+        const float4 *r = reinterpret_cast<const float4 *>(p.ring_in + (static_cast<size_t>(u) * 3 + pw) * 3 * D) + lane;
+#pragma unroll
+        for (int sl = 0; sl < 3; ++sl)
+            pr.ring[sl] = r[sl * (D / 4)];
+    } else {
+        pr.beta = lane < x.T ? load_scalar(p.xb, p.bf16, (static_cast<size_t>(x.lb) * p.T_rows + lane) * p.H + x.h)
+                             : 0.f;
+    }
+}
+
+// channels 4 lane .. +3 of raw row t of stream s in the stage, widened to f32
+__device__ __forceinline__ float4 stage4(const unsigned char *stg, const Layout &lay, int s, int t, int lane)
+{
+    const unsigned char *r = stg + (static_cast<size_t>(s) * lay.tcap + t) * lay.row_bytes();
     if (lay.es == 4)
-        return *reinterpret_cast<const float4 *>(r);
-    const uint2 v = *reinterpret_cast<const uint2 *>(r);
+        return reinterpret_cast<const float4 *>(r)[lane];
+    const uint2 v = reinterpret_cast<const uint2 *>(r)[lane];
     return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
                        __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
 }
 
-// Persistent: each CTA walks units blockIdx.x, +gridDim.x, ...; while it scans
-// one unit out of registers, the copies of its next unit are in flight.
-__global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__ ScanParams p)
+// Key channel i of a d / k-hat / q-hat vector sits at row group i % 8, slot i / 8
+// of a scan-input row (blocks at 0, 16, 32 of the group), so a scan thread finds
+// its 16 rows i = rg + 8 r contiguous.  Lane's channels 4 lane + m have
+// i % 8 = 4 (lane & 1) + m and i / 8 = lane / 2.
+__device__ __forceinline__ void store_perm(float *row, int block, int lane, float4 v)
 {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const Layout lay{p.keep_mode == KEEP_NONE ? p.T_run : p.T_rows, p.bf16 ? 2 : 4};
-    // thread (warp wi, lane = 4 rg + cg) holds key rows i = 16 rg + r (r < 16) of value
-    // columns j = 16 wi + 4 cg + c (c < 4): 64 elements, row pairs packed as float2.
-    // The 8 lanes of one cg (rg = 0..7) together cover all 128 rows of their 4 columns.
-    const int tid = threadIdx.x, lane = tid & 31, wi = tid >> 5, cg = lane & 3, rg = lane >> 2;
-    const int jbase = wi * 16 + 4 * cg;
-    // after the reduce-scatter a lane holds one sum: of u (rg < 4) or e (rg >= 4), column jbase + (rg & 3)
-    const int jsum = jbase + (rg & 3);
-    const int n = p.L * p.B * p.H;  // below 2^31, checked at launch
-    const uint32_t bar_state = smem_addr(smem + lay.bar()), bar_in = bar_state + 8;
-    float *vec = reinterpret_cast<float *>(smem + lay.vec());
-    float *sbeta = reinterpret_cast<float *>(smem + lay.beta());
-    float *skq = reinterpret_cast<float *>(smem + lay.kq());
+    float *g = row + 4 * (lane & 1) * GRP + block + (lane >> 1);
+    g[0] = v.x;
+    g[GRP] = v.y;
+    g[2 * GRP] = v.z;
+    g[3 * GRP] = v.w;
+}
 
-    if (tid == 0) {
-        mbar_init(bar_state, 1);
-        mbar_init(bar_in, NT + 1);
+// Stream pw (0 q, 1 k, 2 v) of one unit: the conv window slides along the rows in
+// registers.  Writes the scan inputs (q-hat, k-hat or v), the ring after the round
+// and, when snapshotting, the ring before it.
+__device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsigned char *stg, float *si,
+                            const Pre &pr, int u, int T, int pw, int lane)
+{
+    const size_t rbase = (static_cast<size_t>(u) * 3 + pw) * 3 * D;
+    if (p.ring_snap) {
+        float4 *rs = reinterpret_cast<float4 *>(p.ring_snap + rbase) + lane;
+        rs[0] = pr.ring[0];
+        rs[D / 4] = pr.ring[1];
+        rs[2 * D / 4] = pr.ring[2];
     }
-    __syncthreads();
-    int u = next_live(p, blockIdx.x, n);
-    if (u < n) {
-        if (tid == 0)
-            prefetch_state(p, lay, smem, bar_state, u);
-        prefetch_inputs(p, lay, smem, bar_in, u, tid);
+    float4 x0 = pr.ring[0], x1 = pr.ring[1], x2 = pr.ring[2];  // x[t-3], x[t-2], x[t-1]
+    const int block = pw == 0 ? 32 : 16;
+    for (int t0 = 0; t0 < T; t0 += 4) {
+        float4 y[4];
+        float ss[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (t0 + j < T) {
+                const float4 x3 = stage4(stg, lay, pw, t0 + j, lane);
+                y[j].x = silu(conv4(pr.w[0], x0.x, x1.x, x2.x, x3.x));
+                y[j].y = silu(conv4(pr.w[1], x0.y, x1.y, x2.y, x3.y));
+                y[j].z = silu(conv4(pr.w[2], x0.z, x1.z, x2.z, x3.z));
+                y[j].w = silu(conv4(pr.w[3], x0.w, x1.w, x2.w, x3.w));
+                x0 = x1;
+                x1 = x2;
+                x2 = x3;
+            } else {
+                y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            ss[j] = __fmaf_rn(y[j].w, y[j].w, __fmaf_rn(y[j].z, y[j].z, __fmaf_rn(y[j].y, y[j].y, __fmul_rn(y[j].x, y[j].x))));
+        }
+        if (pw == 2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (t0 + j < T)
+                    *reinterpret_cast<float4 *>(si + (t0 + j) * SI_ROW + SI_V + 4 * lane) = y[j];
+        } else {
+            // the four rows' sums of squares reduce together (one fixed butterfly per row)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    ss[j] = __fadd_rn(ss[j], __shfl_xor_sync(0xffffffffu, ss[j], off));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (t0 + j < T) {
+                    const float r = rsqrtf(__fadd_rn(ss[j], L2_EPS));
+                    store_perm(si + (t0 + j) * SI_ROW, block, lane,
+                               make_float4(__fmul_rn(y[j].x, r), __fmul_rn(y[j].y, r), __fmul_rn(y[j].z, r),
+                                           __fmul_rn(y[j].w, r)));
+                }
+            }
+        }
     }
-    uint32_t parity_state = 0, parity_in = 0;
+    // the ring after the round: the last 3 of [ring, rows 0..T-1]
+    float4 *ro = reinterpret_cast<float4 *>(p.ring_out + rbase) + lane;
+    ro[0] = x0;
+    ro[D / 4] = x1;
+    ro[2 * D / 4] = x2;
+}
 
-    while (u < n) {
+// Stream 3: the forget gate d = exp(-5 sigmoid(raw_g)) per key channel and beta.
+__device__ void gate_stream(const Layout &lay, const unsigned char *stg, float *si, float *sc, const Pre &pr, int T,
+                            int lane)
+{
+    for (int t = 0; t < T; ++t) {
+        const float4 g = stage4(stg, lay, 3, t, lane);
+        store_perm(si + t * SI_ROW, 0, lane,
+                   make_float4(__expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.x))),
+                               __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.y))),
+                               __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.z))),
+                               __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.w)))));
+    }
+    if (lane < T)
+        sc[2 * lane] = sigmoidf_(pr.beta);
+}
+
+__device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
+{
+    const int pw = (threadIdx.x >> 5) - NSCAN, lane = threadIdx.x & 31;
+    Pre pr;
+    int u = next_live(p, blockIdx.x, n, false);
+    if (u < n)
+        load_pre(p, u, pw, lane, pr);
+    for (int k = 0; u < n; ++k) {
+        const int b = k & 1;
+        const int T = unit_of(p, u).T;
+        const int sb = lay.nstg == 2 ? b : 0, m = lay.nstg == 2 ? k >> 1 : k;
+        const unsigned char *stg = sm + lay.stg(sb);
+        if (!warp_wait(c, B_STG_FULL + sb, m & 1))
+            return;
+        // the scan of unit k-2 has released this scan-input buffer
+        if (k >= 2 && !warp_wait(c, B_SI_EMPTY + b, ((k >> 1) - 1) & 1))
+            return;
+        float *si = reinterpret_cast<float *>(sm + lay.si(b));
+        float *sc = reinterpret_cast<float *>(sm + lay.sc(b));
+        if (pw < 3)
+            conv_stream(p, lay, stg, si, pr, u, T, pw, lane);
+        else
+            gate_stream(lay, stg, si, sc, pr, T, lane);
+        mbar_arrive(c.bar(B_STG_EMPTY + sb));
+        // k.q of each row once q-hat and k-hat are all written
+        mbar_arrive(c.bar(B_PRO));
+        if (!warp_wait(c, B_PRO, k & 1))
+            return;
+        for (int t = pw; t < T; t += NPRO) {
+            const float *g = si + t * SI_ROW + (lane >> 2) * GRP + 4 * (lane & 3);
+            const float4 kk = *reinterpret_cast<const float4 *>(g + 16);
+            const float4 qq = *reinterpret_cast<const float4 *>(g + 32);
+            float s = __fmaf_rn(kk.w, qq.w, __fmaf_rn(kk.z, qq.z, __fmaf_rn(kk.y, qq.y, __fmul_rn(kk.x, qq.x))));
+            s = warp_allsum(s);
+            if (lane == 0)
+                sc[2 * t + 1] = s;
+        }
+        mbar_arrive(c.bar(B_SI_FULL + b));
+        const int un = next_live(p, u + gridDim.x, n, false);
+        if (un < n)
+            load_pre(p, un, pw, lane, pr);
+        u = un;
+    }
+}
+
+// ---- scan warps ---------------------------------------------------------------------
+__device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
+{
+    // lane 4 rg + cg of warp wi holds key rows i = rg + 8 r (r < 16) of value columns
+    // j = 16 wi + 4 cg + c (c < 4): 64 elements, row pairs (2 rp, 2 rp + 1) packed.
+    // The two row groups of a quarter warp read two addresses of a scan-input row,
+    // each broadcast to four lanes.
+    const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5, cg = lane & 3, rg = lane >> 2;
+    const int jbase = 16 * wi + 4 * cg;
+    // after the reduce-scatter a lane holds one sum: of u (b2 = 0) or e (b2 = 1), of
+    // column jbase + 2 b1 + b0, where (b2, b1, b0) are the bits of rg
+    const int b2 = (lane >> 4) & 1, b1 = (lane >> 3) & 1, b0 = (lane >> 2) & 1;
+    const int jsum = jbase + 2 * b1 + b0;
+    // this thread's 16-byte chunk of row rg in its box of the swizzled slot; row
+    // rg + 8 r lies r * 1024 bytes further on with the same swizzle phase
+    const uint32_t soff = (wi >> 1) * 16384 + rg * 128 + ((((wi & 1) * 4 + cg) ^ rg) << 4);
+    int u = next_live(p, blockIdx.x, n, false);
+    for (int k = 0; u < n; ++k) {
         const Unit x = unit_of(p, u);
-        const int T = x.T;
-        bool arrived = mbar_wait(bar_in, parity_in);
-        if (__syncthreads_or(!arrived)) {
-            if (tid == 0 && p.status)
-                atomicOr(p.status, KDA_ST_TIMEOUT);
-            mbar_wait(bar_in, parity_in);  // let copies in flight land before the CTA leaves
-            mbar_wait(bar_state, parity_state);
-            if (tid == 0)
-                bulk_wait_all();
+        const int T = x.T, s = k & 1;
+        const uint32_t ph = (k >> 1) & 1;
+        if (!warp_wait(c, B_STATE_FULL + s, ph))
             return;
-        }
-        parity_in ^= 1u;
-
-        // ---- prologue: conv + SiLU, norms, gates (one warp per row) ----------
+        float2 S[8][4];  // S[rp][c] = (S[rg + 16 rp][jbase + c], S[rg + 16 rp + 8][jbase + c])
         {
-            const float4 *cw = reinterpret_cast<const float4 *>(smem + lay.stage_w());
-            const int c0 = 4 * lane;
-            // conv ring after the round (last 3 of [ring, rows]) and its snapshot; issued
-            // first, they depend on nothing computed here
-            float4 *rout = reinterpret_cast<float4 *>(p.ring_out + static_cast<size_t>(u) * 9 * D);
-            float4 *rsnap = p.ring_snap ? reinterpret_cast<float4 *>(p.ring_snap + static_cast<size_t>(u) * 9 * D)
-                                        : nullptr;
-            for (int idx = tid; idx < 9 * D / 4; idx += NT) {
-                const int s = idx / 96, slot = (idx % 96) / 32, c4 = idx % 32;
-                rout[idx] = fetch4(lay, smem, s, T + slot, 4 * c4);
-                if (rsnap)
-                    rsnap[idx] = fetch4(lay, smem, s, slot, 4 * c4);
-            }
-            for (int t = wi; t < T; t += NW) {
-                // the row's beta load goes out first; its latency hides behind the conv
-                const float rb = lane == 0 ? load_scalar(p.xb, p.bf16, (static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h)
-                                           : 0.f;
-                float y[3][4];
-#pragma unroll
-                for (int s = 0; s < 3; ++s) {
-                    const float4 x0 = fetch4(lay, smem, s, t, c0), x1 = fetch4(lay, smem, s, t + 1, c0);
-                    const float4 x2 = fetch4(lay, smem, s, t + 2, c0), x3 = fetch4(lay, smem, s, t + 3, c0);
-                    y[s][0] = silu(conv4(cw[s * D + c0 + 0], x0.x, x1.x, x2.x, x3.x));
-                    y[s][1] = silu(conv4(cw[s * D + c0 + 1], x0.y, x1.y, x2.y, x3.y));
-                    y[s][2] = silu(conv4(cw[s * D + c0 + 2], x0.z, x1.z, x2.z, x3.z));
-                    y[s][3] = silu(conv4(cw[s * D + c0 + 3], x0.w, x1.w, x2.w, x3.w));
-                }
-                float sq = __fmul_rn(y[0][0], y[0][0]), sk = __fmul_rn(y[1][0], y[1][0]);
-#pragma unroll
-                for (int cc = 1; cc < 4; ++cc) {
-                    sq = __fmaf_rn(y[0][cc], y[0][cc], sq);
-                    sk = __fmaf_rn(y[1][cc], y[1][cc], sk);
-                }
-                sq = warp_allsum(sq);
-                sk = warp_allsum(sk);
-                const float rq = rsqrtf(__fadd_rn(sq, L2_EPS));
-                const float rk = rsqrtf(__fadd_rn(sk, L2_EPS));
-                float qh[4], kh[4];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    qh[cc] = __fmul_rn(y[0][cc], rq);
-                    kh[cc] = __fmul_rn(y[1][cc], rk);
-                }
-                float kq = __fmul_rn(qh[0], kh[0]);
-#pragma unroll
-                for (int cc = 1; cc < 4; ++cc)
-                    kq = __fmaf_rn(qh[cc], kh[cc], kq);
-                kq = warp_allsum(kq);
-                const float4 rg = fetch4(lay, smem, 3, t + 3, c0);  // raw forget-gate row t
-                const float rgv[4] = {rg.x, rg.y, rg.z, rg.w};
-                float dv[4];
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    dv[cc] = __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(rgv[cc])));
-                float *vt = vec + t * 4 * D + c0;
-                *reinterpret_cast<float4 *>(vt) = make_float4(dv[0], dv[1], dv[2], dv[3]);
-                *reinterpret_cast<float4 *>(vt + D) = make_float4(kh[0], kh[1], kh[2], kh[3]);
-                *reinterpret_cast<float4 *>(vt + 2 * D) = make_float4(qh[0], qh[1], qh[2], qh[3]);
-                *reinterpret_cast<float4 *>(vt + 3 * D) = make_float4(y[2][0], y[2][1], y[2][2], y[2][3]);
-                if (lane == 0) {
-                    skq[t] = kq;
-                    sbeta[t] = sigmoidf_(rb);
-                }
-            }
-        }
-        // ---- state: stage -> registers ---------------------------------------------
-        arrived = mbar_wait(bar_state, parity_state);
-        if (__syncthreads_or(!arrived)) {
-            if (tid == 0 && p.status)
-                atomicOr(p.status, KDA_ST_TIMEOUT);
-            mbar_wait(bar_state, parity_state);
-            if (tid == 0)
-                bulk_wait_all();
-            return;
-        }
-        parity_state ^= 1u;
-        if (tid == 0 && p.s_snap) {
-            // the pre-round state leaves as a bulk store straight from the stage; the stage
-            // holds only what the bulk load wrote, so no proxy fence is needed before it
-            for (int c = 0; c < 4; ++c)
-                bulk_store(p.s_snap + static_cast<size_t>(u) * D * D + c * 4096,
-                           smem_addr(smem + lay.stage_state() + c * 16384), 16384);
-            bulk_commit();
-        }
-        float2 S[8][4];  // S[rp][c] = (S[16rg + 2rp][jbase + c], S[16rg + 2rp + 1][jbase + c])
-        {
-            const float *Ss = reinterpret_cast<const float *>(smem + lay.stage_state());
+            const unsigned char *src = sm + lay.slot(s) + soff;
 #pragma unroll
             for (int rp = 0; rp < 8; ++rp) {
-                const int i = 16 * rg + 2 * rp;
-                const float4 a = *reinterpret_cast<const float4 *>(Ss + i * D + jbase);
-                const float4 c = *reinterpret_cast<const float4 *>(Ss + (i + 1) * D + jbase);
-                S[rp][0] = make_float2(a.x, c.x);
-                S[rp][1] = make_float2(a.y, c.y);
-                S[rp][2] = make_float2(a.z, c.z);
-                S[rp][3] = make_float2(a.w, c.w);
+                const float4 a = *reinterpret_cast<const float4 *>(src + (2 * rp) * 1024);
+                const float4 b = *reinterpret_cast<const float4 *>(src + (2 * rp + 1) * 1024);
+                S[rp][0] = make_float2(a.x, b.x);
+                S[rp][1] = make_float2(a.y, b.y);
+                S[rp][2] = make_float2(a.z, b.z);
+                S[rp][3] = make_float2(a.w, b.w);
             }
         }
-        __syncthreads();  // every generic read of the stage is done; vec, beta, k.q are written
-
-        // ---- refill the stage with the next unit while this one scans ----------------
-        const int un = next_live(p, u + gridDim.x, n);
-        // the next unit's state fetch waits until the snapshot store has read the stage
-        bool state_due = un < n;
-        if (state_due && !p.s_snap) {
-            if (tid == 0) {
-                fence_proxy_async();
-                prefetch_state(p, lay, smem, bar_state, un);
-            }
-            state_due = false;
-        }
-        if (un < n)
-            prefetch_inputs(p, lay, smem, bar_in, un, tid);
-
-        // ---- the T-row gated delta rule -----------------------------------------
+        mbar_arrive(c.bar(B_STATE_EMPTY + s));
+        if (!warp_wait(c, B_SI_FULL + s, ph))
+            return;
+        const float *si = reinterpret_cast<const float *>(sm + lay.si(s));
+        const float *sc = reinterpret_cast<const float *>(sm + lay.sc(s));
         float *outp = p.out ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum : nullptr;
-        const int b2 = rg >> 2, b1 = (rg >> 1) & 1, b0 = rg & 1;
+
+        // ---- the T-row gated delta rule ---------------------------------------------
         for (int t = 0; t < T; ++t) {
-            const float *vt = vec + t * 4 * D;
+            const float *vt = si + t * SI_ROW;
+            const float *gp = vt + rg * GRP;
             float2 uacc[4], eacc[4], kk[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                uacc[c] = eacc[c] = make_float2(0.f, 0.f);
+            for (int c4 = 0; c4 < 4; ++c4)
+                uacc[c4] = eacc[c4] = make_float2(0.f, 0.f);
             // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows)
 #pragma unroll
             for (int rq = 0; rq < 4; ++rq) {
-                const int ib = 16 * rg + 4 * rq;
-                const float4 d4 = *reinterpret_cast<const float4 *>(vt + ib);
-                const float4 k4 = *reinterpret_cast<const float4 *>(vt + D + ib);
-                const float4 q4 = *reinterpret_cast<const float4 *>(vt + 2 * D + ib);
+                const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
+                const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
+                const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
                 const float2 dA = make_float2(d4.x, d4.y), dB = make_float2(d4.z, d4.w);
                 const float2 qA = make_float2(q4.x, q4.y), qB = make_float2(q4.z, q4.w);
                 kk[2 * rq] = make_float2(k4.x, k4.y);
                 kk[2 * rq + 1] = make_float2(k4.z, k4.w);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    S[2 * rq][c] = __fmul2_rn(S[2 * rq][c], dA);
-                    uacc[c] = __ffma2_rn(S[2 * rq][c], kk[2 * rq], uacc[c]);
-                    eacc[c] = __ffma2_rn(S[2 * rq][c], qA, eacc[c]);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    S[2 * rq][c4] = __fmul2_rn(S[2 * rq][c4], dA);
+                    uacc[c4] = __ffma2_rn(S[2 * rq][c4], kk[2 * rq], uacc[c4]);
+                    eacc[c4] = __ffma2_rn(S[2 * rq][c4], qA, eacc[c4]);
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    S[2 * rq + 1][c] = __fmul2_rn(S[2 * rq + 1][c], dB);
-                    uacc[c] = __ffma2_rn(S[2 * rq + 1][c], kk[2 * rq + 1], uacc[c]);
-                    eacc[c] = __ffma2_rn(S[2 * rq + 1][c], qB, eacc[c]);
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    S[2 * rq + 1][c4] = __fmul2_rn(S[2 * rq + 1][c4], dB);
+                    uacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], kk[2 * rq + 1], uacc[c4]);
+                    eacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], qB, eacc[c4]);
                 }
             }
-            // reduce-scatter over the 8 row groups: lane bit 4 splits u / e, bits 3 and 2
-            // split the 4 columns; each sum ends on exactly one lane
+            // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
+            // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
             float v8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                v8[c] = __fadd_rn(uacc[c].x, uacc[c].y);
-                v8[4 + c] = __fadd_rn(eacc[c].x, eacc[c].y);
+            for (int c4 = 0; c4 < 4; ++c4) {
+                v8[c4] = __fadd_rn(uacc[c4].x, uacc[c4].y);
+                v8[4 + c4] = __fadd_rn(eacc[c4].x, eacc[c4].y);
             }
             float v4[4], v2[2];
 #pragma unroll
@@ -501,67 +720,140 @@ __global__ void __launch_bounds__(NT, 2) kda_scan_kernel(const __grid_constant__
             const float keep1 = b0 ? v2[1] : v2[0], send1 = b0 ? v2[0] : v2[1];
             const float sum = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
             // u lanes: w = beta (v - u); e lanes: o = (e + w (k.q)) / sqrt(128)
-            const float w = __fmul_rn(sbeta[t], __fsub_rn(vt[3 * D + jsum], sum));
+            const float2 bk = *reinterpret_cast<const float2 *>(sc + 2 * t);  // {beta, k.q}
+            const float w = __fmul_rn(bk.x, __fsub_rn(vt[SI_V + jsum], sum));
             const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
             if (outp && b2)
-                outp[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, skq[t], sum), OUT_SCALE);
-            // every lane gathers w of its 4 columns from the u lanes 4c + cg
+                outp[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
+            // every lane gathers w of its 4 columns from the u lanes 4 c + cg
             float2 wc[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float wv = __shfl_sync(0xffffffffu, w, 4 * c + cg);
-                wc[c] = make_float2(wv, wv);
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const float wv = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
+                wc[c4] = make_float2(wv, wv);
             }
             // S = S' + k w^T
 #pragma unroll
             for (int rp = 0; rp < 8; ++rp)
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    S[rp][c] = __ffma2_rn(kk[rp], wc[c], S[rp][c]);
-            if (state_due && t == (T > 1 ? 1 : 0)) {
-                if (tid == 0) {
-                    bulk_wait_read();  // the snapshot store is done with the stage
-                    fence_proxy_async();
-                    prefetch_state(p, lay, smem, bar_state, un);
-                }
-                state_due = false;
-            }
+                for (int c4 = 0; c4 < 4; ++c4)
+                    S[rp][c4] = __ffma2_rn(kk[rp], wc[c4], S[rp][c4]);
         }
+        mbar_arrive(c.bar(B_SI_EMPTY + s));
 
-        // ---- state write-back ---------------------------------------------------
+        // ---- state write-back -----------------------------------------------------------
         {
-            float *So = p.s_out + static_cast<size_t>(u) * D * D;
+            float *So = p.s_out + static_cast<size_t>(u) * D * D + jbase;
 #pragma unroll
             for (int rp = 0; rp < 8; ++rp) {
-                const int i = 16 * rg + 2 * rp;
-                *reinterpret_cast<float4 *>(So + i * D + jbase) =
+                const int i = rg + 16 * rp;
+                *reinterpret_cast<float4 *>(So + i * D) =
                     make_float4(S[rp][0].x, S[rp][1].x, S[rp][2].x, S[rp][3].x);
-                *reinterpret_cast<float4 *>(So + (i + 1) * D + jbase) =
+                *reinterpret_cast<float4 *>(So + (i + 8) * D) =
                     make_float4(S[rp][0].y, S[rp][1].y, S[rp][2].y, S[rp][3].y);
             }
         }
-        __syncthreads();  // vec, beta, k.q are free for the next unit's prologue
-        u = un;
+        u = next_live(p, u + gridDim.x, n, false);
     }
-    if (tid == 0)
-        bulk_wait_all();  // the last snapshot stores leave before the CTA's shared memory does
+}
+
+// One persistent CTA per SM; warps 0..7 scan, 8..11 run the prologue, 12 copies.
+__global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__ ScanParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const Layout lay{p.tcap, p.bf16 ? 2 : 4, p.nstg};
+    const Ctl c{smem_addr(sm + lay.bars()), reinterpret_cast<volatile int *>(sm + lay.flag()), p.status};
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(c.bar(B_STATE_FULL + s), 1);
+            mbar_init(c.bar(B_STATE_EMPTY + s), NSCAN * 32);
+            mbar_init(c.bar(B_SI_FULL + s), NPRO * 32);
+            mbar_init(c.bar(B_SI_EMPTY + s), NSCAN * 32);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(c.bar(B_STG_FULL + b), 1);
+            mbar_init(c.bar(B_STG_EMPTY + b), NPRO * 32);
+        }
+        mbar_init(c.bar(B_PRO), NPRO * 32);
+        *c.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int n = p.L * p.B * p.H;  // below 2^31 / 128, checked at launch
+    const int wi = threadIdx.x >> 5;
+    if (wi < NSCAN)
+        scan_warp(p, lay, sm, c, n);
+    else if (wi < WCOPY)
+        prologue_warp(p, lay, sm, c, n);
+    else
+        copy_warp(p, lay, sm, c, n);
+}
+
+// ---- host side ----------------------------------------------------------------------
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled lookup_encode()
+{
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<EncodeTiled>(f);
+}
+
+// Tensor map of a state-shaped array [units * 128 rows][128] f32 with boxes of 32
+// columns x 128 rows and the 128-byte swizzle.  Encoding is host-only; the last
+// few maps of the calling thread are kept.
+int state_map(CUtensorMap *m, const float *base, long long units)
+{
+    struct Entry {
+        const float *base = nullptr;
+        long long units = 0;
+        CUtensorMap map;
+    };
+    thread_local Entry cache[4];
+    thread_local int next = 0;
+    for (const Entry &e : cache)
+        if (e.base == base && e.units == units) {
+            *m = e.map;
+            return KDA_OK;
+        }
+    static const EncodeTiled encode = lookup_encode();
+    if (!encode)
+        return fail(KDA_ECUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(units) * D};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * sizeof(float)};
+    const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(D)};
+    const cuuint32_t estr[2] = {1, 1};
+    Entry &e = cache[next];
+    const CUresult r = encode(&e.map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        e.base = nullptr;
+        return fail(KDA_ECUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r)));
+    }
+    e.base = base;
+    e.units = units;
+    next = (next + 1) % 4;
+    *m = e.map;
+    return KDA_OK;
 }
 
 struct DeviceInfo {
     int sms = 0;
-    int smem_set = 0;
-    int per_sm[2][KDA_TMAX + 1] = {};  // CTAs per SM by (raw element size 2/4, rows)
+    int smem_max = 0;  // opt-in shared memory per block, set as the kernel's limit
 };
 
-int launch_scan(const ScanParams &p, int tcap, cudaStream_t stream)
+int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
 {
     const long long units = static_cast<long long>(p.L) * p.B * p.H;
     if (units == 0)
         return ok();
-    if (units > 0x7fffffffLL - 4LL * 152 * 64)
-        return fail(KDA_EINVAL, "L*B*H exceeds the unit index range");
-    const Layout lay{tcap, p.bf16 ? 2 : 4};
-    const size_t smem = lay.total();
+    if (units > 0x7fffffffLL / D)
+        return fail(KDA_EINVAL, "L*B*H exceeds the unit index range (2^31 / 128 units)");
     static DeviceInfo info[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -571,27 +863,31 @@ int launch_scan(const ScanParams &p, int tcap, cudaStream_t stream)
         return fail(KDA_EINVAL, "device ordinal beyond the launch table");
     DeviceInfo &di = info[dev];
     if (di.sms == 0) {
-        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        int sms = 0, optin = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (e != cudaSuccess)
             return fail(KDA_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
-    }
-    if (di.smem_set < static_cast<int>(smem)) {
-        const size_t most = Layout{KDA_TMAX, 4}.total();
-        e = cudaFuncSetAttribute(kda_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(most));
+        const size_t most = Layout{KDA_TMAX, 4, 1}.total();
+        if (static_cast<size_t>(optin) < most)
+            return fail(KDA_ECUDA, "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
+        e = cudaFuncSetAttribute(kda_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess)
             return fail(KDA_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-        di.smem_set = static_cast<int>(most);
+        di.smem_max = optin;
+        di.sms = sms;
     }
-    int &per_sm = di.per_sm[p.bf16 ? 0 : 1][tcap];
-    if (per_sm == 0) {
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_scan_kernel, NT, smem);
-        if (e != cudaSuccess || per_sm < 1) {
-            per_sm = 0;
-            return fail(KDA_ECUDA, "kda_scan_kernel does not fit on an SM");
-        }
-    }
-    const long long grid = std::min<long long>(units, static_cast<long long>(di.sms) * per_sm);
-    kda_scan_kernel<<<static_cast<unsigned>(grid), NT, smem, stream>>>(p);
+    // two raw-row stages (the prologue then never waits for its rows) where they fit
+    p.nstg = Layout{p.tcap, p.bf16 ? 2 : 4, 2}.total() <= static_cast<size_t>(di.smem_max) ? 2 : 1;
+    const Layout lay{p.tcap, p.bf16 ? 2 : 4, p.nstg};
+    int rc = state_map(&p.tm_in, s_in, units);
+    if (rc)
+        return rc;
+    if (p.s_snap && (rc = state_map(&p.tm_snap, p.s_snap, units)))
+        return rc;
+    const long long grid = std::min<long long>(units, di.sms);
+    kda_scan_kernel<<<static_cast<unsigned>(grid), NT, lay.total(), stream>>>(p);
     return check_launch("kda_scan_kernel");
 }
 
@@ -630,7 +926,6 @@ int check_rows(const kda_rows *rows, int dtype)
 }  // namespace kda
 
 using namespace kda;
-
 extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
                                int T, float *out, kda_stash *stash, cudaStream_t stream)
 {
@@ -659,7 +954,6 @@ extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, 
             return fail(KDA_EINVAL, "the snapshots must not alias the resident state");
     }
     ScanParams p{};
-    p.s_in = st->state;
     p.s_out = st->state;
     p.s_snap = stash ? stash->state_snap : nullptr;
     p.ring_in = st->conv_ring;
@@ -671,9 +965,10 @@ extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, 
     p.L = dims->L; p.B = dims->B; p.H = dims->H;
     p.T_rows = T;
     p.T_run = T;
+    p.tcap = T;
     p.bf16 = dims->dtype == KDA_BF16;
     p.keep_mode = KEEP_NONE;
-    if ((rc = launch_scan(p, T, stream)))
+    if ((rc = launch_scan(p, st->state, stream)))
         return rc;
     if (stash) {
         stash->rows = *rows;
@@ -724,7 +1019,6 @@ extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, con
     } else {
         return fail(KDA_EINVAL, "keep_mem must be KDA_MEM_HOST or KDA_MEM_DEVICE");
     }
-    p.s_in = stash->state_snap;
     p.s_out = st->state;
     p.s_snap = nullptr;
     p.ring_in = stash->ring_snap;
@@ -738,6 +1032,7 @@ extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, con
     p.L = dims->L; p.B = dims->B; p.H = dims->H;
     p.T_rows = stash->T;
     p.T_run = stash->T;
+    p.tcap = stash->T;
     p.bf16 = dims->dtype == KDA_BF16;
-    return launch_scan(p, stash->T, stream);
+    return launch_scan(p, stash->state_snap, stream);
 }
