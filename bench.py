@@ -32,6 +32,10 @@ METRIC = "KDA verify rows/s (T=K+1, 64 heads) and achieved HBM GB/s vs 8 TB/s ro
 UNIT = "verify rows/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+# DRAM bytes read + written by one verify launch of the current kda_scan_kernel, from
+# one ncu capture each (profiles/kda_scan_kernel_<workload>.md; dram__bytes_read.sum +
+# dram__bytes_write.sum).  Re-measure whenever the kernel changes.
+TRAFFIC_BYTES = {"stack34": 183_960_832 + 258_220_288, "batched32": 175_732_992 + 247_056_128}
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
@@ -430,7 +434,7 @@ def main():
                      "peak": res["peak"], "unit": "GB/s", "frac": frac,
                      "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
                      "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
-                     "bytes_per_launch": res["verify_bytes"], "traffic": None},
+                     "bytes_per_launch": res["verify_bytes"], "traffic": TRAFFIC_BYTES.get(args.workload)},
         "verify_ms": res["verify_ms"], "accept_ms": res["accept_ms"], "rollback_ms": res["rollback_ms"],
         "step_achieved_gbs": res["step_gbs"],
         "gpu_launches": res["launches_per_step"] * args.steps,
