@@ -352,6 +352,45 @@ def run_gpu(args, rank, world, local_rank):
         res["e2e"] = {"value": world * w.B * w.T / (e2e_ms * 1e-3), "unit": UNIT,
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                       "ms_per_step": e2e_ms, "steps": Ke}
+
+    # per-layer issue: one kda_verify_scan per layer (as a model issues them), then accept
+    # and one all-layer rollback; eagerly, and replayed from CUDA graphs (one per round)
+    if w.L > 1 and not args.no_per_layer:
+        Kp = max(1, min(args.per_layer_steps, K))
+        RP = min(R, 8)
+        lplans = [kb.LayerRoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out,
+                                    status, scratch, stream) for r in range(RP)]
+        side = torch.cuda.Stream(dev)
+        gplans = [kb.LayerRoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out,
+                                    status, scratch, side) for r in range(RP)]
+
+        def timed(fn):
+            for i in range(3):
+                fn(i % RP)
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(Kp):
+                fn(i % RP)
+            b.record(stream)
+            barrier()
+            return a.elapsed_time(b) / Kp
+
+        eager_ms = timed(lambda r: lplans[r]())
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for g in gplans:
+                g()  # one eager round on the capture stream: every one-time setup call has run
+        stream.wait_stream(side)
+        barrier()
+        for g in gplans:
+            g.capture()
+        graph_ms = timed(lambda r: gplans[r].replay())
+        if int(status.item()):
+            raise RuntimeError(f"device status {int(status.item()):#x} after the per-layer steps")
+        res["per_layer"] = {"launches_per_step": w.L + 3, "steps": Kp, "eager_ms_per_step": eager_ms,
+                            "graph_ms_per_step": graph_ms,
+                            "graph_rows_per_s": world * w.B * w.T / (graph_ms * 1e-3)}
     return res
 
 
@@ -366,6 +405,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
+    ap.add_argument("--no-per-layer", action="store_true", help="skip the per-layer (and CUDA graph) rounds")
+    ap.add_argument("--per-layer-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -441,6 +482,7 @@ def main():
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
+        "per_layer": res.get("per_layer"),
     }
     print(json.dumps(line))
 

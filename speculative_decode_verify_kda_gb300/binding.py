@@ -147,6 +147,10 @@ class LayerState:
     def dims(self, dtype: int) -> KdaDims:
         return KdaDims(self.L, self.B, self.H, D, D, dtype)
 
+    def layer(self, l: int) -> "LayerState":
+        """Layer l alone (L = 1), as views of these tensors (layer-major, so contiguous)."""
+        return LayerState(self.state[l:l + 1], self.conv_ring[l:l + 1], self.conv_w[l:l + 1])
+
 
 class Stash:
     """Rollback material of one verify round: snapshots (owned here) + the raw rows.
@@ -154,12 +158,17 @@ class Stash:
     The raw-row tensors are referenced, not copied, and stay alive with the stash.
     """
 
-    def __init__(self, st: LayerState):
-        self.state_snap = torch.empty_like(st.state)
-        self.ring_snap = torch.empty_like(st.conv_ring)
+    def __init__(self, st: LayerState | None = None, state_snap: torch.Tensor | None = None,
+                 ring_snap: torch.Tensor | None = None):
+        self.state_snap = torch.empty_like(st.state) if state_snap is None else state_snap
+        self.ring_snap = torch.empty_like(st.conv_ring) if ring_snap is None else ring_snap
         self.c = KdaStashC(self.state_snap.data_ptr(), self.ring_snap.data_ptr(), KdaRows(), 0)
         self.rows = None
         self.dtype = None
+
+    def layer(self, l: int) -> "Stash":
+        """A stash for layer l alone whose snapshots are views of these snapshots."""
+        return Stash(state_snap=self.state_snap[l:l + 1], ring_snap=self.ring_snap[l:l + 1])
 
     @property
     def T(self) -> int:
@@ -302,3 +311,69 @@ class RoundPlan:
         self.verify()
         self.accept()
         self.rollback()
+
+
+class LayerRoundPlan:
+    """One verify round issued the way a model issues it: one kda_verify_scan per layer
+    (each over that layer's views, in layer order), then spec_accept, then one
+    kda_rollback over all layers from the snapshots the per-layer calls wrote.
+
+    Same arguments as RoundPlan; the results are bit-identical to it.  A plan built on
+    a side stream (a torch.cuda.Stream other than the default one) can capture its round
+    into a CUDA graph with ``capture()`` and replay it with ``replay()``: the library
+    allocates nothing and never synchronises, so the captured launches are the eager ones.
+    """
+
+    def __init__(self, st: LayerState, rows: dict, out, stash: Stash, logits, drafts, j_out, bonus_out,
+                 keep_out, dev_status, scratch, stream=None):
+        self.full = RoundPlan(st, rows, out, stash, logits, drafts, j_out, bonus_out, keep_out, dev_status,
+                              scratch, stream)
+        self.layers = []
+        self._views = []
+        for l in range(st.L):
+            stl, stashl = st.layer(l), stash.layer(l)
+            rl = {n: t[l:l + 1] for n, t in rows.items()}
+            outl = None if out is None else out[l:l + 1]
+            crows, tensors, dt, T = _rows(stl, rl["q"], rl["k"], rl["v"], rl["g"], rl["beta"])
+            dims, cst = stl.dims(dt), stl.c()
+            self._views.append((stl, stashl, rl, outl, crows, dims, cst, tensors))
+            self.layers.append((ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(crows), T, _ptr(outl),
+                                ctypes.byref(stashl.c), ctypes.c_void_p(_stream(stream))))
+        self.stream = stream if isinstance(stream, torch.cuda.Stream) else None
+        self.graph = None
+
+    def verify(self):
+        L = self.full._L
+        for args in self.layers:
+            rc = L.kda_verify_scan(*args)
+            if rc:
+                _check("kda_verify_scan", rc)
+        # the all-layer stash now describes this round: its snapshots were written by
+        # the per-layer calls, its rows are the round's full raw-row tensors
+        f = self.full
+        f._stash.c.rows, f._stash.c.T = f.crows, self.layers[0][3]
+        f._stash.rows, f._stash.dtype = f._tensors, f._dt
+
+    def accept(self):
+        self.full.accept()
+
+    def rollback(self):
+        self.full.rollback()
+
+    def __call__(self):
+        self.verify()
+        self.accept()
+        self.rollback()
+
+    def capture(self):
+        """Capture one round (all launches) into a CUDA graph on the plan's side stream.
+        Run the round eagerly once before, so every one-time setup call has happened."""
+        if self.stream is None:
+            raise ValueError("capture needs a plan built on a side torch.cuda.Stream")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
