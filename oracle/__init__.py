@@ -88,7 +88,12 @@ class Oracle:
         self.lib.kdao_verify.argtypes = [ci, ci, ci] + [vp] * 11
         self.lib.kdao_rollback.argtypes = [ci, ci, ci, ci] + [vp] * 12
         self.lib.kdao_accept.argtypes = [ci, ci, ci, vp, vp, vp, vp, vp]
-        for fn in ("kdao_prepare", "kdao_core", "kdao_verify", "kdao_rollback", "kdao_accept"):
+        cf = ctypes.c_float
+        self.lib.kdao_conf_keep.argtypes = [ci, vp, cf, ci]
+        self.lib.kdao_confidence_vt.argtypes = [ci, vp, cf, ci]
+        self.lib.kdao_slot_confidence_vt.argtypes = [ci, vp, cf, ci]
+        for fn in ("kdao_prepare", "kdao_core", "kdao_verify", "kdao_rollback", "kdao_accept", "kdao_conf_keep",
+                   "kdao_confidence_vt", "kdao_slot_confidence_vt"):
             getattr(self.lib, fn).restype = ci
 
     @staticmethod
@@ -173,6 +178,22 @@ class Oracle:
                                   ctypes.byref(bonus))
         self._check("kdao_accept", rc, (OK, ENAN))
         return j.value, bonus.value, vam, rc
+
+    # -- verify-window policies (f32 decisions) --------------------------------
+    def conf_keep(self, q, p_min, pmin0):
+        """Drafts kept by the p-min break over the slot confidences q (glm5_conf_keep)."""
+        q = _f32(q).reshape(-1)
+        return int(self.lib.kdao_conf_keep(q.size, _p(q) if q.size else None, float(p_min), int(bool(pmin0))))
+
+    def confidence_vt(self, raws, tau, vt_cap):
+        """Verify rows from cumulative survival of sigmoid(raws) (dspark_confidence_vt)."""
+        r = _f32(raws).reshape(-1)
+        return int(self.lib.kdao_confidence_vt(r.size, _p(r) if r.size else None, float(tau), int(vt_cap)))
+
+    def slot_confidence_vt(self, raws, tau, vt_cap):
+        """Verify rows from per-slot sigmoid(raws) (dspark_slot_confidence_vt)."""
+        r = _f32(raws).reshape(-1)
+        return int(self.lib.kdao_slot_confidence_vt(r.size, _p(r) if r.size else None, float(tau), int(vt_cap)))
 
     # -- [L][B] helper ---------------------------------------------------------
     def verify_units(self, rows, conv_w, ring, state, units=None):

@@ -293,3 +293,67 @@ int kdao_accept(int T, int V, int dtype, const void *logits, const int *drafts,
     *bonus_out = vam[j];
     return vam[j] == KDAO_SENTINEL ? KDAO_ENAN : KDAO_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * Verify-window policies: how many drafted rows a session sends through verify.
+ * They decide integers from f32 arithmetic, so they compute in f32 with the
+ * operations the pages use (the host's expf, IEEE division), not in double.
+ * ------------------------------------------------------------------------- */
+
+/* glm_spec.rs, glm5_conf_keep and its conf_keep_tests: the p-min break of the
+ * draft chain.  q[0..n-1] are the drafter's confidences of draft slots 0..n-1.
+ * Slots are kept in order until the first slot whose confidence is strictly
+ * below p_min; a miss at slot 0 only breaks the chain when pmin0 is set (slot 0
+ * is otherwise judged on its own and does not latch).  Returns the kept count. */
+int kdao_conf_keep(int n, const float *q, float p_min, int pmin0)
+{
+    int kept = 0;
+    for (int j = 0; j < n; ++j) {
+        if (q[j] < p_min && (j > 0 || pmin0))
+            break;
+        ++kept;
+    }
+    return kept;
+}
+
+static float sigmoid_f32(float r)
+{
+    return 1.0f / (1.0f + expf(-r));
+}
+
+static int clamp_vt(int kept, int vt_cap)
+{
+    int hi = vt_cap > 2 ? vt_cap : 2;
+    int vt = 1 + kept;
+    return vt < 2 ? 2 : (vt > hi ? hi : vt);
+}
+
+/* dflash.rs, dspark_confidence_vt: raws[k] is the pre-sigmoid accept score of
+ * draft slot k+1; the survival S_k = prod_{j<=k} sigmoid(raws[j]) (accumulated in
+ * f32 in slot order) keeps leading slots while S_k >= tau.  Returns the verify
+ * row count 1 + kept, clamped to [2, max(vt_cap, 2)]. */
+int kdao_confidence_vt(int n, const float *raws, float tau, int vt_cap)
+{
+    float surv = 1.0f;
+    int kept = 0;
+    for (int k = 0; k < n; ++k) {
+        surv *= sigmoid_f32(raws[k]);
+        if (surv < tau)
+            break;
+        ++kept;
+    }
+    return clamp_vt(kept, vt_cap);
+}
+
+/* dflash.rs, dspark_slot_confidence_vt: the same window with the per-slot
+ * statistic: keep the longest prefix whose every slot has sigmoid(raw) >= tau. */
+int kdao_slot_confidence_vt(int n, const float *raws, float tau, int vt_cap)
+{
+    int kept = 0;
+    for (int k = 0; k < n; ++k) {
+        if (sigmoid_f32(raws[k]) < tau)
+            break;
+        ++kept;
+    }
+    return clamp_vt(kept, vt_cap);
+}

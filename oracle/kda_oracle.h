@@ -46,6 +46,10 @@ int kdao_rollback(int H, int T, int keep, int dtype, const void *xq, const void 
 int kdao_accept(int T, int V, int dtype, const void *logits, const int *drafts, int *vam,
                 int *j_out, int *bonus_out);
 
+int kdao_conf_keep(int n, const float *q, float p_min, int pmin0);
+int kdao_confidence_vt(int n, const float *raws, float tau, int vt_cap);
+int kdao_slot_confidence_vt(int n, const float *raws, float tau, int vt_cap);
+
 #ifdef __cplusplus
 }
 #endif

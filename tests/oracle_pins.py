@@ -412,6 +412,73 @@ def pin_accept_ties(orc):
     assert vam[0] == 1 and bonus == 1
 
 
+def _golden_windows():
+    rows = []
+    with open(os.path.join(GOLDEN, "window_policy_fixture.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            kind, vals, param, flag, exp = line.split()
+            v = [] if vals == "-" else [float(x) for x in vals.split(",")]
+            rows.append((kind, np.array(v, np.float32), np.float32(param), int(flag), int(exp)))
+    return rows
+
+
+def _logit_f32(p):
+    """ln(p / (1 - p)) in f32, the way the page's tests build raw scores."""
+    p = np.asarray(p, np.float32)
+    return np.log((p / (np.float32(1.0) - p)).astype(np.float32)).astype(np.float32)
+
+
+def pin_window_page_fixture(orc):
+    """glm5_conf_keep, dspark_confidence_vt and dspark_slot_confidence_vt on the cases
+    printed in the pages' unit tests (tests/golden/window_policy_fixture.txt)."""
+    for kind, vals, param, flag, exp in _golden_windows():
+        if kind == "conf_keep":
+            got = orc.conf_keep(vals, param, flag)
+        elif kind == "confidence":
+            got = orc.confidence_vt(_logit_f32(vals), param, flag)
+        else:
+            got = orc.slot_confidence_vt(_logit_f32(vals), param, flag)
+        assert got == exp, (kind, list(vals), float(param), flag, got, exp)
+
+
+def pin_window_brute_force(orc):
+    """Each window is the longest prefix whose every slot passes its own test, written as
+    a search over prefix lengths; survival never keeps more than the per-slot arm."""
+    rng = np.random.default_rng(2024)
+    for _ in range(400):
+        n = int(rng.integers(0, 9))
+        q = rng.uniform(0, 1, n).astype(np.float32)
+        p_min = np.float32(rng.choice([0.0, 0.3, 0.5, 0.8]))
+        pmin0 = int(rng.integers(0, 2))
+        ok = [bool(q[j] >= p_min or (j == 0 and not pmin0)) for j in range(n)]
+        want = max(m for m in range(n + 1) if all(ok[:m]))
+        assert orc.conf_keep(q, p_min, pmin0) == want
+        raws = rng.normal(0, 3, n).astype(np.float32)
+        sig = (np.float32(1) / (np.float32(1) + np.exp(-raws).astype(np.float32))).astype(np.float32)
+        tau = np.float32(rng.choice([0.05, 0.3, 0.5, 0.9]))
+        cap = int(rng.integers(1, 16))
+        surv = np.cumprod(sig, dtype=np.float32) if n else np.zeros(0, np.float32)
+        clamp = lambda m: min(max(1 + m, 2), max(cap, 2))
+        keep_s = max(m for m in range(n + 1) if all(surv[:m] >= tau))
+        keep_p = max(m for m in range(n + 1) if all(sig[:m] >= tau))
+        vt, vt_slot = orc.confidence_vt(raws, tau, cap), orc.slot_confidence_vt(raws, tau, cap)
+        assert vt == clamp(keep_s) and vt_slot == clamp(keep_p), (raws, tau, cap)
+        assert vt <= vt_slot
+
+
+def pin_window_limits(orc):
+    """Scores at the extremes: certain slots keep every draft up to the cap, hopeless ones
+    keep none (the vt floor is anchor + 1 draft); p_min = 0 switches the break off."""
+    for n in range(0, 15):
+        assert orc.conf_keep(np.zeros(n), 0.0, 1) == n
+        assert orc.conf_keep(np.ones(n), 1.0, 1) == n
+        assert orc.confidence_vt(np.full(n, np.inf, np.float32), 0.5, 15) == max(2, n + 1)
+        assert orc.confidence_vt(np.full(n, -np.inf, np.float32), 0.5, 15) == 2
+        assert orc.slot_confidence_vt(np.full(n, 30.0, np.float32), 0.99, 4) == min(max(2, n + 1), 4)
+
+
 PINS = [
     pin_core_matrix_form,
     pin_core_closed_form_first_write,
@@ -431,4 +498,7 @@ PINS = [
     pin_accept_brute_force,
     pin_accept_nan,
     pin_accept_ties,
+    pin_window_page_fixture,
+    pin_window_brute_force,
+    pin_window_limits,
 ]

@@ -38,6 +38,11 @@ MUTATIONS = {
     "ring_reroll": ("hist[((size_t)s * (T + 3) + T + n) * D + c]",
                     "hist[((size_t)s * (T + 3) + T - 1 + n) * D + c]"),
     "bf16_shift": ("<< 16;", "<< 15;"),
+    "conf_keep_not_strict": ("if (q[j] < p_min && (j > 0 || pmin0))", "if (q[j] <= p_min && (j > 0 || pmin0))"),
+    "conf_keep_slot0_latch": ("if (q[j] < p_min && (j > 0 || pmin0))", "if (q[j] < p_min && (j > 1 || pmin0))"),
+    "survival_not_cumulative": ("        surv *= sigmoid_f32(raws[k]);", "        surv = sigmoid_f32(raws[k]);"),
+    "vt_floor": ("return vt < 2 ? 2 :", "return vt < 1 ? 1 :"),
+    "vt_no_anchor": ("int vt = 1 + kept;", "int vt = kept;"),
     "argmax_last_tie": ("x > bv", "x >= bv"),
     "j_off_by_one": ("*j_out = j;", "*j_out = j + (j < K);"),
     "bonus_prev_row": ("*bonus_out = vam[j];", "*bonus_out = vam[j > 0 ? j - 1 : 0];"),
