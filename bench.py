@@ -72,6 +72,17 @@ def rollback_bytes(w, keeps) -> int:
     return n
 
 
+def verify_bytes_var(w, t_rows) -> int:
+    """verify_bytes with session b running t_rows[b] rows."""
+    es = 2 if w.bf16 else 4
+    D = 128
+    per_head = 3 * D * D * 4 + 3 * 9 * D * 4
+    n = 0
+    for t in t_rows:
+        n += w.L * (w.H * per_head + t * w.H * (4 * D + 1) * es + t * w.H * D * 4)
+    return n + w.L * w.H * 3 * D * 4 * 4
+
+
 def accept_bytes(w) -> int:
     return w.B * w.T * w.V * (2 if w.bf16 else 4) + w.B * (w.T - 1) * 4 + 3 * w.B * 4
 
@@ -391,6 +402,44 @@ def run_gpu(args, rank, world, local_rank):
         res["per_layer"] = {"launches_per_step": w.L + 3, "steps": Kp, "eager_ms_per_step": eager_ms,
                             "graph_ms_per_step": graph_ms,
                             "graph_rows_per_s": world * w.B * w.T / (graph_ms * 1e-3)}
+    # variable T per session: the window of each session's round from seeded drafter
+    # confidences (glm5_conf_keep, p_min 0.5), then verify / accept / rollback with
+    # per-session row counts, all decided on the device
+    if w.B > 1 and not args.no_var_t:
+        g = np.random.default_rng(w.seed + 17)
+        conf = torch.from_numpy(g.uniform(0.3, 1.0, (w.B, w.K)).astype(np.float32)).to(dev)
+        t_dev = kb.spec_window(conf, kb.WIN_CONF_KEEP, 0.5, w.T)
+        t_host = [int(x) for x in t_dev.cpu()]
+        Kv = max(1, min(args.var_t_steps, K))
+
+        def var_step(r, ev):
+            rr = rows[r]
+            ev[0].record(stream)
+            kb.kda_verify_scan_var(st, rr["q"], rr["k"], rr["v"], rr["g"], rr["beta"], t_dev, out=out, stash=stash,
+                                   dev_status=status, stream=stream)
+            ev[1].record(stream)
+            kb.spec_accept_var(logits[r], drafts[r], t_dev, j_out, bonus_out, keep_out, status, scratch, stream)
+            kb.kda_rollback_var(st, stash, t_dev, keep_out, status, stream)
+            ev[2].record(stream)
+
+        evv = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(Kv + 3)]
+        for i in range(3):
+            var_step(i % R, evv[Kv + i])
+        barrier()
+        for i in range(Kv):
+            var_step(i % R, evv[i])
+        barrier()
+        if int(status.item()):
+            raise RuntimeError(f"device status {int(status.item()):#x} after the variable-T steps")
+        v_ms = sum(e[0].elapsed_time(e[1]) for e in evv[:Kv]) / Kv
+        s_ms = sum(e[0].elapsed_time(e[2]) for e in evv[:Kv]) / Kv
+        vb_var = verify_bytes_var(w, t_host)
+        res["var_t"] = {"window": "glm5_conf_keep, p_min 0.5, slot confidences ~ U(0.3, 1) (seeded)",
+                        "rows_mean": sum(t_host) / len(t_host), "rows_min": min(t_host), "rows_max": max(t_host),
+                        "steps": Kv, "verify_ms": v_ms, "round_gpu_ms": s_ms,
+                        "rows_per_s": world * sum(t_host) / (s_ms * 1e-3),
+                        "verify_gbs": vb_var / (v_ms * 1e-3) / 1e9,
+                        "verify_frac_of_peak": vb_var / (v_ms * 1e-3) / 1e9 / peak}
     return res
 
 
@@ -407,6 +456,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-per-layer", action="store_true", help="skip the per-layer (and CUDA graph) rounds")
     ap.add_argument("--per-layer-steps", type=int, default=200)
+    ap.add_argument("--no-var-t", action="store_true", help="skip the variable-T rounds")
+    ap.add_argument("--var-t-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -483,6 +534,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
         "per_layer": res.get("per_layer"),
+        "var_t": res.get("var_t"),
     }
     print(json.dumps(line))
 

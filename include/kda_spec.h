@@ -65,7 +65,9 @@ extern "C" {
 
 /* bits OR-ed into *dev_status by kernels */
 #define KDA_ST_NAN 0x1      /* spec_accept: row j (the bonus row) holds a NaN */
-#define KDA_ST_BADKEEP 0x2  /* kda_rollback: a device keep outside 1..T       */
+#define KDA_ST_BADKEEP 0x2  /* a device keep outside 1..T, or a device row count
+                               outside 1..T (the *_var calls); that session is
+                               left untouched                                    */
 #define KDA_ST_TIMEOUT 0x4  /* a bulk copy into shared memory did not arrive in
                                time (bounded wait); the CTA stopped early       */
 
@@ -146,6 +148,71 @@ int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_r
  */
 int kda_rollback(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash,
                  const int *keep, int keep_mem, int *dev_status, cudaStream_t stream);
+
+/*
+ * Rounds whose length differs per session (variable T inside one batched grid).
+ * glm_spec.rs, glm5_conf_keep and the p-min break of the draft chain, and dflash.rs,
+ * DsparkVtPolicy / dspark_confidence_vt / dspark_slot_confidence_vt: each session
+ * sends its own number of drafted rows through verify.  The raw-row, output and
+ * logits layouts keep T (the cap) rows per session; session b uses rows
+ * 0..t_rows[b]-1 of them and the rest are neither read nor written.
+ *
+ * kda_verify_scan_var -- kda_verify_scan where session b runs t_rows[b] rows
+ *   (1 <= t_rows[b] <= T).  t_mem: KDA_MEM_HOST (validated before launch, B <=
+ *   KDA_HOST_KEEP_MAX) or KDA_MEM_DEVICE (a session whose count is out of range is
+ *   left untouched, its snapshot unwritten, and KDA_ST_BADKEEP is set in
+ *   *dev_status, which may be NULL).  The stash records T; the row counts are
+ *   passed again to kda_rollback_var.  Bit-identical, per session, to
+ *   kda_verify_scan of that session's t_rows[b] rows.
+ */
+int kda_verify_scan_var(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows, int T,
+                        const int *t_rows, int t_mem, float *out, kda_stash *stash, int *dev_status,
+                        cudaStream_t stream);
+
+/*
+ * kda_rollback_var -- accept-j rollback of a round run by kda_verify_scan_var.
+ *   t_rows and keep are both host arrays (mem = KDA_MEM_HOST, validated: 1 <= keep[b]
+ *   <= t_rows[b] <= T) or both device arrays (mem = KDA_MEM_DEVICE; an invalid pair
+ *   leaves the session untouched and sets KDA_ST_BADKEEP).  keep[b] == t_rows[b]:
+ *   nothing to do for that session; otherwise rows 0..keep[b]-1 are replayed from the
+ *   snapshot, as in kda_rollback.
+ */
+int kda_rollback_var(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash,
+                     const int *t_rows, const int *keep, int mem, int *dev_status, cudaStream_t stream);
+
+/*
+ * spec_accept_var -- spec_accept where session b's round has t_rows[b] rows
+ *   (device int32 [B]).  logits stay [B][T][V] and drafts [B][T-1]; session b reads
+ *   logits rows 0..t_rows[b]-1 and drafts 0..t_rows[b]-2: j = the first r <
+ *   t_rows[b]-1 whose draft misses, else t_rows[b]-1; bonus = vam[j]; keep = j+1.
+ *   A count outside 1..T gives j = -1, bonus = -1, keep = 0 and KDA_ST_BADKEEP.
+ *   Scratch as for spec_accept (spec_accept_scratch_bytes(B, T, V)).
+ */
+int spec_accept_var(const void *logits, int logit_dtype, int B, int T, int V, const int *t_rows,
+                    const int *drafts, int *j_out, int *bonus_out, int *keep_out, int *dev_status,
+                    void *scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/* verify-window policies of spec_window */
+#define KDA_WIN_CONF_KEEP 0       /* glm5_conf_keep: scores = draft-slot confidences q;
+                                     param = p_min; pmin0 arms the break at slot 0;
+                                     rows = 1 + kept drafts                          */
+#define KDA_WIN_CONFIDENCE 1      /* dspark_confidence_vt: scores = pre-sigmoid slot
+                                     scores; param = tau on the cumulative survival
+                                     prod sigmoid(score); rows in [2, max(t_cap, 2)] */
+#define KDA_WIN_SLOT_CONFIDENCE 2 /* dspark_slot_confidence_vt: per-slot
+                                     sigmoid(score) >= tau; rows in [2, max(t_cap, 2)] */
+
+/*
+ * spec_window -- per-session verify rows from the drafter's slot scores, on the device.
+ *   scores: device f32 [B][K] (slot k of session b: the score of draft k+1);
+ *   t_out: device int32 [B], the rows of each session's round, capped at t_cap
+ *   (1..15 for KDA_WIN_CONF_KEEP, 2..15 for the confidence policies).  Keeping
+ *   stops at the first slot that fails (a kept draft after a dropped one could never
+ *   be accepted).  The decisions are taken in f32: a strict "<" against the
+ *   threshold, the survival multiplied in slot order, sigmoid(x) = 1 / (1 + exp(-x)).
+ */
+int spec_window(const float *scores, int B, int K, int policy, float param, int pmin0, int t_cap,
+                int *t_out, cudaStream_t stream);
 
 /* Bytes of device scratch spec_accept needs for B sessions of T rows of V logits. */
 size_t spec_accept_scratch_bytes(int B, int T, int V);

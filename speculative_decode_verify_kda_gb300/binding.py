@@ -26,8 +26,11 @@ F32, BF16 = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
-EXPORTS = ("kda_verify_scan", "kda_rollback", "spec_accept_scratch_bytes", "spec_accept",
-           "spec_accept_noalloc", "kda_error_string", "kda_last_error", "kda_abi_version")
+EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "spec_accept_var",
+           "spec_window", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
+           "kda_last_error", "kda_abi_version")
+ABI_VERSION = 2
+WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
 class KdaDims(ctypes.Structure):
@@ -75,6 +78,16 @@ def lib(path: str | None = None):
     L.kda_rollback.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                ctypes.POINTER(KdaStashC), vp, ci, vp, vp]
     L.kda_rollback.restype = ci
+    L.kda_verify_scan_var.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                      ctypes.POINTER(KdaRows), ci, vp, ci, vp, ctypes.POINTER(KdaStashC), vp, vp]
+    L.kda_verify_scan_var.restype = ci
+    L.kda_rollback_var.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                   ctypes.POINTER(KdaStashC), vp, vp, ci, vp, vp]
+    L.kda_rollback_var.restype = ci
+    L.spec_accept_var.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.spec_accept_var.restype = ci
+    L.spec_window.argtypes = [vp, ci, ci, ci, ctypes.c_float, ci, ci, vp, vp]
+    L.spec_window.restype = ci
     L.spec_accept_scratch_bytes.argtypes = [ci, ci, ci]
     L.spec_accept_scratch_bytes.restype = sz
     L.spec_accept.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -227,6 +240,90 @@ def kda_rollback(st: LayerState, stash: Stash, keep, dev_status: torch.Tensor | 
                             _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
     del hold
     _check("kda_rollback", rc)
+
+
+def _int_array(x, B: int, name: str):
+    """A host int array (ctypes) or a device int32 tensor [B] -> (pointer, mem kind, holder)."""
+    if isinstance(x, torch.Tensor) and x.is_cuda:
+        _dev(x, name, torch.int32, (B,))
+        return ctypes.c_void_p(x.data_ptr()), MEM_DEVICE, x
+    vals = [int(v) for v in x]
+    if len(vals) != B:
+        raise ValueError(f"{name} must have {B} entries")
+    hold = (ctypes.c_int * max(B, 1))(*vals)
+    return ctypes.cast(hold, ctypes.c_void_p), MEM_HOST, hold
+
+
+def kda_verify_scan_var(st: LayerState, q, k, v, g, beta, t_rows, out: torch.Tensor | None = None,
+                        stash: Stash | None = None, dev_status: torch.Tensor | None = None, stream=None):
+    """Verify round where session b runs t_rows[b] of the T = q.shape[2] rows.
+
+    t_rows: host sequence of B ints or a device int32 tensor [B]; the other arguments
+    as for kda_verify_scan.
+    """
+    rows, tensors, dt, T = _rows(st, q, k, v, g, beta)
+    if out is not None:
+        _dev(out, "out", torch.float32, (st.L, st.B, T, st.H, D))
+    tp, mem, hold = _int_array(t_rows, st.B, "t_rows")
+    dims, cst = st.dims(dt), st.c()
+    rc = lib().kda_verify_scan_var(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(rows), T, tp, mem, _ptr(out),
+                                   ctypes.byref(stash.c) if stash is not None else None, _ptr(dev_status),
+                                   ctypes.c_void_p(_stream(stream)))
+    del hold
+    _check("kda_verify_scan_var", rc)
+    if stash is not None:
+        stash.rows, stash.dtype = tensors, dt
+    return stash
+
+
+def kda_rollback_var(st: LayerState, stash: Stash, t_rows, keep, dev_status: torch.Tensor | None = None,
+                     stream=None) -> None:
+    """Rollback of a kda_verify_scan_var round: t_rows and keep both host or both device."""
+    if stash.rows is None:
+        raise ValueError("stash holds no verify round")
+    tp, m1, h1 = _int_array(t_rows, st.B, "t_rows")
+    kp, m2, h2 = _int_array(keep, st.B, "keep")
+    if m1 != m2:
+        raise ValueError("t_rows and keep must both be host arrays or both device tensors")
+    dims, cst = st.dims(stash.dtype), st.c()
+    rc = lib().kda_rollback_var(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(stash.c), tp, kp, m1,
+                                _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+    del h1, h2
+    _check("kda_rollback_var", rc)
+
+
+def spec_accept_var(logits: torch.Tensor, drafts: torch.Tensor, t_rows: torch.Tensor, j_out=None, bonus_out=None,
+                    keep_out=None, dev_status=None, scratch: torch.Tensor | None = None, stream=None):
+    """Greedy accept when session b's round has t_rows[b] (device int32 [B]) of the T rows."""
+    _dev(logits, "logits")
+    B, T, V = (int(x) for x in logits.shape)
+    _dev(drafts, "drafts", torch.int32, (B, T - 1))
+    _dev(t_rows, "t_rows", torch.int32, (B,))
+    dev = logits.device
+    j_out = torch.empty(B, dtype=torch.int32, device=dev) if j_out is None else j_out
+    bonus_out = torch.empty(B, dtype=torch.int32, device=dev) if bonus_out is None else bonus_out
+    keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
+    need = spec_accept_scratch_bytes(B, T, V)
+    if scratch is None:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib().spec_accept_var(_ptr(logits), _row_dtype(logits), B, T, V, _ptr(t_rows), _ptr(drafts), _ptr(j_out),
+                               _ptr(bonus_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch),
+                               scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
+    _check("spec_accept_var", rc)
+    return j_out, bonus_out, keep_out
+
+
+def spec_window(scores: torch.Tensor, policy: int, param: float, t_cap: int, pmin0: bool = False,
+                t_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per-session verify rows from slot scores (device f32 [B][K]); returns int32 [B]."""
+    _dev(scores, "scores", torch.float32)
+    B, K = (int(x) for x in scores.shape)
+    t_out = torch.empty(B, dtype=torch.int32, device=scores.device) if t_out is None else t_out
+    _dev(t_out, "t_out", torch.int32, (B,))
+    rc = lib().spec_window(_ptr(scores), B, K, int(policy), float(param), int(bool(pmin0)), int(t_cap), _ptr(t_out),
+                           ctypes.c_void_p(_stream(stream)))
+    _check("spec_window", rc)
+    return t_out
 
 
 def spec_accept_scratch_bytes(B: int, T: int, V: int) -> int:

@@ -84,7 +84,9 @@ constexpr uint64_t WAIT_NS = 1000000000ull;  // an mbarrier wait gives up after 
 enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, B_STG_EMPTY = 10, B_PRO = 12,
        NBARS = 13 };
 
-enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2 };
+// Rows a unit runs: KEEP_NONE all T_run; ROWS_* a verify with per-session row counts
+// (host values in keep_host, or rows_dev); KEEP_* a rollback to per-session keep.
+enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2, ROWS_HOST = 3, ROWS_DEVICE = 4 };
 
 struct ScanParams {
     CUtensorMap tm_in;     // state read: [units * 128 rows][128] f32, box 32 x 128, 128B swizzle
@@ -98,6 +100,7 @@ struct ScanParams {
     const void *xq, *xk, *xv, *xg, *xb;  // [L][B][T_rows][H][D], xb [L][B][T_rows][H]
     float *out;            // nullable: [L][B][T_rows][H][D]
     const int *keep_dev;   // KEEP_DEVICE: [B]
+    const int *rows_dev;   // ROWS_DEVICE, or KEEP_DEVICE after a per-session round: [B] row counts
     int *status;           // nullable device status word
     int L, B, H;
     int T_rows;            // row count of the raw-row tensors
@@ -281,20 +284,30 @@ struct Unit {
     long long lb;  // l * B + b
 };
 
-// rows unit u runs: > 0 to run, 0 nothing to do, -1 an invalid device keep
+// rows unit u runs: > 0 to run, 0 nothing to do, -1 an invalid device keep or row count
 __device__ __forceinline__ int unit_rows(const ScanParams &p, int b)
 {
-    if (p.keep_mode == KEEP_HOST) {
-        const int kp = p.keep_host[b];  // validated 1..T_rows on the host
+    switch (p.keep_mode) {
+    case KEEP_HOST: {
+        const int kp = p.keep_host[b];  // validated on the host; T_rows where nothing is to do
         return kp >= p.T_rows ? 0 : kp;
     }
-    if (p.keep_mode == KEEP_DEVICE) {
+    case KEEP_DEVICE: {
         const int kp = p.keep_dev[b];
-        if (kp < 1 || kp > p.T_rows)
+        const int tb = p.rows_dev ? p.rows_dev[b] : p.T_rows;  // the session's rows in the round
+        if (tb < 1 || tb > p.T_rows || kp < 1 || kp > tb)
             return -1;
-        return kp == p.T_rows ? 0 : kp;
+        return kp == tb ? 0 : kp;
     }
-    return p.T_run;
+    case ROWS_HOST:
+        return p.keep_host[b];  // validated 1..T_rows on the host
+    case ROWS_DEVICE: {
+        const int tb = p.rows_dev[b];
+        return tb < 1 || tb > p.T_rows ? -1 : tb;
+    }
+    default:
+        return p.T_run;
+    }
 }
 
 __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
@@ -926,8 +939,13 @@ int check_rows(const kda_rows *rows, int dtype)
 }  // namespace kda
 
 using namespace kda;
-extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
-                               int T, float *out, kda_stash *stash, cudaStream_t stream)
+namespace kda {
+namespace {
+
+// Shared body of kda_verify_scan and kda_verify_scan_var.  t_rows == nullptr: every
+// session runs T rows; else session b runs t_rows[b] rows (host or device values).
+int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows, int T,
+                  const int *t_rows, int t_mem, float *out, kda_stash *stash, int *dev_status, cudaStream_t stream)
 {
     int rc = check_common(dims, st);
     if (rc)
@@ -954,6 +972,27 @@ extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, 
             return fail(KDA_EINVAL, "the snapshots must not alias the resident state");
     }
     ScanParams p{};
+    p.keep_mode = KEEP_NONE;
+    if (t_rows) {
+        if (t_mem == KDA_MEM_HOST) {
+            if (dims->B > KDA_HOST_KEEP_MAX)
+                return fail(KDA_EINVAL, "B exceeds KDA_HOST_KEEP_MAX for host row counts; pass them on the device");
+            for (int b = 0; b < dims->B; ++b) {
+                if (t_rows[b] < 1 || t_rows[b] > T)
+                    return fail(KDA_EINVAL, "t_rows[" + std::to_string(b) + "] = " + std::to_string(t_rows[b]) +
+                                                " outside 1.." + std::to_string(T));
+                p.keep_host[b] = static_cast<unsigned char>(t_rows[b]);
+            }
+            p.keep_mode = ROWS_HOST;
+        } else if (t_mem == KDA_MEM_DEVICE) {
+            if (reinterpret_cast<uintptr_t>(t_rows) & 3u)
+                return fail(KDA_EINVAL, "device t_rows must be 4-byte aligned");
+            p.keep_mode = ROWS_DEVICE;
+            p.rows_dev = t_rows;
+        } else {
+            return fail(KDA_EINVAL, "t_mem must be KDA_MEM_HOST or KDA_MEM_DEVICE");
+        }
+    }
     p.s_out = st->state;
     p.s_snap = stash ? stash->state_snap : nullptr;
     p.ring_in = st->conv_ring;
@@ -962,12 +1001,12 @@ extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, 
     p.conv_w = st->conv_w;
     p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
     p.out = out;
+    p.status = dev_status;
     p.L = dims->L; p.B = dims->B; p.H = dims->H;
     p.T_rows = T;
     p.T_run = T;
     p.tcap = T;
     p.bf16 = dims->dtype == KDA_BF16;
-    p.keep_mode = KEEP_NONE;
     if ((rc = launch_scan(p, st->state, stream)))
         return rc;
     if (stash) {
@@ -977,8 +1016,32 @@ extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, 
     return ok();
 }
 
-extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash,
-                            const int *keep, int keep_mem, int *dev_status, cudaStream_t stream)
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
+                               int T, float *out, kda_stash *stash, cudaStream_t stream)
+{
+    return verify_common(dims, st, rows, T, nullptr, KDA_MEM_HOST, out, stash, nullptr, stream);
+}
+
+extern "C" int kda_verify_scan_var(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
+                                   int T_cap, const int *t_rows, int t_mem, float *out, kda_stash *stash,
+                                   int *dev_status, cudaStream_t stream)
+{
+    if (!t_rows && dims && static_cast<long long>(dims->L) * dims->B * dims->H > 0)
+        return fail(KDA_EINVAL, "t_rows must not be NULL");
+    return verify_common(dims, st, rows, T_cap, t_rows, t_mem, out, stash, dev_status, stream);
+}
+
+namespace kda {
+namespace {
+
+// Shared body of kda_rollback and kda_rollback_var.  t_rows == nullptr: the round ran
+// stash->T rows for every session; else t_rows[b] rows for session b (same memory kind
+// as keep).
+int rollback_common(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash, const int *t_rows,
+                    const int *keep, int keep_mem, int *dev_status, cudaStream_t stream)
 {
     int rc = check_common(dims, st);
     if (rc)
@@ -1001,21 +1064,27 @@ extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, con
             return fail(KDA_EINVAL, "B exceeds KDA_HOST_KEEP_MAX for a host keep array; pass keep on the device");
         bool any = false;
         for (int b = 0; b < dims->B; ++b) {
-            if (keep[b] < 1 || keep[b] > stash->T)
+            const int tb = t_rows ? t_rows[b] : stash->T;
+            if (tb < 1 || tb > stash->T)
+                return fail(KDA_EINVAL, "t_rows[" + std::to_string(b) + "] = " + std::to_string(tb) + " outside 1.." +
+                                            std::to_string(stash->T));
+            if (keep[b] < 1 || keep[b] > tb)
                 return fail(KDA_EINVAL, "keep[" + std::to_string(b) + "] = " + std::to_string(keep[b]) +
-                                            " outside 1.." + std::to_string(stash->T) +
+                                            " outside 1.." + std::to_string(tb) +
                                             " (the anchor row is always kept; keep = accepted drafts + 1)");
-            p.keep_host[b] = static_cast<unsigned char>(keep[b]);
-            any |= keep[b] < stash->T;
+            // a session that keeps all of its rows has nothing to restore
+            p.keep_host[b] = static_cast<unsigned char>(keep[b] < tb ? keep[b] : stash->T);
+            any |= keep[b] < tb;
         }
         if (!any)
-            return ok();  // every session accepted all rows: nothing to restore
+            return ok();
         p.keep_mode = KEEP_HOST;
     } else if (keep_mem == KDA_MEM_DEVICE) {
-        if (reinterpret_cast<uintptr_t>(keep) & 3u)
-            return fail(KDA_EINVAL, "device keep must be 4-byte aligned");
+        if ((reinterpret_cast<uintptr_t>(keep) & 3u) || (reinterpret_cast<uintptr_t>(t_rows) & 3u))
+            return fail(KDA_EINVAL, "device keep and t_rows must be 4-byte aligned");
         p.keep_mode = KEEP_DEVICE;
         p.keep_dev = keep;
+        p.rows_dev = t_rows;
     } else {
         return fail(KDA_EINVAL, "keep_mem must be KDA_MEM_HOST or KDA_MEM_DEVICE");
     }
@@ -1035,4 +1104,21 @@ extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, con
     p.tcap = stash->T;
     p.bf16 = dims->dtype == KDA_BF16;
     return launch_scan(p, stash->state_snap, stream);
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_rollback(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash,
+                            const int *keep, int keep_mem, int *dev_status, cudaStream_t stream)
+{
+    return rollback_common(dims, st, stash, nullptr, keep, keep_mem, dev_status, stream);
+}
+
+extern "C" int kda_rollback_var(const kda_dims *dims, const kda_layer_state *st, const kda_stash *stash,
+                                const int *t_rows, const int *keep, int mem, int *dev_status, cudaStream_t stream)
+{
+    if (!t_rows && dims && static_cast<long long>(dims->L) * dims->B * dims->H > 0)
+        return fail(KDA_EINVAL, "t_rows must not be NULL");
+    return rollback_common(dims, st, stash, t_rows, keep, mem, dev_status, stream);
 }

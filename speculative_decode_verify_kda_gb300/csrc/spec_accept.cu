@@ -51,10 +51,14 @@ __device__ __forceinline__ void take(float &bv, int &bi, float v, int i)
 
 template <bool BF16>
 __global__ void __launch_bounds__(ACC_THREADS) accept_partial_kernel(const void *__restrict__ logits, int V,
-                                                                      int vs, int chunk, Partial *__restrict__ part)
+                                                                      int vs, int chunk, Partial *__restrict__ part,
+                                                                      const int *__restrict__ t_rows, int T)
 {
     const long long row = blockIdx.x;
     const int s = blockIdx.y;
+    // with per-session row counts, rows past a session's count are never consulted
+    if (t_rows && static_cast<int>(row % T) >= t_rows[row / T])
+        return;
     const int begin = s * chunk;
     const int end = min(V, begin + chunk);
     float bv = -INFINITY;
@@ -135,18 +139,34 @@ __global__ void __launch_bounds__(ACC_THREADS) accept_partial_kernel(const void 
     }
 }
 
+// t_rows (nullable): session b's round has t_rows[b] rows of the T in the layout; its
+// drafts are drafts[b][0 .. t_rows[b]-2] (the layout keeps T-1 draft slots per session).
 __global__ void accept_final_kernel(const Partial *__restrict__ part, int B, int T, int vs,
                                     const int *__restrict__ drafts, int *j_out, int *bonus_out, int *keep_out,
-                                    int *status)
+                                    int *status, const int *__restrict__ t_rows)
 {
     const int warps = blockDim.x / 32;
     const int b = blockIdx.x * warps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (b >= B)
         return;
-    const int K = T - 1;
+    const int Tb = t_rows ? t_rows[b] : T;
+    if (Tb < 1 || Tb > T) {  // an invalid row count: no accept for this session
+        if (lane == 0) {
+            if (j_out)
+                j_out[b] = -1;
+            if (bonus_out)
+                bonus_out[b] = -1;
+            if (keep_out)
+                keep_out[b] = 0;
+            if (status)
+                atomicOr(status, KDA_ST_BADKEEP);
+        }
+        return;
+    }
+    const int K = Tb - 1;
     int vam = -1;
-    if (lane < T) {
+    if (lane < Tb) {
         const Partial *pr = part + (static_cast<long long>(b) * T + lane) * vs;
         float bv = -INFINITY;
         int bi = 0x7fffffff, nan = 0;
@@ -157,7 +177,7 @@ __global__ void accept_final_kernel(const Partial *__restrict__ part, int B, int
         }
         vam = nan ? -1 : bi;
     }
-    const bool miss = lane < K && (vam < 0 || drafts[static_cast<long long>(b) * K + lane] != vam);
+    const bool miss = lane < K && (vam < 0 || drafts[static_cast<long long>(b) * (T - 1) + lane] != vam);
     const unsigned mask = __ballot_sync(0xffffffffu, miss);
     const int j = mask ? __ffs(mask) - 1 : K;
     const int bonus = __shfl_sync(0xffffffffu, vam, j);
@@ -215,15 +235,15 @@ extern "C" int spec_accept(const void *logits, int logit_dtype, int B, int T, in
     Partial *part = static_cast<Partial *>(scratch);
     dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
     if (logit_dtype == KDA_BF16)
-        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, nullptr, T);
     else
-        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, nullptr, T);
     int rc = check_launch("accept_partial_kernel");
     if (rc)
         return rc;
     const int warps = 4;
     accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
-                                                                            bonus_out, keep_out, dev_status);
+                                                                            bonus_out, keep_out, dev_status, nullptr);
     return check_launch("accept_final_kernel");
 }
 
@@ -306,14 +326,137 @@ extern "C" int spec_accept_noalloc(const void *logits, int logit_dtype, int B, i
     Partial *part = static_cast<Partial *>(scratch);
     dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
     if (logit_dtype == KDA_BF16)
-        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, nullptr, T);
     else
-        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part);
+        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, nullptr, T);
     rc = check_launch("accept_partial_kernel");
     if (rc)
         return rc;
     const int warps = 4;
     accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
-                                                                            bonus_out, keep_out, dev_status);
+                                                                            bonus_out, keep_out, dev_status, nullptr);
     return check_launch("accept_final_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// Per-session round lengths: spec_accept_var (greedy accept when session b ran
+// t_rows[b] of the T rows) and spec_window (the verify-window policies that pick
+// t_rows from the drafter's slot scores).
+// ---------------------------------------------------------------------------
+namespace kda {
+namespace {
+
+__device__ __forceinline__ float sigmoid_ieee(float r)
+{
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-r)));
+}
+
+// One thread per session: scores [B][K]; writes t_out[b] = the session's verify rows.
+//   KDA_WIN_CONF_KEEP        glm_spec.rs glm5_conf_keep: scores are slot confidences q,
+//                            param = p_min, pmin0 arms the slot-0 break; rows = 1 + kept.
+//   KDA_WIN_CONFIDENCE       dflash.rs dspark_confidence_vt: scores are pre-sigmoid raws,
+//                            param = tau, cumulative survival; rows in [2, max(t_cap, 2)].
+//   KDA_WIN_SLOT_CONFIDENCE  dflash.rs dspark_slot_confidence_vt: per-slot sigmoid >= tau.
+// Every result is capped at t_cap.
+__global__ void window_kernel(const float *__restrict__ scores, int B, int K, int policy, float param, int pmin0,
+                              int t_cap, int *__restrict__ t_out)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B)
+        return;
+    const float *x = scores + static_cast<long long>(b) * K;
+    int kept = 0;
+    if (policy == KDA_WIN_CONF_KEEP) {
+        for (int j = 0; j < K; ++j) {
+            if (x[j] < param && (j > 0 || pmin0))
+                break;
+            ++kept;
+        }
+        t_out[b] = min(1 + kept, t_cap);
+        return;
+    }
+    float surv = 1.0f;
+    for (int k = 0; k < K; ++k) {
+        const float sg = sigmoid_ieee(x[k]);
+        if (policy == KDA_WIN_CONFIDENCE) {
+            surv = __fmul_rn(surv, sg);
+            if (surv < param)
+                break;
+        } else if (sg < param) {
+            break;
+        }
+        ++kept;
+    }
+    const int hi = t_cap > 2 ? t_cap : 2;
+    t_out[b] = min(max(1 + kept, 2), hi);
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int spec_accept_var(const void *logits, int logit_dtype, int B, int T, int V, const int *t_rows,
+                               const int *drafts, int *j_out, int *bonus_out, int *keep_out, int *dev_status,
+                               void *scratch, size_t scratch_bytes, cudaStream_t stream)
+{
+    if (B < 0)
+        return fail(KDA_EINVAL, "B must be >= 0");
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
+    if (V < 1)
+        return fail(KDA_EINVAL, "V must be >= 1");
+    if (logit_dtype != KDA_F32 && logit_dtype != KDA_BF16)
+        return fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
+    if (B == 0)
+        return ok();
+    if (!logits || !t_rows || (T > 1 && !drafts))
+        return fail(KDA_EINVAL, "logits, t_rows and drafts must not be NULL");
+    if (!aligned16(logits) || (reinterpret_cast<uintptr_t>(t_rows) & 3u))
+        return fail(KDA_EINVAL, "logits must be 16-byte and t_rows 4-byte aligned");
+    const size_t need = spec_accept_scratch_bytes(B, T, V);
+    if (!scratch || scratch_bytes < need || !aligned16(scratch))
+        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " +
+                                    std::to_string(need) + " bytes");
+    if (static_cast<long long>(B) * T > 0x7fffffffLL)
+        return fail(KDA_EINVAL, "B*T exceeds the grid limit");
+    const int vs = slices_for(V);
+    int chunk = (V + vs - 1) / vs;
+    chunk = (chunk + 7) / 8 * 8;
+    Partial *part = static_cast<Partial *>(scratch);
+    dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
+    if (logit_dtype == KDA_BF16)
+        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, t_rows, T);
+    else
+        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, t_rows, T);
+    int rc = check_launch("accept_partial_kernel");
+    if (rc)
+        return rc;
+    const int warps = 4;
+    accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
+                                                                            bonus_out, keep_out, dev_status, t_rows);
+    return check_launch("accept_final_kernel");
+}
+
+extern "C" int spec_window(const float *scores, int B, int K, int policy, float param, int pmin0, int t_cap,
+                           int *t_out, cudaStream_t stream)
+{
+    if (B < 0 || K < 0)
+        return fail(KDA_EINVAL, "B and K must be >= 0");
+    if (policy != KDA_WIN_CONF_KEEP && policy != KDA_WIN_CONFIDENCE && policy != KDA_WIN_SLOT_CONFIDENCE)
+        return fail(KDA_EINVAL, "policy must be KDA_WIN_CONF_KEEP, KDA_WIN_CONFIDENCE or KDA_WIN_SLOT_CONFIDENCE");
+    const int lo = policy == KDA_WIN_CONF_KEEP ? 1 : 2;
+    if (t_cap < lo || t_cap > KDA_TMAX)
+        return fail(KDA_EINVAL, "t_cap must lie in " + std::to_string(lo) + "..15 for this policy, got " +
+                                    std::to_string(t_cap));
+    if (!(param == param))
+        return fail(KDA_EINVAL, "param must not be NaN");
+    if (B == 0)
+        return ok();
+    if ((K > 0 && !scores) || !t_out)
+        return fail(KDA_EINVAL, "scores and t_out must not be NULL");
+    if ((reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(t_out) & 3u))
+        return fail(KDA_EINVAL, "scores and t_out must be 4-byte aligned");
+    const int threads = 128;
+    window_kernel<<<(B + threads - 1) / threads, threads, 0, stream>>>(scores, B, K, policy, param, pmin0, t_cap,
+                                                                       t_out);
+    return check_launch("window_kernel");
 }

@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(L):
     assert set(names) == set(kb.EXPORTS), names
     for n in names:
         assert hasattr(L, n), n
-    assert L.kda_abi_version() == 1
+    assert L.kda_abi_version() == kb.ABI_VERSION
     assert L.kda_error_string(kb.EINVAL) == b"invalid argument"
 
 
@@ -130,3 +130,40 @@ def test_accept_rejects_on_host(L):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="missing"):
         kb.lib(str(tmp_path / "libkda_spec.so"))
+
+
+def test_var_entry_points_reject_on_host(L):
+    dims, st, rows = _state(B=3)
+    t = (ctypes.c_int * 3)(8, 9, 1)   # 9 > T
+    assert L.kda_verify_scan_var(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), 8,
+                                 ctypes.cast(t, ctypes.c_void_p), kb.MEM_HOST, None, None, None, None) == kb.EINVAL
+    assert b"outside 1..8" in L.kda_last_error()
+    assert L.kda_verify_scan_var(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), 8, None, kb.MEM_HOST,
+                                 None, None, None, None) == kb.EINVAL
+    t_ok = (ctypes.c_int * 3)(8, 5, 1)
+    assert L.kda_verify_scan_var(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), 8,
+                                 ctypes.cast(t_ok, ctypes.c_void_p), 7, None, None, None, None) == kb.EINVAL
+    stash = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, rows, 8)
+    keep = (ctypes.c_int * 3)(8, 6, 1)   # keep 6 > t_rows 5
+    assert L.kda_rollback_var(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash),
+                              ctypes.cast(t_ok, ctypes.c_void_p), ctypes.cast(keep, ctypes.c_void_p), kb.MEM_HOST,
+                              None, None) == kb.EINVAL
+    assert b"outside 1..5" in L.kda_last_error()
+    # every session keeps all of its own rows: nothing launched
+    full = (ctypes.c_int * 3)(8, 5, 1)
+    assert L.kda_rollback_var(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash),
+                              ctypes.cast(t_ok, ctypes.c_void_p), ctypes.cast(full, ctypes.c_void_p), kb.MEM_HOST,
+                              None, None) == kb.OK
+
+
+def test_window_and_accept_var_reject_on_host(L):
+    assert L.spec_window(FAKE, 4, 7, 3, 0.5, 0, 8, FAKE, None) == kb.EINVAL           # unknown policy
+    assert L.spec_window(FAKE, 4, 7, kb.WIN_CONFIDENCE, 0.5, 0, 1, FAKE, None) == kb.EINVAL  # cap below 2
+    assert L.spec_window(FAKE, 4, 7, kb.WIN_CONF_KEEP, 0.5, 0, 16, FAKE, None) == kb.EINVAL  # cap above 15
+    assert L.spec_window(FAKE, 4, 7, kb.WIN_CONF_KEEP, float("nan"), 0, 8, FAKE, None) == kb.EINVAL
+    assert L.spec_window(None, 0, 7, kb.WIN_CONF_KEEP, 0.5, 0, 8, None, None) == kb.OK   # nothing to do
+    need = L.spec_accept_scratch_bytes(2, 8, 1000)
+    assert L.spec_accept_var(FAKE, kb.BF16, 2, 8, 1000, None, FAKE, None, None, None, None, FAKE, need,
+                             None) == kb.EINVAL
+    assert L.spec_accept_var(FAKE, kb.BF16, 2, 8, 1000, FAKE + 2, FAKE, None, None, None, None, FAKE, need,
+                             None) == kb.EINVAL
