@@ -92,8 +92,11 @@ class Oracle:
         self.lib.kdao_conf_keep.argtypes = [ci, vp, cf, ci]
         self.lib.kdao_confidence_vt.argtypes = [ci, vp, cf, ci]
         self.lib.kdao_slot_confidence_vt.argtypes = [ci, vp, cf, ci]
+        cd = ctypes.c_double
+        self.lib.kdao_filtered.argtypes = [ci, ci, vp, cd, ci, cd, cd, vp]
+        self.lib.kdao_sampled_accept.argtypes = [ci, ci, ci, vp, vp, vp, vp, cd, cd, ci, cd, cd, vp, vp]
         for fn in ("kdao_prepare", "kdao_core", "kdao_verify", "kdao_rollback", "kdao_accept", "kdao_conf_keep",
-                   "kdao_confidence_vt", "kdao_slot_confidence_vt"):
+                   "kdao_confidence_vt", "kdao_slot_confidence_vt", "kdao_filtered", "kdao_sampled_accept"):
             getattr(self.lib, fn).restype = ci
 
     @staticmethod
@@ -194,6 +197,34 @@ class Oracle:
         """Verify rows from per-slot sigmoid(raws) (dspark_slot_confidence_vt)."""
         r = _f32(raws).reshape(-1)
         return int(self.lib.kdao_slot_confidence_vt(r.size, _p(r) if r.size else None, float(tau), int(vt_cap)))
+
+    # -- sampled acceptance ----------------------------------------------------
+    def filtered(self, row, temperature=1.0, top_k=0, top_p=1.0, min_p=0.0):
+        """Filtered distribution of one logits row (float32 or bf16 bits) as float64 [V]."""
+        row, dt = _raw(row)
+        V = row.shape[-1]
+        p = np.empty(V)
+        rc = self.lib.kdao_filtered(V, dt, _p(row), float(temperature), int(top_k), float(top_p), float(min_p),
+                                    _p(p))
+        self._check("kdao_filtered", rc)
+        return p
+
+    def sampled_accept(self, logits, draft_logits, drafts, u_accept, u_sample, temperature=1.0, top_k=0,
+                       top_p=1.0, min_p=0.0):
+        """Sampled accept walk of one session; returns (j, token)."""
+        logits, dt = _raw(logits)
+        T, V = logits.shape
+        K = T - 1
+        draft_logits = _raw(draft_logits)[0] if K else np.zeros((1, V), logits.dtype)
+        drafts = np.ascontiguousarray(drafts, dtype=np.int32).reshape(-1)
+        u_accept = _f64(u_accept).reshape(-1)
+        assert drafts.shape == (K,) and u_accept.shape == (K,)
+        j, tok = ctypes.c_int(), ctypes.c_int()
+        rc = self.lib.kdao_sampled_accept(T, V, dt, _p(logits), _p(draft_logits), _p(drafts) if K else None,
+                                          _p(u_accept) if K else None, float(u_sample), float(temperature),
+                                          int(top_k), float(top_p), float(min_p), ctypes.byref(j), ctypes.byref(tok))
+        self._check("kdao_sampled_accept", rc)
+        return j.value, tok.value
 
     # -- [L][B] helper ---------------------------------------------------------
     def verify_units(self, rows, conv_w, ring, state, units=None):

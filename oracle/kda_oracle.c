@@ -357,3 +357,153 @@ int kdao_slot_confidence_vt(int n, const float *raws, float tau, int vt_cap)
     }
     return clamp_vt(kept, vt_cap);
 }
+
+/* ---------------------------------------------------------------------------
+ * Sampled acceptance (glm_spec.rs module doc, SAMPLED ACCEPTANCE, and
+ * glm5_sampled_accept / glm5_sampled_bonus): the rejection-sampling walk over the
+ * verify rows, with target p and draft q taken through the same filter.
+ *
+ * Filtered distribution of one logits row x[0..V-1] (filter_stats +
+ * softmax_gather_filtered; their internals are not printed, so this is the plain
+ * reading: each filter is a threshold on the one unfiltered distribution and a
+ * token is kept when it passes all of them):
+ *   z = x / temperature,  e_v = exp(z_v - max z)  (so max e = 1),  S = sum e
+ *   top_k in 1..V-1: kept iff e_v >= the k-th largest e        (ties at it kept)
+ *   top_p < 1:       with e sorted descending, n = the first count whose running
+ *                    sum reaches top_p * S; kept iff e_v >= e_(n) (ties kept)
+ *   min_p > 0:       kept iff e_v >= min_p  (p_v >= min_p * max p)
+ *   p~_v = e_v / Z over the kept tokens, Z = sum of their e; 0 elsewhere.
+ * ------------------------------------------------------------------------- */
+static int cmp_desc(const void *a, const void *b)
+{
+    double x = *(const double *)a, y = *(const double *)b;
+    return x < y ? 1 : (x > y ? -1 : 0);
+}
+
+int kdao_filtered(int V, int dtype, const void *row, double temperature, int top_k, double top_p,
+                  double min_p, double *p)
+{
+    if (V < 1 || !(temperature > 0.0) || top_k < 0 || !(top_p > 0.0) || !(min_p >= 0.0) || min_p >= 1.0)
+        return KDAO_EINVAL;
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double z = widen(row, dtype, (size_t)v) / temperature;
+        if (isnan(z))
+            return KDAO_ENAN;
+        p[v] = z;
+        if (z > m)
+            m = z;
+    }
+    if (isinf(m))  /* every logit -inf, or a +inf logit: no distribution */
+        return KDAO_EINVAL;
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+        p[v] = exp(p[v] - m);
+        S += p[v];
+    }
+    double *sorted = malloc(sizeof(double) * (size_t)V);
+    if (!sorted)
+        return KDAO_ENOMEM;
+    memcpy(sorted, p, sizeof(double) * (size_t)V);
+    qsort(sorted, (size_t)V, sizeof(double), cmp_desc);
+    double th = 0.0;
+    if (top_k > 0 && top_k < V && sorted[top_k - 1] > th)
+        th = sorted[top_k - 1];
+    if (top_p < 1.0) {
+        double run = 0.0;
+        for (int i = 0; i < V; ++i) {
+            run += sorted[i];
+            if (run >= top_p * S) {
+                if (sorted[i] > th)
+                    th = sorted[i];
+                break;
+            }
+        }
+    }
+    free(sorted);
+    if (min_p > th)
+        th = min_p;
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v)
+        if (p[v] >= th)
+            Z += p[v];
+    for (int v = 0; v < V; ++v)
+        p[v] = p[v] >= th ? p[v] / Z : 0.0;
+    return KDAO_OK;
+}
+
+/* One draw from weights w[0..V-1] (not all zero) with the uniform u in [0, 1):
+ * the first index whose running sum, in index order, exceeds u * sum(w). */
+static int draw_index(int V, const double *w, double u)
+{
+    double W = 0.0;
+    for (int v = 0; v < V; ++v)
+        W += w[v];
+    double target = u * W, run = 0.0;
+    int last = -1;
+    for (int v = 0; v < V; ++v) {
+        if (w[v] > 0.0)
+            last = v;
+        run += w[v];
+        if (run > target)
+            return v;
+    }
+    return last;  /* u * W rounded up to W: the last token with weight */
+}
+
+/* The sampled accept walk of one session.  logits [T][V] (target rows),
+ * draft_logits [T-1][V] (the rows the drafts were drawn from), drafts [T-1];
+ * u_accept[r] is the accept-test uniform of draft r, u_sample the uniform of the
+ * final draw.  Draft r is accepted iff u_accept[r] * q~_r(x_r) < p~_r(x_r); the walk
+ * stops at the first rejection j.  j < K: the token is drawn from the residual
+ * max(0, p~_j - q~_j) (from p~_j when that residual is zero everywhere); j = K: the
+ * bonus is drawn from p~_K, the last verify row. */
+int kdao_sampled_accept(int T, int V, int dtype, const void *logits, const void *draft_logits,
+                        const int *drafts, const double *u_accept, double u_sample, double temperature,
+                        int top_k, double top_p, double min_p, int *j_out, int *token_out)
+{
+    if (T < 1 || V < 1)
+        return KDAO_EINVAL;
+    const int K = T - 1;
+    size_t es = dtype == KDAO_BF16 ? 2 : 4;
+    double *pr = malloc(sizeof(double) * (size_t)V), *qr = malloc(sizeof(double) * (size_t)V);
+    if (!pr || !qr) {
+        free(pr);
+        free(qr);
+        return KDAO_ENOMEM;
+    }
+    int rc = KDAO_OK, j = 0;
+    for (; j < K; ++j) {
+        if (drafts[j] < 0 || drafts[j] >= V) {
+            rc = KDAO_EINVAL;
+            goto done;
+        }
+        if ((rc = kdao_filtered(V, dtype, (const char *)logits + (size_t)j * V * es, temperature, top_k, top_p,
+                                min_p, pr)))
+            goto done;
+        if ((rc = kdao_filtered(V, dtype, (const char *)draft_logits + (size_t)j * V * es, temperature, top_k,
+                                top_p, min_p, qr)))
+            goto done;
+        if (!(u_accept[j] * qr[drafts[j]] < pr[drafts[j]]))
+            break;
+    }
+    if (j < K) {  /* pr, qr hold row j */
+        int any = 0;
+        for (int v = 0; v < V; ++v) {
+            double r = pr[v] - qr[v];
+            qr[v] = r > 0.0 ? r : 0.0;
+            any |= qr[v] > 0.0;
+        }
+        *token_out = draw_index(V, any ? qr : pr, u_sample);
+    } else {
+        if ((rc = kdao_filtered(V, dtype, (const char *)logits + (size_t)K * V * es, temperature, top_k, top_p,
+                                min_p, pr)))
+            goto done;
+        *token_out = draw_index(V, pr, u_sample);
+    }
+    *j_out = j;
+done:
+    free(pr);
+    free(qr);
+    return rc;
+}

@@ -50,6 +50,12 @@ int kdao_conf_keep(int n, const float *q, float p_min, int pmin0);
 int kdao_confidence_vt(int n, const float *raws, float tau, int vt_cap);
 int kdao_slot_confidence_vt(int n, const float *raws, float tau, int vt_cap);
 
+int kdao_filtered(int V, int dtype, const void *row, double temperature, int top_k, double top_p,
+                  double min_p, double *p);
+int kdao_sampled_accept(int T, int V, int dtype, const void *logits, const void *draft_logits,
+                        const int *drafts, const double *u_accept, double u_sample, double temperature,
+                        int top_k, double top_p, double min_p, int *j_out, int *token_out);
+
 #ifdef __cplusplus
 }
 #endif

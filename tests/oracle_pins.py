@@ -479,6 +479,135 @@ def pin_window_limits(orc):
         assert orc.slot_confidence_vt(np.full(n, 30.0, np.float32), 0.99, 4) == min(max(2, n + 1), 4)
 
 
+def _softmax(z):
+    z = np.asarray(z, np.float64)
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def pin_filter_closed_forms(orc):
+    """No filter is softmax(x / temperature); top_k = 1 is the argmax; top_k = V, top_p = 1 and
+    min_p = 0 filter nothing; the filtered distribution sums to 1."""
+    rng = np.random.default_rng(31)
+    for V in (1, 2, 7, 100):
+        x = rng.normal(0, 2, V).astype(np.float32)
+        for tau in (0.3, 1.0, 2.5):
+            ref = _softmax(x.astype(np.float64) / tau)
+            assert np.allclose(orc.filtered(x, tau), ref, rtol=1e-12, atol=1e-15)
+            assert np.allclose(orc.filtered(x, tau, top_k=V, top_p=1.0, min_p=0.0), ref, rtol=1e-12, atol=1e-15)
+            one = orc.filtered(x, tau, top_k=1)
+            assert one[int(np.argmax(x))] == 1.0 and one.sum() == 1.0
+            for kw in ({"top_k": 3}, {"top_p": 0.5}, {"min_p": 0.2}, {"top_k": 5, "top_p": 0.8, "min_p": 0.05}):
+                assert abs(orc.filtered(x, tau, **kw).sum() - 1.0) < 1e-12
+
+
+def pin_filter_brute_force(orc):
+    """Kept sets from their set definitions: top-k keeps a token when fewer than k tokens are
+    strictly more likely; top-p keeps it when the tokens strictly more likely hold less than
+    top_p of the mass; min-p keeps p >= min_p * max p.  Ties included."""
+    rng = np.random.default_rng(32)
+    for _ in range(300):
+        V = int(rng.integers(1, 9))
+        x = rng.integers(-3, 4, V).astype(np.float32)  # small integers: ties everywhere
+        tau = float(rng.choice([0.5, 1.0, 3.0]))
+        k = int(rng.integers(0, V + 2))
+        tp = float(rng.choice([1.0, 0.9, 0.5, 0.2]))
+        mp = float(rng.choice([0.0, 0.1, 0.5]))
+        p = _softmax(x.astype(np.float64) / tau)
+        keep = np.ones(V, bool)
+        for v in range(V):
+            larger = p > p[v]
+            if 0 < k < V and larger.sum() >= k:
+                keep[v] = False
+            if tp < 1.0 and p[larger].sum() >= tp:
+                keep[v] = False
+            if mp > 0 and p[v] < mp * p.max():
+                keep[v] = False
+        want = np.where(keep, p, 0.0)
+        want /= want.sum()
+        got = orc.filtered(x, tau, top_k=k, top_p=tp, min_p=mp)
+        assert np.allclose(got, want, rtol=1e-12, atol=1e-15), (x, tau, k, tp, mp, got, want)
+
+
+def pin_filter_top_p_boundary(orc):
+    """top_p reached exactly by the first token's mass keeps that token alone (the running
+    sum "reaches" top_p * S: >=, not >)."""
+    for a in (-1.0, -0.5, -2.0):
+        x = np.array([0.0, a, a], np.float32)
+        e = np.exp(x.astype(np.float64))
+        S = 0.0
+        for v in e:  # the oracle's order of summation
+            S += v
+        tp = 1.0 / S
+        assert tp * S == 1.0
+        got = orc.filtered(x, 1.0, top_p=tp)
+        assert list(got) == [1.0, 0.0, 0.0], (a, got)
+
+
+def _chi2_ok(counts, probs, n):
+    """Pearson chi-square of counts against probs, p-value above 1e-4 (scipy)."""
+    from scipy.stats import chisquare
+    m = probs > 0
+    assert counts[~m].sum() == 0, "a token outside the support was emitted"
+    exp = probs[m] * n
+    return chisquare(counts[m], exp * counts[m].sum() / exp.sum()).pvalue > 1e-4
+
+
+def pin_sampled_accept_is_exact(orc):
+    """Speculative sampling emits its first token distributed exactly as the filtered target
+    p~_0 whatever the draft distribution q~_0 (the draft token is drawn from q~_0, u ~ U(0,1)):
+    Monte Carlo with a chi-square test, for several draft/target pairs and filters."""
+    rng = np.random.default_rng(33)
+    V, n = 6, 20000
+    for case in range(4):
+        p_row = rng.normal(0, 1.5, V).astype(np.float32)
+        q_row = rng.normal(0, 1.5, V).astype(np.float32) if case != 3 else p_row.copy()
+        filt = [{}, {"top_k": 4}, {"top_p": 0.8, "min_p": 0.05}, {"temperature": 0.7}][case]
+        pt = orc.filtered(p_row, **{"temperature": 1.0, **filt})
+        qt = orc.filtered(q_row, **{"temperature": 1.0, **filt})
+        logits = np.stack([p_row, rng.normal(0, 1, V).astype(np.float32)])
+        counts = np.zeros(V, np.int64)
+        xs = rng.choice(V, n, p=qt)
+        us = rng.uniform(0, 1, (n, 2))
+        for i in range(n):
+            j, tok = orc.sampled_accept(logits, q_row[None], [int(xs[i])], [us[i, 0]], us[i, 1],
+                                        **{"temperature": 1.0, **filt})
+            counts[int(xs[i]) if j == 1 else tok] += 1
+        assert _chi2_ok(counts, pt, n), (case, counts, pt)
+        if case == 3:  # q = p: every draft is accepted
+            assert counts.sum() == n
+
+
+def pin_sampled_accept_bonus_and_greedy(orc):
+    """All drafts accepted: the bonus follows p~_K (chi-square).  top_k = 1 turns the walk into
+    greedy acceptance: j and the token equal the greedy accept of the same rows."""
+    rng = np.random.default_rng(34)
+    V, T = 5, 3
+    logits = rng.normal(0, 1, (T, V)).astype(np.float32)
+    pK = orc.filtered(logits[T - 1])
+    counts = np.zeros(V, np.int64)
+    drafts = [int(np.argmax(orc.filtered(logits[r]))) for r in range(T - 1)]
+    n = 20000
+    us = rng.uniform(0, 1, n)
+    for i in range(n):
+        j, tok = orc.sampled_accept(logits, logits[:T - 1], drafts, [0.999999, 0.999999], us[i])
+        assert j == T - 1
+        counts[tok] += 1
+    assert _chi2_ok(counts, pK, n)
+    for _ in range(200):
+        T = int(rng.integers(1, 6))
+        V = int(rng.integers(2, 30))
+        lg = rng.normal(0, 1, (T, V)).astype(np.float32)
+        dl = rng.normal(0, 1, (max(T - 1, 1), V)).astype(np.float32)[:T - 1]
+        d = [int(np.argmax(dl[r])) if rng.uniform() < 0.7 else int(np.argmax(lg[r])) for r in range(T - 1)]
+        jg, bg, _, _ = orc.accept(lg, np.array(d, np.int32))
+        js, ts = orc.sampled_accept(lg, dl, d, rng.uniform(0, 1, T - 1), float(rng.uniform()), top_k=1)
+        assert (js, ts) == (jg, bg), (lg, d)
+        # u = 0 still rejects a draft the filtered target excludes (p~ = 0 at it)
+        js0, ts0 = orc.sampled_accept(lg, dl, d, np.zeros(T - 1), 0.0, top_k=1)
+        assert (js0, ts0) == (jg, bg), (lg, d)
+
+
 PINS = [
     pin_core_matrix_form,
     pin_core_closed_form_first_write,
@@ -501,4 +630,9 @@ PINS = [
     pin_window_page_fixture,
     pin_window_brute_force,
     pin_window_limits,
+    pin_filter_closed_forms,
+    pin_filter_brute_force,
+    pin_filter_top_p_boundary,
+    pin_sampled_accept_is_exact,
+    pin_sampled_accept_bonus_and_greedy,
 ]

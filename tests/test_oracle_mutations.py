@@ -43,6 +43,17 @@ MUTATIONS = {
     "survival_not_cumulative": ("        surv *= sigmoid_f32(raws[k]);", "        surv = sigmoid_f32(raws[k]);"),
     "vt_floor": ("return vt < 2 ? 2 :", "return vt < 1 ? 1 :"),
     "vt_no_anchor": ("int vt = 1 + kept;", "int vt = kept;"),
+    "accept_test_le": ("if (!(u_accept[j] * qr[drafts[j]] < pr[drafts[j]]))",
+                       "if (!(u_accept[j] * qr[drafts[j]] <= pr[drafts[j]]))"),
+    "accept_test_swapped": ("if (!(u_accept[j] * qr[drafts[j]] < pr[drafts[j]]))",
+                            "if (!(u_accept[j] * pr[drafts[j]] < qr[drafts[j]]))"),
+    "residual_sign": ("double r = pr[v] - qr[v];", "double r = qr[v] - pr[v];"),
+    "no_renormalise": ("p[v] = p[v] >= th ? p[v] / Z : 0.0;", "p[v] = p[v] >= th ? p[v] / S : 0.0;"),
+    "top_k_off_by_one": ("th = sorted[top_k - 1];", "th = sorted[top_k];"),
+    "top_p_strict": ("if (run >= top_p * S) {", "if (run > top_p * S + 1e-9) {"),
+    "temperature_mul": ("double z = widen(row, dtype, (size_t)v) / temperature;",
+                        "double z = widen(row, dtype, (size_t)v) * temperature;"),
+    "bonus_row": ("(const char *)logits + (size_t)K * V * es, temperature", "(const char *)logits + (size_t)0 * V * es, temperature"),
     "argmax_last_tie": ("x > bv", "x >= bv"),
     "j_off_by_one": ("*j_out = j;", "*j_out = j + (j < K);"),
     "bonus_prev_row": ("*bonus_out = vam[j];", "*bonus_out = vam[j > 0 ? j - 1 : 0];"),
