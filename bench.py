@@ -402,6 +402,39 @@ def run_gpu(args, rank, world, local_rank):
         res["per_layer"] = {"launches_per_step": w.L + 3, "steps": Kp, "eager_ms_per_step": eager_ms,
                             "graph_ms_per_step": graph_ms,
                             "graph_rows_per_s": world * w.B * w.T / (graph_ms * 1e-3)}
+    # sampled acceptance: the rejection walk with filtered target and draft rows; the
+    # draft rows equal the target rows, so every draft is accepted (the longest walk)
+    if not args.no_sampled:
+        filt = dict(temperature=0.7, top_k=50, top_p=0.9, min_p=0.0)
+        lg0 = logits[0]
+        dl = lg0[:, :w.K].contiguous()
+        dr = torch.argmax(lg0[:, :w.K].float(), dim=-1).to(torch.int32).contiguous()
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        ua = torch.rand((w.B, w.K), generator=g, device=dev)
+        us = torch.rand((w.B,), generator=g, device=dev)
+        tok = torch.empty_like(j_out)
+        Ks = max(1, min(args.sampled_steps, K))
+        for _ in range(3):
+            kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
+                                   dev_status=status, stream=stream, **filt)
+        barrier()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(Ks):
+            kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
+                                   dev_status=status, stream=stream, **filt)
+        b_.record(stream)
+        barrier()
+        if int(status.item()) or int(j_out.min().item()) != w.K:
+            raise RuntimeError("sampled accept: unexpected status or walk length")
+        s_ms = a_.elapsed_time(b_) / Ks
+        nbytes = w.B * (2 * w.K + 1) * w.V * lg0.element_size()
+        res["sampled_accept"] = {"filter": filt, "walk": "every draft accepted (draft rows = target rows)",
+                                 "ms": s_ms, "greedy_accept_ms": res["accept_ms"],
+                                 "logit_rows_per_call": w.B * (2 * w.K + 1),
+                                 "logits_gbs": nbytes / (s_ms * 1e-3) / 1e9}
+
     # variable T per session: the window of each session's round from seeded drafter
     # confidences (glm5_conf_keep, p_min 0.5), then verify / accept / rollback with
     # per-session row counts, all decided on the device
@@ -457,6 +490,8 @@ def main():
     ap.add_argument("--no-per-layer", action="store_true", help="skip the per-layer (and CUDA graph) rounds")
     ap.add_argument("--per-layer-steps", type=int, default=200)
     ap.add_argument("--no-var-t", action="store_true", help="skip the variable-T rounds")
+    ap.add_argument("--no-sampled", action="store_true", help="skip the sampled-accept timing")
+    ap.add_argument("--sampled-steps", type=int, default=200)
     ap.add_argument("--var-t-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     args = ap.parse_args()
@@ -535,6 +570,7 @@ def main():
         "e2e": res.get("e2e"),
         "per_layer": res.get("per_layer"),
         "var_t": res.get("var_t"),
+        "sampled_accept": res.get("sampled_accept"),
     }
     print(json.dumps(line))
 

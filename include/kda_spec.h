@@ -70,6 +70,9 @@ extern "C" {
                                left untouched                                    */
 #define KDA_ST_TIMEOUT 0x4  /* a bulk copy into shared memory did not arrive in
                                time (bounded wait); the CTA stopped early       */
+#define KDA_ST_TIES 0x8     /* spec_accept_sampled: more than 2*KDA_SAMPLED_TOPK_MAX
+                               tokens tie at a row's top-k boundary; that row's
+                               top-p filter was skipped                          */
 
 /* element types of raw rows and logits */
 #define KDA_F32 0
@@ -213,6 +216,43 @@ int spec_accept_var(const void *logits, int logit_dtype, int B, int T, int V, co
  */
 int spec_window(const float *scores, int B, int K, int policy, float param, int pmin0, int t_cap,
                 int *t_out, cudaStream_t stream);
+
+/*
+ * Sampled acceptance.  glm_spec.rs module doc, SAMPLED ACCEPTANCE, and
+ * glm5_sampled_accept / glm5_sampled_bonus: the rejection-sampling walk over the
+ * verify rows.  Target p (verify rows) and draft q (the rows the drafts were drawn
+ * from) go through one filter (filter_stats + softmax_gather_filtered):
+ *   z = x / temperature, e = exp(z - max z), S = sum e; a token is kept when it
+ *   passes every enabled threshold on e: top_k (e >= the k-th largest e, ties kept),
+ *   top_p (e >= e_(n), n the first count of the descending-sorted e whose running
+ *   sum reaches top_p * S), min_p (e >= min_p); p~ = e / Z over the kept tokens.
+ * Draft r is accepted iff u_accept[r] * q~_r(x_r) < p~_r(x_r); the walk stops at the
+ * first rejection j.  j < K: the token is drawn from max(0, p~_j - q~_j) (from p~_j
+ * if that is zero everywhere); j = K: the bonus is drawn from p~_K.  A draw takes
+ * the first token, in vocabulary order, whose running weight exceeds u_sample * (total
+ * weight).  The uniforms are the caller's (e.g. a counter-based generator per
+ * session); every result is reproducible bit for bit from the inputs.
+ */
+#define KDA_SAMPLED_TOPK_MAX 512
+typedef struct kda_sampling {
+    float temperature; /* > 0                                                  */
+    int top_k;         /* 0 (off) or 1..KDA_SAMPLED_TOPK_MAX                    */
+    float top_p;       /* (0, 1]; < 1 needs top_k >= 1 (its candidates are sorted) */
+    float min_p;       /* [0, 1); 0 off                                        */
+} kda_sampling;
+
+/*
+ * spec_accept_sampled -- sampled acceptance for B sessions.
+ *   logits [B][T][V] and draft_logits [B][T-1][V] (logit_dtype), drafts int32
+ *   [B][T-1], u_accept f32 [B][T-1] and u_sample f32 [B] in [0, 1), all device
+ *   memory; sp a host struct.  Outputs device int32 [B]: j_out (accepted drafts),
+ *   token_out (the residual draw, or the bonus at j = K), keep_out (j + 1, may be
+ *   NULL).  A consulted row holding a NaN or no finite maximum gives token -1 and
+ *   sets KDA_ST_NAN.  A draft id outside 0..V-1 is rejected.  Needs no scratch.
+ */
+int spec_accept_sampled(const void *logits, const void *draft_logits, int logit_dtype, int B, int T, int V,
+                        const int *drafts, const float *u_accept, const float *u_sample, const kda_sampling *sp,
+                        int *j_out, int *token_out, int *keep_out, int *dev_status, cudaStream_t stream);
 
 /* Bytes of device scratch spec_accept needs for B sessions of T rows of V logits. */
 size_t spec_accept_scratch_bytes(int B, int T, int V);

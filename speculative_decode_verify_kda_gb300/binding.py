@@ -21,13 +21,14 @@ D = 128
 TMAX = 15
 HOST_KEEP_MAX = 2048
 OK, EINVAL, ENAN, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
-ST_NAN, ST_BADKEEP, ST_TIMEOUT = 0x1, 0x2, 0x4
+ST_NAN, ST_BADKEEP, ST_TIMEOUT, ST_TIES = 0x1, 0x2, 0x4, 0x8
+SAMPLED_TOPK_MAX = 512
 F32, BF16 = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "spec_accept_var",
-           "spec_window", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
+           "spec_window", "spec_accept_sampled", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
 ABI_VERSION = 2
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
@@ -50,6 +51,11 @@ class KdaRows(ctypes.Structure):
 class KdaStashC(ctypes.Structure):
     _fields_ = [("state_snap", ctypes.c_void_p), ("ring_snap", ctypes.c_void_p),
                 ("rows", KdaRows), ("T", ctypes.c_int)]
+
+
+class KdaSampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int), ("top_p", ctypes.c_float),
+                ("min_p", ctypes.c_float)]
 
 
 class KdaError(RuntimeError):
@@ -88,6 +94,9 @@ def lib(path: str | None = None):
     L.spec_accept_var.restype = ci
     L.spec_window.argtypes = [vp, ci, ci, ci, ctypes.c_float, ci, ci, vp, vp]
     L.spec_window.restype = ci
+    L.spec_accept_sampled.argtypes = [vp, vp, ci, ci, ci, ci, vp, vp, vp, ctypes.POINTER(KdaSampling), vp, vp, vp,
+                                      vp, vp]
+    L.spec_accept_sampled.restype = ci
     L.spec_accept_scratch_bytes.argtypes = [ci, ci, ci]
     L.spec_accept_scratch_bytes.restype = sz
     L.spec_accept.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -324,6 +333,30 @@ def spec_window(scores: torch.Tensor, policy: int, param: float, t_cap: int, pmi
                            ctypes.c_void_p(_stream(stream)))
     _check("spec_window", rc)
     return t_out
+
+
+def spec_accept_sampled(logits: torch.Tensor, draft_logits: torch.Tensor, drafts: torch.Tensor,
+                        u_accept: torch.Tensor, u_sample: torch.Tensor, temperature: float = 1.0, top_k: int = 0,
+                        top_p: float = 1.0, min_p: float = 0.0, j_out=None, token_out=None, keep_out=None,
+                        dev_status=None, stream=None):
+    """Sampled acceptance: logits [B][T][V], draft_logits [B][T-1][V] (same dtype), drafts
+    int32 [B][T-1], u_accept f32 [B][T-1], u_sample f32 [B].  Returns (j, token, keep)."""
+    _dev(logits, "logits")
+    B, T, V = (int(x) for x in logits.shape)
+    _dev(draft_logits, "draft_logits", logits.dtype, (B, T - 1, V))
+    _dev(drafts, "drafts", torch.int32, (B, T - 1))
+    _dev(u_accept, "u_accept", torch.float32, (B, T - 1))
+    _dev(u_sample, "u_sample", torch.float32, (B,))
+    dev = logits.device
+    j_out = torch.empty(B, dtype=torch.int32, device=dev) if j_out is None else j_out
+    token_out = torch.empty(B, dtype=torch.int32, device=dev) if token_out is None else token_out
+    keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
+    sp = KdaSampling(float(temperature), int(top_k), float(top_p), float(min_p))
+    rc = lib().spec_accept_sampled(_ptr(logits), _ptr(draft_logits), _row_dtype(logits), B, T, V, _ptr(drafts),
+                                   _ptr(u_accept), _ptr(u_sample), ctypes.byref(sp), _ptr(j_out), _ptr(token_out),
+                                   _ptr(keep_out), _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+    _check("spec_accept_sampled", rc)
+    return j_out, token_out, keep_out
 
 
 def spec_accept_scratch_bytes(B: int, T: int, V: int) -> int:

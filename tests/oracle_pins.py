@@ -549,6 +549,8 @@ def _chi2_ok(counts, probs, n):
     from scipy.stats import chisquare
     m = probs > 0
     assert counts[~m].sum() == 0, "a token outside the support was emitted"
+    if m.sum() == 1:  # one token carries all the mass: every draw must be it
+        return bool(counts[m].sum() == n)
     exp = probs[m] * n
     return chisquare(counts[m], exp * counts[m].sum() / exp.sum()).pvalue > 1e-4
 

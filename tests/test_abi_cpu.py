@@ -167,3 +167,25 @@ def test_window_and_accept_var_reject_on_host(L):
                              None) == kb.EINVAL
     assert L.spec_accept_var(FAKE, kb.BF16, 2, 8, 1000, FAKE + 2, FAKE, None, None, None, None, FAKE, need,
                              None) == kb.EINVAL
+
+
+@pytest.mark.parametrize("sp", [(0.0, 0, 1.0, 0.0), (1.0, -1, 1.0, 0.0), (1.0, kb.SAMPLED_TOPK_MAX + 1, 1.0, 0.0),
+                                (1.0, 0, 0.9, 0.0), (1.0, 10, 0.0, 0.0), (1.0, 10, 1.5, 0.0), (1.0, 0, 1.0, 1.0),
+                                (float("inf"), 0, 1.0, 0.0)])
+def test_sampled_accept_rejects_bad_parameters(L, sp):
+    s = kb.KdaSampling(*sp)
+    rc = L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, ctypes.byref(s), FAKE, FAKE, None,
+                               None, None)
+    assert rc == kb.EINVAL and L.kda_last_error()
+
+
+def test_sampled_accept_rejects_bad_shapes_and_pointers(L):
+    s = kb.KdaSampling(1.0, 50, 0.9, 0.0)
+    call = lambda **k: L.spec_accept_sampled(k.get("lg", FAKE), FAKE, k.get("dt", kb.BF16), k.get("B", 2),
+                                             k.get("T", 8), k.get("V", 1000), FAKE, FAKE, k.get("us", FAKE),
+                                             ctypes.byref(s), FAKE, FAKE, None, None, None)
+    assert call(T=0) == kb.EINVAL and call(T=16) == kb.EINVAL and call(V=0) == kb.EINVAL
+    assert call(dt=9) == kb.EINVAL and call(us=None) == kb.EINVAL and call(lg=FAKE + 1) == kb.EINVAL
+    assert call(B=0) == kb.OK
+    assert L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None,
+                                 None) == kb.EINVAL
