@@ -248,11 +248,16 @@ typedef struct kda_sampling {
  *   memory; sp a host struct.  Outputs device int32 [B]: j_out (accepted drafts),
  *   token_out (the residual draw, or the bonus at j = K), keep_out (j + 1, may be
  *   NULL).  A consulted row holding a NaN or no finite maximum gives token -1 and
- *   sets KDA_ST_NAN.  A draft id outside 0..V-1 is rejected.  Needs no scratch.
+ *   sets KDA_ST_NAN.  A draft id outside 0..V-1 is rejected.
+ *   scratch: device memory of at least spec_accept_sampled_scratch_bytes(B, T)
+ *   bytes, 16-byte aligned, for the per-row filter statistics (the target and draft
+ *   rows are filtered in parallel, then each session walks); no initialisation needed.
  */
+size_t spec_accept_sampled_scratch_bytes(int B, int T);
 int spec_accept_sampled(const void *logits, const void *draft_logits, int logit_dtype, int B, int T, int V,
                         const int *drafts, const float *u_accept, const float *u_sample, const kda_sampling *sp,
-                        int *j_out, int *token_out, int *keep_out, int *dev_status, cudaStream_t stream);
+                        int *j_out, int *token_out, int *keep_out, int *dev_status, void *scratch,
+                        size_t scratch_bytes, cudaStream_t stream);
 
 /* Bytes of device scratch spec_accept needs for B sessions of T rows of V logits. */
 size_t spec_accept_scratch_bytes(int B, int T, int V);

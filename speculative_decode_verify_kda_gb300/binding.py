@@ -28,7 +28,7 @@ MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "spec_accept_var",
-           "spec_window", "spec_accept_sampled", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
+           "spec_window", "spec_accept_sampled", "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
 ABI_VERSION = 2
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
@@ -95,7 +95,9 @@ def lib(path: str | None = None):
     L.spec_window.argtypes = [vp, ci, ci, ci, ctypes.c_float, ci, ci, vp, vp]
     L.spec_window.restype = ci
     L.spec_accept_sampled.argtypes = [vp, vp, ci, ci, ci, ci, vp, vp, vp, ctypes.POINTER(KdaSampling), vp, vp, vp,
-                                      vp, vp]
+                                      vp, vp, sz, vp]
+    L.spec_accept_sampled_scratch_bytes.argtypes = [ci, ci]
+    L.spec_accept_sampled_scratch_bytes.restype = sz
     L.spec_accept_sampled.restype = ci
     L.spec_accept_scratch_bytes.argtypes = [ci, ci, ci]
     L.spec_accept_scratch_bytes.restype = sz
@@ -338,7 +340,7 @@ def spec_window(scores: torch.Tensor, policy: int, param: float, t_cap: int, pmi
 def spec_accept_sampled(logits: torch.Tensor, draft_logits: torch.Tensor, drafts: torch.Tensor,
                         u_accept: torch.Tensor, u_sample: torch.Tensor, temperature: float = 1.0, top_k: int = 0,
                         top_p: float = 1.0, min_p: float = 0.0, j_out=None, token_out=None, keep_out=None,
-                        dev_status=None, stream=None):
+                        dev_status=None, scratch: torch.Tensor | None = None, stream=None):
     """Sampled acceptance: logits [B][T][V], draft_logits [B][T-1][V] (same dtype), drafts
     int32 [B][T-1], u_accept f32 [B][T-1], u_sample f32 [B].  Returns (j, token, keep)."""
     _dev(logits, "logits")
@@ -352,9 +354,13 @@ def spec_accept_sampled(logits: torch.Tensor, draft_logits: torch.Tensor, drafts
     token_out = torch.empty(B, dtype=torch.int32, device=dev) if token_out is None else token_out
     keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
     sp = KdaSampling(float(temperature), int(top_k), float(top_p), float(min_p))
+    need = int(lib().spec_accept_sampled_scratch_bytes(B, T))
+    if scratch is None:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     rc = lib().spec_accept_sampled(_ptr(logits), _ptr(draft_logits), _row_dtype(logits), B, T, V, _ptr(drafts),
                                    _ptr(u_accept), _ptr(u_sample), ctypes.byref(sp), _ptr(j_out), _ptr(token_out),
-                                   _ptr(keep_out), _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+                                   _ptr(keep_out), _ptr(dev_status), _ptr(scratch),
+                                   scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
     _check("spec_accept_sampled", rc)
     return j_out, token_out, keep_out
 

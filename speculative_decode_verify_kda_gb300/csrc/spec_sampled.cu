@@ -14,12 +14,16 @@
 // The uniforms are inputs; the final draw takes the first token whose running
 // weight, in vocabulary order, exceeds u * (total weight).
 //
-// One CTA per session.  Every reduction and scan runs in a fixed order, so the
-// results are reproducible bit for bit.  Per row: max, sum, an exact radix select
-// of the k-th largest logit (four 8-bit histogram passes over order-preserving
-// keys), the candidates at or above it gathered into shared memory and bitonic-
-// sorted by (e descending, index ascending) for the top-p running sum, then the
-// kept mass Z.  The rows stay in L1 between passes.
+// Two launches.  Every reduction and scan runs in a fixed order, so the results
+// are reproducible bit for bit.
+//   1. row_stats_kernel, one CTA per (session, row) of the 2T-1 target and draft
+//      rows: max, sum, an exact radix select of the k-th largest logit (four 8-bit
+//      histogram passes over order-preserving keys), the candidates at or above it
+//      gathered into shared memory and bitonic-sorted by (e descending, index
+//      ascending) for the top-p running sum, then the kept mass Z, into scratch.
+//      The row stays in L1 between its passes, which read 16-byte vectors.
+//   2. walk_kernel, one CTA per session: the accept tests from the row statistics,
+//      then one pass for the total weight of the final draw and one scan for it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -44,6 +48,7 @@ struct SampArgs {
     float temperature, top_p, min_p;
     int top_k;
     int *j_out, *token_out, *keep_out, *status;
+    int vec;  // rows start 16-byte aligned and hold a whole number of 16-byte vectors
 };
 
 struct RowStats {
@@ -52,6 +57,7 @@ struct RowStats {
     float Z;   // kept mass
     int bad;   // the row holds a NaN or no finite maximum
 };
+static_assert(sizeof(RowStats) == 16, "row statistics are 16 bytes in scratch");
 
 struct Shared {
     float red[SNW];
@@ -131,6 +137,37 @@ __device__ __forceinline__ float e_of(float x, float m, float temperature)
     return expf(__fsub_rn(__fdiv_rn(x, temperature), m));
 }
 
+// f(v, x) for every element of the row; each thread takes whole 16-byte vectors
+// (8 bf16 or 4 f32 logits) in a fixed order where the row allows it.
+template <class F>
+__device__ __forceinline__ void for_row(const SampArgs &a, const void *row, F f)
+{
+    if (a.vec && a.bf16) {
+        const uint4 *r = static_cast<const uint4 *>(row);
+        for (int c = threadIdx.x; c < a.V / 8; c += SNT) {
+            const uint4 u = __ldg(r + c);
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                f(8 * c + 2 * m, __uint_as_float(w[m] << 16));
+                f(8 * c + 2 * m + 1, __uint_as_float(w[m] & 0xffff0000u));
+            }
+        }
+    } else if (a.vec) {
+        const float4 *r = static_cast<const float4 *>(row);
+        for (int c = threadIdx.x; c < a.V / 4; c += SNT) {
+            const float4 u = __ldg(r + c);
+            f(4 * c, u.x);
+            f(4 * c + 1, u.y);
+            f(4 * c + 2, u.z);
+            f(4 * c + 3, u.w);
+        }
+    } else {
+        for (int v = threadIdx.x; v < a.V; v += SNT)
+            f(v, load_x(row, a.bf16, v));
+    }
+}
+
 // The k-th largest logit of the row (k >= 1, k <= V), by four 8-bit radix passes.
 __device__ float kth_largest(Shared &sh, const SampArgs &a, const void *row, int k)
 {
@@ -145,11 +182,11 @@ __device__ float kth_largest(Shared &sh, const SampArgs &a, const void *row, int
             sh.hist[i] = 0;
         __syncthreads();
         const unsigned prefix = sh.prefix;
-        for (int v = threadIdx.x; v < a.V; v += SNT) {
-            const unsigned key = okey(load_x(row, a.bf16, v));
+        for_row(a, row, [&](int, float x) {
+            const unsigned key = okey(x);
             if ((key & mask) == prefix)
                 atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
-        }
+        });
         __syncthreads();
         if (threadIdx.x < 32) {  // warp 0: the bin holding the kk-th largest, from the top
             const int lane = threadIdx.x;
@@ -194,11 +231,11 @@ __device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int sl
 {
     float mx = -INFINITY;
     int nan = 0;
-    for (int v = threadIdx.x; v < a.V; v += SNT) {
-        const float z = __fdiv_rn(load_x(row, a.bf16, v), a.temperature);
+    for_row(a, row, [&](int, float x) {
+        const float z = __fdiv_rn(x, a.temperature);
         nan |= z != z;
         mx = fmaxf(mx, z);
-    }
+    });
     nan = block_or(sh, nan);
     const float m = block_max(sh, mx);
     if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
@@ -208,8 +245,7 @@ __device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int sl
         return;
     }
     float s = 0.f;
-    for (int v = threadIdx.x; v < a.V; v += SNT)
-        s = __fadd_rn(s, e_of(load_x(row, a.bf16, v), m, a.temperature));
+    for_row(a, row, [&](int, float x) { s = __fadd_rn(s, e_of(x, m, a.temperature)); });
     const float S = block_sum(sh, s);
     float th = 0.f;
     if (a.top_k > 0 && a.top_k < a.V) {
@@ -221,8 +257,7 @@ __device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int sl
             if (threadIdx.x == 0)
                 sh.ncand = 0;
             __syncthreads();
-            for (int v = threadIdx.x; v < a.V; v += SNT) {
-                const float x = load_x(row, a.bf16, v);
+            for_row(a, row, [&](int v, float x) {
                 if (x >= xk) {
                     const int at = atomicAdd(&sh.ncand, 1);
                     if (at < CAP) {
@@ -230,7 +265,7 @@ __device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int sl
                         sh.ci[at] = v;
                     }
                 }
-            }
+            });
             __syncthreads();
             const int n = sh.ncand;
             if (n > CAP) {
@@ -301,11 +336,11 @@ __device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int sl
     if (a.min_p > 0.f)
         th = fmaxf(th, a.min_p);
     float z = 0.f;
-    for (int v = threadIdx.x; v < a.V; v += SNT) {
-        const float e = e_of(load_x(row, a.bf16, v), m, a.temperature);
+    for_row(a, row, [&](int, float x) {
+        const float e = e_of(x, m, a.temperature);
         if (e >= th)
             z = __fadd_rn(z, e);
-    }
+    });
     const float Z = block_sum(sh, z);
     if (threadIdx.x == 0)
         sh.rs[slot] = RowStats{m, th, Z, 0};
@@ -318,43 +353,57 @@ __device__ __forceinline__ float prob(const RowStats &r, float x, float temperat
     return e >= r.th ? __fdiv_rn(e, r.Z) : 0.f;
 }
 
-__global__ void __launch_bounds__(SNT) sampled_accept_kernel(const SampArgs a)
+// Row ri of session b: target row ri (ri < T) or draft row ri - T.
+__global__ void __launch_bounds__(SNT) row_stats_kernel(const SampArgs a, RowStats *__restrict__ stats)
+{
+    __shared__ Shared sh;
+    const int nr = 2 * a.T - 1;
+    const int b = blockIdx.x / nr, ri = blockIdx.x % nr;
+    const int K = a.T - 1;
+    const size_t es = a.bf16 ? 2 : 4;
+    const unsigned char *row =
+        ri < a.T ? static_cast<const unsigned char *>(a.logits) + (static_cast<size_t>(b) * a.T + ri) * a.V * es
+                 : static_cast<const unsigned char *>(a.draft_logits) +
+                       (static_cast<size_t>(b) * K + (ri - a.T)) * a.V * es;
+    row_stats(sh, a, row, 0);
+    if (threadIdx.x == 0)
+        stats[blockIdx.x] = sh.rs[0];
+}
+
+__global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowStats *__restrict__ stats)
 {
     __shared__ Shared sh;
     const int b = blockIdx.x;
-    const int K = a.T - 1;
+    const int K = a.T - 1, nr = 2 * a.T - 1;
     const size_t es = a.bf16 ? 2 : 4;
+    const RowStats *st = stats + static_cast<size_t>(b) * nr;
     const unsigned char *P = static_cast<const unsigned char *>(a.logits) + static_cast<size_t>(b) * a.T * a.V * es;
     const unsigned char *Q = static_cast<const unsigned char *>(a.draft_logits) + static_cast<size_t>(b) * K * a.V * es;
-    int j = 0;
-    bool bad = false;
-    for (; j < K; ++j) {
-        const int x = a.drafts[static_cast<size_t>(b) * K + j];
-        row_stats(sh, a, P + static_cast<size_t>(j) * a.V * es, 0);
-        row_stats(sh, a, Q + static_cast<size_t>(j) * a.V * es, 1);
-        if (sh.rs[0].bad || sh.rs[1].bad) {
-            bad = true;
-            break;
-        }
-        if (threadIdx.x == 0) {
-            int acc = 0;
-            if (x >= 0 && x < a.V) {  // a draft id outside the vocabulary is rejected
-                const float p = prob(sh.rs[0], load_x(P + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
-                const float q = prob(sh.rs[1], load_x(Q + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
-                const double u = a.u_accept[static_cast<size_t>(b) * K + j];
-                acc = u * static_cast<double>(q) < static_cast<double>(p);
+    if (threadIdx.x == 0) {
+        int j = 0, bad = 0;
+        for (; j < K; ++j) {
+            const RowStats rp = st[j], rq = st[a.T + j];
+            if (rp.bad || rq.bad) {
+                bad = 1;
+                break;
             }
-            sh.flag = acc;
+            const int x = a.drafts[static_cast<size_t>(b) * K + j];
+            if (x < 0 || x >= a.V)  // a draft id outside the vocabulary is rejected
+                break;
+            const float p = prob(rp, load_x(P + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
+            const float q = prob(rq, load_x(Q + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
+            const double u = a.u_accept[static_cast<size_t>(b) * K + j];
+            if (!(u * static_cast<double>(q) < static_cast<double>(p)))
+                break;
         }
-        __syncthreads();
-        if (!sh.flag)
-            break;
+        if (!bad && j == K && st[K].bad)
+            bad = 1;
+        sh.kk = j;
+        sh.flag = bad;
     }
-    if (!bad && j == K) {
-        row_stats(sh, a, P + static_cast<size_t>(K) * a.V * es, 0);
-        bad = sh.rs[0].bad;
-    }
-    if (bad) {
+    __syncthreads();
+    const int j = sh.kk;
+    if (sh.flag) {
         if (threadIdx.x == 0) {
             a.j_out[b] = j;
             a.token_out[b] = -1;
@@ -369,15 +418,22 @@ __global__ void __launch_bounds__(SNT) sampled_accept_kernel(const SampArgs a)
     // zero everywhere), or p~_K
     const unsigned char *prow = P + static_cast<size_t>(j) * a.V * es;
     const unsigned char *qrow = j < K ? Q + static_cast<size_t>(j) * a.V * es : nullptr;
-    const RowStats rp = sh.rs[0], rq = sh.rs[1];
-    int use_resid = 0;
-    if (qrow) {
-        int any = 0;
-        for (int v = threadIdx.x; v < a.V; v += SNT)
-            any |= __fsub_rn(prob(rp, load_x(prow, a.bf16, v), a.temperature),
-                             prob(rq, load_x(qrow, a.bf16, v), a.temperature)) > 0.f;
-        use_resid = block_or(sh, any);
-    }
+    const RowStats rp = st[j];
+    const RowStats rq = j < K ? st[a.T + j] : RowStats{0.f, 0.f, 1.f, 0};
+    float wr = 0.f, wp = 0.f;
+    for_row(a, prow, [&](int v, float x) {
+        const float p = prob(rp, x, a.temperature);
+        wp = __fadd_rn(wp, p);
+        if (qrow) {
+            const float r = __fsub_rn(p, prob(rq, load_x(qrow, a.bf16, v), a.temperature));
+            wr = __fadd_rn(wr, r > 0.f ? r : 0.f);
+        }
+    });
+    const float Wr = block_sum(sh, wr);
+    const float Wp = block_sum(sh, wp);
+    const bool use_resid = qrow && Wr > 0.f;
+    const float W = use_resid ? Wr : Wp;
+    const float target = __fmul_rn(a.u_sample[b], W);
     auto weight = [&](int v) -> float {
         const float p = prob(rp, load_x(prow, a.bf16, v), a.temperature);
         if (!use_resid)
@@ -385,19 +441,21 @@ __global__ void __launch_bounds__(SNT) sampled_accept_kernel(const SampArgs a)
         const float r = __fsub_rn(p, prob(rq, load_x(qrow, a.bf16, v), a.temperature));
         return r > 0.f ? r : 0.f;
     };
-    float w = 0.f;
-    for (int v = threadIdx.x; v < a.V; v += SNT)
-        w = __fadd_rn(w, weight(v));
-    const float W = block_sum(sh, w);
-    const float target = __fmul_rn(a.u_sample[b], W);
-    // the first token whose running weight (index order, chunks of SNT) exceeds target
+    // the first token whose running weight (index order; chunks of SNT x 4 tokens, 4
+    // consecutive tokens per thread) exceeds target
+    constexpr int PER = 4;
     float base = 0.f;
     int token = -1, last = -1;
-    for (int c0 = 0; c0 < a.V && token < 0; c0 += SNT) {
-        const int v = c0 + threadIdx.x;
-        const float wv = v < a.V ? weight(v) : 0.f;
-        float incl = wv;
-        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int c0 = 0; c0 < a.V && token < 0; c0 += SNT * PER) {
+        const int v0 = c0 + PER * threadIdx.x;
+        float wv[PER], own = 0.f;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            wv[i] = v0 + i < a.V ? weight(v0 + i) : 0.f;
+            own = __fadd_rn(own, wv[i]);
+        }
+        float incl = own;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
             const float y = __shfl_up_sync(0xffffffffu, incl, off);
@@ -408,16 +466,23 @@ __global__ void __launch_bounds__(SNT) sampled_accept_kernel(const SampArgs a)
         if (lane == 31)
             sh.red[wid] = incl;
         __syncthreads();
-        float wbase = 0.f;
-        for (int i = 0; i < wid; ++i)
-            wbase = __fadd_rn(wbase, sh.red[i]);
-        float chunk = 0.f;
-        for (int i = 0; i < SNW; ++i)
+        float wbase = 0.f, chunk = 0.f;
+        for (int i = 0; i < SNW; ++i) {
+            if (i < wid)
+                wbase = __fadd_rn(wbase, sh.red[i]);
             chunk = __fadd_rn(chunk, sh.red[i]);
-        const float run = __fadd_rn(base, __fadd_rn(wbase, incl));
-        const int mine = (v < a.V && run > target) ? v : 0x7fffffff;
-        const int haswt = (v < a.V && wv > 0.f) ? v : -1;
-        // lowest crossing index and highest weighted index of the chunk
+        }
+        const float excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
+        float run = __fadd_rn(base, __fadd_rn(wbase, lane ? excl_w : 0.f));
+        int mine = 0x7fffffff, haswt = -1;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            run = __fadd_rn(run, wv[i]);
+            if (v0 + i < a.V && run > target && mine == 0x7fffffff)
+                mine = v0 + i;
+            if (v0 + i < a.V && wv[i] > 0.f)
+                haswt = v0 + i;
+        }
         int lo = mine, hi = haswt;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) {
@@ -456,10 +521,17 @@ __global__ void __launch_bounds__(SNT) sampled_accept_kernel(const SampArgs a)
 
 using namespace kda;
 
+extern "C" size_t spec_accept_sampled_scratch_bytes(int B, int T)
+{
+    if (B <= 0 || T <= 0)
+        return 0;
+    return static_cast<size_t>(B) * (2 * T - 1) * sizeof(RowStats);
+}
+
 extern "C" int spec_accept_sampled(const void *logits, const void *draft_logits, int logit_dtype, int B, int T,
                                    int V, const int *drafts, const float *u_accept, const float *u_sample,
                                    const kda_sampling *sp, int *j_out, int *token_out, int *keep_out,
-                                   int *dev_status, cudaStream_t stream)
+                                   int *dev_status, void *scratch, size_t scratch_bytes, cudaStream_t stream)
 {
     if (B < 0)
         return fail(KDA_EINVAL, "B must be >= 0");
@@ -489,6 +561,12 @@ extern "C" int spec_accept_sampled(const void *logits, const void *draft_logits,
     const uintptr_t al = logit_dtype == KDA_BF16 ? 1u : 3u;
     if ((reinterpret_cast<uintptr_t>(logits) & al) || (reinterpret_cast<uintptr_t>(draft_logits) & al))
         return fail(KDA_EINVAL, "logits must be aligned to their element type");
+    const size_t need = spec_accept_sampled_scratch_bytes(B, T);
+    if (!scratch || scratch_bytes < need || !aligned16(scratch))
+        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " + std::to_string(need) +
+                                    " bytes");
+    if (static_cast<long long>(B) * (2 * T - 1) > 0x7fffffffLL)
+        return fail(KDA_EINVAL, "B*(2T-1) exceeds the grid limit");
     SampArgs a{};
     a.logits = logits;
     a.draft_logits = draft_logits;
@@ -507,6 +585,13 @@ extern "C" int spec_accept_sampled(const void *logits, const void *draft_logits,
     a.token_out = token_out;
     a.keep_out = keep_out;
     a.status = dev_status;
-    sampled_accept_kernel<<<B, SNT, 0, stream>>>(a);
-    return check_launch("sampled_accept_kernel");
+    const size_t row_bytes = static_cast<size_t>(V) * (a.bf16 ? 2 : 4);
+    a.vec = aligned16(logits) && (T == 1 || aligned16(draft_logits)) && row_bytes % 16 == 0;
+    RowStats *stats = static_cast<RowStats *>(scratch);
+    row_stats_kernel<<<static_cast<unsigned>(B * (2 * T - 1)), SNT, 0, stream>>>(a, stats);
+    int rc = check_launch("row_stats_kernel");
+    if (rc)
+        return rc;
+    walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
+    return check_launch("walk_kernel");
 }

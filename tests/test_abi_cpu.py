@@ -175,7 +175,7 @@ def test_window_and_accept_var_reject_on_host(L):
 def test_sampled_accept_rejects_bad_parameters(L, sp):
     s = kb.KdaSampling(*sp)
     rc = L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, ctypes.byref(s), FAKE, FAKE, None,
-                               None, None)
+                               None, FAKE, 1 << 20, None)
     assert rc == kb.EINVAL and L.kda_last_error()
 
 
@@ -183,9 +183,13 @@ def test_sampled_accept_rejects_bad_shapes_and_pointers(L):
     s = kb.KdaSampling(1.0, 50, 0.9, 0.0)
     call = lambda **k: L.spec_accept_sampled(k.get("lg", FAKE), FAKE, k.get("dt", kb.BF16), k.get("B", 2),
                                              k.get("T", 8), k.get("V", 1000), FAKE, FAKE, k.get("us", FAKE),
-                                             ctypes.byref(s), FAKE, FAKE, None, None, None)
+                                             ctypes.byref(s), FAKE, FAKE, None, None, k.get("scr", FAKE),
+                                             k.get("nb", 1 << 20), None)
     assert call(T=0) == kb.EINVAL and call(T=16) == kb.EINVAL and call(V=0) == kb.EINVAL
     assert call(dt=9) == kb.EINVAL and call(us=None) == kb.EINVAL and call(lg=FAKE + 1) == kb.EINVAL
+    assert call(scr=None) == kb.EINVAL and call(scr=FAKE + 8) == kb.EINVAL
+    assert L.spec_accept_sampled_scratch_bytes(2, 8) == 2 * 15 * 16
+    assert call(nb=2 * 15 * 16 - 1) == kb.EINVAL
     assert call(B=0) == kb.OK
     assert L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None,
-                                 None) == kb.EINVAL
+                                 FAKE, 1 << 20, None) == kb.EINVAL
