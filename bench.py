@@ -402,6 +402,49 @@ def run_gpu(args, rank, world, local_rank):
         res["per_layer"] = {"launches_per_step": w.L + 3, "steps": Kp, "eager_ms_per_step": eager_ms,
                             "graph_ms_per_step": graph_ms,
                             "graph_rows_per_s": world * w.B * w.T / (graph_ms * 1e-3)}
+    # column-stash rollback (the alternative to snapshot + replay): the verify also
+    # writes the state and ring after every row, the rollback copies the kept column
+    col_bytes = w.L * w.B * w.H * w.T * (128 * 128 + 9 * 128) * 4
+    if not args.no_cols and col_bytes <= 16e9:
+        cols = kb.ColStash(st, w.T)
+        Kc = max(1, min(args.cols_steps, K))
+        evc = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kc + 3)]
+
+        def col_step(i, ev):
+            r = i % R
+            rr = rows[r]
+            ev[0].record(stream)
+            kb.kda_verify_scan_cols(st, rr["q"], rr["k"], rr["v"], rr["g"], rr["beta"], cols, out=out, stream=stream)
+            ev[1].record(stream)
+            plans[r].accept()
+            ev[2].record(stream)
+            kb.kda_rollback_cols(st, cols, keep_out, dev_status=status, stream=stream)
+            ev[3].record(stream)
+
+        for i in range(3):
+            col_step(i, evc[Kc + i])
+        barrier()
+        for i in range(Kc):
+            col_step(i, evc[i])
+        barrier()
+        if int(status.item()):
+            raise RuntimeError(f"device status {int(status.item()):#x} after the column-stash steps")
+        cv = sum(e[0].elapsed_time(e[1]) for e in evc[:Kc]) / Kc
+        cr = sum(e[2].elapsed_time(e[3]) for e in evc[:Kc]) / Kc
+        cs = sum(e[0].elapsed_time(e[3]) for e in evc[:Kc]) / Kc
+        es = 2 if w.bf16 else 4
+        per_head = (2 + w.T) * 128 * 128 * 4 + (2 + w.T) * 9 * 128 * 4
+        cvb = w.L * w.B * (w.H * per_head + w.T * w.H * (4 * 128 + 1) * es + w.T * w.H * 128 * 4) + \
+            w.L * w.H * 3 * 128 * 4 * 4
+        keeps = [[j + 1 for j in jt[i % R]] for i in range(Kc)]
+        crb = sum(w.L * w.H * sum(1 for k in ks if k < w.T) * 2 * (128 * 128 + 9 * 128) * 4 for ks in keeps) / Kc
+        res["col_stash"] = {"stash_bytes": col_bytes, "steps": Kc, "verify_ms": cv, "rollback_ms": cr,
+                            "round_ms": cs, "verify_bytes": cvb, "rollback_bytes_mean": crb,
+                            "verify_gbs": cvb / (cv * 1e-3) / 1e9,
+                            "snapshot_replay": {"verify_ms": res["verify_ms"], "rollback_ms": res["rollback_ms"],
+                                                "round_ms": res["ms_per_step"],
+                                                "stash_bytes": w.L * w.B * w.H * (128 * 128 + 9 * 128) * 4}}
+
     # sampled acceptance: the rejection walk with filtered target and draft rows; the
     # draft rows equal the target rows, so every draft is accepted (the longest walk)
     if not args.no_sampled:
@@ -491,6 +534,8 @@ def main():
     ap.add_argument("--per-layer-steps", type=int, default=200)
     ap.add_argument("--no-var-t", action="store_true", help="skip the variable-T rounds")
     ap.add_argument("--no-sampled", action="store_true", help="skip the sampled-accept timing")
+    ap.add_argument("--no-cols", action="store_true", help="skip the column-stash rounds")
+    ap.add_argument("--cols-steps", type=int, default=200)
     ap.add_argument("--sampled-steps", type=int, default=200)
     ap.add_argument("--var-t-steps", type=int, default=200)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
@@ -571,6 +616,7 @@ def main():
         "per_layer": res.get("per_layer"),
         "var_t": res.get("var_t"),
         "sampled_accept": res.get("sampled_accept"),
+        "col_stash": res.get("col_stash"),
     }
     print(json.dumps(line))
 

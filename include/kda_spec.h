@@ -184,6 +184,28 @@ int kda_rollback_var(const kda_dims *dims, const kda_layer_state *st, const kda_
                      const int *t_rows, const int *keep, int mem, int *dev_status, cudaStream_t stream);
 
 /*
+ * Column-stash rollback, the alternative the pages weigh against snapshot + replay
+ * (glm_spec.rs module doc, ROLLBACK: vLLM keeps num_spec + 1 KDA state columns and
+ * commits the last accepted one; the pages keep the snapshot + replay, since the
+ * columns cost 136 MiB per column per round).  Offered to measure that trade.
+ *
+ * kda_verify_scan_cols -- kda_verify_scan that also writes the state and conv ring
+ *   after every row:
+ *     state_cols f32 [L][B][H][T][dk][dv], ring_cols f32 [L][B][H][T][3][3][dk],
+ *   caller-owned device memory, 16-byte aligned.  No snapshot is taken.  State, ring
+ *   and outputs are bit-identical to kda_verify_scan; column t is bit-identical to the
+ *   state (ring) a verify of rows 0..t leaves.
+ * kda_rollback_cols -- commit keep[b] rows (1..T) of that round: for keep < T, state
+ *   <- state_cols[keep-1] and conv_ring <- ring_cols[keep-1] (a copy, no replay);
+ *   bit-identical to kda_rollback of a snapshot round.  keep as for kda_rollback.
+ */
+int kda_verify_scan_cols(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows, int T,
+                         float *out, float *state_cols, float *ring_cols, cudaStream_t stream);
+int kda_rollback_cols(const kda_dims *dims, const kda_layer_state *st, const float *state_cols,
+                      const float *ring_cols, int T, const int *keep, int keep_mem, int *dev_status,
+                      cudaStream_t stream);
+
+/*
  * spec_accept_var -- spec_accept where session b's round has t_rows[b] rows
  *   (device int32 [B]).  logits stay [B][T][V] and drafts [B][T-1]; session b reads
  *   logits rows 0..t_rows[b]-1 and drafts 0..t_rows[b]-2: j = the first r <

@@ -27,7 +27,8 @@ F32, BF16 = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
-EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "spec_accept_var",
+EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_cols",
+           "kda_rollback_cols", "spec_accept_var",
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
 ABI_VERSION = 2
@@ -90,6 +91,12 @@ def lib(path: str | None = None):
     L.kda_rollback_var.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                    ctypes.POINTER(KdaStashC), vp, vp, ci, vp, vp]
     L.kda_rollback_var.restype = ci
+    L.kda_verify_scan_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                       ctypes.POINTER(KdaRows), ci, vp, vp, vp, vp]
+    L.kda_verify_scan_cols.restype = ci
+    L.kda_rollback_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState), vp, vp, ci, vp, ci, vp,
+                                    vp]
+    L.kda_rollback_cols.restype = ci
     L.spec_accept_var.argtypes = [vp, ci, ci, ci, ci, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.spec_accept_var.restype = ci
     L.spec_window.argtypes = [vp, ci, ci, ci, ctypes.c_float, ci, ci, vp, vp]
@@ -301,6 +308,43 @@ def kda_rollback_var(st: LayerState, stash: Stash, t_rows, keep, dev_status: tor
                                 _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
     del h1, h2
     _check("kda_rollback_var", rc)
+
+
+class ColStash:
+    """The state and conv ring after every row of one round (column-stash rollback)."""
+
+    def __init__(self, st: LayerState, T: int):
+        dev = st.state.device
+        self.T = int(T)
+        self.state_cols = torch.empty((st.L, st.B, st.H, self.T, D, D), dtype=torch.float32, device=dev)
+        self.ring_cols = torch.empty((st.L, st.B, st.H, self.T, 3, 3, D), dtype=torch.float32, device=dev)
+
+
+def kda_verify_scan_cols(st: LayerState, q, k, v, g, beta, cols: ColStash, out: torch.Tensor | None = None,
+                         stream=None) -> ColStash:
+    """Verify round that also stashes the state and ring after every row."""
+    rows, tensors, dt, T = _rows(st, q, k, v, g, beta)
+    if T != cols.T:
+        raise ValueError(f"the column stash holds {cols.T} rows, the round has {T}")
+    if out is not None:
+        _dev(out, "out", torch.float32, (st.L, st.B, T, st.H, D))
+    dims, cst = st.dims(dt), st.c()
+    rc = lib().kda_verify_scan_cols(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(rows), T, _ptr(out),
+                                    _ptr(cols.state_cols), _ptr(cols.ring_cols), ctypes.c_void_p(_stream(stream)))
+    _check("kda_verify_scan_cols", rc)
+    cols.dtype = dt
+    return cols
+
+
+def kda_rollback_cols(st: LayerState, cols: ColStash, keep, dev_status: torch.Tensor | None = None,
+                      stream=None) -> None:
+    """Commit keep[b] rows of a column-stash round by copying the kept column."""
+    kp, mem, hold = _int_array(keep, st.B, "keep")
+    dims, cst = st.dims(getattr(cols, "dtype", BF16)), st.c()
+    rc = lib().kda_rollback_cols(ctypes.byref(dims), ctypes.byref(cst), _ptr(cols.state_cols), _ptr(cols.ring_cols),
+                                 cols.T, kp, mem, _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+    del hold
+    _check("kda_rollback_cols", rc)
 
 
 def spec_accept_var(logits: torch.Tensor, drafts: torch.Tensor, t_rows: torch.Tensor, j_out=None, bonus_out=None,

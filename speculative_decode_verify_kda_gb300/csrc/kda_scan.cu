@@ -99,6 +99,8 @@ struct ScanParams {
     const float *conv_w;   // [L][H][3][D][4]
     const void *xq, *xk, *xv, *xg, *xb;  // [L][B][T_rows][H][D], xb [L][B][T_rows][H]
     float *out;            // nullable: [L][B][T_rows][H][D]
+    float *s_cols;         // nullable: [L][B][H][T_rows][D][D], the state after each row
+    float *ring_cols;      // with s_cols: [L][B][H][T_rows][3][3][D], the ring after each row
     const int *keep_dev;   // KEEP_DEVICE: [B]
     const int *rows_dev;   // ROWS_DEVICE, or KEEP_DEVICE after a per-session round: [B] row counts
     int *status;           // nullable device status word
@@ -541,6 +543,14 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
                 x0 = x1;
                 x1 = x2;
                 x2 = x3;
+                if (p.ring_cols) {  // the ring after row t0 + j
+                    float4 *rc = reinterpret_cast<float4 *>(
+                                     p.ring_cols + ((static_cast<size_t>(u) * p.T_rows + t0 + j) * 3 + pw) * 3 * D) +
+                                 lane;
+                    rc[0] = x0;
+                    rc[D / 4] = x1;
+                    rc[2 * D / 4] = x2;
+                }
             } else {
                 y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
@@ -638,6 +648,17 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
 }
 
 // ---- scan warps ---------------------------------------------------------------------
+// A thread's register tile to a [128][128] state at So (already offset by its columns).
+__device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[8][4])
+{
+#pragma unroll
+    for (int rp = 0; rp < 8; ++rp) {
+        const int i = rg + 16 * rp;
+        *reinterpret_cast<float4 *>(So + i * D) = make_float4(S[rp][0].x, S[rp][1].x, S[rp][2].x, S[rp][3].x);
+        *reinterpret_cast<float4 *>(So + (i + 8) * D) = make_float4(S[rp][0].y, S[rp][1].y, S[rp][2].y, S[rp][3].y);
+    }
+}
+
 __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     // lane 4 rg + cg of warp wi holds key rows i = rg + 8 r (r < 16) of value columns
@@ -751,21 +772,13 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
                     S[rp][c4] = __ffma2_rn(kk[rp], wc[c4], S[rp][c4]);
+            if (p.s_cols)  // the column stash: the state after row t
+                store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
         }
         mbar_arrive(c.bar(B_SI_EMPTY + s));
 
         // ---- state write-back -----------------------------------------------------------
-        {
-            float *So = p.s_out + static_cast<size_t>(u) * D * D + jbase;
-#pragma unroll
-            for (int rp = 0; rp < 8; ++rp) {
-                const int i = rg + 16 * rp;
-                *reinterpret_cast<float4 *>(So + i * D) =
-                    make_float4(S[rp][0].x, S[rp][1].x, S[rp][2].x, S[rp][3].x);
-                *reinterpret_cast<float4 *>(So + (i + 8) * D) =
-                    make_float4(S[rp][0].y, S[rp][1].y, S[rp][2].y, S[rp][3].y);
-            }
-        }
+        store_tile(p.s_out + static_cast<size_t>(u) * D * D + jbase, rg, S);
         u = next_live(p, u + gridDim.x, n, false);
     }
 }
@@ -1121,4 +1134,125 @@ extern "C" int kda_rollback_var(const kda_dims *dims, const kda_layer_state *st,
     if (!t_rows && dims && static_cast<long long>(dims->L) * dims->B * dims->H > 0)
         return fail(KDA_EINVAL, "t_rows must not be NULL");
     return rollback_common(dims, st, stash, t_rows, keep, mem, dev_status, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Column-stash rollback (the alternative the pages weigh against snapshot + replay:
+// vLLM keeps num_spec + 1 state columns and commits the accepted one).  The verify
+// writes the state and conv ring after every row; rollback copies the kept column.
+// ---------------------------------------------------------------------------
+namespace kda {
+namespace {
+
+// One CTA per unit: state <- state_cols[keep-1], ring <- ring_cols[keep-1] for the
+// units of sessions that keep fewer than all rows.
+__global__ void __launch_bounds__(256) commit_cols_kernel(const __grid_constant__ ScanParams p)
+{
+    const int n = p.L * p.B * p.H;
+    for (int u = blockIdx.x; u < n; u += gridDim.x) {
+        const int kp = unit_rows(p, (u / p.H) % p.B);
+        if (kp < 0 && p.status && threadIdx.x == 0)
+            atomicOr(p.status, KDA_ST_BADKEEP);
+        if (kp <= 0)
+            continue;
+        const float4 *src = reinterpret_cast<const float4 *>(p.s_cols + (static_cast<size_t>(u) * p.T_rows + kp - 1) * D * D);
+        float4 *dst = reinterpret_cast<float4 *>(p.s_out + static_cast<size_t>(u) * D * D);
+        for (int i = threadIdx.x; i < D * D / 4; i += blockDim.x)
+            dst[i] = src[i];
+        const float4 *rsrc =
+            reinterpret_cast<const float4 *>(p.ring_cols + (static_cast<size_t>(u) * p.T_rows + kp - 1) * 9 * D);
+        float4 *rdst = reinterpret_cast<float4 *>(p.ring_out + static_cast<size_t>(u) * 9 * D);
+        for (int i = threadIdx.x; i < 9 * D / 4; i += blockDim.x)
+            rdst[i] = rsrc[i];
+    }
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_verify_scan_cols(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows, int T,
+                                    float *out, float *state_cols, float *ring_cols, cudaStream_t stream)
+{
+    int rc = check_common(dims, st);
+    if (rc)
+        return rc;
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15 (K <= 14 drafts per round), got " + std::to_string(T));
+    if (static_cast<long long>(dims->L) * dims->B * dims->H == 0)
+        return ok();
+    if ((rc = check_rows(rows, dims->dtype)))
+        return rc;
+    if (out && (reinterpret_cast<uintptr_t>(out) & 3u))
+        return fail(KDA_EINVAL, "out must be 4-byte aligned");
+    if (!state_cols || !ring_cols || !aligned16(state_cols) || !aligned16(ring_cols))
+        return fail(KDA_EINVAL, "state_cols and ring_cols must be 16-byte aligned device memory");
+    ScanParams p{};
+    p.keep_mode = KEEP_NONE;
+    p.s_out = st->state;
+    p.ring_in = st->conv_ring;
+    p.ring_out = st->conv_ring;
+    p.conv_w = st->conv_w;
+    p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
+    p.out = out;
+    p.s_cols = state_cols;
+    p.ring_cols = ring_cols;
+    p.L = dims->L; p.B = dims->B; p.H = dims->H;
+    p.T_rows = T;
+    p.T_run = T;
+    p.tcap = T;
+    p.bf16 = dims->dtype == KDA_BF16;
+    return launch_scan(p, st->state, stream);
+}
+
+extern "C" int kda_rollback_cols(const kda_dims *dims, const kda_layer_state *st, const float *state_cols,
+                                 const float *ring_cols, int T, const int *keep, int keep_mem, int *dev_status,
+                                 cudaStream_t stream)
+{
+    int rc = check_common(dims, st);
+    if (rc)
+        return rc;
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
+    const long long units = static_cast<long long>(dims->L) * dims->B * dims->H;
+    if (units == 0)
+        return ok();
+    if (!state_cols || !ring_cols || !aligned16(state_cols) || !aligned16(ring_cols))
+        return fail(KDA_EINVAL, "state_cols and ring_cols must be 16-byte aligned device memory");
+    if (!keep)
+        return fail(KDA_EINVAL, "keep must not be NULL");
+    ScanParams p{};
+    if (keep_mem == KDA_MEM_HOST) {
+        if (dims->B > KDA_HOST_KEEP_MAX)
+            return fail(KDA_EINVAL, "B exceeds KDA_HOST_KEEP_MAX for a host keep array; pass keep on the device");
+        bool any = false;
+        for (int b = 0; b < dims->B; ++b) {
+            if (keep[b] < 1 || keep[b] > T)
+                return fail(KDA_EINVAL, "keep[" + std::to_string(b) + "] = " + std::to_string(keep[b]) +
+                                            " outside 1.." + std::to_string(T));
+            p.keep_host[b] = static_cast<unsigned char>(keep[b]);
+            any |= keep[b] < T;
+        }
+        if (!any)
+            return ok();
+        p.keep_mode = KEEP_HOST;
+    } else if (keep_mem == KDA_MEM_DEVICE) {
+        if (reinterpret_cast<uintptr_t>(keep) & 3u)
+            return fail(KDA_EINVAL, "device keep must be 4-byte aligned");
+        p.keep_mode = KEEP_DEVICE;
+        p.keep_dev = keep;
+    } else {
+        return fail(KDA_EINVAL, "keep_mem must be KDA_MEM_HOST or KDA_MEM_DEVICE");
+    }
+    p.s_out = st->state;
+    p.ring_out = st->conv_ring;
+    p.s_cols = const_cast<float *>(state_cols);
+    p.ring_cols = const_cast<float *>(ring_cols);
+    p.status = dev_status;
+    p.L = dims->L; p.B = dims->B; p.H = dims->H;
+    p.T_rows = T;
+    p.T_run = T;
+    p.bf16 = dims->dtype == KDA_BF16;
+    const long long grid = std::min<long long>(units, 152LL * 8);
+    commit_cols_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
+    return check_launch("commit_cols_kernel");
 }

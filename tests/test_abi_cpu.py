@@ -193,3 +193,19 @@ def test_sampled_accept_rejects_bad_shapes_and_pointers(L):
     assert call(B=0) == kb.OK
     assert L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None,
                                  FAKE, 1 << 20, None) == kb.EINVAL
+
+
+def test_cols_entry_points_reject_on_host(L):
+    dims, st, rows = _state(B=2)
+    assert L.kda_verify_scan_cols(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), 8, None, None, FAKE,
+                                  None) == kb.EINVAL
+    assert L.kda_verify_scan_cols(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), 8, None, FAKE + 4, FAKE,
+                                  None) == kb.EINVAL
+    assert L.kda_verify_scan_cols(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), 16, None, FAKE, FAKE,
+                                  None) == kb.EINVAL
+    keep = (ctypes.c_int * 2)(3, 9)
+    assert L.kda_rollback_cols(ctypes.byref(dims), ctypes.byref(st), FAKE, FAKE, 8, ctypes.cast(keep, ctypes.c_void_p),
+                               kb.MEM_HOST, None, None) == kb.EINVAL
+    full = (ctypes.c_int * 2)(8, 8)
+    assert L.kda_rollback_cols(ctypes.byref(dims), ctypes.byref(st), FAKE, FAKE, 8, ctypes.cast(full, ctypes.c_void_p),
+                               kb.MEM_HOST, None, None) == kb.OK
