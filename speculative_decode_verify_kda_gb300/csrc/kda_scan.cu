@@ -286,30 +286,27 @@ struct Unit {
     long long lb;  // l * B + b
 };
 
-// rows unit u runs: > 0 to run, 0 nothing to do, -1 an invalid device keep or row count
+// rows unit u runs: > 0 to run, 0 nothing to do, -1 an invalid device keep or row
+// count.  The plain verify comes first: this runs for every unit in every warp.
 __device__ __forceinline__ int unit_rows(const ScanParams &p, int b)
 {
-    switch (p.keep_mode) {
-    case KEEP_HOST: {
+    if (p.keep_mode == KEEP_NONE)
+        return p.T_run;
+    if (p.keep_mode == KEEP_HOST) {
         const int kp = p.keep_host[b];  // validated on the host; T_rows where nothing is to do
         return kp >= p.T_rows ? 0 : kp;
     }
-    case KEEP_DEVICE: {
+    if (p.keep_mode == KEEP_DEVICE) {
         const int kp = p.keep_dev[b];
         const int tb = p.rows_dev ? p.rows_dev[b] : p.T_rows;  // the session's rows in the round
         if (tb < 1 || tb > p.T_rows || kp < 1 || kp > tb)
             return -1;
         return kp == tb ? 0 : kp;
     }
-    case ROWS_HOST:
+    if (p.keep_mode == ROWS_HOST)
         return p.keep_host[b];  // validated 1..T_rows on the host
-    case ROWS_DEVICE: {
-        const int tb = p.rows_dev[b];
-        return tb < 1 || tb > p.T_rows ? -1 : tb;
-    }
-    default:
-        return p.T_run;
-    }
+    const int tb = p.rows_dev[b];  // ROWS_DEVICE
+    return tb < 1 || tb > p.T_rows ? -1 : tb;
 }
 
 __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
@@ -517,6 +514,7 @@ __device__ __forceinline__ void store_perm(float *row, int block, int lane, floa
 // Stream pw (0 q, 1 k, 2 v) of one unit: the conv window slides along the rows in
 // registers.  Writes the scan inputs (q-hat, k-hat or v), the ring after the round
 // and, when snapshotting, the ring before it.
+template <bool COLS>
 __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsigned char *stg, float *si,
                             const Pre &pr, int u, int T, int pw, int lane)
 {
@@ -543,7 +541,7 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
                 x0 = x1;
                 x1 = x2;
                 x2 = x3;
-                if (p.ring_cols) {  // the ring after row t0 + j
+                if (COLS) {  // the ring after row t0 + j
                     float4 *rc = reinterpret_cast<float4 *>(
                                      p.ring_cols + ((static_cast<size_t>(u) * p.T_rows + t0 + j) * 3 + pw) * 3 * D) +
                                  lane;
@@ -602,6 +600,7 @@ __device__ void gate_stream(const Layout &lay, const unsigned char *stg, float *
         sc[2 * lane] = sigmoidf_(pr.beta);
 }
 
+template <bool COLS>
 __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     const int pw = (threadIdx.x >> 5) - NSCAN, lane = threadIdx.x & 31;
@@ -622,7 +621,7 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
         float *si = reinterpret_cast<float *>(sm + lay.si(b));
         float *sc = reinterpret_cast<float *>(sm + lay.sc(b));
         if (pw < 3)
-            conv_stream(p, lay, stg, si, pr, u, T, pw, lane);
+            conv_stream<COLS>(p, lay, stg, si, pr, u, T, pw, lane);
         else
             gate_stream(lay, stg, si, sc, pr, T, lane);
         mbar_arrive(c.bar(B_STG_EMPTY + sb));
@@ -659,6 +658,7 @@ __device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[
     }
 }
 
+template <bool COLS>
 __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     // lane 4 rg + cg of warp wi holds key rows i = rg + 8 r (r < 16) of value columns
@@ -772,7 +772,7 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4)
                     S[rp][c4] = __ffma2_rn(kk[rp], wc[c4], S[rp][c4]);
-            if (p.s_cols)  // the column stash: the state after row t
+            if (COLS)  // the column stash: the state after row t
                 store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
         }
         mbar_arrive(c.bar(B_SI_EMPTY + s));
@@ -784,6 +784,8 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
 }
 
 // One persistent CTA per SM; warps 0..7 scan, 8..11 run the prologue, 12 copies.
+// COLS: also write the column stash (the state and ring after every row).
+template <bool COLS>
 __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__ ScanParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -809,9 +811,9 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     const int n = p.L * p.B * p.H;  // below 2^31 / 128, checked at launch
     const int wi = threadIdx.x >> 5;
     if (wi < NSCAN)
-        scan_warp(p, lay, sm, c, n);
+        scan_warp<COLS>(p, lay, sm, c, n);
     else if (wi < WCOPY)
-        prologue_warp(p, lay, sm, c, n);
+        prologue_warp<COLS>(p, lay, sm, c, n);
     else
         copy_warp(p, lay, sm, c, n);
 }
@@ -898,7 +900,9 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
         const size_t most = Layout{KDA_TMAX, 4, 1}.total();
         if (static_cast<size_t>(optin) < most)
             return fail(KDA_ECUDA, "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
-        e = cudaFuncSetAttribute(kda_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncSetAttribute(kda_scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kda_scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
         if (e != cudaSuccess)
             return fail(KDA_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
         di.smem_max = optin;
@@ -913,7 +917,10 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
     if (p.s_snap && (rc = state_map(&p.tm_snap, p.s_snap, units)))
         return rc;
     const long long grid = std::min<long long>(units, di.sms);
-    kda_scan_kernel<<<static_cast<unsigned>(grid), NT, lay.total(), stream>>>(p);
+    if (p.s_cols)
+        kda_scan_kernel<true><<<static_cast<unsigned>(grid), NT, lay.total(), stream>>>(p);
+    else
+        kda_scan_kernel<false><<<static_cast<unsigned>(grid), NT, lay.total(), stream>>>(p);
     return check_launch("kda_scan_kernel");
 }
 
