@@ -316,3 +316,24 @@ def test_stress_full_size_one_round(orc):
         assert_close(host(out[l, b]), o, f"stress unit {l},{b} out")
         assert_close(host(st.state[l, b]), st_k, f"stress unit {l},{b} state")
         assert np.array_equal(host(st.conv_ring[l, b]), ring_k)
+
+
+@pytest.mark.parametrize("name", ["tiny", "layer64"])
+def test_state_does_not_depend_on_asking_for_outputs(name):
+    """A verify that writes output rows and one that does not (the replay path) leave the
+    same state and ring bits; so do rollbacks after each."""
+    w = synth.WORKLOADS[name]
+    state0, ring0, cw = small_case(w)
+    rows = rows_to_dev(synth.all_rows(w, 0), w.bf16)
+    a = layer_state(state0, ring0, cw)
+    b = layer_state(state0, ring0, cw)
+    sa, sb = kb.Stash(a), kb.Stash(b)
+    out = torch.empty((1, 1, w.T, w.H, 128), dtype=torch.float32, device="cuda")
+    kb.kda_verify_scan(a, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"], out=out, stash=sa)
+    kb.kda_verify_scan(b, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"], stash=sb)
+    torch.cuda.synchronize()
+    assert bits_equal(a.state, b.state) and bits_equal(a.conv_ring, b.conv_ring)
+    kb.kda_rollback(a, sa, [3])
+    kb.kda_rollback(b, sb, [3])
+    torch.cuda.synchronize()
+    assert bits_equal(a.state, b.state) and bits_equal(a.conv_ring, b.conv_ring)
