@@ -658,10 +658,7 @@ __device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[
     }
 }
 
-// OUT: the round writes outputs.  Without them (a rollback replay, or a verify that
-// asks for none) the e = S'^T q sweep is skipped; u and the state take the same
-// operations either way, so both instantiations leave the same state bits.
-template <bool COLS, bool OUT>
+template <bool COLS>
 __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     // lane 4 rg + cg of warp wi holds key rows i = rg + 8 r (r < 16) of value columns
@@ -717,7 +714,7 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             for (int rq = 0; rq < 4; ++rq) {
                 const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
                 const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
-                const float4 q4 = OUT ? *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
                 const float2 dA = make_float2(d4.x, d4.y), dB = make_float2(d4.z, d4.w);
                 const float2 qA = make_float2(q4.x, q4.y), qB = make_float2(q4.z, q4.w);
                 kk[2 * rq] = make_float2(k4.x, k4.y);
@@ -726,15 +723,13 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
                 for (int c4 = 0; c4 < 4; ++c4) {
                     S[2 * rq][c4] = __fmul2_rn(S[2 * rq][c4], dA);
                     uacc[c4] = __ffma2_rn(S[2 * rq][c4], kk[2 * rq], uacc[c4]);
-                    if (OUT)
-                        eacc[c4] = __ffma2_rn(S[2 * rq][c4], qA, eacc[c4]);
+                    eacc[c4] = __ffma2_rn(S[2 * rq][c4], qA, eacc[c4]);
                 }
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
                     S[2 * rq + 1][c4] = __fmul2_rn(S[2 * rq + 1][c4], dB);
                     uacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], kk[2 * rq + 1], uacc[c4]);
-                    if (OUT)
-                        eacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], qB, eacc[c4]);
+                    eacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], qB, eacc[c4]);
                 }
             }
             // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
@@ -762,7 +757,7 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             const float2 bk = *reinterpret_cast<const float2 *>(sc + 2 * t);  // {beta, k.q}
             const float w = __fmul_rn(bk.x, __fsub_rn(vt[SI_V + jsum], sum));
             const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
-            if (OUT && b2)
+            if (outp && b2)
                 outp[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
             // every lane gathers w of its 4 columns from the u lanes 4 c + cg
             float2 wc[4];
@@ -789,9 +784,10 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
 }
 
 // One persistent CTA per SM; warps 0..7 scan, 8..11 run the prologue, 12 copies.
-// COLS: also write the column stash (the state and ring after every row).  OUT: the
-// round writes output rows (p.out is not NULL).
-template <bool COLS, bool OUT>
+// COLS: also write the column stash (the state and ring after every row).  Verify and
+// rollback share one instantiation: alternating between two kernels of this size cost
+// the verify 5 % (its code is fetched again after each switch).
+template <bool COLS>
 __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__ ScanParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -817,7 +813,7 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     const int n = p.L * p.B * p.H;  // below 2^31 / 128, checked at launch
     const int wi = threadIdx.x >> 5;
     if (wi < NSCAN)
-        scan_warp<COLS, OUT>(p, lay, sm, c, n);
+        scan_warp<COLS>(p, lay, sm, c, n);
     else if (wi < WCOPY)
         prologue_warp<COLS>(p, lay, sm, c, n);
     else
@@ -906,10 +902,8 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
         const size_t most = Layout{KDA_TMAX, 4, 1}.total();
         if (static_cast<size_t>(optin) < most)
             return fail(KDA_ECUDA, "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
-        const void *kernels[4] = {reinterpret_cast<const void *>(kda_scan_kernel<false, false>),
-                                  reinterpret_cast<const void *>(kda_scan_kernel<false, true>),
-                                  reinterpret_cast<const void *>(kda_scan_kernel<true, false>),
-                                  reinterpret_cast<const void *>(kda_scan_kernel<true, true>)};
+        const void *kernels[2] = {reinterpret_cast<const void *>(kda_scan_kernel<false>),
+                                  reinterpret_cast<const void *>(kda_scan_kernel<true>)};
         for (const void *k : kernels)
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
@@ -929,14 +923,10 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
     const long long grid = std::min<long long>(units, di.sms);
     const unsigned g = static_cast<unsigned>(grid);
     const size_t sb = lay.total();
-    if (p.s_cols && p.out)
-        kda_scan_kernel<true, true><<<g, NT, sb, stream>>>(p);
-    else if (p.s_cols)
-        kda_scan_kernel<true, false><<<g, NT, sb, stream>>>(p);
-    else if (p.out)
-        kda_scan_kernel<false, true><<<g, NT, sb, stream>>>(p);
+    if (p.s_cols)
+        kda_scan_kernel<true><<<g, NT, sb, stream>>>(p);
     else
-        kda_scan_kernel<false, false><<<g, NT, sb, stream>>>(p);
+        kda_scan_kernel<false><<<g, NT, sb, stream>>>(p);
     return check_launch("kda_scan_kernel");
 }
 
