@@ -80,9 +80,11 @@ constexpr float OUT_SCALE = 0.0883883476483184405501f;  // 1 / sqrt(128)
 constexpr uint64_t WAIT_NS = 1000000000ull;  // an mbarrier wait gives up after one second
 
 // mbarriers: state slots full/empty, scan-input buffers full/empty, raw-row stages
-// full/empty, and the prologue warps' own rendezvous before k.q
+// full/empty, the prologue warps' own rendezvous before k.q, and scan-input buffers
+// holding a finished unit's output rows (the copy warp stores them, then frees the
+// buffer)
 enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, B_STG_EMPTY = 10, B_PRO = 12,
-       NBARS = 13 };
+       B_OUT_FULL = 13, NBARS = 15 };
 
 // Rows a unit runs: KEEP_NONE all T_run; ROWS_* a verify with per-session row counts
 // (host values in keep_host, or rows_dev); KEEP_* a rollback to per-session keep.
@@ -210,6 +212,13 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, int x, int y
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
                  ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+
+// 1D bulk copy shared -> global, tracked by bulk groups
+__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -363,6 +372,26 @@ __device__ void issue_stage(const ScanParams &p, const Layout &lay, uint32_t stg
     }
 }
 
+// Unit u's output rows, left by the scan warps in the v slots of scan-input buffer b,
+// leave as one bulk store per row (lanes 0..T-1); then the buffer is free again.
+__device__ void store_outputs(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int u, int b,
+                              int lane)
+{
+    if (p.out) {
+        const Unit x = unit_of(p, u);
+        if (lane < x.T) {
+            const uint32_t src = smem_addr(sm + lay.si(b) + (static_cast<size_t>(lane) * SI_ROW + SI_V) * 4);
+            float *dst = p.out + ((static_cast<size_t>(x.lb) * p.T_rows + lane) * p.H + x.h) * D;
+            bulk_store(dst, src, D * 4);
+            bulk_commit();
+            bulk_wait_read();
+        }
+        __syncwarp();
+    }
+    if (lane == 0)
+        mbar_arrive(c.bar(B_SI_EMPTY + b));
+}
+
 // The copy warp runs two units ahead of the scan for states and nstg units ahead
 // of the prologue for raw rows, and sends each state on to the snapshot as soon
 // as it has landed.  Unit k uses state slot k % 2 and raw-row stage k % nstg.
@@ -396,6 +425,7 @@ __device__ void copy_warp(const ScanParams &p, const Layout &lay, unsigned char 
         }
     }
     bool aborted = false;
+    int uprev = n, last_k = -1;
     for (int k = 0; uk < n; ++k) {
         const int s = k & 1;
         const uint32_t ph = (k >> 1) & 1;
@@ -440,9 +470,26 @@ __device__ void copy_warp(const ScanParams &p, const Layout &lay, unsigned char 
             (s ? pend1 : pend0) = true;
             (s ? par1 : par0) = ((k + 2) >> 1) & 1;
         }
+        // the scan of unit k-1 has finished: its output rows leave, its buffer is freed
+        if (k >= 1) {
+            if (!warp_wait(c, B_OUT_FULL + (s ^ 1), ((k - 1) >> 1) & 1)) {
+                aborted = true;
+                break;
+            }
+            store_outputs(p, lay, sm, c, uprev, s ^ 1, lane);
+        }
+        uprev = uk;
+        last_k = k;
         uk = u1;
         u1 = u2;
         u2 = u2 < n ? next_live(p, u2 + gridDim.x, n, lane == 0) : n;
+    }
+    // the last unit's output rows
+    if (!aborted && last_k >= 0) {
+        if (warp_wait(c, B_OUT_FULL + (last_k & 1), (last_k >> 1) & 1))
+            store_outputs(p, lay, sm, c, uprev, last_k & 1, lane);
+        else
+            aborted = true;
     }
     if (lane == 0) {
         if (aborted) {  // copies still in flight must land before the CTA leaves
@@ -697,13 +744,13 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
         mbar_arrive(c.bar(B_STATE_EMPTY + s));
         if (!warp_wait(c, B_SI_FULL + s, ph))
             return;
-        const float *si = reinterpret_cast<const float *>(sm + lay.si(s));
+        float *si = reinterpret_cast<float *>(sm + lay.si(s));
         const float *sc = reinterpret_cast<const float *>(sm + lay.sc(s));
-        float *outp = p.out ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum : nullptr;
+        const bool outp = p.out != nullptr;
 
         // ---- the T-row gated delta rule ---------------------------------------------
         for (int t = 0; t < T; ++t) {
-            const float *vt = si + t * SI_ROW;
+            float *vt = si + t * SI_ROW;
             const float *gp = vt + rg * GRP;
             float2 uacc[4], eacc[4], kk[8];
 #pragma unroll
@@ -757,8 +804,10 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             const float2 bk = *reinterpret_cast<const float2 *>(sc + 2 * t);  // {beta, k.q}
             const float w = __fmul_rn(bk.x, __fsub_rn(vt[SI_V + jsum], sum));
             const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
+            // o replaces v_j in the row's scan inputs (its u lane has read it: the
+            // shuffle above orders that read first); the copy warp stores the rows
             if (outp && b2)
-                outp[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
+                vt[SI_V + jsum] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
             // every lane gathers w of its 4 columns from the u lanes 4 c + cg
             float2 wc[4];
 #pragma unroll
@@ -775,7 +824,8 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             if (COLS)  // the column stash: the state after row t
                 store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
         }
-        mbar_arrive(c.bar(B_SI_EMPTY + s));
+        fence_proxy_async();  // the output rows, written here, are read by bulk stores
+        mbar_arrive(c.bar(B_OUT_FULL + s));
 
         // ---- state write-back -----------------------------------------------------------
         store_tile(p.s_out + static_cast<size_t>(u) * D * D + jbase, rg, S);
@@ -799,7 +849,8 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
             mbar_init(c.bar(B_STATE_FULL + s), 1);
             mbar_init(c.bar(B_STATE_EMPTY + s), NSCAN * 32);
             mbar_init(c.bar(B_SI_FULL + s), NPRO * 32);
-            mbar_init(c.bar(B_SI_EMPTY + s), NSCAN * 32);
+            mbar_init(c.bar(B_SI_EMPTY + s), 1);
+            mbar_init(c.bar(B_OUT_FULL + s), NSCAN * 32);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(c.bar(B_STG_FULL + b), 1);
