@@ -319,6 +319,34 @@ def run_gpu(args, rank, world, local_rank):
         "launches_per_step": 4,
     }
 
+    # the same rounds replayed from CUDA graphs (one graph per resident round): the
+    # launch gaps between the round's kernels shrink
+    if not args.no_graph:
+        side = torch.cuda.Stream(dev)
+        gp = [kb.RoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+                           scratch, side) for r in range(R)]
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for g in gp:
+                g()
+        stream.wait_stream(side)
+        barrier()
+        for g in gp:
+            g.capture()
+        for i in range(args.warmup):
+            gp[i % R].replay()
+        barrier()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        for i in range(K):
+            gp[(args.warmup + i) % R].replay()
+        gb.record(stream)
+        barrier()
+        g_ms = ga.elapsed_time(gb) / K
+        if int(status.item()):
+            raise RuntimeError(f"device status {int(status.item()):#x} after the graph steps")
+        res["graph"] = {"ms_per_step": g_ms, "rows_per_s": world * w.B * w.T / (g_ms * 1e-3), "steps": K}
+
     # e2e: host buffers through the public API, copies inside the timed region
     if not args.no_e2e:
         HR = min(R, 4)
@@ -531,6 +559,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-per-layer", action="store_true", help="skip the per-layer (and CUDA graph) rounds")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the rounds")
     ap.add_argument("--per-layer-steps", type=int, default=200)
     ap.add_argument("--no-var-t", action="store_true", help="skip the variable-T rounds")
     ap.add_argument("--no-sampled", action="store_true", help="skip the sampled-accept timing")
@@ -613,6 +642,7 @@ def main():
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
         "e2e": res.get("e2e"),
+        "graph": res.get("graph"),
         "per_layer": res.get("per_layer"),
         "var_t": res.get("var_t"),
         "sampled_accept": res.get("sampled_accept"),

@@ -470,6 +470,8 @@ class RoundPlan:
                           _ptr(keep_out), MEM_DEVICE, _ptr(dev_status), s)
         self._stash, self._tensors, self._dt = stash, tensors, dt
         self._L = L
+        self.stream = stream if isinstance(stream, torch.cuda.Stream) else None
+        self.graph = None
 
     def verify(self):
         rc = self._L.kda_verify_scan(*self._verify)
@@ -491,6 +493,20 @@ class RoundPlan:
         self.verify()
         self.accept()
         self.rollback()
+
+    def capture(self):
+        """Capture one round (verify, accept, rollback) into a CUDA graph on the plan's
+        side stream (a torch.cuda.Stream other than the default one).  Run the round
+        eagerly once before, so every one-time setup call has happened."""
+        if self.stream is None:
+            raise ValueError("capture needs a plan built on a side torch.cuda.Stream")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            self()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
 
 
 class LayerRoundPlan:
