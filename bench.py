@@ -97,6 +97,27 @@ def measured_peak():
 
 
 # ---------------------------------------------------------------------------
+# replicas on several GPUs: every rank runs the whole workload (weak scaling, no
+# collective on the data path); a time is the slowest rank's, the throughput counts
+# every rank's rows
+# ---------------------------------------------------------------------------
+def slowest(ms: float, world: int, device=None) -> float:
+    """The largest of every rank's ms (identity with one rank)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(world: int, B: int, T: int, ms: float) -> float:
+    """Verify rows per second of the whole job: world replicas of B sessions x T rows per step."""
+    return world * B * T / (ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
@@ -290,11 +311,7 @@ def run_gpu(args, rank, world, local_rank):
     if st_word:
         raise RuntimeError(f"device status {st_word:#x} after the timed steps")
     ms_step = total_ms / K
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = slowest(ms_step, world, dev)
 
     keeps_all = [[j + 1 for j in jt[(args.warmup + i) % R]] for i in range(K)]
     vb = verify_bytes(w)
@@ -304,7 +321,7 @@ def run_gpu(args, rank, world, local_rank):
     achieved = vb / (verify_avg_ms * 1e-3) / 1e9
 
     res = {
-        "rows_per_s": world * w.B * w.T / (ms_step * 1e-3),
+        "rows_per_s": job_rows_per_s(world, w.B, w.T, ms_step),
         "ms_per_step": ms_step,
         "verify_ms": verify_avg_ms,
         "accept_ms": sum(accept_ms) / K,
@@ -345,7 +362,8 @@ def run_gpu(args, rank, world, local_rank):
         g_ms = ga.elapsed_time(gb) / K
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the graph steps")
-        res["graph"] = {"ms_per_step": g_ms, "rows_per_s": world * w.B * w.T / (g_ms * 1e-3), "steps": K}
+        g_ms = slowest(g_ms, world, dev)
+        res["graph"] = {"ms_per_step": g_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, g_ms), "steps": K}
 
     # e2e: host buffers through the public API, copies inside the timed region
     if not args.no_e2e:
@@ -383,12 +401,8 @@ def run_gpu(args, rank, world, local_rank):
             e2e_step(i % HR)
         barrier()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        res["e2e"] = {"value": world * w.B * w.T / (e2e_ms * 1e-3), "unit": UNIT,
+        e2e_ms = slowest(e2e_ms, world, dev)
+        res["e2e"] = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT,
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                       "ms_per_step": e2e_ms, "steps": Ke}
 
@@ -427,9 +441,10 @@ def run_gpu(args, rank, world, local_rank):
         graph_ms = timed(lambda r: gplans[r].replay())
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the per-layer steps")
+        eager_ms, graph_ms = slowest(eager_ms, world, dev), slowest(graph_ms, world, dev)
         res["per_layer"] = {"launches_per_step": w.L + 3, "steps": Kp, "eager_ms_per_step": eager_ms,
                             "graph_ms_per_step": graph_ms,
-                            "graph_rows_per_s": world * w.B * w.T / (graph_ms * 1e-3)}
+                            "graph_rows_per_s": job_rows_per_s(world, w.B, w.T, graph_ms)}
     # column-stash rollback (the alternative to snapshot + replay): the verify also
     # writes the state and ring after every row, the rollback copies the kept column
     col_bytes = w.L * w.B * w.H * w.T * (128 * 128 + 9 * 128) * 4
@@ -541,7 +556,7 @@ def run_gpu(args, rank, world, local_rank):
         res["var_t"] = {"window": "glm5_conf_keep, p_min 0.5, slot confidences ~ U(0.3, 1) (seeded)",
                         "rows_mean": sum(t_host) / len(t_host), "rows_min": min(t_host), "rows_max": max(t_host),
                         "steps": Kv, "verify_ms": v_ms, "round_gpu_ms": s_ms,
-                        "rows_per_s": world * sum(t_host) / (s_ms * 1e-3),
+                        "rows_per_s": world * sum(t_host) / (slowest(s_ms, world, dev) * 1e-3),
                         "verify_gbs": vb_var / (v_ms * 1e-3) / 1e9,
                         "verify_frac_of_peak": vb_var / (v_ms * 1e-3) / 1e9 / peak}
     return res
