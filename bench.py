@@ -35,7 +35,7 @@ FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes read + written by one verify launch of the current kda_scan_kernel, from
 # one ncu capture each (profiles/kda_scan_kernel_<workload>.md; dram__bytes_read.sum +
 # dram__bytes_write.sum).  Re-measure whenever the kernel changes.
-TRAFFIC_BYTES = {"stack34": 183_960_832 + 258_220_288, "batched32": 175_732_992 + 247_056_128}
+TRAFFIC_BYTES = {"stack34": 183_975_168 + 257_655_040, "batched32": 175_692_288 + 245_857_536}
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "

@@ -30,13 +30,15 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller; the library
  *     keeps none of them past the call except through the kda_stash it fills.
  *   - Every call is asynchronous on `stream` and never synchronises.
- *   - The library allocates no memory.  spec_accept takes caller scratch.
+ *   - The library allocates no memory.  spec_accept and spec_accept_sampled take
+ *     caller scratch.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns KDA_EINVAL and enqueues nothing.  The reason is kept
  *     per thread for kda_last_error().
  *   - Conditions found on the device (a NaN row at the accept point, a device
- *     keep outside 1..T) are OR-ed as KDA_ST_* bits into the caller's device int
- *     `dev_status` (may be NULL); the caller reads it after synchronising.
+ *     keep or row count out of range, a wait that ran out) are OR-ed as KDA_ST_*
+ *     bits into the caller's device int `dev_status` (may be NULL); the caller
+ *     reads it after synchronising.
  *   - Pointers to float / 16-byte vectors must be 16-byte aligned.
  */
 #ifndef KDA_SPEC_H
@@ -64,12 +66,16 @@ extern "C" {
 #define KDA_ETIMEOUT 4 /* reserved for host-side reports of KDA_ST_TIMEOUT   */
 
 /* bits OR-ed into *dev_status by kernels */
-#define KDA_ST_NAN 0x1      /* spec_accept: row j (the bonus row) holds a NaN */
+#define KDA_ST_NAN 0x1      /* accept: a consulted row holds a NaN (greedy: row j,
+                               the bonus row; sampled: any row the walk reads) */
 #define KDA_ST_BADKEEP 0x2  /* a device keep outside 1..T, or a device row count
                                outside 1..T (the *_var calls); that session is
                                left untouched                                    */
-#define KDA_ST_TIMEOUT 0x4  /* a bulk copy into shared memory did not arrive in
-                               time (bounded wait); the CTA stopped early       */
+#define KDA_ST_TIMEOUT 0x4  /* a wait inside the scan kernel ran out (one second:
+                               a bulk copy or a partner warp never arrived); the
+                               CTA stopped early and its units are unfinished.
+                               kda_verify_scan has no status word: a caller that
+                               wants this report uses kda_verify_scan_var        */
 #define KDA_ST_TIES 0x8     /* spec_accept_sampled: more than 2*KDA_SAMPLED_TOPK_MAX
                                tokens tie at a row's top-k boundary; that row's
                                top-p filter was skipped                          */

@@ -11,7 +11,8 @@
 //                      two state slots, two units ahead; as soon as it lands it
 //                      leaves again as four tensor stores to the snapshot (the
 //                      fused snapshot write).  The unit's raw q, k, v, g rows are
-//                      staged with 1D bulk copies one unit ahead.
+//                      staged with 1D bulk copies one or two units ahead, and a
+//                      finished unit's output rows leave as 1D bulk stores.
 //   prologue warps (4) one per stream (q, k, v, g), one unit ahead of the scan:
 //                      width-4 causal conv + SiLU of q, k, v (mini fixture
 //                      linear_attn_config of glm5_spec_ppn_gate.rs:
@@ -24,7 +25,8 @@
 //   scan warps (8)     hold the unit's state in registers for its whole T-row
 //                      loop and write it back once: each 64 KiB head state
 //                      crosses HBM once in and once out per round, plus the
-//                      snapshot copy.
+//                      snapshot copy.  A row's output replaces its consumed v in
+//                      the scan inputs, where the copy warp picks it up.
 //
 // Register tile: lane 4 rg + cg of scan warp wi holds key rows rg + 8 r (r < 16)
 // of value columns 16 wi + 4 cg .. +3, row pairs packed into float2 so each
@@ -42,22 +44,27 @@
 //   o  = (e + w (k.q)) / sqrt(128)   == (S' + k w^T)^T q / sqrt(128)
 //   S  = S' + k w^T              second register sweep
 // Every operation is an explicitly rounded intrinsic and the code for a row does
-// not depend on T or on the unit, so T rows in one launch and T launches of one
-// row give the same bits, and so do a rollback replay and a fresh verify.
+// not depend on T, on the unit or on whether outputs are written, so T rows in one
+// launch and T launches of one row give the same bits, and so do a rollback
+// replay and a fresh verify.
 //
 // Rollback runs the same kernel from the snapshot over rows 0..keep-1 of the
 // stashed raw rows (the conv re-runs inside the replay), with outputs and the
-// snapshot store switched off.
-// Every wait on an mbarrier is bounded.  A wait that runs out sets
-// KDA_ST_TIMEOUT and a shared abort flag that ends every warp of the CTA; the
-// copy warp first lets its copies in flight land.
+// snapshot store switched off.  Rounds whose length differs per session run each
+// unit's own row count in the same grid.  A second instantiation also writes the
+// column stash (the state and ring after every row).
+// Every wait on an mbarrier is bounded by one second.  A wait that runs out sets
+// KDA_ST_TIMEOUT (where the call has a status word) and a shared abort flag that
+// ends every warp of the CTA; the copy warp first lets its copies in flight land.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cstring>
 #include <string>
 
@@ -924,8 +931,9 @@ int state_map(CUtensorMap *m, const float *base, long long units)
 }
 
 struct DeviceInfo {
+    std::atomic<int> ready{0};
     int sms = 0;
-    int smem_max = 0;  // opt-in shared memory per block, set as the kernel's limit
+    int smem_max = 0;  // opt-in shared memory per block, set as the kernels' limit
 };
 
 int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
@@ -936,6 +944,7 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
     if (units > 0x7fffffffLL / D)
         return fail(KDA_EINVAL, "L*B*H exceeds the unit index range (2^31 / 128 units)");
     static DeviceInfo info[64];
+    static std::mutex init_mutex;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -943,25 +952,30 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
     if (dev < 0 || dev >= 64)
         return fail(KDA_EINVAL, "device ordinal beyond the launch table");
     DeviceInfo &di = info[dev];
-    if (di.sms == 0) {
-        int sms = 0, optin = 0;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e == cudaSuccess)
-            e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-        if (e != cudaSuccess)
-            return fail(KDA_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
-        const size_t most = Layout{KDA_TMAX, 4, 1}.total();
-        if (static_cast<size_t>(optin) < most)
-            return fail(KDA_ECUDA, "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
-        const void *kernels[2] = {reinterpret_cast<const void *>(kda_scan_kernel<false>),
-                                  reinterpret_cast<const void *>(kda_scan_kernel<true>)};
-        for (const void *k : kernels)
+    if (!di.ready.load(std::memory_order_acquire)) {  // once per device, under a lock
+        std::lock_guard<std::mutex> lock(init_mutex);
+        if (!di.ready.load(std::memory_order_relaxed)) {
+            int sms = 0, optin = 0;
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-        if (e != cudaSuccess)
-            return fail(KDA_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
-        di.smem_max = optin;
-        di.sms = sms;
+                e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+            if (e != cudaSuccess)
+                return fail(KDA_ECUDA, std::string("cudaDeviceGetAttribute: ") + cudaGetErrorString(e));
+            const size_t most = Layout{KDA_TMAX, 4, 1}.total();
+            if (static_cast<size_t>(optin) < most)
+                return fail(KDA_ECUDA,
+                            "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
+            const void *kernels[2] = {reinterpret_cast<const void *>(kda_scan_kernel<false>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<true>)};
+            for (const void *k : kernels)
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+            if (e != cudaSuccess)
+                return fail(KDA_ECUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+            di.smem_max = optin;
+            di.sms = sms;
+            di.ready.store(1, std::memory_order_release);
+        }
     }
     // two raw-row stages (the prologue then never waits for its rows) where they fit
     p.nstg = Layout{p.tcap, p.bf16 ? 2 : 4, 2}.total() <= static_cast<size_t>(di.smem_max) ? 2 : 1;
@@ -1316,7 +1330,7 @@ extern "C" int kda_rollback_cols(const kda_dims *dims, const kda_layer_state *st
     p.T_rows = T;
     p.T_run = T;
     p.bf16 = dims->dtype == KDA_BF16;
-    const long long grid = std::min<long long>(units, 152LL * 8);
+    const long long grid = std::min<long long>(units, 4096);  // a grid-stride loop over the units
     commit_cols_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(p);
     return check_launch("commit_cols_kernel");
 }
