@@ -1,10 +1,14 @@
 """Benchmark: KDA speculative-verify rounds on one GB300 (or N replicas).
 
 A step is one verify round of the whole hot path on resident inputs:
-  kda_verify_scan  (conv + activations + gated delta rule over T rows, fused
-                    state snapshot)  ->  spec_accept (device argmax per row,
-                    first mismatch, keep = j+1)  ->  kda_rollback (device keep;
-                    replay of rows 0..keep-1 from the snapshot where keep < T).
+  kda_verify_scan_pingpong  (conv + activations + gated delta rule over T rows;
+                    reads the committed state buffer, which stays as the round's
+                    snapshot, and writes the other one)  ->  spec_accept (device
+                    argmax per row, first mismatch, keep = j+1)  ->  kda_rollback
+                    (device keep; replay of rows 0..keep-1 from the snapshot where
+                    keep < T).
+The in-place round (kda_verify_scan copying the snapshot as it reads the state) is
+timed beside it under "in_place".
 Default workload: the 34-layer KDA stack of one session, 64 heads x 128x128 f32
 state per layer, K = 7 drafts (T = 8), 64 seeded rounds cycled, accept j drawn
 per round.
@@ -32,10 +36,10 @@ METRIC = "KDA verify rows/s (T=K+1, 64 heads) and achieved HBM GB/s vs 8 TB/s ro
 UNIT = "verify rows/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes read + written by one verify launch of the current kda_scan_kernel, from
-# one ncu capture each (profiles/kda_scan_kernel_<workload>.md; dram__bytes_read.sum +
-# dram__bytes_write.sum).  Re-measure whenever the kernel changes.
-TRAFFIC_BYTES = {"stack34": 183_975_168 + 257_655_040, "batched32": 175_692_288 + 245_857_536}
+# DRAM bytes read + written by one ping-pong verify launch of the current
+# kda_scan_kernel, from one ncu capture each (profiles/kda_scan_kernel_<workload>.md;
+# dram__bytes_read.sum + dram__bytes_write.sum).  Re-measure whenever the kernel changes.
+TRAFFIC_BYTES = {}
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
@@ -51,10 +55,13 @@ WORKLOAD_TEXT = {
 # ---------------------------------------------------------------------------
 # byte accounting (algorithmic bytes: every tensor element moved once)
 # ---------------------------------------------------------------------------
-def verify_bytes(w) -> int:
+def verify_bytes(w, snapshot_copy: bool = False) -> int:
+    """One verify launch.  Ping-pong (the default): S read + S write, ring read + write.
+    snapshot_copy: the in-place verify that also writes the snapshot of S and ring."""
     es = 2 if w.bf16 else 4
     D = 128
-    per_head = 3 * D * D * 4 + 3 * 9 * D * 4  # S read + snapshot write + S write; ring read/write/snapshot
+    n = 3 if snapshot_copy else 2
+    per_head = n * D * D * 4 + n * 9 * D * 4
     rows = w.T * w.H * (4 * D + 1) * es
     out = w.T * w.H * D * 4
     return w.L * w.B * (w.H * per_head + rows + out) + w.L * w.H * 3 * D * 4 * 4
@@ -73,7 +80,7 @@ def rollback_bytes(w, keeps) -> int:
 
 
 def verify_bytes_var(w, t_rows) -> int:
-    """verify_bytes with session b running t_rows[b] rows."""
+    """verify_bytes (in place, snapshot copied) with session b running t_rows[b] rows."""
     es = 2 if w.bf16 else 4
     D = 128
     per_head = 3 * D * D * 4 + 3 * 9 * D * 4
@@ -266,13 +273,30 @@ def run_gpu(args, rank, world, local_rank):
     scratch = torch.empty(max(kb.spec_accept_scratch_bytes(w.B, w.T, w.V), 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # the timed round: ping-pong state buffers (the resident state and the stash's
+    # snapshot buffers swap roles every round; the verify reads one and writes the other)
+    pp = kb.PingPong(st, spare_state=stash.state_snap, spare_ring=stash.ring_snap)
+    pplans = [kb.PingPongRoundPlan(pp, rows[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+                                   scratch, stream) for r in range(R)]
+    # the in-place round (snapshot copied by the verify), reported beside it
     plans = [kb.RoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
                           scratch, stream) for r in range(R)]
 
-    def step(r, ev=None):
-        p = plans[r]
+    def step(r, ev=None, plans_=None):
+        p = (plans_ or pplans)[r]
         if ev is None:
             p()
+            return
+        if plans_ is None:
+            par = pp.parity
+            ev[0].record(stream)
+            p.verify(par)
+            ev[1].record(stream)
+            p.accept()
+            ev[2].record(stream)
+            p.rollback(par)
+            ev[3].record(stream)
+            p._flip(par)
             return
         ev[0].record(stream)
         p.verify()
@@ -320,6 +344,32 @@ def run_gpu(args, rank, world, local_rank):
     peak, peak_kind = measured_peak()
     achieved = vb / (verify_avg_ms * 1e-3) / 1e9
 
+    # the in-place round: kda_verify_scan writes the snapshot copy as it reads the state
+    Ki = max(1, min(K, 1000))
+    evi = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Ki)]
+    for i in range(3):
+        step(i % R, plans_=plans)
+    barrier()
+    ia, ib = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ia.record(stream)
+    for i in range(Ki):
+        step(i % R, evi[i], plans_=plans)
+    ib.record(stream)
+    barrier()
+    if int(status.item()):
+        raise RuntimeError(f"device status {int(status.item()):#x} after the in-place steps")
+    i_ms = slowest(ia.elapsed_time(ib) / Ki, world, dev)
+    i_verify = sum(e[0].elapsed_time(e[1]) for e in evi) / Ki
+    vb_in = verify_bytes(w, snapshot_copy=True)
+    in_place = {"steps": Ki, "ms_per_step": i_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, i_ms),
+                "verify_ms": i_verify, "accept_ms": sum(e[1].elapsed_time(e[2]) for e in evi) / Ki,
+                "rollback_ms": sum(e[2].elapsed_time(e[3]) for e in evi) / Ki, "verify_bytes": vb_in,
+                "verify_gbs": vb_in / (i_verify * 1e-3) / 1e9,
+                "verify_frac_of_peak": vb_in / (i_verify * 1e-3) / 1e9 / peak}
+    # the committed state is back in the ping-pong buffers' hands from here on: the
+    # in-place rounds above advanced st.state, which is one of them
+    pp.parity = 0
+
     res = {
         "rows_per_s": job_rows_per_s(world, w.B, w.T, ms_step),
         "ms_per_step": ms_step,
@@ -334,17 +384,19 @@ def run_gpu(args, rank, world, local_rank):
         "peak_kind": peak_kind,
         "clocks": clk.summary(),
         "launches_per_step": 4,
+        "in_place": in_place,
     }
 
     # the same rounds replayed from CUDA graphs (one graph per resident round): the
     # launch gaps between the round's kernels shrink
     if not args.no_graph:
         side = torch.cuda.Stream(dev)
-        gp = [kb.RoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
-                           scratch, side) for r in range(R)]
+        gp = [kb.PingPongRoundPlan(pp, rows[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+                                   scratch, side) for r in range(R)]
         side.wait_stream(stream)
         with torch.cuda.stream(side):
             for g in gp:
+                g()  # both parities of every plan run once eagerly before capture
                 g()
         stream.wait_stream(side)
         barrier()
@@ -380,8 +432,8 @@ def run_gpu(args, rank, world, local_rank):
         d2h = host_res.numel() * 4
         Ke = max(1, min(args.e2e_steps, K))
 
-        eplan = kb.RoundPlan(st, dev_rows, out, stash, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
-                             status, scratch, stream)
+        eplan = kb.PingPongRoundPlan(pp, dev_rows, out, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
+                                     status, scratch, stream)
 
         def e2e_step(r):
             for n in dev_rows:
@@ -646,7 +698,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based draws; bf16 raw rows)",
         "config": config,
-        "roofline": {"bound": "hbm", "kernel": "kda_scan_kernel (verify)", "achieved": res["achieved"],
+        "roofline": {"bound": "hbm", "kernel": "kda_scan_kernel (ping-pong verify)", "achieved": res["achieved"],
                      "peak": res["peak"], "unit": "GB/s", "frac": frac,
                      "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
                      "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
@@ -656,6 +708,7 @@ def main():
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
+        "in_place": res.get("in_place"),
         "e2e": res.get("e2e"),
         "graph": res.get("graph"),
         "per_layer": res.get("per_layer"),

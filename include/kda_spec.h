@@ -159,6 +159,30 @@ int kda_rollback(const kda_dims *dims, const kda_layer_state *st, const kda_stas
                  const int *keep, int keep_mem, int *dev_status, cudaStream_t stream);
 
 /*
+ * kda_verify_scan_pingpong -- a verify round with the state kept in two buffers whose
+ * roles swap every round, so that the snapshot costs no copy (the pages' verify
+ * snapshots the state with a device-to-device clone before row 0; glm_spec.rs,
+ * ROLLBACK and the Glm5VerifyCkpt doc).
+ * On entry stash->state_snap and stash->ring_snap hold the PRE-round state and conv
+ * ring of every unit.  They are read and left untouched, and so are this round's
+ * snapshot.  The post-round state and ring are written to st->state and
+ * st->conv_ring, whose previous contents are ignored.  kda_rollback /
+ * kda_rollback_var of the stash then restore from the pre-round buffers as usual.
+ * Before the next round the caller swaps the buffers: st->state and st->conv_ring
+ * (the committed state) become the next stash->state_snap and ring_snap, and the old
+ * snapshot buffers become the next st->state and conv_ring.
+ *   t_rows NULL: every session runs T rows; else per-session row counts with t_mem
+ *   and dev_status as for kda_verify_scan_var (a session whose device count is out
+ *   of range is not written at all and sets KDA_ST_BADKEEP).
+ * State, ring and outputs are bit-identical to kda_verify_scan (or _var) run from the
+ * same pre-round state.  Per head the state moves 2 x 64 KiB instead of 3 x 64 KiB.
+ * The two buffers must not overlap.
+ */
+int kda_verify_scan_pingpong(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows, int T,
+                             const int *t_rows, int t_mem, float *out, kda_stash *stash, int *dev_status,
+                             cudaStream_t stream);
+
+/*
  * Rounds whose length differs per session (variable T inside one batched grid).
  * glm_spec.rs, glm5_conf_keep and the p-min break of the draft chain, and dflash.rs,
  * DsparkVtPolicy / dspark_confidence_vt / dspark_slot_confidence_vt: each session

@@ -27,11 +27,12 @@ F32, BF16 = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
-EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_cols",
+EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_pingpong",
+           "kda_verify_scan_cols",
            "kda_rollback_cols", "spec_accept_var",
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 2
+ABI_VERSION = 3
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -91,6 +92,10 @@ def lib(path: str | None = None):
     L.kda_rollback_var.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                    ctypes.POINTER(KdaStashC), vp, vp, ci, vp, vp]
     L.kda_rollback_var.restype = ci
+    L.kda_verify_scan_pingpong.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                           ctypes.POINTER(KdaRows), ci, vp, ci, vp, ctypes.POINTER(KdaStashC), vp,
+                                           vp]
+    L.kda_verify_scan_pingpong.restype = ci
     L.kda_verify_scan_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                        ctypes.POINTER(KdaRows), ci, vp, vp, vp, vp]
     L.kda_verify_scan_cols.restype = ci
@@ -310,6 +315,92 @@ def kda_rollback_var(st: LayerState, stash: Stash, t_rows, keep, dev_status: tor
     _check("kda_rollback_var", rc)
 
 
+class PingPong:
+    """The state and conv ring of L x B x H units in two buffers whose roles swap
+    every round (kda_verify_scan_pingpong): a round reads the committed buffer, which
+    it leaves untouched as the round's snapshot, and writes the other one.
+
+    ``state()`` / ``ring()`` are the committed tensors.  A round is ``verify`` then,
+    where some session keeps fewer than all rows, ``rollback`` (both address the
+    buffers of the last verify); ``verify`` flips which buffer is committed.
+    """
+
+    def __init__(self, st: LayerState, spare_state: torch.Tensor | None = None,
+                 spare_ring: torch.Tensor | None = None):
+        self.L, self.B, self.H = st.L, st.B, st.H
+        spare_state = torch.empty_like(st.state) if spare_state is None else spare_state
+        spare_ring = torch.empty_like(st.conv_ring) if spare_ring is None else spare_ring
+        _dev(spare_state, "spare_state", torch.float32, tuple(st.state.shape))
+        _dev(spare_ring, "spare_ring", torch.float32, tuple(st.conv_ring.shape))
+        self.conv_w = st.conv_w
+        self.states = (st.state, spare_state)
+        self.rings = (st.conv_ring, spare_ring)
+        # a round of parity p reads buffer p (its stash) and writes buffer 1 - p
+        self.cst = [KdaLayerState(self.states[1 - p].data_ptr(), self.rings[1 - p].data_ptr(),
+                                  st.conv_w.data_ptr()) for p in (0, 1)]
+        self.cstash = [KdaStashC(self.states[p].data_ptr(), self.rings[p].data_ptr(), KdaRows(), 0) for p in (0, 1)]
+        self.parity = 0  # the committed state is in buffer `parity`
+        self.last = None  # parity of the last verify
+        self.rows, self.dtype = None, None
+
+    def state(self) -> torch.Tensor:
+        return self.states[self.parity]
+
+    def ring(self) -> torch.Tensor:
+        return self.rings[self.parity]
+
+    def dims(self, dtype: int) -> KdaDims:
+        return KdaDims(self.L, self.B, self.H, D, D, dtype)
+
+
+def kda_verify_scan_pingpong(pp: PingPong, q, k, v, g, beta, out: torch.Tensor | None = None, t_rows=None,
+                             dev_status: torch.Tensor | None = None, stream=None) -> PingPong:
+    """One verify round from the committed buffer of ``pp`` into the other one.
+
+    Arguments as for kda_verify_scan (t_rows: None, or per-session rows as for
+    kda_verify_scan_var).  Afterwards the other buffer is committed.
+    """
+    shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
+    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
+    if out is not None:
+        _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
+    tp, mem, hold = (None, MEM_HOST, None) if t_rows is None else _int_array(t_rows, pp.B, "t_rows")
+    p = pp.parity
+    dims = pp.dims(dt)
+    rc = lib().kda_verify_scan_pingpong(ctypes.byref(dims), ctypes.byref(pp.cst[p]), ctypes.byref(rows), T, tp, mem,
+                                        _ptr(out), ctypes.byref(pp.cstash[p]), _ptr(dev_status),
+                                        ctypes.c_void_p(_stream(stream)))
+    del hold
+    _check("kda_verify_scan_pingpong", rc)
+    pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, p, 1 - p
+    return pp
+
+
+def kda_rollback_pingpong(pp: PingPong, keep, t_rows=None, dev_status: torch.Tensor | None = None,
+                          stream=None) -> None:
+    """kda_rollback (or kda_rollback_var with t_rows) of the last ping-pong round: the
+    sessions that keep fewer than all rows are replayed from the round's pre-round
+    buffer into the committed one."""
+    if pp.last is None:
+        raise ValueError("no ping-pong verify round to roll back")
+    p = pp.last
+    dims = pp.dims(pp.dtype)
+    kp, m2, h2 = _int_array(keep, pp.B, "keep")
+    if t_rows is None:
+        rc = lib().kda_rollback(ctypes.byref(dims), ctypes.byref(pp.cst[p]), ctypes.byref(pp.cstash[p]), kp, m2,
+                                _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+        fn, h1 = "kda_rollback", None
+    else:
+        tp, m1, h1 = _int_array(t_rows, pp.B, "t_rows")
+        if m1 != m2:
+            raise ValueError("t_rows and keep must both be host arrays or both device tensors")
+        rc = lib().kda_rollback_var(ctypes.byref(dims), ctypes.byref(pp.cst[p]), ctypes.byref(pp.cstash[p]), tp, kp,
+                                    m1, _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+        fn = "kda_rollback_var"
+    del h1, h2
+    _check(fn, rc)
+
+
 class ColStash:
     """The state and conv ring after every row of one round (column-stash rollback)."""
 
@@ -507,6 +598,94 @@ class RoundPlan:
 
     def replay(self):
         self.graph.replay()
+
+
+class PingPongRoundPlan:
+    """RoundPlan for ping-pong rounds: kda_verify_scan_pingpong, spec_accept and
+    kda_rollback (device keep) with their arguments marshalled once for each parity
+    of the shared PingPong buffers.  Each call runs the round at the buffers' current
+    parity and flips it.  ``capture()`` records one CUDA graph per parity; ``replay()``
+    replays the one of the current parity and flips it.
+    """
+
+    def __init__(self, pp: PingPong, rows: dict, out, logits, drafts, j_out, bonus_out, keep_out, dev_status,
+                 scratch, stream=None):
+        self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch)
+        self.pp = pp
+        shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
+        crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
+        B, Tl, V = (int(x) for x in logits.shape)
+        if Tl != T or B != pp.B:
+            raise ValueError("logits must be [B][T][V] of the round")
+        _dev(drafts, "drafts", torch.int32, (B, T - 1))
+        for name, t in (("j_out", j_out), ("bonus_out", bonus_out), ("keep_out", keep_out)):
+            _dev(t, name, torch.int32, (B,))
+        if out is not None:
+            _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
+        self.dims, self.crows = pp.dims(dt), crows
+        # per-parity copies of the structs: the library records the rows in the stash
+        self.cst = [KdaLayerState(c.state, c.conv_ring, c.conv_w) for c in pp.cst]
+        self.cstash = [KdaStashC(c.state_snap, c.ring_snap, KdaRows(), 0) for c in pp.cstash]
+        s = ctypes.c_void_p(_stream(stream))
+        self._verify = [(ctypes.byref(self.dims), ctypes.byref(self.cst[p]), ctypes.byref(self.crows), T, None,
+                         MEM_HOST, _ptr(out), ctypes.byref(self.cstash[p]), _ptr(dev_status), s) for p in (0, 1)]
+        nbytes = scratch.numel() * scratch.element_size()
+        self._accept = (_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out), _ptr(bonus_out),
+                        _ptr(keep_out), _ptr(dev_status), _ptr(scratch), nbytes, s)
+        self._rollback = [(ctypes.byref(self.dims), ctypes.byref(self.cst[p]), ctypes.byref(self.cstash[p]),
+                           _ptr(keep_out), MEM_DEVICE, _ptr(dev_status), s) for p in (0, 1)]
+        self._tensors, self._dt = tensors, dt
+        self._L = lib()
+        self.stream = stream if isinstance(stream, torch.cuda.Stream) else None
+        self.graphs = None
+
+    def verify(self, p: int):
+        rc = self._L.kda_verify_scan_pingpong(*self._verify[p])
+        if rc:
+            _check("kda_verify_scan_pingpong", rc)
+
+    def accept(self):
+        rc = self._L.spec_accept(*self._accept)
+        if rc:
+            _check("spec_accept", rc)
+
+    def rollback(self, p: int):
+        rc = self._L.kda_rollback(*self._rollback[p])
+        if rc:
+            _check("kda_rollback", rc)
+
+    def _flip(self, p: int):
+        pp = self.pp
+        pp.rows, pp.dtype, pp.last, pp.parity = self._tensors, self._dt, p, 1 - p
+        pp.cstash[p].rows, pp.cstash[p].T = self.crows, self.cstash[p].T
+
+    def __call__(self):
+        p = self.pp.parity
+        self.verify(p)
+        self.accept()
+        self.rollback(p)
+        self._flip(p)
+
+    def capture(self):
+        """Capture the round at each parity into a CUDA graph on the plan's side stream.
+        Run the round eagerly at both parities before, so every one-time setup call has
+        happened."""
+        if self.stream is None:
+            raise ValueError("capture needs a plan built on a side torch.cuda.Stream")
+        self.graphs = []
+        for p in (0, 1):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.verify(p)
+                self.accept()
+                self.rollback(p)
+            self.graphs.append(g)
+        return self.graphs
+
+    def replay(self):
+        p = self.pp.parity
+        self.graphs[p].replay()
+        self._flip(p)
 
 
 class LayerRoundPlan:

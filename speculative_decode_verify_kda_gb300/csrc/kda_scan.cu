@@ -29,11 +29,14 @@
 //                      the scan inputs, where the copy warp picks it up.
 //
 // Register tile: lane 4 rg + cg of scan warp wi holds key rows rg + 8 r (r < 16)
-// of value columns 16 wi + 4 cg .. +3, row pairs packed into float2 so each
+// of value columns 16 wi + 4 cg .. +3, column pairs packed into float2 so each
 // element operation is one lane of a packed f32x2 instruction (__fmul2_rn,
-// __ffma2_rn).  Rows rg + 8 r share their 128-byte swizzle phase.  The scan
-// inputs of a row hold each row group's d, k and q contiguously, so a quarter
-// warp reads two broadcast addresses per load.
+// __ffma2_rn) and each row of the tile is the 16-byte vector it is loaded from and
+// stored as (a row-pair packing needs register moves against those vectors, which
+// cost the T-loop 40 %).  The row scalars d, k, q are broadcast into both halves of
+// a pair.  Rows rg + 8 r share their 128-byte swizzle phase.  The scan inputs of a
+// row hold each row group's d, k and q contiguously, so a quarter warp reads two
+// broadcast addresses per load.
 // Per row t (glm_spec.rs module doc, VERIFY-ROW BATCHING: the recurrence stays
 // sequential inside one launch, the in-kernel T-loop being the chained t=1
 // program):
@@ -701,24 +704,24 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
 }
 
 // ---- scan warps ---------------------------------------------------------------------
-// A thread's register tile to a [128][128] state at So (already offset by its columns).
-__device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[8][4])
+// A thread's register tile to a [128][128] state at So (already offset by its columns):
+// row rg + 8 r is the column pairs S[r][0], S[r][1], one 16-byte store.
+__device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[16][2])
 {
 #pragma unroll
-    for (int rp = 0; rp < 8; ++rp) {
-        const int i = rg + 16 * rp;
-        *reinterpret_cast<float4 *>(So + i * D) = make_float4(S[rp][0].x, S[rp][1].x, S[rp][2].x, S[rp][3].x);
-        *reinterpret_cast<float4 *>(So + (i + 8) * D) = make_float4(S[rp][0].y, S[rp][1].y, S[rp][2].y, S[rp][3].y);
-    }
+    for (int r = 0; r < 16; ++r)
+        *reinterpret_cast<float4 *>(So + (rg + 8 * r) * D) = make_float4(S[r][0].x, S[r][0].y, S[r][1].x, S[r][1].y);
 }
 
 template <bool COLS>
 __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     // lane 4 rg + cg of warp wi holds key rows i = rg + 8 r (r < 16) of value columns
-    // j = 16 wi + 4 cg + c (c < 4): 64 elements, row pairs (2 rp, 2 rp + 1) packed.
-    // The two row groups of a quarter warp read two addresses of a scan-input row,
-    // each broadcast to four lanes.
+    // j = 16 wi + 4 cg + c (c < 4): 64 elements, column pairs (c, c + 1) packed, the
+    // way they arrive from and leave for memory as 16-byte vectors.  The row scalars
+    // d, k, q of a row are broadcast into both halves of a pair.  The two row groups
+    // of a quarter warp read two addresses of a scan-input row, each broadcast to four
+    // lanes.
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5, cg = lane & 3, rg = lane >> 2;
     const int jbase = 16 * wi + 4 * cg;
     // after the reduce-scatter a lane holds one sum: of u (b2 = 0) or e (b2 = 1), of
@@ -735,17 +738,14 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
         const uint32_t ph = (k >> 1) & 1;
         if (!warp_wait(c, B_STATE_FULL + s, ph))
             return;
-        float2 S[8][4];  // S[rp][c] = (S[rg + 16 rp][jbase + c], S[rg + 16 rp + 8][jbase + c])
+        float2 S[16][2];  // S[r][h] = (S[rg + 8 r][jbase + 2 h], S[rg + 8 r][jbase + 2 h + 1])
         {
             const unsigned char *src = sm + lay.slot(s) + soff;
 #pragma unroll
-            for (int rp = 0; rp < 8; ++rp) {
-                const float4 a = *reinterpret_cast<const float4 *>(src + (2 * rp) * 1024);
-                const float4 b = *reinterpret_cast<const float4 *>(src + (2 * rp + 1) * 1024);
-                S[rp][0] = make_float2(a.x, b.x);
-                S[rp][1] = make_float2(a.y, b.y);
-                S[rp][2] = make_float2(a.z, b.z);
-                S[rp][3] = make_float2(a.w, b.w);
+            for (int r = 0; r < 16; ++r) {
+                const float4 a = *reinterpret_cast<const float4 *>(src + r * 1024);
+                S[r][0] = make_float2(a.x, a.y);
+                S[r][1] = make_float2(a.z, a.w);
             }
         }
         mbar_arrive(c.bar(B_STATE_EMPTY + s));
@@ -759,41 +759,36 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
         for (int t = 0; t < T; ++t) {
             float *vt = si + t * SI_ROW;
             const float *gp = vt + rg * GRP;
-            float2 uacc[4], eacc[4], kk[8];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                uacc[c4] = eacc[c4] = make_float2(0.f, 0.f);
-            // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows)
+            float2 uacc[2], eacc[2];
+            float kv[16];
+            uacc[0] = uacc[1] = eacc[0] = eacc[1] = make_float2(0.f, 0.f);
+            // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows, in order)
 #pragma unroll
             for (int rq = 0; rq < 4; ++rq) {
                 const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
                 const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
                 const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
-                const float2 dA = make_float2(d4.x, d4.y), dB = make_float2(d4.z, d4.w);
-                const float2 qA = make_float2(q4.x, q4.y), qB = make_float2(q4.z, q4.w);
-                kk[2 * rq] = make_float2(k4.x, k4.y);
-                kk[2 * rq + 1] = make_float2(k4.z, k4.w);
+                const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+                kv[4 * rq] = k4.x;
+                kv[4 * rq + 1] = k4.y;
+                kv[4 * rq + 2] = k4.z;
+                kv[4 * rq + 3] = k4.w;
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    S[2 * rq][c4] = __fmul2_rn(S[2 * rq][c4], dA);
-                    uacc[c4] = __ffma2_rn(S[2 * rq][c4], kk[2 * rq], uacc[c4]);
-                    eacc[c4] = __ffma2_rn(S[2 * rq][c4], qA, eacc[c4]);
-                }
+                for (int m = 0; m < 4; ++m) {
+                    const int r = 4 * rq + m;
+                    const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[r], kv[r]);
+                    const float2 qq = make_float2(qv[m], qv[m]);
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    S[2 * rq + 1][c4] = __fmul2_rn(S[2 * rq + 1][c4], dB);
-                    uacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], kk[2 * rq + 1], uacc[c4]);
-                    eacc[c4] = __ffma2_rn(S[2 * rq + 1][c4], qB, eacc[c4]);
+                    for (int h = 0; h < 2; ++h) {
+                        S[r][h] = __fmul2_rn(S[r][h], dd);
+                        uacc[h] = __ffma2_rn(S[r][h], kk, uacc[h]);
+                        eacc[h] = __ffma2_rn(S[r][h], qq, eacc[h]);
+                    }
                 }
             }
             // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
             // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
-            float v8[8];
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                v8[c4] = __fadd_rn(uacc[c4].x, uacc[c4].y);
-                v8[4 + c4] = __fadd_rn(eacc[c4].x, eacc[c4].y);
-            }
+            const float v8[8] = {uacc[0].x, uacc[0].y, uacc[1].x, uacc[1].y, eacc[0].x, eacc[0].y, eacc[1].x, eacc[1].y};
             float v4[4], v2[2];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -816,18 +811,18 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             if (outp && b2)
                 vt[SI_V + jsum] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
             // every lane gathers w of its 4 columns from the u lanes 4 c + cg
-            float2 wc[4];
+            float wv[4];
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                const float wv = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
-                wc[c4] = make_float2(wv, wv);
-            }
+            for (int c4 = 0; c4 < 4; ++c4)
+                wv[c4] = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
+            const float2 w01 = make_float2(wv[0], wv[1]), w23 = make_float2(wv[2], wv[3]);
             // S = S' + k w^T
 #pragma unroll
-            for (int rp = 0; rp < 8; ++rp)
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    S[rp][c4] = __ffma2_rn(kk[rp], wc[c4], S[rp][c4]);
+            for (int r = 0; r < 16; ++r) {
+                const float2 kk = make_float2(kv[r], kv[r]);
+                S[r][0] = __ffma2_rn(kk, w01, S[r][0]);
+                S[r][1] = __ffma2_rn(kk, w23, S[r][1]);
+            }
             if (COLS)  // the column stash: the state after row t
                 store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
         }
@@ -1035,8 +1030,11 @@ namespace {
 
 // Shared body of kda_verify_scan and kda_verify_scan_var.  t_rows == nullptr: every
 // session runs T rows; else session b runs t_rows[b] rows (host or device values).
+// pingpong: the pre-round state and ring are read from the stash (left untouched, so
+// they are the round's snapshot) and the post-round ones written to st.
 int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows, int T,
-                  const int *t_rows, int t_mem, float *out, kda_stash *stash, int *dev_status, cudaStream_t stream)
+                  const int *t_rows, int t_mem, float *out, kda_stash *stash, int *dev_status, bool pingpong,
+                  cudaStream_t stream)
 {
     int rc = check_common(dims, st);
     if (rc)
@@ -1054,6 +1052,8 @@ int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_row
         return rc;
     if (out && (reinterpret_cast<uintptr_t>(out) & 3u))
         return fail(KDA_EINVAL, "out must be 4-byte aligned");
+    if (pingpong && !stash)
+        return fail(KDA_EINVAL, "kda_verify_scan_pingpong needs a stash holding the pre-round state and ring");
     if (stash) {
         if (!stash->state_snap || !stash->ring_snap)
             return fail(KDA_EINVAL, "stash->state_snap and stash->ring_snap must be allocated by the caller");
@@ -1085,10 +1085,10 @@ int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_row
         }
     }
     p.s_out = st->state;
-    p.s_snap = stash ? stash->state_snap : nullptr;
-    p.ring_in = st->conv_ring;
+    p.s_snap = stash && !pingpong ? stash->state_snap : nullptr;
+    p.ring_in = pingpong ? stash->ring_snap : st->conv_ring;
     p.ring_out = st->conv_ring;
-    p.ring_snap = stash ? stash->ring_snap : nullptr;
+    p.ring_snap = stash && !pingpong ? stash->ring_snap : nullptr;
     p.conv_w = st->conv_w;
     p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
     p.out = out;
@@ -1098,7 +1098,7 @@ int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_row
     p.T_run = T;
     p.tcap = T;
     p.bf16 = dims->dtype == KDA_BF16;
-    if ((rc = launch_scan(p, st->state, stream)))
+    if ((rc = launch_scan(p, pingpong ? stash->state_snap : st->state, stream)))
         return rc;
     if (stash) {
         stash->rows = *rows;
@@ -1113,7 +1113,7 @@ int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_row
 extern "C" int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
                                int T, float *out, kda_stash *stash, cudaStream_t stream)
 {
-    return verify_common(dims, st, rows, T, nullptr, KDA_MEM_HOST, out, stash, nullptr, stream);
+    return verify_common(dims, st, rows, T, nullptr, KDA_MEM_HOST, out, stash, nullptr, false, stream);
 }
 
 extern "C" int kda_verify_scan_var(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
@@ -1122,7 +1122,14 @@ extern "C" int kda_verify_scan_var(const kda_dims *dims, const kda_layer_state *
 {
     if (!t_rows && dims && static_cast<long long>(dims->L) * dims->B * dims->H > 0)
         return fail(KDA_EINVAL, "t_rows must not be NULL");
-    return verify_common(dims, st, rows, T_cap, t_rows, t_mem, out, stash, dev_status, stream);
+    return verify_common(dims, st, rows, T_cap, t_rows, t_mem, out, stash, dev_status, false, stream);
+}
+
+extern "C" int kda_verify_scan_pingpong(const kda_dims *dims, const kda_layer_state *st, const kda_rows *rows,
+                                        int T, const int *t_rows, int t_mem, float *out, kda_stash *stash,
+                                        int *dev_status, cudaStream_t stream)
+{
+    return verify_common(dims, st, rows, T, t_rows, t_mem, out, stash, dev_status, true, stream);
 }
 
 namespace kda {

@@ -209,3 +209,24 @@ def test_cols_entry_points_reject_on_host(L):
     full = (ctypes.c_int * 2)(8, 8)
     assert L.kda_rollback_cols(ctypes.byref(dims), ctypes.byref(st), FAKE, FAKE, 8, ctypes.cast(full, ctypes.c_void_p),
                                kb.MEM_HOST, None, None) == kb.OK
+
+
+def test_pingpong_rejects_on_host(L):
+    dims, st, rows = _state(B=2)
+
+    def call(stash, T=8, t=None, mem=kb.MEM_HOST):
+        return L.kda_verify_scan_pingpong(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(rows), T,
+                                          ctypes.cast(t, ctypes.c_void_p) if t is not None else None, mem, None,
+                                          ctypes.byref(stash) if stash is not None else None, None, None)
+    good = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(), 0)
+    assert call(None) == kb.EINVAL  # the stash holds the pre-round state: required
+    assert b"pre-round" in L.kda_last_error()
+    assert call(kb.KdaStashC(FAKE, FAKE + 0x2000, kb.KdaRows(), 0)) == kb.EINVAL  # state buffers alias
+    assert call(kb.KdaStashC(None, FAKE + 0x2000, kb.KdaRows(), 0)) == kb.EINVAL
+    assert call(good, T=16) == kb.EINVAL
+    bad_t = (ctypes.c_int * 2)(8, 0)
+    assert call(good, t=bad_t) == kb.EINVAL
+    assert call(good, t=(ctypes.c_int * 2)(8, 8), mem=9) == kb.EINVAL
+    empty = kb.KdaDims(0, 2, 64, 128, 128, kb.BF16)
+    assert L.kda_verify_scan_pingpong(ctypes.byref(empty), ctypes.byref(st), ctypes.byref(rows), 8, None,
+                                      kb.MEM_HOST, None, ctypes.byref(good), None, None) == kb.OK
