@@ -3,16 +3,9 @@
 //
 // A unit is one (layer, session, head): its 128 x 128 f32 state, the raw rows of
 // its T drafted positions, its conv ring and conv weights.  One persistent CTA per
-// SM walks the units blockIdx.x, +gridDim.x, ... with three kinds of warps that
-// hand work to each other through mbarriers in shared memory:
+// SM walks the units blockIdx.x, +gridDim.x, ... with two kinds of warps that hand
+// work to each other through mbarriers in shared memory:
 //
-//   copy warp (1)      TMA: the unit's state arrives as four 2D tensor copies
-//                      (32 columns x 128 rows each, 128-byte swizzle) into one of
-//                      two state slots, two units ahead; as soon as it lands it
-//                      leaves again as four tensor stores to the snapshot (the
-//                      fused snapshot write).  The unit's raw q, k, v, g rows are
-//                      staged with 1D bulk copies one or two units ahead, and a
-//                      finished unit's output rows leave as 1D bulk stores.
 //   prologue warps (4) one per stream (q, k, v, g), one unit ahead of the scan:
 //                      width-4 causal conv + SiLU of q, k, v (mini fixture
 //                      linear_attn_config of glm5_spec_ppn_gate.rs:
@@ -21,12 +14,20 @@
 //                      q and k, k.q, the forget gate d = exp(-5 sigmoid(raw_g))
 //                      and beta = sigmoid(raw_beta), written as the round's scan
 //                      inputs into one of two shared buffers; they also re-roll
-//                      the conv ring (and snapshot it).
+//                      the conv ring (and snapshot it).  The g warp also stages the
+//                      raw q, k, v, g rows with 1D bulk copies, one or two units
+//                      ahead, once the prologue is done with a stage.
 //   scan warps (8)     hold the unit's state in registers for its whole T-row
 //                      loop and write it back once: each 64 KiB head state
-//                      crosses HBM once in and once out per round, plus the
-//                      snapshot copy.  A row's output replaces its consumed v in
-//                      the scan inputs, where the copy warp picks it up.
+//                      crosses HBM once in and once out per round (plus the
+//                      snapshot copy of the in-place verify).  Output rows go
+//                      straight to global memory.  Scan warp 0 also loads the
+//                      states: a unit's state arrives as four 2D tensor copies (32
+//                      columns x 128 rows each, 128-byte swizzle) into one of two
+//                      slots, two units ahead, and leaves again from the slot as
+//                      four tensor stores to the snapshot (the fused snapshot write).
+// Twelve warps put three on each SM sub-partition, which leaves 168 registers per
+// thread for the scan warps' 64-element tiles (thirteen would cap them at 128).
 //
 // Register tile: lane 4 rg + cg of scan warp wi holds key rows rg + 8 r (r < 16)
 // of value columns 16 wi + 4 cg .. +3, column pairs packed into float2 so each
@@ -58,7 +59,7 @@
 // column stash (the state and ring after every row).
 // Every wait on an mbarrier is bounded by one second.  A wait that runs out sets
 // KDA_ST_TIMEOUT (where the call has a status word) and a shared abort flag that
-// ends every warp of the CTA; the copy warp first lets its copies in flight land.
+// ends every warp of the CTA; the warps that issue copies first let theirs land.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -68,6 +69,7 @@
 #include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <unordered_map>
 #include <cstring>
 #include <string>
 
@@ -77,10 +79,9 @@ namespace kda {
 namespace {
 
 constexpr int D = 128;
-constexpr int NSCAN = 8;                   // scan warps
-constexpr int NPRO = 4;                    // prologue warps: q, k, v, g
-constexpr int WCOPY = NSCAN + NPRO;        // the copy warp
-constexpr int NT = (NSCAN + NPRO + 1) * 32;
+constexpr int NSCAN = 8;                   // scan warps; warp 0 also loads the states
+constexpr int NPRO = 4;                    // prologue warps: q, k, v, g; g also stages the raw rows
+constexpr int NT = (NSCAN + NPRO) * 32;    // 12 warps: 3 per SM sub-partition, so up to 168 registers
 constexpr int GRP = 52;                    // floats per row group of a scan-input row: d, k, q (16 each), pad
 constexpr int SI_V = 8 * GRP;              // offset of v (natural order) in a scan-input row
 constexpr int SI_ROW = SI_V + D;           // floats per scan-input row
@@ -90,11 +91,9 @@ constexpr float OUT_SCALE = 0.0883883476483184405501f;  // 1 / sqrt(128)
 constexpr uint64_t WAIT_NS = 1000000000ull;  // an mbarrier wait gives up after one second
 
 // mbarriers: state slots full/empty, scan-input buffers full/empty, raw-row stages
-// full/empty, the prologue warps' own rendezvous before k.q, and scan-input buffers
-// holding a finished unit's output rows (the copy warp stores them, then frees the
-// buffer)
-enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, B_STG_EMPTY = 10, B_PRO = 12,
-       B_OUT_FULL = 13, NBARS = 15 };
+// full, and the prologue warps' own rendezvous (after it no prologue warp reads the
+// unit's stage again)
+enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, B_PRO = 10, NBARS = 11 };
 
 // Rows a unit runs: KEEP_NONE all T_run; ROWS_* a verify with per-session row counts
 // (host values in keep_host, or rows_dev); KEEP_* a rollback to per-session keep.
@@ -103,6 +102,7 @@ enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2, ROWS_HOST = 3, RO
 struct ScanParams {
     CUtensorMap tm_in;     // state read: [units * 128 rows][128] f32, box 32 x 128, 128B swizzle
     CUtensorMap tm_snap;   // snapshot write, same geometry (unused without s_snap)
+    CUtensorMap tm_rows[4];  // raw rows q, k, v, g: [L*B][T_rows][H][128], box 128 x 1 x T_rows x 1
     float *s_out;          // [L][B][H][D][D]
     float *s_snap;         // nullable: receives the state read through tm_in
     const float *ring_in;  // [L][B][H][3][3][D]
@@ -202,13 +202,6 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// 1D bulk copy global -> shared, counted in bytes by `bar`
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
-}
-
 // 2D tensor copy global -> shared of the box at (x, y), counted in bytes by `bar`
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm, int x, int y, uint32_t bar)
 {
@@ -217,18 +210,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *tm,
                  ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
+// 4D tensor copy global -> shared of the box at (c0, c1, c2, c3), counted in bytes by `bar`
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, int c0, int c1, int c2, int c3,
+                                            uint32_t bar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];"
+                 ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+                 : "memory");
+}
+
 // 2D tensor copy shared -> global of the box at (x, y), tracked by bulk groups
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, int x, int y, uint32_t src)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
                  ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
-}
-
-// 1D bulk copy shared -> global, tracked by bulk groups
-__device__ __forceinline__ void bulk_store(void *dst, uint32_t src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
@@ -340,7 +336,7 @@ __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
 }
 
 // The first unit at or after u (stepping by the grid) that has rows to run.  Every
-// warp walks the same sequence; only the copy warp's lane 0 reports bad keeps.
+// warp walks the same sequence; only lane 0 of scan warp 0 reports bad keeps.
 __device__ int next_live(const ScanParams &p, int u, int n, bool report)
 {
     for (; u < n; u += gridDim.x) {
@@ -353,7 +349,7 @@ __device__ int next_live(const ScanParams &p, int u, int n, bool report)
     return n;
 }
 
-// ---- copy warp ----------------------------------------------------------------------
+// ---- copies issued by scan warp 0 (states) and prologue warp g (raw rows) -----------
 // Unit u's 64 KiB state into a slot: four boxes of 32 columns x 128 rows (lane 0).
 __device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, uint32_t bar, int u)
 {
@@ -363,156 +359,19 @@ __device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, 
         tma_load_2d(slot + b * 16384, &p.tm_in, 32 * b, u * D, bar);
 }
 
-// Unit u's raw q, k, v, g rows into the stage, one bulk copy per (stream, row),
-// spread over the warp; lane 0 arms the barrier with the byte count first.
-__device__ void issue_stage(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, int u, int lane)
+// Unit u's raw rows of stream s (0 q, 1 k, 2 v, 3 g) into the stage: one tensor copy
+// of the T_rows rows of its head (a unit that runs fewer rows gets all T_rows; the
+// rest are not read).  Lane 0 arms the barrier with the byte count; each prologue
+// warp stages its own stream, so the barrier counts four arrivals.
+__device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, int u, int s,
+                             int lane)
 {
     const Unit x = unit_of(p, u);
     const uint32_t rb = static_cast<uint32_t>(lay.row_bytes());
-    if (lane == 0)
-        mbar_expect_tx(bar, 4u * x.T * rb);
-    __syncwarp();
     fence_proxy_async();  // the prologue's generic reads of the stage come first
-    for (int i = lane; i < 4 * x.T; i += 32) {
-        const int s = i / x.T, t = i - s * x.T;
-        const void *base = s == 0 ? p.xq : s == 1 ? p.xk : s == 2 ? p.xv : p.xg;
-        const char *src = static_cast<const char *>(base) +
-                          ((static_cast<size_t>(x.lb) * p.T_rows + t) * p.H + x.h) * rb;
-        bulk_load(stg + (s * lay.tcap + t) * rb, src, rb, bar);
-    }
-}
-
-// Unit u's output rows, left by the scan warps in the v slots of scan-input buffer b,
-// leave as one bulk store per row (lanes 0..T-1); then the buffer is free again.
-__device__ void store_outputs(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int u, int b,
-                              int lane)
-{
-    if (p.out) {
-        const Unit x = unit_of(p, u);
-        if (lane < x.T) {
-            const uint32_t src = smem_addr(sm + lay.si(b) + (static_cast<size_t>(lane) * SI_ROW + SI_V) * 4);
-            float *dst = p.out + ((static_cast<size_t>(x.lb) * p.T_rows + lane) * p.H + x.h) * D;
-            bulk_store(dst, src, D * 4);
-            bulk_commit();
-            bulk_wait_read();
-        }
-        __syncwarp();
-    }
-    if (lane == 0)
-        mbar_arrive(c.bar(B_SI_EMPTY + b));
-}
-
-// The copy warp runs two units ahead of the scan for states and nstg units ahead
-// of the prologue for raw rows, and sends each state on to the snapshot as soon
-// as it has landed.  Unit k uses state slot k % 2 and raw-row stage k % nstg.
-__device__ void copy_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
-{
-    const int lane = threadIdx.x & 31;
-    const uint32_t slot0 = smem_addr(sm + lay.slot(0)), stg0 = smem_addr(sm + lay.stg(0));
-    const uint32_t stage_bytes = static_cast<uint32_t>(lay.stg(1) - lay.stg(0));
-    constexpr uint32_t SLOT = D * D * 4;
-    // copies in flight, for the drain on abort: state slot s / stage b and the
-    // parity of the phase that will count them
-    bool pend0 = false, pend1 = false, pstg0 = false, pstg1 = false;
-    uint32_t par0 = 0, par1 = 0, spar0 = 0, spar1 = 0;
-    int uk = next_live(p, blockIdx.x, n, lane == 0);
-    int u1 = uk < n ? next_live(p, uk + gridDim.x, n, lane == 0) : n;
-    int u2 = u1 < n ? next_live(p, u1 + gridDim.x, n, lane == 0) : n;
-    if (uk < n) {
-        if (lane == 0)
-            issue_state(p, slot0, c.bar(B_STATE_FULL), uk);
-        pend0 = true;
-        issue_stage(p, lay, stg0, c.bar(B_STG_FULL), uk, lane);
-        pstg0 = true;
-    }
-    if (u1 < n) {
-        if (lane == 0)
-            issue_state(p, slot0 + SLOT, c.bar(B_STATE_FULL + 1), u1);
-        pend1 = true;
-        if (lay.nstg == 2) {
-            issue_stage(p, lay, stg0 + stage_bytes, c.bar(B_STG_FULL + 1), u1, lane);
-            pstg1 = true;
-        }
-    }
-    bool aborted = false;
-    int uprev = n, last_k = -1;
-    for (int k = 0; uk < n; ++k) {
-        const int s = k & 1;
-        const uint32_t ph = (k >> 1) & 1;
-        // unit k's state has landed: the fused snapshot leaves straight from the slot
-        if (!warp_wait(c, B_STATE_FULL + s, ph)) {
-            aborted = true;
-            break;
-        }
-        (s ? pend1 : pend0) = false;
-        if (p.s_snap && lane == 0) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                tma_store_2d(&p.tm_snap, 32 * b, uk * D, slot0 + s * SLOT + b * 16384);
-            bulk_commit();
-        }
-        // the prologue is done with unit k's raw rows: stage unit k + nstg's there
-        const int b = lay.nstg == 2 ? s : 0;
-        const int m = lay.nstg == 2 ? k >> 1 : k;  // uses of stage b before unit k
-        if (!warp_wait(c, B_STG_EMPTY + b, m & 1)) {
-            aborted = true;
-            break;
-        }
-        (b ? pstg1 : pstg0) = false;
-        const int ustg = lay.nstg == 2 ? u2 : u1;
-        if (ustg < n) {
-            issue_stage(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + b), ustg, lane);
-            (b ? pstg1 : pstg0) = true;
-            (b ? spar1 : spar0) = (m + 1) & 1;
-        }
-        // the scan warps hold unit k in registers and the snapshot store has read
-        // the slot: load unit k+2 into it
-        if (u2 < n) {
-            if (!warp_wait(c, B_STATE_EMPTY + s, ph)) {
-                aborted = true;
-                break;
-            }
-            if (lane == 0) {
-                bulk_wait_read();
-                fence_proxy_async();
-                issue_state(p, slot0 + s * SLOT, c.bar(B_STATE_FULL + s), u2);
-            }
-            (s ? pend1 : pend0) = true;
-            (s ? par1 : par0) = ((k + 2) >> 1) & 1;
-        }
-        // the scan of unit k-1 has finished: its output rows leave, its buffer is freed
-        if (k >= 1) {
-            if (!warp_wait(c, B_OUT_FULL + (s ^ 1), ((k - 1) >> 1) & 1)) {
-                aborted = true;
-                break;
-            }
-            store_outputs(p, lay, sm, c, uprev, s ^ 1, lane);
-        }
-        uprev = uk;
-        last_k = k;
-        uk = u1;
-        u1 = u2;
-        u2 = u2 < n ? next_live(p, u2 + gridDim.x, n, lane == 0) : n;
-    }
-    // the last unit's output rows
-    if (!aborted && last_k >= 0) {
-        if (warp_wait(c, B_OUT_FULL + (last_k & 1), (last_k >> 1) & 1))
-            store_outputs(p, lay, sm, c, uprev, last_k & 1, lane);
-        else
-            aborted = true;
-    }
     if (lane == 0) {
-        if (aborted) {  // copies still in flight must land before the CTA leaves
-            if (pend0)
-                drain_wait(c.bar(B_STATE_FULL), par0);
-            if (pend1)
-                drain_wait(c.bar(B_STATE_FULL + 1), par1);
-            if (pstg0)
-                drain_wait(c.bar(B_STG_FULL), spar0);
-            if (pstg1)
-                drain_wait(c.bar(B_STG_FULL + 1), spar1);
-        }
-        bulk_wait_all();  // the snapshot stores leave before the CTA's shared memory does
+        mbar_expect_tx(bar, static_cast<uint32_t>(p.T_rows) * rb);
+        tma_load_4d(stg + s * lay.tcap * rb, &p.tm_rows[s], 0, x.h, 0, static_cast<int>(x.lb), bar);
     }
 }
 
@@ -569,8 +428,10 @@ __device__ __forceinline__ void store_perm(float *row, int block, int lane, floa
 }
 
 // Stream pw (0 q, 1 k, 2 v) of one unit: the conv window slides along the rows in
-// registers.  Writes the scan inputs (q-hat, k-hat or v), the ring after the round
-// and, when snapshotting, the ring before it.
+// registers, four rows at a time with no branch around the arithmetic (rows past T
+// repeat row T-1 and are not stored), so the four rows' dependency chains overlap.
+// Writes the scan inputs (q-hat, k-hat or v), the ring after the round and, when
+// snapshotting, the ring before it.
 template <bool COLS>
 __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsigned char *stg, float *si,
                             const Pre &pr, int u, int T, int pw, int lane)
@@ -582,34 +443,39 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
         rs[D / 4] = pr.ring[1];
         rs[2 * D / 4] = pr.ring[2];
     }
-    float4 x0 = pr.ring[0], x1 = pr.ring[1], x2 = pr.ring[2];  // x[t-3], x[t-2], x[t-1]
+    // the window before row t0: x[t0-3], x[t0-2], x[t0-1] of the sequence [ring, rows]
+    float4 x0 = pr.ring[0], x1 = pr.ring[1], x2 = pr.ring[2];
     const int block = pw == 0 ? 32 : 16;
     for (int t0 = 0; t0 < T; t0 += 4) {
+        float4 W[7];  // the sequence from x[t0-3]: W[j .. j+3] is row t0+j's window
+        W[0] = x0;
+        W[1] = x1;
+        W[2] = x2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            W[3 + j] = stage4(stg, lay, pw, min(t0 + j, T - 1), lane);
         float4 y[4];
         float ss[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            if (t0 + j < T) {
-                const float4 x3 = stage4(stg, lay, pw, t0 + j, lane);
-                y[j].x = silu(conv4(pr.w[0], x0.x, x1.x, x2.x, x3.x));
-                y[j].y = silu(conv4(pr.w[1], x0.y, x1.y, x2.y, x3.y));
-                y[j].z = silu(conv4(pr.w[2], x0.z, x1.z, x2.z, x3.z));
-                y[j].w = silu(conv4(pr.w[3], x0.w, x1.w, x2.w, x3.w));
-                x0 = x1;
-                x1 = x2;
-                x2 = x3;
-                if (COLS) {  // the ring after row t0 + j
+            // w.x multiplies x[t-3], w.w the current row
+            y[j].x = silu(conv4(pr.w[0], W[j].x, W[j + 1].x, W[j + 2].x, W[j + 3].x));
+            y[j].y = silu(conv4(pr.w[1], W[j].y, W[j + 1].y, W[j + 2].y, W[j + 3].y));
+            y[j].z = silu(conv4(pr.w[2], W[j].z, W[j + 1].z, W[j + 2].z, W[j + 3].z));
+            y[j].w = silu(conv4(pr.w[3], W[j].w, W[j + 1].w, W[j + 2].w, W[j + 3].w));
+            ss[j] = __fmaf_rn(y[j].w, y[j].w, __fmaf_rn(y[j].z, y[j].z, __fmaf_rn(y[j].y, y[j].y, __fmul_rn(y[j].x, y[j].x))));
+        }
+        if (COLS) {  // the ring after row t0 + j: W[j+1 .. j+3]
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (t0 + j < T) {
                     float4 *rc = reinterpret_cast<float4 *>(
                                      p.ring_cols + ((static_cast<size_t>(u) * p.T_rows + t0 + j) * 3 + pw) * 3 * D) +
                                  lane;
-                    rc[0] = x0;
-                    rc[D / 4] = x1;
-                    rc[2 * D / 4] = x2;
+                    rc[0] = W[j + 1];
+                    rc[D / 4] = W[j + 2];
+                    rc[2 * D / 4] = W[j + 3];
                 }
-            } else {
-                y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            ss[j] = __fmaf_rn(y[j].w, y[j].w, __fmaf_rn(y[j].z, y[j].z, __fmaf_rn(y[j].y, y[j].y, __fmul_rn(y[j].x, y[j].x))));
         }
         if (pw == 2) {
 #pragma unroll
@@ -625,44 +491,80 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
                     ss[j] = __fadd_rn(ss[j], __shfl_xor_sync(0xffffffffu, ss[j], off));
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (t0 + j < T) {
-                    const float r = rsqrtf(__fadd_rn(ss[j], L2_EPS));
-                    store_perm(si + (t0 + j) * SI_ROW, block, lane,
-                               make_float4(__fmul_rn(y[j].x, r), __fmul_rn(y[j].y, r), __fmul_rn(y[j].z, r),
-                                           __fmul_rn(y[j].w, r)));
-                }
+                const float r = rsqrtf(__fadd_rn(ss[j], L2_EPS));
+                const float4 yn = make_float4(__fmul_rn(y[j].x, r), __fmul_rn(y[j].y, r), __fmul_rn(y[j].z, r),
+                                              __fmul_rn(y[j].w, r));
+                if (t0 + j < T)
+                    store_perm(si + (t0 + j) * SI_ROW, block, lane, yn);
             }
         }
+        x0 = W[4];
+        x1 = W[5];
+        x2 = W[6];
     }
-    // the ring after the round: the last 3 of [ring, rows 0..T-1]
+    // the ring after the round: x[T-3], x[T-2], x[T-1] of the sequence [ring, rows]
+    const float4 r0 = T >= 3 ? stage4(stg, lay, pw, T - 3, lane) : T == 2 ? pr.ring[2] : pr.ring[1];
+    const float4 r1 = T >= 2 ? stage4(stg, lay, pw, T - 2, lane) : pr.ring[2];
+    const float4 r2 = stage4(stg, lay, pw, T - 1, lane);
     float4 *ro = reinterpret_cast<float4 *>(p.ring_out + rbase) + lane;
-    ro[0] = x0;
-    ro[D / 4] = x1;
-    ro[2 * D / 4] = x2;
+    ro[0] = r0;
+    ro[D / 4] = r1;
+    ro[2 * D / 4] = r2;
 }
 
-// Stream 3: the forget gate d = exp(-5 sigmoid(raw_g)) per key channel and beta.
+// Stream 3: the forget gate d = exp(-5 sigmoid(raw_g)) per key channel and beta, four
+// rows at a time with no branch around the arithmetic.
 __device__ void gate_stream(const Layout &lay, const unsigned char *stg, float *si, float *sc, const Pre &pr, int T,
                             int lane)
 {
-    for (int t = 0; t < T; ++t) {
-        const float4 g = stage4(stg, lay, 3, t, lane);
-        store_perm(si + t * SI_ROW, 0, lane,
-                   make_float4(__expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.x))),
-                               __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.y))),
-                               __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.z))),
-                               __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.w)))));
+    for (int t0 = 0; t0 < T; t0 += 4) {
+        float4 dg[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 g = stage4(stg, lay, 3, min(t0 + j, T - 1), lane);
+            dg[j] = make_float4(__expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.x))),
+                                __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.y))),
+                                __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.z))),
+                                __expf(__fmul_rn(GATE_LOWER_BOUND, sigmoidf_(g.w))));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (t0 + j < T)
+                store_perm(si + (t0 + j) * SI_ROW, 0, lane, dg[j]);
     }
     if (lane < T)
         sc[2 * lane] = sigmoidf_(pr.beta);
 }
 
+// Each prologue warp also stages its stream's raw rows: unit k's go to stage
+// k % nstg, issued once every prologue warp is done with the stage's previous unit
+// (the B_PRO rendezvous), nstg units ahead.
+struct Stager {
+    int next;             // the unit staged next
+    bool pend0, pend1;    // a copy in flight into stage 0 / 1, for the drain on abort
+    uint32_t par0, par1;  // and the phase parity that completes it
+};
+
 template <bool COLS>
 __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     const int pw = (threadIdx.x >> 5) - NSCAN, lane = threadIdx.x & 31;
+    const uint32_t stg0 = smem_addr(sm + lay.stg(0));
+    const uint32_t stage_bytes = static_cast<uint32_t>(lay.stg(1) - lay.stg(0));
     Pre pr;
     int u = next_live(p, blockIdx.x, n, false);
+    Stager sg{n, false, false, 0, 0};
+    {
+        // the first nstg units' raw rows
+        int v = u;
+        for (int b = 0; b < lay.nstg && v < n; ++b) {
+            issue_stream(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + b), v, pw, lane);
+            (b ? sg.pend1 : sg.pend0) = true;
+            v = next_live(p, v + gridDim.x, n, false);
+        }
+        sg.next = v;
+    }
+    bool ok = true;
     if (u < n)
         load_pre(p, u, pw, lane, pr);
     for (int k = 0; u < n; ++k) {
@@ -670,22 +572,40 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
         const int T = unit_of(p, u).T;
         const int sb = lay.nstg == 2 ? b : 0, m = lay.nstg == 2 ? k >> 1 : k;
         const unsigned char *stg = sm + lay.stg(sb);
-        if (!warp_wait(c, B_STG_FULL + sb, m & 1))
-            return;
+        if (!warp_wait(c, B_STG_FULL + sb, m & 1)) {
+            ok = false;
+            break;
+        }
+        (sb ? sg.pend1 : sg.pend0) = false;
         // the scan of unit k-2 has released this scan-input buffer
-        if (k >= 2 && !warp_wait(c, B_SI_EMPTY + b, ((k >> 1) - 1) & 1))
-            return;
+        if (k >= 2 && !warp_wait(c, B_SI_EMPTY + b, ((k >> 1) - 1) & 1)) {
+            ok = false;
+            break;
+        }
         float *si = reinterpret_cast<float *>(sm + lay.si(b));
         float *sc = reinterpret_cast<float *>(sm + lay.sc(b));
         if (pw < 3)
             conv_stream<COLS>(p, lay, stg, si, pr, u, T, pw, lane);
         else
             gate_stream(lay, stg, si, sc, pr, T, lane);
-        mbar_arrive(c.bar(B_STG_EMPTY + sb));
-        // k.q of each row once q-hat and k-hat are all written
+        // the next unit's conv weights, ring and beta: the loads are in flight during
+        // the rendezvous and k.q below
+        const int un = next_live(p, u + gridDim.x, n, false);
+        if (un < n)
+            load_pre(p, un, pw, lane, pr);
+        // k.q of each row once q-hat and k-hat are all written; past this rendezvous no
+        // prologue warp reads the stage of unit k again
         mbar_arrive(c.bar(B_PRO));
-        if (!warp_wait(c, B_PRO, k & 1))
-            return;
+        if (!warp_wait(c, B_PRO, k & 1)) {
+            ok = false;
+            break;
+        }
+        if (sg.next < n) {
+            issue_stream(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + sb), sg.next, pw, lane);
+            (sb ? sg.pend1 : sg.pend0) = true;
+            (sb ? sg.par1 : sg.par0) = (m + 1) & 1;
+            sg.next = next_live(p, sg.next + gridDim.x, n, false);
+        }
         for (int t = pw; t < T; t += NPRO) {
             const float *g = si + t * SI_ROW + (lane >> 2) * GRP + 4 * (lane & 3);
             const float4 kk = *reinterpret_cast<const float4 *>(g + 16);
@@ -696,10 +616,13 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
                 sc[2 * t + 1] = s;
         }
         mbar_arrive(c.bar(B_SI_FULL + b));
-        const int un = next_live(p, u + gridDim.x, n, false);
-        if (un < n)
-            load_pre(p, un, pw, lane, pr);
         u = un;
+    }
+    if (!ok && lane == 0) {  // stage copies in flight must land before the CTA leaves
+        if (sg.pend0)
+            drain_wait(c.bar(B_STG_FULL), sg.par0);
+        if (sg.pend1)
+            drain_wait(c.bar(B_STG_FULL + 1), sg.par1);
     }
 }
 
@@ -731,13 +654,45 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
     // this thread's 16-byte chunk of row rg in its box of the swizzled slot; row
     // rg + 8 r lies r * 1024 bytes further on with the same swizzle phase
     const uint32_t soff = (wi >> 1) * 16384 + rg * 128 + ((((wi & 1) * 4 + cg) ^ rg) << 4);
-    int u = next_live(p, blockIdx.x, n, false);
+    // Scan warp 0 (the lead) also loads the states: unit k's into slot k % 2, two
+    // units ahead, with the fused snapshot store leaving from the slot as soon as the
+    // state has landed.  Its lane 0 reports invalid device keeps.
+    const bool lead = wi == 0;
+    const uint32_t slot0 = smem_addr(sm + lay.slot(0));
+    constexpr uint32_t SLOT = D * D * 4;
+    // lead: state copies in flight into slot 0 / 1, for the drain on abort, and the
+    // phase parity that completes each
+    bool pend0 = false, pend1 = false;
+    uint32_t par0 = 0, par1 = 0;
+    int u = next_live(p, blockIdx.x, n, lead && lane == 0);
+    int u1 = u < n ? next_live(p, u + gridDim.x, n, lead && lane == 0) : n;
+    int u2 = u1 < n ? next_live(p, u1 + gridDim.x, n, lead && lane == 0) : n;
+    if (lead) {
+        if (lane == 0 && u < n)
+            issue_state(p, slot0, c.bar(B_STATE_FULL), u);
+        if (lane == 0 && u1 < n)
+            issue_state(p, slot0 + SLOT, c.bar(B_STATE_FULL + 1), u1);
+        pend0 = u < n;
+        pend1 = u1 < n;
+    }
+    bool ok = true;
     for (int k = 0; u < n; ++k) {
         const Unit x = unit_of(p, u);
         const int T = x.T, s = k & 1;
         const uint32_t ph = (k >> 1) & 1;
-        if (!warp_wait(c, B_STATE_FULL + s, ph))
-            return;
+        if (!warp_wait(c, B_STATE_FULL + s, ph)) {
+            ok = false;
+            break;
+        }
+        if (lead) {
+            (s ? pend1 : pend0) = false;
+            if (p.s_snap && lane == 0) {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    tma_store_2d(&p.tm_snap, 32 * b, u * D, slot0 + s * SLOT + b * 16384);
+                bulk_commit();
+            }
+        }
         float2 S[16][2];  // S[r][h] = (S[rg + 8 r][jbase + 2 h], S[rg + 8 r][jbase + 2 h + 1])
         {
             const unsigned char *src = sm + lay.slot(s) + soff;
@@ -749,15 +704,18 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             }
         }
         mbar_arrive(c.bar(B_STATE_EMPTY + s));
-        if (!warp_wait(c, B_SI_FULL + s, ph))
-            return;
-        float *si = reinterpret_cast<float *>(sm + lay.si(s));
+        if (!warp_wait(c, B_SI_FULL + s, ph)) {
+            ok = false;
+            break;
+        }
+        const float *si = reinterpret_cast<const float *>(sm + lay.si(s));
         const float *sc = reinterpret_cast<const float *>(sm + lay.sc(s));
-        const bool outp = p.out != nullptr;
+        // the output row t of this unit: lanes with b2 = 1 store column jsum
+        float *orow = p.out ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum : nullptr;
 
         // ---- the T-row gated delta rule ---------------------------------------------
         for (int t = 0; t < T; ++t) {
-            float *vt = si + t * SI_ROW;
+            const float *vt = si + t * SI_ROW;
             const float *gp = vt + rg * GRP;
             float2 uacc[2], eacc[2];
             float kv[16];
@@ -806,10 +764,9 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             const float2 bk = *reinterpret_cast<const float2 *>(sc + 2 * t);  // {beta, k.q}
             const float w = __fmul_rn(bk.x, __fsub_rn(vt[SI_V + jsum], sum));
             const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
-            // o replaces v_j in the row's scan inputs (its u lane has read it: the
-            // shuffle above orders that read first); the copy warp stores the rows
-            if (outp && b2)
-                vt[SI_V + jsum] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
+            // a warp's 16 e lanes store 16 consecutive columns of the output row
+            if (orow && b2)
+                orow[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
             // every lane gathers w of its 4 columns from the u lanes 4 c + cg
             float wv[4];
 #pragma unroll
@@ -826,16 +783,43 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             if (COLS)  // the column stash: the state after row t
                 store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
         }
-        fence_proxy_async();  // the output rows, written here, are read by bulk stores
-        mbar_arrive(c.bar(B_OUT_FULL + s));
+        mbar_arrive(c.bar(B_SI_EMPTY + s));  // the scan inputs of unit k are consumed
+
+        // lead: every scan warp holds unit k in registers and the snapshot store has
+        // read the slot: load unit k+2 into it
+        if (lead && u2 < n) {
+            if (!warp_wait(c, B_STATE_EMPTY + s, ph)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                bulk_wait_read();
+                fence_proxy_async();
+                issue_state(p, slot0 + s * SLOT, c.bar(B_STATE_FULL + s), u2);
+            }
+            (s ? pend1 : pend0) = true;
+            (s ? par1 : par0) = ((k + 2) >> 1) & 1;
+        }
 
         // ---- state write-back -----------------------------------------------------------
         store_tile(p.s_out + static_cast<size_t>(u) * D * D + jbase, rg, S);
-        u = next_live(p, u + gridDim.x, n, false);
+        u = u1;
+        u1 = u2;
+        u2 = u2 < n ? next_live(p, u2 + gridDim.x, n, lead && lane == 0) : n;
+    }
+    if (lead && lane == 0) {
+        if (!ok) {  // state copies in flight must land before the CTA leaves
+            if (pend0)
+                drain_wait(c.bar(B_STATE_FULL), par0);
+            if (pend1)
+                drain_wait(c.bar(B_STATE_FULL + 1), par1);
+        }
+        bulk_wait_all();  // the snapshot stores leave before the CTA's shared memory does
     }
 }
 
-// One persistent CTA per SM; warps 0..7 scan, 8..11 run the prologue, 12 copies.
+// One persistent CTA per SM; warps 0..7 scan (warp 0 also loads the states), 8..11 run
+// the prologue (warp 11 also stages the raw rows).
 // COLS: also write the column stash (the state and ring after every row).  Verify and
 // rollback share one instantiation: alternating between two kernels of this size cost
 // the verify 5 % (its code is fetched again after each switch).
@@ -851,13 +835,10 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
             mbar_init(c.bar(B_STATE_FULL + s), 1);
             mbar_init(c.bar(B_STATE_EMPTY + s), NSCAN * 32);
             mbar_init(c.bar(B_SI_FULL + s), NPRO * 32);
-            mbar_init(c.bar(B_SI_EMPTY + s), 1);
-            mbar_init(c.bar(B_OUT_FULL + s), NSCAN * 32);
+            mbar_init(c.bar(B_SI_EMPTY + s), NSCAN * 32);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(c.bar(B_STG_FULL + b), 1);
-            mbar_init(c.bar(B_STG_EMPTY + b), NPRO * 32);
-        }
+        for (int b = 0; b < 2; ++b)
+            mbar_init(c.bar(B_STG_FULL + b), NPRO);  // one armed arrival per prologue warp
         mbar_init(c.bar(B_PRO), NPRO * 32);
         *c.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -867,10 +848,8 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     const int wi = threadIdx.x >> 5;
     if (wi < NSCAN)
         scan_warp<COLS>(p, lay, sm, c, n);
-    else if (wi < WCOPY)
-        prologue_warp<COLS>(p, lay, sm, c, n);
     else
-        copy_warp(p, lay, sm, c, n);
+        prologue_warp<COLS>(p, lay, sm, c, n);
 }
 
 // ---- host side ----------------------------------------------------------------------
@@ -922,6 +901,59 @@ int state_map(CUtensorMap *m, const float *base, long long units)
     e.units = units;
     next = (next + 1) % 4;
     *m = e.map;
+    return KDA_OK;
+}
+
+// Tensor map of a raw-row tensor [LB][T_rows][H][128] (bf16 or f32) with boxes of one
+// head's T_rows rows.  Encoding is host-only; the calling thread keeps the maps it
+// encoded (cleared past 4096 entries).
+int rows_map(CUtensorMap *m, const void *base, bool bf16, long long LB, int T_rows, int H)
+{
+    struct Key {
+        const void *base;
+        long long LB;
+        int T_rows, H, bf16;
+        bool operator==(const Key &o) const
+        {
+            return base == o.base && LB == o.LB && T_rows == o.T_rows && H == o.H && bf16 == o.bf16;
+        }
+    };
+    struct Hash {
+        size_t operator()(const Key &k) const
+        {
+            return std::hash<const void *>()(k.base) ^ (std::hash<long long>()(k.LB) * 31u) ^
+                   (static_cast<size_t>(k.T_rows) << 20) ^ (static_cast<size_t>(k.H) << 8) ^ k.bf16;
+        }
+    };
+    thread_local std::unordered_map<Key, CUtensorMap, Hash> cache;
+    const Key key{base, LB, T_rows, H, bf16 ? 1 : 0};
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+        *m = it->second;
+        return KDA_OK;
+    }
+    static const EncodeTiled encode = lookup_encode();
+    if (!encode)
+        return fail(KDA_ECUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+    const cuuint64_t es = bf16 ? 2 : 4;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(T_rows), static_cast<cuuint64_t>(LB)};
+    const cuuint64_t strides[3] = {D * es, static_cast<cuuint64_t>(H) * D * es,
+                                   static_cast<cuuint64_t>(T_rows) * H * D * es};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(T_rows), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUtensorMap map;
+    const CUresult r = encode(&map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(KDA_ECUDA, "cuTensorMapEncodeTiled (raw rows) failed with CUresult " +
+                                   std::to_string(static_cast<int>(r)));
+    if (cache.size() >= 4096)
+        cache.clear();
+    cache.emplace(key, map);
+    *m = map;
     return KDA_OK;
 }
 
@@ -980,6 +1012,12 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
         return rc;
     if (p.s_snap && (rc = state_map(&p.tm_snap, p.s_snap, units)))
         return rc;
+    if (p.tcap != p.T_rows)
+        return fail(KDA_EINVAL, "internal: the raw-row stage must hold T_rows rows");
+    const void *raw[4] = {p.xq, p.xk, p.xv, p.xg};
+    for (int s = 0; s < 4; ++s)
+        if ((rc = rows_map(&p.tm_rows[s], raw[s], p.bf16 != 0, static_cast<long long>(p.L) * p.B, p.T_rows, p.H)))
+            return rc;
     const long long grid = std::min<long long>(units, di.sms);
     const unsigned g = static_cast<unsigned>(grid);
     const size_t sb = lay.total();
