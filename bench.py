@@ -1,14 +1,15 @@
 """Benchmark: KDA speculative-verify rounds on one GB300 (or N replicas).
 
 A step is one verify round of the whole hot path on resident inputs:
-  kda_verify_scan_pingpong  (conv + activations + gated delta rule over T rows;
-                    reads the committed state buffer, which stays as the round's
-                    snapshot, and writes the other one)  ->  spec_accept (device
-                    argmax per row, first mismatch, keep = j+1)  ->  kda_rollback
-                    (device keep; replay of rows 0..keep-1 from the snapshot where
-                    keep < T).
-The in-place round (kda_verify_scan copying the snapshot as it reads the state) is
-timed beside it under "in_place".
+  kda_verify_scan_deferred  (one launch: the previous round's accept-j rollback, i.e.
+                    the replay of its rows 0..keep-1 from its snapshot where keep < T,
+                    then this round's conv + activations + gated delta rule over T
+                    rows; ping-pong state buffers, no snapshot copy)  ->  spec_accept
+                    (device argmax per row, first mismatch, keep = j+1, applied by the
+                    next round's launch).
+Beside it: the same rounds with the rollback as its own launch ("separate_rollback":
+kda_verify_scan_pingpong, spec_accept, kda_rollback) and the in-place round
+("in_place": kda_verify_scan copying the snapshot as it reads the state).
 Default workload: the 34-layer KDA stack of one session, 64 heads x 128x128 f32
 state per layer, K = 7 drafts (T = 8), 64 seeded rounds cycled, accept j drawn
 per round.
@@ -65,6 +66,22 @@ def verify_bytes(w, snapshot_copy: bool = False) -> int:
     rows = w.T * w.H * (4 * D + 1) * es
     out = w.T * w.H * D * 4
     return w.L * w.B * (w.H * per_head + rows + out) + w.L * w.H * 3 * D * 4 * 4
+
+
+def deferred_bytes(w, prev_keeps) -> int:
+    """One kda_verify_scan_deferred launch: per session that rolls back (keep < T) the
+    state is read, written as the snapshot and written again, the ring likewise, and
+    the replayed rows are read besides this round's; a session that kept every row
+    reads and writes its state and ring once."""
+    es = 2 if w.bf16 else 4
+    D = 128
+    row = w.H * (4 * D + 1) * es
+    n = 0
+    for k in prev_keeps:
+        pending = k < w.T
+        m = 3 if pending else 2
+        n += w.L * (w.H * m * (D * D * 4 + 9 * D * 4) + (k if pending else 0) * row + w.T * row + w.T * w.H * D * 4)
+    return n + w.L * w.H * 3 * D * 4 * 4
 
 
 def rollback_bytes(w, keeps) -> int:
@@ -312,37 +329,87 @@ def run_gpu(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for i in range(args.warmup):
-        step(i % R)
+    # the timed round: kda_verify_scan_deferred (the previous round's rollback and this
+    # round's verify in one launch) then spec_accept, whose keep the next round applies
+    dplans = [kb.DeferredRoundPlan(pp, rows[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+                                   scratch, stream) for r in range(R)]
+
+    def dstep(r, ev=None):
+        p = dplans[r]
+        par = pp.last
+        if ev is not None:
+            ev[0].record(stream)
+        p.verify(par)
+        if ev is not None:
+            ev[1].record(stream)
+        p.accept()
+        if ev is not None:
+            ev[2].record(stream)
+        p._flip(par)
+
+    # round 0 opens the chain: a ping-pong verify and its accept (its rollback runs
+    # inside round 1's launch)
+    par0 = pp.parity
+    pplans[0].verify(par0)
+    pplans[0].accept()
+    pplans[0]._flip(par0)
+    for i in range(1, args.warmup + 1):
+        dstep(i % R)
     barrier()
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local_rank) as clk:
         barrier()
         t_wall = time.perf_counter()
         e0.record(stream)
         for i in range(K):
-            step((args.warmup + i) % R, evs[i])
+            dstep((args.warmup + 1 + i) % R, evs[i])
         e1.record(stream)
         barrier()
         t_wall = time.perf_counter() - t_wall
     total_ms = e0.elapsed_time(e1)
-    verify_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    round_ms = [e[0].elapsed_time(e[1]) for e in evs]
     accept_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    roll_ms = [e[2].elapsed_time(e[3]) for e in evs]
     st_word = int(status.item())
     if st_word:
         raise RuntimeError(f"device status {st_word:#x} after the timed steps")
     ms_step = total_ms / K
     ms_step = slowest(ms_step, world, dev)
+    # commit the last round, so the committed state is in the ping-pong buffers
+    kb.kda_rollback_pingpong(pp, keep_out, dev_status=status, stream=stream)
 
-    keeps_all = [[j + 1 for j in jt[(args.warmup + i) % R]] for i in range(K)]
-    vb = verify_bytes(w)
-    step_bytes = [vb + accept_bytes(w) + rollback_bytes(w, k) for k in keeps_all]
-    verify_avg_ms = sum(verify_ms) / K
+    # the kept rows each timed round replays: the previous round's accept
+    prev_keeps = [[j + 1 for j in jt[(args.warmup + i) % R]] for i in range(K)]
+    round_bytes = [deferred_bytes(w, k) for k in prev_keeps]
+    step_bytes = [rb + accept_bytes(w) for rb in round_bytes]
+    round_avg_ms = sum(round_ms) / K
     peak, peak_kind = measured_peak()
-    achieved = vb / (verify_avg_ms * 1e-3) / 1e9
+    achieved = sum(round_bytes) / (sum(round_ms) * 1e-3) / 1e9
+
+    # the same rounds with the rollback as its own launch: ping-pong verify, accept,
+    # rollback
+    Kp = max(1, min(K, 1000))
+    evp = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(Kp)]
+    for i in range(3):
+        step(i % R)
+    barrier()
+    pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pa.record(stream)
+    for i in range(Kp):
+        step((3 + i) % R, evp[i])
+    pb.record(stream)
+    barrier()
+    if int(status.item()):
+        raise RuntimeError(f"device status {int(status.item()):#x} after the ping-pong steps")
+    s_ms = slowest(pa.elapsed_time(pb) / Kp, world, dev)
+    s_verify = sum(e[0].elapsed_time(e[1]) for e in evp) / Kp
+    vb = verify_bytes(w)
+    separate = {"steps": Kp, "ms_per_step": s_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, s_ms),
+                "verify_ms": s_verify, "accept_ms": sum(e[1].elapsed_time(e[2]) for e in evp) / Kp,
+                "rollback_ms": sum(e[2].elapsed_time(e[3]) for e in evp) / Kp, "verify_bytes": vb,
+                "verify_gbs": vb / (s_verify * 1e-3) / 1e9, "verify_frac_of_peak": vb / (s_verify * 1e-3) / 1e9 / peak,
+                "launches_per_step": 4}
 
     # the in-place round: kda_verify_scan writes the snapshot copy as it reads the state
     Ki = max(1, min(K, 1000))
@@ -373,17 +440,17 @@ def run_gpu(args, rank, world, local_rank):
     res = {
         "rows_per_s": job_rows_per_s(world, w.B, w.T, ms_step),
         "ms_per_step": ms_step,
-        "verify_ms": verify_avg_ms,
+        "round_kernel_ms": round_avg_ms,
         "accept_ms": sum(accept_ms) / K,
-        "rollback_ms": sum(roll_ms) / K,
         "wall_s": t_wall,
-        "verify_bytes": vb,
+        "round_bytes_mean": sum(round_bytes) / K,
         "step_gbs": sum(step_bytes) / (total_ms * 1e-3) / 1e9,
         "achieved": achieved,
         "peak": peak,
         "peak_kind": peak_kind,
         "clocks": clk.summary(),
-        "launches_per_step": 4,
+        "launches_per_step": 3,
+        "separate_rollback": separate,
         "in_place": in_place,
     }
 
@@ -415,7 +482,8 @@ def run_gpu(args, rank, world, local_rank):
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the graph steps")
         g_ms = slowest(g_ms, world, dev)
-        res["graph"] = {"ms_per_step": g_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, g_ms), "steps": K}
+        res["graph"] = {"ms_per_step": g_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, g_ms), "steps": K,
+                        "round": "ping-pong verify, accept, rollback (separate launches), one graph per round"}
 
     # e2e: host buffers through the public API, copies inside the timed region
     if not args.no_e2e:
@@ -423,7 +491,8 @@ def run_gpu(args, rank, world, local_rank):
         host_rows = [{n: t.cpu().pin_memory() for n, t in rows[r].items()} for r in range(HR)]
         host_logits = [logits[r].cpu().pin_memory() for r in range(HR)]
         host_drafts = [drafts[r].cpu().pin_memory() for r in range(HR)]
-        dev_rows = {n: torch.empty_like(t) for n, t in rows[0].items()}
+        # two input buffer sets: a deferred round reads the previous round's raw rows
+        dev_rows = [{n: torch.empty_like(t) for n, t in rows[0].items()} for _ in range(2)]
         dev_logits = torch.empty_like(logits[0])
         dev_drafts = torch.empty_like(drafts[0])
         host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
@@ -432,28 +501,43 @@ def run_gpu(args, rank, world, local_rank):
         d2h = host_res.numel() * 4
         Ke = max(1, min(args.e2e_steps, K))
 
-        eplan = kb.PingPongRoundPlan(pp, dev_rows, out, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
+        eplans = [kb.DeferredRoundPlan(pp, dev_rows[b], out, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
+                                       status, scratch, stream) for b in range(2)]
+        eopen = kb.PingPongRoundPlan(pp, dev_rows[1], out, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
                                      status, scratch, stream)
 
-        def e2e_step(r):
-            for n in dev_rows:
-                dev_rows[n].copy_(host_rows[r][n], non_blocking=True)
+        def e2e_load(i):
+            r = i % HR
+            for n in dev_rows[i % 2]:
+                dev_rows[i % 2][n].copy_(host_rows[r][n], non_blocking=True)
             dev_logits.copy_(host_logits[r], non_blocking=True)
             dev_drafts.copy_(host_drafts[r], non_blocking=True)
-            eplan()
+
+        def e2e_step(i):
+            e2e_load(i)
+            eplans[i % 2]()
             host_res[0].copy_(j_out, non_blocking=True)
             host_res[1].copy_(bonus_out, non_blocking=True)
             stream.synchronize()  # the host needs j and the bonus before the next round
 
-        for i in range(3):
-            e2e_step(i % HR)
+        # open the chain with a ping-pong round on buffer set 1, then deferred rounds
+        e2e_load(1)
+        par = pp.parity
+        eopen.verify(par)
+        eopen.accept()
+        eopen._flip(par)
+        for i in range(2, 5):
+            e2e_step(i)
         barrier()
         t0 = time.perf_counter()
-        for i in range(Ke):
-            e2e_step(i % HR)
+        for i in range(5, 5 + Ke):
+            e2e_step(i)
         barrier()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
         e2e_ms = slowest(e2e_ms, world, dev)
+        kb.kda_rollback_pingpong(pp, keep_out, dev_status=status, stream=stream)
+        if int(status.item()):
+            raise RuntimeError(f"device status {int(status.item()):#x} after the e2e steps")
         res["e2e"] = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT,
                       "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                       "ms_per_step": e2e_ms, "steps": Ke}
@@ -536,8 +620,9 @@ def run_gpu(args, rank, world, local_rank):
         res["col_stash"] = {"stash_bytes": col_bytes, "steps": Kc, "verify_ms": cv, "rollback_ms": cr,
                             "round_ms": cs, "verify_bytes": cvb, "rollback_bytes_mean": crb,
                             "verify_gbs": cvb / (cv * 1e-3) / 1e9,
-                            "snapshot_replay": {"verify_ms": res["verify_ms"], "rollback_ms": res["rollback_ms"],
-                                                "round_ms": res["ms_per_step"],
+                            "snapshot_replay": {"verify_ms": res["separate_rollback"]["verify_ms"],
+                                                "rollback_ms": res["separate_rollback"]["rollback_ms"],
+                                                "round_ms": res["separate_rollback"]["ms_per_step"],
                                                 "stash_bytes": w.L * w.B * w.H * (128 * 128 + 9 * 128) * 4}}
 
     # sampled acceptance: the rejection walk with filtered target and draft rows; the
@@ -698,16 +783,17 @@ def main():
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based draws; bf16 raw rows)",
         "config": config,
-        "roofline": {"bound": "hbm", "kernel": "kda_scan_kernel (ping-pong verify)", "achieved": res["achieved"],
-                     "peak": res["peak"], "unit": "GB/s", "frac": frac,
+        "roofline": {"bound": "hbm", "kernel": "kda_scan_kernel (deferred round: rollback + verify)",
+                     "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s", "frac": frac,
                      "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
                      "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
-                     "bytes_per_launch": res["verify_bytes"], "traffic": TRAFFIC_BYTES.get(args.workload)},
-        "verify_ms": res["verify_ms"], "accept_ms": res["accept_ms"], "rollback_ms": res["rollback_ms"],
+                     "bytes_per_launch": res["round_bytes_mean"], "traffic": TRAFFIC_BYTES.get(args.workload)},
+        "round_kernel_ms": res["round_kernel_ms"], "accept_ms": res["accept_ms"],
         "step_achieved_gbs": res["step_gbs"],
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
+        "separate_rollback": res.get("separate_rollback"),
         "in_place": res.get("in_place"),
         "e2e": res.get("e2e"),
         "graph": res.get("graph"),

@@ -183,6 +183,34 @@ int kda_verify_scan_pingpong(const kda_dims *dims, const kda_layer_state *st, co
                              cudaStream_t stream);
 
 /*
+ * kda_verify_scan_deferred -- a ping-pong verify round that first applies the
+ * previous round's accept, in the same launch (the rollback of glm_spec.rs,
+ * glm5_verify_rollback, deferred into the next round's verify).
+ * On entry the stash and st describe the previous ping-pong round exactly as
+ * kda_verify_scan_pingpong left them: stash->state_snap / ring_snap its pre-round
+ * state and ring, stash->rows / stash->T its raw rows (still alive), st->state /
+ * conv_ring its post-round state and ring.  prev_keep is a DEVICE int32 [B] array,
+ * the previous round's keep (e.g. spec_accept's keep_out).
+ * Per session b, the committed state is the previous post-round state when
+ * prev_keep[b] == stash->T, else the replay of the previous rows 0..prev_keep[b]-1
+ * from the previous pre-round state (bit-identical to kda_rollback); this round's T
+ * rows (`rows`, outputs to `out`) then run from the committed state.
+ * On return the library has exchanged st->state with stash->state_snap and
+ * st->conv_ring with stash->ring_snap, and recorded `rows` and T in the stash, so that
+ * the stash holds this round's snapshot (the committed state) and st its post-round
+ * state: the pair is again as a ping-pong verify leaves it, ready for kda_rollback, a
+ * further deferred round or (after swapping the pointers back) a ping-pong verify.
+ * Results are bit-identical to kda_rollback of the previous round followed by
+ * kda_verify_scan_pingpong of this one.  A session whose prev_keep lies outside
+ * 1..stash->T is not processed at all (KDA_ST_BADKEEP is set in *dev_status, which
+ * may be NULL).  Per head the state moves 3 x 64 KiB when the session rolls back and
+ * 2 x 64 KiB when it kept every row, against 4 x 64 KiB for the two separate launches.
+ * The last round of a sequence is committed with an ordinary kda_rollback.
+ */
+int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, const int *prev_keep,
+                             const kda_rows *rows, int T, float *out, int *dev_status, cudaStream_t stream);
+
+/*
  * Rounds whose length differs per session (variable T inside one batched grid).
  * glm_spec.rs, glm5_conf_keep and the p-min break of the draft chain, and dflash.rs,
  * DsparkVtPolicy / dspark_confidence_vt / dspark_slot_confidence_vt: each session

@@ -28,11 +28,12 @@ MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_pingpong",
+           "kda_verify_scan_deferred",
            "kda_verify_scan_cols",
            "kda_rollback_cols", "spec_accept_var",
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 3
+ABI_VERSION = 4
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -96,6 +97,9 @@ def lib(path: str | None = None):
                                            ctypes.POINTER(KdaRows), ci, vp, ci, vp, ctypes.POINTER(KdaStashC), vp,
                                            vp]
     L.kda_verify_scan_pingpong.restype = ci
+    L.kda_verify_scan_deferred.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                           ctypes.POINTER(KdaStashC), vp, ctypes.POINTER(KdaRows), ci, vp, vp, vp]
+    L.kda_verify_scan_deferred.restype = ci
     L.kda_verify_scan_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                        ctypes.POINTER(KdaRows), ci, vp, vp, vp, vp]
     L.kda_verify_scan_cols.restype = ci
@@ -373,6 +377,38 @@ def kda_verify_scan_pingpong(pp: PingPong, q, k, v, g, beta, out: torch.Tensor |
     del hold
     _check("kda_verify_scan_pingpong", rc)
     pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, p, 1 - p
+    return pp
+
+
+def kda_verify_scan_deferred(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Tensor, out: torch.Tensor | None = None,
+                             dev_status: torch.Tensor | None = None, stream=None) -> PingPong:
+    """A ping-pong round that first commits the previous one: each session with
+    prev_keep[b] < the previous T is replayed from the previous pre-round buffer (the
+    rollback), then this round's rows run from the committed state.  prev_keep: device
+    int32 [B] (the previous round's keep).  Afterwards, as after kda_verify_scan_pingpong,
+    the round's snapshot is kept and the post-round buffer is the one to commit next.
+    """
+    if pp.last is None:
+        raise ValueError("a deferred round follows a ping-pong round (no previous round to commit)")
+    shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
+    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
+    if dt != pp.dtype:
+        raise TypeError("the raw rows must have the previous round's element type")
+    if out is not None:
+        _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
+    _dev(prev_keep, "prev_keep", torch.int32, (pp.B,))
+    p = pp.last
+    prev = pp.cstash[p]
+    cst = KdaLayerState(pp.states[1 - p].data_ptr(), pp.rings[1 - p].data_ptr(), pp.conv_w.data_ptr())
+    cstash = KdaStashC(pp.states[p].data_ptr(), pp.rings[p].data_ptr(), prev.rows, prev.T)
+    dims = pp.dims(dt)
+    rc = lib().kda_verify_scan_deferred(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(cstash), _ptr(prev_keep),
+                                        ctypes.byref(rows), T, _ptr(out), _ptr(dev_status),
+                                        ctypes.c_void_p(_stream(stream)))
+    _check("kda_verify_scan_deferred", rc)
+    # this round's snapshot is in buffer 1 - p, its post-round state in buffer p
+    pp.cstash[1 - p].rows, pp.cstash[1 - p].T = rows, T
+    pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, 1 - p, p
     return pp
 
 
@@ -685,6 +721,73 @@ class PingPongRoundPlan:
     def replay(self):
         p = self.pp.parity
         self.graphs[p].replay()
+        self._flip(p)
+
+
+class DeferredRoundPlan:
+    """A round whose rollback is deferred into the next round's verify: one call runs
+    kda_verify_scan_deferred (committing the previous round with the device keep_out
+    that the previous round's spec_accept left) and then spec_accept of this round.
+    The previous round must be a ping-pong round (or a deferred one) of the same
+    PingPong buffers whose keep is in keep_out.  Arguments as for PingPongRoundPlan.
+    """
+
+    def __init__(self, pp: PingPong, rows: dict, out, logits, drafts, j_out, bonus_out, keep_out, dev_status,
+                 scratch, stream=None):
+        self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch)
+        self.pp = pp
+        shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
+        crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
+        B, Tl, V = (int(x) for x in logits.shape)
+        if Tl != T or B != pp.B:
+            raise ValueError("logits must be [B][T][V] of the round")
+        _dev(drafts, "drafts", torch.int32, (B, T - 1))
+        for name, t in (("j_out", j_out), ("bonus_out", bonus_out), ("keep_out", keep_out)):
+            _dev(t, name, torch.int32, (B,))
+        if out is not None:
+            _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
+        self.dims, self.crows, self.T = pp.dims(dt), crows, T
+        w = pp.conv_w.data_ptr()
+        # for the previous round's snapshot in buffer p: st is buffer 1 - p, the stash buffer p
+        self.cst = [KdaLayerState(pp.states[1 - p].data_ptr(), pp.rings[1 - p].data_ptr(), w) for p in (0, 1)]
+        self.cstash = [KdaStashC(pp.states[p].data_ptr(), pp.rings[p].data_ptr(), KdaRows(), 0) for p in (0, 1)]
+        s = ctypes.c_void_p(_stream(stream))
+        self._verify = [(ctypes.byref(self.dims), ctypes.byref(self.cst[p]), ctypes.byref(self.cstash[p]),
+                         _ptr(keep_out), ctypes.byref(self.crows), T, _ptr(out), _ptr(dev_status), s) for p in (0, 1)]
+        nbytes = scratch.numel() * scratch.element_size()
+        self._accept = (_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out), _ptr(bonus_out),
+                        _ptr(keep_out), _ptr(dev_status), _ptr(scratch), nbytes, s)
+        self._tensors, self._dt = tensors, dt
+        self._L = lib()
+
+    def verify(self, p: int):
+        pp = self.pp
+        prev = pp.cstash[p]
+        # the library swaps the pointers in the structs it is given: restore them
+        c, st = self.cst[p], self.cstash[p]
+        c.state, c.conv_ring = pp.states[1 - p].data_ptr(), pp.rings[1 - p].data_ptr()
+        st.state_snap, st.ring_snap = pp.states[p].data_ptr(), pp.rings[p].data_ptr()
+        st.rows, st.T = prev.rows, prev.T
+        rc = self._L.kda_verify_scan_deferred(*self._verify[p])
+        if rc:
+            _check("kda_verify_scan_deferred", rc)
+
+    def accept(self):
+        rc = self._L.spec_accept(*self._accept)
+        if rc:
+            _check("spec_accept", rc)
+
+    def _flip(self, p: int):
+        pp = self.pp
+        pp.cstash[1 - p].rows, pp.cstash[1 - p].T = self.crows, self.T
+        pp.rows, pp.dtype, pp.last, pp.parity = self._tensors, self._dt, 1 - p, p
+
+    def __call__(self):
+        p = self.pp.last
+        if p is None:
+            raise ValueError("a deferred round follows a ping-pong round")
+        self.verify(p)
+        self.accept()
         self._flip(p)
 
 

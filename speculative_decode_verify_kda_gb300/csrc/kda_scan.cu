@@ -11,7 +11,7 @@
 //                      linear_attn_config of glm5_spec_ppn_gate.rs:
 //                      short_conv_kernel_size 4, head_dim 128, gate_lower_bound
 //                      -5.0) sliding along the rows in registers, the L2 norms of
-//                      q and k, k.q, the forget gate d = exp(-5 sigmoid(raw_g))
+//                      q and k, the forget gate d = exp(-5 sigmoid(raw_g))
 //                      and beta = sigmoid(raw_beta), written as the round's scan
 //                      inputs into one of two shared buffers; they also re-roll
 //                      the conv ring (and snapshot it).  The g warp also stages the
@@ -42,8 +42,8 @@
 // sequential inside one launch, the in-kernel T-loop being the chained t=1
 // program):
 //   S' = d_t (.) S               d = exp(g)
-//   u  = S'^T k,  e = S'^T q     one register sweep, then a 3-step shuffle
-//                                reduce-scatter over the 8 row groups
+//   u  = S'^T k,  e = S'^T q     one register sweep (which also sums k.q), then a
+//                                3-step shuffle reduce-scatter over the 8 row groups
 //   w  = beta (v - u)
 //   o  = (e + w (k.q)) / sqrt(128)   == (S' + k w^T)^T q / sqrt(128)
 //   S  = S' + k w^T              second register sweep
@@ -54,9 +54,11 @@
 //
 // Rollback runs the same kernel from the snapshot over rows 0..keep-1 of the
 // stashed raw rows (the conv re-runs inside the replay), with outputs and the
-// snapshot store switched off.  Rounds whose length differs per session run each
-// unit's own row count in the same grid.  A second instantiation also writes the
-// column stash (the state and ring after every row).
+// snapshot store switched off.  A deferred round runs that replay and the next
+// round's rows as two items of one unit, the state staying in registers between
+// them.  Rounds whose length differs per session run each unit's own row count in
+// the same grid.  A second instantiation also writes the column stash (the state
+// and ring after every row).
 // Every wait on an mbarrier is bounded by one second.  A wait that runs out sets
 // KDA_ST_TIMEOUT (where the call has a status word) and a shared abort flag that
 // ends every warp of the CTA; the warps that issue copies first let theirs land.
@@ -90,19 +92,22 @@ constexpr float GATE_LOWER_BOUND = -5.0f;
 constexpr float OUT_SCALE = 0.0883883476483184405501f;  // 1 / sqrt(128)
 constexpr uint64_t WAIT_NS = 1000000000ull;  // an mbarrier wait gives up after one second
 
-// mbarriers: state slots full/empty, scan-input buffers full/empty, raw-row stages
-// full, and the prologue warps' own rendezvous (after it no prologue warp reads the
-// unit's stage again)
-enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, B_PRO = 10, NBARS = 11 };
+// mbarriers: state slots full/empty, scan-input buffers full/empty, and raw-row stage
+// b of stream s full (B_STG_FULL + 4 b + s: each prologue warp stages its own stream)
+enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG_FULL = 8, NBARS = 16 };
 
 // Rows a unit runs: KEEP_NONE all T_run; ROWS_* a verify with per-session row counts
-// (host values in keep_host, or rows_dev); KEEP_* a rollback to per-session keep.
-enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2, ROWS_HOST = 3, ROWS_DEVICE = 4 };
+// (host values in keep_host, or rows_dev); KEEP_* a rollback to per-session keep;
+// DEFERRED a verify of T_run rows that first replays the previous round's kept rows
+// (keep_dev holds the previous round's keep, T_prev its row count).
+enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2, ROWS_HOST = 3, ROWS_DEVICE = 4, DEFERRED = 5 };
 
 struct ScanParams {
     CUtensorMap tm_in;     // state read: [units * 128 rows][128] f32, box 32 x 128, 128B swizzle
+    CUtensorMap tm_in2;    // DEFERRED: the state read of units with nothing to replay
     CUtensorMap tm_snap;   // snapshot write, same geometry (unused without s_snap)
     CUtensorMap tm_rows[4];  // raw rows q, k, v, g: [L*B][T_rows][H][128], box 128 x 1 x T_rows x 1
+    CUtensorMap tm_prev[4];  // DEFERRED: the previous round's raw rows, box 128 x 1 x T_prev x 1
     float *s_out;          // [L][B][H][D][D]
     float *s_snap;         // nullable: receives the state read through tm_in
     const float *ring_in;  // [L][B][H][3][3][D]
@@ -111,6 +116,10 @@ struct ScanParams {
     const float *conv_w;   // [L][H][3][D][4]
     const void *xq, *xk, *xv, *xg, *xb;  // [L][B][T_rows][H][D], xb [L][B][T_rows][H]
     float *out;            // nullable: [L][B][T_rows][H][D]
+    float *s_snap_out;     // DEFERRED: receives the state after the replay (this round's snapshot)
+    const float *ring_in2; // DEFERRED: the ring of units with nothing to replay
+    float *ring_snap_out;  // DEFERRED: receives the ring after the replay
+    const void *xb_prev;   // DEFERRED: the previous round's raw beta [L][B][T_prev][H]
     float *s_cols;         // nullable: [L][B][H][T_rows][D][D], the state after each row
     float *ring_cols;      // with s_cols: [L][B][H][T_rows][3][3][D], the ring after each row
     const int *keep_dev;   // KEEP_DEVICE: [B]
@@ -118,7 +127,8 @@ struct ScanParams {
     int *status;           // nullable device status word
     int L, B, H;
     int T_rows;            // row count of the raw-row tensors
-    int T_run;             // rows to run for KEEP_NONE
+    int T_run;             // rows to run for KEEP_NONE and DEFERRED
+    int T_prev;            // DEFERRED: row count of the previous round's raw-row tensors
     int tcap;              // most rows any unit runs (sizes the buffers)
     int nstg;              // raw-row stages: 2 where shared memory allows, else 1
     int bf16;
@@ -128,7 +138,7 @@ struct ScanParams {
 
 // Shared memory, from a 1024-byte aligned base (the 128-byte swizzle repeats
 // every 1024 bytes): two 64 KiB state slots, two scan-input buffers of tcap rows,
-// their {beta, k.q} scalars, nstg raw-row stages [4 streams][tcap][128], the
+// their beta scalars, nstg raw-row stages [4 streams][tcap][128], the
 // mbarriers and the abort flag.
 struct Layout {
     int tcap, es, nstg;
@@ -156,15 +166,6 @@ __device__ __forceinline__ float load_scalar(const void *base, int bf16, size_t 
     if (bf16)
         return __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t *>(base)[idx]) << 16);
     return static_cast<const float *>(base)[idx];
-}
-
-// butterfly all-reduce over the warp; every lane ends with the same bits
-__device__ __forceinline__ float warp_allsum(float x)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
-    return x;
 }
 
 __device__ __forceinline__ float conv4(float4 w, float x0, float x1, float x2, float x3)
@@ -298,6 +299,7 @@ __device__ bool drain_wait(uint32_t a, uint32_t parity)
 // ---- units --------------------------------------------------------------------------
 struct Unit {
     int h, b, l, T;
+    int R;         // DEFERRED: the previous round's rows to replay first (0: none)
     long long lb;  // l * B + b
 };
 
@@ -320,8 +322,22 @@ __device__ __forceinline__ int unit_rows(const ScanParams &p, int b)
     }
     if (p.keep_mode == ROWS_HOST)
         return p.keep_host[b];  // validated 1..T_rows on the host
+    if (p.keep_mode == DEFERRED) {
+        const int kp = p.keep_dev[b];
+        return kp < 1 || kp > p.T_prev ? -1 : p.T_run;
+    }
     const int tb = p.rows_dev[b];  // ROWS_DEVICE
     return tb < 1 || tb > p.T_rows ? -1 : tb;
+}
+
+// DEFERRED: the previous round's rows session b replays before its verify (0 when it
+// kept them all); 0 in every other mode.
+__device__ __forceinline__ int replay_rows(const ScanParams &p, int b)
+{
+    if (p.keep_mode != DEFERRED)
+        return 0;
+    const int kp = p.keep_dev[b];
+    return kp < p.T_prev ? kp : 0;
 }
 
 __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
@@ -332,7 +348,21 @@ __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
     x.b = static_cast<int>(x.lb % p.B);
     x.l = static_cast<int>(x.lb / p.B);
     x.T = unit_rows(p, x.b);
+    x.R = replay_rows(p, x.b);
     return x;
+}
+
+// A unit's work items: part 0 the replay of the previous round's kept rows (DEFERRED
+// units with rows to replay), part 1 this call's rows.  Items pass through the
+// raw-row stages and scan-input buffers in order; a unit's state stays in the scan
+// warps' registers from its first item to its last.
+struct Item {
+    int u, part;
+};
+
+__device__ __forceinline__ Item first_item(const ScanParams &p, int u, int n)
+{
+    return Item{u, u < n && replay_rows(p, (u / p.H) % p.B) > 0 ? 0 : 1};
 }
 
 // The first unit at or after u (stepping by the grid) that has rows to run.  Every
@@ -349,57 +379,72 @@ __device__ int next_live(const ScanParams &p, int u, int n, bool report)
     return n;
 }
 
-// ---- copies issued by scan warp 0 (states) and prologue warp g (raw rows) -----------
-// Unit u's 64 KiB state into a slot: four boxes of 32 columns x 128 rows (lane 0).
+__device__ __forceinline__ Item next_item(const ScanParams &p, Item it, int n)
+{
+    if (it.part == 0)
+        return Item{it.u, 1};
+    return first_item(p, next_live(p, it.u + gridDim.x, n, false), n);
+}
+
+// ---- copies issued by scan warp 0 (states) and the prologue warps (raw rows) ----------
+// Unit u's 64 KiB state into a slot: four boxes of 32 columns x 128 rows (lane 0).  A
+// DEFERRED unit with nothing to replay starts from the other buffer (tm_in2).
 __device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, uint32_t bar, int u)
 {
+    const CUtensorMap *tm =
+        p.keep_mode == DEFERRED && replay_rows(p, (u / p.H) % p.B) == 0 ? &p.tm_in2 : &p.tm_in;
     mbar_expect_tx(bar, D * D * 4);
 #pragma unroll
     for (int b = 0; b < 4; ++b)
-        tma_load_2d(slot + b * 16384, &p.tm_in, 32 * b, u * D, bar);
+        tma_load_2d(slot + b * 16384, tm, 32 * b, u * D, bar);
 }
 
-// Unit u's raw rows of stream s (0 q, 1 k, 2 v, 3 g) into the stage: one tensor copy
-// of the T_rows rows of its head (a unit that runs fewer rows gets all T_rows; the
-// rest are not read).  Lane 0 arms the barrier with the byte count; each prologue
-// warp stages its own stream, so the barrier counts four arrivals.
-__device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, int u, int s,
+// An item's raw rows of stream s (0 q, 1 k, 2 v, 3 g) into the stage: one tensor copy
+// of all rows of its head in the round it belongs to (a unit that runs fewer rows
+// gets them all; the rest are not read).  Lane 0 arms the barrier with the byte
+// count; each prologue warp stages its own stream, with a barrier per stream and stage.
+__device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, Item it, int s,
                              int lane)
 {
-    const Unit x = unit_of(p, u);
+    const int h = it.u % p.H, lb = it.u / p.H;
     const uint32_t rb = static_cast<uint32_t>(lay.row_bytes());
     fence_proxy_async();  // the prologue's generic reads of the stage come first
     if (lane == 0) {
-        mbar_expect_tx(bar, static_cast<uint32_t>(p.T_rows) * rb);
-        tma_load_4d(stg + s * lay.tcap * rb, &p.tm_rows[s], 0, x.h, 0, static_cast<int>(x.lb), bar);
+        mbar_expect_tx(bar, static_cast<uint32_t>(it.part == 0 ? p.T_prev : p.T_rows) * rb);
+        tma_load_4d(stg + s * lay.tcap * rb, it.part == 0 ? &p.tm_prev[s] : &p.tm_rows[s], 0, h, 0, lb, bar);
     }
 }
 
 // ---- prologue warps -----------------------------------------------------------------
-// What a prologue lane loads for a unit before it needs it: for q, k, v the conv
-// weights and ring slots of its 4 channels, for g the raw beta of row `lane`.
+// What a prologue lane loads for an item before it needs it: for q, k, v the conv
+// weights of its 4 channels and, for a unit's first item, their ring slots; for g the
+// raw beta of row `lane` of the item's round.
 struct Pre {
     float4 w[4];     // w[m]: the 4 taps of channel 4 lane + m
     float4 ring[3];  // ring slot 0 (oldest) .. 2 of channels 4 lane .. +3
     float beta;
 };
 
-__device__ __forceinline__ void load_pre(const ScanParams &p, int u, int pw, int lane, Pre &pr)
+__device__ __forceinline__ void load_pre(const ScanParams &p, Item it, int pw, int lane, Pre &pr)
 {
-    const Unit x = unit_of(p, u);
+    const Unit x = unit_of(p, it.u);
     if (pw < 3) {
         const float4 *w = reinterpret_cast<const float4 *>(p.conv_w) +
                           ((static_cast<size_t>(x.l) * p.H + x.h) * 3 + pw) * D + 4 * lane;
 #pragma unroll
         for (int m = 0; m < 4; ++m)
             pr.w[m] = w[m];
-        const float4 *r = reinterpret_cast<const float4 *>(p.ring_in + (static_cast<size_t>(u) * 3 + pw) * 3 * D) + lane;
+        if (it.part == 0 || x.R == 0) {  // a verify item after a replay continues its window
+            const float *src = p.keep_mode == DEFERRED && it.part == 1 ? p.ring_in2 : p.ring_in;
+            const float4 *r = reinterpret_cast<const float4 *>(src + (static_cast<size_t>(it.u) * 3 + pw) * 3 * D) + lane;
 #pragma unroll
-        for (int sl = 0; sl < 3; ++sl)
-            pr.ring[sl] = r[sl * (D / 4)];
+            for (int sl = 0; sl < 3; ++sl)
+                pr.ring[sl] = r[sl * (D / 4)];
+        }
     } else {
-        pr.beta = lane < x.T ? load_scalar(p.xb, p.bf16, (static_cast<size_t>(x.lb) * p.T_rows + lane) * p.H + x.h)
-                             : 0.f;
+        const int T = it.part == 0 ? x.R : x.T, trows = it.part == 0 ? p.T_prev : p.T_rows;
+        const void *xb = it.part == 0 ? p.xb_prev : p.xb;
+        pr.beta = lane < T ? load_scalar(xb, p.bf16, (static_cast<size_t>(x.lb) * trows + lane) * p.H + x.h) : 0.f;
     }
 }
 
@@ -427,24 +472,25 @@ __device__ __forceinline__ void store_perm(float *row, int block, int lane, floa
     g[3 * GRP] = v.w;
 }
 
-// Stream pw (0 q, 1 k, 2 v) of one unit: the conv window slides along the rows in
+// Stream pw (0 q, 1 k, 2 v) of one item: the conv window slides along the rows in
 // registers, four rows at a time with no branch around the arithmetic (rows past T
 // repeat row T-1 and are not stored), so the four rows' dependency chains overlap.
-// Writes the scan inputs (q-hat, k-hat or v), the ring after the round and, when
+// win holds the window (the last 3 raw inputs) before the item and after it.  Writes
+// the scan inputs (q-hat, k-hat or v), the ring after the item to ring_dst and, when
 // snapshotting, the ring before it.
 template <bool COLS>
 __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsigned char *stg, float *si,
-                            const Pre &pr, int u, int T, int pw, int lane)
+                            const float4 (&wt)[4], float4 (&win)[3], int u, int T, int pw, int lane, float *ring_dst)
 {
     const size_t rbase = (static_cast<size_t>(u) * 3 + pw) * 3 * D;
     if (p.ring_snap) {
         float4 *rs = reinterpret_cast<float4 *>(p.ring_snap + rbase) + lane;
-        rs[0] = pr.ring[0];
-        rs[D / 4] = pr.ring[1];
-        rs[2 * D / 4] = pr.ring[2];
+        rs[0] = win[0];
+        rs[D / 4] = win[1];
+        rs[2 * D / 4] = win[2];
     }
     // the window before row t0: x[t0-3], x[t0-2], x[t0-1] of the sequence [ring, rows]
-    float4 x0 = pr.ring[0], x1 = pr.ring[1], x2 = pr.ring[2];
+    float4 x0 = win[0], x1 = win[1], x2 = win[2];
     const int block = pw == 0 ? 32 : 16;
     for (int t0 = 0; t0 < T; t0 += 4) {
         float4 W[7];  // the sequence from x[t0-3]: W[j .. j+3] is row t0+j's window
@@ -459,10 +505,10 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             // w.x multiplies x[t-3], w.w the current row
-            y[j].x = silu(conv4(pr.w[0], W[j].x, W[j + 1].x, W[j + 2].x, W[j + 3].x));
-            y[j].y = silu(conv4(pr.w[1], W[j].y, W[j + 1].y, W[j + 2].y, W[j + 3].y));
-            y[j].z = silu(conv4(pr.w[2], W[j].z, W[j + 1].z, W[j + 2].z, W[j + 3].z));
-            y[j].w = silu(conv4(pr.w[3], W[j].w, W[j + 1].w, W[j + 2].w, W[j + 3].w));
+            y[j].x = silu(conv4(wt[0], W[j].x, W[j + 1].x, W[j + 2].x, W[j + 3].x));
+            y[j].y = silu(conv4(wt[1], W[j].y, W[j + 1].y, W[j + 2].y, W[j + 3].y));
+            y[j].z = silu(conv4(wt[2], W[j].z, W[j + 1].z, W[j + 2].z, W[j + 3].z));
+            y[j].w = silu(conv4(wt[3], W[j].w, W[j + 1].w, W[j + 2].w, W[j + 3].w));
             ss[j] = __fmaf_rn(y[j].w, y[j].w, __fmaf_rn(y[j].z, y[j].z, __fmaf_rn(y[j].y, y[j].y, __fmul_rn(y[j].x, y[j].x))));
         }
         if (COLS) {  // the ring after row t0 + j: W[j+1 .. j+3]
@@ -502,14 +548,17 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
         x1 = W[5];
         x2 = W[6];
     }
-    // the ring after the round: x[T-3], x[T-2], x[T-1] of the sequence [ring, rows]
-    const float4 r0 = T >= 3 ? stage4(stg, lay, pw, T - 3, lane) : T == 2 ? pr.ring[2] : pr.ring[1];
-    const float4 r1 = T >= 2 ? stage4(stg, lay, pw, T - 2, lane) : pr.ring[2];
+    // the ring after the item: x[T-3], x[T-2], x[T-1] of the sequence [window, rows]
+    const float4 r0 = T >= 3 ? stage4(stg, lay, pw, T - 3, lane) : T == 2 ? win[2] : win[1];
+    const float4 r1 = T >= 2 ? stage4(stg, lay, pw, T - 2, lane) : win[2];
     const float4 r2 = stage4(stg, lay, pw, T - 1, lane);
-    float4 *ro = reinterpret_cast<float4 *>(p.ring_out + rbase) + lane;
+    float4 *ro = reinterpret_cast<float4 *>(ring_dst + rbase) + lane;
     ro[0] = r0;
     ro[D / 4] = r1;
     ro[2 * D / 4] = r2;
+    win[0] = r0;
+    win[1] = r1;
+    win[2] = r2;
 }
 
 // Stream 3: the forget gate d = exp(-5 sigmoid(raw_g)) per key channel and beta, four
@@ -533,14 +582,14 @@ __device__ void gate_stream(const Layout &lay, const unsigned char *stg, float *
                 store_perm(si + (t0 + j) * SI_ROW, 0, lane, dg[j]);
     }
     if (lane < T)
-        sc[2 * lane] = sigmoidf_(pr.beta);
+        sc[lane] = sigmoidf_(pr.beta);
 }
 
-// Each prologue warp also stages its stream's raw rows: unit k's go to stage
-// k % nstg, issued once every prologue warp is done with the stage's previous unit
-// (the B_PRO rendezvous), nstg units ahead.
+// Each prologue warp also stages its stream's raw rows: item i's go to stage
+// i % nstg, issued as soon as the warp is done with the stage's previous item, nstg
+// items ahead.  The four prologue warps meet only at the scan-input buffers.
 struct Stager {
-    int next;             // the unit staged next
+    Item next;            // the item staged next
     bool pend0, pend1;    // a copy in flight into stage 0 / 1, for the drain on abort
     uint32_t par0, par1;  // and the phase parity that completes it
 };
@@ -552,77 +601,66 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
     const uint32_t stg0 = smem_addr(sm + lay.stg(0));
     const uint32_t stage_bytes = static_cast<uint32_t>(lay.stg(1) - lay.stg(0));
     Pre pr;
-    int u = next_live(p, blockIdx.x, n, false);
-    Stager sg{n, false, false, 0, 0};
-    {
-        // the first nstg units' raw rows
-        int v = u;
-        for (int b = 0; b < lay.nstg && v < n; ++b) {
-            issue_stream(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + b), v, pw, lane);
-            (b ? sg.pend1 : sg.pend0) = true;
-            v = next_live(p, v + gridDim.x, n, false);
-        }
-        sg.next = v;
+    float4 win[3];  // the conv window carried from a unit's replay item into its verify item
+    Item it = first_item(p, next_live(p, blockIdx.x, n, false), n);
+    Stager sg{it, false, false, 0, 0};
+    for (int b = 0; b < lay.nstg && sg.next.u < n; ++b) {  // the first nstg items' raw rows
+        issue_stream(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + 4 * b + pw), sg.next, pw, lane);
+        (b ? sg.pend1 : sg.pend0) = true;
+        sg.next = next_item(p, sg.next, n);
     }
     bool ok = true;
-    if (u < n)
-        load_pre(p, u, pw, lane, pr);
-    for (int k = 0; u < n; ++k) {
-        const int b = k & 1;
-        const int T = unit_of(p, u).T;
-        const int sb = lay.nstg == 2 ? b : 0, m = lay.nstg == 2 ? k >> 1 : k;
+    if (it.u < n)
+        load_pre(p, it, pw, lane, pr);
+    for (int i = 0; it.u < n; ++i) {
+        const int b = i & 1;
+        const Unit x = unit_of(p, it.u);
+        const int T = it.part == 0 ? x.R : x.T;
+        const int sb = lay.nstg == 2 ? b : 0, m = lay.nstg == 2 ? i >> 1 : i;
         const unsigned char *stg = sm + lay.stg(sb);
-        if (!warp_wait(c, B_STG_FULL + sb, m & 1)) {
+        if (!warp_wait(c, B_STG_FULL + 4 * sb + pw, m & 1)) {
             ok = false;
             break;
         }
         (sb ? sg.pend1 : sg.pend0) = false;
-        // the scan of unit k-2 has released this scan-input buffer
-        if (k >= 2 && !warp_wait(c, B_SI_EMPTY + b, ((k >> 1) - 1) & 1)) {
+        // the scan of item i-2 has released this scan-input buffer
+        if (i >= 2 && !warp_wait(c, B_SI_EMPTY + b, ((i >> 1) - 1) & 1)) {
             ok = false;
             break;
         }
         float *si = reinterpret_cast<float *>(sm + lay.si(b));
         float *sc = reinterpret_cast<float *>(sm + lay.sc(b));
-        if (pw < 3)
-            conv_stream<COLS>(p, lay, stg, si, pr, u, T, pw, lane);
-        else
+        if (pw < 3) {
+            if (it.part == 0 || x.R == 0) {  // a unit's first item starts from its ring
+                win[0] = pr.ring[0];
+                win[1] = pr.ring[1];
+                win[2] = pr.ring[2];
+            }
+            // a replay ends in the committed ring (this round's ring snapshot)
+            conv_stream<COLS>(p, lay, stg, si, pr.w, win, it.u, T, pw, lane,
+                              it.part == 0 ? p.ring_snap_out : p.ring_out);
+        } else {
             gate_stream(lay, stg, si, sc, pr, T, lane);
-        // the next unit's conv weights, ring and beta: the loads are in flight during
-        // the rendezvous and k.q below
-        const int un = next_live(p, u + gridDim.x, n, false);
-        if (un < n)
-            load_pre(p, un, pw, lane, pr);
-        // k.q of each row once q-hat and k-hat are all written; past this rendezvous no
-        // prologue warp reads the stage of unit k again
-        mbar_arrive(c.bar(B_PRO));
-        if (!warp_wait(c, B_PRO, k & 1)) {
-            ok = false;
-            break;
-        }
-        if (sg.next < n) {
-            issue_stream(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + sb), sg.next, pw, lane);
-            (sb ? sg.pend1 : sg.pend0) = true;
-            (sb ? sg.par1 : sg.par0) = (m + 1) & 1;
-            sg.next = next_live(p, sg.next + gridDim.x, n, false);
-        }
-        for (int t = pw; t < T; t += NPRO) {
-            const float *g = si + t * SI_ROW + (lane >> 2) * GRP + 4 * (lane & 3);
-            const float4 kk = *reinterpret_cast<const float4 *>(g + 16);
-            const float4 qq = *reinterpret_cast<const float4 *>(g + 32);
-            float s = __fmaf_rn(kk.w, qq.w, __fmaf_rn(kk.z, qq.z, __fmaf_rn(kk.y, qq.y, __fmul_rn(kk.x, qq.x))));
-            s = warp_allsum(s);
-            if (lane == 0)
-                sc[2 * t + 1] = s;
         }
         mbar_arrive(c.bar(B_SI_FULL + b));
-        u = un;
+        // the next item's conv weights, ring and beta, and the raw rows of item i + nstg
+        // into the stage this warp is done with
+        const Item nx = next_item(p, it, n);
+        if (nx.u < n)
+            load_pre(p, nx, pw, lane, pr);
+        if (sg.next.u < n) {
+            issue_stream(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + 4 * sb + pw), sg.next, pw, lane);
+            (sb ? sg.pend1 : sg.pend0) = true;
+            (sb ? sg.par1 : sg.par0) = (m + 1) & 1;
+            sg.next = next_item(p, sg.next, n);
+        }
+        it = nx;
     }
     if (!ok && lane == 0) {  // stage copies in flight must land before the CTA leaves
         if (sg.pend0)
-            drain_wait(c.bar(B_STG_FULL), sg.par0);
+            drain_wait(c.bar(B_STG_FULL + pw), sg.par0);
         if (sg.pend1)
-            drain_wait(c.bar(B_STG_FULL + 1), sg.par1);
+            drain_wait(c.bar(B_STG_FULL + 4 + pw), sg.par1);
     }
 }
 
@@ -676,9 +714,10 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
         pend1 = u1 < n;
     }
     bool ok = true;
+    int i = 0;  // items through the scan-input buffers so far
     for (int k = 0; u < n; ++k) {
         const Unit x = unit_of(p, u);
-        const int T = x.T, s = k & 1;
+        const int s = k & 1;
         const uint32_t ph = (k >> 1) & 1;
         if (!warp_wait(c, B_STATE_FULL + s, ph)) {
             ok = false;
@@ -704,86 +743,104 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             }
         }
         mbar_arrive(c.bar(B_STATE_EMPTY + s));
-        if (!warp_wait(c, B_SI_FULL + s, ph)) {
-            ok = false;
-            break;
-        }
-        const float *si = reinterpret_cast<const float *>(sm + lay.si(s));
-        const float *sc = reinterpret_cast<const float *>(sm + lay.sc(s));
-        // the output row t of this unit: lanes with b2 = 1 store column jsum
-        float *orow = p.out ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum : nullptr;
+        // part 0: the replay of the previous round's kept rows (no outputs), after which
+        // the state is this round's snapshot; part 1: this call's rows
+        for (int part = x.R > 0 ? 0 : 1; part < 2; ++part, ++i) {
+            const int T = part == 0 ? x.R : x.T;
+            const int ib = i & 1;
+            if (!warp_wait(c, B_SI_FULL + ib, (i >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const float *si = reinterpret_cast<const float *>(sm + lay.si(ib));
+            const float *sc = reinterpret_cast<const float *>(sm + lay.sc(ib));
+            // the output row t of this unit: lanes with b2 = 1 store column jsum
+            float *orow = p.out && part == 1
+                              ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum
+                              : nullptr;
 
-        // ---- the T-row gated delta rule ---------------------------------------------
-        for (int t = 0; t < T; ++t) {
-            const float *vt = si + t * SI_ROW;
-            const float *gp = vt + rg * GRP;
-            float2 uacc[2], eacc[2];
-            float kv[16];
-            uacc[0] = uacc[1] = eacc[0] = eacc[1] = make_float2(0.f, 0.f);
-            // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows, in order)
+            // ---- the T-row gated delta rule ---------------------------------------------
+            for (int t = 0; t < T; ++t) {
+                const float *vt = si + t * SI_ROW;
+                const float *gp = vt + rg * GRP;
+                float2 uacc[2], eacc[2];
+                float kv[16];
+                float kq = 0.f;  // k.q over this thread's 16 rows, in order
+                uacc[0] = uacc[1] = eacc[0] = eacc[1] = make_float2(0.f, 0.f);
+                // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows, in order)
 #pragma unroll
-            for (int rq = 0; rq < 4; ++rq) {
-                const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
-                const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
-                const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
-                const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
-                kv[4 * rq] = k4.x;
-                kv[4 * rq + 1] = k4.y;
-                kv[4 * rq + 2] = k4.z;
-                kv[4 * rq + 3] = k4.w;
+                for (int rq = 0; rq < 4; ++rq) {
+                    const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
+                    const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
+                    const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
+                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+                    kv[4 * rq] = k4.x;
+                    kv[4 * rq + 1] = k4.y;
+                    kv[4 * rq + 2] = k4.z;
+                    kv[4 * rq + 3] = k4.w;
+                    kq = __fmaf_rn(k4.w, q4.w, __fmaf_rn(k4.z, q4.z, __fmaf_rn(k4.y, q4.y, __fmaf_rn(k4.x, q4.x, kq))));
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const int r = 4 * rq + m;
-                    const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[r], kv[r]);
-                    const float2 qq = make_float2(qv[m], qv[m]);
+                    for (int m = 0; m < 4; ++m) {
+                        const int r = 4 * rq + m;
+                        const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[r], kv[r]);
+                        const float2 qq = make_float2(qv[m], qv[m]);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        S[r][h] = __fmul2_rn(S[r][h], dd);
-                        uacc[h] = __ffma2_rn(S[r][h], kk, uacc[h]);
-                        eacc[h] = __ffma2_rn(S[r][h], qq, eacc[h]);
+                        for (int h = 0; h < 2; ++h) {
+                            S[r][h] = __fmul2_rn(S[r][h], dd);
+                            uacc[h] = __ffma2_rn(S[r][h], kk, uacc[h]);
+                            eacc[h] = __ffma2_rn(S[r][h], qq, eacc[h]);
+                        }
                     }
                 }
-            }
-            // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
-            // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
-            const float v8[8] = {uacc[0].x, uacc[0].y, uacc[1].x, uacc[1].y, eacc[0].x, eacc[0].y, eacc[1].x, eacc[1].y};
-            float v4[4], v2[2];
+                // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
+                // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
+                const float v8[8] = {uacc[0].x, uacc[0].y, uacc[1].x, uacc[1].y, eacc[0].x, eacc[0].y, eacc[1].x, eacc[1].y};
+                float v4[4], v2[2];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float keep = b2 ? v8[4 + m] : v8[m], send = b2 ? v8[m] : v8[4 + m];
-                v4[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-            }
+                for (int m = 0; m < 4; ++m) {
+                    const float keep = b2 ? v8[4 + m] : v8[m], send = b2 ? v8[m] : v8[4 + m];
+                    v4[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+                }
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const float keep = b1 ? v4[2 + m] : v4[m], send = b1 ? v4[m] : v4[2 + m];
-                v2[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-            }
-            const float keep1 = b0 ? v2[1] : v2[0], send1 = b0 ? v2[0] : v2[1];
-            const float sum = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
-            // u lanes: w = beta (v - u); e lanes: o = (e + w (k.q)) / sqrt(128)
-            const float2 bk = *reinterpret_cast<const float2 *>(sc + 2 * t);  // {beta, k.q}
-            const float w = __fmul_rn(bk.x, __fsub_rn(vt[SI_V + jsum], sum));
-            const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
-            // a warp's 16 e lanes store 16 consecutive columns of the output row
-            if (orow && b2)
-                orow[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, bk.y, sum), OUT_SCALE);
-            // every lane gathers w of its 4 columns from the u lanes 4 c + cg
-            float wv[4];
+                for (int m = 0; m < 2; ++m) {
+                    const float keep = b1 ? v4[2 + m] : v4[m], send = b1 ? v4[m] : v4[2 + m];
+                    v2[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+                }
+                const float keep1 = b0 ? v2[1] : v2[0], send1 = b0 ? v2[0] : v2[1];
+                const float sum = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
+                // k.q over the 8 row groups: a butterfly, so every lane holds the same bits
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                wv[c4] = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
-            const float2 w01 = make_float2(wv[0], wv[1]), w23 = make_float2(wv[2], wv[3]);
-            // S = S' + k w^T
+                for (int off = 4; off < 32; off <<= 1)
+                    kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
+                // u lanes: w = beta (v - u); e lanes: o = (e + w (k.q)) / sqrt(128)
+                const float beta = sc[t];
+                const float w = __fmul_rn(beta, __fsub_rn(vt[SI_V + jsum], sum));
+                const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
+                // a warp's 16 e lanes store 16 consecutive columns of the output row
+                if (orow && b2)
+                    orow[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, kq, sum), OUT_SCALE);
+                // every lane gathers w of its 4 columns from the u lanes 4 c + cg
+                float wv[4];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const float2 kk = make_float2(kv[r], kv[r]);
-                S[r][0] = __ffma2_rn(kk, w01, S[r][0]);
-                S[r][1] = __ffma2_rn(kk, w23, S[r][1]);
+                for (int c4 = 0; c4 < 4; ++c4)
+                    wv[c4] = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
+                const float2 w01 = make_float2(wv[0], wv[1]), w23 = make_float2(wv[2], wv[3]);
+                // S = S' + k w^T
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float2 kk = make_float2(kv[r], kv[r]);
+                    S[r][0] = __ffma2_rn(kk, w01, S[r][0]);
+                    S[r][1] = __ffma2_rn(kk, w23, S[r][1]);
+                }
+                if (COLS)  // the column stash: the state after row t
+                    store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
             }
-            if (COLS)  // the column stash: the state after row t
-                store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
+            mbar_arrive(c.bar(B_SI_EMPTY + ib));  // the scan inputs of item i are consumed
+            if (part == 0)  // the committed state: this round's snapshot
+                store_tile(p.s_snap_out + static_cast<size_t>(u) * D * D + jbase, rg, S);
         }
-        mbar_arrive(c.bar(B_SI_EMPTY + s));  // the scan inputs of unit k are consumed
+        if (!ok)
+            break;
 
         // lead: every scan warp holds unit k in registers and the snapshot store has
         // read the slot: load unit k+2 into it
@@ -837,9 +894,8 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
             mbar_init(c.bar(B_SI_FULL + s), NPRO * 32);
             mbar_init(c.bar(B_SI_EMPTY + s), NSCAN * 32);
         }
-        for (int b = 0; b < 2; ++b)
-            mbar_init(c.bar(B_STG_FULL + b), NPRO);  // one armed arrival per prologue warp
-        mbar_init(c.bar(B_PRO), NPRO * 32);
+        for (int b = 0; b < 8; ++b)
+            mbar_init(c.bar(B_STG_FULL + b), 1);
         *c.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -963,7 +1019,10 @@ struct DeviceInfo {
     int smem_max = 0;  // opt-in shared memory per block, set as the kernels' limit
 };
 
-int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
+// s_in: the state tm_in reads; for DEFERRED also s_in2 (tm_in2) and the previous
+// round's raw rows.
+int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const float *s_in2 = nullptr,
+                const kda_rows *prev = nullptr)
 {
     const long long units = static_cast<long long>(p.L) * p.B * p.H;
     if (units == 0)
@@ -1012,12 +1071,23 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream)
         return rc;
     if (p.s_snap && (rc = state_map(&p.tm_snap, p.s_snap, units)))
         return rc;
-    if (p.tcap != p.T_rows)
-        return fail(KDA_EINVAL, "internal: the raw-row stage must hold T_rows rows");
+    if (p.tcap < p.T_rows || (p.keep_mode == DEFERRED && p.tcap < p.T_prev))
+        return fail(KDA_EINVAL, "internal: the raw-row stage must hold every round's rows");
+    const long long LB = static_cast<long long>(p.L) * p.B;
     const void *raw[4] = {p.xq, p.xk, p.xv, p.xg};
     for (int s = 0; s < 4; ++s)
-        if ((rc = rows_map(&p.tm_rows[s], raw[s], p.bf16 != 0, static_cast<long long>(p.L) * p.B, p.T_rows, p.H)))
+        if ((rc = rows_map(&p.tm_rows[s], raw[s], p.bf16 != 0, LB, p.T_rows, p.H)))
             return rc;
+    if (p.keep_mode == DEFERRED) {
+        if (!s_in2 || !prev)
+            return fail(KDA_EINVAL, "internal: a deferred round needs both state buffers and the previous rows");
+        if ((rc = state_map(&p.tm_in2, s_in2, units)))
+            return rc;
+        const void *praw[4] = {prev->q, prev->k, prev->v, prev->g};
+        for (int s = 0; s < 4; ++s)
+            if ((rc = rows_map(&p.tm_prev[s], praw[s], p.bf16 != 0, LB, p.T_prev, p.H)))
+                return rc;
+    }
     const long long grid = std::min<long long>(units, di.sms);
     const unsigned g = static_cast<unsigned>(grid);
     const size_t sb = lay.total();
@@ -1168,6 +1238,66 @@ extern "C" int kda_verify_scan_pingpong(const kda_dims *dims, const kda_layer_st
                                         int *dev_status, cudaStream_t stream)
 {
     return verify_common(dims, st, rows, T, t_rows, t_mem, out, stash, dev_status, true, stream);
+}
+
+extern "C" int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
+                                        const int *prev_keep, const kda_rows *rows, int T, float *out,
+                                        int *dev_status, cudaStream_t stream)
+{
+    int rc = check_common(dims, st);
+    if (rc)
+        return rc;
+    if (!stash)
+        return fail(KDA_EINVAL, "kda_verify_scan_deferred needs the stash of the previous ping-pong round");
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15 (K <= 14 drafts per round), got " + std::to_string(T));
+    if (stash->T < 1 || stash->T > KDA_TMAX)
+        return fail(KDA_EINVAL, "stash->T is not a verify round's row count (run a ping-pong verify first)");
+    const bool empty = static_cast<long long>(dims->L) * dims->B * dims->H == 0;
+    if (!empty) {
+        if ((rc = check_rows(rows, dims->dtype)) || (rc = check_rows(&stash->rows, dims->dtype)))
+            return rc;
+        if (!stash->state_snap || !stash->ring_snap || !aligned16(stash->state_snap) || !aligned16(stash->ring_snap))
+            return fail(KDA_EINVAL, "stash snapshots must be non-NULL and 16-byte aligned");
+        if (stash->state_snap == st->state || stash->ring_snap == st->conv_ring)
+            return fail(KDA_EINVAL, "the two state buffers (and the two ring buffers) must be distinct");
+        if (!prev_keep || (reinterpret_cast<uintptr_t>(prev_keep) & 3u))
+            return fail(KDA_EINVAL, "prev_keep must be a 4-byte aligned device array of B ints");
+        if (out && (reinterpret_cast<uintptr_t>(out) & 3u))
+            return fail(KDA_EINVAL, "out must be 4-byte aligned");
+        ScanParams p{};
+        p.keep_mode = DEFERRED;
+        p.keep_dev = prev_keep;
+        p.T_prev = stash->T;
+        // P (the stash's buffers): the previous round's pre-round state, replayed from,
+        // then this round's post-round state; Q (st's buffers): the previous round's
+        // post-round state, then this round's snapshot
+        p.s_out = stash->state_snap;
+        p.s_snap_out = st->state;
+        p.ring_in = stash->ring_snap;
+        p.ring_in2 = st->conv_ring;
+        p.ring_out = stash->ring_snap;
+        p.ring_snap_out = st->conv_ring;
+        p.conv_w = st->conv_w;
+        p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
+        p.xb_prev = stash->rows.beta;
+        p.out = out;
+        p.status = dev_status;
+        p.L = dims->L; p.B = dims->B; p.H = dims->H;
+        p.T_rows = T;
+        p.T_run = T;
+        p.tcap = std::max(T, stash->T);
+        p.bf16 = dims->dtype == KDA_BF16;
+        if ((rc = launch_scan(p, stash->state_snap, stream, st->state, &stash->rows)))
+            return rc;
+    }
+    // the stash now describes this round (its snapshot is in Q) and st its post-round
+    // state (in P): the buffers exchange roles
+    std::swap(st->state, stash->state_snap);
+    std::swap(st->conv_ring, stash->ring_snap);
+    stash->rows = rows ? *rows : kda_rows{};
+    stash->T = T;
+    return ok();
 }
 
 namespace kda {

@@ -230,3 +230,28 @@ def test_pingpong_rejects_on_host(L):
     empty = kb.KdaDims(0, 2, 64, 128, 128, kb.BF16)
     assert L.kda_verify_scan_pingpong(ctypes.byref(empty), ctypes.byref(st), ctypes.byref(rows), 8, None,
                                       kb.MEM_HOST, None, ctypes.byref(good), None, None) == kb.OK
+
+
+def test_deferred_rejects_on_host(L):
+    dims, st, rows = _state(B=2)
+
+    def call(stash, keep=FAKE + 0x3000, T=8):
+        return L.kda_verify_scan_deferred(ctypes.byref(dims), ctypes.byref(st),
+                                          ctypes.byref(stash) if stash is not None else None, keep,
+                                          ctypes.byref(rows), T, None, None, None)
+    prev = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)
+    assert call(None) == kb.EINVAL
+    assert call(kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 0)) == kb.EINVAL
+    assert b"ping-pong" in L.kda_last_error()
+    assert call(prev, keep=None) == kb.EINVAL
+    assert call(prev, keep=FAKE + 2) == kb.EINVAL
+    assert call(prev, T=16) == kb.EINVAL
+    assert call(kb.KdaStashC(FAKE, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)) == kb.EINVAL
+    assert call(kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(), 8)) == kb.EINVAL  # no previous rows
+    # an empty problem only exchanges the buffers and records the round
+    empty = kb.KdaDims(0, 2, 64, 128, 128, kb.BF16)
+    st2 = kb.KdaLayerState(FAKE, FAKE + 0x100, FAKE + 0x200)
+    s2 = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(), 8)
+    assert L.kda_verify_scan_deferred(ctypes.byref(empty), ctypes.byref(st2), ctypes.byref(s2), None,
+                                      ctypes.byref(rows), 5, None, None, None) == kb.OK
+    assert st2.state == FAKE + 0x1000 and s2.state_snap == FAKE and s2.T == 5

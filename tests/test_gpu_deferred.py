@@ -1,0 +1,175 @@
+"""GPU: a round whose verify first applies the previous round's accept
+(kda_verify_scan_deferred) gives the same bits as the previous round's kda_rollback
+followed by a ping-pong verify, and matches the oracle.
+
+The rollback (glm_spec.rs, glm5_verify_rollback: restore the per-round snapshot and
+replay rows 0..keep-1) is the same replay; it runs inside the next round's launch, so
+the state crosses HBM once per round instead of twice for a session that rolls back.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_close, bits_equal, host, layer_state, rows_to_dev, small_case
+from libs import ensure_built
+
+from speculative_decode_verify_kda_gb300 import binding as kb
+from speculative_decode_verify_kda_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("q", "k", "v", "g", "beta")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    ensure_built()
+    kb.lib()
+
+
+def _rounds(L, B, H, Ts, bf16, seed):
+    """Raw rows of consecutive rounds with the given row counts (one workload per T)."""
+    out = []
+    for r, T in enumerate(Ts):
+        w = synth.Workload(f"d{T}", L=L, B=B, H=H, T=T, bf16=bf16, V=64, rounds=r + 1, seed=seed + 7 * T,
+                           accept="uniform")
+        out.append(synth.all_rows(w, r))
+    return out
+
+
+def _keeps(B, Ts, seed):
+    """Per round and session a keep in 1..T, with full keeps and keep = 1 among them."""
+    g = np.random.default_rng(seed)
+    ks = []
+    for T in Ts:
+        k = g.integers(1, T + 1, B)
+        k[0] = T          # a session that keeps every row: nothing to replay
+        k[-1] = 1         # the shortest replay
+        ks.append([int(x) for x in k])
+    return ks
+
+
+@pytest.mark.parametrize("bf16,Ts", [(True, [8, 8, 8, 8]), (True, [8, 5, 15, 1, 3]), (False, [6, 9, 2])])
+def test_deferred_rounds_equal_rollback_then_pingpong(bf16, Ts):
+    L, B, H = 2, 4, 6
+    w0 = synth.Workload("d", L=L, B=B, H=H, T=Ts[0], bf16=bf16, V=64, rounds=1, seed=0x9930, accept="uniform")
+    state0, ring0, cw = small_case(w0)
+    rounds = [rows_to_dev(r, bf16) for r in _rounds(L, B, H, Ts, bf16, 0x9931)]
+    keeps = _keeps(B, Ts, 0x9932)
+    a = kb.PingPong(layer_state(state0, ring0, cw))  # rollback, then ping-pong verify
+    b = kb.PingPong(layer_state(state0, ring0, cw))  # deferred rounds
+    for r, T in enumerate(Ts):
+        out_a = torch.full((L, B, T, H, 128), float("nan"), device="cuda")
+        out_b = torch.full_like(out_a, float("nan"))
+        x = [rounds[r][n] for n in NAMES]
+        if r > 0:
+            kb.kda_rollback_pingpong(a, keeps[r - 1])
+        kb.kda_verify_scan_pingpong(a, *x, out=out_a)
+        if r == 0:
+            kb.kda_verify_scan_pingpong(b, *x, out=out_b)
+        else:
+            kb.kda_verify_scan_deferred(b, *x, torch.tensor(keeps[r - 1], dtype=torch.int32, device="cuda"),
+                                        out=out_b)
+        torch.cuda.synchronize()
+        assert bits_equal(out_a, out_b), f"round {r}: outputs"
+        # this round's snapshot (the committed state) and post-round state, state and ring
+        for nm, ta, tb in (("snapshot", a.states[a.last], b.states[b.last]),
+                           ("post-round", a.state(), b.state()),
+                           ("ring snapshot", a.rings[a.last], b.rings[b.last]),
+                           ("post-round ring", a.ring(), b.ring())):
+            assert bits_equal(ta, tb), f"round {r}: {nm}"
+    # the last round commits with an ordinary rollback on both sides
+    kb.kda_rollback_pingpong(a, keeps[-1])
+    kb.kda_rollback_pingpong(b, keeps[-1])
+    torch.cuda.synchronize()
+    assert bits_equal(a.state(), b.state()) and bits_equal(a.ring(), b.ring())
+
+
+def test_deferred_matches_the_oracle(orc):
+    L, B, H, Ts = 1, 3, 2, [7, 5]
+    w0 = synth.Workload("do", L=L, B=B, H=H, T=7, bf16=True, V=64, rounds=1, seed=0x9933, accept="uniform")
+    state0, ring0, cw = small_case(w0)
+    rounds_np = _rounds(L, B, H, Ts, True, 0x9934)
+    keep0 = [7, 4, 1]
+    pp = kb.PingPong(layer_state(state0, ring0, cw))
+    x0 = [rows_to_dev(rounds_np[0], True)[n] for n in NAMES]
+    x1 = [rows_to_dev(rounds_np[1], True)[n] for n in NAMES]
+    out = torch.empty((L, B, 5, H, 128), dtype=torch.float32, device="cuda")
+    kb.kda_verify_scan_pingpong(pp, *x0)
+    kb.kda_verify_scan_deferred(pp, *x1, torch.tensor(keep0, dtype=torch.int32, device="cuda"), out=out)
+    torch.cuda.synchronize()
+    for b in range(B):
+        u0 = {n: rounds_np[0][n][0, b] for n in rounds_np[0]}
+        u1 = {n: rounds_np[1][n][0, b] for n in rounds_np[1]}
+        a0 = (u0["q"], u0["k"], u0["v"], u0["g"], u0["beta"], cw[0])
+        s_T, r_T, _ = orc.verify(*a0, ring0[0, b], state0[0, b])
+        s_c, r_c = orc.rollback(keep0[b], *a0, ring0[0, b], state0[0, b], r_T, s_T)
+        s1, r1, o1 = orc.verify(u1["q"], u1["k"], u1["v"], u1["g"], u1["beta"], cw[0], r_c, s_c)
+        assert_close(host(out[0, b]), o1, f"outputs of session {b}")
+        assert_close(host(pp.state()[0, b]), s1, f"post-round state of session {b}")
+        assert_close(host(pp.states[pp.last][0, b]), s_c, f"snapshot of session {b}")
+        assert np.array_equal(host(pp.ring()[0, b]), r1) and np.array_equal(host(pp.rings[pp.last][0, b]), r_c)
+
+
+def test_deferred_bad_keep_leaves_the_session_and_reports():
+    L, B, H, Ts = 1, 3, 4, [6, 6]
+    w0 = synth.Workload("db", L=L, B=B, H=H, T=6, bf16=True, V=64, rounds=1, seed=0x9935, accept="uniform")
+    state0, ring0, cw = small_case(w0)
+    rounds = [rows_to_dev(r, True) for r in _rounds(L, B, H, Ts, True, 0x9936)]
+    good = [6, 2, 3]
+    a = kb.PingPong(layer_state(state0, ring0, cw))
+    b = kb.PingPong(layer_state(state0, ring0, cw))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for pp in (a, b):
+        kb.kda_verify_scan_pingpong(pp, *[rounds[0][n] for n in NAMES])
+    kb.kda_rollback_pingpong(a, good)
+    kb.kda_verify_scan_pingpong(a, *[rounds[1][n] for n in NAMES])
+    bad = [6, 0, 3]  # session 1's keep is outside 1..6
+    kb.kda_verify_scan_deferred(b, *[rounds[1][n] for n in NAMES], torch.tensor(bad, dtype=torch.int32, device="cuda"),
+                                dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) & kb.ST_BADKEEP
+    for s in (0, 2):  # the other sessions are processed as usual
+        assert bits_equal(a.state()[:, s], b.state()[:, s]) and bits_equal(a.states[a.last][:, s], b.states[b.last][:, s])
+
+
+def test_deferred_plan_equals_the_functions():
+    L, B, H = 2, 3, 5
+    w = synth.Workload("dp", L=L, B=B, H=H, T=8, bf16=True, V=500, rounds=4, seed=0x9937, accept="uniform")
+    state0, ring0, cw = small_case(w)
+    from gpu_util import to_dev
+    rows = [rows_to_dev(synth.all_rows(w, r), True) for r in range(w.rounds)]
+    logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
+    drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
+              for r in range(w.rounds)]
+    j, bonus, keep = (torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(3))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(kb.spec_accept_scratch_bytes(B, w.T, w.V), dtype=torch.uint8, device="cuda")
+    out_a = torch.empty((L, B, w.T, H, 128), dtype=torch.float32, device="cuda")
+    out_b = torch.empty_like(out_a)
+    a = kb.PingPong(layer_state(state0, ring0, cw))
+    b = kb.PingPong(layer_state(state0, ring0, cw))
+    plans = [kb.DeferredRoundPlan(b, rows[r], out_b, logits[r], drafts[r], j, bonus, keep, status, scratch)
+             for r in range(w.rounds)]
+    first = kb.PingPongRoundPlan(b, rows[0], out_b, logits[0], drafts[0], j, bonus, keep, status, scratch)
+    # plan side: round 0 verify + accept (no rollback yet), then deferred rounds
+    first.verify(b.parity)
+    first.accept()
+    p0 = b.parity
+    first._flip(p0)
+    for r in range(w.rounds):
+        x = [rows[r][n] for n in NAMES]
+        if r > 0:
+            kb.kda_rollback_pingpong(a, [int(t) + 1 for t in synth.accept_targets(w, r - 1)])
+        kb.kda_verify_scan_pingpong(a, *x, out=out_a)
+        if r > 0:
+            plans[r]()
+        torch.cuda.synchronize()
+        assert [int(t) for t in j.cpu()] == list(synth.accept_targets(w, r))
+        assert bits_equal(out_a, out_b), f"round {r}: outputs"
+        assert bits_equal(a.state(), b.state()) and bits_equal(a.states[a.last], b.states[b.last]), f"round {r}"
+    assert int(status[0]) == 0
