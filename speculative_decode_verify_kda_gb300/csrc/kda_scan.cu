@@ -102,6 +102,15 @@ enum { B_STATE_FULL = 0, B_STATE_EMPTY = 2, B_SI_FULL = 4, B_SI_EMPTY = 6, B_STG
 // (keep_dev holds the previous round's keep, T_prev its row count).
 enum KeepMode { KEEP_NONE = 0, KEEP_HOST = 1, KEEP_DEVICE = 2, ROWS_HOST = 3, ROWS_DEVICE = 4, DEFERRED = 5 };
 
+// Division by a fixed divisor d as a multiply and shift (Granlund and Montgomery,
+// "Division by invariant integers using multiplication", 1994, round-up method):
+// with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1, n / d = (mulhi(n, m) + n)
+// >> l for every 32-bit n.  The unit index walks divide by H and B several times per
+// work item, and a general integer division is a long instruction sequence.
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
 struct ScanParams {
     CUtensorMap tm_in;     // state read: [units * 128 rows][128] f32, box 32 x 128, 128B swizzle
     CUtensorMap tm_in2;    // DEFERRED: the state read of units with nothing to replay
@@ -126,6 +135,7 @@ struct ScanParams {
     const int *rows_dev;   // ROWS_DEVICE, or KEEP_DEVICE after a per-session round: [B] row counts
     int *status;           // nullable device status word
     int L, B, H;
+    FastDiv divH, divB;    // u / H and lb / B
     int T_rows;            // row count of the raw-row tensors
     int T_run;             // rows to run for KEEP_NONE and DEFERRED
     int T_prev;            // DEFERRED: row count of the previous round's raw-row tensors
@@ -340,13 +350,27 @@ __device__ __forceinline__ int replay_rows(const ScanParams &p, int b)
     return kp < p.T_prev ? kp : 0;
 }
 
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, FastDiv f)
+{
+    return static_cast<uint32_t>((static_cast<uint64_t>(__umulhi(n, f.m)) + n) >> f.l);
+}
+
+// the session of unit u = (l * B + b) * H + h
+__device__ __forceinline__ int session_of(const ScanParams &p, int u)
+{
+    const uint32_t lb = fdiv(static_cast<uint32_t>(u), p.divH);
+    return static_cast<int>(lb - fdiv(lb, p.divB) * static_cast<uint32_t>(p.B));
+}
+
 __device__ __forceinline__ Unit unit_of(const ScanParams &p, int u)
 {
     Unit x;
-    x.h = u % p.H;
-    x.lb = u / p.H;
-    x.b = static_cast<int>(x.lb % p.B);
-    x.l = static_cast<int>(x.lb / p.B);
+    const uint32_t lb = fdiv(static_cast<uint32_t>(u), p.divH);
+    const uint32_t l = fdiv(lb, p.divB);
+    x.h = static_cast<int>(static_cast<uint32_t>(u) - lb * static_cast<uint32_t>(p.H));
+    x.lb = lb;
+    x.b = static_cast<int>(lb - l * static_cast<uint32_t>(p.B));
+    x.l = static_cast<int>(l);
     x.T = unit_rows(p, x.b);
     x.R = replay_rows(p, x.b);
     return x;
@@ -362,7 +386,7 @@ struct Item {
 
 __device__ __forceinline__ Item first_item(const ScanParams &p, int u, int n)
 {
-    return Item{u, u < n && replay_rows(p, (u / p.H) % p.B) > 0 ? 0 : 1};
+    return Item{u, u < n && replay_rows(p, session_of(p, u)) > 0 ? 0 : 1};
 }
 
 // The first unit at or after u (stepping by the grid) that has rows to run.  Every
@@ -370,7 +394,7 @@ __device__ __forceinline__ Item first_item(const ScanParams &p, int u, int n)
 __device__ int next_live(const ScanParams &p, int u, int n, bool report)
 {
     for (; u < n; u += gridDim.x) {
-        const int T = unit_rows(p, (u / p.H) % p.B);
+        const int T = unit_rows(p, session_of(p, u));
         if (T > 0)
             return u;
         if (T < 0 && report && p.status)
@@ -392,7 +416,7 @@ __device__ __forceinline__ Item next_item(const ScanParams &p, Item it, int n)
 __device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, uint32_t bar, int u)
 {
     const CUtensorMap *tm =
-        p.keep_mode == DEFERRED && replay_rows(p, (u / p.H) % p.B) == 0 ? &p.tm_in2 : &p.tm_in;
+        p.keep_mode == DEFERRED && replay_rows(p, session_of(p, u)) == 0 ? &p.tm_in2 : &p.tm_in;
     mbar_expect_tx(bar, D * D * 4);
 #pragma unroll
     for (int b = 0; b < 4; ++b)
@@ -406,7 +430,7 @@ __device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, 
 __device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, Item it, int s,
                              int lane)
 {
-    const int h = it.u % p.H, lb = it.u / p.H;
+    const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(it.u), p.divH)), h = it.u - lb * p.H;
     const uint32_t rb = static_cast<uint32_t>(lay.row_bytes());
     fence_proxy_async();  // the prologue's generic reads of the stage come first
     if (lane == 0) {
@@ -643,17 +667,18 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
             gate_stream(lay, stg, si, sc, pr, T, lane);
         }
         mbar_arrive(c.bar(B_SI_FULL + b));
-        // the next item's conv weights, ring and beta, and the raw rows of item i + nstg
-        // into the stage this warp is done with
-        const Item nx = next_item(p, it, n);
-        if (nx.u < n)
-            load_pre(p, nx, pw, lane, pr);
+        // the raw rows of item i + nstg into the stage this warp is done with (before the
+        // loads below: the proxy fence would wait for them), then the next item's conv
+        // weights, ring and beta
         if (sg.next.u < n) {
             issue_stream(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + 4 * sb + pw), sg.next, pw, lane);
             (sb ? sg.pend1 : sg.pend0) = true;
             (sb ? sg.par1 : sg.par0) = (m + 1) & 1;
             sg.next = next_item(p, sg.next, n);
         }
+        const Item nx = next_item(p, it, n);
+        if (nx.u < n)
+            load_pre(p, nx, pw, lane, pr);
         it = nx;
     }
     if (!ok && lane == 0) {  // stage copies in flight must land before the CTA leaves
@@ -1021,6 +1046,15 @@ struct DeviceInfo {
 
 // s_in: the state tm_in reads; for DEFERRED also s_in2 (tm_in2) and the previous
 // round's raw rows.
+FastDiv make_fastdiv(uint32_t d)
+{
+    uint32_t l = 0;
+    while ((1ull << l) < d)
+        ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), l};
+}
+
 int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const float *s_in2 = nullptr,
                 const kda_rows *prev = nullptr)
 {
@@ -1029,6 +1063,8 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
         return ok();
     if (units > 0x7fffffffLL / D)
         return fail(KDA_EINVAL, "L*B*H exceeds the unit index range (2^31 / 128 units)");
+    p.divH = make_fastdiv(static_cast<uint32_t>(p.H));
+    p.divB = make_fastdiv(static_cast<uint32_t>(p.B));
     static DeviceInfo info[64];
     static std::mutex init_mutex;
     int dev = 0;
