@@ -37,10 +37,13 @@ METRIC = "KDA verify rows/s (T=K+1, 64 heads) and achieved HBM GB/s vs 8 TB/s ro
 UNIT = "verify rows/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes read + written by one ping-pong verify launch of the current
-# kda_scan_kernel, from one ncu capture each (profiles/kda_scan_kernel_<workload>.md;
-# dram__bytes_read.sum + dram__bytes_write.sum).  Re-measure whenever the kernel changes.
-TRAFFIC_BYTES = {}
+# DRAM bytes read + written by one deferred-round launch of the current kda_scan_kernel
+# and that launch's algorithmic bytes, from one ncu capture each
+# (profiles/kda_scan_kernel_deferred_<workload>.md; dram__bytes_read.sum +
+# dram__bytes_write.sum).  The reported traffic scales the capture to the run's mean
+# algorithmic bytes per launch.  Re-measure whenever the kernel changes.
+TRAFFIC_BYTES = {"stack34": (201_803_264 + 258_193_408, 504_740_608),
+                 "batched32": (204_213_504 + 233_296_384, 478_401_792)}
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
@@ -787,7 +790,10 @@ def main():
                      "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s", "frac": frac,
                      "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
                      "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
-                     "bytes_per_launch": res["round_bytes_mean"], "traffic": TRAFFIC_BYTES.get(args.workload)},
+                     "bytes_per_launch": res["round_bytes_mean"],
+                     "traffic": (TRAFFIC_BYTES[args.workload][0] * res["round_bytes_mean"] /
+                                 TRAFFIC_BYTES[args.workload][1]) if args.workload in TRAFFIC_BYTES else None,
+                     "traffic_source": "ncu capture of one launch, scaled to the mean bytes per launch"},
         "round_kernel_ms": res["round_kernel_ms"], "accept_ms": res["accept_ms"],
         "step_achieved_gbs": res["step_gbs"],
         "gpu_launches": res["launches_per_step"] * args.steps,
