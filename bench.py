@@ -488,39 +488,59 @@ def run_gpu(args, rank, world, local_rank):
         res["graph"] = {"ms_per_step": g_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, g_ms), "steps": K,
                         "round": "ping-pong verify, accept, rollback (separate launches), one graph per round"}
 
-    # e2e: host buffers through the public API, copies inside the timed region
+    # e2e: host buffers through the public API, copies inside the timed region.  A round's
+    # inputs (raw rows, logits, drafts) sit in one pinned host block and go over in one
+    # copy into one device block the tensors are views of; j and the bonus come back in
+    # one copy.
     if not args.no_e2e:
         HR = min(R, 4)
-        host_rows = [{n: t.cpu().pin_memory() for n, t in rows[r].items()} for r in range(HR)]
-        host_logits = [logits[r].cpu().pin_memory() for r in range(HR)]
-        host_drafts = [drafts[r].cpu().pin_memory() for r in range(HR)]
-        # two input buffer sets: a deferred round reads the previous round's raw rows
-        dev_rows = [{n: torch.empty_like(t) for n, t in rows[0].items()} for _ in range(2)]
-        dev_logits = torch.empty_like(logits[0])
-        dev_drafts = torch.empty_like(drafts[0])
+        parts = [(n, rows[0][n]) for n in ("q", "k", "v", "g", "beta")] + [("logits", logits[0]),
+                                                                           ("drafts", drafts[0])]
+        offs, off = {}, 0
+        for n, t in parts:
+            offs[n] = off
+            off += (t.numel() * t.element_size() + 255) // 256 * 256
+        block_bytes = off
+
+        def views(buf):
+            out_ = {}
+            for n, t in parts:
+                nb = t.numel() * t.element_size()
+                out_[n] = buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+            return out_
+
+        host_blocks = []
+        for r in range(HR):
+            hb = torch.empty(block_bytes, dtype=torch.uint8).pin_memory()
+            hv = views(hb)
+            src = dict(rows[r], logits=logits[r], drafts=drafts[r])
+            for n, _ in parts:
+                hv[n].copy_(src[n].cpu())
+            host_blocks.append(hb)
+        # two device input sets: a deferred round reads the previous round's raw rows
+        dev_blocks = [torch.empty(block_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+        dev_views = [views(b) for b in dev_blocks]
+        res_dev = torch.empty((3, w.B), dtype=torch.int32, device=dev)  # j, bonus, keep
         host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host_rows[0].values()) + \
-            host_logits[0].numel() * host_logits[0].element_size() + host_drafts[0].numel() * 4
+        h2d = sum(t.numel() * t.element_size() for _, t in parts)
         d2h = host_res.numel() * 4
         Ke = max(1, min(args.e2e_steps, K))
 
-        eplans = [kb.DeferredRoundPlan(pp, dev_rows[b], out, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
-                                       status, scratch, stream) for b in range(2)]
-        eopen = kb.PingPongRoundPlan(pp, dev_rows[1], out, dev_logits, dev_drafts, j_out, bonus_out, keep_out,
-                                     status, scratch, stream)
+        def eplan(b, cls):
+            v = dev_views[b]
+            return cls(pp, {n: v[n] for n in ("q", "k", "v", "g", "beta")}, out, v["logits"], v["drafts"], res_dev[0],
+                       res_dev[1], res_dev[2], status, scratch, stream)
+
+        eplans = [eplan(b, kb.DeferredRoundPlan) for b in range(2)]
+        eopen = eplan(1, kb.PingPongRoundPlan)
 
         def e2e_load(i):
-            r = i % HR
-            for n in dev_rows[i % 2]:
-                dev_rows[i % 2][n].copy_(host_rows[r][n], non_blocking=True)
-            dev_logits.copy_(host_logits[r], non_blocking=True)
-            dev_drafts.copy_(host_drafts[r], non_blocking=True)
+            dev_blocks[i % 2].copy_(host_blocks[i % HR], non_blocking=True)
 
         def e2e_step(i):
             e2e_load(i)
             eplans[i % 2]()
-            host_res[0].copy_(j_out, non_blocking=True)
-            host_res[1].copy_(bonus_out, non_blocking=True)
+            host_res.copy_(res_dev[:2], non_blocking=True)
             stream.synchronize()  # the host needs j and the bonus before the next round
 
         # open the chain with a ping-pong round on buffer set 1, then deferred rounds
@@ -538,7 +558,7 @@ def run_gpu(args, rank, world, local_rank):
         barrier()
         e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
         e2e_ms = slowest(e2e_ms, world, dev)
-        kb.kda_rollback_pingpong(pp, keep_out, dev_status=status, stream=stream)
+        kb.kda_rollback_pingpong(pp, res_dev[2], dev_status=status, stream=stream)
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the e2e steps")
         res["e2e"] = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT,
