@@ -6,14 +6,21 @@
 // bonus token vam[j]; keep = j + 1 (the anchor row is always committed).  A row
 // holding a NaN has no argmax; reaching it refuses loudly (guard_vocab_token).
 //
-// Two launches, no inter-CTA waiting:
+// spec_accept and spec_accept_var: one launch of thread-block clusters, one cluster
+// of CL CTAs per session.  CTA c of a cluster reduces vocabulary slice c of every
+// row of the session (warp w takes rows w, w + 8) to (max, lowest index of the max,
+// NaN seen) and writes that triple into the shared memory of the cluster's first
+// CTA (distributed shared memory); after the cluster barrier, lane r of that CTA's
+// first warp folds the CL triples of row r in slice order, and a ballot over the
+// mismatch predicate gives j.
+// spec_accept_noalloc keeps the two-launch form, whose partial results go through a
+// scratch array:
 //   1. accept_partial_kernel: grid (B*T rows, VS slices of the vocabulary); each
-//      CTA reduces its slice to (max, lowest index of the max, NaN seen) and
-//      writes that triple to the caller's scratch.
-//   2. accept_final_kernel: one warp per session; lane r folds the VS triples of
-//      row r in slice order, then a ballot over the mismatch predicate gives j.
+//      CTA reduces its slice to the triple and writes it to scratch.
+//   2. accept_final_kernel: one warp per session folds the VS triples of each row.
 // The selection is a total order on (value, -index), so the reduction order
 // never changes the result.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -193,6 +200,160 @@ __global__ void accept_final_kernel(const Partial *__restrict__ part, int B, int
     }
 }
 
+constexpr int CL = 8;  // CTAs (vocabulary slices) per session: one cluster
+
+// The (max, lowest index, NaN seen) triple of logits [begin, end) of one row, reduced
+// over a warp (every lane ends with the triple).  A lane issues up to NB 16-byte loads
+// before it compares any of them, so a slice costs one load latency, not NB.
+constexpr int NB = 16;
+
+template <bool BF16>
+__device__ __forceinline__ Partial warp_slice(const void *logits, long long row, int V, int begin, int end, int lane)
+{
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    int nan = 0;
+    constexpr int PER = BF16 ? 8 : 4;  // logits per 16-byte vector
+    const char *x = static_cast<const char *>(logits) + row * V * (BF16 ? 2 : 4);
+    if (V % PER == 0 && begin % PER == 0 && end % PER == 0) {
+        const uint4 *xv = reinterpret_cast<const uint4 *>(x);
+        for (int c0 = begin / PER; c0 < end / PER; c0 += 32 * NB) {
+            uint4 r[NB];
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                const int c = c0 + lane + 32 * i;
+                r[i] = c < end / PER ? xv[c] : make_uint4(0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu);
+            }
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                const int c = c0 + lane + 32 * i;
+                if (c >= end / PER)
+                    break;
+                const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+                if (BF16) {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float lo = __uint_as_float(w[m] << 16), hi = __uint_as_float(w[m] & 0xffff0000u);
+                        nan |= (lo != lo) | (hi != hi);
+                        take(bv, bi, lo, 8 * c + 2 * m);
+                        take(bv, bi, hi, 8 * c + 2 * m + 1);
+                    }
+                } else {
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const float v = __uint_as_float(w[m]);
+                        nan |= (v != v);
+                        take(bv, bi, v, 4 * c + m);
+                    }
+                }
+            }
+        }
+    } else {
+        for (int c = begin + lane; c < end; c += 32) {
+            const float v = BF16 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(x)[c]) << 16)
+                                 : reinterpret_cast<const float *>(x)[c];
+            nan |= (v != v);
+            take(bv, bi, v, c);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        nan |= __shfl_xor_sync(0xffffffffu, nan, off);
+        take(bv, bi, ov, oi);
+    }
+    return Partial{bv, bi, nan, 0};
+}
+
+// grid B * CL CTAs of ACC_THREADS, clusters of CL; chunk: logits per slice (a multiple
+// of 8).  t_rows (nullable) as for accept_final_kernel.
+template <bool BF16>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(ACC_THREADS)
+    accept_cluster_kernel(const void *__restrict__ logits, int V, int T, int chunk, const int *__restrict__ drafts,
+                          int *j_out, int *bonus_out, int *keep_out, int *status, const int *__restrict__ t_rows)
+{
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    __shared__ Partial part[KDA_TMAX][CL];  // in the first CTA: every slice's triple of every row
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int b = blockIdx.x / CL;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int Tb = t_rows ? t_rows[b] : T;
+    const bool valid = Tb >= 1 && Tb <= T;
+    const int begin = min(V, rank * chunk), end = min(V, begin + chunk);
+    Partial *lead = cluster.map_shared_rank(&part[0][0], 0);
+    if (valid) {
+        // rows past a session's count are never consulted
+        for (int r = wid; r < Tb; r += ACC_THREADS / 32) {
+            const Partial pt = BF16 ? warp_slice<true>(logits, static_cast<long long>(b) * T + r, V, begin, end, lane)
+                                    : warp_slice<false>(logits, static_cast<long long>(b) * T + r, V, begin, end, lane);
+            if (lane == 0)
+                lead[r * CL + rank] = pt;
+        }
+    }
+    cluster.sync();  // every slice's triples are in the first CTA's shared memory
+    if (rank != 0 || wid != 0)
+        return;
+    if (!valid) {  // an invalid row count: no accept for this session
+        if (lane == 0) {
+            if (j_out)
+                j_out[b] = -1;
+            if (bonus_out)
+                bonus_out[b] = -1;
+            if (keep_out)
+                keep_out[b] = 0;
+            if (status)
+                atomicOr(status, KDA_ST_BADKEEP);
+        }
+        return;
+    }
+    const int K = Tb - 1;
+    int vam = -1;
+    if (lane < Tb) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff, nan = 0;
+        for (int c = 0; c < CL; ++c) {
+            const Partial q = part[lane][c];
+            nan |= q.nan;
+            take(bv, bi, q.v, q.idx);
+        }
+        vam = nan ? -1 : bi;
+    }
+    const bool miss = lane < K && (vam < 0 || drafts[static_cast<long long>(b) * (T - 1) + lane] != vam);
+    const unsigned mask = __ballot_sync(0xffffffffu, miss);
+    const int j = mask ? __ffs(mask) - 1 : K;
+    const int bonus = __shfl_sync(0xffffffffu, vam, j);
+    if (lane == 0) {
+        if (j_out)
+            j_out[b] = j;
+        if (bonus_out)
+            bonus_out[b] = bonus;
+        if (keep_out)
+            keep_out[b] = j + 1;
+        if (bonus < 0 && status)
+            atomicOr(status, KDA_ST_NAN);
+    }
+}
+
+// One cluster launch for B sessions.
+int launch_accept_cluster(const void *logits, int logit_dtype, int B, int T, int V, const int *drafts, int *j_out,
+                          int *bonus_out, int *keep_out, int *dev_status, const int *t_rows, cudaStream_t stream)
+{
+    if (static_cast<long long>(B) * CL > 0x7fffffffLL)
+        return fail(KDA_EINVAL, "B exceeds the grid limit");
+    int chunk = (V + CL - 1) / CL;
+    chunk = (chunk + 7) / 8 * 8;
+    const unsigned grid = static_cast<unsigned>(B) * CL;
+    if (logit_dtype == KDA_BF16)
+        accept_cluster_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, T, chunk, drafts, j_out, bonus_out,
+                                                                       keep_out, dev_status, t_rows);
+    else
+        accept_cluster_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, T, chunk, drafts, j_out, bonus_out,
+                                                                        keep_out, dev_status, t_rows);
+    return check_launch("accept_cluster_kernel");
+}
+
 }  // namespace
 }  // namespace kda
 
@@ -223,28 +384,14 @@ extern "C" int spec_accept(const void *logits, int logit_dtype, int B, int T, in
         return fail(KDA_EINVAL, "logits and drafts must not be NULL");
     if (!aligned16(logits))
         return fail(KDA_EINVAL, "logits must be 16-byte aligned");
+    // the scratch stays in the signature (and is checked) so that callers keep one
+    // contract; the cluster form passes its partial results through shared memory
     const size_t need = spec_accept_scratch_bytes(B, T, V);
     if (!scratch || scratch_bytes < need || !aligned16(scratch))
         return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " +
                                     std::to_string(need) + " bytes");
-    if (static_cast<long long>(B) * T > 0x7fffffffLL)
-        return fail(KDA_EINVAL, "B*T exceeds the grid limit");
-    const int vs = slices_for(V);
-    int chunk = (V + vs - 1) / vs;
-    chunk = (chunk + 7) / 8 * 8;
-    Partial *part = static_cast<Partial *>(scratch);
-    dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
-    if (logit_dtype == KDA_BF16)
-        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, nullptr, T);
-    else
-        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, nullptr, T);
-    int rc = check_launch("accept_partial_kernel");
-    if (rc)
-        return rc;
-    const int warps = 4;
-    accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
-                                                                            bonus_out, keep_out, dev_status, nullptr);
-    return check_launch("accept_final_kernel");
+    return launch_accept_cluster(logits, logit_dtype, B, T, V, drafts, j_out, bonus_out, keep_out, dev_status,
+                                 nullptr, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -416,24 +563,8 @@ extern "C" int spec_accept_var(const void *logits, int logit_dtype, int B, int T
     if (!scratch || scratch_bytes < need || !aligned16(scratch))
         return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " +
                                     std::to_string(need) + " bytes");
-    if (static_cast<long long>(B) * T > 0x7fffffffLL)
-        return fail(KDA_EINVAL, "B*T exceeds the grid limit");
-    const int vs = slices_for(V);
-    int chunk = (V + vs - 1) / vs;
-    chunk = (chunk + 7) / 8 * 8;
-    Partial *part = static_cast<Partial *>(scratch);
-    dim3 grid(static_cast<unsigned>(B * T), static_cast<unsigned>(vs));
-    if (logit_dtype == KDA_BF16)
-        accept_partial_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, t_rows, T);
-    else
-        accept_partial_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, vs, chunk, part, t_rows, T);
-    int rc = check_launch("accept_partial_kernel");
-    if (rc)
-        return rc;
-    const int warps = 4;
-    accept_final_kernel<<<(B + warps - 1) / warps, warps * 32, 0, stream>>>(part, B, T, vs, drafts, j_out,
-                                                                            bonus_out, keep_out, dev_status, t_rows);
-    return check_launch("accept_final_kernel");
+    return launch_accept_cluster(logits, logit_dtype, B, T, V, drafts, j_out, bonus_out, keep_out, dev_status,
+                                 t_rows, stream);
 }
 
 extern "C" int spec_window(const float *scores, int B, int K, int policy, float param, int pmin0, int t_cap,
