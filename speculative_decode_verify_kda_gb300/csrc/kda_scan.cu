@@ -911,6 +911,8 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const Layout lay{p.tcap, p.bf16 ? 2 : 4, p.nstg};
+    // launched as a programmatic dependent: wait for the previous kernel's results
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const Ctl c{smem_addr(sm + lay.bars()), reinterpret_cast<volatile int *>(sm + lay.flag()), p.status};
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
@@ -1127,10 +1129,23 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
     const long long grid = std::min<long long>(units, di.sms);
     const unsigned g = static_cast<unsigned>(grid);
     const size_t sb = lay.total();
-    if (p.s_cols)
-        kda_scan_kernel<true><<<g, NT, sb, stream>>>(p);
-    else
-        kda_scan_kernel<false><<<g, NT, sb, stream>>>(p);
+    // programmatic dependent launch: the kernel may be scheduled while the previous
+    // kernel in the stream finishes; it waits for that kernel's results
+    // (griddepcontrol.wait) before it touches global memory, so stream order holds
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(g);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = sb;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le = p.s_cols ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<true>, p)
+                                    : cudaLaunchKernelEx(&cfg, kda_scan_kernel<false>, p);
+    if (le != cudaSuccess)
+        return fail(KDA_ECUDA, std::string("kda_scan_kernel launch: ") + cudaGetErrorString(le));
     return check_launch("kda_scan_kernel");
 }
 

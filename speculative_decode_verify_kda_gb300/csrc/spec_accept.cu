@@ -276,6 +276,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(ACC_THREADS)
     namespace cg = cooperative_groups;
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ Partial part[KDA_TMAX][CL];  // in the first CTA: every slice's triple of every row
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // launched as a programmatic dependent
     const int rank = static_cast<int>(cluster.block_rank());
     const int b = blockIdx.x / CL;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -345,12 +346,26 @@ int launch_accept_cluster(const void *logits, int logit_dtype, int B, int T, int
     int chunk = (V + CL - 1) / CL;
     chunk = (chunk + 7) / 8 * 8;
     const unsigned grid = static_cast<unsigned>(B) * CL;
-    if (logit_dtype == KDA_BF16)
-        accept_cluster_kernel<true><<<grid, ACC_THREADS, 0, stream>>>(logits, V, T, chunk, drafts, j_out, bonus_out,
-                                                                       keep_out, dev_status, t_rows);
-    else
-        accept_cluster_kernel<false><<<grid, ACC_THREADS, 0, stream>>>(logits, V, T, chunk, drafts, j_out, bonus_out,
-                                                                        keep_out, dev_status, t_rows);
+    // programmatic dependent launch, as the scan kernel: the kernel waits for the
+    // previous kernel's results before it reads anything
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(ACC_THREADS);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le =
+        logit_dtype == KDA_BF16
+            ? cudaLaunchKernelEx(&cfg, accept_cluster_kernel<true>, logits, V, T, chunk, drafts, j_out, bonus_out,
+                                 keep_out, dev_status, t_rows)
+            : cudaLaunchKernelEx(&cfg, accept_cluster_kernel<false>, logits, V, T, chunk, drafts, j_out, bonus_out,
+                                 keep_out, dev_status, t_rows);
+    if (le != cudaSuccess)
+        return fail(KDA_ECUDA, std::string("accept_cluster_kernel launch: ") + cudaGetErrorString(le));
     return check_launch("accept_cluster_kernel");
 }
 
