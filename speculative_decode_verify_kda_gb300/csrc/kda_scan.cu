@@ -699,6 +699,96 @@ __device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[
         *reinterpret_cast<float4 *>(So + (rg + 8 * r) * D) = make_float4(S[r][0].x, S[r][0].y, S[r][1].x, S[r][1].y);
 }
 
+// The rows of one work item on the register tile S.  OUT: write the output rows to
+// orow (lanes with b2 = 1, column jsum); without outputs (replays) neither e = S'^T q
+// nor k.q is formed.  The state arithmetic, and so the state bits, do not depend on OUT.
+template <bool COLS, bool OUT>
+__device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, const float *sc, float *orow,
+                                         float2 (&S)[16][2], int T, int u, int rg, int cg, int jbase, int jsum,
+                                         int b0, int b1, int b2)
+{
+    // ---- the T-row gated delta rule ---------------------------------------------
+    for (int t = 0; t < T; ++t) {
+        const float *vt = si + t * SI_ROW;
+        const float *gp = vt + rg * GRP;
+        float2 uacc[2], eacc[2];
+        float kv[16];
+        float kq = 0.f;  // k.q over this thread's 16 rows, in order (outputs only)
+        uacc[0] = uacc[1] = eacc[0] = eacc[1] = make_float2(0.f, 0.f);
+        // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows, in order)
+#pragma unroll
+        for (int rq = 0; rq < 4; ++rq) {
+            const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
+            const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
+            const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
+            kv[4 * rq] = k4.x;
+            kv[4 * rq + 1] = k4.y;
+            kv[4 * rq + 2] = k4.z;
+            kv[4 * rq + 3] = k4.w;
+            if (OUT)
+                kq = __fmaf_rn(k4.w, q4.w, __fmaf_rn(k4.z, q4.z, __fmaf_rn(k4.y, q4.y, __fmaf_rn(k4.x, q4.x, kq))));
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = 4 * rq + m;
+                const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[r], kv[r]);
+                const float2 qq = make_float2(qv[m], qv[m]);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    S[r][h] = __fmul2_rn(S[r][h], dd);
+                    uacc[h] = __ffma2_rn(S[r][h], kk, uacc[h]);
+                    if (OUT)
+                        eacc[h] = __ffma2_rn(S[r][h], qq, eacc[h]);
+                }
+            }
+        }
+        // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
+        // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
+        const float v8[8] = {uacc[0].x, uacc[0].y, uacc[1].x, uacc[1].y, eacc[0].x, eacc[0].y, eacc[1].x, eacc[1].y};
+        float v4[4], v2[2];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const float keep = b2 ? v8[4 + m] : v8[m], send = b2 ? v8[m] : v8[4 + m];
+            v4[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const float keep = b1 ? v4[2 + m] : v4[m], send = b1 ? v4[m] : v4[2 + m];
+            v2[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+        }
+        const float keep1 = b0 ? v2[1] : v2[0], send1 = b0 ? v2[0] : v2[1];
+        const float sum = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
+        // k.q over the 8 row groups: a butterfly, so every lane holds the same bits
+        if (OUT) {
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+                kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
+        }
+        // u lanes: w = beta (v - u); e lanes: o = (e + w (k.q)) / sqrt(128)
+        const float beta = sc[t];
+        const float w = __fmul_rn(beta, __fsub_rn(vt[SI_V + jsum], sum));
+        const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
+        // a warp's 16 e lanes store 16 consecutive columns of the output row
+        if (OUT && b2)
+            orow[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, kq, sum), OUT_SCALE);
+        // every lane gathers w of its 4 columns from the u lanes 4 c + cg
+        float wv[4];
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+            wv[c4] = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
+        const float2 w01 = make_float2(wv[0], wv[1]), w23 = make_float2(wv[2], wv[3]);
+        // S = S' + k w^T
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const float2 kk = make_float2(kv[r], kv[r]);
+            S[r][0] = __ffma2_rn(kk, w01, S[r][0]);
+            S[r][1] = __ffma2_rn(kk, w23, S[r][1]);
+        }
+        if (COLS)  // the column stash: the state after row t
+            store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
+    }
+}
+
 template <bool COLS>
 __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
@@ -784,82 +874,10 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
                               ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum
                               : nullptr;
 
-            // ---- the T-row gated delta rule ---------------------------------------------
-            for (int t = 0; t < T; ++t) {
-                const float *vt = si + t * SI_ROW;
-                const float *gp = vt + rg * GRP;
-                float2 uacc[2], eacc[2];
-                float kv[16];
-                float kq = 0.f;  // k.q over this thread's 16 rows, in order
-                uacc[0] = uacc[1] = eacc[0] = eacc[1] = make_float2(0.f, 0.f);
-                // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows, in order)
-#pragma unroll
-                for (int rq = 0; rq < 4; ++rq) {
-                    const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
-                    const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
-                    const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
-                    const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
-                    kv[4 * rq] = k4.x;
-                    kv[4 * rq + 1] = k4.y;
-                    kv[4 * rq + 2] = k4.z;
-                    kv[4 * rq + 3] = k4.w;
-                    kq = __fmaf_rn(k4.w, q4.w, __fmaf_rn(k4.z, q4.z, __fmaf_rn(k4.y, q4.y, __fmaf_rn(k4.x, q4.x, kq))));
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int r = 4 * rq + m;
-                        const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[r], kv[r]);
-                        const float2 qq = make_float2(qv[m], qv[m]);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            S[r][h] = __fmul2_rn(S[r][h], dd);
-                            uacc[h] = __ffma2_rn(S[r][h], kk, uacc[h]);
-                            eacc[h] = __ffma2_rn(S[r][h], qq, eacc[h]);
-                        }
-                    }
-                }
-                // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
-                // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
-                const float v8[8] = {uacc[0].x, uacc[0].y, uacc[1].x, uacc[1].y, eacc[0].x, eacc[0].y, eacc[1].x, eacc[1].y};
-                float v4[4], v2[2];
-#pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float keep = b2 ? v8[4 + m] : v8[m], send = b2 ? v8[m] : v8[4 + m];
-                    v4[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-                }
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const float keep = b1 ? v4[2 + m] : v4[m], send = b1 ? v4[m] : v4[2 + m];
-                    v2[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-                }
-                const float keep1 = b0 ? v2[1] : v2[0], send1 = b0 ? v2[0] : v2[1];
-                const float sum = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
-                // k.q over the 8 row groups: a butterfly, so every lane holds the same bits
-#pragma unroll
-                for (int off = 4; off < 32; off <<= 1)
-                    kq = __fadd_rn(kq, __shfl_xor_sync(0xffffffffu, kq, off));
-                // u lanes: w = beta (v - u); e lanes: o = (e + w (k.q)) / sqrt(128)
-                const float beta = sc[t];
-                const float w = __fmul_rn(beta, __fsub_rn(vt[SI_V + jsum], sum));
-                const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
-                // a warp's 16 e lanes store 16 consecutive columns of the output row
-                if (orow && b2)
-                    orow[static_cast<size_t>(t) * p.H * D] = __fmul_rn(__fmaf_rn(w_of_col, kq, sum), OUT_SCALE);
-                // every lane gathers w of its 4 columns from the u lanes 4 c + cg
-                float wv[4];
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4)
-                    wv[c4] = __shfl_sync(0xffffffffu, w, 4 * c4 + cg);
-                const float2 w01 = make_float2(wv[0], wv[1]), w23 = make_float2(wv[2], wv[3]);
-                // S = S' + k w^T
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float2 kk = make_float2(kv[r], kv[r]);
-                    S[r][0] = __ffma2_rn(kk, w01, S[r][0]);
-                    S[r][1] = __ffma2_rn(kk, w23, S[r][1]);
-                }
-                if (COLS)  // the column stash: the state after row t
-                    store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
-            }
+            if (orow)
+                run_rows<COLS, true>(p, si, sc, orow, S, T, u, rg, cg, jbase, jsum, b0, b1, b2);
+            else
+                run_rows<COLS, false>(p, si, sc, orow, S, T, u, rg, cg, jbase, jsum, b0, b1, b2);
             mbar_arrive(c.bar(B_SI_EMPTY + ib));  // the scan inputs of item i are consumed
             if (part == 0)  // the committed state: this round's snapshot
                 store_tile(p.s_snap_out + static_cast<size_t>(u) * D * D + jbase, rg, S);
