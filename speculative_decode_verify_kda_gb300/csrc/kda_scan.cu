@@ -496,6 +496,31 @@ __device__ __forceinline__ void store_perm(float *row, int block, int lane, floa
     g[3 * GRP] = v.w;
 }
 
+// The conv window of stream pw after an item's T rows without the conv itself (the
+// last 3 raw inputs of [window, rows]): writes the ring after the item to ring_dst and,
+// when snapshotting, the ring before it.
+__device__ void roll_window(const ScanParams &p, const Layout &lay, const unsigned char *stg, float4 (&win)[3], int u,
+                            int T, int pw, int lane, float *ring_dst)
+{
+    const size_t rbase = (static_cast<size_t>(u) * 3 + pw) * 3 * D;
+    if (p.ring_snap) {
+        float4 *rs = reinterpret_cast<float4 *>(p.ring_snap + rbase) + lane;
+        rs[0] = win[0];
+        rs[D / 4] = win[1];
+        rs[2 * D / 4] = win[2];
+    }
+    const float4 r0 = T >= 3 ? stage4(stg, lay, pw, T - 3, lane) : T == 2 ? win[2] : win[1];
+    const float4 r1 = T >= 2 ? stage4(stg, lay, pw, T - 2, lane) : win[2];
+    const float4 r2 = stage4(stg, lay, pw, T - 1, lane);
+    float4 *ro = reinterpret_cast<float4 *>(ring_dst + rbase) + lane;
+    ro[0] = r0;
+    ro[D / 4] = r1;
+    ro[2 * D / 4] = r2;
+    win[0] = r0;
+    win[1] = r1;
+    win[2] = r2;
+}
+
 // Stream pw (0 q, 1 k, 2 v) of one item: the conv window slides along the rows in
 // registers, four rows at a time with no branch around the arithmetic (rows past T
 // repeat row T-1 and are not stored), so the four rows' dependency chains overlap.
@@ -661,8 +686,13 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
                 win[2] = pr.ring[2];
             }
             // a replay ends in the committed ring (this round's ring snapshot)
-            conv_stream<COLS>(p, lay, stg, si, pr.w, win, it.u, T, pw, lane,
-                              it.part == 0 ? p.ring_snap_out : p.ring_out);
+            float *ring_dst = it.part == 0 ? p.ring_snap_out : p.ring_out;
+            // an item without outputs never reads q-hat (the column stash still wants the
+            // ring after every row)
+            if (!COLS && pw == 0 && (it.part == 0 || !p.out))
+                roll_window(p, lay, stg, win, it.u, T, pw, lane, ring_dst);
+            else
+                conv_stream<COLS>(p, lay, stg, si, pr.w, win, it.u, T, pw, lane, ring_dst);
         } else {
             gate_stream(lay, stg, si, sc, pr, T, lane);
         }
