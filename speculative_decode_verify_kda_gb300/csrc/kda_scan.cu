@@ -742,7 +742,7 @@ __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, c
         const float *vt = si + t * SI_ROW;
         const float *gp = vt + rg * GRP;
         float2 uacc[2], eacc[2];
-        float kv[16];
+        float2 kk2[16];  // (k, k) of each row, built once for both sweeps
         float kq = 0.f;  // k.q over this thread's 16 rows, in order (outputs only)
         uacc[0] = uacc[1] = eacc[0] = eacc[1] = make_float2(0.f, 0.f);
         // S' = d S ;  u = S'^T k ;  e = S'^T q   (this thread's 16 rows, in order)
@@ -752,17 +752,15 @@ __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, c
             const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
             const float4 q4 = *reinterpret_cast<const float4 *>(gp + 32 + 4 * rq);
             const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, qv[4] = {q4.x, q4.y, q4.z, q4.w};
-            kv[4 * rq] = k4.x;
-            kv[4 * rq + 1] = k4.y;
-            kv[4 * rq + 2] = k4.z;
-            kv[4 * rq + 3] = k4.w;
+            const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
             if (OUT)
                 kq = __fmaf_rn(k4.w, q4.w, __fmaf_rn(k4.z, q4.z, __fmaf_rn(k4.y, q4.y, __fmaf_rn(k4.x, q4.x, kq))));
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int r = 4 * rq + m;
-                const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[r], kv[r]);
+                const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[m], kv[m]);
                 const float2 qq = make_float2(qv[m], qv[m]);
+                kk2[r] = kk;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     S[r][h] = __fmul2_rn(S[r][h], dd);
@@ -772,23 +770,29 @@ __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, c
                 }
             }
         }
-        // reduce-scatter over the 8 row groups (lane bits 2..4): bit 4 splits u / e,
-        // bits 3 and 2 split the 4 columns; each sum ends on exactly one lane
-        const float v8[8] = {uacc[0].x, uacc[0].y, uacc[1].x, uacc[1].y, eacc[0].x, eacc[0].y, eacc[1].x, eacc[1].y};
-        float v4[4], v2[2];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const float keep = b2 ? v8[4 + m] : v8[m], send = b2 ? v8[m] : v8[4 + m];
-            v4[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        // reduce-scatter over the 8 row groups (lane bits 2..4): bits 3 and 2 split the 4
+        // columns, then bit 4 splits u / e, so each sum ends on one lane; u is summed in
+        // the same order with and without outputs (without, e is not carried at all)
+        float sum;
+        {
+            // columns 0..3 of this thread: u in uacc, e in eacc; level 1 keeps columns
+            // 2 b1, 2 b1 + 1 and sends the other two
+            const float u0 = uacc[0].x, u1 = uacc[0].y, u2 = uacc[1].x, u3 = uacc[1].y;
+            const float ua = __fadd_rn(b1 ? u2 : u0, __shfl_xor_sync(0xffffffffu, b1 ? u0 : u2, 8));
+            const float ub = __fadd_rn(b1 ? u3 : u1, __shfl_xor_sync(0xffffffffu, b1 ? u1 : u3, 8));
+            // level 2 keeps column 2 b1 + b0
+            const float uc = __fadd_rn(b0 ? ub : ua, __shfl_xor_sync(0xffffffffu, b0 ? ua : ub, 4));
+            if (OUT) {
+                const float e0 = eacc[0].x, e1 = eacc[0].y, e2 = eacc[1].x, e3 = eacc[1].y;
+                const float ea = __fadd_rn(b1 ? e2 : e0, __shfl_xor_sync(0xffffffffu, b1 ? e0 : e2, 8));
+                const float eb = __fadd_rn(b1 ? e3 : e1, __shfl_xor_sync(0xffffffffu, b1 ? e1 : e3, 8));
+                const float ec = __fadd_rn(b0 ? eb : ea, __shfl_xor_sync(0xffffffffu, b0 ? ea : eb, 4));
+                // level 3: bit 4 splits u (b2 = 0) from e (b2 = 1)
+                sum = __fadd_rn(b2 ? ec : uc, __shfl_xor_sync(0xffffffffu, b2 ? uc : ec, 16));
+            } else {
+                sum = __fadd_rn(uc, __shfl_xor_sync(0xffffffffu, uc, 16));
+            }
         }
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const float keep = b1 ? v4[2 + m] : v4[m], send = b1 ? v4[m] : v4[2 + m];
-            v2[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-        }
-        const float keep1 = b0 ? v2[1] : v2[0], send1 = b0 ? v2[0] : v2[1];
-        const float sum = __fadd_rn(keep1, __shfl_xor_sync(0xffffffffu, send1, 4));
-        // k.q over the 8 row groups: a butterfly, so every lane holds the same bits
         if (OUT) {
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1)
@@ -810,9 +814,8 @@ __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, c
         // S = S' + k w^T
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            const float2 kk = make_float2(kv[r], kv[r]);
-            S[r][0] = __ffma2_rn(kk, w01, S[r][0]);
-            S[r][1] = __ffma2_rn(kk, w23, S[r][1]);
+            S[r][0] = __ffma2_rn(kk2[r], w01, S[r][0]);
+            S[r][1] = __ffma2_rn(kk2[r], w23, S[r][1]);
         }
         if (COLS)  // the column stash: the state after row t
             store_tile(p.s_cols + (static_cast<size_t>(u) * p.T_rows + t) * D * D + jbase, rg, S);
