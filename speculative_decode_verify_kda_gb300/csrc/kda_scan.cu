@@ -962,8 +962,11 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const Layout lay{p.tcap, p.bf16 ? 2 : 4, p.nstg};
-    // launched as a programmatic dependent: wait for the previous kernel's results
+    // launched as a programmatic dependent: wait for the previous kernel's results.
+    // The next kernel may be scheduled as soon as every CTA of this one is resident
+    // (it waits for this kernel's results in turn).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Ctl c{smem_addr(sm + lay.bars()), reinterpret_cast<volatile int *>(sm + lay.flag()), p.status};
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {

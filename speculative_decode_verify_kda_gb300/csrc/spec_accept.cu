@@ -277,6 +277,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(ACC_THREADS)
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ Partial part[KDA_TMAX][CL];  // in the first CTA: every slice's triple of every row
     asm volatile("griddepcontrol.wait;" ::: "memory");  // launched as a programmatic dependent
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int rank = static_cast<int>(cluster.block_rank());
     const int b = blockIdx.x / CL;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
