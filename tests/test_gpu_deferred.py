@@ -173,3 +173,37 @@ def test_deferred_plan_equals_the_functions():
         assert bits_equal(out_a, out_b), f"round {r}: outputs"
         assert bits_equal(a.state(), b.state()) and bits_equal(a.states[a.last], b.states[b.last]), f"round {r}"
     assert int(status[0]) == 0
+
+
+@pytest.mark.parametrize("wl", ["stack34", "batched32"])
+def test_deferred_full_size_equals_separate(wl):
+    """The full-size workloads put 13 to 15 units on every CTA, so replay and verify
+    items alternate through the stages and scan-input buffers across units; every
+    state, ring and output bit must equal the separate rollback + ping-pong rounds.
+    Keeps vary per session and round (a full keep, keep 1, and seeded ones)."""
+    from speculative_decode_verify_kda_gb300 import synth_gpu
+    w = synth.WORKLOADS[wl]
+    dev = torch.device("cuda", 0)
+    a = kb.PingPong(kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev)))
+    b = kb.PingPong(kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev)))
+    R = 4
+    rows = [synth_gpu.rows(w, r, dev) for r in range(R)]
+    keeps = _keeps(w.B, [w.T] * R, 0x9938)
+    if w.B == 1:  # one session: cycle a partial keep, a full keep and keep 1 over the rounds
+        keeps = [[3], [w.T], [1], [w.T - 1]]
+    out_a = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev)
+    out_b = torch.empty_like(out_a)
+    for r in range(R):
+        x = [rows[r][n] for n in NAMES]
+        if r > 0:
+            kb.kda_rollback_pingpong(a, keeps[r - 1])
+        kb.kda_verify_scan_pingpong(a, *x, out=out_a)
+        if r == 0:
+            kb.kda_verify_scan_pingpong(b, *x, out=out_b)
+        else:
+            kb.kda_verify_scan_deferred(b, *x, torch.tensor(keeps[r - 1], dtype=torch.int32, device=dev), out=out_b)
+        torch.cuda.synchronize()
+        assert bits_equal(out_a, out_b), f"round {r}: outputs"
+        assert bits_equal(a.state(), b.state()) and bits_equal(a.ring(), b.ring()), f"round {r}: post-round"
+        assert bits_equal(a.states[a.last], b.states[b.last]) and bits_equal(a.rings[a.last], b.rings[b.last]), \
+            f"round {r}: snapshot"
