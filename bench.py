@@ -601,9 +601,26 @@ def run_gpu(args, rank, world, local_rank):
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the per-layer steps")
         eager_ms, graph_ms = slowest(eager_ms, world, dev), slowest(graph_ms, world, dev)
+        # deferred rounds issued one launch per layer, then the accept (the round's
+        # rollbacks run inside the layer launches)
+        pp.parity = 0  # the in-place rounds above left the committed state in st.state
+        par = pp.parity
+        pplans[0].verify(par)
+        pplans[0].accept()
+        pplans[0]._flip(par)
+        lps = kb.layer_pingpongs(pp)
+        dl_plans = [kb.LayerDeferredRoundPlan(pp, lps, rows[r], out, logits[r], drafts[r], j_out, bonus_out,
+                                              keep_out, status, scratch, stream) for r in range(RP)]
+        deferred_ms = timed(lambda r: dl_plans[(r + 1) % RP]())
+        kb.kda_rollback_pingpong(pp, keep_out, dev_status=status, stream=stream)
+        if int(status.item()):
+            raise RuntimeError(f"device status {int(status.item()):#x} after the per-layer deferred steps")
+        deferred_ms = slowest(deferred_ms, world, dev)
         res["per_layer"] = {"launches_per_step": w.L + 3, "steps": Kp, "eager_ms_per_step": eager_ms,
                             "graph_ms_per_step": graph_ms,
-                            "graph_rows_per_s": job_rows_per_s(world, w.B, w.T, graph_ms)}
+                            "graph_rows_per_s": job_rows_per_s(world, w.B, w.T, graph_ms),
+                            "deferred": {"launches_per_step": w.L + 1, "eager_ms_per_step": deferred_ms,
+                                         "rows_per_s": job_rows_per_s(world, w.B, w.T, deferred_ms)}}
     # column-stash rollback (the alternative to snapshot + replay): the verify also
     # writes the state and ring after every row, the rollback copies the kept column
     col_bytes = w.L * w.B * w.H * w.T * (128 * 128 + 9 * 128) * 4

@@ -791,6 +791,57 @@ class DeferredRoundPlan:
         self._flip(p)
 
 
+class LayerDeferredRoundPlan:
+    """A deferred round issued the way a model issues it: one kda_verify_scan_deferred
+    per layer (each over that layer's views of the PingPong buffers and raw rows, in
+    layer order), then one spec_accept.  Each layer commits its own part of the
+    previous round.  ``layers`` are the per-layer PingPong views of ``pp``, made by
+    ``layer_pingpongs(pp)`` and shared by every plan of the sequence; bit-identical to
+    DeferredRoundPlan over all layers.
+    """
+
+    def __init__(self, pp: PingPong, layers: list, rows: dict, out, logits, drafts, j_out, bonus_out, keep_out,
+                 dev_status, scratch, stream=None):
+        self.pp, self.layers = pp, layers
+        self.full = DeferredRoundPlan(pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch,
+                                      stream)
+        self.plans = []
+        for l, lp in enumerate(layers):
+            rl = {n: t[l:l + 1] for n, t in rows.items()}
+            self.plans.append(DeferredRoundPlan(lp, rl, None if out is None else out[l:l + 1], logits, drafts, j_out,
+                                                bonus_out, keep_out, dev_status, scratch, stream))
+
+    def __call__(self):
+        p = self.pp.last
+        if p is None:
+            raise ValueError("a deferred round follows a ping-pong round")
+        for lp, plan in zip(self.layers, self.plans):
+            plan.verify(p)
+            plan._flip(p)
+        self.full.accept()
+        self.full._flip(p)
+
+
+def layer_pingpongs(pp: PingPong) -> list:
+    """Per-layer PingPong views of pp's buffers (layer-major, so each is contiguous),
+    with pp's parity and last round.  For LayerDeferredRoundPlan; the last round must be
+    recorded in pp by a ping-pong or deferred round over all layers."""
+    out = []
+    for l in range(pp.L):
+        st = LayerState(pp.states[0][l:l + 1], pp.rings[0][l:l + 1], pp.conv_w[l:l + 1])
+        lp = PingPong(st, spare_state=pp.states[1][l:l + 1], spare_ring=pp.rings[1][l:l + 1])
+        lp.parity, lp.last, lp.dtype = pp.parity, pp.last, pp.dtype
+        if pp.last is not None:
+            full = pp.cstash[pp.last]
+            rows = {n: t[l:l + 1] for n, t in zip(("q", "k", "v", "g", "beta"), pp.rows)} if pp.rows else None
+            if rows is not None:
+                lp.rows = [rows[n] for n in ("q", "k", "v", "g", "beta")]
+                lp.cstash[pp.last].rows = KdaRows(*(rows[n].data_ptr() for n in ("q", "k", "v", "g", "beta")))
+                lp.cstash[pp.last].T = full.T
+        out.append(lp)
+    return out
+
+
 class LayerRoundPlan:
     """One verify round issued the way a model issues it: one kda_verify_scan per layer
     (each over that layer's views, in layer order), then spec_accept, then one

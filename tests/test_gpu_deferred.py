@@ -207,3 +207,45 @@ def test_deferred_full_size_equals_separate(wl):
         assert bits_equal(a.state(), b.state()) and bits_equal(a.ring(), b.ring()), f"round {r}: post-round"
         assert bits_equal(a.states[a.last], b.states[b.last]) and bits_equal(a.rings[a.last], b.rings[b.last]), \
             f"round {r}: snapshot"
+
+
+def test_per_layer_deferred_rounds_equal_one_launch():
+    """A deferred round issued one launch per layer (as a model issues it) equals the
+    one-launch deferred round bit for bit."""
+    from gpu_util import to_dev
+    L, B, H = 3, 2, 5
+    w = synth.Workload("dl", L=L, B=B, H=H, T=6, bf16=True, V=300, rounds=5, seed=0x9939, accept="uniform")
+    state0, ring0, cw = small_case(w)
+    rows = [rows_to_dev(synth.all_rows(w, r), True) for r in range(w.rounds)]
+    logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
+    drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
+              for r in range(w.rounds)]
+
+    def case():
+        pp = kb.PingPong(layer_state(state0, ring0, cw))
+        j, bonus, keep = (torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(3))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        scratch = torch.empty(kb.spec_accept_scratch_bytes(B, w.T, w.V), dtype=torch.uint8, device="cuda")
+        out = torch.empty((L, B, w.T, H, 128), dtype=torch.float32, device="cuda")
+        first = kb.PingPongRoundPlan(pp, rows[0], out, logits[0], drafts[0], j, bonus, keep, status, scratch)
+        par = pp.parity
+        first.verify(par)
+        first.accept()
+        first._flip(par)
+        return pp, j, keep, status, scratch, out
+
+    pa, ja, ka, sa, xa, oa = case()
+    pb, jb, kb_, sb, xb, ob = case()
+    lps = kb.layer_pingpongs(pb)
+    for r in range(1, w.rounds):
+        kb.DeferredRoundPlan(pa, rows[r], oa, logits[r], drafts[r], ja, torch.empty_like(ja), ka, sa, xa)()
+        kb.LayerDeferredRoundPlan(pb, lps, rows[r], ob, logits[r], drafts[r], jb, torch.empty_like(jb), kb_, sb, xb)()
+        torch.cuda.synchronize()
+        assert torch.equal(ja, jb) and [int(x) for x in ja.cpu()] == list(synth.accept_targets(w, r))
+        assert bits_equal(oa, ob), f"round {r}: outputs"
+        assert bits_equal(pa.state(), pb.state()) and bits_equal(pa.ring(), pb.ring()), f"round {r}"
+        assert bits_equal(pa.states[pa.last], pb.states[pb.last]), f"round {r}: snapshot"
+    kb.kda_rollback_pingpong(pa, ka)
+    kb.kda_rollback_pingpong(pb, kb_)
+    torch.cuda.synchronize()
+    assert bits_equal(pa.state(), pb.state()) and int(sa[0]) == 0 and int(sb[0]) == 0
