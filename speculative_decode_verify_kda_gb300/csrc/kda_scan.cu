@@ -231,6 +231,20 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
                  : "memory");
 }
 
+// L2 prefetch of the 2D / 4D box at the given coordinates (a hint: no data is consumed,
+// so it may run before the previous kernel's results are visible)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *tm, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y) : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *tm, int c0, int c1, int c2, int c3)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
+}
+
 // 2D tensor copy shared -> global of the box at (x, y), tracked by bulk groups
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, int x, int y, uint32_t src)
 {
@@ -853,13 +867,12 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
     int u = next_live(p, blockIdx.x, n, lead && lane == 0);
     int u1 = u < n ? next_live(p, u + gridDim.x, n, lead && lane == 0) : n;
     int u2 = u1 < n ? next_live(p, u1 + gridDim.x, n, lead && lane == 0) : n;
+    // the second unit's state is requested once the first has landed, so that the
+    // first loads of all CTAs share the memory system with nothing else
     if (lead) {
         if (lane == 0 && u < n)
             issue_state(p, slot0, c.bar(B_STATE_FULL), u);
-        if (lane == 0 && u1 < n)
-            issue_state(p, slot0 + SLOT, c.bar(B_STATE_FULL + 1), u1);
         pend0 = u < n;
-        pend1 = u1 < n;
     }
     bool ok = true;
     int i = 0;  // items through the scan-input buffers so far
@@ -873,6 +886,11 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
         }
         if (lead) {
             (s ? pend1 : pend0) = false;
+            if (k == 0 && u1 < n) {
+                if (lane == 0)
+                    issue_state(p, slot0 + SLOT, c.bar(B_STATE_FULL + 1), u1);
+                pend1 = true;  // phase 0 of slot 1
+            }
             if (p.s_snap && lane == 0) {
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
@@ -962,12 +980,26 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     extern __shared__ unsigned char smem_raw[];
     unsigned char *sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const Layout lay{p.tcap, p.bf16 ? 2 : 4, p.nstg};
-    // launched as a programmatic dependent: wait for the previous kernel's results.
-    // The next kernel may be scheduled as soon as every CTA of this one is resident
-    // (it waits for this kernel's results in turn).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Ctl c{smem_addr(sm + lay.bars()), reinterpret_cast<volatile int *>(sm + lay.flag()), p.status};
+    const int n = p.L * p.B * p.H;  // below 2^31 / 128, checked at launch
+    const int wi = threadIdx.x >> 5;
+    // While the previous kernel finishes: L2 prefetches of the first two candidate
+    // units' states (the buffer a replaying unit reads) and of the first unit's raw rows
+    // of each stream, and the barrier set-up (shared memory only).
+    if ((threadIdx.x & 31) == 0) {
+        const int u0 = blockIdx.x, u1 = blockIdx.x + gridDim.x;
+        if (wi == 0) {
+            for (int b = 0; b < 4 && u0 < n; ++b)
+                tma_prefetch_2d(&p.tm_in, 32 * b, u0 * D);
+            for (int b = 0; b < 4 && u1 < n; ++b)
+                tma_prefetch_2d(&p.tm_in, 32 * b, u1 * D);
+        } else if (wi >= NSCAN && u0 < n) {
+            const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(u0), p.divH)), h = u0 - lb * p.H;
+            tma_prefetch_4d(&p.tm_rows[wi - NSCAN], 0, h, 0, lb);
+            if (p.keep_mode == DEFERRED)
+                tma_prefetch_4d(&p.tm_prev[wi - NSCAN], 0, h, 0, lb);
+        }
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(c.bar(B_STATE_FULL + s), 1);
@@ -981,8 +1013,11 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int n = p.L * p.B * p.H;  // below 2^31 / 128, checked at launch
-    const int wi = threadIdx.x >> 5;
+    // launched as a programmatic dependent: wait for the previous kernel's results.
+    // The next kernel may be scheduled as soon as every CTA of this one is resident
+    // (it waits for this kernel's results in turn).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (wi < NSCAN)
         scan_warp<COLS>(p, lay, sm, c, n);
     else
