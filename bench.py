@@ -270,6 +270,135 @@ def oracle_baseline(w, budget_s: float):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc):
+    """The deferred round end to end from pinned host buffers through the public API.
+
+    A round's inputs sit in one pinned host block (logits, drafts, then each raw-row
+    tensor whole).  nc == 1: one copy of the block, then the deferred round launch.
+    nc > 1: the launch (kda_verify_scan_deferred_staged) goes first; on a copy stream the
+    logits and drafts, then the raw rows of nc consecutive layer ranges are copied, each
+    range followed by a stream write of its ready flag, so the scan of the layers in place
+    overlaps the copy of the rest.  Then one accept, and j and the bonus come back in one
+    copy.  The next round's copies start after the host has read this round's j (a
+    round's inputs follow from the previous accept).  Leaves pp committed."""
+    import time
+
+    import torch
+    from speculative_decode_verify_kda_gb300 import binding as kb
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    HR = min(R, 4)
+    names = ("q", "k", "v", "g", "beta")
+    parts = [("logits", logits[0]), ("drafts", drafts[0])] + [(n, rows[0][n]) for n in names]
+    offs, off = {}, 0
+    for n, t in parts:
+        offs[n] = off
+        off += (t.numel() * t.element_size() + 255) // 256 * 256
+    block_bytes = off
+    lpf = -(-w.L // max(1, min(nc, w.L)))  # layers a flag covers
+    ranges = [(l0, min(w.L, l0 + lpf)) for l0 in range(0, w.L, lpf)]
+
+    def views(buf):
+        out_ = {}
+        for n, t in parts:
+            nb = t.numel() * t.element_size()
+            out_[n] = buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
+        return out_
+
+    host_blocks, host_views = [], []
+    for r in range(HR):
+        hb = torch.empty(block_bytes, dtype=torch.uint8).pin_memory()
+        hv = views(hb)
+        src = dict(rows[r], logits=logits[r], drafts=drafts[r])
+        for n, _ in parts:
+            hv[n].copy_(src[n].cpu())
+        host_blocks.append(hb)
+        host_views.append(hv)
+    # two device blocks: a deferred round reads the previous round's raw rows
+    dev_blocks = [torch.empty(block_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    dev_views = [views(b) for b in dev_blocks]
+    res_dev = torch.empty((3, w.B), dtype=torch.int32, device=dev)  # j, bonus, keep
+    host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for _, t in parts)
+    d2h = host_res.numel() * 4
+    Ke = max(1, min(args.e2e_steps, args.steps))
+    copy_stream = torch.cuda.Stream(dev)
+    copied = torch.cuda.Event()
+    flags = torch.zeros(len(ranges), dtype=torch.int32, device=dev)
+    staged = nc > 1
+    # kda_upload_rows_staged of host block r into device block b (one library call: the
+    # copies of each layer range, each followed by its flag)
+    uploads = {(r, b): kb.StagedUpload({n: dev_views[b][n] for n in names}, {n: host_views[r][n] for n in names},
+                                       flags, lpf) for r in range(HR) for b in range(2)}
+
+    def plan(b, cls, **kw):
+        v = dev_views[b]
+        return cls(pp, {n: v[n] for n in names}, out, v["logits"], v["drafts"], res_dev[0], res_dev[1], res_dev[2],
+                   status, scratch, stream, **kw)
+
+    eplans = [plan(b, kb.DeferredRoundPlan, **({"layer_ready": flags, "layers_per_flag": lpf} if staged else {}))
+              for b in range(2)]
+    eopen = plan(1, kb.PingPongRoundPlan)
+    epoch = [0]
+
+    def load_all(i):  # the whole block in one copy, on the launch stream
+        dev_blocks[i % 2].copy_(host_blocks[i % HR], non_blocking=True)
+
+    def load_staged(i):  # the rows by range with their flags, then the logits and drafts
+        b, r = i % 2, i % HR
+        uploads[(r, b)](epoch[0], copy_stream)
+        with torch.cuda.stream(copy_stream):
+            a0, a1 = offs["logits"], offs["q"]
+            dev_blocks[b][a0:a1].copy_(host_blocks[r][a0:a1], non_blocking=True)
+            copied.record(copy_stream)
+
+    def step(i):
+        rp = eplans[i % 2]
+        p = pp.last
+        if staged:
+            epoch[0] += 1
+            rp.verify(p, epoch[0])  # waits on the device for each layer range's flag
+            load_staged(i)
+            stream.wait_event(copied)  # the accept reads the logits
+        else:
+            load_all(i)
+            rp.verify(p)
+        rp.accept()
+        rp._flip(p)
+        host_res.copy_(res_dev[:2], non_blocking=True)
+        stream.synchronize()  # the host needs j and the bonus before the next round
+
+    # open the chain with a ping-pong round on device block 1, then deferred rounds
+    load_all(1)
+    par = pp.parity
+    eopen.verify(par)
+    eopen.accept()
+    eopen._flip(par)
+    for i in range(2, 5):
+        step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(5, 5 + Ke):
+        step(i)
+    barrier()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
+    e2e_ms = slowest(e2e_ms, world, dev)
+    kb.kda_rollback_pingpong(pp, res_dev[2], dev_status=status, stream=stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()):
+        raise RuntimeError(f"device status {int(status.item()):#x} after the e2e steps")
+    res = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": Ke}
+    if staged:
+        res["staged_layer_ranges"] = len(ranges)
+    return res
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     from speculative_decode_verify_kda_gb300 import binding as kb
@@ -488,82 +617,15 @@ def run_gpu(args, rank, world, local_rank):
         res["graph"] = {"ms_per_step": g_ms, "rows_per_s": job_rows_per_s(world, w.B, w.T, g_ms), "steps": K,
                         "round": "ping-pong verify, accept, rollback (separate launches), one graph per round"}
 
-    # e2e: host buffers through the public API, copies inside the timed region.  A round's
-    # inputs (raw rows, logits, drafts) sit in one pinned host block and go over in one
-    # copy into one device block the tensors are views of; j and the bonus come back in
-    # one copy.
+    # e2e: host buffers through the public API, copies inside the timed region (run_e2e):
+    # the raw rows stream in by layer range while the one launch scans the ranges already
+    # in place; the one-copy round (the whole block, then the launch) is reported beside it.
     if not args.no_e2e:
-        HR = min(R, 4)
-        parts = [(n, rows[0][n]) for n in ("q", "k", "v", "g", "beta")] + [("logits", logits[0]),
-                                                                           ("drafts", drafts[0])]
-        offs, off = {}, 0
-        for n, t in parts:
-            offs[n] = off
-            off += (t.numel() * t.element_size() + 255) // 256 * 256
-        block_bytes = off
-
-        def views(buf):
-            out_ = {}
-            for n, t in parts:
-                nb = t.numel() * t.element_size()
-                out_[n] = buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
-            return out_
-
-        host_blocks = []
-        for r in range(HR):
-            hb = torch.empty(block_bytes, dtype=torch.uint8).pin_memory()
-            hv = views(hb)
-            src = dict(rows[r], logits=logits[r], drafts=drafts[r])
-            for n, _ in parts:
-                hv[n].copy_(src[n].cpu())
-            host_blocks.append(hb)
-        # two device input sets: a deferred round reads the previous round's raw rows
-        dev_blocks = [torch.empty(block_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
-        dev_views = [views(b) for b in dev_blocks]
-        res_dev = torch.empty((3, w.B), dtype=torch.int32, device=dev)  # j, bonus, keep
-        host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for _, t in parts)
-        d2h = host_res.numel() * 4
-        Ke = max(1, min(args.e2e_steps, K))
-
-        def eplan(b, cls):
-            v = dev_views[b]
-            return cls(pp, {n: v[n] for n in ("q", "k", "v", "g", "beta")}, out, v["logits"], v["drafts"], res_dev[0],
-                       res_dev[1], res_dev[2], status, scratch, stream)
-
-        eplans = [eplan(b, kb.DeferredRoundPlan) for b in range(2)]
-        eopen = eplan(1, kb.PingPongRoundPlan)
-
-        def e2e_load(i):
-            dev_blocks[i % 2].copy_(host_blocks[i % HR], non_blocking=True)
-
-        def e2e_step(i):
-            e2e_load(i)
-            eplans[i % 2]()
-            host_res.copy_(res_dev[:2], non_blocking=True)
-            stream.synchronize()  # the host needs j and the bonus before the next round
-
-        # open the chain with a ping-pong round on buffer set 1, then deferred rounds
-        e2e_load(1)
-        par = pp.parity
-        eopen.verify(par)
-        eopen.accept()
-        eopen._flip(par)
-        for i in range(2, 5):
-            e2e_step(i)
-        barrier()
-        t0 = time.perf_counter()
-        for i in range(5, 5 + Ke):
-            e2e_step(i)
-        barrier()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
-        e2e_ms = slowest(e2e_ms, world, dev)
-        kb.kda_rollback_pingpong(pp, res_dev[2], dev_status=status, stream=stream)
-        if int(status.item()):
-            raise RuntimeError(f"device status {int(status.item()):#x} after the e2e steps")
-        res["e2e"] = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT,
-                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                      "ms_per_step": e2e_ms, "steps": Ke}
+        res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
+                             args.e2e_chunks)
+        if args.e2e_chunks != 1:
+            one = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, 1)
+            res["e2e"]["one_copy"] = {"value": one["value"], "ms_per_step": one["ms_per_step"]}
 
     # per-layer issue: one kda_verify_scan per layer (as a model issues them), then accept
     # and one all-layer rollback; eagerly, and replayed from CUDA graphs (one per round)
@@ -749,6 +811,9 @@ def main():
     ap.add_argument("--rounds", type=int, default=0, help="distinct input rounds kept resident (0: all)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="layer ranges the e2e round's raw rows are copied in (the one launch waits for each "
+                         "range's ready flag); 1: one copy, then the launch")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-per-layer", action="store_true", help="skip the per-layer (and CUDA graph) rounds")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the rounds")

@@ -211,6 +211,48 @@ int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *st, kda_stas
                              const kda_rows *rows, int T, float *out, int *dev_status, cudaStream_t stream);
 
 /*
+ * kda_verify_scan_deferred_staged -- kda_verify_scan_deferred whose raw rows may still
+ * be arriving when it starts (the round's inputs streamed in by layer range, so that the
+ * host-to-device copy overlaps the scan of the layers already in place; glm_spec.rs,
+ * VERIFY-ROW BATCHING: one launch a round).
+ * layer_ready: DEVICE array of unsigned flags; the rows of layer l (q, k, v, g and beta
+ * of every session) may be read once layer_ready[l / layers_per_flag] has reached
+ * `epoch` (compared as (int)(flag - epoch) >= 0, so a counter may wrap).  The caller
+ * copies each range of rows and then sets its flag in stream order after the copy,
+ * with kda_stream_write_u32 on the copy's stream.  The kernel waits for a flag at most
+ * one second; a flag that does not arrive sets KDA_ST_TIMEOUT in *dev_status and the
+ * launch ends early, its results undefined.  The previous round's rows (stash->rows)
+ * must be in place.  Everything else, including the results, is as for
+ * kda_verify_scan_deferred.  layers_per_flag must be >= 1; layer_ready 4-byte aligned.
+ */
+int kda_verify_scan_deferred_staged(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
+                                    const int *prev_keep, const kda_rows *rows, int T, float *out,
+                                    const unsigned *layer_ready, int layers_per_flag, unsigned epoch,
+                                    int *dev_status, cudaStream_t stream);
+
+/*
+ * kda_stream_write_u32 -- *flag = value (a 4-byte aligned device address) in the order
+ * of `stream`, written by the stream itself (a stream memory operation, no kernel), as
+ * the ready flags of kda_verify_scan_deferred_staged want.  KDA_ECUDA when the driver
+ * refuses it.
+ */
+int kda_stream_write_u32(unsigned *flag, unsigned value, cudaStream_t stream);
+
+/*
+ * kda_upload_rows_staged -- the host-to-device copy that feeds
+ * kda_verify_scan_deferred_staged: for each range of layers_per_flag layers (the last
+ * may be shorter), one cudaMemcpyAsync per raw-row tensor (q, k, v, g, beta, layout as
+ * for kda_verify_scan) of that range from src (host memory, pinned for the copies to be
+ * asynchronous) to dst (device), then layer_ready[range] = epoch, all in the order of
+ * `stream` (a stream other than the launch's, so that the copies overlap the scan).
+ * dims gives L, B, H and the element type; T the rows a round.  Allocates nothing and
+ * does not synchronise.  KDA_EINVAL for NULL pointers, T outside 1..15 or
+ * layers_per_flag < 1; KDA_ECUDA when a copy or the flag write is refused.
+ */
+int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_rows *src, int T,
+                           unsigned *layer_ready, int layers_per_flag, unsigned epoch, cudaStream_t stream);
+
+/*
  * Rounds whose length differs per session (variable T inside one batched grid).
  * glm_spec.rs, glm5_conf_keep and the p-min break of the draft chain, and dflash.rs,
  * DsparkVtPolicy / dspark_confidence_vt / dspark_slot_confidence_vt: each session

@@ -28,12 +28,13 @@ MEM_HOST, MEM_DEVICE = 0, 1
 
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_pingpong",
-           "kda_verify_scan_deferred",
+           "kda_verify_scan_deferred", "kda_verify_scan_deferred_staged", "kda_stream_write_u32",
+           "kda_upload_rows_staged",
            "kda_verify_scan_cols",
            "kda_rollback_cols", "spec_accept_var",
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 4
+ABI_VERSION = 5
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -100,6 +101,15 @@ def lib(path: str | None = None):
     L.kda_verify_scan_deferred.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                            ctypes.POINTER(KdaStashC), vp, ctypes.POINTER(KdaRows), ci, vp, vp, vp]
     L.kda_verify_scan_deferred.restype = ci
+    L.kda_verify_scan_deferred_staged.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                                  ctypes.POINTER(KdaStashC), vp, ctypes.POINTER(KdaRows), ci, vp, vp,
+                                                  ci, ctypes.c_uint, vp, vp]
+    L.kda_verify_scan_deferred_staged.restype = ci
+    L.kda_stream_write_u32.argtypes = [vp, ctypes.c_uint, vp]
+    L.kda_stream_write_u32.restype = ci
+    L.kda_upload_rows_staged.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaRows), ctypes.POINTER(KdaRows),
+                                         ci, vp, ci, ctypes.c_uint, vp]
+    L.kda_upload_rows_staged.restype = ci
     L.kda_verify_scan_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                        ctypes.POINTER(KdaRows), ci, vp, vp, vp, vp]
     L.kda_verify_scan_cols.restype = ci
@@ -410,6 +420,77 @@ def kda_verify_scan_deferred(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Te
     pp.cstash[1 - p].rows, pp.cstash[1 - p].T = rows, T
     pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, 1 - p, p
     return pp
+
+
+def kda_verify_scan_deferred_staged(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Tensor,
+                                    layer_ready: torch.Tensor, layers_per_flag: int, epoch: int,
+                                    out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                                    stream=None) -> PingPong:
+    """kda_verify_scan_deferred whose raw rows of layer l may be read once
+    layer_ready[l // layers_per_flag] has reached epoch (see kda_stream_write_u32).
+    layer_ready: device int32 flags (compared as unsigned)."""
+    if pp.last is None:
+        raise ValueError("a deferred round follows a ping-pong round (no previous round to commit)")
+    nflags = -(-pp.L // max(1, int(layers_per_flag)))
+    _dev(layer_ready, "layer_ready", torch.int32, (nflags,))
+    shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
+    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
+    if dt != pp.dtype:
+        raise TypeError("the raw rows must have the previous round's element type")
+    if out is not None:
+        _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
+    _dev(prev_keep, "prev_keep", torch.int32, (pp.B,))
+    p = pp.last
+    prev = pp.cstash[p]
+    cst = KdaLayerState(pp.states[1 - p].data_ptr(), pp.rings[1 - p].data_ptr(), pp.conv_w.data_ptr())
+    cstash = KdaStashC(pp.states[p].data_ptr(), pp.rings[p].data_ptr(), prev.rows, prev.T)
+    dims = pp.dims(dt)
+    rc = lib().kda_verify_scan_deferred_staged(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(cstash),
+                                               _ptr(prev_keep), ctypes.byref(rows), T, _ptr(out), _ptr(layer_ready),
+                                               int(layers_per_flag), ctypes.c_uint(epoch & 0xffffffff),
+                                               _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+    _check("kda_verify_scan_deferred_staged", rc)
+    pp.cstash[1 - p].rows, pp.cstash[1 - p].T = rows, T
+    pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, 1 - p, p
+    return pp
+
+
+def kda_stream_write_u32(flag: torch.Tensor, value: int, stream=None) -> None:
+    """flag[0] = value in the order of ``stream``, written by the stream itself (a stream
+    memory operation): the ready flags of kda_verify_scan_deferred_staged.  flag: a
+    device int32 tensor (its first element is written)."""
+    if not isinstance(flag, torch.Tensor) or not flag.is_cuda or flag.dtype != torch.int32 or flag.numel() < 1:
+        raise TypeError("flag must be a device int32 tensor")
+    _check("kda_stream_write_u32", lib().kda_stream_write_u32(_ptr(flag), ctypes.c_uint(value & 0xffffffff),
+                                                              ctypes.c_void_p(_stream(stream))))
+
+
+class StagedUpload:
+    """kda_upload_rows_staged for one pair of raw-row sets: ``host`` (pinned CPU tensors)
+    into ``dev`` (device tensors of the same shapes and element type), by ranges of
+    layers_per_flag layers, each range's flag in ``layer_ready`` set to the call's epoch
+    after its copies.  ``__call__(epoch, stream)`` issues the copies on ``stream``."""
+
+    def __init__(self, dev: dict, host: dict, layer_ready: torch.Tensor, layers_per_flag: int):
+        names = ("q", "k", "v", "g", "beta")
+        L_, B, T, H = (int(x) for x in dev["q"].shape[:4])
+        for n in names:
+            if tuple(host[n].shape) != tuple(dev[n].shape) or host[n].dtype != dev[n].dtype:
+                raise ValueError(f"host and device {n} must have the same shape and element type")
+            if not dev[n].is_cuda or host[n].is_cuda or not host[n].is_contiguous() or not dev[n].is_contiguous():
+                raise ValueError(f"{n}: dev must be a contiguous device tensor and host a contiguous CPU tensor")
+        dt = BF16 if dev["q"].dtype == torch.bfloat16 else F32
+        _dev(layer_ready, "layer_ready", torch.int32, (-(-L_ // max(1, int(layers_per_flag))),))
+        self.dims = KdaDims(L_, B, H, D, D, dt)
+        self.dst = KdaRows(*(dev[n].data_ptr() for n in names))
+        self.src = KdaRows(*(host[n].data_ptr() for n in names))
+        self.T, self.flags, self.lpf = T, layer_ready, int(layers_per_flag)
+        self._keep = (dev, host)
+
+    def __call__(self, epoch: int, stream=None):
+        _check("kda_upload_rows_staged", lib().kda_upload_rows_staged(
+            ctypes.byref(self.dims), ctypes.byref(self.dst), ctypes.byref(self.src), self.T, _ptr(self.flags),
+            self.lpf, ctypes.c_uint(epoch & 0xffffffff), ctypes.c_void_p(_stream(stream))))
 
 
 def kda_rollback_pingpong(pp: PingPong, keep, t_rows=None, dev_status: torch.Tensor | None = None,
@@ -733,8 +814,8 @@ class DeferredRoundPlan:
     """
 
     def __init__(self, pp: PingPong, rows: dict, out, logits, drafts, j_out, bonus_out, keep_out, dev_status,
-                 scratch, stream=None):
-        self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch)
+                 scratch, stream=None, layer_ready=None, layers_per_flag: int = 1):
+        self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch, layer_ready)
         self.pp = pp
         shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
         crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
@@ -754,13 +835,23 @@ class DeferredRoundPlan:
         s = ctypes.c_void_p(_stream(stream))
         self._verify = [(ctypes.byref(self.dims), ctypes.byref(self.cst[p]), ctypes.byref(self.cstash[p]),
                          _ptr(keep_out), ctypes.byref(self.crows), T, _ptr(out), _ptr(dev_status), s) for p in (0, 1)]
+        # staged raw rows (kda_verify_scan_deferred_staged): the epoch is given per call
+        self._staged = None
+        if layer_ready is not None:
+            _dev(layer_ready, "layer_ready", torch.int32, (-(-pp.L // max(1, int(layers_per_flag))),))
+            self._staged = [(ctypes.byref(self.dims), ctypes.byref(self.cst[p]), ctypes.byref(self.cstash[p]),
+                             _ptr(keep_out), ctypes.byref(self.crows), T, _ptr(out), _ptr(layer_ready),
+                             int(layers_per_flag)) for p in (0, 1)]
+            self._staged_tail = (_ptr(dev_status), s)
         nbytes = scratch.numel() * scratch.element_size()
         self._accept = (_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out), _ptr(bonus_out),
                         _ptr(keep_out), _ptr(dev_status), _ptr(scratch), nbytes, s)
         self._tensors, self._dt = tensors, dt
         self._L = lib()
 
-    def verify(self, p: int):
+    def verify(self, p: int, epoch: int | None = None):
+        """The deferred verify launch; with staged rows (layer_ready given) ``epoch`` is
+        the flag value that marks this call's rows as in place."""
         pp = self.pp
         prev = pp.cstash[p]
         # the library swaps the pointers in the structs it is given: restore them
@@ -768,6 +859,14 @@ class DeferredRoundPlan:
         c.state, c.conv_ring = pp.states[1 - p].data_ptr(), pp.rings[1 - p].data_ptr()
         st.state_snap, st.ring_snap = pp.states[p].data_ptr(), pp.rings[p].data_ptr()
         st.rows, st.T = prev.rows, prev.T
+        if self._staged is not None:
+            if epoch is None:
+                raise ValueError("a plan with staged rows needs the call's epoch")
+            rc = self._L.kda_verify_scan_deferred_staged(*self._staged[p], ctypes.c_uint(epoch & 0xffffffff),
+                                                         *self._staged_tail)
+            if rc:
+                _check("kda_verify_scan_deferred_staged", rc)
+            return
         rc = self._L.kda_verify_scan_deferred(*self._verify[p])
         if rc:
             _check("kda_verify_scan_deferred", rc)
@@ -795,20 +894,24 @@ class LayerDeferredRoundPlan:
     """A deferred round issued the way a model issues it: one kda_verify_scan_deferred
     per layer (each over that layer's views of the PingPong buffers and raw rows, in
     layer order), then one spec_accept.  Each layer commits its own part of the
-    previous round.  ``layers`` are the per-layer PingPong views of ``pp``, made by
-    ``layer_pingpongs(pp)`` and shared by every plan of the sequence; bit-identical to
-    DeferredRoundPlan over all layers.
+    previous round.  ``layers`` are the PingPong views of ``pp`` made by
+    ``layer_pingpongs(pp, bounds)`` and shared by every plan of the sequence (one view a
+    layer by default; ``bounds`` groups consecutive layers into one launch); the
+    results are bit-identical to DeferredRoundPlan over all layers.
     """
 
     def __init__(self, pp: PingPong, layers: list, rows: dict, out, logits, drafts, j_out, bonus_out, keep_out,
-                 dev_status, scratch, stream=None):
+                 dev_status, scratch, stream=None, bounds=None):
+        bounds = layer_bounds(pp.L, bounds)
+        if len(bounds) != len(layers):
+            raise ValueError("one PingPong view per layer range")
         self.pp, self.layers = pp, layers
         self.full = DeferredRoundPlan(pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch,
                                       stream)
         self.plans = []
-        for l, lp in enumerate(layers):
-            rl = {n: t[l:l + 1] for n, t in rows.items()}
-            self.plans.append(DeferredRoundPlan(lp, rl, None if out is None else out[l:l + 1], logits, drafts, j_out,
+        for (l0, l1), lp in zip(bounds, layers):
+            rl = {n: t[l0:l1] for n, t in rows.items()}
+            self.plans.append(DeferredRoundPlan(lp, rl, None if out is None else out[l0:l1], logits, drafts, j_out,
                                                 bonus_out, keep_out, dev_status, scratch, stream))
 
     def __call__(self):
@@ -822,18 +925,35 @@ class LayerDeferredRoundPlan:
         self.full._flip(p)
 
 
-def layer_pingpongs(pp: PingPong) -> list:
-    """Per-layer PingPong views of pp's buffers (layer-major, so each is contiguous),
-    with pp's parity and last round.  For LayerDeferredRoundPlan; the last round must be
-    recorded in pp by a ping-pong or deferred round over all layers."""
+def layer_bounds(L: int, bounds=None) -> list:
+    """[(l0, l1), ...]: consecutive layer ranges covering 0..L-1, one a layer by default;
+    an int n splits the layers into n ranges of near-equal length."""
+    if bounds is None:
+        return [(l, l + 1) for l in range(L)]
+    if isinstance(bounds, int):
+        n = max(1, min(bounds, L))
+        edges = [L * i // n for i in range(n + 1)]
+        return [(edges[i], edges[i + 1]) for i in range(n)]
+    bounds = [(int(a), int(b)) for a, b in bounds]
+    if not bounds or bounds[0][0] != 0 or bounds[-1][1] != L or any(
+            b0[1] != b1[0] for b0, b1 in zip(bounds, bounds[1:])) or any(a >= b for a, b in bounds):
+        raise ValueError("layer ranges must be consecutive, non-empty and cover 0..L-1")
+    return bounds
+
+
+def layer_pingpongs(pp: PingPong, bounds=None) -> list:
+    """PingPong views of pp's buffers over consecutive layer ranges (``layer_bounds``:
+    one view a layer by default; layer-major, so each is contiguous), with pp's parity
+    and last round.  For LayerDeferredRoundPlan and per-range deferred rounds; the last
+    round must be recorded in pp by a ping-pong or deferred round over all layers."""
     out = []
-    for l in range(pp.L):
-        st = LayerState(pp.states[0][l:l + 1], pp.rings[0][l:l + 1], pp.conv_w[l:l + 1])
-        lp = PingPong(st, spare_state=pp.states[1][l:l + 1], spare_ring=pp.rings[1][l:l + 1])
+    for l0, l1 in layer_bounds(pp.L, bounds):
+        st = LayerState(pp.states[0][l0:l1], pp.rings[0][l0:l1], pp.conv_w[l0:l1])
+        lp = PingPong(st, spare_state=pp.states[1][l0:l1], spare_ring=pp.rings[1][l0:l1])
         lp.parity, lp.last, lp.dtype = pp.parity, pp.last, pp.dtype
         if pp.last is not None:
             full = pp.cstash[pp.last]
-            rows = {n: t[l:l + 1] for n, t in zip(("q", "k", "v", "g", "beta"), pp.rows)} if pp.rows else None
+            rows = {n: t[l0:l1] for n, t in zip(("q", "k", "v", "g", "beta"), pp.rows)} if pp.rows else None
             if rows is not None:
                 lp.rows = [rows[n] for n in ("q", "k", "v", "g", "beta")]
                 lp.cstash[pp.last].rows = KdaRows(*(rows[n].data_ptr() for n in ("q", "k", "v", "g", "beta")))

@@ -134,6 +134,10 @@ struct ScanParams {
     const int *keep_dev;   // KEEP_DEVICE: [B]
     const int *rows_dev;   // ROWS_DEVICE, or KEEP_DEVICE after a per-session round: [B] row counts
     int *status;           // nullable device status word
+    const unsigned *ready; // nullable: this call's raw rows of layer l are in place once
+                           // ready[l / ready_lpf] has reached epoch (written by the copy's stream)
+    unsigned epoch;
+    int ready_lpf;
     int L, B, H;
     FastDiv divH, divB;    // u / H and lb / B
     int T_rows;            // row count of the raw-row tensors
@@ -424,6 +428,54 @@ __device__ __forceinline__ Item next_item(const ScanParams &p, Item it, int n)
     return first_item(p, next_live(p, it.u + gridDim.x, n, false), n);
 }
 
+// Staged raw rows: before a prologue warp copies an item's rows of this call (part 1)
+// it waits, bounded like warp_wait, until the flag of the item's layer range has reached
+// the call's epoch.  The flag is written by a stream memory operation after the rows'
+// host-to-device copy on another stream (no kernel writes it).  Lane 0 reads it with
+// acquire semantics; the proxy fence orders the tensor copies that follow after it.  A
+// warp walks its units in increasing layer order, so it reads each flag once: last_f is
+// the flag it saw set last.
+__device__ bool rows_ready(const ScanParams &p, const Ctl &c, int u, int part, int lane, int &last_f)
+{
+    if (!p.ready || part == 0)
+        return true;
+    const uint32_t lb = fdiv(static_cast<uint32_t>(u), p.divH);
+    const int fi = static_cast<int>(fdiv(lb, p.divB)) / p.ready_lpf;
+    if (fi == last_f)
+        return true;
+    int ok = 1;
+    if (lane == 0) {
+        const unsigned *f = p.ready + fi;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t n = 0;; ++n) {
+            unsigned v;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+            if (static_cast<int>(v - p.epoch) >= 0)
+                break;
+            if ((n & 15) == 15) {
+                if (*c.abort != 0) {
+                    ok = 0;
+                    break;
+                }
+                if (globaltimer_ns() - t0 > WAIT_NS) {
+                    if (c.status)
+                        atomicOr(c.status, KDA_ST_TIMEOUT);
+                    *c.abort = 1;
+                    ok = 0;
+                    break;
+                }
+            }
+            __nanosleep(n < 64 ? 32 : 256);
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    if (ok)
+        last_f = fi;
+    return ok != 0;
+}
+
 // ---- copies issued by scan warp 0 (states) and the prologue warps (raw rows) ----------
 // Unit u's 64 KiB state into a slot: four boxes of 32 columns x 128 rows (lane 0).  A
 // DEFERRED unit with nothing to replay starts from the other buffer (tm_in2).
@@ -667,15 +719,20 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
     float4 win[3];  // the conv window carried from a unit's replay item into its verify item
     Item it = first_item(p, next_live(p, blockIdx.x, n, false), n);
     Stager sg{it, false, false, 0, 0};
+    bool ok = true;
+    int last_f = -1;  // the staged-rows flag this warp saw set last
     for (int b = 0; b < lay.nstg && sg.next.u < n; ++b) {  // the first nstg items' raw rows
+        if (!rows_ready(p, c, sg.next.u, sg.next.part, lane, last_f)) {
+            ok = false;
+            break;
+        }
         issue_stream(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + 4 * b + pw), sg.next, pw, lane);
         (b ? sg.pend1 : sg.pend0) = true;
         sg.next = next_item(p, sg.next, n);
     }
-    bool ok = true;
-    if (it.u < n)
+    if (ok && it.u < n)
         load_pre(p, it, pw, lane, pr);
-    for (int i = 0; it.u < n; ++i) {
+    for (int i = 0; ok && it.u < n; ++i) {
         const int b = i & 1;
         const Unit x = unit_of(p, it.u);
         const int T = it.part == 0 ? x.R : x.T;
@@ -715,6 +772,10 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
         // loads below: the proxy fence would wait for them), then the next item's conv
         // weights, ring and beta
         if (sg.next.u < n) {
+            if (!rows_ready(p, c, sg.next.u, sg.next.part, lane, last_f)) {
+                ok = false;
+                break;
+            }
             issue_stream(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + 4 * sb + pw), sg.next, pw, lane);
             (sb ? sg.pend1 : sg.pend0) = true;
             (sb ? sg.par1 : sg.par0) = (m + 1) & 1;
@@ -1380,9 +1441,14 @@ extern "C" int kda_verify_scan_pingpong(const kda_dims *dims, const kda_layer_st
     return verify_common(dims, st, rows, T, t_rows, t_mem, out, stash, dev_status, true, stream);
 }
 
-extern "C" int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
-                                        const int *prev_keep, const kda_rows *rows, int T, float *out,
-                                        int *dev_status, cudaStream_t stream)
+namespace kda {
+namespace {
+
+// Shared body of kda_verify_scan_deferred and kda_verify_scan_deferred_staged (ready:
+// nullptr for rows already in place).
+int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, const int *prev_keep,
+                    const kda_rows *rows, int T, float *out, const unsigned *ready, int lpf, unsigned epoch,
+                    int *dev_status, cudaStream_t stream)
 {
     int rc = check_common(dims, st);
     if (rc)
@@ -1428,6 +1494,9 @@ extern "C" int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *s
         p.T_run = T;
         p.tcap = std::max(T, stash->T);
         p.bf16 = dims->dtype == KDA_BF16;
+        p.ready = ready;
+        p.ready_lpf = lpf;
+        p.epoch = epoch;
         if ((rc = launch_scan(p, stash->state_snap, stream, st->state, &stash->rows)))
             return rc;
     }
@@ -1438,6 +1507,107 @@ extern "C" int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *s
     stash->rows = rows ? *rows : kda_rows{};
     stash->T = T;
     return ok();
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
+                                        const int *prev_keep, const kda_rows *rows, int T, float *out,
+                                        int *dev_status, cudaStream_t stream)
+{
+    return kda::deferred_common(dims, st, stash, prev_keep, rows, T, out, nullptr, 1, 0, dev_status, stream);
+}
+
+extern "C" int kda_verify_scan_deferred_staged(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
+                                               const int *prev_keep, const kda_rows *rows, int T, float *out,
+                                               const unsigned *layer_ready, int layers_per_flag, unsigned epoch,
+                                               int *dev_status, cudaStream_t stream)
+{
+    if (!layer_ready || (reinterpret_cast<uintptr_t>(layer_ready) & 3u))
+        return kda::fail(KDA_EINVAL, "layer_ready must be a 4-byte aligned device array of flags");
+    if (layers_per_flag < 1)
+        return kda::fail(KDA_EINVAL, "layers_per_flag must be >= 1");
+    return kda::deferred_common(dims, st, stash, prev_keep, rows, T, out, layer_ready, layers_per_flag, epoch,
+                                dev_status, stream);
+}
+
+namespace kda {
+namespace {
+
+// *flag = value in stream order, by the stream (cuStreamWriteValue32 from the driver)
+int write_flag(unsigned *flag, unsigned value, cudaStream_t stream)
+{
+    using WriteValue = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+    static const WriteValue write = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<WriteValue>(nullptr);
+        return reinterpret_cast<WriteValue>(f);
+    }();
+    if (!write)
+        return fail(KDA_ECUDA, "cuStreamWriteValue32 is not available from the CUDA driver");
+    const CUresult r = write(reinterpret_cast<CUstream>(stream), reinterpret_cast<CUdeviceptr>(flag), value,
+                             CU_STREAM_WRITE_VALUE_DEFAULT);
+    if (r != CUDA_SUCCESS)
+        return fail(KDA_ECUDA, "cuStreamWriteValue32 failed with CUresult " + std::to_string(static_cast<int>(r)));
+    return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_stream_write_u32(unsigned *flag, unsigned value, cudaStream_t stream)
+{
+    if (!flag || (reinterpret_cast<uintptr_t>(flag) & 3u))
+        return kda::fail(KDA_EINVAL, "flag must be a 4-byte aligned device pointer");
+    const int rc = kda::write_flag(flag, value, stream);
+    return rc ? rc : kda::ok();
+}
+
+extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_rows *src, int T,
+                                      unsigned *layer_ready, int layers_per_flag, unsigned epoch,
+                                      cudaStream_t stream)
+{
+    if (!dims || !dst || !src)
+        return kda::fail(KDA_EINVAL, "dims, dst and src must not be NULL");
+    if (dims->L < 0 || dims->B < 0 || dims->H < 0)
+        return kda::fail(KDA_EINVAL, "L, B, H must be >= 0");
+    if (dims->dtype != KDA_F32 && dims->dtype != KDA_BF16)
+        return kda::fail(KDA_EINVAL, "dtype must be KDA_F32 or KDA_BF16");
+    if (T < 1 || T > KDA_TMAX)
+        return kda::fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
+    if (!layer_ready || (reinterpret_cast<uintptr_t>(layer_ready) & 3u))
+        return kda::fail(KDA_EINVAL, "layer_ready must be a 4-byte aligned device array of flags");
+    if (layers_per_flag < 1)
+        return kda::fail(KDA_EINVAL, "layers_per_flag must be >= 1");
+    const void *d[5] = {dst->q, dst->k, dst->v, dst->g, dst->beta};
+    const void *h[5] = {src->q, src->k, src->v, src->g, src->beta};
+    const size_t es = dims->dtype == KDA_BF16 ? 2 : 4;
+    const size_t per_layer = static_cast<size_t>(dims->B) * T * dims->H * es;  // beta; x128 for q, k, v, g
+    if (per_layer == 0 || dims->L == 0)
+        return kda::ok();
+    for (int i = 0; i < 5; ++i)
+        if (!d[i] || !h[i])
+            return kda::fail(KDA_EINVAL, "every raw-row pointer of dst and src must be non-NULL");
+    for (int l0 = 0, f = 0; l0 < dims->L; l0 += layers_per_flag, ++f) {
+        const int n = std::min(layers_per_flag, dims->L - l0);
+        for (int i = 0; i < 5; ++i) {
+            const size_t row = i < 4 ? per_layer * D : per_layer;
+            const cudaError_t e = cudaMemcpyAsync(static_cast<char *>(const_cast<void *>(d[i])) + row * l0,
+                                                  static_cast<const char *>(h[i]) + row * l0, row * n,
+                                                  cudaMemcpyHostToDevice, stream);
+            if (e != cudaSuccess)
+                return kda::fail(KDA_ECUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
+        }
+        const int rc = kda::write_flag(layer_ready + f, epoch, stream);
+        if (rc)
+            return rc;
+    }
+    return kda::ok();
 }
 
 namespace kda {

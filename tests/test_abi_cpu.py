@@ -255,3 +255,37 @@ def test_deferred_rejects_on_host(L):
     assert L.kda_verify_scan_deferred(ctypes.byref(empty), ctypes.byref(st2), ctypes.byref(s2), None,
                                       ctypes.byref(rows), 5, None, None, None) == kb.OK
     assert st2.state == FAKE + 0x1000 and s2.state_snap == FAKE and s2.T == 5
+
+
+def test_layer_bounds_cover_the_layers_in_order():
+    assert kb.layer_bounds(3) == [(0, 1), (1, 2), (2, 3)]
+    assert kb.layer_bounds(34, 4) == [(0, 8), (8, 17), (17, 25), (25, 34)]
+    assert kb.layer_bounds(2, 5) == [(0, 1), (1, 2)]  # at most one range a layer
+    assert kb.layer_bounds(5, [(0, 2), (2, 5)]) == [(0, 2), (2, 5)]
+    for bad in ([(0, 2), (3, 5)], [(1, 5)], [(0, 4)], [(0, 0), (0, 5)], []):
+        with pytest.raises(ValueError):
+            kb.layer_bounds(5, bad)
+
+
+def test_staged_deferred_and_flag_writer_reject_on_host(L):
+    dims, st, rows = _state(B=2)
+    prev = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)
+
+    def call(ready=FAKE + 0x4000, lpf=1, keep=FAKE + 0x3000):
+        return L.kda_verify_scan_deferred_staged(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(prev), keep,
+                                                 ctypes.byref(rows), 8, None, ready, lpf, 1, None, None)
+    assert call(ready=None) == kb.EINVAL and b"layer_ready" in L.kda_last_error()
+    assert call(ready=FAKE + 0x4002) == kb.EINVAL
+    assert call(lpf=0) == kb.EINVAL and b"layers_per_flag" in L.kda_last_error()
+    assert call(keep=None) == kb.EINVAL  # the deferred round's own checks still apply
+    assert L.kda_stream_write_u32(None, 1, None) == kb.EINVAL
+    assert L.kda_stream_write_u32(FAKE + 2, 1, None) == kb.EINVAL
+
+    def upload(dst=rows, src=rows, T=8, ready=FAKE + 0x4000, lpf=1, d=dims):
+        return L.kda_upload_rows_staged(ctypes.byref(d), ctypes.byref(dst) if dst is not None else None,
+                                        ctypes.byref(src) if src is not None else None, T, ready, lpf, 1, None)
+    assert upload(dst=None) == kb.EINVAL and upload(src=None) == kb.EINVAL
+    assert upload(T=0) == kb.EINVAL and upload(T=16) == kb.EINVAL
+    assert upload(ready=None) == kb.EINVAL and upload(ready=FAKE + 1) == kb.EINVAL and upload(lpf=0) == kb.EINVAL
+    assert upload(src=kb.KdaRows(FAKE, FAKE, None, FAKE, FAKE)) == kb.EINVAL
+    assert upload(d=kb.KdaDims(0, 2, 64, 128, 128, kb.BF16)) == kb.OK  # nothing to copy

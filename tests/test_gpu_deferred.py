@@ -209,7 +209,8 @@ def test_deferred_full_size_equals_separate(wl):
             f"round {r}: snapshot"
 
 
-def test_per_layer_deferred_rounds_equal_one_launch():
+@pytest.mark.parametrize("bounds", [None, [(0, 2), (2, 3)]], ids=["per-layer", "ranges"])
+def test_per_layer_deferred_rounds_equal_one_launch(bounds):
     """A deferred round issued one launch per layer (as a model issues it) equals the
     one-launch deferred round bit for bit."""
     from gpu_util import to_dev
@@ -236,10 +237,11 @@ def test_per_layer_deferred_rounds_equal_one_launch():
 
     pa, ja, ka, sa, xa, oa = case()
     pb, jb, kb_, sb, xb, ob = case()
-    lps = kb.layer_pingpongs(pb)
+    lps = kb.layer_pingpongs(pb, bounds)
     for r in range(1, w.rounds):
         kb.DeferredRoundPlan(pa, rows[r], oa, logits[r], drafts[r], ja, torch.empty_like(ja), ka, sa, xa)()
-        kb.LayerDeferredRoundPlan(pb, lps, rows[r], ob, logits[r], drafts[r], jb, torch.empty_like(jb), kb_, sb, xb)()
+        kb.LayerDeferredRoundPlan(pb, lps, rows[r], ob, logits[r], drafts[r], jb, torch.empty_like(jb), kb_, sb, xb,
+                                  bounds=bounds)()
         torch.cuda.synchronize()
         assert torch.equal(ja, jb) and [int(x) for x in ja.cpu()] == list(synth.accept_targets(w, r))
         assert bits_equal(oa, ob), f"round {r}: outputs"
@@ -249,3 +251,93 @@ def test_per_layer_deferred_rounds_equal_one_launch():
     kb.kda_rollback_pingpong(pb, kb_)
     torch.cuda.synchronize()
     assert bits_equal(pa.state(), pb.state()) and int(sa[0]) == 0 and int(sb[0]) == 0
+
+
+@pytest.mark.parametrize("lpf,upload", [(1, "library"), (2, "library"), (2, "torch")])
+def test_staged_deferred_rounds_equal_deferred_rounds(lpf, upload):
+    """Deferred rounds whose raw rows arrive while the launch runs (copied from pinned host
+    memory by layer range on a side stream, each range's flag set after its copy, by
+    kda_upload_rows_staged or by torch copies and kda_stream_write_u32) give the bits of
+    deferred rounds on resident rows."""
+    ensure_built()
+    from gpu_util import to_dev
+    L, B, H = 3, 2, 5
+    w = synth.Workload("st", L=L, B=B, H=H, T=6, bf16=True, V=300, rounds=5, seed=0x5791, accept="uniform")
+    state0, ring0, cw = small_case(w)
+    host_rows = [synth.all_rows(w, r) for r in range(w.rounds)]
+    rows = [rows_to_dev(hr, True) for hr in host_rows]
+    logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
+    drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
+              for r in range(w.rounds)]
+    bounds = [(l0, min(L, l0 + lpf)) for l0 in range(0, L, lpf)]  # flag f covers layers f*lpf ..
+    flags = torch.zeros(-(-L // lpf), dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+
+    def case():
+        pp = kb.PingPong(layer_state(state0, ring0, cw))
+        j, bonus, keep = (torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(3))
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        scratch = torch.empty(kb.spec_accept_scratch_bytes(B, w.T, w.V), dtype=torch.uint8, device="cuda")
+        out = torch.empty((L, B, w.T, H, 128), dtype=torch.float32, device="cuda")
+        first = kb.PingPongRoundPlan(pp, rows[0], out, logits[0], drafts[0], j, bonus, keep, status, scratch)
+        par = pp.parity
+        first.verify(par)
+        first.accept()
+        first._flip(par)
+        return pp, j, bonus, keep, status, scratch, out
+
+    pa, ja, ba, ka, sa, xa, oa = case()
+    pb, jb, bb, kb_, sb, xb, ob = case()
+    for r in range(1, w.rounds):
+        kb.DeferredRoundPlan(pa, rows[r], oa, logits[r], drafts[r], ja, ba, ka, sa, xa)()
+        # this round's rows for pb: fresh device tensors, filled while the launch waits
+        pinned = {n: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
+                  for n, a in host_rows[r].items()}
+        staged = {n: torch.empty(t.shape, dtype=torch.int16, device="cuda") for n, t in pinned.items()}
+        views = {n: t.view(torch.bfloat16) for n, t in staged.items()}
+        plan = kb.DeferredRoundPlan(pb, views, ob, logits[r], drafts[r], jb, bb, kb_, sb, xb, layer_ready=flags,
+                                    layers_per_flag=lpf)
+        p = pb.last
+        plan.verify(p, epoch=r)
+        if upload == "library":
+            kb.StagedUpload(views, {n: t.view(torch.bfloat16) for n, t in pinned.items()}, flags, lpf)(r, side)
+        else:
+            with torch.cuda.stream(side):
+                for f, (l0, l1) in enumerate(bounds):
+                    for n in staged:
+                        staged[n][l0:l1].copy_(pinned[n][l0:l1], non_blocking=True)
+                    kb.kda_stream_write_u32(flags[f:f + 1], r, stream=side)
+        plan.accept()
+        plan._flip(p)
+        torch.cuda.synchronize()
+        assert int(sb[0]) == 0, f"round {r}: status {int(sb[0]):#x}"
+        assert torch.equal(ja, jb) and [int(x) for x in ja.cpu()] == list(synth.accept_targets(w, r))
+        assert bits_equal(oa, ob), f"round {r}: outputs"
+        assert bits_equal(pa.state(), pb.state()) and bits_equal(pa.ring(), pb.ring()), f"round {r}"
+        assert bits_equal(pa.states[pa.last], pb.states[pb.last]), f"round {r}: snapshot"
+        pb.rows = [views[n] for n in ("q", "k", "v", "g", "beta")]  # keep this round's rows alive
+    kb.kda_rollback_pingpong(pa, ka)
+    kb.kda_rollback_pingpong(pb, kb_)
+    torch.cuda.synchronize()
+    assert bits_equal(pa.state(), pb.state()) and int(sa[0]) == 0 and int(sb[0]) == 0
+
+
+def test_staged_rows_that_never_arrive_time_out():
+    """A ready flag that nothing sets: the launch gives up after its bounded wait, reports
+    KDA_ST_TIMEOUT, and the device stays usable."""
+    ensure_built()
+    L, B, H = 2, 1, 3
+    w = synth.Workload("to", L=L, B=B, H=H, T=4, bf16=True, V=64, rounds=2, seed=0x7101, accept="uniform")
+    state0, ring0, cw = small_case(w)
+    rows = [rows_to_dev(synth.all_rows(w, r), True) for r in range(2)]
+    pp = kb.PingPong(layer_state(state0, ring0, cw))
+    kb.kda_verify_scan_pingpong(pp, *[rows[0][n] for n in ("q", "k", "v", "g", "beta")])
+    keep = torch.full((B,), 2, dtype=torch.int32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kb.kda_verify_scan_deferred_staged(pp, *[rows[1][n] for n in ("q", "k", "v", "g", "beta")], keep, flags, L, 7,
+                                       dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status[0]) & kb.ST_TIMEOUT
+    x = torch.arange(8, device="cuda", dtype=torch.float32)
+    assert float((x * 2).sum()) == 56.0
