@@ -245,6 +245,8 @@ int kda_stream_write_u32(unsigned *flag, unsigned value, cudaStream_t stream);
  * for kda_verify_scan) of that range from src (host memory, pinned for the copies to be
  * asynchronous) to dst (device), then layer_ready[range] = epoch, all in the order of
  * `stream` (a stream other than the launch's, so that the copies overlap the scan).
+ * Where q, k, v and g lie at one distance from each other in both dst and src (four
+ * equal tensors in one allocation), a range of the four is one 2D copy.
  * dims gives L, B, H and the element type; T the rows a round.  Allocates nothing and
  * does not synchronise.  KDA_EINVAL for NULL pointers, T outside 1..15 or
  * layers_per_flag < 1; KDA_ECUDA when a copy or the flag write is refused.

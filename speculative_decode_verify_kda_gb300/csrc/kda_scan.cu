@@ -1593,13 +1593,40 @@ extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst,
     for (int i = 0; i < 5; ++i)
         if (!d[i] || !h[i])
             return kda::fail(KDA_EINVAL, "every raw-row pointer of dst and src must be non-NULL");
+    // q, k, v, g at one distance from each other on both sides (one allocation of four
+    // equal tensors): a layer range of all four is one 2D copy (four rows of the range's
+    // bytes, pitch that distance), since the copy engine pays for every copy
+    const auto gap = [](const void *a, const void *b) {
+        return static_cast<long long>(reinterpret_cast<uintptr_t>(b)) -
+               static_cast<long long>(reinterpret_cast<uintptr_t>(a));
+    };
+    const size_t tensor_bytes = per_layer * D * dims->L;
+    const long long dp = gap(d[0], d[1]), hp = gap(h[0], h[1]);
+    const long long max_pitch = 0x7fffffffLL;  // the copy engine's pitch limit, and then some
+    bool two_d = dp >= static_cast<long long>(tensor_bytes) && hp >= static_cast<long long>(tensor_bytes) &&
+                       dp <= max_pitch && hp <= max_pitch &&
+                       gap(d[1], d[2]) == dp && gap(d[2], d[3]) == dp && gap(h[1], h[2]) == hp &&
+                       gap(h[2], h[3]) == hp;
     for (int l0 = 0, f = 0; l0 < dims->L; l0 += layers_per_flag, ++f) {
         const int n = std::min(layers_per_flag, dims->L - l0);
         for (int i = 0; i < 5; ++i) {
             const size_t row = i < 4 ? per_layer * D : per_layer;
-            const cudaError_t e = cudaMemcpyAsync(static_cast<char *>(const_cast<void *>(d[i])) + row * l0,
-                                                  static_cast<const char *>(h[i]) + row * l0, row * n,
-                                                  cudaMemcpyHostToDevice, stream);
+            char *dd = static_cast<char *>(const_cast<void *>(d[i])) + row * l0;
+            const char *hh = static_cast<const char *>(h[i]) + row * l0;
+            cudaError_t e;
+            if (two_d && i == 0) {
+                // the runtime checks the whole span: four tensors of separate allocations
+                // are refused before anything is queued, and then go one by one
+                e = cudaMemcpy2DAsync(dd, static_cast<size_t>(dp), hh, static_cast<size_t>(hp), row * n, 4,
+                                      cudaMemcpyHostToDevice, stream);
+                if (e == cudaSuccess) {
+                    i = 3;  // q, k, v and g are done
+                    continue;
+                }
+                cudaGetLastError();
+                two_d = false;
+            }
+            e = cudaMemcpyAsync(dd, hh, row * n, cudaMemcpyHostToDevice, stream);
             if (e != cudaSuccess)
                 return kda::fail(KDA_ECUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
         }

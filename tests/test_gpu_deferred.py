@@ -293,7 +293,19 @@ def test_staged_deferred_rounds_equal_deferred_rounds(lpf, upload):
         # this round's rows for pb: fresh device tensors, filled while the launch waits
         pinned = {n: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
                   for n, a in host_rows[r].items()}
-        staged = {n: torch.empty(t.shape, dtype=torch.int16, device="cuda") for n, t in pinned.items()}
+        if upload == "library" and lpf == 2:
+            # q, k, v, g as four equal tensors of one allocation on both sides: the library
+            # then copies a range of the four as one 2D copy
+            shp = tuple(pinned["q"].shape)
+            hblk = torch.empty((4,) + shp, dtype=torch.int16).pin_memory()
+            dblk = torch.empty((4,) + shp, dtype=torch.int16, device="cuda")
+            for i, n in enumerate(("q", "k", "v", "g")):
+                hblk[i].copy_(pinned[n])
+                pinned[n] = hblk[i]
+            staged = {n: dblk[i] for i, n in enumerate(("q", "k", "v", "g"))}
+            staged["beta"] = torch.empty(tuple(pinned["beta"].shape), dtype=torch.int16, device="cuda")
+        else:
+            staged = {n: torch.empty(t.shape, dtype=torch.int16, device="cuda") for n, t in pinned.items()}
         views = {n: t.view(torch.bfloat16) for n, t in staged.items()}
         plan = kb.DeferredRoundPlan(pb, views, ob, logits[r], drafts[r], jb, bb, kb_, sb, xb, layer_ready=flags,
                                     layers_per_flag=lpf)
