@@ -42,8 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 # (profiles/kda_scan_kernel_deferred_<workload>.md; dram__bytes_read.sum +
 # dram__bytes_write.sum).  The reported traffic scales the capture to the run's mean
 # algorithmic bytes per launch.  Re-measure whenever the kernel changes.
-TRAFFIC_BYTES = {"stack34": (201_797_120 + 258_024_704, 504_740_608),
-                 "batched32": (204_264_960 + 233_644_800, 478_401_792)}
+TRAFFIC_BYTES = {"stack34": (201_783_040 + 258_356_992, 504_740_608),
+                 "batched32": (204_223_488 + 233_344_000, 478_401_792)}
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
@@ -330,7 +330,7 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     copy_stream = torch.cuda.Stream(dev)
     copied = torch.cuda.Event()
     flags = torch.zeros(len(ranges), dtype=torch.int32, device=dev)
-    staged = nc > 1
+    staged = len(ranges) > 1
     # kda_upload_rows_staged of host block r into device block b (one library call: the
     # copies of each layer range, each followed by its flag)
     uploads = {(r, b): kb.StagedUpload({n: dev_views[b][n] for n in names}, {n: host_views[r][n] for n in names},
@@ -581,7 +581,7 @@ def run_gpu(args, rank, world, local_rank):
         "peak": peak,
         "peak_kind": peak_kind,
         "clocks": clk.summary(),
-        "launches_per_step": 3,
+        "launches_per_step": 2,  # kda_scan_kernel (deferred round) and accept_cluster_kernel
         "separate_rollback": separate,
         "in_place": in_place,
     }
@@ -623,7 +623,7 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
                              args.e2e_chunks)
-        if args.e2e_chunks != 1:
+        if "staged_layer_ranges" in res["e2e"]:
             one = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, 1)
             res["e2e"]["one_copy"] = {"value": one["value"], "ms_per_step": one["ms_per_step"]}
 
