@@ -276,10 +276,10 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     A round's inputs sit in one pinned host block (logits, drafts, then each raw-row
     tensor whole).  nc == 1: one copy of the block, then the deferred round launch.
     nc > 1: the launch (kda_verify_scan_deferred_staged) goes first; on a copy stream the
-    logits and drafts, then the raw rows of nc consecutive layer ranges are copied, each
-    range followed by a stream write of its ready flag, so the scan of the layers in place
-    overlaps the copy of the rest.  Then one accept, and j and the bonus come back in one
-    copy.  The next round's copies start after the host has read this round's j (a
+    raw rows of nc consecutive ranges of (layer, session) pairs are copied, each range
+    followed by a stream write of its ready flag, so the scan of the pairs in place
+    overlaps the copy of the rest; then the logits and drafts, one accept, and j and the
+    bonus come back in one copy.  The next round's copies start after the host has read this round's j (a
     round's inputs follow from the previous accept).  Leaves pp committed."""
     import time
 
@@ -300,8 +300,9 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
         offs[n] = off
         off += (t.numel() * t.element_size() + 255) // 256 * 256
     block_bytes = off
-    lpf = -(-w.L // max(1, min(nc, w.L)))  # layers a flag covers
-    ranges = [(l0, min(w.L, l0 + lpf)) for l0 in range(0, w.L, lpf)]
+    pairs = w.L * w.B  # (layer, session) pairs, the unit of a staged range
+    ppf = -(-pairs // max(1, min(nc, pairs)))  # pairs a flag covers
+    ranges = [(p0, min(pairs, p0 + ppf)) for p0 in range(0, pairs, ppf)]
 
     def views(buf):
         out_ = {}
@@ -332,16 +333,16 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     flags = torch.zeros(len(ranges), dtype=torch.int32, device=dev)
     staged = len(ranges) > 1
     # kda_upload_rows_staged of host block r into device block b (one library call: the
-    # copies of each layer range, each followed by its flag)
+    # copies of each range of pairs, each followed by its flag)
     uploads = {(r, b): kb.StagedUpload({n: dev_views[b][n] for n in names}, {n: host_views[r][n] for n in names},
-                                       flags, lpf) for r in range(HR) for b in range(2)}
+                                       flags, ppf) for r in range(HR) for b in range(2)}
 
     def plan(b, cls, **kw):
         v = dev_views[b]
         return cls(pp, {n: v[n] for n in names}, out, v["logits"], v["drafts"], res_dev[0], res_dev[1], res_dev[2],
                    status, scratch, stream, **kw)
 
-    eplans = [plan(b, kb.DeferredRoundPlan, **({"layer_ready": flags, "layers_per_flag": lpf} if staged else {}))
+    eplans = [plan(b, kb.DeferredRoundPlan, **({"ready_flags": flags, "pairs_per_flag": ppf} if staged else {}))
               for b in range(2)]
     eopen = plan(1, kb.PingPongRoundPlan)
     epoch = [0]
@@ -362,7 +363,7 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
         p = pp.last
         if staged:
             epoch[0] += 1
-            rp.verify(p, epoch[0])  # waits on the device for each layer range's flag
+            rp.verify(p, epoch[0])  # waits on the device for each range's flag
             load_staged(i)
             stream.wait_event(copied)  # the accept reads the logits
         else:
@@ -395,7 +396,8 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     res = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": Ke}
     if staged:
-        res["staged_layer_ranges"] = len(ranges)
+        res["staged_ranges"] = len(ranges)
+        res["pairs_per_range"] = ppf
     return res
 
 
@@ -618,12 +620,13 @@ def run_gpu(args, rank, world, local_rank):
                         "round": "ping-pong verify, accept, rollback (separate launches), one graph per round"}
 
     # e2e: host buffers through the public API, copies inside the timed region (run_e2e):
-    # the raw rows stream in by layer range while the one launch scans the ranges already
-    # in place; the one-copy round (the whole block, then the launch) is reported beside it.
+    # the raw rows stream in by range of (layer, session) pairs while the one launch
+    # scans the ranges already in place; the one-copy round (the whole block, then the
+    # launch) is reported beside it.
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
                              args.e2e_chunks)
-        if "staged_layer_ranges" in res["e2e"]:
+        if "staged_ranges" in res["e2e"]:
             one = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, 1)
             res["e2e"]["one_copy"] = {"value": one["value"], "ms_per_step": one["ms_per_step"]}
 
@@ -812,8 +815,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=1000)
     ap.add_argument("--e2e-chunks", type=int, default=4,
-                    help="layer ranges the e2e round's raw rows are copied in (the one launch waits for each "
-                         "range's ready flag); 1: one copy, then the launch")
+                    help="ranges of (layer, session) pairs the e2e round's raw rows are copied in (the one "
+                         "launch waits for each range's ready flag); 1: one copy, then the launch")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline")
     ap.add_argument("--no-per-layer", action="store_true", help="skip the per-layer (and CUDA graph) rounds")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay of the rounds")

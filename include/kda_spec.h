@@ -212,22 +212,23 @@ int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *st, kda_stas
 
 /*
  * kda_verify_scan_deferred_staged -- kda_verify_scan_deferred whose raw rows may still
- * be arriving when it starts (the round's inputs streamed in by layer range, so that the
- * host-to-device copy overlaps the scan of the layers already in place; glm_spec.rs,
- * VERIFY-ROW BATCHING: one launch a round).
- * layer_ready: DEVICE array of unsigned flags; the rows of layer l (q, k, v, g and beta
- * of every session) may be read once layer_ready[l / layers_per_flag] has reached
- * `epoch` (compared as (int)(flag - epoch) >= 0, so a counter may wrap).  The caller
- * copies each range of rows and then sets its flag in stream order after the copy,
- * with kda_stream_write_u32 on the copy's stream.  The kernel waits for a flag at most
- * one second; a flag that does not arrive sets KDA_ST_TIMEOUT in *dev_status and the
- * launch ends early, its results undefined.  The previous round's rows (stash->rows)
- * must be in place.  Everything else, including the results, is as for
- * kda_verify_scan_deferred.  layers_per_flag must be >= 1; layer_ready 4-byte aligned.
+ * be arriving when it starts (the round's inputs streamed in by range of (layer,
+ * session) pairs, so that the host-to-device copy overlaps the scan of the pairs already
+ * in place; glm_spec.rs, VERIFY-ROW BATCHING: one launch a round).
+ * ready_flags: DEVICE array of unsigned flags; the raw rows of pair lb = l * B + b
+ * (q, k, v, g and beta of layer l, session b) may be read once
+ * ready_flags[lb / pairs_per_flag] has reached `epoch` (compared as
+ * (int)(flag - epoch) >= 0, so a counter may wrap).  The caller copies each range of
+ * pairs and then sets its flag in stream order after the copy (kda_upload_rows_staged,
+ * or its own copies and kda_stream_write_u32 on the copy's stream).  The kernel waits
+ * for a flag at most one second; a flag that does not arrive sets KDA_ST_TIMEOUT in
+ * *dev_status and the launch ends early, its results undefined.  The previous round's
+ * rows (stash->rows) must be in place.  Everything else, including the results, is as
+ * for kda_verify_scan_deferred.  pairs_per_flag must be >= 1; ready_flags 4-byte aligned.
  */
 int kda_verify_scan_deferred_staged(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
                                     const int *prev_keep, const kda_rows *rows, int T, float *out,
-                                    const unsigned *layer_ready, int layers_per_flag, unsigned epoch,
+                                    const unsigned *ready_flags, int pairs_per_flag, unsigned epoch,
                                     int *dev_status, cudaStream_t stream);
 
 /*
@@ -240,19 +241,19 @@ int kda_stream_write_u32(unsigned *flag, unsigned value, cudaStream_t stream);
 
 /*
  * kda_upload_rows_staged -- the host-to-device copy that feeds
- * kda_verify_scan_deferred_staged: for each range of layers_per_flag layers (the last
- * may be shorter), one cudaMemcpyAsync per raw-row tensor (q, k, v, g, beta, layout as
- * for kda_verify_scan) of that range from src (host memory, pinned for the copies to be
- * asynchronous) to dst (device), then layer_ready[range] = epoch, all in the order of
- * `stream` (a stream other than the launch's, so that the copies overlap the scan).
- * Where q, k, v and g lie at one distance from each other in both dst and src (four
- * equal tensors in one allocation), a range of the four is one 2D copy.
+ * kda_verify_scan_deferred_staged: for each range of pairs_per_flag (layer, session)
+ * pairs (the last may be shorter), one cudaMemcpyAsync per raw-row tensor (q, k, v, g,
+ * beta, layout as for kda_verify_scan) of that range from src (host memory, pinned for
+ * the copies to be asynchronous) to dst (device), then ready_flags[range] = epoch, all in
+ * the order of `stream` (a stream other than the launch's, so that the copies overlap
+ * the scan).  Where q, k, v and g lie at one distance from each other in both dst and
+ * src (four equal tensors in one allocation), a range of the four is one 2D copy.
  * dims gives L, B, H and the element type; T the rows a round.  Allocates nothing and
  * does not synchronise.  KDA_EINVAL for NULL pointers, T outside 1..15 or
- * layers_per_flag < 1; KDA_ECUDA when a copy or the flag write is refused.
+ * pairs_per_flag < 1; KDA_ECUDA when a copy or the flag write is refused.
  */
 int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_rows *src, int T,
-                           unsigned *layer_ready, int layers_per_flag, unsigned epoch, cudaStream_t stream);
+                           unsigned *ready_flags, int pairs_per_flag, unsigned epoch, cudaStream_t stream);
 
 /*
  * Rounds whose length differs per session (variable T inside one batched grid).

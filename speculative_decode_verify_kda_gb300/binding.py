@@ -423,16 +423,16 @@ def kda_verify_scan_deferred(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Te
 
 
 def kda_verify_scan_deferred_staged(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Tensor,
-                                    layer_ready: torch.Tensor, layers_per_flag: int, epoch: int,
+                                    ready_flags: torch.Tensor, pairs_per_flag: int, epoch: int,
                                     out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
                                     stream=None) -> PingPong:
-    """kda_verify_scan_deferred whose raw rows of layer l may be read once
-    layer_ready[l // layers_per_flag] has reached epoch (see kda_stream_write_u32).
-    layer_ready: device int32 flags (compared as unsigned)."""
+    """kda_verify_scan_deferred whose raw rows of (layer, session) pair lb = l B + b may
+    be read once ready_flags[lb // pairs_per_flag] has reached epoch (see
+    kda_upload_rows_staged, kda_stream_write_u32).  ready_flags: device int32 flags
+    (compared as unsigned)."""
     if pp.last is None:
         raise ValueError("a deferred round follows a ping-pong round (no previous round to commit)")
-    nflags = -(-pp.L // max(1, int(layers_per_flag)))
-    _dev(layer_ready, "layer_ready", torch.int32, (nflags,))
+    _dev(ready_flags, "ready_flags", torch.int32, (staged_flag_count(pp.L, pp.B, pairs_per_flag),))
     shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
     rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
     if dt != pp.dtype:
@@ -446,13 +446,20 @@ def kda_verify_scan_deferred_staged(pp: PingPong, q, k, v, g, beta, prev_keep: t
     cstash = KdaStashC(pp.states[p].data_ptr(), pp.rings[p].data_ptr(), prev.rows, prev.T)
     dims = pp.dims(dt)
     rc = lib().kda_verify_scan_deferred_staged(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(cstash),
-                                               _ptr(prev_keep), ctypes.byref(rows), T, _ptr(out), _ptr(layer_ready),
-                                               int(layers_per_flag), ctypes.c_uint(epoch & 0xffffffff),
+                                               _ptr(prev_keep), ctypes.byref(rows), T, _ptr(out), _ptr(ready_flags),
+                                               int(pairs_per_flag), ctypes.c_uint(epoch & 0xffffffff),
                                                _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
     _check("kda_verify_scan_deferred_staged", rc)
     pp.cstash[1 - p].rows, pp.cstash[1 - p].T = rows, T
     pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, 1 - p, p
     return pp
+
+
+def staged_flag_count(L: int, B: int, pairs_per_flag: int) -> int:
+    """Flags of a staged round: one a range of pairs_per_flag (layer, session) pairs."""
+    if int(pairs_per_flag) < 1:
+        raise ValueError("pairs_per_flag must be >= 1")
+    return -(-(int(L) * int(B)) // int(pairs_per_flag))
 
 
 def kda_stream_write_u32(flag: torch.Tensor, value: int, stream=None) -> None:
@@ -468,10 +475,11 @@ def kda_stream_write_u32(flag: torch.Tensor, value: int, stream=None) -> None:
 class StagedUpload:
     """kda_upload_rows_staged for one pair of raw-row sets: ``host`` (pinned CPU tensors)
     into ``dev`` (device tensors of the same shapes and element type), by ranges of
-    layers_per_flag layers, each range's flag in ``layer_ready`` set to the call's epoch
-    after its copies.  ``__call__(epoch, stream)`` issues the copies on ``stream``."""
+    pairs_per_flag (layer, session) pairs, each range's flag in ``ready_flags`` set to the
+    call's epoch after its copies.  ``__call__(epoch, stream)`` issues the copies on
+    ``stream``."""
 
-    def __init__(self, dev: dict, host: dict, layer_ready: torch.Tensor, layers_per_flag: int):
+    def __init__(self, dev: dict, host: dict, ready_flags: torch.Tensor, pairs_per_flag: int):
         names = ("q", "k", "v", "g", "beta")
         L_, B, T, H = (int(x) for x in dev["q"].shape[:4])
         for n in names:
@@ -480,17 +488,17 @@ class StagedUpload:
             if not dev[n].is_cuda or host[n].is_cuda or not host[n].is_contiguous() or not dev[n].is_contiguous():
                 raise ValueError(f"{n}: dev must be a contiguous device tensor and host a contiguous CPU tensor")
         dt = BF16 if dev["q"].dtype == torch.bfloat16 else F32
-        _dev(layer_ready, "layer_ready", torch.int32, (-(-L_ // max(1, int(layers_per_flag))),))
+        _dev(ready_flags, "ready_flags", torch.int32, (staged_flag_count(L_, B, pairs_per_flag),))
         self.dims = KdaDims(L_, B, H, D, D, dt)
         self.dst = KdaRows(*(dev[n].data_ptr() for n in names))
         self.src = KdaRows(*(host[n].data_ptr() for n in names))
-        self.T, self.flags, self.lpf = T, layer_ready, int(layers_per_flag)
+        self.T, self.flags, self.ppf = T, ready_flags, int(pairs_per_flag)
         self._keep = (dev, host)
 
     def __call__(self, epoch: int, stream=None):
         _check("kda_upload_rows_staged", lib().kda_upload_rows_staged(
             ctypes.byref(self.dims), ctypes.byref(self.dst), ctypes.byref(self.src), self.T, _ptr(self.flags),
-            self.lpf, ctypes.c_uint(epoch & 0xffffffff), ctypes.c_void_p(_stream(stream))))
+            self.ppf, ctypes.c_uint(epoch & 0xffffffff), ctypes.c_void_p(_stream(stream))))
 
 
 def kda_rollback_pingpong(pp: PingPong, keep, t_rows=None, dev_status: torch.Tensor | None = None,
@@ -814,8 +822,8 @@ class DeferredRoundPlan:
     """
 
     def __init__(self, pp: PingPong, rows: dict, out, logits, drafts, j_out, bonus_out, keep_out, dev_status,
-                 scratch, stream=None, layer_ready=None, layers_per_flag: int = 1):
-        self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch, layer_ready)
+                 scratch, stream=None, ready_flags=None, pairs_per_flag: int = 1):
+        self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch, ready_flags)
         self.pp = pp
         shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
         crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
@@ -837,11 +845,11 @@ class DeferredRoundPlan:
                          _ptr(keep_out), ctypes.byref(self.crows), T, _ptr(out), _ptr(dev_status), s) for p in (0, 1)]
         # staged raw rows (kda_verify_scan_deferred_staged): the epoch is given per call
         self._staged = None
-        if layer_ready is not None:
-            _dev(layer_ready, "layer_ready", torch.int32, (-(-pp.L // max(1, int(layers_per_flag))),))
+        if ready_flags is not None:
+            _dev(ready_flags, "ready_flags", torch.int32, (staged_flag_count(pp.L, pp.B, pairs_per_flag),))
             self._staged = [(ctypes.byref(self.dims), ctypes.byref(self.cst[p]), ctypes.byref(self.cstash[p]),
-                             _ptr(keep_out), ctypes.byref(self.crows), T, _ptr(out), _ptr(layer_ready),
-                             int(layers_per_flag)) for p in (0, 1)]
+                             _ptr(keep_out), ctypes.byref(self.crows), T, _ptr(out), _ptr(ready_flags),
+                             int(pairs_per_flag)) for p in (0, 1)]
             self._staged_tail = (_ptr(dev_status), s)
         nbytes = scratch.numel() * scratch.element_size()
         self._accept = (_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out), _ptr(bonus_out),
@@ -850,7 +858,7 @@ class DeferredRoundPlan:
         self._L = lib()
 
     def verify(self, p: int, epoch: int | None = None):
-        """The deferred verify launch; with staged rows (layer_ready given) ``epoch`` is
+        """The deferred verify launch; with staged rows (ready_flags given) ``epoch`` is
         the flag value that marks this call's rows as in place."""
         pp = self.pp
         prev = pp.cstash[p]

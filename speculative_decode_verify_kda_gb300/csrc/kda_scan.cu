@@ -134,10 +134,10 @@ struct ScanParams {
     const int *keep_dev;   // KEEP_DEVICE: [B]
     const int *rows_dev;   // ROWS_DEVICE, or KEEP_DEVICE after a per-session round: [B] row counts
     int *status;           // nullable device status word
-    const unsigned *ready; // nullable: this call's raw rows of layer l are in place once
-                           // ready[l / ready_lpf] has reached epoch (written by the copy's stream)
+    const unsigned *ready; // nullable: this call's raw rows of (layer, session) pair lb = l B + b
+                           // are in place once ready[lb / ready_ppf] has reached epoch
     unsigned epoch;
-    int ready_lpf;
+    int ready_ppf;
     int L, B, H;
     FastDiv divH, divB;    // u / H and lb / B
     int T_rows;            // row count of the raw-row tensors
@@ -429,18 +429,17 @@ __device__ __forceinline__ Item next_item(const ScanParams &p, Item it, int n)
 }
 
 // Staged raw rows: before a prologue warp copies an item's rows of this call (part 1)
-// it waits, bounded like warp_wait, until the flag of the item's layer range has reached
-// the call's epoch.  The flag is written by a stream memory operation after the rows'
+// it waits, bounded like warp_wait, until the flag of the item's range of (layer,
+// session) pairs has reached the call's epoch.  The flag is written by a stream memory operation after the rows'
 // host-to-device copy on another stream (no kernel writes it).  Lane 0 reads it with
 // acquire semantics; the proxy fence orders the tensor copies that follow after it.  A
-// warp walks its units in increasing layer order, so it reads each flag once: last_f is
-// the flag it saw set last.
+// warp walks its units in increasing (layer, session) order, so it reads each flag
+// once: last_f is the flag it saw set last.
 __device__ bool rows_ready(const ScanParams &p, const Ctl &c, int u, int part, int lane, int &last_f)
 {
     if (!p.ready || part == 0)
         return true;
-    const uint32_t lb = fdiv(static_cast<uint32_t>(u), p.divH);
-    const int fi = static_cast<int>(fdiv(lb, p.divB)) / p.ready_lpf;
+    const int fi = static_cast<int>(fdiv(static_cast<uint32_t>(u), p.divH)) / p.ready_ppf;
     if (fi == last_f)
         return true;
     int ok = 1;
@@ -1447,7 +1446,7 @@ namespace {
 // Shared body of kda_verify_scan_deferred and kda_verify_scan_deferred_staged (ready:
 // nullptr for rows already in place).
 int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, const int *prev_keep,
-                    const kda_rows *rows, int T, float *out, const unsigned *ready, int lpf, unsigned epoch,
+                    const kda_rows *rows, int T, float *out, const unsigned *ready, int ppf, unsigned epoch,
                     int *dev_status, cudaStream_t stream)
 {
     int rc = check_common(dims, st);
@@ -1495,7 +1494,7 @@ int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
         p.tcap = std::max(T, stash->T);
         p.bf16 = dims->dtype == KDA_BF16;
         p.ready = ready;
-        p.ready_lpf = lpf;
+        p.ready_ppf = ppf;
         p.epoch = epoch;
         if ((rc = launch_scan(p, stash->state_snap, stream, st->state, &stash->rows)))
             return rc;
@@ -1521,14 +1520,14 @@ extern "C" int kda_verify_scan_deferred(const kda_dims *dims, kda_layer_state *s
 
 extern "C" int kda_verify_scan_deferred_staged(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
                                                const int *prev_keep, const kda_rows *rows, int T, float *out,
-                                               const unsigned *layer_ready, int layers_per_flag, unsigned epoch,
+                                               const unsigned *ready_flags, int pairs_per_flag, unsigned epoch,
                                                int *dev_status, cudaStream_t stream)
 {
-    if (!layer_ready || (reinterpret_cast<uintptr_t>(layer_ready) & 3u))
-        return kda::fail(KDA_EINVAL, "layer_ready must be a 4-byte aligned device array of flags");
-    if (layers_per_flag < 1)
-        return kda::fail(KDA_EINVAL, "layers_per_flag must be >= 1");
-    return kda::deferred_common(dims, st, stash, prev_keep, rows, T, out, layer_ready, layers_per_flag, epoch,
+    if (!ready_flags || (reinterpret_cast<uintptr_t>(ready_flags) & 3u))
+        return kda::fail(KDA_EINVAL, "ready_flags must be a 4-byte aligned device array of flags");
+    if (pairs_per_flag < 1)
+        return kda::fail(KDA_EINVAL, "pairs_per_flag must be >= 1");
+    return kda::deferred_common(dims, st, stash, prev_keep, rows, T, out, ready_flags, pairs_per_flag, epoch,
                                 dev_status, stream);
 }
 
@@ -1569,7 +1568,7 @@ extern "C" int kda_stream_write_u32(unsigned *flag, unsigned value, cudaStream_t
 }
 
 extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_rows *src, int T,
-                                      unsigned *layer_ready, int layers_per_flag, unsigned epoch,
+                                      unsigned *ready_flags, int pairs_per_flag, unsigned epoch,
                                       cudaStream_t stream)
 {
     if (!dims || !dst || !src)
@@ -1580,15 +1579,16 @@ extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst,
         return kda::fail(KDA_EINVAL, "dtype must be KDA_F32 or KDA_BF16");
     if (T < 1 || T > KDA_TMAX)
         return kda::fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
-    if (!layer_ready || (reinterpret_cast<uintptr_t>(layer_ready) & 3u))
-        return kda::fail(KDA_EINVAL, "layer_ready must be a 4-byte aligned device array of flags");
-    if (layers_per_flag < 1)
-        return kda::fail(KDA_EINVAL, "layers_per_flag must be >= 1");
+    if (!ready_flags || (reinterpret_cast<uintptr_t>(ready_flags) & 3u))
+        return kda::fail(KDA_EINVAL, "ready_flags must be a 4-byte aligned device array of flags");
+    if (pairs_per_flag < 1)
+        return kda::fail(KDA_EINVAL, "pairs_per_flag must be >= 1");
     const void *d[5] = {dst->q, dst->k, dst->v, dst->g, dst->beta};
     const void *h[5] = {src->q, src->k, src->v, src->g, src->beta};
     const size_t es = dims->dtype == KDA_BF16 ? 2 : 4;
-    const size_t per_layer = static_cast<size_t>(dims->B) * T * dims->H * es;  // beta; x128 for q, k, v, g
-    if (per_layer == 0 || dims->L == 0)
+    const int pairs = dims->L * dims->B;  // (layer, session) pairs, lb = l B + b
+    const size_t per_pair = static_cast<size_t>(T) * dims->H * es;  // beta; x128 for q, k, v, g
+    if (per_pair == 0 || pairs == 0)
         return kda::ok();
     for (int i = 0; i < 5; ++i)
         if (!d[i] || !h[i])
@@ -1600,19 +1600,19 @@ extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst,
         return static_cast<long long>(reinterpret_cast<uintptr_t>(b)) -
                static_cast<long long>(reinterpret_cast<uintptr_t>(a));
     };
-    const size_t tensor_bytes = per_layer * D * dims->L;
+    const size_t tensor_bytes = per_pair * D * pairs;
     const long long dp = gap(d[0], d[1]), hp = gap(h[0], h[1]);
     const long long max_pitch = 0x7fffffffLL;  // the copy engine's pitch limit, and then some
     bool two_d = dp >= static_cast<long long>(tensor_bytes) && hp >= static_cast<long long>(tensor_bytes) &&
                        dp <= max_pitch && hp <= max_pitch &&
                        gap(d[1], d[2]) == dp && gap(d[2], d[3]) == dp && gap(h[1], h[2]) == hp &&
                        gap(h[2], h[3]) == hp;
-    for (int l0 = 0, f = 0; l0 < dims->L; l0 += layers_per_flag, ++f) {
-        const int n = std::min(layers_per_flag, dims->L - l0);
+    for (int p0 = 0, f = 0; p0 < pairs; p0 += pairs_per_flag, ++f) {
+        const int n = std::min(pairs_per_flag, pairs - p0);
         for (int i = 0; i < 5; ++i) {
-            const size_t row = i < 4 ? per_layer * D : per_layer;
-            char *dd = static_cast<char *>(const_cast<void *>(d[i])) + row * l0;
-            const char *hh = static_cast<const char *>(h[i]) + row * l0;
+            const size_t row = i < 4 ? per_pair * D : per_pair;
+            char *dd = static_cast<char *>(const_cast<void *>(d[i])) + row * p0;
+            const char *hh = static_cast<const char *>(h[i]) + row * p0;
             cudaError_t e;
             if (two_d && i == 0) {
                 // the runtime checks the whole span: four tensors of separate allocations
@@ -1630,7 +1630,7 @@ extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst,
             if (e != cudaSuccess)
                 return kda::fail(KDA_ECUDA, std::string("cudaMemcpyAsync: ") + cudaGetErrorString(e));
         }
-        const int rc = kda::write_flag(layer_ready + f, epoch, stream);
+        const int rc = kda::write_flag(ready_flags + f, epoch, stream);
         if (rc)
             return rc;
     }

@@ -274,9 +274,9 @@ def test_staged_deferred_and_flag_writer_reject_on_host(L):
     def call(ready=FAKE + 0x4000, lpf=1, keep=FAKE + 0x3000):
         return L.kda_verify_scan_deferred_staged(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(prev), keep,
                                                  ctypes.byref(rows), 8, None, ready, lpf, 1, None, None)
-    assert call(ready=None) == kb.EINVAL and b"layer_ready" in L.kda_last_error()
+    assert call(ready=None) == kb.EINVAL and b"ready_flags" in L.kda_last_error()
     assert call(ready=FAKE + 0x4002) == kb.EINVAL
-    assert call(lpf=0) == kb.EINVAL and b"layers_per_flag" in L.kda_last_error()
+    assert call(lpf=0) == kb.EINVAL and b"pairs_per_flag" in L.kda_last_error()
     assert call(keep=None) == kb.EINVAL  # the deferred round's own checks still apply
     assert L.kda_stream_write_u32(None, 1, None) == kb.EINVAL
     assert L.kda_stream_write_u32(FAKE + 2, 1, None) == kb.EINVAL
@@ -289,3 +289,7 @@ def test_staged_deferred_and_flag_writer_reject_on_host(L):
     assert upload(ready=None) == kb.EINVAL and upload(ready=FAKE + 1) == kb.EINVAL and upload(lpf=0) == kb.EINVAL
     assert upload(src=kb.KdaRows(FAKE, FAKE, None, FAKE, FAKE)) == kb.EINVAL
     assert upload(d=kb.KdaDims(0, 2, 64, 128, 128, kb.BF16)) == kb.OK  # nothing to copy
+    assert kb.staged_flag_count(34, 1, 9) == 4 and kb.staged_flag_count(1, 32, 8) == 4
+    assert kb.staged_flag_count(3, 2, 4) == 2 and kb.staged_flag_count(3, 2, 1) == 6
+    with pytest.raises(ValueError):
+        kb.staged_flag_count(3, 2, 0)

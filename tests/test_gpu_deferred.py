@@ -253,12 +253,12 @@ def test_per_layer_deferred_rounds_equal_one_launch(bounds):
     assert bits_equal(pa.state(), pb.state()) and int(sa[0]) == 0 and int(sb[0]) == 0
 
 
-@pytest.mark.parametrize("lpf,upload", [(1, "library"), (2, "library"), (2, "torch")])
-def test_staged_deferred_rounds_equal_deferred_rounds(lpf, upload):
+@pytest.mark.parametrize("ppf,upload", [(1, "library"), (4, "library"), (3, "torch")])
+def test_staged_deferred_rounds_equal_deferred_rounds(ppf, upload):
     """Deferred rounds whose raw rows arrive while the launch runs (copied from pinned host
-    memory by layer range on a side stream, each range's flag set after its copy, by
-    kda_upload_rows_staged or by torch copies and kda_stream_write_u32) give the bits of
-    deferred rounds on resident rows."""
+    memory by ranges of (layer, session) pairs on a side stream, each range's flag set
+    after its copy, by kda_upload_rows_staged or by torch copies and kda_stream_write_u32)
+    give the bits of deferred rounds on resident rows."""
     ensure_built()
     from gpu_util import to_dev
     L, B, H = 3, 2, 5
@@ -269,8 +269,9 @@ def test_staged_deferred_rounds_equal_deferred_rounds(lpf, upload):
     logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
     drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
               for r in range(w.rounds)]
-    bounds = [(l0, min(L, l0 + lpf)) for l0 in range(0, L, lpf)]  # flag f covers layers f*lpf ..
-    flags = torch.zeros(-(-L // lpf), dtype=torch.int32, device="cuda")
+    pairs = L * B
+    bounds = [(p0, min(pairs, p0 + ppf)) for p0 in range(0, pairs, ppf)]  # flag f covers pairs f*ppf ..
+    flags = torch.zeros(kb.staged_flag_count(L, B, ppf), dtype=torch.int32, device="cuda")
     side = torch.cuda.Stream()
 
     def case():
@@ -293,7 +294,7 @@ def test_staged_deferred_rounds_equal_deferred_rounds(lpf, upload):
         # this round's rows for pb: fresh device tensors, filled while the launch waits
         pinned = {n: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).pin_memory()
                   for n, a in host_rows[r].items()}
-        if upload == "library" and lpf == 2:
+        if upload == "library" and ppf == 4:
             # q, k, v, g as four equal tensors of one allocation on both sides: the library
             # then copies a range of the four as one 2D copy
             shp = tuple(pinned["q"].shape)
@@ -307,17 +308,17 @@ def test_staged_deferred_rounds_equal_deferred_rounds(lpf, upload):
         else:
             staged = {n: torch.empty(t.shape, dtype=torch.int16, device="cuda") for n, t in pinned.items()}
         views = {n: t.view(torch.bfloat16) for n, t in staged.items()}
-        plan = kb.DeferredRoundPlan(pb, views, ob, logits[r], drafts[r], jb, bb, kb_, sb, xb, layer_ready=flags,
-                                    layers_per_flag=lpf)
+        plan = kb.DeferredRoundPlan(pb, views, ob, logits[r], drafts[r], jb, bb, kb_, sb, xb, ready_flags=flags,
+                                    pairs_per_flag=ppf)
         p = pb.last
         plan.verify(p, epoch=r)
         if upload == "library":
-            kb.StagedUpload(views, {n: t.view(torch.bfloat16) for n, t in pinned.items()}, flags, lpf)(r, side)
+            kb.StagedUpload(views, {n: t.view(torch.bfloat16) for n, t in pinned.items()}, flags, ppf)(r, side)
         else:
             with torch.cuda.stream(side):
-                for f, (l0, l1) in enumerate(bounds):
-                    for n in staged:
-                        staged[n][l0:l1].copy_(pinned[n][l0:l1], non_blocking=True)
+                for f, (p0, p1) in enumerate(bounds):
+                    for n in staged:  # [L][B] ... as pairs
+                        staged[n].flatten(0, 1)[p0:p1].copy_(pinned[n].flatten(0, 1)[p0:p1], non_blocking=True)
                     kb.kda_stream_write_u32(flags[f:f + 1], r, stream=side)
         plan.accept()
         plan._flip(p)
@@ -347,8 +348,8 @@ def test_staged_rows_that_never_arrive_time_out():
     keep = torch.full((B,), 2, dtype=torch.int32, device="cuda")
     flags = torch.zeros(1, dtype=torch.int32, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kb.kda_verify_scan_deferred_staged(pp, *[rows[1][n] for n in ("q", "k", "v", "g", "beta")], keep, flags, L, 7,
-                                       dev_status=status)
+    kb.kda_verify_scan_deferred_staged(pp, *[rows[1][n] for n in ("q", "k", "v", "g", "beta")], keep, flags,
+                                       L * B, 7, dev_status=status)
     torch.cuda.synchronize()
     assert int(status[0]) & kb.ST_TIMEOUT
     x = torch.arange(8, device="cuda", dtype=torch.float32)
