@@ -354,3 +354,58 @@ def test_staged_rows_that_never_arrive_time_out():
     assert int(status[0]) & kb.ST_TIMEOUT
     x = torch.arange(8, device="cuda", dtype=torch.float32)
     assert float((x * 2).sum()) == 56.0
+
+
+@pytest.mark.parametrize("wl,ppf", [("stack34", 9), ("batched32", 8)])
+def test_staged_full_size_equals_resident(wl, ppf):
+    """The e2e arrangement at full size: each round's raw rows streamed from one pinned
+    block (q, k, v, g as four equal tensors, so a range of them is one 2D copy) into one
+    device block by ranges of (layer, session) pairs while the staged launch runs; every
+    output, state, ring and snapshot bit equals the deferred rounds on resident rows."""
+    from speculative_decode_verify_kda_gb300 import synth_gpu
+    w = synth.WORKLOADS[wl]
+    dev = torch.device("cuda", 0)
+    a = kb.PingPong(kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev)))
+    b = kb.PingPong(kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev)))
+    R = 3
+    rows = [synth_gpu.rows(w, r, dev) for r in range(R)]
+    keeps = _keeps(w.B, [w.T] * R, 0x9940)
+    if w.B == 1:
+        keeps = [[3], [1], [w.T]]
+    shp, bshp = tuple(rows[0]["q"].shape), tuple(rows[0]["beta"].shape)
+    flags = torch.zeros(kb.staged_flag_count(w.L, w.B, ppf), dtype=torch.int32, device=dev)
+    side = torch.cuda.Stream()
+
+    def block(on_dev):  # q, k, v, g in one allocation, beta apart
+        kw = {"device": dev} if on_dev else {}
+        qkvg = torch.empty((4,) + shp, dtype=torch.bfloat16, **kw)
+        beta = torch.empty(bshp, dtype=torch.bfloat16, **kw)
+        if not on_dev:
+            qkvg, beta = qkvg.pin_memory(), beta.pin_memory()
+        return dict(zip(NAMES, [qkvg[0], qkvg[1], qkvg[2], qkvg[3], beta]))
+
+    out_a = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev)
+    out_b = torch.empty_like(out_a)
+    dev_blocks = [block(True) for _ in range(2)]
+    for r in range(R):
+        x = [rows[r][n] for n in NAMES]
+        db = dev_blocks[r % 2]
+        if r == 0:
+            kb.kda_verify_scan_pingpong(a, *x, out=out_a)
+            for n in NAMES:
+                db[n].copy_(rows[r][n])
+            kb.kda_verify_scan_pingpong(b, *[db[n] for n in NAMES], out=out_b)
+        else:
+            keep = torch.tensor(keeps[r - 1], dtype=torch.int32, device=dev)
+            kb.kda_verify_scan_deferred(a, *x, keep, out=out_a)
+            hb = block(False)
+            for n in NAMES:
+                hb[n].copy_(rows[r][n].cpu())
+            torch.cuda.synchronize()
+            kb.kda_verify_scan_deferred_staged(b, *[db[n] for n in NAMES], keep, flags, ppf, r, out=out_b)
+            kb.StagedUpload(db, hb, flags, ppf)(r, side)
+        torch.cuda.synchronize()
+        assert bits_equal(out_a, out_b), f"round {r}: outputs"
+        assert bits_equal(a.state(), b.state()) and bits_equal(a.ring(), b.ring()), f"round {r}: post-round"
+        assert bits_equal(a.states[a.last], b.states[b.last]) and bits_equal(a.rings[a.last], b.rings[b.last]), \
+            f"round {r}: snapshot"
