@@ -481,8 +481,8 @@ def run_gpu(args, rank, world, local_rank):
             ev[2].record(stream)
         p._flip(par)
 
-    # round 0 opens the chain: a ping-pong verify and its accept (its rollback runs
-    # inside round 1's launch)
+    # the first round opens the chain: a ping-pong verify and its accept (its rollback
+    # runs inside the next round's launch)
     par0 = pp.parity
     pplans[0].verify(par0)
     pplans[0].accept()
