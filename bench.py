@@ -42,8 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 # (profiles/kda_scan_kernel_deferred_<workload>.md; dram__bytes_read.sum +
 # dram__bytes_write.sum).  The reported traffic scales the capture to the run's mean
 # algorithmic bytes per launch.  Re-measure whenever the kernel changes.
-TRAFFIC_BYTES = {"stack34": (201_783_040 + 258_356_992, 504_740_608),
-                 "batched32": (204_223_488 + 233_344_000, 478_401_792)}
+TRAFFIC_BYTES = {"stack34": (201_875_456 + 257_812_992, 504_740_608),
+                 "batched32": (204_221_440 + 233_559_808, 478_401_792)}
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
