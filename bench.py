@@ -267,6 +267,35 @@ def oracle_baseline(w, budget_s: float):
     return {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
 
 
+def oracle_baseline_threads(w, budget_s: float, threads: int):
+    """A second CPU figure: the same oracle, unchanged, on independent (layer, session)
+    units in `threads` host threads at once (the C calls release the interpreter lock),
+    for about budget_s seconds of wall time."""
+    from concurrent.futures import ThreadPoolExecutor
+    arms = [OracleArm(w) for _ in range(threads)]
+
+    def work(arm):
+        heads = rounds = 0
+        t_end = time.perf_counter() + budget_s
+        while time.perf_counter() < t_end or rounds == 0:
+            _, _, n = arm.step(w.H)
+            heads, rounds = heads + n, rounds + 1
+        return heads, rounds
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        done = list(ex.map(work, arms))
+    wall = time.perf_counter() - t0
+    heads = sum(d[0] for d in done)
+    rounds = sum(d[1] for d in done)
+    # a round of the workload is L*B unit-rounds of H heads; here every unit-round also ran
+    # its accept, so the figure errs low
+    round_s = wall / heads * (w.H * w.L * w.B)
+    desc = (f"{rounds} unit-rounds of {w.name} ({w.H} heads, T={w.T}: accept + verify + rollback) in {threads} "
+            f"threads over {wall:.1f} s of wall time, extrapolated linearly to {w.L} layers x {w.B} sessions")
+    return {"value": w.B * w.T / round_s, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+
+
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
@@ -877,9 +906,10 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_gpu(args, rank, world, local_rank)
-    cpu = None
+    cpu = cpu_threads = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = oracle_baseline(w, args.cpu_budget)
+        cpu_threads = oracle_baseline_threads(w, args.cpu_budget, os.cpu_count() or 1)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -904,6 +934,7 @@ def main():
         "gpu_launches": res["launches_per_step"] * args.steps,
         "clocks": res["clocks"],
         "cpu_baseline": cpu,
+        "cpu_baseline_threads": cpu_threads,
         "separate_rollback": res.get("separate_rollback"),
         "in_place": res.get("in_place"),
         "e2e": res.get("e2e"),
