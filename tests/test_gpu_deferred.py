@@ -409,3 +409,36 @@ def test_staged_full_size_equals_resident(wl, ppf):
         assert bits_equal(a.state(), b.state()) and bits_equal(a.ring(), b.ring()), f"round {r}: post-round"
         assert bits_equal(a.states[a.last], b.states[b.last]) and bits_equal(a.rings[a.last], b.rings[b.last]), \
             f"round {r}: snapshot"
+
+
+def test_staged_rounds_with_f32_rows():
+    """f32 raw rows through kda_upload_rows_staged (4-byte elements) and the staged launch:
+    the bits of deferred rounds on resident rows."""
+    ensure_built()
+    L, B, H = 2, 3, 4
+    w = synth.Workload("sf", L=L, B=B, H=H, T=5, bf16=False, V=64, rounds=4, seed=0x5F32, accept="uniform")
+    state0, ring0, cw = small_case(w)
+    host_rows = [synth.all_rows(w, r) for r in range(w.rounds)]
+    rows = [rows_to_dev(hr, False) for hr in host_rows]
+    keeps = _keeps(B, [w.T] * w.rounds, 0x5F33)
+    ppf = 2
+    flags = torch.zeros(kb.staged_flag_count(L, B, ppf), dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    pa = kb.PingPong(layer_state(state0, ring0, cw))
+    pb = kb.PingPong(layer_state(state0, ring0, cw))
+    out_a = torch.empty((L, B, w.T, H, 128), dtype=torch.float32, device="cuda")
+    out_b = torch.empty_like(out_a)
+    kb.kda_verify_scan_pingpong(pa, *[rows[0][n] for n in NAMES], out=out_a)
+    kb.kda_verify_scan_pingpong(pb, *[rows[0][n] for n in NAMES], out=out_b)
+    keep_alive = []
+    for r in range(1, w.rounds):
+        keep = torch.tensor(keeps[r - 1], dtype=torch.int32, device="cuda")
+        kb.kda_verify_scan_deferred(pa, *[rows[r][n] for n in NAMES], keep, out=out_a)
+        pinned = {n: torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for n, a in host_rows[r].items()}
+        staged = {n: torch.empty(t.shape, dtype=torch.float32, device="cuda") for n, t in pinned.items()}
+        keep_alive.append(staged)
+        kb.kda_verify_scan_deferred_staged(pb, *[staged[n] for n in NAMES], keep, flags, ppf, r, out=out_b)
+        kb.StagedUpload(staged, pinned, flags, ppf)(r, side)
+        torch.cuda.synchronize()
+        assert bits_equal(out_a, out_b), f"round {r}: outputs"
+        assert bits_equal(pa.state(), pb.state()) and bits_equal(pa.ring(), pb.ring()), f"round {r}"
