@@ -27,7 +27,8 @@
  *   glm_spec.rs, glm5_verify_rows (t <= 15: the decode-exact cap)
  *
  * Conventions for every entry point:
- *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *   - All tensor pointers are DEVICE pointers owned by the caller (the one
+ *     exception: the source of kda_upload_rows_staged, host memory); the library
  *     keeps none of them past the call except through the kda_stash it fills.
  *   - Every call is asynchronous on `stream` and never synchronises.
  *   - The library allocates no memory.  spec_accept and spec_accept_sampled take
