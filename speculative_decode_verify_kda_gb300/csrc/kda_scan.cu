@@ -1594,7 +1594,7 @@ extern "C" int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst,
         if (!d[i] || !h[i])
             return kda::fail(KDA_EINVAL, "every raw-row pointer of dst and src must be non-NULL");
     // q, k, v, g at one distance from each other on both sides (one allocation of four
-    // equal tensors): a layer range of all four is one 2D copy (four rows of the range's
+    // equal tensors): a range of pairs of all four is one 2D copy (four rows of the range's
     // bytes, pitch that distance), since the copy engine pays for every copy
     const auto gap = [](const void *a, const void *b) {
         return static_cast<long long>(reinterpret_cast<uintptr_t>(b)) -
