@@ -37,13 +37,45 @@ METRIC = "KDA verify rows/s (T=K+1, 64 heads) and achieved HBM GB/s vs 8 TB/s ro
 UNIT = "verify rows/s"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-# DRAM bytes read + written by one deferred-round launch of the current kda_scan_kernel
-# and that launch's algorithmic bytes, from one ncu capture each
-# (profiles/kda_scan_kernel_deferred_<workload>.md; dram__bytes_read.sum +
-# dram__bytes_write.sum).  The reported traffic scales the capture to the run's mean
-# algorithmic bytes per launch.  Re-measure whenever the kernel changes.
+# DRAM bytes read + written by one deferred-round launch of kda_scan_kernel, from one
+# ncu capture per workload (dram__bytes_read.sum + dram__bytes_write.sum), with the
+# kernel's own byte count (deferred_bytes) of the captured launch, so the figure can
+# be scaled to a run's mean launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
+# only: comments and blank space removed) the captures were taken on; with any other
+# source the traffic is reported as null.
+TRAFFIC_SOURCE = "3d4f03dcb519c16059bdfa8aa76e82e3a2e3220f19b3286718812a795e365ad2"
 TRAFFIC_BYTES = {"stack34": (201_875_456 + 257_812_992, 504_740_608),
                  "batched32": (204_221_440 + 233_559_808, 478_401_792)}
+SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
+
+
+def code_hash(path: str) -> str:
+    """sha256 of a C/C++/CUDA source with its comments and white space removed."""
+    import hashlib
+    import re
+    with open(path) as f:
+        src = f.read()
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":  # string or char literal, copied whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    code = re.sub(r"\s+", "", "".join(out))
+    return hashlib.sha256(code.encode()).hexdigest()
+
 
 WORKLOAD_TEXT = {
     "stack34": "34 KDA layers x 64 heads x 128x128 f32 state (136 MiB/round), K=7 (T=8), 1 session, "
@@ -85,6 +117,28 @@ def deferred_bytes(w, prev_keeps) -> int:
         m = 3 if pending else 2
         n += w.L * (w.H * m * (D * D * 4 + 9 * D * 4) + (k if pending else 0) * row + w.T * row + w.T * w.H * D * 4)
     return n + w.L * w.H * 3 * D * 4 * 4
+
+
+def algorithmic_bytes(w, prev_keeps) -> int:
+    """The bytes the round's steps must move, each tensor once: this round's verify at
+    the ping-pong minimum (per session and layer the state read and written, 2 x 4 MiB
+    at 64 heads; T raw rows of 65,664 B; T output rows of 32 KiB; the conv ring read
+    and written, 2 x 288 KiB) plus the layer's conv weights (384 KiB), and the
+    previous accept's rollback of every session that kept fewer than T rows (the
+    snapshot read and the state written, the ring snapshot read and the ring written,
+    and the kept raw rows).  This is what the roofline fraction divides by: a launch
+    that folds the rollback into the verify moves fewer bytes than this."""
+    es = 2 if w.bf16 else 4
+    D = 128
+    row = w.H * (4 * D + 1) * es
+    state = w.H * D * D * 4
+    ring = w.H * 9 * D * 4
+    verify = 2 * state + 2 * ring + w.T * row + w.T * w.H * D * 4
+    n = w.L * w.B * verify + w.L * w.H * 3 * D * 4 * 4
+    for k in prev_keeps:
+        if k < w.T:
+            n += w.L * (2 * state + 2 * ring + k * row)
+    return n
 
 
 def rollback_bytes(w, keeps) -> int:
@@ -148,9 +202,12 @@ def job_rows_per_s(world: int, B: int, T: int, ms: float) -> float:
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
+    """nvidia-smi every 20 ms from before the first warm-up step to after the last timed
+    section; the summary keeps the samples taken while the GPU was busy (utilization
+    at least 50 %)."""
     FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
               "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap", "utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -160,7 +217,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -179,24 +236,35 @@ class ClockSampler:
         return False
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons, total = [], [], [], set(), 0
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for ln in getattr(self, "lines", []):
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != len(self.FIELDS):
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                clk, cmax, util = float(parts[0]), float(parts[1]), float(parts[7])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[3:]):
+            total += 1
+            if util < 50:
+                continue
+            sm.append(clk)
+            mx.append(cmax)
+            try:
+                pw.append(float(parts[2]))
+            except ValueError:
+                pass
+            for n, v in zip(names, parts[3:7]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "samples_total": total}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "samples_total": total, "power_w_max": max(pw) if pw else None,
+                "window": "from before the first warm-up step to after the last timed section, "
+                          "samples at >= 50 % GPU utilization"}
 
 
 # ---------------------------------------------------------------------------
@@ -321,7 +389,6 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    HR = min(R, 4)
     names = ("q", "k", "v", "g", "beta")
     parts = [("logits", logits[0]), ("drafts", drafts[0])] + [(n, rows[0][n]) for n in names]
     offs, off = {}, 0
@@ -329,6 +396,7 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
         offs[n] = off
         off += (t.numel() * t.element_size() + 255) // 256 * 256
     block_bytes = off
+    HR = min(R, 4 if block_bytes < (1 << 30) else 2)  # pinned host rounds cycled
     pairs = w.L * w.B  # (layer, session) pairs, the unit of a staged range
     ppf = -(-pairs // max(1, min(nc, pairs)))  # pairs a flag covers
     ranges = [(p0, min(pairs, p0 + ppf)) for p0 in range(0, pairs, ppf)]
@@ -430,14 +498,16 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     return res
 
 
-def run_gpu(args, rank, world, local_rank):
+def run_gpu(args, rank, world, local_rank, wname, full=True):
+    """One workload on this rank's GPU.  full: every section; else the timed deferred
+    rounds and the e2e rounds only."""
     import torch
     from speculative_decode_verify_kda_gb300 import binding as kb
     from speculative_decode_verify_kda_gb300 import synth, synth_gpu
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = synth.WORKLOADS[args.workload]
+    w = synth.WORKLOADS[wname]
     R = min(w.rounds, args.rounds) if args.rounds else w.rounds
 
     st = kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev))
@@ -522,15 +592,14 @@ def run_gpu(args, rank, world, local_rank):
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
-        barrier()
-        t_wall = time.perf_counter()
-        e0.record(stream)
-        for i in range(K):
-            dstep((args.warmup + 1 + i) % R, evs[i])
-        e1.record(stream)
-        barrier()
-        t_wall = time.perf_counter() - t_wall
+    barrier()
+    t_wall = time.perf_counter()
+    e0.record(stream)
+    for i in range(K):
+        dstep((args.warmup + 1 + i) % R, evs[i])
+    e1.record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
     total_ms = e0.elapsed_time(e1)
     round_ms = [e[0].elapsed_time(e[1]) for e in evs]
     accept_ms = [e[1].elapsed_time(e[2]) for e in evs]
@@ -545,10 +614,33 @@ def run_gpu(args, rank, world, local_rank):
     # the kept rows each timed round replays: the previous round's accept
     prev_keeps = [[j + 1 for j in jt[(args.warmup + i) % R]] for i in range(K)]
     round_bytes = [deferred_bytes(w, k) for k in prev_keeps]
+    algo_bytes = [algorithmic_bytes(w, k) for k in prev_keeps]
     step_bytes = [rb + accept_bytes(w) for rb in round_bytes]
     round_avg_ms = sum(round_ms) / K
     peak, peak_kind = measured_peak()
-    achieved = sum(round_bytes) / (sum(round_ms) * 1e-3) / 1e9
+    achieved = sum(algo_bytes) / (sum(round_ms) * 1e-3) / 1e9
+    achieved_kernel = sum(round_bytes) / (sum(round_ms) * 1e-3) / 1e9
+    res = {
+        "rows_per_s": job_rows_per_s(world, w.B, w.T, ms_step),
+        "ms_per_step": ms_step,
+        "round_kernel_ms": round_avg_ms,
+        "accept_ms": sum(accept_ms) / K,
+        "wall_s": t_wall,
+        "round_bytes_mean": sum(round_bytes) / K,
+        "algo_bytes_mean": sum(algo_bytes) / K,
+        "step_bytes_mean": sum(step_bytes) / K,
+        "step_gbs": sum(step_bytes) / (total_ms * 1e-3) / 1e9,
+        "achieved": achieved,
+        "achieved_kernel": achieved_kernel,
+        "peak": peak,
+        "peak_kind": peak_kind,
+        "launches_per_step": 2,  # kda_scan_kernel (deferred round) and accept_cluster_kernel
+    }
+    if not full:
+        if not args.no_e2e:
+            res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
+                                 args.e2e_chunks)
+        return res
 
     # the same rounds with the rollback as its own launch: ping-pong verify, accept,
     # rollback
@@ -600,22 +692,8 @@ def run_gpu(args, rank, world, local_rank):
     # in-place rounds above advanced st.state, which is one of them
     pp.parity = 0
 
-    res = {
-        "rows_per_s": job_rows_per_s(world, w.B, w.T, ms_step),
-        "ms_per_step": ms_step,
-        "round_kernel_ms": round_avg_ms,
-        "accept_ms": sum(accept_ms) / K,
-        "wall_s": t_wall,
-        "round_bytes_mean": sum(round_bytes) / K,
-        "step_gbs": sum(step_bytes) / (total_ms * 1e-3) / 1e9,
-        "achieved": achieved,
-        "peak": peak,
-        "peak_kind": peak_kind,
-        "clocks": clk.summary(),
-        "launches_per_step": 2,  # kda_scan_kernel (deferred round) and accept_cluster_kernel
-        "separate_rollback": separate,
-        "in_place": in_place,
-    }
+    res["separate_rollback"] = separate
+    res["in_place"] = in_place
 
     # the same rounds replayed from CUDA graphs (one graph per resident round): the
     # launch gaps between the round's kernels shrink
@@ -833,16 +911,88 @@ def run_gpu(args, rank, world, local_rank):
     return res
 
 
+def host_cpu() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith("model name"):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def workload_config(wname, args, step_bytes=None):
+    from speculative_decode_verify_kda_gb300 import synth
+    w = synth.WORKLOADS[wname]
+    if step_bytes:
+        l2 = (f"no flush: each step moves {step_bytes / 1e9:.2f} GB (the launch's own bytes and the accept's "
+              f"logits), {step_bytes / 129e6:.1f}x the 129 MB L2")
+    else:
+        l2 = "no flush: every step moves more bytes than the 129 MB L2"
+    return {"workload": wname, "description": WORKLOAD_TEXT[wname], "L": w.L, "B": w.B, "H": w.H, "T": w.T,
+            "V": w.V, "rows_dtype": "bf16" if w.bf16 else "f32", "state_dtype": "f32", "l2": l2,
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def roofline_of(wname, res, clocks) -> dict:
+    """The roofline object of the deferred-round launch: achieved = algorithmic bytes per
+    launch over its mean time; the kernel's own bytes and the DRAM traffic of an ncu
+    capture (while the kernel source is the captured one) beside it."""
+    peak = res["peak"]
+    traffic = frac_dram = None
+    same = code_hash(SCAN_SOURCE) == TRAFFIC_SOURCE
+    if wname in TRAFFIC_BYTES and same:
+        dram, own = TRAFFIC_BYTES[wname]
+        traffic = dram * res["round_bytes_mean"] / own
+        frac_dram = traffic / (res["round_kernel_ms"] * 1e-3) / 1e9 / peak
+    if wname not in TRAFFIC_BYTES:
+        tsrc = "no ncu capture of this workload's launch"
+    elif same:
+        tsrc = ("ncu capture of one launch (dram__bytes_read.sum + dram__bytes_write.sum) on this kernel "
+                "source, scaled to the run's mean kernel bytes per launch")
+    else:
+        tsrc = "null: kda_scan.cu differs from the source the ncu capture was taken on"
+    out = {"bound": "hbm", "kernel": "kda_scan_kernel (deferred round: rollback + verify)",
+           "achieved": res["achieved"], "peak": peak, "unit": "GB/s", "frac": res["achieved"] / peak,
+           "basis": "algorithmic bytes per launch: this round's verify at the ping-pong minimum and the "
+                    "previous accept's rollback, each tensor once; over the launch's mean CUDA-event time",
+           "target": "frac >= 0.70 on the 64-head, 34-layer workloads",
+           "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
+           "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
+           "bytes_per_launch": res["algo_bytes_mean"],
+           "kernel_bytes_per_launch": res["round_bytes_mean"],
+           "frac_kernel_bytes": res["achieved_kernel"] / peak,
+           "traffic": traffic, "frac_dram": frac_dram, "traffic_source": tsrc,
+           "launch_ms": res["round_kernel_ms"]}
+    if clocks and clocks.get("sm_mhz"):
+        out["launch_kcycles_at_median_clock"] = res["round_kernel_ms"] * clocks["sm_mhz"]
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=6000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="stack34", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="stack34", choices=sorted(WORKLOAD_TEXT),
+                    help="the headline workload (every section)")
+    ap.add_argument("--workloads", default="batched32,stress64x34",
+                    help="further workloads timed in the same run (deferred rounds and e2e), reported under "
+                         "'workloads'; empty for none")
     ap.add_argument("--rounds", type=int, default=0, help="distinct input rounds kept resident (0: all)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=1000)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="ranges of (layer, session) pairs the e2e round's raw rows are copied in (the one "
                          "launch waits for each range's ready flag); 1: one copy, then the launch")
@@ -867,14 +1017,11 @@ def main():
 
     from speculative_decode_verify_kda_gb300 import synth
     w = synth.WORKLOADS[args.workload]
-    config = {"workload": args.workload, "description": WORKLOAD_TEXT[args.workload],
-              "L": w.L, "B": w.B, "H": w.H, "T": w.T, "V": w.V, "rows_dtype": "bf16" if w.bf16 else "f32",
-              "state_dtype": "f32", "l2": "no flush: >= 0.8 GB moved per step, larger than the 129 MB L2",
-              "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
     if args.impl == "reference":
         if rank != 0:
             return
+        config = workload_config(args.workload, args)
         arm = OracleArm(w)
         ts, ta, n = arm.step(w.H)  # calibration: one whole unit-round
         per_head = ts / n
@@ -882,62 +1029,87 @@ def main():
         hps = int(max(1, min(w.H, budget // max(per_head, 1e-9))))
         t_scan = t_acc = 0.0
         heads = rounds = 0
+        t_steps = 0.0
         for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
             ts, ta, n = arm.step(hps)
+            dt = time.perf_counter() - t0
             if i >= args.warmup:
                 t_scan += ts
+                t_steps += dt
                 heads += n
                 t_acc += ta * n / w.H  # one accept per round, spread over the round's heads
         val = arm.rows_per_s(t_scan / heads, t_acc / heads * w.H)
-        sample = (f"{args.steps} steps of {hps} heads each of one (layer, session) unit of {args.workload} "
-                  f"(accept + verify + rollback, single-threaded oracle), extrapolated linearly to "
-                  f"{w.H} heads x {w.L} layers x {w.B} sessions per round")
+        sample = (f"each step: accept + verify + rollback of {hps} heads of one (layer, session) unit of "
+                  f"{args.workload} (single-threaded oracle); value extrapolated linearly to {w.H} heads x "
+                  f"{w.L} layers x {w.B} sessions per round")
+        cores = 1
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.B * w.T / val * 1e3,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_steps * 1e3 / args.steps,
+                "step": f"{hps} heads of one (layer, session) unit: accept + verify + rollback",
+                "extrapolated_ms_per_round": w.B * w.T / val * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded counter-based draws)", "config": config,
-                "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                                 "cpu_model": host_cpu(), "host_cores": os.cpu_count()},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
 
+    import gc
+
+    import torch
     if world > 1:
-        import torch
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    res = run_gpu(args, rank, world, local_rank)
+    subs = [x for x in args.workloads.split(",") if x and x != args.workload]
+    for x in subs:
+        if x not in WORKLOAD_TEXT:
+            ap.error(f"unknown workload {x}")
+    with ClockSampler(local_rank) as clk:
+        res = run_gpu(args, rank, world, local_rank, args.workload, full=True)
+        subres = {}
+        for wn in subs:
+            gc.collect()
+            torch.cuda.empty_cache()
+            subres[wn] = run_gpu(args, rank, world, local_rank, wn, full=False)
+    clocks = clk.summary()
     cpu = cpu_threads = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = oracle_baseline(w, args.cpu_budget)
         cpu_threads = oracle_baseline_threads(w, args.cpu_budget, os.cpu_count() or 1)
+        model = host_cpu()
+        for c in (cpu, cpu_threads):
+            c["cpu_model"] = model
+            c["host_cores"] = os.cpu_count()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     if rank != 0:
         return
-    frac = res["achieved"] / res["peak"]
+    workloads = {}
+    for wn, r in subres.items():
+        workloads[wn] = {"config": workload_config(wn, args, r["step_bytes_mean"]), "value": r["rows_per_s"],
+                         "unit": UNIT, "steps": args.steps, "ms_per_step": r["ms_per_step"],
+                         "round_kernel_ms": r["round_kernel_ms"], "accept_ms": r["accept_ms"],
+                         "roofline": roofline_of(wn, r, clocks), "e2e": r.get("e2e"),
+                         "gpu_launches": r["launches_per_step"] * args.steps}
     line = {
         "metric": METRIC, "value": res["rows_per_s"], "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based draws; bf16 raw rows)",
-        "config": config,
-        "roofline": {"bound": "hbm", "kernel": "kda_scan_kernel (deferred round: rollback + verify)",
-                     "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s", "frac": frac,
-                     "frac_of_nominal_8tbs": res["achieved"] / NOMINAL_HBM_GBS,
-                     "peak_source": f"{res['peak_kind']} (MEASURED_PEAKS.json hbm_gbs)",
-                     "bytes_per_launch": res["round_bytes_mean"],
-                     "traffic": (TRAFFIC_BYTES[args.workload][0] * res["round_bytes_mean"] /
-                                 TRAFFIC_BYTES[args.workload][1]) if args.workload in TRAFFIC_BYTES else None,
-                     "traffic_source": "ncu capture of one launch, scaled to the mean bytes per launch"},
+        "config": workload_config(args.workload, args, res["step_bytes_mean"]),
+        "roofline": roofline_of(args.workload, res, clocks),
         "round_kernel_ms": res["round_kernel_ms"], "accept_ms": res["accept_ms"],
         "step_achieved_gbs": res["step_gbs"],
         "gpu_launches": res["launches_per_step"] * args.steps,
-        "clocks": res["clocks"],
+        "clocks": clocks,
         "cpu_baseline": cpu,
         "cpu_baseline_threads": cpu_threads,
+        "e2e": res.get("e2e"),
+        "workloads": workloads,
         "separate_rollback": res.get("separate_rollback"),
         "in_place": res.get("in_place"),
-        "e2e": res.get("e2e"),
         "graph": res.get("graph"),
         "per_layer": res.get("per_layer"),
         "var_t": res.get("var_t"),
