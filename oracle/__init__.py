@@ -95,8 +95,16 @@ class Oracle:
         cd = ctypes.c_double
         self.lib.kdao_filtered.argtypes = [ci, ci, vp, cd, ci, cd, cd, vp]
         self.lib.kdao_sampled_accept.argtypes = [ci, ci, ci, vp, vp, vp, vp, cd, cd, ci, cd, cd, vp, vp]
+        cu, cull = ctypes.c_uint, ctypes.c_ulonglong
+        self.lib.kdao_philox4x32_10.argtypes = [vp, vp, vp]
+        self.lib.kdao_philox4x32_10.restype = None
+        self.lib.kdao_u01.argtypes = [cull, cu, cu]
+        self.lib.kdao_u01.restype = cf
+        self.lib.kdao_sampled_accept_session.argtypes = [ci, ci, ci, vp, vp, vp, cull, vp, vp, cd, ci, cd, cd, vp,
+                                                         vp]
         for fn in ("kdao_prepare", "kdao_core", "kdao_verify", "kdao_rollback", "kdao_accept", "kdao_conf_keep",
-                   "kdao_confidence_vt", "kdao_slot_confidence_vt", "kdao_filtered", "kdao_sampled_accept"):
+                   "kdao_confidence_vt", "kdao_slot_confidence_vt", "kdao_filtered", "kdao_sampled_accept",
+                   "kdao_sampled_accept_session"):
             getattr(self.lib, fn).restype = ci
 
     @staticmethod
@@ -225,6 +233,37 @@ class Oracle:
                                           int(top_k), float(top_p), float(min_p), ctypes.byref(j), ctypes.byref(tok))
         self._check("kdao_sampled_accept", rc)
         return j.value, tok.value
+
+    def philox(self, ctr, key):
+        """Philox4x32-10 of one 4-word counter under a 2-word key; returns 4 uint32."""
+        c = np.ascontiguousarray(ctr, dtype=np.uint32).reshape(4)
+        k = np.ascontiguousarray(key, dtype=np.uint32).reshape(2)
+        o = np.empty(4, np.uint32)
+        self.lib.kdao_philox4x32_10(_p(c), _p(k), _p(o))
+        return o
+
+    def u01(self, seed, counter, tag):
+        """The uniform of a session's stream at (counter, tag)."""
+        return float(self.lib.kdao_u01(int(seed) & (2**64 - 1), int(counter) & 0xFFFFFFFF, int(tag) & 0xFFFFFFFF))
+
+    def sampled_accept_session(self, logits, draft_logits, drafts, seed, uctr, sctr, temperature=1.0, top_k=0,
+                               top_p=1.0, min_p=0.0):
+        """Sampled accept walk of one session drawing from its Philox counters; returns
+        (j, token, uctr after, sctr after)."""
+        logits, dt = _raw(logits)
+        T, V = logits.shape
+        K = T - 1
+        draft_logits = _raw(draft_logits)[0] if K else np.zeros((1, V), logits.dtype)
+        drafts = np.ascontiguousarray(drafts, dtype=np.int32).reshape(-1)
+        assert drafts.shape == (K,)
+        j, tok = ctypes.c_int(), ctypes.c_int()
+        uc, sc = ctypes.c_uint(int(uctr) & 0xFFFFFFFF), ctypes.c_uint(int(sctr) & 0xFFFFFFFF)
+        rc = self.lib.kdao_sampled_accept_session(T, V, dt, _p(logits), _p(draft_logits), _p(drafts) if K else None,
+                                                  int(seed) & (2**64 - 1), ctypes.byref(uc), ctypes.byref(sc),
+                                                  float(temperature), int(top_k), float(top_p), float(min_p),
+                                                  ctypes.byref(j), ctypes.byref(tok))
+        self._check("kdao_sampled_accept_session", rc)
+        return j.value, tok.value, uc.value, sc.value
 
     # -- [L][B] helper ---------------------------------------------------------
     def verify_units(self, rows, conv_w, ring, state, units=None):

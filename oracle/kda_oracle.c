@@ -484,7 +484,9 @@ int kdao_sampled_accept(int T, int V, int dtype, const void *logits, const void 
         if ((rc = kdao_filtered(V, dtype, (const char *)draft_logits + (size_t)j * V * es, temperature, top_k,
                                 top_p, min_p, qr)))
             goto done;
-        if (!(u_accept[j] * qr[drafts[j]] < pr[drafts[j]]))
+        /* the page compares its f32 gathers of p~ and q~ in double:
+         * (u as f64) * (qj as f64) < pj as f64 */
+        if (!(u_accept[j] * (double)(float)qr[drafts[j]] < (double)(float)pr[drafts[j]]))
             break;
     }
     if (j < K) {  /* pr, qr hold row j */
@@ -506,4 +508,79 @@ done:
     free(pr);
     free(qr);
     return rc;
+}
+
+/* Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy
+ * as 1, 2, 3", SC'11): ten rounds on a 128-bit counter under a 64-bit key.  A round
+ * multiplies counter words 0 and 2 by the two round multipliers (full 64-bit
+ * products), and the new counter is (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2),
+ * hi(M0 c0) ^ c3 ^ k1, lo(M0 c0)); the key is bumped by the two Weyl constants
+ * between rounds. */
+void kdao_philox4x32_10(const unsigned int ctr[4], const unsigned int key[2], unsigned int out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint64_t p0 = (uint64_t)M0 * c0, p1 = (uint64_t)M1 * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        const uint32_t n3 = (uint32_t)p0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* One uniform in [0, 1) of a session's stream: Philox4x32-10 under key (seed low,
+ * seed high) at counter (counter, 0, 0, tag), the top 24 bits of output word 0 times
+ * 2^-24 (exact in f32).  glm_spec.rs draws the accept-test uniforms on the host from
+ * the session's uctr with stream tag 0xFFFF_FFFE (spec::host_u01), and the device
+ * draws from its sctr; the word layout is this library's reading. */
+float kdao_u01(unsigned long long seed, unsigned int counter, unsigned int tag)
+{
+    const unsigned int key[2] = {(unsigned int)seed, (unsigned int)(seed >> 32)};
+    const unsigned int ctr[4] = {counter, 0u, 0u, tag};
+    unsigned int o[4];
+    kdao_philox4x32_10(ctr, key, o);
+    return (float)((double)(o[0] >> 8) * (1.0 / 16777216.0));
+}
+
+/* The sampled accept walk with the session's counters (glm_spec.rs,
+ * glm5_sampled_accept / glm5_sampled_bonus, and the Glm5SpecSession doc: the
+ * counters live on the session and are never reset).  Accept test r draws
+ * u01(seed, uctr, KDAO_TAG_ACCEPT) and advances uctr by one; the walk stops at the
+ * first rejection, so a round runs j + 1 tests when it rejects draft j and K when it
+ * accepts every draft.  The residual or bonus draw takes u01(seed, sctr,
+ * KDAO_TAG_DRAW) and advances sctr by one. */
+int kdao_sampled_accept_session(int T, int V, int dtype, const void *logits, const void *draft_logits,
+                                const int *drafts, unsigned long long seed, unsigned int *uctr,
+                                unsigned int *sctr, double temperature, int top_k, double top_p,
+                                double min_p, int *j_out, int *token_out)
+{
+    if (T < 1 || T > KDAO_TMAX)
+        return KDAO_EINVAL;
+    const int K = T - 1;
+    double u_accept[KDAO_TMAX];
+    for (int r = 0; r < K; ++r)
+        u_accept[r] = kdao_u01(seed, *uctr + (unsigned int)r, KDAO_TAG_ACCEPT);
+    const double u_sample = kdao_u01(seed, *sctr, KDAO_TAG_DRAW);
+    const int rc = kdao_sampled_accept(T, V, dtype, logits, draft_logits, drafts, u_accept, u_sample, temperature,
+                                       top_k, top_p, min_p, j_out, token_out);
+    if (rc)
+        return rc;
+    *uctr += (unsigned int)(*j_out < K ? *j_out + 1 : K);
+    *sctr += 1u;
+    return KDAO_OK;
 }

@@ -14,6 +14,9 @@
 #define KDAO_L2_EPS 1e-6             /* inside the sqrt of the L2 normalisation  */
 #define KDAO_SENTINEL (-1)           /* argmax of a row holding a NaN            */
 
+#define KDAO_TAG_ACCEPT 0xFFFFFFFEu /* counter word 3 of the accept-test uniforms */
+#define KDAO_TAG_DRAW 0xFFFFFFFFu   /* counter word 3 of the residual / bonus draw  */
+
 #define KDAO_F32 0
 #define KDAO_BF16 1
 
@@ -55,6 +58,13 @@ int kdao_filtered(int V, int dtype, const void *row, double temperature, int top
 int kdao_sampled_accept(int T, int V, int dtype, const void *logits, const void *draft_logits,
                         const int *drafts, const double *u_accept, double u_sample, double temperature,
                         int top_k, double top_p, double min_p, int *j_out, int *token_out);
+
+void kdao_philox4x32_10(const unsigned int ctr[4], const unsigned int key[2], unsigned int out[4]);
+float kdao_u01(unsigned long long seed, unsigned int counter, unsigned int tag);
+int kdao_sampled_accept_session(int T, int V, int dtype, const void *logits, const void *draft_logits,
+                                const int *drafts, unsigned long long seed, unsigned int *uctr,
+                                unsigned int *sctr, double temperature, int top_k, double top_p,
+                                double min_p, int *j_out, int *token_out);
 
 #ifdef __cplusplus
 }

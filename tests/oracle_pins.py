@@ -610,6 +610,67 @@ def pin_sampled_accept_bonus_and_greedy(orc):
         assert (js0, ts0) == (jg, bg), (lg, d)
 
 
+def _philox_kat():
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                w = [int(x, 16) for x in ln.split()]
+                rows.append((w[0:4], w[4:6], w[6:10]))
+    return rows
+
+
+def pin_philox_known_answers(orc):
+    """Philox4x32-10 reproduces the generator's published known-answer vectors
+    (tests/golden/philox4x32_10_kat.txt)."""
+    kat = _philox_kat()
+    assert len(kat) == 3
+    for ctr, key, want in kat:
+        assert [int(x) for x in orc.philox(ctr, key)] == want, (ctr, key)
+
+
+def pin_u01_layout(orc):
+    """A session uniform is output word 0 of Philox4x32-10 at counter (n, 0, 0, tag) under
+    key (seed low, seed high), top 24 bits times 2^-24: exact in f32, in [0, 1), and
+    uniform (chi-square over 16 bins of 20000 draws)."""
+    rng = np.random.default_rng(40)
+    for _ in range(50):
+        seed = int(rng.integers(0, 2**63)) * 2 + int(rng.integers(0, 2))
+        n = int(rng.integers(0, 2**32))
+        tag = int(rng.choice([0xFFFFFFFE, 0xFFFFFFFF, 0]))
+        w0 = int(orc.philox([n, 0, 0, tag], [seed & 0xFFFFFFFF, seed >> 32])[0])
+        u = orc.u01(seed, n, tag)
+        assert u == (w0 >> 8) / 16777216.0 and 0.0 <= u < 1.0 and float(np.float32(u)) == u
+    us = np.array([orc.u01(99, n, 0xFFFFFFFE) for n in range(20000)])
+    assert _chi2_ok(np.histogram(us, bins=16, range=(0, 1))[0], np.full(16, 1 / 16), us.size)
+    assert orc.u01(99, 5, 0xFFFFFFFE) != orc.u01(99, 5, 0xFFFFFFFF)  # the two tags are two streams
+
+
+def pin_sampled_session_counters(orc):
+    """The session walk equals the uniform-input walk fed from its counters: accept test r
+    uses u01(seed, uctr + r, 0xFFFFFFFE) and the final draw u01(seed, sctr, 0xFFFFFFFF);
+    uctr advances by the tests run (j + 1 on a rejection, K when every draft is accepted),
+    sctr by one.  Rounds in a row never reuse a counter."""
+    rng = np.random.default_rng(41)
+    V = 40
+    for case in range(200):
+        T = int(rng.integers(1, 8))
+        K = T - 1
+        lg = rng.normal(0, 1.5, (T, V)).astype(np.float32)
+        dl = (lg[:K] + rng.normal(0, 1.0, (K, V)).astype(np.float32)).astype(np.float32)
+        d = [int(np.argmax(dl[r])) if rng.uniform() < 0.7 else int(rng.integers(0, V)) for r in range(K)]
+        seed, uctr, sctr = int(rng.integers(0, 2**62)), int(rng.integers(0, 2**32 - 20)), int(rng.integers(0, 2**32 - 2))
+        filt = dict(temperature=0.8, top_k=int(rng.choice([0, 5])), top_p=float(rng.choice([1.0, 0.9])))
+        j, tok, u2, s2 = orc.sampled_accept_session(lg, dl, d, seed, uctr, sctr, **filt)
+        ua = [orc.u01(seed, uctr + r, 0xFFFFFFFE) for r in range(K)]
+        us = orc.u01(seed, sctr, 0xFFFFFFFF)
+        assert (j, tok) == orc.sampled_accept(lg, dl, d, ua, us, **filt)
+        assert u2 == uctr + (j + 1 if j < K else K) and s2 == sctr + 1
+        # the next round starts where this one stopped: its first test uniform is new
+        if K:
+            assert u2 > uctr
+
+
 PINS = [
     pin_core_matrix_form,
     pin_core_closed_form_first_write,
@@ -637,4 +698,7 @@ PINS = [
     pin_filter_top_p_boundary,
     pin_sampled_accept_is_exact,
     pin_sampled_accept_bonus_and_greedy,
+    pin_philox_known_answers,
+    pin_u01_layout,
+    pin_sampled_session_counters,
 ]

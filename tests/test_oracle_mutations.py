@@ -43,10 +43,10 @@ MUTATIONS = {
     "survival_not_cumulative": ("        surv *= sigmoid_f32(raws[k]);", "        surv = sigmoid_f32(raws[k]);"),
     "vt_floor": ("return vt < 2 ? 2 :", "return vt < 1 ? 1 :"),
     "vt_no_anchor": ("int vt = 1 + kept;", "int vt = kept;"),
-    "accept_test_le": ("if (!(u_accept[j] * qr[drafts[j]] < pr[drafts[j]]))",
-                       "if (!(u_accept[j] * qr[drafts[j]] <= pr[drafts[j]]))"),
-    "accept_test_swapped": ("if (!(u_accept[j] * qr[drafts[j]] < pr[drafts[j]]))",
-                            "if (!(u_accept[j] * pr[drafts[j]] < qr[drafts[j]]))"),
+    "accept_test_le": ("if (!(u_accept[j] * (double)(float)qr[drafts[j]] < (double)(float)pr[drafts[j]]))",
+                       "if (!(u_accept[j] * (double)(float)qr[drafts[j]] <= (double)(float)pr[drafts[j]]))"),
+    "accept_test_swapped": ("if (!(u_accept[j] * (double)(float)qr[drafts[j]] < (double)(float)pr[drafts[j]]))",
+                            "if (!(u_accept[j] * (double)(float)pr[drafts[j]] < (double)(float)qr[drafts[j]]))"),
     "residual_sign": ("double r = pr[v] - qr[v];", "double r = qr[v] - pr[v];"),
     "no_renormalise": ("p[v] = p[v] >= th ? p[v] / Z : 0.0;", "p[v] = p[v] >= th ? p[v] / S : 0.0;"),
     "top_k_off_by_one": ("th = sorted[top_k - 1];", "th = sorted[top_k];"),
@@ -58,6 +58,17 @@ MUTATIONS = {
     "j_off_by_one": ("*j_out = j;", "*j_out = j + (j < K);"),
     "bonus_prev_row": ("*bonus_out = vam[j];", "*bonus_out = vam[j > 0 ? j - 1 : 0];"),
     "nan_ignored": ("nan_row = 1;", "nan_row = 0;"),
+    "philox_no_key_bump": ("            k0 += W0;", "            k0 += 0u;"),
+    "philox_words_swapped": ("const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;",
+                             "const uint32_t n0 = (uint32_t)(p0 >> 32) ^ c1 ^ k0;"),
+    "philox_nine_rounds": ("for (int r = 0; r < 10; ++r) {", "for (int r = 0; r < 9; ++r) {"),
+    "u01_bits": ("(double)(o[0] >> 8) * (1.0 / 16777216.0)", "(double)(o[1] >> 8) * (1.0 / 16777216.0)"),
+    "u01_tag_slot": ("const unsigned int ctr[4] = {counter, 0u, 0u, tag};",
+                     "const unsigned int ctr[4] = {counter, tag, 0u, 0u};"),
+    "uctr_advance": ("*uctr += (unsigned int)(*j_out < K ? *j_out + 1 : K);",
+                     "*uctr += (unsigned int)(*j_out < K ? *j_out : K);"),
+    "sample_tag": ("const double u_sample = kdao_u01(seed, *sctr, KDAO_TAG_DRAW);",
+                   "const double u_sample = kdao_u01(seed, *sctr, KDAO_TAG_ACCEPT);"),
     "rollback_keep_early": ("if (keep == T) {", "if (keep >= T - 1) {"),
     "rollback_from_current": ("ring_snap, state_snap,\n                       ring_out, state_out, NULL);",
                               "ring_cur, state_cur,\n                       ring_out, state_out, NULL);"),
