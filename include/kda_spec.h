@@ -77,9 +77,8 @@ extern "C" {
                                CTA stopped early and its units are unfinished.
                                kda_verify_scan has no status word: a caller that
                                wants this report uses kda_verify_scan_var        */
-#define KDA_ST_TIES 0x8     /* spec_accept_sampled: more than 2*KDA_SAMPLED_TOPK_MAX
-                               tokens tie at a row's top-k boundary; that row's
-                               top-p filter was skipped                          */
+/* 0x8 is reserved (no call raises it: the sampled filter is exact for any
+   number of ties) */
 
 /* element types of raw rows and logits */
 #define KDA_F32 0
@@ -348,27 +347,30 @@ int spec_window(const float *scores, int B, int K, int policy, float param, int 
  * glm5_sampled_accept / glm5_sampled_bonus: the rejection-sampling walk over the
  * verify rows.  Target p (verify rows) and draft q (the rows the drafts were drawn
  * from) go through one filter (filter_stats + softmax_gather_filtered):
- *   z = x / temperature, e = exp(z - max z), S = sum e; a token is kept when it
- *   passes every enabled threshold on e: top_k (e >= the k-th largest e, ties kept),
- *   top_p (e >= e_(n), n the first count of the descending-sorted e whose running
- *   sum reaches top_p * S), min_p (e >= min_p); p~ = e / Z over the kept tokens.
- * Draft r is accepted iff u_accept[r] * q~_r(x_r) < p~_r(x_r); the walk stops at the
- * first rejection j.  j < K: the token is drawn from max(0, p~_j - q~_j) (from p~_j
- * if that is zero everywhere); j = K: the bonus is drawn from p~_K.  A draw takes
- * the first token, in vocabulary order, whose running weight exceeds u_sample * (total
- * weight).  The uniforms are the caller's (e.g. a counter-based generator per
- * session); every result is reproducible bit for bit from the inputs.
+ *   z = x / temperature, e = exp(z - max z) (both f32), S = sum e; a token is kept
+ *   when it passes every enabled threshold on e: top_k (e >= the k-th largest e,
+ *   ties kept), top_p (e >= e_(n), n the first count of the descending-sorted e
+ *   whose running sum reaches top_p * S, ties kept), min_p (e >= min_p);
+ *   p~ = e / Z over the kept tokens, Z their sum.  S, Z and every running sum are
+ *   exact integer sums of the weights in units of 2^-46 (no sum depends on the order
+ *   of its terms); top_p is exact for any top_k (0 included) and any number of ties.
+ * Draft r is accepted iff u_r * q~_r(x_r) < p~_r(x_r), compared in double on the f32
+ * values of p~ and q~ (the page's (u as f64) * (qj as f64) < pj as f64); the walk
+ * stops at the first rejection j.  j < K: the token is drawn from max(0, p~_j - q~_j)
+ * (from p~_j if that is zero everywhere); j = K: the bonus is drawn from p~_K.  A
+ * draw takes the first token, in vocabulary order, whose running weight exceeds
+ * u * (total weight).  Every result is reproducible bit for bit from the
+ * inputs (and, for the session form, the counters).
  */
-#define KDA_SAMPLED_TOPK_MAX 512
 typedef struct kda_sampling {
     float temperature; /* > 0                                                  */
-    int top_k;         /* 0 (off) or 1..KDA_SAMPLED_TOPK_MAX                    */
-    float top_p;       /* (0, 1]; < 1 needs top_k >= 1 (its candidates are sorted) */
+    int top_k;         /* 0 off; >= 1 keeps the k largest (>= V: every token)  */
+    float top_p;       /* (0, 1]; 1 off                                        */
     float min_p;       /* [0, 1); 0 off                                        */
 } kda_sampling;
 
 /*
- * spec_accept_sampled -- sampled acceptance for B sessions.
+ * spec_accept_sampled -- sampled acceptance for B sessions with caller uniforms.
  *   logits [B][T][V] and draft_logits [B][T-1][V] (logit_dtype), drafts int32
  *   [B][T-1], u_accept f32 [B][T-1] and u_sample f32 [B] in [0, 1), all device
  *   memory; sp a host struct.  Outputs device int32 [B]: j_out (accepted drafts),
@@ -384,6 +386,36 @@ int spec_accept_sampled(const void *logits, const void *draft_logits, int logit_
                         const int *drafts, const float *u_accept, const float *u_sample, const kda_sampling *sp,
                         int *j_out, int *token_out, int *keep_out, int *dev_status, void *scratch,
                         size_t scratch_bytes, cudaStream_t stream);
+
+/*
+ * spec_accept_sampled_session -- the same walk drawing its uniforms from each
+ * session's own counter-based stream.  glm_spec.rs, SAMPLED ACCEPTANCE and the
+ * Glm5SpecSession doc: the accept-test uniforms come from the session's uctr on the
+ * Philox4x32-10 stream tagged 0xFFFF_FFFE (spec::host_u01), every device draw
+ * advances its sctr, and the counters live on the session so randomness never
+ * repeats across calls.
+ *   seeds    uint64 [B], device: the key of session b's stream is (seed low, seed high)
+ *   counters uint32 [B][2], device, read and written: (uctr, sctr) of session b
+ * Uniform of counter n under tag t: output word 0 of Philox4x32-10 at counter
+ * (n, 0, 0, t), its top 24 bits times 2^-24.  Accept test r of a round uses
+ * (uctr + r, 0xFFFFFFFE); the residual or bonus draw uses (sctr, 0xFFFFFFFF).  After
+ * the call uctr has advanced by the tests run (j + 1 when draft j was rejected, K
+ * when every draft passed) and sctr by one.  Other arguments and results as
+ * spec_accept_sampled; the same scratch size.  seeds and counters 8-byte aligned.
+ */
+int spec_accept_sampled_session(const void *logits, const void *draft_logits, int logit_dtype, int B, int T, int V,
+                                const int *drafts, const unsigned long long *seeds, unsigned *counters,
+                                const kda_sampling *sp, int *j_out, int *token_out, int *keep_out, int *dev_status,
+                                void *scratch, size_t scratch_bytes, cudaStream_t stream);
+
+/*
+ * kda_philox4x32_10 -- the library's counter-based generator on the device:
+ * out[i] = Philox4x32-10(ctr[i], key[i]) (Salmon, Moraes, Dror and Shaw, "Parallel
+ * random numbers: as easy as 1, 2, 3", SC'11; ten rounds), for i < n.
+ *   ctr uint32 [n][4] and out uint32 [n][4], 16-byte aligned; key uint32 [n][2],
+ *   8-byte aligned; device memory.
+ */
+int kda_philox4x32_10(const unsigned *ctr, const unsigned *key, unsigned *out, int n, cudaStream_t stream);
 
 /* Bytes of device scratch spec_accept needs for B sessions of T rows of V logits. */
 size_t spec_accept_scratch_bytes(int B, int T, int V);

@@ -21,8 +21,8 @@ D = 128
 TMAX = 15
 HOST_KEEP_MAX = 2048
 OK, EINVAL, ENAN, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
-ST_NAN, ST_BADKEEP, ST_TIMEOUT, ST_TIES = 0x1, 0x2, 0x4, 0x8
-SAMPLED_TOPK_MAX = 512
+ST_NAN, ST_BADKEEP, ST_TIMEOUT = 0x1, 0x2, 0x4
+TAG_ACCEPT, TAG_DRAW = 0xFFFFFFFE, 0xFFFFFFFF  # counter word 3 of a session's accept tests / draws
 F32, BF16 = 0, 1
 MEM_HOST, MEM_DEVICE = 0, 1
 
@@ -32,9 +32,10 @@ EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollba
            "kda_upload_rows_staged",
            "kda_verify_scan_cols",
            "kda_rollback_cols", "spec_accept_var",
-           "spec_window", "spec_accept_sampled", "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
+           "spec_window", "spec_accept_sampled", "spec_accept_sampled_session", "kda_philox4x32_10",
+           "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 5
+ABI_VERSION = 6
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -122,6 +123,11 @@ def lib(path: str | None = None):
     L.spec_window.restype = ci
     L.spec_accept_sampled.argtypes = [vp, vp, ci, ci, ci, ci, vp, vp, vp, ctypes.POINTER(KdaSampling), vp, vp, vp,
                                       vp, vp, sz, vp]
+    L.spec_accept_sampled_session.argtypes = [vp, vp, ci, ci, ci, ci, vp, vp, vp, ctypes.POINTER(KdaSampling), vp,
+                                              vp, vp, vp, vp, sz, vp]
+    L.spec_accept_sampled_session.restype = ci
+    L.kda_philox4x32_10.argtypes = [vp, vp, vp, ci, vp]
+    L.kda_philox4x32_10.restype = ci
     L.spec_accept_sampled_scratch_bytes.argtypes = [ci, ci]
     L.spec_accept_sampled_scratch_bytes.restype = sz
     L.spec_accept_sampled.restype = ci
@@ -623,6 +629,47 @@ def spec_accept_sampled(logits: torch.Tensor, draft_logits: torch.Tensor, drafts
                                    scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
     _check("spec_accept_sampled", rc)
     return j_out, token_out, keep_out
+
+
+def spec_accept_sampled_session(logits: torch.Tensor, draft_logits: torch.Tensor, drafts: torch.Tensor,
+                                seeds: torch.Tensor, counters: torch.Tensor, temperature: float = 1.0, top_k: int = 0,
+                                top_p: float = 1.0, min_p: float = 0.0, j_out=None, token_out=None, keep_out=None,
+                                dev_status=None, scratch: torch.Tensor | None = None, stream=None):
+    """Sampled acceptance drawing from each session's Philox stream: seeds int64 [B] (the
+    64-bit key, two's complement), counters int32 [B][2] (uctr, sctr; advanced in place on
+    the device).  Other arguments as spec_accept_sampled.  Returns (j, token, keep)."""
+    _dev(logits, "logits")
+    B, T, V = (int(x) for x in logits.shape)
+    _dev(draft_logits, "draft_logits", logits.dtype, (B, T - 1, V))
+    _dev(drafts, "drafts", torch.int32, (B, T - 1))
+    _dev(seeds, "seeds", torch.int64, (B,))
+    _dev(counters, "counters", torch.int32, (B, 2))
+    dev = logits.device
+    j_out = torch.empty(B, dtype=torch.int32, device=dev) if j_out is None else j_out
+    token_out = torch.empty(B, dtype=torch.int32, device=dev) if token_out is None else token_out
+    keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
+    sp = KdaSampling(float(temperature), int(top_k), float(top_p), float(min_p))
+    need = int(lib().spec_accept_sampled_scratch_bytes(B, T))
+    if scratch is None:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    rc = lib().spec_accept_sampled_session(_ptr(logits), _ptr(draft_logits), _row_dtype(logits), B, T, V,
+                                           _ptr(drafts), _ptr(seeds), _ptr(counters), ctypes.byref(sp), _ptr(j_out),
+                                           _ptr(token_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch),
+                                           scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
+    _check("spec_accept_sampled_session", rc)
+    return j_out, token_out, keep_out
+
+
+def philox4x32_10(ctr: torch.Tensor, key: torch.Tensor, stream=None) -> torch.Tensor:
+    """The library's Philox4x32-10 on the device: ctr int32 [n][4] and key int32 [n][2] (the
+    uint32 bit patterns); returns int32 [n][4]."""
+    n = int(ctr.shape[0])
+    _dev(ctr, "ctr", torch.int32, (n, 4))
+    _dev(key, "key", torch.int32, (n, 2))
+    out = torch.empty((n, 4), dtype=torch.int32, device=ctr.device)
+    rc = lib().kda_philox4x32_10(_ptr(ctr), _ptr(key), _ptr(out), n, ctypes.c_void_p(_stream(stream)))
+    _check("kda_philox4x32_10", rc)
+    return out
 
 
 def spec_accept_scratch_bytes(B: int, T: int, V: int) -> int:

@@ -7,25 +7,36 @@
 //   bonus draw from p~_K, the last verify row (j = K);
 // with the target p (verify rows) and the draft q (the rows the drafts were drawn
 // from) taken through the same filter (filter_stats + softmax_gather_filtered):
-//   z = x / temperature, e = exp(z - max z), S = sum e; a token is kept when
-//   e >= the k-th largest e (top_k), when e >= e_(n) with n the first count of
+//   z = x / temperature (f32), e = exp(z - max z) (f32), S = sum e; a token is kept
+//   when e >= the k-th largest e (top_k), when e >= e_(n) with n the first count of
 //   the descending-sorted e whose running sum reaches top_p * S (top_p), and when
-//   e >= min_p (min_p); p~ = e / Z over the kept tokens.
-// The uniforms are inputs; the final draw takes the first token whose running
-// weight, in vocabulary order, exceeds u * (total weight).
+//   e >= min_p (min_p); p~ = e / Z over the kept tokens, Z their sum.
+// Precision: e is f32 (the pages' filter kernels are f32).  S, Z and every running
+// sum are exact integer sums of the weights as multiples of 2^-46 (e <= 1, truncated
+// to 46 fractional bits), so no sum depends on the order of its terms; the walk
+// compares the f32 values of p~ and q~ in double, as the page does ((u as f64) *
+// (qj as f64) < pj as f64); the final draw takes the first token, in vocabulary
+// order, whose running weight exceeds u * (total weight).
+// Uniforms: the caller's (spec_accept_sampled), or drawn from each session's
+// Philox4x32-10 stream at its counters (spec_accept_sampled_session): accept test r
+// at (uctr + r, 0, 0, 0xFFFFFFFE), the final draw at (sctr, 0, 0, 0xFFFFFFFF), under
+// key (seed low, seed high); uctr advances by the tests run and sctr by one, on the
+// device, so randomness never repeats across calls.
 //
-// Two launches.  Every reduction and scan runs in a fixed order, so the results
-// are reproducible bit for bit.
+// Two launches.  Every reduction and scan runs in a fixed order (or on integers), so
+// the results are reproducible bit for bit.
 //   1. row_stats_kernel, one CTA per (session, row) of the 2T-1 target and draft
-//      rows: max, sum, an exact radix select of the k-th largest logit (four 8-bit
-//      histogram passes over order-preserving keys), the candidates at or above it
-//      gathered into shared memory and bitonic-sorted by (e descending, index
-//      ascending) for the top-p running sum, then the kept mass Z, into scratch.
-//      The row stays in L1 between its passes, which read 16-byte vectors.
+//      rows: max, S, an exact radix select of the k-th largest logit (four 8-bit
+//      count passes over order-preserving keys), the top-p threshold by four 8-bit
+//      passes of e-mass histograms (fixed-point integer sums, per-warp bins) that
+//      find the key at which the descending running sum reaches top_p * S, then
+//      the kept mass Z, into scratch.  The row stays in L1 between its passes,
+//      which read 16-byte vectors.
 //   2. walk_kernel, one CTA per session: the accept tests from the row statistics,
 //      then one pass for the total weight of the final draw and one scan for it.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <string>
 
@@ -34,17 +45,21 @@
 namespace kda {
 namespace {
 
-constexpr int SNT = 512;                   // threads per session CTA
+constexpr int SNT = 512;  // threads per CTA
 constexpr int SNW = SNT / 32;
-constexpr int CAP = 2 * KDA_SAMPLED_TOPK_MAX;  // candidates at the top-k boundary, ties included
+constexpr float FX_SCALE = 70368744177664.0f;  // 2^46: e in (0, 1] as a 46-bit fixed-point integer
+constexpr uint32_t TAG_ACCEPT = 0xFFFFFFFEu;    // counter word 3 of the accept-test uniforms
+constexpr uint32_t TAG_DRAW = 0xFFFFFFFFu;      // counter word 3 of the residual / bonus draw
 
 struct SampArgs {
     const void *logits;        // [B][T][V]
     const void *draft_logits;  // [B][T-1][V]
     int bf16, B, T, V;
     const int *drafts;         // [B][T-1]
-    const float *u_accept;     // [B][T-1]
+    const float *u_accept;     // [B][T-1]   (caller uniforms)
     const float *u_sample;     // [B]
+    const unsigned long long *seeds;  // [B]      (session streams; then u_* are unused)
+    unsigned *counters;        // [B][2]: uctr, sctr, advanced in place
     float temperature, top_p, min_p;
     int top_k;
     int *j_out, *token_out, *keep_out, *status;
@@ -54,25 +69,68 @@ struct SampArgs {
 struct RowStats {
     float m;   // max z
     float th;  // kept iff e >= th
-    float Z;   // kept mass
+    double Z;  // kept mass (its exact fixed-point sum, as a double)
     int bad;   // the row holds a NaN or no finite maximum
+    int pad[3];
 };
-static_assert(sizeof(RowStats) == 16, "row statistics are 16 bytes in scratch");
+static_assert(sizeof(RowStats) == 32, "row statistics are 32 bytes in scratch");
 
-struct Shared {
+struct RowShared {
     float red[SNW];
-    int ired[SNW];
+    unsigned long long ured[SNW];
     unsigned hist[256];
-    float ce[CAP];
-    int ci[CAP];
-    int ncand;
+    unsigned long long hw[SNW][256];  // per-warp e-mass bins of one radix pass
+    unsigned long long tot[256];
     unsigned prefix;
     int kk;
-    RowStats rs[2];
-    float pick[2];
-    int flag;
+    unsigned long long above;
+    RowStats rs;
 };
 
+struct WalkShared {
+    unsigned long long ured[SNW];
+    int ired[SNW], ired2[SNW];
+    int jsh, flag;
+    float u_sample;
+};
+
+// ---- Philox4x32-10 and the session uniforms ---------------------------------------
+// Salmon, Moraes, Dror and Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11):
+// each of ten rounds multiplies counter words 0 and 2 by the round multipliers (64-bit
+// products) and forms (hi(B c2) ^ c1 ^ k0, lo(B c2), hi(A c0) ^ c3 ^ k1, lo(A c0));
+// the key advances by the two Weyl increments before every round but the first.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k)
+{
+    constexpr uint32_t A = 0xD2511F53u, B = 0xCD9E8D57u;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r) {
+            k.x += 0x9E3779B9u;
+            k.y += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = A * c.x, hi0 = __umulhi(A, c.x);
+        const uint32_t lo1 = B * c.z, hi1 = __umulhi(B, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+    }
+    return c;
+}
+
+// the uniform of session key `seed` at (n, 0, 0, tag): output word 0, top 24 bits x 2^-24
+__device__ __forceinline__ float session_u01(unsigned long long seed, uint32_t n, uint32_t tag)
+{
+    const uint4 o = philox4x32_10(make_uint4(n, 0u, 0u, tag),
+                                  make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)));
+    return __uint2float_rn(o.x >> 8) * 5.9604644775390625e-8f;  // 2^-24, exact
+}
+
+__global__ void philox_kernel(const uint4 *__restrict__ ctr, const uint2 *__restrict__ key, uint4 *__restrict__ out,
+                              int n)
+{
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        out[i] = philox4x32_10(ctr[i], key[i]);
+}
+
+// ---- row statistics -------------------------------------------------------------------
 __device__ __forceinline__ float load_x(const void *row, int bf16, int v)
 {
     if (bf16)
@@ -92,25 +150,35 @@ __device__ __forceinline__ float unkey(unsigned k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// fixed-order block reductions: each thread's strided terms in order, then a tree
-__device__ float block_sum(Shared &sh, float x)
+__device__ __forceinline__ float e_of(float x, float m, float temperature)
+{
+    return expf(__fsub_rn(__fdiv_rn(x, temperature), m));
+}
+
+// a weight in [0, 1] as an integer multiple of 2^-46 (truncated): exact integer sums,
+// so no sum depends on the order of its additions
+__device__ __forceinline__ unsigned long long fx(float e) { return __float2ull_rz(e * FX_SCALE); }
+constexpr double FX_UNIT = 1.4210854715202004e-14;  // 2^-46
+
+// block reductions: integer sums (any order gives the same result) and the maximum
+__device__ unsigned long long block_sum_u64(unsigned long long *red, unsigned long long x)
 {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
-        x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, off));
+        x += __shfl_xor_sync(0xffffffffu, x, off);
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     __syncthreads();
     if (lane == 0)
-        sh.red[w] = x;
+        red[w] = x;
     __syncthreads();
-    float t = lane < SNW ? sh.red[lane] : 0.f;
+    unsigned long long t = lane < SNW ? red[lane] : 0ull;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
-        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off));
+        t += __shfl_xor_sync(0xffffffffu, t, off);
     return t;
 }
 
-__device__ float block_max(Shared &sh, float x)
+__device__ float block_max(float *red, float x)
 {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
@@ -118,23 +186,13 @@ __device__ float block_max(Shared &sh, float x)
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     __syncthreads();
     if (lane == 0)
-        sh.red[w] = x;
+        red[w] = x;
     __syncthreads();
-    float t = lane < SNW ? sh.red[lane] : -INFINITY;
+    float t = lane < SNW ? red[lane] : -INFINITY;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         t = fmaxf(t, __shfl_xor_sync(0xffffffffu, t, off));
     return t;
-}
-
-__device__ int block_or(Shared &sh, int x)
-{
-    return __syncthreads_or(x);
-}
-
-__device__ __forceinline__ float e_of(float x, float m, float temperature)
-{
-    return expf(__fsub_rn(__fdiv_rn(x, temperature), m));
 }
 
 // f(v, x) for every element of the row; each thread takes whole 16-byte vectors
@@ -168,8 +226,39 @@ __device__ __forceinline__ void for_row(const SampArgs &a, const void *row, F f)
     }
 }
 
-// The k-th largest logit of the row (k >= 1, k <= V), by four 8-bit radix passes.
-__device__ float kth_largest(Shared &sh, const SampArgs &a, const void *row, int k)
+// The same traversal as for_row, chunk by chunk: chunk c of the row into xs[0..n), the
+// elements for_row hands thread threadIdx.x in that order.
+__device__ __forceinline__ int row_chunks(const SampArgs &a)
+{
+    return a.vec ? (a.bf16 ? a.V / 8 : a.V / 4) : a.V;
+}
+
+__device__ __forceinline__ int load_chunk(const SampArgs &a, const void *row, int c, float (&xs)[8])
+{
+    if (a.vec && a.bf16) {
+        const uint4 u = __ldg(static_cast<const uint4 *>(row) + c);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            xs[2 * m] = __uint_as_float(w[m] << 16);
+            xs[2 * m + 1] = __uint_as_float(w[m] & 0xffff0000u);
+        }
+        return 8;
+    }
+    if (a.vec) {
+        const float4 u = __ldg(static_cast<const float4 *>(row) + c);
+        xs[0] = u.x;
+        xs[1] = u.y;
+        xs[2] = u.z;
+        xs[3] = u.w;
+        return 4;
+    }
+    xs[0] = load_x(row, a.bf16, c);
+    return 1;
+}
+
+// The key of the k-th largest logit of the row (k >= 1, k <= V), by four 8-bit count passes.
+__device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void *row, int k)
 {
     if (threadIdx.x == 0) {
         sh.prefix = 0;
@@ -182,11 +271,30 @@ __device__ float kth_largest(Shared &sh, const SampArgs &a, const void *row, int
             sh.hist[i] = 0;
         __syncthreads();
         const unsigned prefix = sh.prefix;
-        for_row(a, row, [&](int, float x) {
-            const unsigned key = okey(x);
-            if ((key & mask) == prefix)
-                atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
-        });
+        // a thread's consecutive elements mostly share the top bytes: count runs of one
+        // bin in a register and add each run once
+        int cur = -1;
+        unsigned run = 0;
+        const int nc = row_chunks(a);
+        for (int c = threadIdx.x; c < nc; c += SNT) {
+            float xs[8];
+            const int n = load_chunk(a, row, c, xs);
+            for (int i = 0; i < n; ++i) {
+                const unsigned key = okey(xs[i]);
+                if ((key & mask) != prefix)
+                    continue;
+                const int bin = static_cast<int>((key >> shift) & 255u);
+                if (bin != cur) {
+                    if (cur >= 0)
+                        atomicAdd(&sh.hist[cur], run);
+                    cur = bin;
+                    run = 0;
+                }
+                ++run;
+            }
+        }
+        if (cur >= 0)
+            atomicAdd(&sh.hist[cur], run);
         __syncthreads();
         if (threadIdx.x < 32) {  // warp 0: the bin holding the kk-th largest, from the top
             const int lane = threadIdx.x;
@@ -205,8 +313,7 @@ __device__ float kth_largest(Shared &sh, const SampArgs &a, const void *row, int
             }
             const unsigned excl = incl - tot;
             const int kk = sh.kk;
-            const bool here = excl < static_cast<unsigned>(kk) && static_cast<unsigned>(kk) <= incl;
-            if (here) {
+            if (excl < static_cast<unsigned>(kk) && static_cast<unsigned>(kk) <= incl) {
                 unsigned run = excl;
                 int bin = 255 - 8 * lane;
                 for (int i = 0; i < 8; ++i) {
@@ -223,11 +330,112 @@ __device__ float kth_largest(Shared &sh, const SampArgs &a, const void *row, int
         mask |= 255u << shift;
         __syncthreads();
     }
-    return unkey(sh.prefix);
+    return sh.prefix;
 }
 
-// Filter statistics of one row into sh.rs[slot].
-__device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int slot)
+// The key of the top-p boundary: the largest key kappa whose mass F(kappa) = sum of e
+// over the tokens with key >= kappa reaches `target` (top_p * S, in fixed-point units).
+// Tokens in key order are tokens in e order, so kappa is the key of the token at which
+// the descending running sum first reaches the target, and e(kappa) is the threshold.
+// Four 8-bit passes from the top byte; each pass bins the e-mass of the tokens under the
+// current prefix, and warp 0 walks the bins from the top (above: the mass of the keys
+// already passed).
+__device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, float m, double target)
+{
+    const int w = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        sh.prefix = 0;
+        sh.above = 0;
+    }
+    unsigned mask = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = threadIdx.x; i < SNW * 256; i += SNT)
+            (&sh.hw[0][0])[i] = 0;
+        __syncthreads();
+        const unsigned prefix = sh.prefix;
+        // runs of one bin summed in a register (integer sums: the order does not matter)
+        int cur = -1;
+        unsigned long long run = 0;
+        const int nc = row_chunks(a);
+        for (int c = threadIdx.x; c < nc; c += SNT) {
+            float xs[8];
+            const int n = load_chunk(a, row, c, xs);
+            for (int i = 0; i < n; ++i) {
+                const unsigned key = okey(xs[i]);
+                if ((key & mask) != prefix)
+                    continue;
+                const int bin = static_cast<int>((key >> shift) & 255u);
+                if (bin != cur) {
+                    if (cur >= 0)
+                        atomicAdd(&sh.hw[w][cur], run);
+                    cur = bin;
+                    run = 0;
+                }
+                run += fx(e_of(xs[i], m, a.temperature));
+            }
+        }
+        if (cur >= 0)
+            atomicAdd(&sh.hw[w][cur], run);
+        __syncthreads();
+        for (int d = threadIdx.x; d < 256; d += SNT) {
+            unsigned long long t = 0;
+            for (int i = 0; i < SNW; ++i)
+                t += sh.hw[i][d];
+            sh.tot[d] = t;
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            const unsigned long long above = sh.above;
+            unsigned long long c[8], tot = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                c[i] = sh.tot[255 - (8 * lane + i)];
+                tot += c[i];
+            }
+            unsigned long long incl = tot;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off)
+                    incl += y;
+            }
+            const unsigned long long excl = incl - tot;
+            const bool here = static_cast<double>(above + excl) < target && static_cast<double>(above + incl) >= target;
+            const unsigned hit = __ballot_sync(0xffffffffu, here);
+            if (here) {
+                unsigned long long run = excl;
+                int bin = 255 - (8 * lane + 7);
+                for (int i = 0; i < 8; ++i) {
+                    if (static_cast<double>(above + run + c[i]) >= target) {
+                        bin = 255 - (8 * lane + i);
+                        break;
+                    }
+                    run += c[i];
+                }
+                sh.prefix = prefix | (static_cast<unsigned>(bin) << shift);
+                sh.above = above + run;
+            }
+            if (!hit && lane == 0) {  // rounding left the target above the mass: the lowest bin with mass
+                int bin = 0;
+                while (bin < 255 && sh.tot[bin] == 0)
+                    ++bin;
+                unsigned long long run = 0;
+                for (int d = 255; d > bin; --d)
+                    run += sh.tot[d];
+                sh.prefix = prefix | (static_cast<unsigned>(bin) << shift);
+                sh.above = above + run;
+            }
+        }
+        mask |= 255u << shift;
+        __syncthreads();
+    }
+    return sh.prefix;
+}
+
+// Filter statistics of one row into sh.rs.
+__device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
 {
     float mx = -INFINITY;
     int nan = 0;
@@ -236,127 +444,49 @@ __device__ void row_stats(Shared &sh, const SampArgs &a, const void *row, int sl
         nan |= z != z;
         mx = fmaxf(mx, z);
     });
-    nan = block_or(sh, nan);
-    const float m = block_max(sh, mx);
+    nan = __syncthreads_or(nan);
+    const float m = block_max(sh.red, mx);
     if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
         if (threadIdx.x == 0)
-            sh.rs[slot] = RowStats{m, 0.f, 0.f, 1};
+            sh.rs = RowStats{m, 0.f, 0.0, 1, {0, 0, 0}};
         __syncthreads();
         return;
     }
-    float s = 0.f;
-    for_row(a, row, [&](int, float x) { s = __fadd_rn(s, e_of(x, m, a.temperature)); });
-    const float S = block_sum(sh, s);
     float th = 0.f;
-    if (a.top_k > 0 && a.top_k < a.V) {
-        const float xk = kth_largest(sh, a, row, a.top_k);
-        const float ek = e_of(xk, m, a.temperature);
-        th = ek;
-        if (a.top_p < 1.0f) {
-            // gather every token at or above the k-th largest logit (ties included)
-            if (threadIdx.x == 0)
-                sh.ncand = 0;
-            __syncthreads();
-            for_row(a, row, [&](int v, float x) {
-                if (x >= xk) {
-                    const int at = atomicAdd(&sh.ncand, 1);
-                    if (at < CAP) {
-                        sh.ce[at] = e_of(x, m, a.temperature);
-                        sh.ci[at] = v;
-                    }
-                }
-            });
-            __syncthreads();
-            const int n = sh.ncand;
-            if (n > CAP) {
-                if (threadIdx.x == 0 && a.status)
-                    atomicOr(a.status, KDA_ST_TIES);  // top-p skipped for this row
-            } else {
-                int np = 1;
-                while (np < n)
-                    np <<= 1;
-                for (int i = n + threadIdx.x; i < np; i += SNT) {
-                    sh.ce[i] = -1.f;
-                    sh.ci[i] = 0x7fffffff;
-                }
-                __syncthreads();
-                // bitonic sort: e descending, then index ascending
-                for (int size = 2; size <= np; size <<= 1) {
-                    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                        for (int i = threadIdx.x; i < np; i += SNT) {
-                            const int jx = i ^ stride;
-                            if (jx > i) {
-                                const bool up = (i & size) == 0;
-                                const float e0 = sh.ce[i], e1 = sh.ce[jx];
-                                const int i0 = sh.ci[i], i1 = sh.ci[jx];
-                                const bool first_before = e0 > e1 || (e0 == e1 && i0 < i1);
-                                if (first_before != up) {
-                                    sh.ce[i] = e1;
-                                    sh.ce[jx] = e0;
-                                    sh.ci[i] = i1;
-                                    sh.ci[jx] = i0;
-                                }
-                            }
-                        }
-                        __syncthreads();
-                    }
-                }
-                // the running sum in sorted order (warp 0, 32 at a time, carried)
-                if (threadIdx.x < 32) {
-                    const float target = __fmul_rn(a.top_p, S);
-                    float carry = 0.f;
-                    float found = 0.f;
-                    bool got = false;
-                    for (int base = 0; base < n && !got; base += 32) {
-                        const int i = base + static_cast<int>(threadIdx.x);
-                        float incl = i < n ? sh.ce[i] : 0.f;
-#pragma unroll
-                        for (int off = 1; off < 32; off <<= 1) {
-                            const float y = __shfl_up_sync(0xffffffffu, incl, off);
-                            if (static_cast<int>(threadIdx.x) >= off)
-                                incl = __fadd_rn(incl, y);
-                        }
-                        const float run = __fadd_rn(carry, incl);
-                        const unsigned hit = __ballot_sync(0xffffffffu, i < n && run >= target);
-                        if (hit) {
-                            const int l = __ffs(hit) - 1;
-                            found = __shfl_sync(0xffffffffu, i < n ? sh.ce[i] : 0.f, l);
-                            got = true;
-                        }
-                        carry = __shfl_sync(0xffffffffu, run, 31);
-                    }
-                    if (threadIdx.x == 0)
-                        sh.pick[0] = got ? found : 0.f;
-                }
-                __syncthreads();
-                th = fmaxf(th, sh.pick[0]);
-            }
-        }
+    if (a.top_k > 0 && a.top_k < a.V)
+        th = e_of(unkey(kth_largest_key(sh, a, row, a.top_k)), m, a.temperature);
+    if (a.top_p < 1.0f) {
+        unsigned long long s = 0;
+        for_row(a, row, [&](int, float x) { s += fx(e_of(x, m, a.temperature)); });
+        const unsigned long long S = block_sum_u64(sh.ured, s);
+        const double target = static_cast<double>(a.top_p) * static_cast<double>(S);
+        th = fmaxf(th, e_of(unkey(topp_key(sh, a, row, m, target)), m, a.temperature));
     }
     if (a.min_p > 0.f)
         th = fmaxf(th, a.min_p);
-    float z = 0.f;
+    unsigned long long z = 0;
     for_row(a, row, [&](int, float x) {
         const float e = e_of(x, m, a.temperature);
         if (e >= th)
-            z = __fadd_rn(z, e);
+            z += fx(e);
     });
-    const float Z = block_sum(sh, z);
+    const double Z = static_cast<double>(block_sum_u64(sh.ured, z)) * FX_UNIT;
     if (threadIdx.x == 0)
-        sh.rs[slot] = RowStats{m, th, Z, 0};
+        sh.rs = RowStats{m, th, Z, 0, {0, 0, 0}};
     __syncthreads();
 }
 
-__device__ __forceinline__ float prob(const RowStats &r, float x, float temperature)
+// p~ of logit x under row statistics r, as the f32 value the walk compares
+__device__ __forceinline__ float prob32(const RowStats &r, float x, float temperature)
 {
     const float e = e_of(x, r.m, temperature);
-    return e >= r.th ? __fdiv_rn(e, r.Z) : 0.f;
+    return e >= r.th ? __double2float_rn(__ddiv_rn(static_cast<double>(e), r.Z)) : 0.f;
 }
 
 // Row ri of session b: target row ri (ri < T) or draft row ri - T.
 __global__ void __launch_bounds__(SNT) row_stats_kernel(const SampArgs a, RowStats *__restrict__ stats)
 {
-    __shared__ Shared sh;
+    __shared__ RowShared sh;
     const int nr = 2 * a.T - 1;
     const int b = blockIdx.x / nr, ri = blockIdx.x % nr;
     const int K = a.T - 1;
@@ -365,14 +495,14 @@ __global__ void __launch_bounds__(SNT) row_stats_kernel(const SampArgs a, RowSta
         ri < a.T ? static_cast<const unsigned char *>(a.logits) + (static_cast<size_t>(b) * a.T + ri) * a.V * es
                  : static_cast<const unsigned char *>(a.draft_logits) +
                        (static_cast<size_t>(b) * K + (ri - a.T)) * a.V * es;
-    row_stats(sh, a, row, 0);
+    row_stats(sh, a, row);
     if (threadIdx.x == 0)
-        stats[blockIdx.x] = sh.rs[0];
+        stats[blockIdx.x] = sh.rs;
 }
 
 __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowStats *__restrict__ stats)
 {
-    __shared__ Shared sh;
+    __shared__ WalkShared sh;
     const int b = blockIdx.x;
     const int K = a.T - 1, nr = 2 * a.T - 1;
     const size_t es = a.bf16 ? 2 : 4;
@@ -380,6 +510,9 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
     const unsigned char *P = static_cast<const unsigned char *>(a.logits) + static_cast<size_t>(b) * a.T * a.V * es;
     const unsigned char *Q = static_cast<const unsigned char *>(a.draft_logits) + static_cast<size_t>(b) * K * a.V * es;
     if (threadIdx.x == 0) {
+        const bool session = a.seeds != nullptr;
+        const unsigned long long seed = session ? a.seeds[b] : 0ull;
+        const uint32_t uctr = session ? a.counters[2 * b] : 0u, sctr = session ? a.counters[2 * b + 1] : 0u;
         int j = 0, bad = 0;
         for (; j < K; ++j) {
             const RowStats rp = st[j], rq = st[a.T + j];
@@ -387,22 +520,28 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
                 bad = 1;
                 break;
             }
+            const float u = session ? session_u01(seed, uctr + static_cast<uint32_t>(j), TAG_ACCEPT)
+                                    : a.u_accept[static_cast<size_t>(b) * K + j];
             const int x = a.drafts[static_cast<size_t>(b) * K + j];
             if (x < 0 || x >= a.V)  // a draft id outside the vocabulary is rejected
                 break;
-            const float p = prob(rp, load_x(P + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
-            const float q = prob(rq, load_x(Q + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
-            const double u = a.u_accept[static_cast<size_t>(b) * K + j];
-            if (!(u * static_cast<double>(q) < static_cast<double>(p)))
+            const float p = prob32(rp, load_x(P + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
+            const float q = prob32(rq, load_x(Q + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
+            if (!(static_cast<double>(u) * static_cast<double>(q) < static_cast<double>(p)))
                 break;
         }
         if (!bad && j == K && st[K].bad)
             bad = 1;
-        sh.kk = j;
+        sh.jsh = j;
         sh.flag = bad;
+        sh.u_sample = session ? session_u01(seed, sctr, TAG_DRAW) : a.u_sample[b];
+        if (session) {  // the tests run (j + 1 on a rejection, K when every draft passed), one draw
+            a.counters[2 * b] = uctr + static_cast<uint32_t>(j < K ? j + 1 : K);
+            a.counters[2 * b + 1] = sctr + 1u;
+        }
     }
     __syncthreads();
-    const int j = sh.kk;
+    const int j = sh.jsh;
     if (sh.flag) {
         if (threadIdx.x == 0) {
             a.j_out[b] = j;
@@ -414,73 +553,76 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
         }
         return;
     }
-    // weights of the final draw: the residual max(0, p~_j - q~_j) (p~_j where it is
-    // zero everywhere), or p~_K
+    // weights of the final draw as fixed-point integers: the residual max(0, p~_j - q~_j)
+    // (p~_j where it is zero everywhere), or p~_K scaled by its mass (e itself)
     const unsigned char *prow = P + static_cast<size_t>(j) * a.V * es;
     const unsigned char *qrow = j < K ? Q + static_cast<size_t>(j) * a.V * es : nullptr;
     const RowStats rp = st[j];
-    const RowStats rq = j < K ? st[a.T + j] : RowStats{0.f, 0.f, 1.f, 0};
-    float wr = 0.f, wp = 0.f;
+    const RowStats rq = j < K ? st[a.T + j] : RowStats{0.f, 0.f, 1.0, 0, {0, 0, 0}};
+    const float ip = __double2float_rn(1.0 / rp.Z), iq = __double2float_rn(1.0 / rq.Z);
+    auto wp_of = [&](float x) -> unsigned long long {
+        const float e = e_of(x, rp.m, a.temperature);
+        return e >= rp.th ? fx(e) : 0ull;
+    };
+    auto wr_of = [&](float x, int v) -> unsigned long long {
+        const float ep = e_of(x, rp.m, a.temperature), eq = e_of(load_x(qrow, a.bf16, v), rq.m, a.temperature);
+        const float r = __fsub_rn(ep >= rp.th ? __fmul_rn(ep, ip) : 0.f, eq >= rq.th ? __fmul_rn(eq, iq) : 0.f);
+        return r > 0.f ? fx(r) : 0ull;
+    };
+    unsigned long long sr = 0, sp = 0;
     for_row(a, prow, [&](int v, float x) {
-        const float p = prob(rp, x, a.temperature);
-        wp = __fadd_rn(wp, p);
-        if (qrow) {
-            const float r = __fsub_rn(p, prob(rq, load_x(qrow, a.bf16, v), a.temperature));
-            wr = __fadd_rn(wr, r > 0.f ? r : 0.f);
-        }
+        sp += wp_of(x);
+        if (qrow)
+            sr += wr_of(x, v);
     });
-    const float Wr = block_sum(sh, wr);
-    const float Wp = block_sum(sh, wp);
-    const bool use_resid = qrow && Wr > 0.f;
-    const float W = use_resid ? Wr : Wp;
-    const float target = __fmul_rn(a.u_sample[b], W);
-    auto weight = [&](int v) -> float {
-        const float p = prob(rp, load_x(prow, a.bf16, v), a.temperature);
-        if (!use_resid)
-            return p;
-        const float r = __fsub_rn(p, prob(rq, load_x(qrow, a.bf16, v), a.temperature));
-        return r > 0.f ? r : 0.f;
+    const unsigned long long Wr = block_sum_u64(sh.ured, sr);
+    const unsigned long long Wp = block_sum_u64(sh.ured, sp);
+    const bool use_resid = qrow && Wr > 0;
+    const unsigned long long W = use_resid ? Wr : Wp;
+    const double target = static_cast<double>(sh.u_sample) * static_cast<double>(W);
+    auto weight = [&](int v) -> unsigned long long {
+        const float x = load_x(prow, a.bf16, v);
+        return use_resid ? wr_of(x, v) : wp_of(x);
     };
     // the first token whose running weight (index order; chunks of SNT x 4 tokens, 4
     // consecutive tokens per thread) exceeds target
     constexpr int PER = 4;
-    float base = 0.f;
+    unsigned long long base = 0;
     int token = -1, last = -1;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     for (int c0 = 0; c0 < a.V && token < 0; c0 += SNT * PER) {
         const int v0 = c0 + PER * threadIdx.x;
-        float wv[PER], own = 0.f;
+        unsigned long long wv[PER], own = 0;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            wv[i] = v0 + i < a.V ? weight(v0 + i) : 0.f;
-            own = __fadd_rn(own, wv[i]);
+            wv[i] = v0 + i < a.V ? weight(v0 + i) : 0ull;
+            own += wv[i];
         }
-        float incl = own;
+        unsigned long long incl = own;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, incl, off);
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
             if (lane >= off)
-                incl = __fadd_rn(incl, y);
+                incl += y;
         }
         __syncthreads();
         if (lane == 31)
-            sh.red[wid] = incl;
+            sh.ured[wid] = incl;
         __syncthreads();
-        float wbase = 0.f, chunk = 0.f;
+        unsigned long long wbase = 0, chunk = 0;
         for (int i = 0; i < SNW; ++i) {
             if (i < wid)
-                wbase = __fadd_rn(wbase, sh.red[i]);
-            chunk = __fadd_rn(chunk, sh.red[i]);
+                wbase += sh.ured[i];
+            chunk += sh.ured[i];
         }
-        const float excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
-        float run = __fadd_rn(base, __fadd_rn(wbase, lane ? excl_w : 0.f));
+        unsigned long long run = base + wbase + incl - own;
         int mine = 0x7fffffff, haswt = -1;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            run = __fadd_rn(run, wv[i]);
-            if (v0 + i < a.V && run > target && mine == 0x7fffffff)
+            run += wv[i];
+            if (v0 + i < a.V && static_cast<double>(run) > target && mine == 0x7fffffff)
                 mine = v0 + i;
-            if (v0 + i < a.V && wv[i] > 0.f)
+            if (v0 + i < a.V && wv[i] > 0)
                 haswt = v0 + i;
         }
         int lo = mine, hi = haswt;
@@ -492,19 +634,19 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
         __syncthreads();
         if (lane == 0) {
             sh.ired[wid] = lo;
-            sh.ci[wid] = hi;
+            sh.ired2[wid] = hi;
         }
         __syncthreads();
         int clo = 0x7fffffff, chi = -1;
         for (int i = 0; i < SNW; ++i) {
             clo = min(clo, sh.ired[i]);
-            chi = max(chi, sh.ci[i]);
+            chi = max(chi, sh.ired2[i]);
         }
         if (clo != 0x7fffffff)
             token = clo;
         if (chi >= 0)
             last = chi;
-        base = __fadd_rn(base, chunk);
+        base += chunk;
     }
     if (token < 0)
         token = last;  // target rounded up to the total: the last token with weight
@@ -514,6 +656,86 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
         if (a.keep_out)
             a.keep_out[b] = j + 1;
     }
+}
+
+int check_sampling(const kda_sampling *sp)
+{
+    if (!sp)
+        return fail(KDA_EINVAL, "sampling parameters must not be NULL");
+    if (!(sp->temperature > 0.f) || !(sp->temperature < INFINITY))
+        return fail(KDA_EINVAL, "temperature must be positive and finite");
+    if (sp->top_k < 0)
+        return fail(KDA_EINVAL, "top_k must be >= 0 (0: off; >= V keeps every token)");
+    if (!(sp->top_p > 0.f) || sp->top_p > 1.f)
+        return fail(KDA_EINVAL, "top_p must lie in (0, 1]");
+    if (!(sp->min_p >= 0.f) || !(sp->min_p < 1.f))
+        return fail(KDA_EINVAL, "min_p must lie in [0, 1)");
+    return KDA_OK;
+}
+
+// Shared body of both entry points: u_accept/u_sample or seeds/counters.
+int sampled_common(const void *logits, const void *draft_logits, int logit_dtype, int B, int T, int V,
+                   const int *drafts, const float *u_accept, const float *u_sample, const unsigned long long *seeds,
+                   unsigned *counters, const kda_sampling *sp, int *j_out, int *token_out, int *keep_out,
+                   int *dev_status, void *scratch, size_t scratch_bytes, cudaStream_t stream)
+{
+    if (B < 0)
+        return fail(KDA_EINVAL, "B must be >= 0");
+    if (T < 1 || T > KDA_TMAX)
+        return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
+    if (V < 1)
+        return fail(KDA_EINVAL, "V must be >= 1");
+    if (logit_dtype != KDA_F32 && logit_dtype != KDA_BF16)
+        return fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
+    int rc = check_sampling(sp);
+    if (rc)
+        return rc;
+    if (B == 0)
+        return ok();
+    const bool session = seeds != nullptr;
+    if (!logits || !j_out || !token_out || (T > 1 && (!draft_logits || !drafts)))
+        return fail(KDA_EINVAL, "logits, draft_logits, drafts, j_out and token_out must not be NULL");
+    if (session ? !counters : (!u_sample || (T > 1 && !u_accept)))
+        return fail(KDA_EINVAL, session ? "counters must not be NULL" : "u_accept and u_sample must not be NULL");
+    if (session && ((reinterpret_cast<uintptr_t>(seeds) & 7u) || (reinterpret_cast<uintptr_t>(counters) & 7u)))
+        return fail(KDA_EINVAL, "seeds and counters must be 8-byte aligned");
+    const uintptr_t al = logit_dtype == KDA_BF16 ? 1u : 3u;
+    if ((reinterpret_cast<uintptr_t>(logits) & al) || (reinterpret_cast<uintptr_t>(draft_logits) & al))
+        return fail(KDA_EINVAL, "logits must be aligned to their element type");
+    const size_t need = static_cast<size_t>(B) * (2 * T - 1) * sizeof(RowStats);
+    if (!scratch || scratch_bytes < need || !aligned16(scratch))
+        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " + std::to_string(need) +
+                                    " bytes");
+    if (static_cast<long long>(B) * (2 * T - 1) > 0x7fffffffLL)
+        return fail(KDA_EINVAL, "B*(2T-1) exceeds the grid limit");
+    SampArgs a{};
+    a.logits = logits;
+    a.draft_logits = draft_logits;
+    a.bf16 = logit_dtype == KDA_BF16;
+    a.B = B;
+    a.T = T;
+    a.V = V;
+    a.drafts = drafts;
+    a.u_accept = u_accept;
+    a.u_sample = u_sample;
+    a.seeds = seeds;
+    a.counters = counters;
+    a.temperature = sp->temperature;
+    a.top_p = sp->top_p;
+    a.min_p = sp->min_p;
+    a.top_k = sp->top_k;
+    a.j_out = j_out;
+    a.token_out = token_out;
+    a.keep_out = keep_out;
+    a.status = dev_status;
+    const size_t row_bytes = static_cast<size_t>(V) * (a.bf16 ? 2 : 4);
+    a.vec = aligned16(logits) && (T == 1 || aligned16(draft_logits)) && row_bytes % 16 == 0;
+    RowStats *stats = static_cast<RowStats *>(scratch);
+    row_stats_kernel<<<static_cast<unsigned>(B * (2 * T - 1)), SNT, 0, stream>>>(a, stats);
+    if ((rc = check_launch("row_stats_kernel")))
+        return rc;
+    walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
+    return check_launch("walk_kernel");
 }
 
 }  // namespace
@@ -533,65 +755,34 @@ extern "C" int spec_accept_sampled(const void *logits, const void *draft_logits,
                                    const kda_sampling *sp, int *j_out, int *token_out, int *keep_out,
                                    int *dev_status, void *scratch, size_t scratch_bytes, cudaStream_t stream)
 {
-    if (B < 0)
-        return fail(KDA_EINVAL, "B must be >= 0");
-    if (T < 1 || T > KDA_TMAX)
-        return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
-    if (V < 1)
-        return fail(KDA_EINVAL, "V must be >= 1");
-    if (logit_dtype != KDA_F32 && logit_dtype != KDA_BF16)
-        return fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
-    if (!sp)
-        return fail(KDA_EINVAL, "sampling parameters must not be NULL");
-    if (!(sp->temperature > 0.f) || !(sp->temperature < INFINITY))
-        return fail(KDA_EINVAL, "temperature must be positive and finite");
-    if (sp->top_k < 0 || sp->top_k > KDA_SAMPLED_TOPK_MAX)
-        return fail(KDA_EINVAL, "top_k must lie in 0..KDA_SAMPLED_TOPK_MAX");
-    if (!(sp->top_p > 0.f) || sp->top_p > 1.f)
-        return fail(KDA_EINVAL, "top_p must lie in (0, 1]");
-    if (sp->top_p < 1.f && sp->top_k == 0)
-        return fail(KDA_EINVAL, "top_p < 1 needs top_k in 1..KDA_SAMPLED_TOPK_MAX (the candidates it sorts)");
-    if (!(sp->min_p >= 0.f) || !(sp->min_p < 1.f))
-        return fail(KDA_EINVAL, "min_p must lie in [0, 1)");
-    if (B == 0)
+    return sampled_common(logits, draft_logits, logit_dtype, B, T, V, drafts, u_accept, u_sample, nullptr, nullptr,
+                          sp, j_out, token_out, keep_out, dev_status, scratch, scratch_bytes, stream);
+}
+
+extern "C" int spec_accept_sampled_session(const void *logits, const void *draft_logits, int logit_dtype, int B,
+                                           int T, int V, const int *drafts, const unsigned long long *seeds,
+                                           unsigned *counters, const kda_sampling *sp, int *j_out, int *token_out,
+                                           int *keep_out, int *dev_status, void *scratch, size_t scratch_bytes,
+                                           cudaStream_t stream)
+{
+    if (B > 0 && !seeds)
+        return fail(KDA_EINVAL, "seeds must not be NULL");
+    return sampled_common(logits, draft_logits, logit_dtype, B, T, V, drafts, nullptr, nullptr, seeds, counters, sp,
+                          j_out, token_out, keep_out, dev_status, scratch, scratch_bytes, stream);
+}
+
+extern "C" int kda_philox4x32_10(const unsigned *ctr, const unsigned *key, unsigned *out, int n, cudaStream_t stream)
+{
+    if (n < 0)
+        return fail(KDA_EINVAL, "n must be >= 0");
+    if (n == 0)
         return ok();
-    if (!logits || !u_sample || !j_out || !token_out || (T > 1 && (!draft_logits || !drafts || !u_accept)))
-        return fail(KDA_EINVAL, "logits, draft_logits, drafts, u_accept, u_sample, j_out and token_out must not "
-                                "be NULL");
-    const uintptr_t al = logit_dtype == KDA_BF16 ? 1u : 3u;
-    if ((reinterpret_cast<uintptr_t>(logits) & al) || (reinterpret_cast<uintptr_t>(draft_logits) & al))
-        return fail(KDA_EINVAL, "logits must be aligned to their element type");
-    const size_t need = spec_accept_sampled_scratch_bytes(B, T);
-    if (!scratch || scratch_bytes < need || !aligned16(scratch))
-        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " + std::to_string(need) +
-                                    " bytes");
-    if (static_cast<long long>(B) * (2 * T - 1) > 0x7fffffffLL)
-        return fail(KDA_EINVAL, "B*(2T-1) exceeds the grid limit");
-    SampArgs a{};
-    a.logits = logits;
-    a.draft_logits = draft_logits;
-    a.bf16 = logit_dtype == KDA_BF16;
-    a.B = B;
-    a.T = T;
-    a.V = V;
-    a.drafts = drafts;
-    a.u_accept = u_accept;
-    a.u_sample = u_sample;
-    a.temperature = sp->temperature;
-    a.top_p = sp->top_p;
-    a.min_p = sp->min_p;
-    a.top_k = sp->top_k;
-    a.j_out = j_out;
-    a.token_out = token_out;
-    a.keep_out = keep_out;
-    a.status = dev_status;
-    const size_t row_bytes = static_cast<size_t>(V) * (a.bf16 ? 2 : 4);
-    a.vec = aligned16(logits) && (T == 1 || aligned16(draft_logits)) && row_bytes % 16 == 0;
-    RowStats *stats = static_cast<RowStats *>(scratch);
-    row_stats_kernel<<<static_cast<unsigned>(B * (2 * T - 1)), SNT, 0, stream>>>(a, stats);
-    int rc = check_launch("row_stats_kernel");
-    if (rc)
-        return rc;
-    walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
-    return check_launch("walk_kernel");
+    if (!ctr || !key || !out)
+        return fail(KDA_EINVAL, "ctr, key and out must not be NULL");
+    if (!aligned16(ctr) || !aligned16(out) || (reinterpret_cast<uintptr_t>(key) & 7u))
+        return fail(KDA_EINVAL, "ctr and out must be 16-byte aligned, key 8-byte aligned");
+    const int grid = static_cast<int>(std::min<long long>((n + 255) / 256, 4096));
+    philox_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint4 *>(ctr), reinterpret_cast<const uint2 *>(key),
+                                            reinterpret_cast<uint4 *>(out), n);
+    return check_launch("philox_kernel");
 }

@@ -169,9 +169,9 @@ def test_window_and_accept_var_reject_on_host(L):
                              None) == kb.EINVAL
 
 
-@pytest.mark.parametrize("sp", [(0.0, 0, 1.0, 0.0), (1.0, -1, 1.0, 0.0), (1.0, kb.SAMPLED_TOPK_MAX + 1, 1.0, 0.0),
-                                (1.0, 0, 0.9, 0.0), (1.0, 10, 0.0, 0.0), (1.0, 10, 1.5, 0.0), (1.0, 0, 1.0, 1.0),
-                                (float("inf"), 0, 1.0, 0.0)])
+@pytest.mark.parametrize("sp", [(0.0, 0, 1.0, 0.0), (1.0, -1, 1.0, 0.0), (1.0, 10, 0.0, 0.0), (1.0, 10, 1.5, 0.0),
+                                (1.0, 0, 1.0, 1.0), (float("inf"), 0, 1.0, 0.0), (float("nan"), 0, 1.0, 0.0),
+                                (1.0, 0, float("nan"), 0.0), (1.0, 0, 1.0, -0.1)])
 def test_sampled_accept_rejects_bad_parameters(L, sp):
     s = kb.KdaSampling(*sp)
     rc = L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, ctypes.byref(s), FAKE, FAKE, None,
@@ -188,11 +188,39 @@ def test_sampled_accept_rejects_bad_shapes_and_pointers(L):
     assert call(T=0) == kb.EINVAL and call(T=16) == kb.EINVAL and call(V=0) == kb.EINVAL
     assert call(dt=9) == kb.EINVAL and call(us=None) == kb.EINVAL and call(lg=FAKE + 1) == kb.EINVAL
     assert call(scr=None) == kb.EINVAL and call(scr=FAKE + 8) == kb.EINVAL
-    assert L.spec_accept_sampled_scratch_bytes(2, 8) == 2 * 15 * 16
-    assert call(nb=2 * 15 * 16 - 1) == kb.EINVAL
+    assert L.spec_accept_sampled_scratch_bytes(2, 8) == 2 * 15 * 32
+    assert call(nb=2 * 15 * 32 - 1) == kb.EINVAL
     assert call(B=0) == kb.OK
     assert L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 2, 8, 1000, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, None,
                                  FAKE, 1 << 20, None) == kb.EINVAL
+
+
+def test_sampled_filters_need_no_top_k():
+    """top_p alone and any top_k >= 1 are valid filters (checked on the host before launch: with
+    B = 0 nothing is launched and the call succeeds)."""
+    L = kb.lib()
+    for sp in ((1.0, 0, 0.9, 0.0), (1.0, 100000, 1.0, 0.0), (0.7, 0, 0.5, 0.05)):
+        s = kb.KdaSampling(*sp)
+        assert L.spec_accept_sampled(FAKE, FAKE, kb.BF16, 0, 8, 1000, FAKE, FAKE, FAKE, ctypes.byref(s), FAKE, FAKE,
+                                     None, None, FAKE, 1 << 20, None) == kb.OK
+
+
+def test_sampled_session_rejects_on_host(L):
+    s = kb.KdaSampling(1.0, 50, 0.9, 0.0)
+    call = lambda **k: L.spec_accept_sampled_session(FAKE, FAKE, kb.BF16, k.get("B", 2), 8, 1000, FAKE,
+                                                     k.get("seeds", FAKE), k.get("ctr", FAKE), ctypes.byref(s), FAKE,
+                                                     FAKE, None, None, FAKE, 1 << 20, None)
+    assert call(seeds=None) == kb.EINVAL and call(ctr=None) == kb.EINVAL
+    assert call(seeds=FAKE + 4) == kb.EINVAL and call(ctr=FAKE + 4) == kb.EINVAL
+    assert call(B=0) == kb.OK
+
+
+def test_philox_rejects_on_host(L):
+    assert L.kda_philox4x32_10(FAKE, FAKE, FAKE, -1, None) == kb.EINVAL
+    assert L.kda_philox4x32_10(None, FAKE, FAKE, 4, None) == kb.EINVAL
+    assert L.kda_philox4x32_10(FAKE + 8, FAKE, FAKE, 4, None) == kb.EINVAL
+    assert L.kda_philox4x32_10(FAKE, FAKE + 4, FAKE, 4, None) == kb.EINVAL
+    assert L.kda_philox4x32_10(None, None, None, 0, None) == kb.OK
 
 
 def test_cols_entry_points_reject_on_host(L):
