@@ -193,6 +193,24 @@ def slowest(ms: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+class nvtx_range:
+    """An NVTX range around a bench section, so a profiler can pick a section's launches
+    (ncu --nvtx --nvtx-include "<name>/")."""
+
+    def __init__(self, name: str):
+        self.name = name
+
+    def __enter__(self):
+        import torch
+        torch.cuda.nvtx.range_push(self.name)
+        return self
+
+    def __exit__(self, *exc):
+        import torch
+        torch.cuda.nvtx.range_pop()
+        return False
+
+
 def job_rows_per_s(world: int, B: int, T: int, ms: float) -> float:
     """Verify rows per second of the whole job: world replicas of B sessions x T rows per step."""
     return world * B * T / (ms * 1e-3)
@@ -594,10 +612,11 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     t_wall = time.perf_counter()
-    e0.record(stream)
-    for i in range(K):
-        dstep((args.warmup + 1 + i) % R, evs[i])
-    e1.record(stream)
+    with nvtx_range("deferred"):
+        e0.record(stream)
+        for i in range(K):
+            dstep((args.warmup + 1 + i) % R, evs[i])
+        e1.record(stream)
     barrier()
     t_wall = time.perf_counter() - t_wall
     total_ms = e0.elapsed_time(e1)
@@ -650,10 +669,11 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         step(i % R)
     barrier()
     pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    pa.record(stream)
-    for i in range(Kp):
-        step((3 + i) % R, evp[i])
-    pb.record(stream)
+    with nvtx_range("separate"):
+        pa.record(stream)
+        for i in range(Kp):
+            step((3 + i) % R, evp[i])
+        pb.record(stream)
     barrier()
     if int(status.item()):
         raise RuntimeError(f"device status {int(status.item()):#x} after the ping-pong steps")
@@ -673,10 +693,11 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         step(i % R, plans_=plans)
     barrier()
     ia, ib = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ia.record(stream)
-    for i in range(Ki):
-        step(i % R, evi[i], plans_=plans)
-    ib.record(stream)
+    with nvtx_range("in_place"):
+        ia.record(stream)
+        for i in range(Ki):
+            step(i % R, evi[i], plans_=plans)
+        ib.record(stream)
     barrier()
     if int(status.item()):
         raise RuntimeError(f"device status {int(status.item()):#x} after the in-place steps")
@@ -855,11 +876,12 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
                                    dev_status=status, stream=stream, **filt)
         barrier()
         a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a_.record(stream)
-        for _ in range(Ks):
-            kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
-                                   dev_status=status, stream=stream, **filt)
-        b_.record(stream)
+        with nvtx_range("sampled"):
+            a_.record(stream)
+            for _ in range(Ks):
+                kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
+                                       dev_status=status, stream=stream, **filt)
+            b_.record(stream)
         barrier()
         if int(status.item()) or int(j_out.min().item()) != w.K:
             raise RuntimeError("sampled accept: unexpected status or walk length")
@@ -871,11 +893,12 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
             kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok, keep_out=keep_out,
                                            dev_status=status, stream=stream, **filt)
         barrier()
-        a_.record(stream)
-        for _ in range(Ks):
-            kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok, keep_out=keep_out,
-                                           dev_status=status, stream=stream, **filt)
-        b_.record(stream)
+        with nvtx_range("sampled_session"):
+            a_.record(stream)
+            for _ in range(Ks):
+                kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok,
+                                               keep_out=keep_out, dev_status=status, stream=stream, **filt)
+            b_.record(stream)
         barrier()
         if int(status.item()) or int(j_out.min().item()) != w.K:
             raise RuntimeError("sampled accept (session): unexpected status or walk length")

@@ -47,7 +47,6 @@ namespace {
 
 constexpr int SNT = 512;  // threads per CTA
 constexpr int SNW = SNT / 32;
-constexpr float FX_SCALE = 70368744177664.0f;  // 2^46: e in (0, 1] as a 46-bit fixed-point integer
 constexpr uint32_t TAG_ACCEPT = 0xFFFFFFFEu;    // counter word 3 of the accept-test uniforms
 constexpr uint32_t TAG_DRAW = 0xFFFFFFFFu;      // counter word 3 of the residual / bonus draw
 
@@ -82,7 +81,7 @@ struct RowShared {
     unsigned long long hw[SNW][256];  // per-warp e-mass bins of one radix pass
     unsigned long long tot[256];
     unsigned prefix;
-    int kk;
+    int kk, done;
     unsigned long long above;
     RowStats rs;
 };
@@ -156,8 +155,19 @@ __device__ __forceinline__ float e_of(float x, float m, float temperature)
 }
 
 // a weight in [0, 1] as an integer multiple of 2^-46 (truncated): exact integer sums,
-// so no sum depends on the order of its additions
-__device__ __forceinline__ unsigned long long fx(float e) { return __float2ull_rz(e * FX_SCALE); }
+// so no sum depends on the order of its additions.  Formed from the float's fields
+// with integer shifts (a float-to-64-bit conversion runs on the FP64 pipe, which is
+// narrow on this GPU): e = m 2^(E - 150) with m the 24-bit significand, so
+// e 2^46 = m 2^(E - 104).
+__device__ __forceinline__ unsigned long long fx(float e)
+{
+    const uint32_t b = __float_as_uint(e);
+    const int E = static_cast<int>(b >> 23);
+    if (E < 81)  // below 2^-46, or zero
+        return 0ull;
+    const unsigned long long m = (b & 0x7fffffu) | 0x800000u;
+    return E >= 104 ? m << (E - 104) : m >> (104 - E);
+}
 constexpr double FX_UNIT = 1.4210854715202004e-14;  // 2^-46
 
 // block reductions: integer sums (any order gives the same result) and the maximum
@@ -339,13 +349,17 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
 // the descending running sum first reaches the target, and e(kappa) is the threshold.
 // Four 8-bit passes from the top byte; each pass bins the e-mass of the tokens under the
 // current prefix, and warp 0 walks the bins from the top (above: the mass of the keys
-// already passed).
-__device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, float m, double target)
+// already passed).  Only keys >= floor take part (the k-th largest key under top_k):
+// when their whole mass stays below the target, the top-p threshold lies under the
+// top-k one and floor is returned.
+__device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, float m, double target,
+                             unsigned floor)
 {
     const int w = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         sh.prefix = 0;
         sh.above = 0;
+        sh.done = 0;
     }
     unsigned mask = 0;
     for (int pass = 0; pass < 4; ++pass) {
@@ -363,7 +377,7 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
             const int n = load_chunk(a, row, c, xs);
             for (int i = 0; i < n; ++i) {
                 const unsigned key = okey(xs[i]);
-                if ((key & mask) != prefix)
+                if ((key & mask) != prefix || key < floor)
                     continue;
                 const int bin = static_cast<int>((key >> shift) & 255u);
                 if (bin != cur) {
@@ -402,7 +416,16 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
                     incl += y;
             }
             const unsigned long long excl = incl - tot;
-            const bool here = static_cast<double>(above + excl) < target && static_cast<double>(above + incl) >= target;
+            const unsigned long long all = __shfl_sync(0xffffffffu, incl, 31);
+            if (pass == 0 && static_cast<double>(all) < target) {  // top-k binds
+                if (lane == 0) {
+                    sh.prefix = floor;
+                    sh.done = 1;
+                }
+                __syncwarp();
+            }
+            const bool here = !sh.done && static_cast<double>(above + excl) < target &&
+                              static_cast<double>(above + incl) >= target;
             const unsigned hit = __ballot_sync(0xffffffffu, here);
             if (here) {
                 unsigned long long run = excl;
@@ -417,7 +440,7 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
                 sh.prefix = prefix | (static_cast<unsigned>(bin) << shift);
                 sh.above = above + run;
             }
-            if (!hit && lane == 0) {  // rounding left the target above the mass: the lowest bin with mass
+            if (!hit && !sh.done && lane == 0) {  // rounding left the target above the mass: the lowest bin with mass
                 int bin = 0;
                 while (bin < 255 && sh.tot[bin] == 0)
                     ++bin;
@@ -430,6 +453,8 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
         }
         mask |= 255u << shift;
         __syncthreads();
+        if (sh.done)
+            break;
     }
     return sh.prefix;
 }
@@ -453,14 +478,17 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
         return;
     }
     float th = 0.f;
-    if (a.top_k > 0 && a.top_k < a.V)
-        th = e_of(unkey(kth_largest_key(sh, a, row, a.top_k)), m, a.temperature);
+    unsigned floor = 0;  // the k-th largest key: top-p looks no lower
+    if (a.top_k > 0 && a.top_k < a.V) {
+        floor = kth_largest_key(sh, a, row, a.top_k);
+        th = e_of(unkey(floor), m, a.temperature);
+    }
     if (a.top_p < 1.0f) {
         unsigned long long s = 0;
         for_row(a, row, [&](int, float x) { s += fx(e_of(x, m, a.temperature)); });
         const unsigned long long S = block_sum_u64(sh.ured, s);
         const double target = static_cast<double>(a.top_p) * static_cast<double>(S);
-        th = fmaxf(th, e_of(unkey(topp_key(sh, a, row, m, target)), m, a.temperature));
+        th = fmaxf(th, e_of(unkey(topp_key(sh, a, row, m, target, floor)), m, a.temperature));
     }
     if (a.min_p > 0.f)
         th = fmaxf(th, a.min_p);
@@ -564,90 +592,97 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
         const float e = e_of(x, rp.m, a.temperature);
         return e >= rp.th ? fx(e) : 0ull;
     };
-    auto wr_of = [&](float x, int v) -> unsigned long long {
-        const float ep = e_of(x, rp.m, a.temperature), eq = e_of(load_x(qrow, a.bf16, v), rq.m, a.temperature);
+    auto wr_of = [&](float x, float xq) -> unsigned long long {
+        const float ep = e_of(x, rp.m, a.temperature), eq = e_of(xq, rq.m, a.temperature);
         const float r = __fsub_rn(ep >= rp.th ? __fmul_rn(ep, ip) : 0.f, eq >= rq.th ? __fmul_rn(eq, iq) : 0.f);
         return r > 0.f ? fx(r) : 0ull;
     };
+    // thread t owns a contiguous run of the row's 16-byte chunks (the for_row chunks):
+    // one pass sums both weight kinds per run; the block's exclusive scan of the run sums
+    // finds the run holding the target, and its thread walks it
+    const int nc = row_chunks(a), per = a.vec ? (a.bf16 ? 8 : 4) : 1;
+    const int cs = (nc + SNT - 1) / SNT;
+    const int c0 = threadIdx.x * cs, c1 = min(nc, c0 + cs);
     unsigned long long sr = 0, sp = 0;
-    for_row(a, prow, [&](int v, float x) {
-        sp += wp_of(x);
+    for (int c = c0; c < c1; ++c) {
+        float xp[8], xq[8];
+        const int n = load_chunk(a, prow, c, xp);
         if (qrow)
-            sr += wr_of(x, v);
-    });
+            load_chunk(a, qrow, c, xq);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < n) {
+                sp += wp_of(xp[i]);
+                if (qrow)
+                    sr += wr_of(xp[i], xq[i]);
+            }
+    }
     const unsigned long long Wr = block_sum_u64(sh.ured, sr);
     const unsigned long long Wp = block_sum_u64(sh.ured, sp);
     const bool use_resid = qrow && Wr > 0;
-    const unsigned long long W = use_resid ? Wr : Wp;
-    const double target = static_cast<double>(sh.u_sample) * static_cast<double>(W);
-    auto weight = [&](int v) -> unsigned long long {
-        const float x = load_x(prow, a.bf16, v);
-        return use_resid ? wr_of(x, v) : wp_of(x);
-    };
-    // the first token whose running weight (index order; chunks of SNT x 4 tokens, 4
-    // consecutive tokens per thread) exceeds target
-    constexpr int PER = 4;
-    unsigned long long base = 0;
-    int token = -1, last = -1;
+    const unsigned long long W = use_resid ? Wr : Wp, own = use_resid ? sr : sp;
+    // run > u W  <=>  run > floor(u W) for the integer running weights
+    const unsigned long long target =
+        static_cast<unsigned long long>(static_cast<double>(sh.u_sample) * static_cast<double>(W));
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    for (int c0 = 0; c0 < a.V && token < 0; c0 += SNT * PER) {
-        const int v0 = c0 + PER * threadIdx.x;
-        unsigned long long wv[PER], own = 0;
+    unsigned long long incl = own;
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            wv[i] = v0 + i < a.V ? weight(v0 + i) : 0ull;
-            own += wv[i];
-        }
-        unsigned long long incl = own;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off)
-                incl += y;
-        }
-        __syncthreads();
-        if (lane == 31)
-            sh.ured[wid] = incl;
-        __syncthreads();
-        unsigned long long wbase = 0, chunk = 0;
-        for (int i = 0; i < SNW; ++i) {
-            if (i < wid)
-                wbase += sh.ured[i];
-            chunk += sh.ured[i];
-        }
-        unsigned long long run = base + wbase + incl - own;
-        int mine = 0x7fffffff, haswt = -1;
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            run += wv[i];
-            if (v0 + i < a.V && static_cast<double>(run) > target && mine == 0x7fffffff)
-                mine = v0 + i;
-            if (v0 + i < a.V && wv[i] > 0)
-                haswt = v0 + i;
-        }
-        int lo = mine, hi = haswt;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
-        }
-        __syncthreads();
-        if (lane == 0) {
-            sh.ired[wid] = lo;
-            sh.ired2[wid] = hi;
-        }
-        __syncthreads();
-        int clo = 0x7fffffff, chi = -1;
-        for (int i = 0; i < SNW; ++i) {
-            clo = min(clo, sh.ired[i]);
-            chi = max(chi, sh.ired2[i]);
-        }
-        if (clo != 0x7fffffff)
-            token = clo;
-        if (chi >= 0)
-            last = chi;
-        base += chunk;
+    for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off)
+            incl += y;
     }
+    __syncthreads();
+    if (lane == 31)
+        sh.ured[wid] = incl;
+    __syncthreads();
+    unsigned long long wbase = 0;
+    for (int i = 0; i < wid; ++i)
+        wbase += sh.ured[i];
+    const unsigned long long excl = wbase + incl - own;
+    if (threadIdx.x == 0)
+        sh.ired[0] = -1;
+    __syncthreads();
+    if (excl <= target && target < excl + own) {  // exactly one thread: the run of the draw
+        unsigned long long run = excl;
+        for (int c = c0, found = 0; c < c1 && !found; ++c) {
+            float xp[8], xq[8];
+            const int n = load_chunk(a, prow, c, xp);
+            if (use_resid)
+                load_chunk(a, qrow, c, xq);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i < n && !found) {
+                    run += use_resid ? wr_of(xp[i], xq[i]) : wp_of(xp[i]);
+                    if (run > target) {
+                        sh.ired[0] = c * per + i;
+                        found = 1;
+                    }
+                }
+        }
+    }
+    // the last token with weight, for a target rounded up to the total
+    int haswt = -1;
+    if (own > 0)
+        for (int c = c1 - 1; c >= c0 && haswt < 0; --c) {
+            float xp[8], xq[8];
+            const int n = load_chunk(a, prow, c, xp);
+            if (use_resid)
+                load_chunk(a, qrow, c, xq);
+#pragma unroll
+            for (int i = 7; i >= 0; --i)
+                if (i < n && haswt < 0 && (use_resid ? wr_of(xp[i], xq[i]) : wp_of(xp[i])) > 0)
+                    haswt = c * per + i;
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        haswt = max(haswt, __shfl_xor_sync(0xffffffffu, haswt, off));
+    if (lane == 0)
+        sh.ired2[wid] = haswt;
+    __syncthreads();
+    int token = sh.ired[0], last = -1;
+    for (int i = 0; i < SNW; ++i)
+        last = max(last, sh.ired2[i]);
     if (token < 0)
         token = last;  // target rounded up to the total: the last token with weight
     if (threadIdx.x == 0) {
