@@ -45,7 +45,8 @@ FALLBACK_HBM_GBS = 6800.0
 # source the traffic is reported as null.
 TRAFFIC_SOURCE = "3d4f03dcb519c16059bdfa8aa76e82e3a2e3220f19b3286718812a795e365ad2"
 TRAFFIC_BYTES = {"stack34": (201_875_456 + 257_812_992, 504_740_608),
-                 "batched32": (204_221_440 + 233_559_808, 478_401_792)}
+                 "batched32": (204_221_440 + 233_559_808, 478_401_792),
+                 "stress64x34": (13_474_439_936 + 17_652_109_824, 30_453_346_304)}
 SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
 
 
