@@ -129,6 +129,10 @@ typedef struct kda_stash {
 
 /*
  * kda_verify_scan -- one verify round over every (layer, session, head) unit.
+ * glm_spec.rs, module doc VERIFY-ROW BATCHING (the T rows of a round run sequentially
+ * inside one launch; the in-kernel T-loop over the register-resident state is the
+ * chained t=1 program) and glm5_verify_rows (t <= 15); the snapshot is the pre-row-0
+ * state of glm_spec.rs, ROLLBACK and the Glm5VerifyCkpt doc.
  * Rows 0..T-1 of `rows` pass through conv + SiLU, normalisation, gates and the
  * gated delta rule in one launch; state and conv_ring advance by T rows in place.
  *   out   f32 [L][B][T][H][dv] the attention outputs o_t, or NULL.
@@ -143,6 +147,9 @@ int kda_verify_scan(const kda_dims *dims, const kda_layer_state *st, const kda_r
 
 /*
  * kda_rollback -- accept-j rollback of the round recorded in `stash`.
+ * glm_spec.rs, glm5_verify_rollback and the KDA arm of glm5_rollback_layer (keep in
+ * 1..t; keep == t keeps the resident state; else restore the snapshot and replay the
+ * stolen rows 0..keep-1), module doc ROLLBACK.
  * keep[b] (= accepted drafts + 1, the anchor row is always kept) selects, per
  * session b, the state after row keep-1:
  *   keep == stash->T : nothing to do (the resident state is that state);
@@ -314,7 +321,7 @@ int kda_rollback_cols(const kda_dims *dims, const kda_layer_state *st, const flo
  *   logits rows 0..t_rows[b]-1 and drafts 0..t_rows[b]-2: j = the first r <
  *   t_rows[b]-1 whose draft misses, else t_rows[b]-1; bonus = vam[j]; keep = j+1.
  *   A count outside 1..T gives j = -1, bonus = -1, keep = 0 and KDA_ST_BADKEEP.
- *   Scratch as for spec_accept (spec_accept_scratch_bytes(B, T, V)).
+ *   scratch, scratch_bytes: not used, as for spec_accept.
  */
 int spec_accept_var(const void *logits, int logit_dtype, int B, int T, int V, const int *t_rows,
                     const int *drafts, int *j_out, int *bonus_out, int *keep_out, int *dev_status,
@@ -417,11 +424,15 @@ int spec_accept_sampled_session(const void *logits, const void *draft_logits, in
  */
 int kda_philox4x32_10(const unsigned *ctr, const unsigned *key, unsigned *out, int n, cudaStream_t stream);
 
-/* Bytes of device scratch spec_accept needs for B sessions of T rows of V logits. */
+/* Bytes of the per-slice partial results of B sessions of T rows of V logits in the
+ * two-launch accept (the bound of spec_accept_noalloc). */
 size_t spec_accept_scratch_bytes(int B, int T, int V);
 
 /*
  * spec_accept -- greedy acceptance for B sessions.
+ * glm_spec.rs, glm5_spec_round step 4 (one device argmax per verify row, lowest index
+ * wins, then the longest matching prefix; keep = j + 1) and guard_vocab_token (a NaN
+ * row is refused).
  *   logits [B][T][V] (KDA_F32 or KDA_BF16, logit_dtype), drafts int32 [B][T-1]
  *   (drafts[b][r] is the token drafted for the position that row r predicts).
  * Per session: vam[r] = index of the maximum of row r, the lowest index winning
@@ -430,8 +441,10 @@ size_t spec_accept_scratch_bytes(int B, int T, int V);
  * bonus = vam[j]; keep = j + 1.
  * Outputs (device int32 [B], each may be NULL): j_out, bonus_out, keep_out.  If
  * row j holds a NaN, bonus is -1 and KDA_ST_NAN is set in *dev_status.
- * scratch: device memory of at least spec_accept_scratch_bytes(B, T, V) bytes,
- * 16-byte aligned; its contents need no initialisation.
+ * scratch, scratch_bytes: not used (NULL and 0 are fine).  The one launch of
+ * thread-block clusters passes its partial results through shared memory; the
+ * arguments remain for existing callers.  spec_accept_scratch_bytes(B, T, V) is the
+ * size of the partial results of the two-launch form (spec_accept_noalloc).
  */
 int spec_accept(const void *logits, int logit_dtype, int B, int T, int V, const int *drafts,
                 int *j_out, int *bonus_out, int *keep_out, int *dev_status, void *scratch,
@@ -449,8 +462,11 @@ int spec_accept(const void *logits, int logit_dtype, int B, int T, int V, const 
  * every GPU that loads the library holds until the process exits.  Calls whose
  * spec_accept_scratch_bytes(B, T, V) exceeds it return KDA_EINVAL and launch
  * nothing.  The first call on a device looks up the array's device address with
- * that device current; make that first call before any stream capture.  The
- * array keeps the last call's contents; nothing in it needs to start at zero.
+ * that device current and keeps it with the context it belongs to; make that
+ * first call before any stream capture.  A later call in another context (after
+ * cudaDeviceReset, or in a context the caller made current) looks the address up
+ * again, and the same advice holds for it.  The array keeps the last call's
+ * contents; nothing in it needs to start at zero.
  * All calls share the one array, so calls that overlap on the GPU (for instance
  * on two streams at once) race; order them on one stream or with events.
  * The library calls no allocation routine for this entry point.

@@ -580,12 +580,10 @@ def spec_accept_var(logits: torch.Tensor, drafts: torch.Tensor, t_rows: torch.Te
     j_out = torch.empty(B, dtype=torch.int32, device=dev) if j_out is None else j_out
     bonus_out = torch.empty(B, dtype=torch.int32, device=dev) if bonus_out is None else bonus_out
     keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
-    need = spec_accept_scratch_bytes(B, T, V)
-    if scratch is None:
-        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    nb = 0 if scratch is None else scratch.numel() * scratch.element_size()  # not used by the library
     rc = lib().spec_accept_var(_ptr(logits), _row_dtype(logits), B, T, V, _ptr(t_rows), _ptr(drafts), _ptr(j_out),
-                               _ptr(bonus_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch),
-                               scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
+                               _ptr(bonus_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch), nb,
+                               ctypes.c_void_p(_stream(stream)))
     _check("spec_accept_var", rc)
     return j_out, bonus_out, keep_out
 
@@ -690,12 +688,10 @@ def spec_accept(logits: torch.Tensor, drafts: torch.Tensor, j_out=None, bonus_ou
     j_out = torch.empty(B, dtype=torch.int32, device=dev) if j_out is None else j_out
     bonus_out = torch.empty(B, dtype=torch.int32, device=dev) if bonus_out is None else bonus_out
     keep_out = torch.empty(B, dtype=torch.int32, device=dev) if keep_out is None else keep_out
-    need = spec_accept_scratch_bytes(B, T, V)
-    if scratch is None:
-        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    nb = 0 if scratch is None else scratch.numel() * scratch.element_size()  # not used by the library
     rc = lib().spec_accept(_ptr(logits), _row_dtype(logits), B, T, V, _ptr(drafts), _ptr(j_out),
-                           _ptr(bonus_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch),
-                           scratch.numel() * scratch.element_size(), ctypes.c_void_p(_stream(stream)))
+                           _ptr(bonus_out), _ptr(keep_out), _ptr(dev_status), _ptr(scratch), nb,
+                           ctypes.c_void_p(_stream(stream)))
     _check("spec_accept", rc)
     return j_out, bonus_out, keep_out
 

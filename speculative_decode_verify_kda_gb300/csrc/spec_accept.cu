@@ -21,6 +21,8 @@
 // The selection is a total order on (value, -index), so the reduction order
 // never changes the result.
 #include <cooperative_groups.h>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -400,12 +402,10 @@ extern "C" int spec_accept(const void *logits, int logit_dtype, int B, int T, in
         return fail(KDA_EINVAL, "logits and drafts must not be NULL");
     if (!aligned16(logits))
         return fail(KDA_EINVAL, "logits must be 16-byte aligned");
-    // the scratch stays in the signature (and is checked) so that callers keep one
-    // contract; the cluster form passes its partial results through shared memory
-    const size_t need = spec_accept_scratch_bytes(B, T, V);
-    if (!scratch || scratch_bytes < need || !aligned16(scratch))
-        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " +
-                                    std::to_string(need) + " bytes");
+    // the cluster form passes its partial results through shared memory: the scratch
+    // arguments stay in the signature for existing callers and are not used
+    (void)scratch;
+    (void)scratch_bytes;
     return launch_accept_cluster(logits, logit_dtype, B, T, V, drafts, j_out, bonus_out, keep_out, dev_status,
                                  nullptr, stream);
 }
@@ -428,11 +428,29 @@ constexpr int MAX_DEVICES = 64;
 static __device__ __align__(256) unsigned char g_accept_scratch[NOALLOC_SCRATCH];
 
 std::mutex g_scratch_mutex;
-void *g_scratch_addr[MAX_DEVICES] = {};
+struct ScratchAddr {
+    CUcontext ctx;  // the context the address was looked up in
+    void *addr;
+};
+ScratchAddr g_scratch_addr[MAX_DEVICES] = {};
+
+using CtxGetCurrent = PFN_cuCtxGetCurrent_v4000;
+
+CtxGetCurrent lookup_ctx_get_current()
+{
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<CtxGetCurrent>(f);
+}
 
 // Device address of g_accept_scratch on the current device.  On the host the
-// symbol is only a stand-in, so its address is looked up once per device (with
-// that device current) and cached.
+// symbol is only a stand-in, so its address is looked up with the device current
+// and kept per device together with the context it belongs to; a call in another
+// context (after cudaDeviceReset, say, or with a context of the caller's own) looks
+// it up again.
 int noalloc_scratch(void **addr)
 {
     int dev = 0;
@@ -441,15 +459,25 @@ int noalloc_scratch(void **addr)
         return fail(KDA_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= MAX_DEVICES)
         return fail(KDA_EINVAL, "device ordinal beyond the no-allocation table");
+    static const CtxGetCurrent ctx_get = lookup_ctx_get_current();
+    if (!ctx_get)
+        return fail(KDA_ECUDA, "cuCtxGetCurrent is not available from the CUDA driver");
+    CUcontext ctx = nullptr;
+    if (ctx_get(&ctx) != CUDA_SUCCESS)
+        return fail(KDA_ECUDA, "cuCtxGetCurrent failed");
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr &sa = g_scratch_addr[dev];
+    if (!ctx || !sa.addr || sa.ctx != ctx) {
         void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_accept_scratch);
+        e = cudaGetSymbolAddress(&p, g_accept_scratch);  // makes the device's context current if none was
         if (e != cudaSuccess || !p)
             return fail(KDA_ECUDA, std::string("cudaGetSymbolAddress(accept scratch): ") + cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
+        if (ctx_get(&ctx) != CUDA_SUCCESS || !ctx)
+            return fail(KDA_ECUDA, "cuCtxGetCurrent failed");
+        sa.ctx = ctx;
+        sa.addr = p;
     }
-    *addr = g_scratch_addr[dev];
+    *addr = sa.addr;
     return KDA_OK;
 }
 
@@ -575,10 +603,8 @@ extern "C" int spec_accept_var(const void *logits, int logit_dtype, int B, int T
         return fail(KDA_EINVAL, "logits, t_rows and drafts must not be NULL");
     if (!aligned16(logits) || (reinterpret_cast<uintptr_t>(t_rows) & 3u))
         return fail(KDA_EINVAL, "logits must be 16-byte and t_rows 4-byte aligned");
-    const size_t need = spec_accept_scratch_bytes(B, T, V);
-    if (!scratch || scratch_bytes < need || !aligned16(scratch))
-        return fail(KDA_EINVAL, "scratch must be 16-byte aligned device memory of at least " +
-                                    std::to_string(need) + " bytes");
+    (void)scratch;  // not used by the cluster form, as in spec_accept
+    (void)scratch_bytes;
     return launch_accept_cluster(logits, logit_dtype, B, T, V, drafts, j_out, bonus_out, keep_out, dev_status,
                                  t_rows, stream);
 }

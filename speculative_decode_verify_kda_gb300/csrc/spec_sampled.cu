@@ -91,6 +91,8 @@ struct WalkShared {
     int ired[SNW], ired2[SNW];
     int jsh, flag;
     float u_sample;
+    float tu[KDA_TMAX], tp[KDA_TMAX], tq[KDA_TMAX];  // accept test r: its uniform, p~ and q~
+    int tcode[KDA_TMAX];                             // 0 ok, 1 a NaN row, 2 draft id outside the vocabulary
 };
 
 // ---- Philox4x32-10 and the session uniforms ---------------------------------------
@@ -537,25 +539,33 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
     const RowStats *st = stats + static_cast<size_t>(b) * nr;
     const unsigned char *P = static_cast<const unsigned char *>(a.logits) + static_cast<size_t>(b) * a.T * a.V * es;
     const unsigned char *Q = static_cast<const unsigned char *>(a.draft_logits) + static_cast<size_t>(b) * K * a.V * es;
+    const bool session = a.seeds != nullptr;
+    const unsigned long long seed = session ? a.seeds[b] : 0ull;
+    const uint32_t uctr = session ? a.counters[2 * b] : 0u, sctr = session ? a.counters[2 * b + 1] : 0u;
+    // every accept test's inputs at once (thread r: test r), then the walk in order
+    if (threadIdx.x < K) {
+        const int r = threadIdx.x;
+        const RowStats rp = st[r], rq = st[a.T + r];
+        const int x = a.drafts[static_cast<size_t>(b) * K + r];
+        sh.tu[r] = session ? session_u01(seed, uctr + static_cast<uint32_t>(r), TAG_ACCEPT)
+                           : a.u_accept[static_cast<size_t>(b) * K + r];
+        sh.tcode[r] = rp.bad || rq.bad ? 1 : (x < 0 || x >= a.V ? 2 : 0);
+        if (sh.tcode[r] == 0) {
+            sh.tp[r] = prob32(rp, load_x(P + static_cast<size_t>(r) * a.V * es, a.bf16, x), a.temperature);
+            sh.tq[r] = prob32(rq, load_x(Q + static_cast<size_t>(r) * a.V * es, a.bf16, x), a.temperature);
+        }
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-        const bool session = a.seeds != nullptr;
-        const unsigned long long seed = session ? a.seeds[b] : 0ull;
-        const uint32_t uctr = session ? a.counters[2 * b] : 0u, sctr = session ? a.counters[2 * b + 1] : 0u;
         int j = 0, bad = 0;
         for (; j < K; ++j) {
-            const RowStats rp = st[j], rq = st[a.T + j];
-            if (rp.bad || rq.bad) {
+            if (sh.tcode[j] == 1) {
                 bad = 1;
                 break;
             }
-            const float u = session ? session_u01(seed, uctr + static_cast<uint32_t>(j), TAG_ACCEPT)
-                                    : a.u_accept[static_cast<size_t>(b) * K + j];
-            const int x = a.drafts[static_cast<size_t>(b) * K + j];
-            if (x < 0 || x >= a.V)  // a draft id outside the vocabulary is rejected
+            if (sh.tcode[j] == 2)  // a draft id outside the vocabulary is rejected
                 break;
-            const float p = prob32(rp, load_x(P + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
-            const float q = prob32(rq, load_x(Q + static_cast<size_t>(j) * a.V * es, a.bf16, x), a.temperature);
-            if (!(static_cast<double>(u) * static_cast<double>(q) < static_cast<double>(p)))
+            if (!(static_cast<double>(sh.tu[j]) * static_cast<double>(sh.tq[j]) < static_cast<double>(sh.tp[j])))
                 break;
         }
         if (!bad && j == K && st[K].bad)

@@ -6,10 +6,10 @@ allocate or free because those calls can synchronise the device.  For them the
 library keeps the accept's partial results in a fixed array of its own.
 
 These tests call it through the C ABI (ctypes on libkda_spec.so) and compare it
-with spec_accept given caller scratch, on two calls in a row with different
-inputs, so a stale array from the first call cannot hide behind the second.  The
-file sorts last so that a run stopping at the first failure has run everything
-else first; it also passes alone in a fresh process.
+with spec_accept and with the CPU oracle on the same inputs, on two calls in a row
+with different inputs, so a stale array from the first call cannot hide behind the
+second.  The file sorts last so that a run stopping at the first failure has run
+everything else first; it also passes alone in a fresh process.
 """
 import ctypes
 
@@ -45,7 +45,7 @@ def test_noalloc_rejects_oversized_problem_before_any_launch():
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_caller_scratch_twice_in_a_row():
+def test_noalloc_matches_spec_accept_and_oracle_twice_in_a_row(orc):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     L, fn = _noalloc_fn()
@@ -61,7 +61,7 @@ def test_noalloc_matches_caller_scratch_twice_in_a_row():
         logits = torch.from_numpy(lg)
         logits = (logits.view(torch.bfloat16) if w.bf16 else logits).cuda()
         drafts = torch.from_numpy(d).cuda()
-        # existing entry point, caller scratch
+        # the existing entry point
         st_ref = torch.zeros(1, dtype=torch.int32, device="cuda")
         j_ref, b_ref, k_ref = kb.spec_accept(logits, drafts, dev_status=st_ref)
         # no-allocation entry point
@@ -75,3 +75,12 @@ def test_noalloc_matches_caller_scratch_twice_in_a_row():
         assert int(st[0]) == int(st_ref[0])
         if w.name == "na1":
             assert [int(x) for x in out[0].cpu()] == [int(x) for x in jt]
+        # the oracle on the same rows: j and bonus per session, a NaN row reached gives
+        # bonus -1 and the device status bit
+        got = out.cpu().numpy()
+        nan_seen = False
+        for b in range(w.B):
+            jr, br, _, rc = orc.accept(lg[b], d[b])
+            assert (int(got[0, b]), int(got[1, b]), int(got[2, b])) == (jr, br, jr + 1), (w.name, b)
+            nan_seen |= rc == 2
+        assert bool(int(st[0]) & kb.ST_NAN) == nan_seen
