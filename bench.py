@@ -39,14 +39,15 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 # DRAM bytes read + written by one deferred-round launch of kda_scan_kernel, from one
 # ncu capture per workload (dram__bytes_read.sum + dram__bytes_write.sum), with the
-# kernel's own byte count (deferred_bytes) of the captured launch, so the figure can
-# be scaled to a run's mean launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
+# kernel's own byte count (deferred_bytes with the update vectors stored and read back,
+# the default) of the captured launch, so the figure can be scaled to a run's mean
+# launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
 # only: comments and blank space removed) the captures were taken on; with any other
 # source the traffic is reported as null.
-TRAFFIC_SOURCE = "3d4f03dcb519c16059bdfa8aa76e82e3a2e3220f19b3286718812a795e365ad2"
-TRAFFIC_BYTES = {"stack34": (201_875_456 + 257_812_992, 504_740_608),
-                 "batched32": (204_221_440 + 233_559_808, 478_401_792),
-                 "stress64x34": (13_474_439_936 + 17_652_109_824, 30_453_346_304)}
+TRAFFIC_SOURCE = "da11fbe1982f7bca29f1da6bfd6c4d96c8d5f881e2429befa19cd69a3d4f6f99"
+TRAFFIC_BYTES = {"stack34": (205_136_128 + 266_748_416, 516_995_840),
+                 "batched32": (213_746_176 + 258_133_248, 512_188_800),
+                 "stress64x34": (13_892_460_288 + 18_721_622_016, 31_932_887_040)}
 SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
 
 
@@ -92,31 +93,37 @@ WORKLOAD_TEXT = {
 # ---------------------------------------------------------------------------
 # byte accounting (algorithmic bytes: every tensor element moved once)
 # ---------------------------------------------------------------------------
-def verify_bytes(w, snapshot_copy: bool = False) -> int:
+def verify_bytes(w, snapshot_copy: bool = False, stored_w: bool = False) -> int:
     """One verify launch.  Ping-pong (the default): S read + S write, ring read + write.
-    snapshot_copy: the in-place verify that also writes the snapshot of S and ring."""
+    snapshot_copy: the in-place verify that also writes the snapshot of S and ring.
+    stored_w: the verify also writes each row's update vector (f32, 512 B a head)."""
     es = 2 if w.bf16 else 4
     D = 128
     n = 3 if snapshot_copy else 2
     per_head = n * D * D * 4 + n * 9 * D * 4
     rows = w.T * w.H * (4 * D + 1) * es
     out = w.T * w.H * D * 4
-    return w.L * w.B * (w.H * per_head + rows + out) + w.L * w.H * 3 * D * 4 * 4
+    wv = w.T * w.H * D * 4 if stored_w else 0
+    return w.L * w.B * (w.H * per_head + rows + out + wv) + w.L * w.H * 3 * D * 4 * 4
 
 
-def deferred_bytes(w, prev_keeps) -> int:
+def deferred_bytes(w, prev_keeps, stored_w: bool = False) -> int:
     """One kda_verify_scan_deferred launch: per session that rolls back (keep < T) the
     state is read, written as the snapshot and written again, the ring likewise, and
     the replayed rows are read besides this round's; a session that kept every row
-    reads and writes its state and ring once."""
+    reads and writes its state and ring once.  stored_w: the launch also writes this
+    round's update vectors and reads the replayed rows' (f32, 512 B a head and row)."""
     es = 2 if w.bf16 else 4
     D = 128
     row = w.H * (4 * D + 1) * es
+    wrow = w.H * D * 4 if stored_w else 0
     n = 0
     for k in prev_keeps:
         pending = k < w.T
         m = 3 if pending else 2
-        n += w.L * (w.H * m * (D * D * 4 + 9 * D * 4) + (k if pending else 0) * row + w.T * row + w.T * w.H * D * 4)
+        kr = k if pending else 0
+        n += w.L * (w.H * m * (D * D * 4 + 9 * D * 4) + kr * (row + wrow) + w.T * (row + wrow) +
+                    w.T * w.H * D * 4)
     return n + w.L * w.H * 3 * D * 4 * 4
 
 
@@ -154,14 +161,14 @@ def rollback_bytes(w, keeps) -> int:
     return n
 
 
-def verify_bytes_var(w, t_rows) -> int:
+def verify_bytes_var(w, t_rows, stored_w: bool = False) -> int:
     """verify_bytes (in place, snapshot copied) with session b running t_rows[b] rows."""
     es = 2 if w.bf16 else 4
     D = 128
     per_head = 3 * D * D * 4 + 3 * 9 * D * 4
     n = 0
     for t in t_rows:
-        n += w.L * (w.H * per_head + t * w.H * (4 * D + 1) * es + t * w.H * D * 4)
+        n += w.L * (w.H * per_head + t * w.H * (4 * D + 1) * es + t * w.H * D * 4 * (2 if stored_w else 1))
     return n + w.L * w.H * 3 * D * 4 * 4
 
 
@@ -386,7 +393,7 @@ def oracle_baseline_threads(w, budget_s: float, threads: int):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc):
+def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc, use_w=False):
     """The deferred round end to end from pinned host buffers through the public API.
 
     A round's inputs sit in one pinned host block (logits, drafts, then each raw-row
@@ -439,6 +446,9 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     # two device blocks: a deferred round reads the previous round's raw rows
     dev_blocks = [torch.empty(block_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
     dev_views = [views(b) for b in dev_blocks]
+    # the update vectors stay on the device (two: a round's replay reads the previous one's)
+    ewb = [torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev) if use_w else None
+           for _ in range(2)]
     res_dev = torch.empty((3, w.B), dtype=torch.int32, device=dev)  # j, bonus, keep
     host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for _, t in parts)
@@ -455,7 +465,10 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
 
     def plan(b, cls, **kw):
         v = dev_views[b]
-        return cls(pp, {n: v[n] for n in names}, out, v["logits"], v["drafts"], res_dev[0], res_dev[1], res_dev[2],
+        rw = {n: v[n] for n in names}
+        if ewb[b] is not None:
+            rw["w"] = ewb[b]
+        return cls(pp, rw, out, v["logits"], v["drafts"], res_dev[0], res_dev[1], res_dev[2],
                    status, scratch, stream, **kw)
 
     eplans = [plan(b, kb.DeferredRoundPlan, **({"ready_flags": flags, "pairs_per_flag": ppf} if staged else {}))
@@ -528,10 +541,21 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     dev = torch.device("cuda", local_rank)
     w = synth.WORKLOADS[wname]
     R = min(w.rounds, args.rounds) if args.rounds else w.rounds
+    # stored update vectors, for the deferred rounds only (a deferred round's replay
+    # reads the previous round's, so consecutive rounds need different w buffers and
+    # the cycle of rounds is even); the rounds with a separate rollback run without them
+    # (with them a separate verify measured ~3 % slower and the rollback ~8 %)
+    use_w = args.replay_w == "on" and R >= 2
+    if use_w and R % 2:
+        R -= 1
 
     st = kb.LayerState(synth_gpu.state(w, dev), synth_gpu.ring(w, dev), synth_gpu.conv_w(w, dev))
     stash = kb.Stash(st)
     rows = [synth_gpu.rows(w, r, dev) for r in range(R)]
+    plain = rows  # q, k, v, g, beta
+    if use_w:
+        wbufs = [torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev) for _ in range(2)]
+        rows = [dict(rows[r], w=wbufs[r % 2]) for r in range(R)]
     logits = [synth_gpu.logits(w, r, dev) for r in range(R)]
     drafts, jt = zip(*[synth_gpu.drafts(w, r, dev) for r in range(R)])
     out = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev)
@@ -545,10 +569,10 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     # the timed round: ping-pong state buffers (the resident state and the stash's
     # snapshot buffers swap roles every round; the verify reads one and writes the other)
     pp = kb.PingPong(st, spare_state=stash.state_snap, spare_ring=stash.ring_snap)
-    pplans = [kb.PingPongRoundPlan(pp, rows[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+    pplans = [kb.PingPongRoundPlan(pp, plain[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
                                    scratch, stream) for r in range(R)]
     # the in-place round (snapshot copied by the verify), reported beside it
-    plans = [kb.RoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+    plans = [kb.RoundPlan(st, plain[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
                           scratch, stream) for r in range(R)]
 
     def step(r, ev=None, plans_=None):
@@ -633,7 +657,7 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
 
     # the kept rows each timed round replays: the previous round's accept
     prev_keeps = [[j + 1 for j in jt[(args.warmup + i) % R]] for i in range(K)]
-    round_bytes = [deferred_bytes(w, k) for k in prev_keeps]
+    round_bytes = [deferred_bytes(w, k, stored_w=use_w) for k in prev_keeps]
     algo_bytes = [algorithmic_bytes(w, k) for k in prev_keeps]
     step_bytes = [rb + accept_bytes(w) for rb in round_bytes]
     round_avg_ms = sum(round_ms) / K
@@ -655,11 +679,12 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         "peak": peak,
         "peak_kind": peak_kind,
         "launches_per_step": 2,  # kda_scan_kernel (deferred round) and accept_cluster_kernel
+        "replay_w": use_w,
     }
     if not full:
         if not args.no_e2e:
             res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
-                                 args.e2e_chunks)
+                                 args.e2e_chunks, use_w)
         return res
 
     # the same rounds with the rollback as its own launch: ping-pong verify, accept,
@@ -721,7 +746,7 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     # launch gaps between the round's kernels shrink
     if not args.no_graph:
         side = torch.cuda.Stream(dev)
-        gp = [kb.PingPongRoundPlan(pp, rows[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
+        gp = [kb.PingPongRoundPlan(pp, plain[r], out, logits[r], drafts[r], j_out, bonus_out, keep_out, status,
                                    scratch, side) for r in range(R)]
         side.wait_stream(stream)
         with torch.cuda.stream(side):
@@ -754,9 +779,9 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     # launch) is reported beside it.
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
-                             args.e2e_chunks)
+                             args.e2e_chunks, use_w)
         if "staged_ranges" in res["e2e"]:
-            one = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, 1)
+            one = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, 1, use_w)
             res["e2e"]["one_copy"] = {"value": one["value"], "ms_per_step": one["ms_per_step"]}
 
     # per-layer issue: one kda_verify_scan per layer (as a model issues them), then accept
@@ -764,14 +789,14 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     if w.L > 1 and not args.no_per_layer:
         Kp = max(1, min(args.per_layer_steps, K))
         RP = min(R, 8)
-        lplans = [kb.LayerRoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out,
+        lplans = [kb.LayerRoundPlan(st, plain[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out,
                                     status, scratch, stream) for r in range(RP)]
         side = torch.cuda.Stream(dev)
-        gplans = [kb.LayerRoundPlan(st, rows[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out,
+        gplans = [kb.LayerRoundPlan(st, plain[r], out, stash, logits[r], drafts[r], j_out, bonus_out, keep_out,
                                     status, scratch, side) for r in range(RP)]
 
         def timed(fn):
-            for i in range(3):
+            for i in range(4):  # even: a deferred round's update vectors alternate with the round's parity
                 fn(i % RP)
             barrier()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -825,7 +850,7 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
 
         def col_step(i, ev):
             r = i % R
-            rr = rows[r]
+            rr = plain[r]
             ev[0].record(stream)
             kb.kda_verify_scan_cols(st, rr["q"], rr["k"], rr["v"], rr["g"], rr["beta"], cols, out=out, stream=stream)
             ev[1].record(stream)
@@ -921,7 +946,7 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         Kv = max(1, min(args.var_t_steps, K))
 
         def var_step(r, ev):
-            rr = rows[r]
+            rr = plain[r]
             ev[0].record(stream)
             kb.kda_verify_scan_var(st, rr["q"], rr["k"], rr["v"], rr["g"], rr["beta"], t_dev, out=out, stash=stash,
                                    dev_status=status, stream=stream)
@@ -981,6 +1006,8 @@ def workload_config(wname, args, step_bytes=None):
         l2 = "no flush: every step moves more bytes than the 129 MB L2"
     return {"workload": wname, "description": WORKLOAD_TEXT[wname], "L": w.L, "B": w.B, "H": w.H, "T": w.T,
             "V": w.V, "rows_dtype": "bf16" if w.bf16 else "f32", "state_dtype": "f32", "l2": l2,
+            "update_vectors": ("stored by each verify, read back by the replay" if args.replay_w == "on"
+                               else "formed again by the replay"),
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
@@ -991,12 +1018,15 @@ def roofline_of(wname, res, clocks) -> dict:
     peak = res["peak"]
     traffic = frac_dram = None
     same = code_hash(SCAN_SOURCE) == TRAFFIC_SOURCE
-    if wname in TRAFFIC_BYTES and same:
+    captured_form = res.get("replay_w", True)  # the captures ran the launch that stores update vectors
+    if wname in TRAFFIC_BYTES and same and captured_form:
         dram, own = TRAFFIC_BYTES[wname]
         traffic = dram * res["round_bytes_mean"] / own
         frac_dram = traffic / (res["round_kernel_ms"] * 1e-3) / 1e9 / peak
     if wname not in TRAFFIC_BYTES:
         tsrc = "no ncu capture of this workload's launch"
+    elif same and not captured_form:
+        tsrc = "null: the ncu captures ran the launch that stores the update vectors (--replay-w on)"
     elif same:
         tsrc = ("ncu capture of one launch (dram__bytes_read.sum + dram__bytes_write.sum) on this kernel "
                 "source, scaled to the run's mean kernel bytes per launch")
@@ -1032,6 +1062,8 @@ def main():
                          "'workloads'; empty for none")
     ap.add_argument("--rounds", type=int, default=0, help="distinct input rounds kept resident (0: all)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--replay-w", choices=["on", "off"], default="on",
+                    help="verifies store each row's update vector and replays read it back")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="ranges of (layer, session) pairs the e2e round's raw rows are copied in (the one "

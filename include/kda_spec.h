@@ -109,9 +109,25 @@ typedef struct kda_layer_state {
 } kda_layer_state;
 
 /* Raw (pre-conv, pre-activation) rows of one round, element type dims.dtype:
- *   q, k, v, g [L][B][T][H][128];  beta [L][B][T][H]. */
+ *   q, k, v, g [L][B][T][H][128];  beta [L][B][T][H].
+ * w (optional, NULL for none; zero-initialise the struct to leave it out): f32
+ *   [L][B][T][H][128], 16-byte aligned, written by the verify of these rows with the
+ *   update vector w_t = beta_t (v_t - S'^T k_t) of every row it runs.  A replay of
+ *   these rows (kda_rollback, or the first part of the next deferred round) then
+ *   reads w_t instead of forming S'^T k_t again: per row only S' = d S and
+ *   S = S' + k w^T remain, the same operations on the same operands, so the state it
+ *   leaves is bit-identical to a replay without w.  Like the raw rows, w is held by
+ *   pointer in the stash and must stay unchanged until the replay has run; the next
+ *   deferred round's rows need a different w buffer (two alternate).  The per-layer
+ *   column-stash path (kda_verify_scan_cols) and kda_upload_rows_staged ignore it.
+ *   Measured on GB300: a chain of deferred rounds runs 2-4 % faster with w (a
+ *   replayed row costs about half a verify row); a verify followed by a separate
+ *   kda_rollback runs slower with it (the verify ~3 %, the rollback 3-8 %: that
+ *   replay is bound by the state's memory traffic, not by its rows), so leave w NULL
+ *   for rounds committed by kda_rollback. */
 typedef struct kda_rows {
     const void *q, *k, *v, *g, *beta;
+    float *w;
 } kda_rows;
 
 /* Rollback material of one round (the KDA fields of the pages' verify

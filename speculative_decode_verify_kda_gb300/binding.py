@@ -35,7 +35,7 @@ EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollba
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_session", "kda_philox4x32_10",
            "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 6
+ABI_VERSION = 7
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -50,7 +50,7 @@ class KdaLayerState(ctypes.Structure):
 
 class KdaRows(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
-                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p)]
+                ("g", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("w", ctypes.c_void_p)]
 
 
 class KdaStashC(ctypes.Structure):
@@ -231,25 +231,32 @@ class Stash:
         return int(self.c.T)
 
 
-def _rows(st: LayerState, q, k, v, g, beta, T: int | None = None):
+def _rows(st: LayerState, q, k, v, g, beta, T: int | None = None, w: torch.Tensor | None = None):
+    """The kda_rows of one round; w (optional): f32 [L][B][T][H][128], the update vectors
+    the verify writes and a replay of these rows reads."""
     dt = q.dtype
     if T is None:
         T = int(q.shape[2])
     shp = (st.L, st.B, T, st.H, D)
     tensors = [_dev(q, "q", dt, shp), _dev(k, "k", dt, shp), _dev(v, "v", dt, shp),
                _dev(g, "g", dt, shp), _dev(beta, "beta", dt, shp[:4])]
-    return KdaRows(*(x.data_ptr() for x in tensors)), tensors, _row_dtype(q), T
+    wp = None
+    if w is not None:
+        tensors.append(_dev(w, "w", torch.float32, shp))
+        wp = w.data_ptr()
+    return KdaRows(*(x.data_ptr() for x in tensors[:5]), wp), tensors, _row_dtype(q), T
 
 
 def kda_verify_scan(st: LayerState, q, k, v, g, beta, out: torch.Tensor | None = None,
-                    stash: Stash | None = None, stream=None) -> Stash | None:
+                    stash: Stash | None = None, stream=None, w: torch.Tensor | None = None) -> Stash | None:
     """One verify round of T = q.shape[2] rows for every (layer, session, head).
 
     q, k, v, g: [L][B][T][H][128], beta [L][B][T][H] (float32 or bfloat16, raw rows);
     out: None or f32 [L][B][T][H][128].  state and conv_ring advance in place.
-    With a stash, its snapshots receive the pre-round state and ring.
+    With a stash, its snapshots receive the pre-round state and ring.  w: None or f32
+    [L][B][T][H][128], receives the rows' update vectors, which the rollback then reads.
     """
-    rows, tensors, dt, T = _rows(st, q, k, v, g, beta)
+    rows, tensors, dt, T = _rows(st, q, k, v, g, beta, w=w)
     if out is not None:
         _dev(out, "out", torch.float32, (st.L, st.B, T, st.H, D))
     dims, cst = st.dims(dt), st.c()
@@ -298,13 +305,14 @@ def _int_array(x, B: int, name: str):
 
 
 def kda_verify_scan_var(st: LayerState, q, k, v, g, beta, t_rows, out: torch.Tensor | None = None,
-                        stash: Stash | None = None, dev_status: torch.Tensor | None = None, stream=None):
+                        stash: Stash | None = None, dev_status: torch.Tensor | None = None, stream=None,
+                        w: torch.Tensor | None = None):
     """Verify round where session b runs t_rows[b] of the T = q.shape[2] rows.
 
     t_rows: host sequence of B ints or a device int32 tensor [B]; the other arguments
     as for kda_verify_scan.
     """
-    rows, tensors, dt, T = _rows(st, q, k, v, g, beta)
+    rows, tensors, dt, T = _rows(st, q, k, v, g, beta, w=w)
     if out is not None:
         _dev(out, "out", torch.float32, (st.L, st.B, T, st.H, D))
     tp, mem, hold = _int_array(t_rows, st.B, "t_rows")
@@ -374,14 +382,15 @@ class PingPong:
 
 
 def kda_verify_scan_pingpong(pp: PingPong, q, k, v, g, beta, out: torch.Tensor | None = None, t_rows=None,
-                             dev_status: torch.Tensor | None = None, stream=None) -> PingPong:
+                             dev_status: torch.Tensor | None = None, stream=None,
+                             w: torch.Tensor | None = None) -> PingPong:
     """One verify round from the committed buffer of ``pp`` into the other one.
 
     Arguments as for kda_verify_scan (t_rows: None, or per-session rows as for
     kda_verify_scan_var).  Afterwards the other buffer is committed.
     """
     shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
-    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
+    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta, w=w)
     if out is not None:
         _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
     tp, mem, hold = (None, MEM_HOST, None) if t_rows is None else _int_array(t_rows, pp.B, "t_rows")
@@ -397,17 +406,20 @@ def kda_verify_scan_pingpong(pp: PingPong, q, k, v, g, beta, out: torch.Tensor |
 
 
 def kda_verify_scan_deferred(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Tensor, out: torch.Tensor | None = None,
-                             dev_status: torch.Tensor | None = None, stream=None) -> PingPong:
+                             dev_status: torch.Tensor | None = None, stream=None,
+                             w: torch.Tensor | None = None) -> PingPong:
     """A ping-pong round that first commits the previous one: each session with
     prev_keep[b] < the previous T is replayed from the previous pre-round buffer (the
     rollback), then this round's rows run from the committed state.  prev_keep: device
     int32 [B] (the previous round's keep).  Afterwards, as after kda_verify_scan_pingpong,
     the round's snapshot is kept and the post-round buffer is the one to commit next.
+    w: None or f32 [L][B][T][H][128], this round's update vectors; the replay reads
+    the previous round's (when that round had them), so two w buffers alternate.
     """
     if pp.last is None:
         raise ValueError("a deferred round follows a ping-pong round (no previous round to commit)")
     shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
-    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
+    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta, w=w)
     if dt != pp.dtype:
         raise TypeError("the raw rows must have the previous round's element type")
     if out is not None:
@@ -431,7 +443,7 @@ def kda_verify_scan_deferred(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Te
 def kda_verify_scan_deferred_staged(pp: PingPong, q, k, v, g, beta, prev_keep: torch.Tensor,
                                     ready_flags: torch.Tensor, pairs_per_flag: int, epoch: int,
                                     out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
-                                    stream=None) -> PingPong:
+                                    stream=None, w: torch.Tensor | None = None) -> PingPong:
     """kda_verify_scan_deferred whose raw rows of (layer, session) pair lb = l B + b may
     be read once ready_flags[lb // pairs_per_flag] has reached epoch (see
     kda_upload_rows_staged, kda_stream_write_u32).  ready_flags: device int32 flags
@@ -440,7 +452,7 @@ def kda_verify_scan_deferred_staged(pp: PingPong, q, k, v, g, beta, prev_keep: t
         raise ValueError("a deferred round follows a ping-pong round (no previous round to commit)")
     _dev(ready_flags, "ready_flags", torch.int32, (staged_flag_count(pp.L, pp.B, pairs_per_flag),))
     shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
-    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta)
+    rows, tensors, dt, T = _rows(shape_ref, q, k, v, g, beta, w=w)
     if dt != pp.dtype:
         raise TypeError("the raw rows must have the previous round's element type")
     if out is not None:
@@ -702,14 +714,16 @@ class RoundPlan:
     Holds the ctypes argument tuples of kda_verify_scan, spec_accept and
     kda_rollback (device keep from spec_accept's keep_out) for fixed tensors, so
     each call is one foreign call with no per-call marshalling.  The tensors are
-    referenced and must keep their storage while the plan is used.
+    referenced and must keep their storage while the plan is used.  ``rows`` holds
+    q, k, v, g, beta and optionally w (the update vectors; see _rows), in which case
+    the verify writes them and the replay reads them.
     """
 
     def __init__(self, st: LayerState, rows: dict, out, stash: Stash, logits, drafts, j_out, bonus_out,
                  keep_out, dev_status, scratch, stream=None):
         L = lib()
         self._keep = (st, rows, out, stash, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch)
-        crows, tensors, dt, T = _rows(st, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
+        crows, tensors, dt, T = _rows(st, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"], w=rows.get("w"))
         B, Tl, V = (int(x) for x in logits.shape)
         if Tl != T or B != st.B:
             raise ValueError("logits must be [B][T][V] of the round")
@@ -781,7 +795,8 @@ class PingPongRoundPlan:
         self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch)
         self.pp = pp
         shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
-        crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
+        crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"],
+                                      w=rows.get("w"))
         B, Tl, V = (int(x) for x in logits.shape)
         if Tl != T or B != pp.B:
             raise ValueError("logits must be [B][T][V] of the round")
@@ -869,7 +884,8 @@ class DeferredRoundPlan:
         self._keep = (pp, rows, out, logits, drafts, j_out, bonus_out, keep_out, dev_status, scratch, ready_flags)
         self.pp = pp
         shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
-        crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"])
+        crows, tensors, dt, T = _rows(shape_ref, rows["q"], rows["k"], rows["v"], rows["g"], rows["beta"],
+                                      w=rows.get("w"))
         B, Tl, V = (int(x) for x in logits.shape)
         if Tl != T or B != pp.B:
             raise ValueError("logits must be [B][T][V] of the round")
@@ -1004,10 +1020,11 @@ def layer_pingpongs(pp: PingPong, bounds=None) -> list:
         lp.parity, lp.last, lp.dtype = pp.parity, pp.last, pp.dtype
         if pp.last is not None:
             full = pp.cstash[pp.last]
-            rows = {n: t[l0:l1] for n, t in zip(("q", "k", "v", "g", "beta"), pp.rows)} if pp.rows else None
+            rows = {n: t[l0:l1] for n, t in zip(("q", "k", "v", "g", "beta", "w"), pp.rows)} if pp.rows else None
             if rows is not None:
-                lp.rows = [rows[n] for n in ("q", "k", "v", "g", "beta")]
-                lp.cstash[pp.last].rows = KdaRows(*(rows[n].data_ptr() for n in ("q", "k", "v", "g", "beta")))
+                names = ("q", "k", "v", "g", "beta", "w") if "w" in rows else ("q", "k", "v", "g", "beta")
+                lp.rows = [rows[n] for n in names]
+                lp.cstash[pp.last].rows = KdaRows(*(rows[n].data_ptr() for n in names))
                 lp.cstash[pp.last].T = full.T
         out.append(lp)
     return out
@@ -1034,7 +1051,7 @@ class LayerRoundPlan:
             stl, stashl = st.layer(l), stash.layer(l)
             rl = {n: t[l:l + 1] for n, t in rows.items()}
             outl = None if out is None else out[l:l + 1]
-            crows, tensors, dt, T = _rows(stl, rl["q"], rl["k"], rl["v"], rl["g"], rl["beta"])
+            crows, tensors, dt, T = _rows(stl, rl["q"], rl["k"], rl["v"], rl["g"], rl["beta"], w=rl.get("w"))
             dims, cst = stl.dims(dt), stl.c()
             self._views.append((stl, stashl, rl, outl, crows, dims, cst, tensors))
             self.layers.append((ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(crows), T, _ptr(outl),

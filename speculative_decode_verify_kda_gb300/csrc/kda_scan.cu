@@ -129,6 +129,9 @@ struct ScanParams {
     const float *ring_in2; // DEFERRED: the ring of units with nothing to replay
     float *ring_snap_out;  // DEFERRED: receives the ring after the replay
     const void *xb_prev;   // DEFERRED: the previous round's raw beta [L][B][T_prev][H]
+    float *w_out;          // nullable: [L][B][T_rows][H][D], the update vector w_t of every verify row
+    const float *w_in;     // nullable: the update vectors of the rows a replay re-runs, [L][B][T_w][H][D]
+    int T_w;               // row count of w_in (the replayed round's T)
     float *s_cols;         // nullable: [L][B][H][T_rows][D][D], the state after each row
     float *ring_cols;      // with s_cols: [L][B][H][T_rows][3][3][D], the ring after each row
     const int *keep_dev;   // KEEP_DEVICE: [B]
@@ -356,6 +359,13 @@ __device__ __forceinline__ int unit_rows(const ScanParams &p, int b)
     }
     const int tb = p.rows_dev[b];  // ROWS_DEVICE
     return tb < 1 || tb > p.T_rows ? -1 : tb;
+}
+
+// Whether item `part` of a unit re-runs rows of an earlier verify (the replay of a
+// rollback, or a deferred round's first item), whose update vectors w_in may hold.
+__device__ __forceinline__ bool is_replay(const ScanParams &p, int part)
+{
+    return part == 0 || p.keep_mode == KEEP_HOST || p.keep_mode == KEEP_DEVICE;
 }
 
 // DEFERRED: the previous round's rows session b replays before its verify (0 when it
@@ -675,6 +685,28 @@ __device__ void conv_stream(const ScanParams &p, const Layout &lay, const unsign
     win[2] = r2;
 }
 
+// A replayed item whose verify stored its update vectors: the v warp copies w_t of
+// every row into the v slot of the scan-input row (natural order), which the replay
+// loop reads instead of forming u and w again.  Four rows' loads in flight at a time
+// (loading every row one item ahead held 60 more registers and measured slower).
+__device__ void copy_w_rows(const ScanParams &p, float *si, int u, int T, int lane)
+{
+    const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(u), p.divH)), h = u - lb * p.H;
+    const float4 *src = reinterpret_cast<const float4 *>(p.w_in + (static_cast<size_t>(lb) * p.T_w * p.H + h) * D) + lane;
+    const size_t step = static_cast<size_t>(p.H) * D / 4;
+    for (int t0 = 0; t0 < T; t0 += 4) {
+        float4 r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (t0 + j < T)
+                r[j] = src[(t0 + j) * step];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (t0 + j < T)
+                *reinterpret_cast<float4 *>(si + (t0 + j) * SI_ROW + SI_V + 4 * lane) = r[j];
+    }
+}
+
 // Stream 3: the forget gate d = exp(-5 sigmoid(raw_g)) per key channel and beta, four
 // rows at a time with no branch around the arithmetic.
 __device__ void gate_stream(const Layout &lay, const unsigned char *stg, float *si, float *sc, const Pre &pr, int T,
@@ -708,7 +740,7 @@ struct Stager {
     uint32_t par0, par1;  // and the phase parity that completes it
 };
 
-template <bool COLS>
+template <bool COLS, bool W>
 __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     const int pw = (threadIdx.x >> 5) - NSCAN, lane = threadIdx.x & 31;
@@ -758,11 +790,16 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
             // a replay ends in the committed ring (this round's ring snapshot)
             float *ring_dst = it.part == 0 ? p.ring_snap_out : p.ring_out;
             // an item without outputs never reads q-hat (the column stash still wants the
-            // ring after every row)
-            if (!COLS && pw == 0 && (it.part == 0 || !p.out))
+            // ring after every row); a replay with stored update vectors never reads v
+            const bool stored_w = W && p.w_in && is_replay(p, it.part);
+            if (!COLS && pw == 0 && (it.part == 0 || !p.out)) {
                 roll_window(p, lay, stg, win, it.u, T, pw, lane, ring_dst);
-            else
+            } else if (pw == 2 && stored_w) {
+                copy_w_rows(p, si, it.u, T, lane);
+                roll_window(p, lay, stg, win, it.u, T, pw, lane, ring_dst);
+            } else {
                 conv_stream<COLS>(p, lay, stg, si, pr.w, win, it.u, T, pw, lane, ring_dst);
+            }
         } else {
             gate_stream(lay, stg, si, sc, pr, T, lane);
         }
@@ -806,10 +843,10 @@ __device__ __forceinline__ void store_tile(float *So, int rg, const float2 (&S)[
 // The rows of one work item on the register tile S.  OUT: write the output rows to
 // orow (lanes with b2 = 1, column jsum); without outputs (replays) neither e = S'^T q
 // nor k.q is formed.  The state arithmetic, and so the state bits, do not depend on OUT.
-template <bool COLS, bool OUT>
+template <bool COLS, bool OUT, bool W>
 __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, const float *sc, float *orow,
-                                         float2 (&S)[16][2], int T, int u, int rg, int cg, int jbase, int jsum,
-                                         int b0, int b1, int b2)
+                                         float *wrow, float2 (&S)[16][2], int T, int u, int rg, int cg, int jbase,
+                                         int jsum, int b0, int b1, int b2)
 {
     // ---- the T-row gated delta rule ---------------------------------------------
     for (int t = 0; t < T; ++t) {
@@ -875,6 +912,9 @@ __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, c
         // u lanes: w = beta (v - u); e lanes: o = (e + w (k.q)) / sqrt(128)
         const float beta = sc[t];
         const float w = __fmul_rn(beta, __fsub_rn(vt[SI_V + jsum], sum));
+        // the u lanes (b2 = 0) hold w of column jsum: stored for a later replay
+        if (W && wrow && !b2)
+            wrow[static_cast<size_t>(t) * p.H * D] = w;
         const float w_of_col = __shfl_xor_sync(0xffffffffu, w, 16);
         // a warp's 16 e lanes store 16 consecutive columns of the output row
         if (OUT && b2)
@@ -896,7 +936,34 @@ __device__ __forceinline__ void run_rows(const ScanParams &p, const float *si, c
     }
 }
 
-template <bool COLS>
+// The rows of a replayed item whose update vectors the verify stored: per row
+// S' = d S, then S = S' + k w^T with w_t read from the scan-input row.  These are the
+// same two operations, on the same operands, that the verify applied to each element,
+// so the state bits equal those of a replay that forms u and w again.
+__device__ __forceinline__ void replay_rows_w(const float *si, float2 (&S)[16][2], int T, int rg, int jbase)
+{
+    for (int t = 0; t < T; ++t) {
+        const float *vt = si + t * SI_ROW;
+        const float *gp = vt + rg * GRP;
+        const float4 w4 = *reinterpret_cast<const float4 *>(vt + SI_V + jbase);
+        const float2 w01 = make_float2(w4.x, w4.y), w23 = make_float2(w4.z, w4.w);
+#pragma unroll
+        for (int rq = 0; rq < 4; ++rq) {
+            const float4 d4 = *reinterpret_cast<const float4 *>(gp + 4 * rq);
+            const float4 k4 = *reinterpret_cast<const float4 *>(gp + 16 + 4 * rq);
+            const float dv[4] = {d4.x, d4.y, d4.z, d4.w}, kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const int r = 4 * rq + m;
+                const float2 dd = make_float2(dv[m], dv[m]), kk = make_float2(kv[m], kv[m]);
+                S[r][0] = __ffma2_rn(kk, w01, __fmul2_rn(S[r][0], dd));
+                S[r][1] = __ffma2_rn(kk, w23, __fmul2_rn(S[r][1], dd));
+            }
+        }
+    }
+}
+
+template <bool COLS, bool W>
 __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     // lane 4 rg + cg of warp wi holds key rows i = rg + 8 r (r < 16) of value columns
@@ -980,15 +1047,21 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
             }
             const float *si = reinterpret_cast<const float *>(sm + lay.si(ib));
             const float *sc = reinterpret_cast<const float *>(sm + lay.sc(ib));
-            // the output row t of this unit: lanes with b2 = 1 store column jsum
+            // the output row t of this unit: lanes with b2 = 1 store column jsum; the
+            // update vectors of a verify item go to w_out (lanes with b2 = 0)
             float *orow = p.out && part == 1
                               ? p.out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum
                               : nullptr;
+            float *wrow = W && p.w_out && !is_replay(p, part)
+                              ? p.w_out + (static_cast<size_t>(x.lb) * p.T_rows * p.H + x.h) * D + jsum
+                              : nullptr;
 
-            if (orow)
-                run_rows<COLS, true>(p, si, sc, orow, S, T, u, rg, cg, jbase, jsum, b0, b1, b2);
+            if (W && p.w_in && is_replay(p, part))
+                replay_rows_w(si, S, T, rg, jbase);
+            else if (orow)
+                run_rows<COLS, true, W>(p, si, sc, orow, wrow, S, T, u, rg, cg, jbase, jsum, b0, b1, b2);
             else
-                run_rows<COLS, false>(p, si, sc, orow, S, T, u, rg, cg, jbase, jsum, b0, b1, b2);
+                run_rows<COLS, false, W>(p, si, sc, orow, wrow, S, T, u, rg, cg, jbase, jsum, b0, b1, b2);
             mbar_arrive(c.bar(B_SI_EMPTY + ib));  // the scan inputs of item i are consumed
             if (part == 0)  // the committed state: this round's snapshot
                 store_tile(p.s_snap_out + static_cast<size_t>(u) * D * D + jbase, rg, S);
@@ -1031,10 +1104,12 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
 
 // One persistent CTA per SM; warps 0..7 scan (warp 0 also loads the states), 8..11 run
 // the prologue (warp 11 also stages the raw rows).
-// COLS: also write the column stash (the state and ring after every row).  Verify and
-// rollback share one instantiation: alternating between two kernels of this size cost
-// the verify 5 % (its code is fetched again after each switch).
-template <bool COLS>
+// COLS: also write the column stash (the state and ring after every row).  W: the
+// verify stores each row's update vector (w_out) and a replay reads them (w_in); an
+// instantiation of its own, so the loop without them carries none of their code.
+// Verify and rollback share one instantiation: alternating between two kernels of this
+// size cost the verify 5 % (its code is fetched again after each switch).
+template <bool COLS, bool W>
 __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__ ScanParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -1079,9 +1154,9 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (wi < NSCAN)
-        scan_warp<COLS>(p, lay, sm, c, n);
+        scan_warp<COLS, W>(p, lay, sm, c, n);
     else
-        prologue_warp<COLS>(p, lay, sm, c, n);
+        prologue_warp<COLS, W>(p, lay, sm, c, n);
 }
 
 // ---- host side ----------------------------------------------------------------------
@@ -1238,8 +1313,9 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
             if (static_cast<size_t>(optin) < most)
                 return fail(KDA_ECUDA,
                             "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
-            const void *kernels[2] = {reinterpret_cast<const void *>(kda_scan_kernel<false>),
-                                      reinterpret_cast<const void *>(kda_scan_kernel<true>)};
+            const void *kernels[3] = {reinterpret_cast<const void *>(kda_scan_kernel<false, false>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<false, true>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<true, false>)};
             for (const void *k : kernels)
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
@@ -1291,8 +1367,10 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t le = p.s_cols ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<true>, p)
-                                    : cudaLaunchKernelEx(&cfg, kda_scan_kernel<false>, p);
+    // the column stash never carries update vectors (its rollback copies columns)
+    const cudaError_t le = p.s_cols                ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<true, false>, p)
+                           : (p.w_in || p.w_out) ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, true>, p)
+                                                 : cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, false>, p);
     if (le != cudaSuccess)
         return fail(KDA_ECUDA, std::string("kda_scan_kernel launch: ") + cudaGetErrorString(le));
     return check_launch("kda_scan_kernel");
@@ -1326,6 +1404,8 @@ int check_rows(const kda_rows *rows, int dtype)
     const uintptr_t bal = dtype == KDA_BF16 ? 1u : 3u;
     if (reinterpret_cast<uintptr_t>(rows->beta) & bal)
         return fail(KDA_EINVAL, "beta is not aligned to its element type");
+    if (rows->w && !aligned16(rows->w))
+        return fail(KDA_EINVAL, "rows->w (the update vectors) must be 16-byte aligned");
     return KDA_OK;
 }
 
@@ -1399,6 +1479,7 @@ int verify_common(const kda_dims *dims, const kda_layer_state *st, const kda_row
     p.ring_snap = stash && !pingpong ? stash->ring_snap : nullptr;
     p.conv_w = st->conv_w;
     p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
+    p.w_out = rows->w;
     p.out = out;
     p.status = dev_status;
     p.L = dims->L; p.B = dims->B; p.H = dims->H;
@@ -1486,6 +1567,11 @@ int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
         p.conv_w = st->conv_w;
         p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
         p.xb_prev = stash->rows.beta;
+        p.w_out = rows->w;
+        p.w_in = stash->rows.w;
+        p.T_w = stash->T;
+        if (p.w_out && p.w_out == p.w_in)
+            return fail(KDA_EINVAL, "rows->w must not be the previous round's update vectors (stash->rows.w)");
         p.out = out;
         p.status = dev_status;
         p.L = dims->L; p.B = dims->B; p.H = dims->H;
@@ -1699,6 +1785,8 @@ int rollback_common(const kda_dims *dims, const kda_layer_state *st, const kda_s
     p.conv_w = st->conv_w;
     p.xq = stash->rows.q; p.xk = stash->rows.k; p.xv = stash->rows.v;
     p.xg = stash->rows.g; p.xb = stash->rows.beta;
+    p.w_in = stash->rows.w;
+    p.T_w = stash->T;
     p.out = nullptr;
     p.status = dev_status;
     p.L = dims->L; p.B = dims->B; p.H = dims->H;

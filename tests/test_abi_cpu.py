@@ -43,7 +43,7 @@ def _state(H=64, B=1, L_=1, dtype=kb.BF16, dk=128):
 
 
 @pytest.mark.parametrize("case", ["T0", "T16", "dk64", "dtype", "null_state", "null_rows", "misaligned",
-                                  "snap_alias", "snap_null", "negB"])
+                                  "w_misaligned", "snap_alias", "snap_null", "negB"])
 def test_verify_rejects_on_host(L, case):
     dims, st, rows = _state()
     T, stash = 8, None
@@ -61,6 +61,8 @@ def test_verify_rejects_on_host(L, case):
         rows.v = None
     elif case == "misaligned":
         rows.q = FAKE + 2
+    elif case == "w_misaligned":  # the update vectors are read as 16-byte vectors
+        rows.w = FAKE + 4
     elif case == "snap_alias":
         stash = kb.KdaStashC(FAKE, FAKE + 0x100, kb.KdaRows(), 0)
     elif case == "snap_null":
@@ -275,6 +277,17 @@ def test_deferred_rejects_on_host(L):
     assert call(prev, T=16) == kb.EINVAL
     assert call(kb.KdaStashC(FAKE, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)) == kb.EINVAL
     assert call(kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(), 8)) == kb.EINVAL  # no previous rows
+    # the update vectors: this round's must not overwrite the previous round's, which
+    # the replay reads, and both are 16-byte aligned
+    rows.w = FAKE + 0x4000
+    assert call(kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 0x4000),
+                             8)) == kb.EINVAL
+    assert b"previous round" in L.kda_last_error()
+    assert call(kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 0x4008),
+                             8)) == kb.EINVAL
+    rows.w = FAKE + 0x4004
+    assert call(prev) == kb.EINVAL
+    rows.w = None
     # an empty problem only exchanges the buffers and records the round
     empty = kb.KdaDims(0, 2, 64, 128, 128, kb.BF16)
     st2 = kb.KdaLayerState(FAKE, FAKE + 0x100, FAKE + 0x200)
