@@ -394,16 +394,17 @@ def oracle_baseline_threads(w, budget_s: float, threads: int):
 # the GPU arm
 # ---------------------------------------------------------------------------
 def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc, use_w=False):
-    """The deferred round end to end from pinned host buffers through the public API.
+    """The deferred round end to end from pinned host buffers through the public API:
+    one kda_round_host call a round (binding.HostRounds).
 
     A round's inputs sit in one pinned host block (logits, drafts, then each raw-row
-    tensor whole).  nc == 1: one copy of the block, then the deferred round launch.
-    nc > 1: the launch (kda_verify_scan_deferred_staged) goes first; on a copy stream the
-    raw rows of nc consecutive ranges of (layer, session) pairs are copied, each range
-    followed by a stream write of its ready flag, so the scan of the pairs in place
-    overlaps the copy of the rest; then the logits and drafts, one accept, and j and the
-    bonus come back in one copy.  The next round's copies start after the host has read this round's j (a
-    round's inputs follow from the previous accept).  Leaves pp committed."""
+    tensor whole).  Each call copies the raw rows by nc consecutive ranges of (layer,
+    session) pairs on a copy stream, each range followed by a stream write of its ready
+    flag, then the logits and drafts; the deferred round launch scans each range once
+    its flag is set, so the copy of the rest overlaps the scan; then the accept, and j and
+    the bonus come back in one copy.  The call returns once the host has j (a round's
+    inputs follow from the previous accept).  nc == 1: one range, i.e. the whole block
+    before the scan.  Leaves pp committed."""
     import time
 
     import torch
@@ -425,7 +426,7 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     HR = min(R, 4 if block_bytes < (1 << 30) else 2)  # pinned host rounds cycled
     pairs = w.L * w.B  # (layer, session) pairs, the unit of a staged range
     ppf = -(-pairs // max(1, min(nc, pairs)))  # pairs a flag covers
-    ranges = [(p0, min(pairs, p0 + ppf)) for p0 in range(0, pairs, ppf)]
+    nranges = -(-pairs // ppf)
 
     def views(buf):
         out_ = {}
@@ -434,98 +435,52 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
             out_[n] = buf[offs[n]:offs[n] + nb].view(t.dtype).view(t.shape)
         return out_
 
-    host_blocks, host_views = [], []
+    host_views = []
     for r in range(HR):
         hb = torch.empty(block_bytes, dtype=torch.uint8).pin_memory()
         hv = views(hb)
         src = dict(rows[r], logits=logits[r], drafts=drafts[r])
         for n, _ in parts:
             hv[n].copy_(src[n].cpu())
-        host_blocks.append(hb)
         host_views.append(hv)
-    # two device blocks: a deferred round reads the previous round's raw rows
-    dev_blocks = [torch.empty(block_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
-    dev_views = [views(b) for b in dev_blocks]
-    # the update vectors stay on the device (two: a round's replay reads the previous one's)
-    ewb = [torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev) if use_w else None
-           for _ in range(2)]
-    res_dev = torch.empty((3, w.B), dtype=torch.int32, device=dev)  # j, bonus, keep
-    host_res = torch.empty((2, w.B), dtype=torch.int32).pin_memory()
+    # two device blocks: a deferred round reads the previous round's raw rows (and the
+    # update vectors, two buffers, stay on the device)
+    dev_sets = []
+    for _ in range(2):
+        v = views(torch.empty(block_bytes, dtype=torch.uint8, device=dev))
+        if use_w:
+            v["w"] = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev)
+        dev_sets.append(v)
     h2d = sum(t.numel() * t.element_size() for _, t in parts)
-    d2h = host_res.numel() * 4
+    d2h = 2 * w.B * 4  # j and the bonus
     Ke = max(1, min(args.e2e_steps, args.steps))
     copy_stream = torch.cuda.Stream(dev)
-    copied = torch.cuda.Event()
-    flags = torch.zeros(len(ranges), dtype=torch.int32, device=dev)
-    staged = len(ranges) > 1
-    # kda_upload_rows_staged of host block r into device block b (one library call: the
-    # copies of each range of pairs, each followed by its flag)
-    uploads = {(r, b): kb.StagedUpload({n: dev_views[b][n] for n in names}, {n: host_views[r][n] for n in names},
-                                       flags, ppf) for r in range(HR) for b in range(2)}
-
-    def plan(b, cls, **kw):
-        v = dev_views[b]
-        rw = {n: v[n] for n in names}
-        if ewb[b] is not None:
-            rw["w"] = ewb[b]
-        return cls(pp, rw, out, v["logits"], v["drafts"], res_dev[0], res_dev[1], res_dev[2],
-                   status, scratch, stream, **kw)
-
-    eplans = [plan(b, kb.DeferredRoundPlan, **({"ready_flags": flags, "pairs_per_flag": ppf} if staged else {}))
-              for b in range(2)]
-    eopen = plan(1, kb.PingPongRoundPlan)
-    epoch = [0]
-
-    def load_all(i):  # the whole block in one copy, on the launch stream
-        dev_blocks[i % 2].copy_(host_blocks[i % HR], non_blocking=True)
-
-    def load_staged(i):  # the rows by range with their flags, then the logits and drafts
-        b, r = i % 2, i % HR
-        uploads[(r, b)](epoch[0], copy_stream)
-        with torch.cuda.stream(copy_stream):
-            a0, a1 = offs["logits"], offs["q"]
-            dev_blocks[b][a0:a1].copy_(host_blocks[r][a0:a1], non_blocking=True)
-            copied.record(copy_stream)
-
-    def step(i):
-        rp = eplans[i % 2]
-        p = pp.last
-        if staged:
-            epoch[0] += 1
-            rp.verify(p, epoch[0])  # waits on the device for each range's flag
-            load_staged(i)
-            stream.wait_event(copied)  # the accept reads the logits
-        else:
-            load_all(i)
-            rp.verify(p)
-        rp.accept()
-        rp._flip(p)
-        host_res.copy_(res_dev[:2], non_blocking=True)
-        stream.synchronize()  # the host needs j and the bonus before the next round
-
-    # open the chain with a ping-pong round on device block 1, then deferred rounds
-    load_all(1)
-    par = pp.parity
-    eopen.verify(par)
-    eopen.accept()
-    eopen._flip(par)
-    for i in range(2, 5):
-        step(i)
+    p = pp.parity
+    hr = kb.HostRounds(kb.LayerState(pp.states[p], pp.rings[p], pp.conv_w), dev_sets, out=out,
+                       pairs_per_flag=ppf, dev_status=status, stream=stream, copy_stream=copy_stream,
+                       spare_state=pp.states[1 - p], spare_ring=pp.rings[1 - p])
+    # the chain opens with a ping-pong round, then deferred rounds
+    for i in range(4):
+        hr(host_views[i % HR])
     barrier()
     t0 = time.perf_counter()
-    for i in range(5, 5 + Ke):
-        step(i)
+    for i in range(4, 4 + Ke):
+        hr(host_views[i % HR])
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
     e2e_ms = slowest(e2e_ms, world, dev)
-    kb.kda_rollback_pingpong(pp, res_dev[2], dev_status=status, stream=stream)
+    hr.commit()
     torch.cuda.synchronize(dev)
     if int(status.item()):
         raise RuntimeError(f"device status {int(status.item()):#x} after the e2e steps")
+    # the committed state is in one of pp's two buffers
+    pp.parity = 0 if hr.state().data_ptr() == pp.states[0].data_ptr() else 1
+    pp.last = None
     res = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-           "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": Ke}
-    if staged:
-        res["staged_ranges"] = len(ranges)
+           "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": Ke,
+           "call": "kda_round_host (one call a round)"}
+    if nranges > 1:
+        res["staged_ranges"] = nranges
         res["pairs_per_range"] = ppf
     return res
 

@@ -279,6 +279,44 @@ int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_
                            unsigned *ready_flags, int pairs_per_flag, unsigned epoch, cudaStream_t stream);
 
 /*
+ * kda_round_host -- one speculative round end to end from host memory, in one call:
+ * glm_spec.rs, glm5_spec_round (a round is verify, accept and rollback, and the next
+ * round's drafts follow from this round's accept, so the host reads j every round).
+ *   host_rows, host_logits [B][T][V] (logit_dtype), host_drafts int32 [B][T-1]: the
+ *     round's inputs in host memory (pinned, for the copies to be asynchronous);
+ *   dev_rows, dev_logits, dev_drafts: device buffers of the same shapes they go to.
+ *     A deferred round replays the previous round's raw rows, so consecutive calls
+ *     need different dev_rows (two sets alternate), and different dev_rows.w when
+ *     the update vectors are kept;
+ *   dev_jbk: device int32 [3][B]: j, bonus and keep of this round; the keep row is also
+ *     the previous round's keep that this round's verify applies (same buffer every call);
+ *   host_jb: host int32 [2][B] (pinned) receiving j and the bonus;
+ *   ready_flags, pairs_per_flag, epoch: as for kda_verify_scan_deferred_staged (a new
+ *     epoch each call);
+ *   stream: the verify and the accept; copy_stream: the uploads (another stream);
+ *   wait != 0: return after the results are in host_jb (cudaStreamSynchronize(stream)).
+ * First call of a chain (stash->T == 0): the committed state and ring are in
+ * stash->state_snap / ring_snap, st's buffers are the spare pair; the rows, logits and
+ * drafts go up on `stream`, then kda_verify_scan_pingpong, spec_accept and the copy of
+ * j and the bonus.  Later calls: kda_verify_scan_deferred_staged on `stream` (the
+ * previous round's accept folded in; it scans a range once its flag is set, so only
+ * the first range's copy precedes the scan), then on copy_stream kda_upload_rows_staged
+ * of the rows by range and the logits and drafts, spec_accept once those have landed,
+ * then the results.  A copy refused after the launch leaves the launch waiting for its
+ * flag until the one-second bound (KDA_ST_TIMEOUT in *dev_status).  On return st and stash describe this round as those entry points leave
+ * them (the last round of a chain is committed with kda_rollback and the keep row of
+ * dev_jbk).  The results are bit-identical to issuing those calls one by one.
+ * Allocates no memory (one CUDA event is created and released per call).  KDA_EINVAL
+ * for NULL buffers, T outside 1..15, V < 1, a bad logit_dtype or copy_stream ==
+ * stream after the first call, and whatever the entry points it issues refuse.
+ */
+int kda_round_host(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, int T, const kda_rows *host_rows,
+                   const kda_rows *dev_rows, const void *host_logits, void *dev_logits, int logit_dtype, int V,
+                   const int *host_drafts, int *dev_drafts, int *dev_jbk, int *host_jb, float *out,
+                   unsigned *ready_flags, int pairs_per_flag, unsigned epoch, int *dev_status, cudaStream_t stream,
+                   cudaStream_t copy_stream, int wait);
+
+/*
  * Rounds whose length differs per session (variable T inside one batched grid).
  * glm_spec.rs, glm5_conf_keep and the p-min break of the draft chain, and dflash.rs,
  * DsparkVtPolicy / dspark_confidence_vt / dspark_slot_confidence_vt: each session

@@ -29,13 +29,13 @@ MEM_HOST, MEM_DEVICE = 0, 1
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_pingpong",
            "kda_verify_scan_deferred", "kda_verify_scan_deferred_staged", "kda_stream_write_u32",
-           "kda_upload_rows_staged",
+           "kda_upload_rows_staged", "kda_round_host",
            "kda_verify_scan_cols",
            "kda_rollback_cols", "spec_accept_var",
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_session", "kda_philox4x32_10",
            "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 7
+ABI_VERSION = 8
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -111,6 +111,10 @@ def lib(path: str | None = None):
     L.kda_upload_rows_staged.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaRows), ctypes.POINTER(KdaRows),
                                          ci, vp, ci, ctypes.c_uint, vp]
     L.kda_upload_rows_staged.restype = ci
+    L.kda_round_host.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState), ctypes.POINTER(KdaStashC),
+                                 ci, ctypes.POINTER(KdaRows), ctypes.POINTER(KdaRows), vp, vp, ci, ci, vp, vp, vp,
+                                 vp, vp, vp, ci, ctypes.c_uint, vp, vp, vp, ci]
+    L.kda_round_host.restype = ci
     L.kda_verify_scan_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                        ctypes.POINTER(KdaRows), ci, vp, vp, vp, vp]
     L.kda_verify_scan_cols.restype = ci
@@ -1094,3 +1098,111 @@ class LayerRoundPlan:
 
     def replay(self):
         self.graph.replay()
+
+
+class HostRounds:
+    """A chain of speculative rounds driven from host memory, one kda_round_host call a
+    round: the round's raw rows, logits and drafts go up from pinned host tensors, the
+    verify folds in the previous round's accept, the accept runs and j and the bonus
+    come back.
+
+    st: the committed state and ring (and conv weights); spare_state / spare_ring: the
+    second buffer pair (allocated here when None).  dev_sets: two dicts of device
+    tensors, each with q, k, v, g, beta (optionally w), logits [B][T][V] and drafts
+    int32 [B][T-1]; the rounds alternate between them.  The per-round host inputs are
+    dicts of pinned CPU tensors with the same keys (w excepted).  pairs_per_flag: the
+    (layer, session) pairs of a staged range (default: four ranges).  ``commit()`` applies
+    the last round's accept; ``state()`` / ``ring()`` are then the committed tensors.
+    """
+
+    def __init__(self, st: LayerState, dev_sets: list, out=None, ready_flags=None, pairs_per_flag: int | None = None,
+                 dev_status=None, stream=None, copy_stream=None, spare_state=None, spare_ring=None):
+        if len(dev_sets) != 2:
+            raise ValueError("two device input sets alternate")
+        self.L, self.B, self.H = st.L, st.B, st.H
+        spare_state = torch.empty_like(st.state) if spare_state is None else spare_state
+        spare_ring = torch.empty_like(st.conv_ring) if spare_ring is None else spare_ring
+        _dev(spare_state, "spare_state", torch.float32, tuple(st.state.shape))
+        _dev(spare_ring, "spare_ring", torch.float32, tuple(st.conv_ring.shape))
+        self._bufs = {st.state.data_ptr(): st.state, spare_state.data_ptr(): spare_state,
+                      st.conv_ring.data_ptr(): st.conv_ring, spare_ring.data_ptr(): spare_ring}
+        # the first round reads the committed pair from the stash's buffers
+        self.cst = KdaLayerState(spare_state.data_ptr(), spare_ring.data_ptr(), st.conv_w.data_ptr())
+        self.cstash = KdaStashC(st.state.data_ptr(), st.conv_ring.data_ptr(), KdaRows(), 0)
+        q0 = dev_sets[0]["q"]
+        self.T = int(q0.shape[2])
+        self.dt = _row_dtype(q0)
+        self.dims = KdaDims(self.L, self.B, self.H, D, D, self.dt)
+        self.sets, self.crows = [], []
+        for ds in dev_sets:
+            crows, tensors, _, T = _rows(st, ds["q"], ds["k"], ds["v"], ds["g"], ds["beta"], w=ds.get("w"))
+            lg, dr = ds["logits"], ds["drafts"]
+            _dev(lg, "logits")
+            if lg.dim() != 3 or int(lg.shape[0]) != self.B or int(lg.shape[1]) != self.T:
+                raise ValueError("logits must be [B][T][V] of the round")
+            _dev(dr, "drafts", torch.int32, (self.B, self.T - 1))
+            self.sets.append((crows, tensors, lg, dr))
+        self.V = int(dev_sets[0]["logits"].shape[2])
+        self.ldt = _row_dtype(dev_sets[0]["logits"])
+        self.jbk = torch.zeros((3, self.B), dtype=torch.int32, device=q0.device)
+        self.host_jb = torch.zeros((2, self.B), dtype=torch.int32).pin_memory()
+        if out is not None:
+            _dev(out, "out", torch.float32, (self.L, self.B, self.T, self.H, D))
+        pairs = self.L * self.B
+        if pairs_per_flag is None:  # four ranges (measured best of 1, 2, 4, 8 on stack34 and batched32)
+            pairs_per_flag = max(1, -(-pairs // 4))
+        if ready_flags is None:
+            ready_flags = torch.zeros(staged_flag_count(self.L, self.B, pairs_per_flag), dtype=torch.int32,
+                                   device=q0.device)
+        _dev(ready_flags, "ready_flags", torch.int32, (staged_flag_count(self.L, self.B, pairs_per_flag),))
+        self.out, self.flags, self.ppf, self.status = out, ready_flags, int(pairs_per_flag), dev_status
+        self.stream = stream
+        self.copy_stream = copy_stream if copy_stream is not None else torch.cuda.Stream(q0.device)
+        self._hold = (st, spare_state, spare_ring, dev_sets, ready_flags, dev_status, out, pairs)
+        self._host = {}
+        self.epoch = 0
+        self.rounds = 0
+        self._L = lib()
+
+    def _host_rows(self, hs: dict):
+        key = id(hs)
+        if key not in self._host:
+            names = ("q", "k", "v", "g", "beta")
+            for n in names + ("logits", "drafts"):
+                if hs[n].is_cuda or not hs[n].is_contiguous():
+                    raise ValueError(f"host input {n} must be a contiguous CPU tensor (pinned)")
+            self._host[key] = (KdaRows(*(hs[n].data_ptr() for n in names)), hs)
+        return self._host[key][0]
+
+    def __call__(self, hs: dict, wait: bool = True):
+        """One round from the host inputs hs; returns (j, bonus) as host int32 tensors
+        [B] (views of one pinned buffer, overwritten by the next round) when wait."""
+        crows, _, lg, dr = self.sets[self.rounds % 2]
+        hrows = self._host_rows(hs)
+        self.epoch = (self.epoch + 1) & 0xffffffff
+        rc = self._L.kda_round_host(ctypes.byref(self.dims), ctypes.byref(self.cst), ctypes.byref(self.cstash),
+                                    self.T, ctypes.byref(hrows), ctypes.byref(crows), hs["logits"].data_ptr(),
+                                    lg.data_ptr(), self.ldt, self.V, hs["drafts"].data_ptr(), dr.data_ptr(),
+                                    self.jbk.data_ptr(), self.host_jb.data_ptr(), _ptr(self.out),
+                                    self.flags.data_ptr(), self.ppf, ctypes.c_uint(self.epoch), _ptr(self.status),
+                                    ctypes.c_void_p(_stream(self.stream)),
+                                    ctypes.c_void_p(_stream(self.copy_stream)), 1 if wait else 0)
+        if rc:
+            _check("kda_round_host", rc)
+        self.rounds += 1
+        return (self.host_jb[0], self.host_jb[1]) if wait else None
+
+    def commit(self):
+        """Apply the last round's accept (kda_rollback with the device keep)."""
+        if self.rounds == 0:
+            return
+        rc = self._L.kda_rollback(ctypes.byref(self.dims), ctypes.byref(self.cst), ctypes.byref(self.cstash),
+                                  ctypes.c_void_p(self.jbk[2].data_ptr()), MEM_DEVICE, _ptr(self.status),
+                                  ctypes.c_void_p(_stream(self.stream)))
+        _check("kda_rollback", rc)
+
+    def state(self):
+        return self._bufs[self.cst.state]
+
+    def ring(self):
+        return self._bufs[self.cst.conv_ring]

@@ -24,7 +24,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
 LIBS = {
-    "libkda_spec.so": ["kda_scan.cu", "spec_accept.cu", "spec_sampled.cu", "kda_abi.cpp"],
+    "libkda_spec.so": ["kda_scan.cu", "spec_accept.cu", "spec_sampled.cu", "kda_round.cpp", "kda_abi.cpp"],
     "libkda_synth.so": ["synth_fill.cu"],
 }
 

@@ -333,3 +333,22 @@ def test_staged_deferred_and_flag_writer_reject_on_host(L):
     assert kb.staged_flag_count(3, 2, 4) == 2 and kb.staged_flag_count(3, 2, 1) == 6
     with pytest.raises(ValueError):
         kb.staged_flag_count(3, 2, 0)
+
+
+def test_round_host_rejects_on_host(L):
+    dims, st, rows = _state(B=2)
+    hrows = kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE)
+
+    def call(stash, T=8, V=1000, ldt=kb.BF16, jbk=FAKE + 0x5000, s1=None, s2=None, hl=FAKE):
+        return L.kda_round_host(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash) if stash else None, T,
+                                ctypes.byref(hrows), ctypes.byref(rows), hl, FAKE, ldt, V, FAKE, FAKE, jbk,
+                                FAKE + 0x6000, None, FAKE + 0x7000, 1, 1, None, s1, s2, 0)
+    prev = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)
+    assert call(None) == kb.EINVAL
+    assert call(prev, T=0) == kb.EINVAL and call(prev, T=16) == kb.EINVAL
+    assert call(prev, V=0) == kb.EINVAL and call(prev, ldt=5) == kb.EINVAL
+    assert call(prev, jbk=FAKE + 0x5002) == kb.EINVAL
+    assert call(prev, hl=None) == kb.EINVAL
+    # after the first round the copies need a stream of their own: the verify waits for them
+    assert call(prev, s1=None, s2=None) == kb.EINVAL
+    assert b"copy_stream" in L.kda_last_error()
