@@ -315,7 +315,7 @@ class OracleArm:
         self.cw = synth.layer_conv_w(w, l)
         self.rounds = []
         for r in range(min(n_rounds, w.rounds)):
-            d = synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V)[b]
+            d = synth.drafts_for(synth.logit_argmax(w, r, [b]), synth.accept_targets(w, r)[b:b + 1], w.V)[0]
             self.rounds.append((synth.unit_rows(w, r, l, b), synth.logits(w, r, sessions=[b])[0], d))
         self.r = 0
         self.h0 = 0
@@ -512,7 +512,7 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         wbufs = [torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev) for _ in range(2)]
         rows = [dict(rows[r], w=wbufs[r % 2]) for r in range(R)]
     logits = [synth_gpu.logits(w, r, dev) for r in range(R)]
-    drafts, jt = zip(*[synth_gpu.drafts(w, r, dev) for r in range(R)])
+    drafts, jt = zip(*[synth_gpu.drafts(w, r, dev, lg=logits[r]) for r in range(R)])
     out = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device=dev)
     j_out = torch.empty(w.B, dtype=torch.int32, device=dev)
     bonus_out = torch.empty_like(j_out)

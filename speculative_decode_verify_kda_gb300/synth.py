@@ -37,13 +37,12 @@ KEY_MUL = 0xD1B54A32D192ED03
 
 D = 128
 TAPS = 4
-PLANT_VALUE = 16.0  # planted maximum of a logits row; every other draw lies in [-6, 6]
 
 # stable tensor ids: keys must never change, stored fixtures depend on them
 TENSOR_IDS = {
     "state": 1, "ring": 2, "conv_w": 3,
     "q": 4, "k": 5, "v": 6, "g": 7, "beta": 8,
-    "logits": 9, "plant": 10, "accept": 11,
+    "logits": 9, "plant": 10, "accept": 11,  # "plant": no longer drawn, its id stays reserved
 }
 ROW_TENSORS = ("q", "k", "v", "g", "beta")
 
@@ -227,7 +226,7 @@ def all_conv_w(w: Workload) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
-# Accept-side inputs: logits with a planted row maximum and drafts built from it
+# Accept-side inputs: normal logits and drafts that follow the row argmax up to j
 # ---------------------------------------------------------------------------
 def accept_targets(w: Workload, round_idx: int) -> np.ndarray:
     """Target accepted-draft count j per session for one round."""
@@ -244,28 +243,34 @@ def accept_targets(w: Workload, round_idx: int) -> np.ndarray:
     raise ValueError(w.accept)
 
 
-def planted_argmax(w: Workload, round_idx: int) -> np.ndarray:
-    """The token id planted as the maximum of each logits row, [B][T]."""
-    return integers(tensor_key(w.seed, "plant", round_idx), 0, w.B * w.T, w.V).reshape(w.B, w.T)
-
-
-def drafts_for(plant: np.ndarray, j: np.ndarray, V: int) -> np.ndarray:
-    """Drafts [B][T-1]: the planted maximum before position j, a different id from j on."""
-    B, T = plant.shape
+def drafts_for(vam: np.ndarray, j: np.ndarray, V: int) -> np.ndarray:
+    """Drafts [B][T-1]: the row argmax (vam [B][T]) before position j, a different id from
+    j on, so that greedy acceptance accepts exactly j drafts."""
+    B, T = vam.shape
     r = np.arange(T - 1)[None, :]
-    hit = plant[:, : T - 1]
+    hit = vam[:, : T - 1]
     miss = (hit + 1) % V
     return np.where(r < np.asarray(j)[:, None], hit, miss).astype(np.int32)
 
 
 def logits(w: Workload, round_idx: int, sessions=None) -> np.ndarray:
-    """Logits [B][T][V]: normal-like draws with the planted maximum set to 16.0."""
+    """Logits [B][T][V]: normal draws (mean 0, variance 1), rounded to bf16 for bf16
+    workloads, so that at V = 32768 a row's maximum can tie."""
     sessions = range(w.B) if sessions is None else sessions
-    plant = planted_argmax(w, round_idx)
     key = tensor_key(w.seed, "logits", round_idx)
     rows = []
     for b in sessions:
         x = normal(key, b * w.T * w.V, w.T * w.V).reshape(w.T, w.V)
-        x[np.arange(w.T), plant[b]] = np.float32(PLANT_VALUE)
         rows.append(to_bf16_bits(x) if w.bf16 else x)
     return np.stack(rows)
+
+
+def logit_argmax(w: Workload, round_idx: int, sessions=None) -> np.ndarray:
+    """The argmax of each logits row, [B][T], the lowest index winning ties (bf16 rows
+    compared after exact widening): the token a draft must equal to be accepted."""
+    sessions = range(w.B) if sessions is None else sessions
+    out = []
+    for b in sessions:
+        x = logits(w, round_idx, [b])[0]
+        out.append((bf16_bits_to_f32(x) if w.bf16 else x).argmax(-1))
+    return np.stack(out).astype(np.int64)

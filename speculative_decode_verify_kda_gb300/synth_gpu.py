@@ -85,18 +85,28 @@ def conv_w(w: synth.Workload, device="cuda") -> torch.Tensor:
 
 
 def logits(w: synth.Workload, round_idx: int, device="cuda") -> torch.Tensor:
-    """Logits [B][T][V] with the planted row maximum (16.0) of synth.logits."""
+    """Logits [B][T][V] of synth.logits: normal draws, bf16 for bf16 workloads."""
     t = torch.empty((w.B, w.T, w.V), dtype=row_dtype(w), device=device)
-    fill_normal(t, synth.tensor_key(w.seed, "logits", round_idx))
-    plant = torch.as_tensor(synth.planted_argmax(w, round_idx), device=device)
-    b = torch.arange(w.B, device=device)[:, None].expand(w.B, w.T)
-    r = torch.arange(w.T, device=device)[None, :].expand(w.B, w.T)
-    t[b, r, plant] = synth.PLANT_VALUE
-    return t
+    return fill_normal(t, synth.tensor_key(w.seed, "logits", round_idx))
 
 
-def drafts(w: synth.Workload, round_idx: int, device="cuda") -> tuple[torch.Tensor, list]:
-    """Drafts int32 [B][T-1] that accept exactly the round's target j per session."""
+def logit_argmax(lg: torch.Tensor) -> torch.Tensor:
+    """The argmax of each row of lg [..][V], the lowest index winning ties (input
+    preparation: the value V - i of a maximal element i is unique, so their maximum
+    names the first maximal index)."""
+    V = int(lg.shape[-1])
+    m = lg.amax(-1, keepdim=True)
+    rev = torch.arange(V, 0, -1, device=lg.device, dtype=torch.int32)
+    return V - torch.where(lg == m, rev, torch.zeros_like(rev)).amax(-1).to(torch.int64)
+
+
+def drafts(w: synth.Workload, round_idx: int, device="cuda", lg: torch.Tensor | None = None
+           ) -> tuple[torch.Tensor, list]:
+    """Drafts int32 [B][T-1] that accept exactly the round's target j per session: the
+    argmax of the round's logits (lg, or drawn here) up to j, then a different token."""
     j = synth.accept_targets(w, round_idx)
-    d = synth.drafts_for(synth.planted_argmax(w, round_idx), j, w.V)
+    if lg is None:
+        lg = logits(w, round_idx, device)
+    vam = logit_argmax(lg).cpu().numpy()
+    d = synth.drafts_for(vam, j, w.V)
     return torch.as_tensor(d, device=device), [int(x) for x in j]

@@ -144,7 +144,7 @@ def test_deferred_plan_equals_the_functions():
     from gpu_util import to_dev
     rows = [rows_to_dev(synth.all_rows(w, r), True) for r in range(w.rounds)]
     logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
-    drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
+    drafts = [to_dev(synth.drafts_for(synth.logit_argmax(w, r), synth.accept_targets(w, r), w.V))
               for r in range(w.rounds)]
     j, bonus, keep = (torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(3))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -219,7 +219,7 @@ def test_per_layer_deferred_rounds_equal_one_launch(bounds):
     state0, ring0, cw = small_case(w)
     rows = [rows_to_dev(synth.all_rows(w, r), True) for r in range(w.rounds)]
     logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
-    drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
+    drafts = [to_dev(synth.drafts_for(synth.logit_argmax(w, r), synth.accept_targets(w, r), w.V))
               for r in range(w.rounds)]
 
     def case():
@@ -267,7 +267,7 @@ def test_staged_deferred_rounds_equal_deferred_rounds(ppf, upload):
     host_rows = [synth.all_rows(w, r) for r in range(w.rounds)]
     rows = [rows_to_dev(hr, True) for hr in host_rows]
     logits = [to_dev(synth.logits(w, r), True) for r in range(w.rounds)]
-    drafts = [to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V))
+    drafts = [to_dev(synth.drafts_for(synth.logit_argmax(w, r), synth.accept_targets(w, r), w.V))
               for r in range(w.rounds)]
     pairs = L * B
     bounds = [(p0, min(pairs, p0 + ppf)) for p0 in range(0, pairs, ppf)]  # flag f covers pairs f*ppf ..

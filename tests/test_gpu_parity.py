@@ -60,7 +60,7 @@ def test_tiny_every_accept_j(orc):
     for r in range(w.rounds):
         rows = synth.all_rows(w, r)
         lg = synth.logits(w, r)
-        d = synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V)
+        d = synth.drafts_for(synth.logit_argmax(w, r), synth.accept_targets(w, r), w.V)
         pre_state = st.state.clone()
         j, bonus, keep = _run_round(st, rows_to_dev(rows, False), to_dev(lg), to_dev(d), stash, out)
         torch.cuda.synchronize()
@@ -86,7 +86,7 @@ def test_layer64_rounds(orc):
         rows = synth.all_rows(w, r)
         lg = synth.logits(w, r)
         jt = synth.accept_targets(w, r)
-        d = synth.drafts_for(synth.planted_argmax(w, r), jt, w.V)
+        d = synth.drafts_for(synth.logit_argmax(w, r), jt, w.V)
         j, bonus, keep = _run_round(st, rows_to_dev(rows, True), to_dev(lg, True), to_dev(d), stash, out)
         torch.cuda.synchronize()
         jr, br, _, _ = orc.accept(lg[0], d[0])

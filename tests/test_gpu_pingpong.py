@@ -119,7 +119,7 @@ def _plan_case(w, plan_cls, stream=None):
     st = layer_state(state0, ring0, cw)
     rows, _ = _inputs(w, 0)
     lg = to_dev(synth.logits(w, 0), w.bf16)
-    d = to_dev(synth.drafts_for(synth.planted_argmax(w, 0), synth.accept_targets(w, 0), w.V))
+    d = to_dev(synth.drafts_for(synth.logit_argmax(w, 0), synth.accept_targets(w, 0), w.V))
     out = torch.empty((w.L, w.B, w.T, w.H, 128), dtype=torch.float32, device="cuda")
     j, bonus, keep = (torch.empty(w.B, dtype=torch.int32, device="cuda") for _ in range(3))
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -140,7 +140,7 @@ def _load(case, w, r):
     for n, x in rows.items():
         case["rows"][n].copy_(x)
     case["lg"].copy_(to_dev(synth.logits(w, r), w.bf16))
-    case["d"].copy_(to_dev(synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V)))
+    case["d"].copy_(to_dev(synth.drafts_for(synth.logit_argmax(w, r), synth.accept_targets(w, r), w.V)))
 
 
 def test_pingpong_plan_eager_and_graph_equal_round_plan():

@@ -41,7 +41,7 @@ def _host_round(w, r):
     lg = torch.from_numpy(np.ascontiguousarray(synth.logits(w, r)))
     h["logits"] = (lg.view(torch.bfloat16) if w.bf16 else lg).to(dt).pin_memory()
     j = synth.accept_targets(w, r)
-    h["drafts"] = torch.from_numpy(synth.drafts_for(synth.planted_argmax(w, r), j, w.V)).pin_memory()
+    h["drafts"] = torch.from_numpy(synth.drafts_for(synth.logit_argmax(w, r), j, w.V)).pin_memory()
     return h, [int(x) for x in j]
 
 

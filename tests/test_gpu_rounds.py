@@ -34,7 +34,7 @@ def _built():
 def _round_inputs(w, r):
     rows = synth.all_rows(w, r)
     lg = synth.logits(w, r)
-    d = synth.drafts_for(synth.planted_argmax(w, r), synth.accept_targets(w, r), w.V)
+    d = synth.drafts_for(synth.logit_argmax(w, r), synth.accept_targets(w, r), w.V)
     return rows, lg, d
 
 

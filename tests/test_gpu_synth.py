@@ -38,3 +38,18 @@ def test_device_fill_at_large_offsets():
     t = torch.empty(100_000, dtype=torch.bfloat16, device="cuda")
     synth_gpu.fill_normal(t, key, start=3_000_000_000)
     assert np.array_equal(host(t), synth.to_bf16_bits(synth.normal(key, 3_000_000_000, 100_000)))
+
+
+def test_device_drafts_equal_cpu_drafts_with_ties():
+    """The bench's drafts (row argmax of the device logits, the lowest index among equal
+    maxima) equal the CPU's at V = 32768 in bf16, where row maxima tie now and then."""
+    w = synth.Workload("dr", L=1, B=4, H=1, T=15, bf16=True, V=32768, rounds=3, seed=0x79, accept="uniform")
+    ties = 0
+    for r in range(3):
+        d_gpu, j = synth_gpu.drafts(w, r)
+        vam = synth.logit_argmax(w, r)
+        assert np.array_equal(host(d_gpu), synth.drafts_for(vam, synth.accept_targets(w, r), w.V))
+        assert j == [int(x) for x in synth.accept_targets(w, r)]
+        x = synth.bf16_bits_to_f32(synth.logits(w, r))
+        ties += int(((x == x.max(-1, keepdims=True)).sum(-1) > 1).sum())
+    assert ties > 0

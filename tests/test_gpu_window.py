@@ -208,7 +208,7 @@ def test_device_round_window_verify_accept_rollback(orc):
     t = kb.spec_window(to_dev(conf), kb.WIN_CONF_KEEP, 0.5, W.T)
     t_host = [min(orc.conf_keep(conf[b], 0.5, False) + 1, W.T) for b in range(W.B)]
     lg = synth.logits(W, 0)
-    plant = synth.planted_argmax(W, 0)
+    plant = synth.logit_argmax(W, 0)
     jt = np.array([rng.integers(0, n) for n in t_host])
     d = synth.drafts_for(plant, jt, W.V)
     st = layer_state(state0, ring0, cw)

@@ -52,11 +52,28 @@ def test_accept_targets_and_drafts():
     js = np.concatenate([synth.accept_targets(w, r) for r in range(16)])
     assert js.min() >= 0 and js.max() <= w.K
     assert 0.2 < np.mean(js == w.K) < 0.4
-    plant = synth.planted_argmax(w, 0)
-    j = synth.accept_targets(w, 0)
-    d = synth.drafts_for(plant, j, w.V)
-    for b in range(w.B):
-        for r in range(w.K):
-            assert (d[b, r] == plant[b, r]) == (r < j[b])
-    lg = synth.logits(synth.WORKLOADS["tiny"], 0)
-    assert lg.shape == (1, 8, 32) and np.all(lg.argmax(-1) == synth.planted_argmax(synth.WORKLOADS["tiny"], 0))
+    # the drafts follow the row argmax up to j, then differ from it
+    wl = synth.Workload("d", L=1, B=6, H=1, T=15, bf16=True, V=4096, rounds=1, seed=0x77, accept="uniform")
+    vam = synth.logit_argmax(wl, 0)
+    j = synth.accept_targets(wl, 0)
+    d = synth.drafts_for(vam, j, wl.V)
+    for b in range(wl.B):
+        for r in range(wl.K):
+            assert (d[b, r] == vam[b, r]) == (r < j[b])
+
+
+def test_logits_are_normal_and_argmax_takes_the_first_tie():
+    """Logits are the normal draws (mean 0, variance 1), bf16-rounded for bf16 workloads;
+    the argmax is the lowest index among equal maxima (brute force per row)."""
+    w = synth.Workload("l", L=1, B=2, H=1, T=8, bf16=True, V=32768, rounds=4, seed=0x78, accept="uniform")
+    ties = 0
+    for r in range(4):
+        x = synth.bf16_bits_to_f32(synth.logits(w, r))
+        assert abs(float(x.mean())) < 0.01 and abs(float(x.var()) - 1.0) < 0.02
+        vam = synth.logit_argmax(w, r)
+        for b in range(w.B):
+            for t in range(w.T):
+                hits = np.flatnonzero(x[b, t] == x[b, t].max())
+                assert vam[b, t] == hits[0]
+                ties += len(hits) > 1
+    assert ties > 0  # at V = 32768 in bf16 a row maximum ties now and then

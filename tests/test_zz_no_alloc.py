@@ -57,7 +57,7 @@ def test_noalloc_matches_spec_accept_and_oracle_twice_in_a_row(orc):
         if w.name == "na2":
             lg[3, 1, 17] = np.nan  # a NaN row in session 3: reached only if drafts match row 0
         jt = synth.accept_targets(w, 0)
-        d = synth.drafts_for(synth.planted_argmax(w, 0), jt, w.V)
+        d = synth.drafts_for(synth.logit_argmax(w, 0), jt, w.V)
         logits = torch.from_numpy(lg)
         logits = (logits.view(torch.bfloat16) if w.bf16 else logits).cuda()
         drafts = torch.from_numpy(d).cuda()
