@@ -290,11 +290,17 @@ int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_
  *     the update vectors are kept;
  *   dev_jbk: device int32 [3][B]: j, bonus and keep of this round; the keep row is also
  *     the previous round's keep that this round's verify applies (same buffer every call);
- *   host_jb: host int32 [2][B] (pinned) receiving j and the bonus;
+ *   host_jb: host int32 [2][B] (pinned) receiving j and the bonus; where the device can
+ *     address it (cudaHostGetDevicePointer succeeds) the accept writes them there
+ *     directly and dev_jbk's j and bonus rows are not written, else they are copied back;
  *   ready_flags, pairs_per_flag, epoch: as for kda_verify_scan_deferred_staged (a new
  *     epoch each call);
  *   stream: the verify and the accept; copy_stream: the uploads (another stream);
- *   wait != 0: return after the results are in host_jb (cudaStreamSynchronize(stream)).
+ *   wait != 0: return after the results are in host_jb: when the accept writes them
+ *     there directly, the call fills host_jb with INT_MIN first and reads it until every
+ *     entry has been written (at most one second, then cudaStreamSynchronize), which
+ *     returns before the stream's own completion is signalled; else
+ *     cudaStreamSynchronize(stream).
  * First call of a chain (stash->T == 0): the committed state and ring are in
  * stash->state_snap / ring_snap, st's buffers are the spare pair; the rows, logits and
  * drafts go up on `stream`, then kda_verify_scan_pingpong, spec_accept and the copy of

@@ -8,12 +8,17 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
+#include <climits>
 #include <string>
 
 #include "kda_internal.h"
 #include "kda_spec.h"
 
 namespace {
+
+constexpr int KDA_JB_PENDING = INT_MIN;  // no j or bonus takes this value
 
 // The host-to-device copy of a raw-row set: one copy per tensor (q, k, v, g, beta).
 int upload_rows(const kda_dims *dims, const kda_rows *dst, const kda_rows *src, int T, cudaStream_t s)
@@ -112,15 +117,57 @@ extern "C" int kda_round_host(const kda_dims *dims, kda_layer_state *st, kda_sta
         if (e != cudaSuccess)
             return kda::fail(KDA_ECUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
     }
-    if ((rc = spec_accept(dev_logits, logit_dtype, B, T, V, dev_drafts, j_out, bonus_out, keep, dev_status, nullptr,
-                          0, stream)))
+    // j and the bonus: written by the accept straight into host_jb where the device can
+    // address it (pinned memory mapped into the device's address space), else copied
+    // back after it; keep stays on the device for the next round's verify
+    void *mapped = nullptr;
+    if (cudaHostGetDevicePointer(&mapped, host_jb, 0) != cudaSuccess) {
+        cudaGetLastError();  // not mapped: the copy below
+        mapped = nullptr;
+    }
+    int *jo = mapped ? static_cast<int *>(mapped) : j_out, *bo = mapped ? static_cast<int *>(mapped) + B : bonus_out;
+    // mapped and waited for: the results are awaited by reading host_jb until the
+    // accept has replaced a value no result takes (the stream's earlier work was waited
+    // for by the previous call, or is ordered before this accept)
+    const bool poll = mapped && wait;
+    if (poll)
+        for (int i = 0; i < 2 * B; ++i)
+            reinterpret_cast<volatile int *>(host_jb)[i] = KDA_JB_PENDING;
+    if ((rc = spec_accept(dev_logits, logit_dtype, B, T, V, dev_drafts, jo, bo, keep, dev_status, nullptr, 0,
+                          stream)))
         return rc;
-    if ((rc = copy(host_jb, dev_jbk, 2 * static_cast<size_t>(B) * sizeof(int), cudaMemcpyDeviceToHost, stream)))
+    if (!mapped &&
+        (rc = copy(host_jb, dev_jbk, 2 * static_cast<size_t>(B) * sizeof(int), cudaMemcpyDeviceToHost, stream)))
         return rc;
+    if (poll) {
+        // spin on the mapped results (a second at most, then the stream's own wait,
+        // which also reports a failed launch)
+        const volatile int *r = host_jb;
+        const auto t0 = std::chrono::steady_clock::now();
+        for (int i = 0; i < 2 * B;) {
+            if (r[i] != KDA_JB_PENDING) {
+                ++i;
+                continue;
+            }
+            if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(1))
+                break;
+        }
+        std::atomic_thread_fence(std::memory_order_acquire);
+    }
     if (wait) {
-        const cudaError_t e = cudaStreamSynchronize(stream);
-        if (e != cudaSuccess)
+        const cudaError_t e = poll ? cudaStreamQuery(stream) : cudaStreamSynchronize(stream);
+        if (e != cudaSuccess && e != cudaErrorNotReady)
             return kda::fail(KDA_ECUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e));
+        if (poll && e == cudaErrorNotReady) {
+            cudaGetLastError();
+            for (int i = 0; i < 2 * B; ++i)
+                if (host_jb[i] == KDA_JB_PENDING) {  // the accept has not written: wait for the stream
+                    const cudaError_t e2 = cudaStreamSynchronize(stream);
+                    if (e2 != cudaSuccess)
+                        return kda::fail(KDA_ECUDA, std::string("cudaStreamSynchronize: ") + cudaGetErrorString(e2));
+                    break;
+                }
+        }
     }
     return kda::ok();
 }
