@@ -44,10 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 # launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
 # only: comments and blank space removed) the captures were taken on; with any other
 # source the traffic is reported as null.
-TRAFFIC_SOURCE = "da11fbe1982f7bca29f1da6bfd6c4d96c8d5f881e2429befa19cd69a3d4f6f99"
-TRAFFIC_BYTES = {"stack34": (205_136_128 + 266_748_416, 516_995_840),
-                 "batched32": (213_746_176 + 258_133_248, 512_188_800),
-                 "stress64x34": (13_892_460_288 + 18_721_622_016, 31_932_887_040)}
+TRAFFIC_SOURCE = "6413b865c23328f1bf607561987fa4d2efe2eb4124289b6ec85d06591dc84b1c"
+TRAFFIC_BYTES = {"stack34": (205_153_024 + 266_854_400, 516_995_840),
+                 "batched32": (213_602_304 + 257_977_344, 512_188_800),
+                 "stress64x34": (13_890_182_912 + 18_721_224_960, 31_932_887_040)}
 SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
 
 
@@ -393,18 +393,21 @@ def oracle_baseline_threads(w, budget_s: float, threads: int):
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
-def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc, use_w=False):
+def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc, use_w=False,
+            in_place=True):
     """The deferred round end to end from pinned host buffers through the public API:
     one kda_round_host call a round (binding.HostRounds).
 
     A round's inputs sit in one pinned host block (logits, drafts, then each raw-row
-    tensor whole).  Each call copies the raw rows by nc consecutive ranges of (layer,
-    session) pairs on a copy stream, each range followed by a stream write of its ready
-    flag, then the logits and drafts; the deferred round launch scans each range once
-    its flag is set, so the copy of the rest overlaps the scan; then the accept, and j and
-    the bonus come back in one copy.  The call returns once the host has j (a round's
-    inputs follow from the previous accept).  nc == 1: one range, i.e. the whole block
-    before the scan.  Leaves pp committed."""
+    tensor whole).  in_place: the deferred round launch reads the raw rows in place from
+    the host block over the host link while it runs (leaving their device copy for the
+    next round's replay), the logits and drafts go up on a copy stream meanwhile.  Else
+    the call copies the raw rows by nc consecutive ranges of (layer, session) pairs on a
+    copy stream, each range followed by a stream write of its ready flag, and the launch
+    scans each range once its flag is set (nc == 1: the whole block before the scan).
+    Then the accept, whose j and bonus land in pinned host memory.  The call returns once
+    the host has j (a round's inputs follow from the previous accept).  Leaves pp
+    committed."""
     import time
 
     import torch
@@ -458,7 +461,7 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     p = pp.parity
     hr = kb.HostRounds(kb.LayerState(pp.states[p], pp.rings[p], pp.conv_w), dev_sets, out=out,
                        pairs_per_flag=ppf, dev_status=status, stream=stream, copy_stream=copy_stream,
-                       spare_state=pp.states[1 - p], spare_ring=pp.rings[1 - p])
+                       spare_state=pp.states[1 - p], spare_ring=pp.rings[1 - p], in_place=in_place)
     # the chain opens with a ping-pong round, then deferred rounds
     for i in range(4):
         hr(host_views[i % HR])
@@ -478,8 +481,10 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     pp.last = None
     res = {"value": job_rows_per_s(world, w.B, w.T, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_ms, "steps": Ke,
-           "call": "kda_round_host (one call a round)"}
-    if nranges > 1:
+           "call": "kda_round_host (one call a round)",
+           "raw_rows": ("read in place from the pinned host block by the verify launch over the host link"
+                        if in_place else f"copied in {nranges} range(s) of (layer, session) pairs")}
+    if not in_place and nranges > 1:
         res["staged_ranges"] = nranges
         res["pairs_per_range"] = ppf
     return res
@@ -639,7 +644,7 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     if not full:
         if not args.no_e2e:
             res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
-                                 args.e2e_chunks, use_w)
+                                 args.e2e_chunks, use_w, in_place=args.e2e_rows == "in_place")
         return res
 
     # the same rounds with the rollback as its own launch: ping-pong verify, accept,
@@ -734,10 +739,13 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
     # launch) is reported beside it.
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
-                             args.e2e_chunks, use_w)
-        if "staged_ranges" in res["e2e"]:
-            one = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, 1, use_w)
-            res["e2e"]["one_copy"] = {"value": one["value"], "ms_per_step": one["ms_per_step"]}
+                             args.e2e_chunks, use_w, in_place=args.e2e_rows == "in_place")
+        # the copy-based rounds beside it: the rows staged by range, and in one copy
+        for key, nc_, ip in (("staged_copy", args.e2e_chunks, False), ("one_copy", 1, False)):
+            if args.e2e_rows == "in_place" or key == "one_copy":
+                alt = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world, nc_,
+                              use_w, in_place=ip)
+                res["e2e"][key] = {"value": alt["value"], "ms_per_step": alt["ms_per_step"]}
 
     # per-layer issue: one kda_verify_scan per layer (as a model issues them), then accept
     # and one all-layer rollback; eagerly, and replayed from CUDA graphs (one per round)
@@ -1020,6 +1028,9 @@ def main():
     ap.add_argument("--replay-w", choices=["on", "off"], default="on",
                     help="verifies store each row's update vector and replays read it back")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--e2e-rows", choices=["in_place", "staged"], default="in_place",
+                    help="e2e raw rows: read in place from pinned host memory by the verify launch, or copied "
+                         "to the device by range first")
     ap.add_argument("--e2e-chunks", type=int, default=4,
                     help="ranges of (layer, session) pairs the e2e round's raw rows are copied in (the one "
                          "launch waits for each range's ready flag); 1: one copy, then the launch")

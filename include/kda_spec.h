@@ -255,6 +255,24 @@ int kda_verify_scan_deferred_staged(const kda_dims *dims, kda_layer_state *st, k
                                     int *dev_status, cudaStream_t stream);
 
 /*
+ * kda_verify_scan_deferred_host -- kda_verify_scan_deferred whose raw rows this round
+ * are read in place from pinned host memory (host_rows: q, k, v, g, beta in the layout
+ * of kda_rows, allocated so that the device can address them, e.g. cudaHostAlloc; the
+ * call takes their device addresses from cudaHostGetDevicePointer) over the host link
+ * while the launch runs, instead of being copied to the device first.  `rows` names
+ * device tensors of the same shapes that receive a copy of them, written by the launch
+ * (and rows->w, the update vectors, as for the other entry points); the stash records
+ * `rows`, so the next round's replay reads the device copy and host_rows may change as
+ * soon as the launch has completed.  Everything else, and the results, as for
+ * kda_verify_scan_deferred.  A session whose prev_keep is invalid is not processed and
+ * its rows are not copied.  KDA_EINVAL when host_rows is NULL or not addressable by the
+ * device, and for whatever kda_verify_scan_deferred refuses.
+ */
+int kda_verify_scan_deferred_host(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, const int *prev_keep,
+                                  const kda_rows *host_rows, const kda_rows *rows, int T, float *out, int *dev_status,
+                                  cudaStream_t stream);
+
+/*
  * kda_stream_write_u32 -- *flag = value (a 4-byte aligned device address) in the order
  * of `stream`, written by the stream itself (a stream memory operation, no kernel), as
  * the ready flags of kda_verify_scan_deferred_staged want.  KDA_ECUDA when the driver
@@ -296,6 +314,9 @@ int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_
  *   ready_flags, pairs_per_flag, epoch: as for kda_verify_scan_deferred_staged (a new
  *     epoch each call);
  *   stream: the verify and the accept; copy_stream: the uploads (another stream);
+ *   rows_in_place != 0: after the first call the raw rows are not copied: the verify
+ *     reads them in place from host_rows and writes dev_rows as their device copy
+ *     (kda_verify_scan_deferred_host; ready_flags and pairs_per_flag are then unused);
  *   wait != 0: return after the results are in host_jb: when the accept writes them
  *     there directly, the call fills host_jb with INT_MIN first and reads it until every
  *     entry has been written (at most one second, then cudaStreamSynchronize), which
@@ -320,7 +341,7 @@ int kda_round_host(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, 
                    const kda_rows *dev_rows, const void *host_logits, void *dev_logits, int logit_dtype, int V,
                    const int *host_drafts, int *dev_drafts, int *dev_jbk, int *host_jb, float *out,
                    unsigned *ready_flags, int pairs_per_flag, unsigned epoch, int *dev_status, cudaStream_t stream,
-                   cudaStream_t copy_stream, int wait);
+                   cudaStream_t copy_stream, int rows_in_place, int wait);
 
 /*
  * Rounds whose length differs per session (variable T inside one batched grid).

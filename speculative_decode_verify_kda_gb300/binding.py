@@ -29,13 +29,13 @@ MEM_HOST, MEM_DEVICE = 0, 1
 # every symbol the header declares (checked by the CPU test of the library load)
 EXPORTS = ("kda_verify_scan", "kda_rollback", "kda_verify_scan_var", "kda_rollback_var", "kda_verify_scan_pingpong",
            "kda_verify_scan_deferred", "kda_verify_scan_deferred_staged", "kda_stream_write_u32",
-           "kda_upload_rows_staged", "kda_round_host",
+           "kda_upload_rows_staged", "kda_round_host", "kda_verify_scan_deferred_host",
            "kda_verify_scan_cols",
            "kda_rollback_cols", "spec_accept_var",
            "spec_window", "spec_accept_sampled", "spec_accept_sampled_session", "kda_philox4x32_10",
            "spec_accept_sampled_scratch_bytes", "spec_accept_scratch_bytes", "spec_accept", "spec_accept_noalloc", "kda_error_string",
            "kda_last_error", "kda_abi_version")
-ABI_VERSION = 8
+ABI_VERSION = 9
 WIN_CONF_KEEP, WIN_CONFIDENCE, WIN_SLOT_CONFIDENCE = 0, 1, 2
 
 
@@ -113,8 +113,12 @@ def lib(path: str | None = None):
     L.kda_upload_rows_staged.restype = ci
     L.kda_round_host.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState), ctypes.POINTER(KdaStashC),
                                  ci, ctypes.POINTER(KdaRows), ctypes.POINTER(KdaRows), vp, vp, ci, ci, vp, vp, vp,
-                                 vp, vp, vp, ci, ctypes.c_uint, vp, vp, vp, ci]
+                                 vp, vp, vp, ci, ctypes.c_uint, vp, vp, vp, ci, ci]
     L.kda_round_host.restype = ci
+    L.kda_verify_scan_deferred_host.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
+                                                ctypes.POINTER(KdaStashC), vp, ctypes.POINTER(KdaRows),
+                                                ctypes.POINTER(KdaRows), ci, vp, vp, vp]
+    L.kda_verify_scan_deferred_host.restype = ci
     L.kda_verify_scan_cols.argtypes = [ctypes.POINTER(KdaDims), ctypes.POINTER(KdaLayerState),
                                        ctypes.POINTER(KdaRows), ci, vp, vp, vp, vp]
     L.kda_verify_scan_cols.restype = ci
@@ -472,6 +476,41 @@ def kda_verify_scan_deferred_staged(pp: PingPong, q, k, v, g, beta, prev_keep: t
                                                int(pairs_per_flag), ctypes.c_uint(epoch & 0xffffffff),
                                                _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
     _check("kda_verify_scan_deferred_staged", rc)
+    pp.cstash[1 - p].rows, pp.cstash[1 - p].T = rows, T
+    pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, 1 - p, p
+    return pp
+
+
+def kda_verify_scan_deferred_host(pp: PingPong, host: dict, dev: dict, prev_keep: torch.Tensor,
+                                  out: torch.Tensor | None = None, dev_status: torch.Tensor | None = None,
+                                  stream=None) -> PingPong:
+    """kda_verify_scan_deferred whose raw rows are read in place from pinned host memory:
+    host holds CPU tensors q, k, v, g, beta (pinned); dev device tensors of the same
+    shapes (and optionally w) that receive their copy, which the stash records."""
+    if pp.last is None:
+        raise ValueError("a deferred round follows a ping-pong round (no previous round to commit)")
+    shape_ref = LayerState(pp.states[0], pp.rings[0], pp.conv_w)
+    rows, tensors, dt, T = _rows(shape_ref, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], w=dev.get("w"))
+    names = ("q", "k", "v", "g", "beta")
+    for n in names:
+        h = host[n]
+        if h.is_cuda or not h.is_contiguous() or h.dtype != dev[n].dtype or tuple(h.shape) != tuple(dev[n].shape):
+            raise ValueError(f"host {n} must be a contiguous CPU tensor of the device tensor's shape and type")
+    hrows = KdaRows(*(host[n].data_ptr() for n in names))
+    if dt != pp.dtype:
+        raise TypeError("the raw rows must have the previous round's element type")
+    if out is not None:
+        _dev(out, "out", torch.float32, (pp.L, pp.B, T, pp.H, D))
+    _dev(prev_keep, "prev_keep", torch.int32, (pp.B,))
+    p = pp.last
+    prev = pp.cstash[p]
+    cst = KdaLayerState(pp.states[1 - p].data_ptr(), pp.rings[1 - p].data_ptr(), pp.conv_w.data_ptr())
+    cstash = KdaStashC(pp.states[p].data_ptr(), pp.rings[p].data_ptr(), prev.rows, prev.T)
+    dims = pp.dims(dt)
+    rc = lib().kda_verify_scan_deferred_host(ctypes.byref(dims), ctypes.byref(cst), ctypes.byref(cstash),
+                                             _ptr(prev_keep), ctypes.byref(hrows), ctypes.byref(rows), T, _ptr(out),
+                                             _ptr(dev_status), ctypes.c_void_p(_stream(stream)))
+    _check("kda_verify_scan_deferred_host", rc)
     pp.cstash[1 - p].rows, pp.cstash[1 - p].T = rows, T
     pp.rows, pp.dtype, pp.last, pp.parity = tensors, dt, 1 - p, p
     return pp
@@ -1111,12 +1150,15 @@ class HostRounds:
     tensors, each with q, k, v, g, beta (optionally w), logits [B][T][V] and drafts
     int32 [B][T-1]; the rounds alternate between them.  The per-round host inputs are
     dicts of pinned CPU tensors with the same keys (w excepted).  pairs_per_flag: the
-    (layer, session) pairs of a staged range (default: four ranges).  ``commit()`` applies
+    (layer, session) pairs of a staged range (default: four ranges).  in_place: after the
+    first round the verify reads the raw rows in place from the host tensors (they must
+    be addressable by the device) and leaves their copy in the device set.  ``commit()`` applies
     the last round's accept; ``state()`` / ``ring()`` are then the committed tensors.
     """
 
     def __init__(self, st: LayerState, dev_sets: list, out=None, ready_flags=None, pairs_per_flag: int | None = None,
-                 dev_status=None, stream=None, copy_stream=None, spare_state=None, spare_ring=None):
+                 dev_status=None, stream=None, copy_stream=None, spare_state=None, spare_ring=None,
+                 in_place: bool = False):
         if len(dev_sets) != 2:
             raise ValueError("two device input sets alternate")
         self.L, self.B, self.H = st.L, st.B, st.H
@@ -1162,6 +1204,7 @@ class HostRounds:
         self._host = {}
         self.epoch = 0
         self.rounds = 0
+        self.in_place = bool(in_place)
         self._L = lib()
 
     def _host_rows(self, hs: dict):
@@ -1186,7 +1229,8 @@ class HostRounds:
                                     self.jbk.data_ptr(), self.host_jb.data_ptr(), _ptr(self.out),
                                     self.flags.data_ptr(), self.ppf, ctypes.c_uint(self.epoch), _ptr(self.status),
                                     ctypes.c_void_p(_stream(self.stream)),
-                                    ctypes.c_void_p(_stream(self.copy_stream)), 1 if wait else 0)
+                                    ctypes.c_void_p(_stream(self.copy_stream)), 1 if self.in_place else 0,
+                                    1 if wait else 0)
         if rc:
             _check("kda_round_host", rc)
         self.rounds += 1

@@ -45,4 +45,4 @@ extern "C" const char *kda_error_string(int code)
 
 extern "C" const char *kda_last_error(void) { return kda::g_last_error.c_str(); }
 
-extern "C" int kda_abi_version(void) { return 8; }
+extern "C" int kda_abi_version(void) { return 9; }

@@ -56,7 +56,7 @@ extern "C" int kda_round_host(const kda_dims *dims, kda_layer_state *st, kda_sta
                               void *dev_logits, int logit_dtype, int V, const int *host_drafts, int *dev_drafts,
                               int *dev_jbk, int *host_jb, float *out, unsigned *ready_flags, int pairs_per_flag,
                               unsigned epoch, int *dev_status, cudaStream_t stream, cudaStream_t copy_stream,
-                              int wait)
+                              int rows_in_place, int wait)
 {
     if (!dims || !st || !stash || !host_rows || !dev_rows)
         return kda::fail(KDA_EINVAL, "dims, st, stash, host_rows and dev_rows must not be NULL");
@@ -72,7 +72,7 @@ extern "C" int kda_round_host(const kda_dims *dims, kda_layer_state *st, kda_sta
         return kda::fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
     if (reinterpret_cast<uintptr_t>(dev_jbk) & 3u)
         return kda::fail(KDA_EINVAL, "dev_jbk must be a 4-byte aligned device array [3][B]");
-    if (stream == copy_stream && stash->T > 0)
+    if (stream == copy_stream && stash->T > 0 && !rows_in_place)
         return kda::fail(KDA_EINVAL, "copy_stream must differ from stream (the copies overlap the verify)");
     const int B = dims->B;
     int *j_out = dev_jbk, *bonus_out = dev_jbk + B, *keep = dev_jbk + 2 * B;
@@ -90,6 +90,25 @@ extern "C" int kda_round_host(const kda_dims *dims, kda_layer_state *st, kda_sta
         if ((rc = kda_verify_scan_pingpong(dims, st, dev_rows, T, nullptr, KDA_MEM_HOST, out, stash, dev_status,
                                            stream)))
             return rc;
+    } else if (rows_in_place) {
+        // the verify reads the rows in place from host memory and leaves their device
+        // copy in dev_rows; the logits and drafts go up meanwhile
+        if ((rc = kda_verify_scan_deferred_host(dims, st, stash, keep, host_rows, dev_rows, T, out, dev_status,
+                                                stream)))
+            return rc;
+        if ((rc = copy(dev_logits, host_logits, logit_bytes, cudaMemcpyHostToDevice, copy_stream)) ||
+            (rc = copy(dev_drafts, host_drafts, draft_bytes, cudaMemcpyHostToDevice, copy_stream)))
+            return rc;
+        cudaEvent_t copied;
+        cudaError_t e = cudaEventCreateWithFlags(&copied, cudaEventDisableTiming);
+        if (e == cudaSuccess) {
+            e = cudaEventRecord(copied, copy_stream);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(stream, copied, 0);
+            cudaEventDestroy(copied);
+        }
+        if (e != cudaSuccess)
+            return kda::fail(KDA_ECUDA, std::string("cudaStreamWaitEvent: ") + cudaGetErrorString(e));
     } else {
         // the launch first (its start-up overlaps the first range's copy; it scans each
         // range once its flag is set), then the rows by range of pairs_per_flag (layer,

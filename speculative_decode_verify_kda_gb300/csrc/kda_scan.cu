@@ -117,6 +117,7 @@ struct ScanParams {
     CUtensorMap tm_snap;   // snapshot write, same geometry (unused without s_snap)
     CUtensorMap tm_rows[4];  // raw rows q, k, v, g: [L*B][T_rows][H][128], box 128 x 1 x T_rows x 1
     CUtensorMap tm_prev[4];  // DEFERRED: the previous round's raw rows, box 128 x 1 x T_prev x 1
+    CUtensorMap tm_copy[4];  // rows_host: the device copy of this call's raw rows, as tm_rows
     float *s_out;          // [L][B][H][D][D]
     float *s_snap;         // nullable: receives the state read through tm_in
     const float *ring_in;  // [L][B][H][3][3][D]
@@ -129,6 +130,7 @@ struct ScanParams {
     const float *ring_in2; // DEFERRED: the ring of units with nothing to replay
     float *ring_snap_out;  // DEFERRED: receives the ring after the replay
     const void *xb_prev;   // DEFERRED: the previous round's raw beta [L][B][T_prev][H]
+    void *copy_beta;       // rows_host: the device copy of this call's raw beta
     float *w_out;          // nullable: [L][B][T_rows][H][D], the update vector w_t of every verify row
     const float *w_in;     // nullable: the update vectors of the rows a replay re-runs, [L][B][T_w][H][D]
     int T_w;               // row count of w_in (the replayed round's T)
@@ -149,6 +151,7 @@ struct ScanParams {
     int tcap;              // most rows any unit runs (sizes the buffers)
     int nstg;              // raw-row stages: 2 where shared memory allows, else 1
     int bf16;
+    int rows_host;         // this call's raw rows (xq..xb) are read in place from host memory
     int keep_mode;
     unsigned char keep_host[KDA_HOST_KEEP_MAX];
 };
@@ -250,6 +253,13 @@ __device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap *tm, int c0, i
 {
     asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
                  ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3) : "memory");
+}
+
+// 4D tensor copy shared -> global of the box at (c0, c1, c2, c3), tracked by bulk groups
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *tm, int c0, int c1, int c2, int c3, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3, %4}], [%5];"
+                 ::"l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src) : "memory");
 }
 
 // 2D tensor copy shared -> global of the box at (x, y), tracked by bulk groups
@@ -502,15 +512,57 @@ __device__ __forceinline__ void issue_state(const ScanParams &p, uint32_t slot, 
 // of all rows of its head in the round it belongs to (a unit that runs fewer rows
 // gets them all; the rest are not read).  Lane 0 arms the barrier with the byte
 // count; each prologue warp stages its own stream, with a barrier per stream and stage.
+template <bool HR>
 __device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t stg, uint32_t bar, Item it, int s,
                              int lane)
 {
     const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(it.u), p.divH)), h = it.u - lb * p.H;
     const uint32_t rb = static_cast<uint32_t>(lay.row_bytes());
+    if (HR && it.part == 1) {
+        // rows in host memory: each lane copies its 8 (bf16) or 16 (f32) bytes of every
+        // row with an asynchronous copy the barrier tracks (the copy engine of the SM
+        // reads host memory like global memory), once the device copy of the stage's
+        // previous item has read the stage
+        if (lane == 0)
+            bulk_wait_read();
+        __syncwarp();
+        const uint32_t cb = rb / 32;
+        const char *base = static_cast<const char *>(s == 0 ? p.xq : s == 1 ? p.xk : s == 2 ? p.xv : p.xg);
+        const char *src = base + (static_cast<size_t>(lb) * p.T_rows * p.H + h) * rb + lane * cb;
+        const size_t pitch = static_cast<size_t>(p.H) * rb;
+        const uint32_t dst = stg + s * lay.tcap * rb + lane * cb;
+        for (int t = 0; t < p.T_rows; ++t) {
+            if (cb == 16)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + t * rb), "l"(src + t * pitch)
+                             : "memory");
+            else
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + t * rb), "l"(src + t * pitch)
+                             : "memory");
+        }
+        asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(bar);  // the barrier's one arrival; it completes once the copies land
+        return;
+    }
     fence_proxy_async();  // the prologue's generic reads of the stage come first
     if (lane == 0) {
         mbar_expect_tx(bar, static_cast<uint32_t>(it.part == 0 ? p.T_prev : p.T_rows) * rb);
         tma_load_4d(stg + s * lay.tcap * rb, it.part == 0 ? &p.tm_prev[s] : &p.tm_rows[s], 0, h, 0, lb, bar);
+    }
+}
+
+// rows_host: the device copy of an item's rows of stream s, sent from the stage once
+// they have landed (the stash records the copy for the next round's replay).
+__device__ __forceinline__ void copy_stage_out(const ScanParams &p, const Layout &lay, uint32_t stg, int u, int s,
+                                               int lane)
+{
+    const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(u), p.divH)), h = u - lb * p.H;
+    fence_proxy_async();  // the stage's rows, landed, before the tensor store reads them
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_4d(&p.tm_copy[s], 0, h, 0, lb, stg + s * lay.tcap * static_cast<uint32_t>(lay.row_bytes()));
+        bulk_commit();
     }
 }
 
@@ -524,6 +576,7 @@ struct Pre {
     float beta;
 };
 
+template <bool HR>
 __device__ __forceinline__ void load_pre(const ScanParams &p, Item it, int pw, int lane, Pre &pr)
 {
     const Unit x = unit_of(p, it.u);
@@ -543,7 +596,14 @@ __device__ __forceinline__ void load_pre(const ScanParams &p, Item it, int pw, i
     } else {
         const int T = it.part == 0 ? x.R : x.T, trows = it.part == 0 ? p.T_prev : p.T_rows;
         const void *xb = it.part == 0 ? p.xb_prev : p.xb;
-        pr.beta = lane < T ? load_scalar(xb, p.bf16, (static_cast<size_t>(x.lb) * trows + lane) * p.H + x.h) : 0.f;
+        const size_t bi = (static_cast<size_t>(x.lb) * trows + lane) * p.H + x.h;
+        pr.beta = lane < T ? load_scalar(xb, p.bf16, bi) : 0.f;
+        if (HR && it.part == 1 && lane < p.T_rows) {  // the device copy of the raw beta
+            if (p.bf16)
+                static_cast<uint16_t *>(p.copy_beta)[bi] = static_cast<const uint16_t *>(xb)[bi];
+            else
+                static_cast<uint32_t *>(p.copy_beta)[bi] = static_cast<const uint32_t *>(xb)[bi];
+        }
     }
 }
 
@@ -740,7 +800,7 @@ struct Stager {
     uint32_t par0, par1;  // and the phase parity that completes it
 };
 
-template <bool COLS, bool W>
+template <bool COLS, bool W, bool HR>
 __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned char *sm, const Ctl &c, int n)
 {
     const int pw = (threadIdx.x >> 5) - NSCAN, lane = threadIdx.x & 31;
@@ -757,12 +817,12 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
             ok = false;
             break;
         }
-        issue_stream(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + 4 * b + pw), sg.next, pw, lane);
+        issue_stream<HR>(p, lay, stg0 + b * stage_bytes, c.bar(B_STG_FULL + 4 * b + pw), sg.next, pw, lane);
         (b ? sg.pend1 : sg.pend0) = true;
         sg.next = next_item(p, sg.next, n);
     }
     if (ok && it.u < n)
-        load_pre(p, it, pw, lane, pr);
+        load_pre<HR>(p, it, pw, lane, pr);
     for (int i = 0; ok && it.u < n; ++i) {
         const int b = i & 1;
         const Unit x = unit_of(p, it.u);
@@ -774,6 +834,8 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
             break;
         }
         (sb ? sg.pend1 : sg.pend0) = false;
+        if (HR && it.part == 1)
+            copy_stage_out(p, lay, stg0 + sb * stage_bytes, it.u, pw, lane);
         // the scan of item i-2 has released this scan-input buffer
         if (i >= 2 && !warp_wait(c, B_SI_EMPTY + b, ((i >> 1) - 1) & 1)) {
             ok = false;
@@ -812,14 +874,14 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
                 ok = false;
                 break;
             }
-            issue_stream(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + 4 * sb + pw), sg.next, pw, lane);
+            issue_stream<HR>(p, lay, stg0 + sb * stage_bytes, c.bar(B_STG_FULL + 4 * sb + pw), sg.next, pw, lane);
             (sb ? sg.pend1 : sg.pend0) = true;
             (sb ? sg.par1 : sg.par0) = (m + 1) & 1;
             sg.next = next_item(p, sg.next, n);
         }
         const Item nx = next_item(p, it, n);
         if (nx.u < n)
-            load_pre(p, nx, pw, lane, pr);
+            load_pre<HR>(p, nx, pw, lane, pr);
         it = nx;
     }
     if (!ok && lane == 0) {  // stage copies in flight must land before the CTA leaves
@@ -827,6 +889,11 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
             drain_wait(c.bar(B_STG_FULL + pw), sg.par0);
         if (sg.pend1)
             drain_wait(c.bar(B_STG_FULL + 4 + pw), sg.par1);
+    }
+    if (HR) {  // this warp's copies: landed in, and sent out, before the CTA leaves
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0)
+            bulk_wait_all();
     }
 }
 
@@ -1105,11 +1172,12 @@ __device__ void scan_warp(const ScanParams &p, const Layout &lay, unsigned char 
 // One persistent CTA per SM; warps 0..7 scan (warp 0 also loads the states), 8..11 run
 // the prologue (warp 11 also stages the raw rows).
 // COLS: also write the column stash (the state and ring after every row).  W: the
-// verify stores each row's update vector (w_out) and a replay reads them (w_in); an
-// instantiation of its own, so the loop without them carries none of their code.
+// verify stores each row's update vector (w_out) and a replay reads them (w_in); HR:
+// this call's raw rows are read in place from host memory.  Each an instantiation of
+// its own, so the launches without them carry none of their code.
 // Verify and rollback share one instantiation: alternating between two kernels of this
 // size cost the verify 5 % (its code is fetched again after each switch).
-template <bool COLS, bool W>
+template <bool COLS, bool W, bool HR>
 __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__ ScanParams p)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -1130,7 +1198,8 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
                 tma_prefetch_2d(&p.tm_in, 32 * b, u1 * D);
         } else if (wi >= NSCAN && u0 < n) {
             const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(u0), p.divH)), h = u0 - lb * p.H;
-            tma_prefetch_4d(&p.tm_rows[wi - NSCAN], 0, h, 0, lb);
+            if (!HR)
+                tma_prefetch_4d(&p.tm_rows[wi - NSCAN], 0, h, 0, lb);
             if (p.keep_mode == DEFERRED)
                 tma_prefetch_4d(&p.tm_prev[wi - NSCAN], 0, h, 0, lb);
         }
@@ -1156,7 +1225,7 @@ __global__ void __launch_bounds__(NT, 1) kda_scan_kernel(const __grid_constant__
     if (wi < NSCAN)
         scan_warp<COLS, W>(p, lay, sm, c, n);
     else
-        prologue_warp<COLS, W>(p, lay, sm, c, n);
+        prologue_warp<COLS, W, HR>(p, lay, sm, c, n);
 }
 
 // ---- host side ----------------------------------------------------------------------
@@ -1282,7 +1351,7 @@ FastDiv make_fastdiv(uint32_t d)
 }
 
 int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const float *s_in2 = nullptr,
-                const kda_rows *prev = nullptr)
+                const kda_rows *prev = nullptr, const kda_rows *copy = nullptr)
 {
     const long long units = static_cast<long long>(p.L) * p.B * p.H;
     if (units == 0)
@@ -1313,9 +1382,11 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
             if (static_cast<size_t>(optin) < most)
                 return fail(KDA_ECUDA,
                             "kda_scan_kernel needs " + std::to_string(most) + " bytes of shared memory per block");
-            const void *kernels[3] = {reinterpret_cast<const void *>(kda_scan_kernel<false, false>),
-                                      reinterpret_cast<const void *>(kda_scan_kernel<false, true>),
-                                      reinterpret_cast<const void *>(kda_scan_kernel<true, false>)};
+            const void *kernels[5] = {reinterpret_cast<const void *>(kda_scan_kernel<false, false, false>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<false, true, false>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<true, false, false>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<false, false, true>),
+                                      reinterpret_cast<const void *>(kda_scan_kernel<false, true, true>)};
             for (const void *k : kernels)
                 if (e == cudaSuccess)
                     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
@@ -1337,9 +1408,15 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
     if (p.tcap < p.T_rows || (p.keep_mode == DEFERRED && p.tcap < p.T_prev))
         return fail(KDA_EINVAL, "internal: the raw-row stage must hold every round's rows");
     const long long LB = static_cast<long long>(p.L) * p.B;
+    // rows in host memory are read with per-lane copies; their device copy has the maps
     const void *raw[4] = {p.xq, p.xk, p.xv, p.xg};
+    if (p.rows_host && !copy)
+        return fail(KDA_EINVAL, "internal: rows read in place need their device copy");
+    const void *dst[4] = {copy ? copy->q : nullptr, copy ? copy->k : nullptr, copy ? copy->v : nullptr,
+                          copy ? copy->g : nullptr};
     for (int s = 0; s < 4; ++s)
-        if ((rc = rows_map(&p.tm_rows[s], raw[s], p.bf16 != 0, LB, p.T_rows, p.H)))
+        if ((rc = p.rows_host ? rows_map(&p.tm_copy[s], dst[s], p.bf16 != 0, LB, p.T_rows, p.H)
+                              : rows_map(&p.tm_rows[s], raw[s], p.bf16 != 0, LB, p.T_rows, p.H)))
             return rc;
     if (p.keep_mode == DEFERRED) {
         if (!s_in2 || !prev)
@@ -1368,9 +1445,16 @@ int launch_scan(ScanParams &p, const float *s_in, cudaStream_t stream, const flo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // the column stash never carries update vectors (its rollback copies columns)
-    const cudaError_t le = p.s_cols                ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<true, false>, p)
-                           : (p.w_in || p.w_out) ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, true>, p)
-                                                 : cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, false>, p);
+    const bool w = p.w_in || p.w_out;
+    cudaError_t le;
+    if (p.s_cols)
+        le = cudaLaunchKernelEx(&cfg, kda_scan_kernel<true, false, false>, p);
+    else if (p.rows_host)
+        le = w ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, true, true>, p)
+               : cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, false, true>, p);
+    else
+        le = w ? cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, true, false>, p)
+               : cudaLaunchKernelEx(&cfg, kda_scan_kernel<false, false, false>, p);
     if (le != cudaSuccess)
         return fail(KDA_ECUDA, std::string("kda_scan_kernel launch: ") + cudaGetErrorString(le));
     return check_launch("kda_scan_kernel");
@@ -1524,11 +1608,31 @@ extern "C" int kda_verify_scan_pingpong(const kda_dims *dims, const kda_layer_st
 namespace kda {
 namespace {
 
-// Shared body of kda_verify_scan_deferred and kda_verify_scan_deferred_staged (ready:
-// nullptr for rows already in place).
+// The device address of each raw-row pointer of host rows (pinned host memory mapped
+// into the device's address space), checked like device rows.
+int host_rows_on_device(const kda_rows *host_rows, int dtype, kda_rows *dev)
+{
+    int rc = check_rows(host_rows, dtype);
+    if (rc)
+        return rc;
+    const void *h[5] = {host_rows->q, host_rows->k, host_rows->v, host_rows->g, host_rows->beta};
+    void *d[5];
+    for (int i = 0; i < 5; ++i)
+        if (cudaHostGetDevicePointer(&d[i], const_cast<void *>(h[i]), 0) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(KDA_EINVAL, "host_rows must be pinned host memory the device can address "
+                                    "(cudaHostGetDevicePointer refused one of them)");
+        }
+    *dev = kda_rows{d[0], d[1], d[2], d[3], d[4], nullptr};
+    return check_rows(dev, dtype);
+}
+
+// Shared body of kda_verify_scan_deferred, kda_verify_scan_deferred_staged (ready:
+// nullptr for rows already in place) and kda_verify_scan_deferred_host (host_rows: this
+// call's rows read in place from host memory, `rows` their device copy).
 int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash, const int *prev_keep,
                     const kda_rows *rows, int T, float *out, const unsigned *ready, int ppf, unsigned epoch,
-                    int *dev_status, cudaStream_t stream)
+                    int *dev_status, cudaStream_t stream, const kda_rows *host_rows = nullptr)
 {
     int rc = check_common(dims, st);
     if (rc)
@@ -1551,6 +1655,9 @@ int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
             return fail(KDA_EINVAL, "prev_keep must be a 4-byte aligned device array of B ints");
         if (out && (reinterpret_cast<uintptr_t>(out) & 3u))
             return fail(KDA_EINVAL, "out must be 4-byte aligned");
+        kda_rows hdev{};
+        if (host_rows && (rc = host_rows_on_device(host_rows, dims->dtype, &hdev)))
+            return rc;
         ScanParams p{};
         p.keep_mode = DEFERRED;
         p.keep_dev = prev_keep;
@@ -1566,6 +1673,11 @@ int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
         p.ring_snap_out = st->conv_ring;
         p.conv_w = st->conv_w;
         p.xq = rows->q; p.xk = rows->k; p.xv = rows->v; p.xg = rows->g; p.xb = rows->beta;
+        if (host_rows) {  // read in place; `rows` receives their device copy
+            p.xq = hdev.q; p.xk = hdev.k; p.xv = hdev.v; p.xg = hdev.g; p.xb = hdev.beta;
+            p.copy_beta = const_cast<void *>(rows->beta);
+            p.rows_host = 1;
+        }
         p.xb_prev = stash->rows.beta;
         p.w_out = rows->w;
         p.w_in = stash->rows.w;
@@ -1582,7 +1694,7 @@ int deferred_common(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
         p.ready = ready;
         p.ready_ppf = ppf;
         p.epoch = epoch;
-        if ((rc = launch_scan(p, stash->state_snap, stream, st->state, &stash->rows)))
+        if ((rc = launch_scan(p, stash->state_snap, stream, st->state, &stash->rows, host_rows ? rows : nullptr)))
             return rc;
     }
     // the stash now describes this round (its snapshot is in Q) and st its post-round
@@ -1615,6 +1727,16 @@ extern "C" int kda_verify_scan_deferred_staged(const kda_dims *dims, kda_layer_s
         return kda::fail(KDA_EINVAL, "pairs_per_flag must be >= 1");
     return kda::deferred_common(dims, st, stash, prev_keep, rows, T, out, ready_flags, pairs_per_flag, epoch,
                                 dev_status, stream);
+}
+
+extern "C" int kda_verify_scan_deferred_host(const kda_dims *dims, kda_layer_state *st, kda_stash *stash,
+                                             const int *prev_keep, const kda_rows *host_rows, const kda_rows *rows,
+                                             int T, float *out, int *dev_status, cudaStream_t stream)
+{
+    if (!host_rows)
+        return kda::fail(KDA_EINVAL, "host_rows must not be NULL");
+    return kda::deferred_common(dims, st, stash, prev_keep, rows, T, out, nullptr, 1, 0, dev_status, stream,
+                                host_rows);
 }
 
 namespace kda {

@@ -342,7 +342,7 @@ def test_round_host_rejects_on_host(L):
     def call(stash, T=8, V=1000, ldt=kb.BF16, jbk=FAKE + 0x5000, s1=None, s2=None, hl=FAKE):
         return L.kda_round_host(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(stash) if stash else None, T,
                                 ctypes.byref(hrows), ctypes.byref(rows), hl, FAKE, ldt, V, FAKE, FAKE, jbk,
-                                FAKE + 0x6000, None, FAKE + 0x7000, 1, 1, None, s1, s2, 0)
+                                FAKE + 0x6000, None, FAKE + 0x7000, 1, 1, None, s1, s2, 0, 0)
     prev = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)
     assert call(None) == kb.EINVAL
     assert call(prev, T=0) == kb.EINVAL and call(prev, T=16) == kb.EINVAL
@@ -352,3 +352,13 @@ def test_round_host_rejects_on_host(L):
     # after the first round the copies need a stream of their own: the verify waits for them
     assert call(prev, s1=None, s2=None) == kb.EINVAL
     assert b"copy_stream" in L.kda_last_error()
+
+
+def test_deferred_host_rejects_on_host(L):
+    dims, st, rows = _state(B=2)
+    prev = kb.KdaStashC(FAKE + 0x1000, FAKE + 0x2000, kb.KdaRows(FAKE, FAKE, FAKE, FAKE, FAKE), 8)
+    assert L.kda_verify_scan_deferred_host(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(prev), FAKE + 0x3000,
+                                           None, ctypes.byref(rows), 8, None, None, None) == kb.EINVAL
+    bad = kb.KdaRows(FAKE, FAKE, FAKE, FAKE + 2, FAKE)  # misaligned before any device query
+    assert L.kda_verify_scan_deferred_host(ctypes.byref(dims), ctypes.byref(st), ctypes.byref(prev), FAKE + 0x3000,
+                                           ctypes.byref(bad), ctypes.byref(rows), 8, None, None, None) == kb.EINVAL

@@ -442,3 +442,61 @@ def test_staged_rounds_with_f32_rows():
         torch.cuda.synchronize()
         assert bits_equal(out_a, out_b), f"round {r}: outputs"
         assert bits_equal(pa.state(), pb.state()) and bits_equal(pa.ring(), pb.ring()), f"round {r}"
+
+
+@pytest.mark.parametrize("bf16,with_w", [(True, False), (True, True), (False, False)])
+def test_deferred_rows_read_in_place_from_host(bf16, with_w):
+    """kda_verify_scan_deferred_host reads this round's raw rows in place from pinned host
+    memory: outputs, snapshots, states and rings bit-identical to the same rounds from
+    device rows, and the device copy it leaves equals the host rows byte for byte (the
+    next round replays from it)."""
+    L, B, H, Ts = 2, 4, 5, [8, 6, 15, 3]
+    w0 = synth.Workload("dh", L=L, B=B, H=H, T=Ts[0], bf16=bf16, V=64, rounds=1, seed=0x9940, accept="uniform")
+    state0, ring0, cw = small_case(w0)
+    rounds_np = _rounds(L, B, H, Ts, bf16, 0x9941)
+    keeps = _keeps(B, Ts, 0x9942)
+    dt = torch.bfloat16 if bf16 else torch.float32
+
+    def host_set(r):
+        out = {}
+        for n in NAMES:
+            t = torch.from_numpy(np.ascontiguousarray(rounds_np[r][n]))
+            out[n] = (t.view(torch.bfloat16) if bf16 else t).pin_memory()
+        return out
+
+    a = kb.PingPong(layer_state(state0, ring0, cw))
+    b = kb.PingPong(layer_state(state0, ring0, cw))
+    hold = []
+    for r, T in enumerate(Ts):
+        x = rows_to_dev(rounds_np[r], bf16)
+        out_a = torch.full((L, B, T, H, 128), float("nan"), device="cuda")
+        out_b = torch.full_like(out_a, float("nan"))
+        wa = torch.empty((L, B, T, H, 128), dtype=torch.float32, device="cuda") if with_w else None
+        wb = torch.empty_like(wa) if with_w else None
+        if r == 0:
+            kb.kda_verify_scan_pingpong(a, *[x[n] for n in NAMES], out=out_a, w=wa)
+            kb.kda_verify_scan_pingpong(b, *[x[n] for n in NAMES], out=out_b, w=wb)
+            hold.append((x, wa, wb))
+            continue
+        keep = torch.tensor(keeps[r - 1], dtype=torch.int32, device="cuda")
+        kb.kda_verify_scan_deferred(a, *[x[n] for n in NAMES], keep, out=out_a, w=wa)
+        h = host_set(r)
+        dev = {n: torch.full_like(x[n], 0) for n in NAMES}
+        if with_w:
+            dev["w"] = wb
+        kb.kda_verify_scan_deferred_host(b, h, dev, keep, out=out_b)
+        torch.cuda.synchronize()
+        hold.append((x, h, dev, wa, wb))
+        assert bits_equal(out_a, out_b), f"round {r}: outputs"
+        for n in NAMES:
+            assert torch.equal(dev[n].cpu().view(torch.int16 if bf16 else torch.int32),
+                               h[n].view(torch.int16 if bf16 else torch.int32)), f"round {r}: device copy of {n}"
+        for nm, ta, tb in (("snapshot", a.states[a.last], b.states[b.last]),
+                           ("post-round", a.state(), b.state()),
+                           ("ring snapshot", a.rings[a.last], b.rings[b.last]),
+                           ("post-round ring", a.ring(), b.ring())):
+            assert bits_equal(ta, tb), f"round {r}: {nm}"
+    kb.kda_rollback_pingpong(a, keeps[-1])
+    kb.kda_rollback_pingpong(b, keeps[-1])
+    torch.cuda.synchronize()
+    assert bits_equal(a.state(), b.state()) and bits_equal(a.ring(), b.ring())

@@ -57,8 +57,10 @@ def _dev_set(w, with_w):
     return d
 
 
-@pytest.mark.parametrize("bf16,ppf,with_w", [(True, 2, False), (True, 1, True), (False, 4, False)])
-def test_host_rounds_equal_the_entry_points(bf16, ppf, with_w):
+@pytest.mark.parametrize("bf16,ppf,with_w,in_place", [(True, 2, False, False), (True, 1, True, False),
+                                                      (False, 4, False, False), (True, 2, False, True),
+                                                      (True, 1, True, True), (False, 1, False, True)])
+def test_host_rounds_equal_the_entry_points(bf16, ppf, with_w, in_place):
     w = synth.Workload("rh", L=2, B=3, H=4, T=8, bf16=bf16, V=96, rounds=6, seed=0x5150, accept="uniform")
     state0, ring0, cw = small_case(w)
     R = 5
@@ -85,7 +87,7 @@ def test_host_rounds_equal_the_entry_points(bf16, ppf, with_w):
     out = torch.full((w.L, w.B, w.T, w.H, 128), float("nan"), device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     hr = kb.HostRounds(st, [_dev_set(w, with_w), _dev_set(w, with_w)], out=out, pairs_per_flag=ppf,
-                       dev_status=status)
+                       dev_status=status, in_place=in_place)
     for r in range(R):
         h, jt = host[r]
         j, bonus = hr(h)
