@@ -321,7 +321,8 @@ int kda_upload_rows_staged(const kda_dims *dims, const kda_rows *dst, const kda_
  *     there directly, the call fills host_jb with INT_MIN first and reads it until every
  *     entry has been written (at most one second, then cudaStreamSynchronize), which
  *     returns before the stream's own completion is signalled; else
- *     cudaStreamSynchronize(stream).
+ *     cudaStreamSynchronize(stream).  An earlier call made with wait == 0 must have
+ *     completed first (its accept could otherwise still write host_jb);
  * First call of a chain (stash->T == 0): the committed state and ring are in
  * stash->state_snap / ring_snap, st's buffers are the spare pair; the rows, logits and
  * drafts go up on `stream`, then kda_verify_scan_pingpong, spec_accept and the copy of
