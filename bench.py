@@ -664,11 +664,13 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         step(i % R)
     barrier()
     pa, pb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with nvtx_range("separate"):
+    with nvtx_range("separate"):  # the step time without events between the launches
         pa.record(stream)
         for i in range(Kp):
-            step((3 + i) % R, evp[i])
+            step((3 + i) % R)
         pb.record(stream)
+        for i in range(Kp):  # the per-kernel times
+            step((3 + Kp + i) % R, evp[i])
     barrier()
     if int(status.item()):
         raise RuntimeError(f"device status {int(status.item()):#x} after the ping-pong steps")
@@ -688,11 +690,13 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         step(i % R, plans_=plans)
     barrier()
     ia, ib = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with nvtx_range("in_place"):
+    with nvtx_range("in_place"):  # the step time without events between the launches
         ia.record(stream)
         for i in range(Ki):
-            step(i % R, evi[i], plans_=plans)
+            step(i % R, plans_=plans)
         ib.record(stream)
+        for i in range(Ki):  # the per-kernel times
+            step((Ki + i) % R, evi[i], plans_=plans)
     barrier()
     if int(status.item()):
         raise RuntimeError(f"device status {int(status.item()):#x} after the in-place steps")
