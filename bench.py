@@ -44,10 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 # launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
 # only: comments and blank space removed) the captures were taken on; with any other
 # source the traffic is reported as null.
-TRAFFIC_SOURCE = "6413b865c23328f1bf607561987fa4d2efe2eb4124289b6ec85d06591dc84b1c"
-TRAFFIC_BYTES = {"stack34": (205_153_024 + 266_854_400, 516_995_840),
-                 "batched32": (213_602_304 + 257_977_344, 512_188_800),
-                 "stress64x34": (13_890_182_912 + 18_721_224_960, 31_932_887_040)}
+TRAFFIC_SOURCE = "b03f73f54794a912a09dd8314d0b88ccb31e298aafdbd2d4e43f31c24124a432"
+TRAFFIC_BYTES = {"stack34": (205_133_056 + 266_535_424, 516_995_840),
+                 "batched32": (213_602_816 + 257_861_376, 512_188_800),
+                 "stress64x34": (13_888_683_520 + 18_721_341_440, 31_932_887_040)}
 SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
 
 
@@ -467,8 +467,9 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
         hr(host_views[i % HR])
     barrier()
     t0 = time.perf_counter()
-    for i in range(4, 4 + Ke):
-        hr(host_views[i % HR])
+    with nvtx_range("e2e_in_place" if in_place else "e2e_staged"):
+        for i in range(4, 4 + Ke):
+            hr(host_views[i % HR])
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / Ke
     e2e_ms = slowest(e2e_ms, world, dev)

@@ -547,6 +547,8 @@ __device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t st
     }
     fence_proxy_async();  // the prologue's generic reads of the stage come first
     if (lane == 0) {
+        if (HR)
+            bulk_wait_read();  // and the device copy of the stage's previous item has read it
         mbar_expect_tx(bar, static_cast<uint32_t>(it.part == 0 ? p.T_prev : p.T_rows) * rb);
         tma_load_4d(stg + s * lay.tcap * rb, it.part == 0 ? &p.tm_prev[s] : &p.tm_rows[s], 0, h, 0, lb, bar);
     }
