@@ -44,10 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 # launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
 # only: comments and blank space removed) the captures were taken on; with any other
 # source the traffic is reported as null.
-TRAFFIC_SOURCE = "b03f73f54794a912a09dd8314d0b88ccb31e298aafdbd2d4e43f31c24124a432"
-TRAFFIC_BYTES = {"stack34": (205_133_056 + 266_535_424, 516_995_840),
-                 "batched32": (213_602_816 + 257_861_376, 512_188_800),
-                 "stress64x34": (13_888_683_520 + 18_721_341_440, 31_932_887_040)}
+TRAFFIC_SOURCE = "4f4e2354f086c424e5230ea472c11dd0fba30fb502264f8ae488cdfe7ca754ba"
+TRAFFIC_BYTES = {"stack34": (205_133_312 + 266_716_160, 516_995_840),
+                 "batched32": (213_603_328 + 258_101_504, 512_188_800),
+                 "stress64x34": (13_886_914_816 + 18_721_277_696, 31_932_887_040)}
 SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
 
 

@@ -599,13 +599,9 @@ __device__ __forceinline__ void load_pre(const ScanParams &p, Item it, int pw, i
         const int T = it.part == 0 ? x.R : x.T, trows = it.part == 0 ? p.T_prev : p.T_rows;
         const void *xb = it.part == 0 ? p.xb_prev : p.xb;
         const size_t bi = (static_cast<size_t>(x.lb) * trows + lane) * p.H + x.h;
-        pr.beta = lane < T ? load_scalar(xb, p.bf16, bi) : 0.f;
-        if (HR && it.part == 1 && lane < p.T_rows) {  // the device copy of the raw beta
-            if (p.bf16)
-                static_cast<uint16_t *>(p.copy_beta)[bi] = static_cast<const uint16_t *>(xb)[bi];
-            else
-                static_cast<uint32_t *>(p.copy_beta)[bi] = static_cast<const uint32_t *>(xb)[bi];
-        }
+        // host rows: every row's beta, for the device copy the prologue writes once it
+        // has used the value (a store right here would wait for the host read)
+        pr.beta = lane < (HR && it.part == 1 ? p.T_rows : T) ? load_scalar(xb, p.bf16, bi) : 0.f;
     }
 }
 
@@ -866,6 +862,14 @@ __device__ void prologue_warp(const ScanParams &p, const Layout &lay, unsigned c
             }
         } else {
             gate_stream(lay, stg, si, sc, pr, T, lane);
+            if (HR && it.part == 1 && lane < p.T_rows) {  // the device copy of the raw beta
+                const size_t bi = (static_cast<size_t>(x.lb) * p.T_rows + lane) * p.H + x.h;
+                const uint32_t bits = __float_as_uint(pr.beta);  // bf16 widened exactly: its top half
+                if (p.bf16)
+                    static_cast<uint16_t *>(p.copy_beta)[bi] = static_cast<uint16_t>(bits >> 16);
+                else
+                    static_cast<uint32_t *>(p.copy_beta)[bi] = bits;
+            }
         }
         mbar_arrive(c.bar(B_SI_FULL + b));
         // the raw rows of item i + nstg into the stage this warp is done with (before the
