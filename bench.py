@@ -44,10 +44,10 @@ FALLBACK_HBM_GBS = 6800.0
 # launch.  TRAFFIC_SOURCE is the hash of kda_scan.cu (code
 # only: comments and blank space removed) the captures were taken on; with any other
 # source the traffic is reported as null.
-TRAFFIC_SOURCE = "4f4e2354f086c424e5230ea472c11dd0fba30fb502264f8ae488cdfe7ca754ba"
-TRAFFIC_BYTES = {"stack34": (205_133_312 + 266_716_160, 516_995_840),
-                 "batched32": (213_603_328 + 258_101_504, 512_188_800),
-                 "stress64x34": (13_886_914_816 + 18_721_277_696, 31_932_887_040)}
+TRAFFIC_SOURCE = "4210bf2b757b85d42b500a53fa83fda9836cbd789d37a1bbbe01722c582abe9f"
+TRAFFIC_BYTES = {"stack34": (205_133_056 + 266_830_080, 516_995_840),
+                 "batched32": (213_674_496 + 258_313_984, 512_188_800),
+                 "stress64x34": (13_887_103_232 + 18_720_913_664, 31_932_887_040)}
 SCAN_SOURCE = os.path.join(ROOT, "speculative_decode_verify_kda_gb300", "csrc", "kda_scan.cu")
 
 

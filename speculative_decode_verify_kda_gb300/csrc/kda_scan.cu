@@ -519,26 +519,23 @@ __device__ void issue_stream(const ScanParams &p, const Layout &lay, uint32_t st
     const int lb = static_cast<int>(fdiv(static_cast<uint32_t>(it.u), p.divH)), h = it.u - lb * p.H;
     const uint32_t rb = static_cast<uint32_t>(lay.row_bytes());
     if (HR && it.part == 1) {
-        // rows in host memory: each lane copies its 8 (bf16) or 16 (f32) bytes of every
-        // row with an asynchronous copy the barrier tracks (the copy engine of the SM
-        // reads host memory like global memory), once the device copy of the stage's
-        // previous item has read the stage
+        // rows in host memory: asynchronous 16-byte copies per lane that the barrier
+        // tracks (the SM reads host memory like global memory), once the device copy of
+        // the stage's previous item has read the stage
         if (lane == 0)
             bulk_wait_read();
         __syncwarp();
-        const uint32_t cb = rb / 32;
+        // 16 bytes a lane: a bf16 row (256 bytes) is half a warp, so a warp copies two rows
+        // an instruction
+        const int lpr = static_cast<int>(rb / 16);  // lanes a row: 16 (bf16) or 32 (f32)
+        const int sub = lane % lpr, r0 = lane / lpr, rstep = 32 / lpr;
         const char *base = static_cast<const char *>(s == 0 ? p.xq : s == 1 ? p.xk : s == 2 ? p.xv : p.xg);
-        const char *src = base + (static_cast<size_t>(lb) * p.T_rows * p.H + h) * rb + lane * cb;
+        const char *src = base + (static_cast<size_t>(lb) * p.T_rows * p.H + h) * rb + sub * 16;
         const size_t pitch = static_cast<size_t>(p.H) * rb;
-        const uint32_t dst = stg + s * lay.tcap * rb + lane * cb;
-        for (int t = 0; t < p.T_rows; ++t) {
-            if (cb == 16)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + t * rb), "l"(src + t * pitch)
-                             : "memory");
-            else
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst + t * rb), "l"(src + t * pitch)
-                             : "memory");
-        }
+        const uint32_t dst = stg + s * lay.tcap * rb + sub * 16;
+        for (int t = r0; t < p.T_rows; t += rstep)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + t * rb), "l"(src + t * pitch)
+                         : "memory");
         asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
         __syncwarp();
         if (lane == 0)
