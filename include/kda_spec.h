@@ -27,12 +27,14 @@
  *   glm_spec.rs, glm5_verify_rows (t <= 15: the decode-exact cap)
  *
  * Conventions for every entry point:
- *   - All tensor pointers are DEVICE pointers owned by the caller (the one
- *     exception: the source of kda_upload_rows_staged, host memory); the library
- *     keeps none of them past the call except through the kda_stash it fills.
- *   - Every call is asynchronous on `stream` and never synchronises.
- *   - The library allocates no memory.  spec_accept and spec_accept_sampled take
- *     caller scratch.
+ *   - All tensor pointers are DEVICE pointers owned by the caller (the exceptions,
+ *     pinned host memory: the source of kda_upload_rows_staged, the host rows of
+ *     kda_verify_scan_deferred_host and the host buffers of kda_round_host); the
+ *     library keeps none of them past the call except through the kda_stash it fills.
+ *   - Every call is asynchronous on `stream` and never synchronises (the exception:
+ *     kda_round_host, which waits for the round's results when asked to).
+ *   - The library allocates no device memory.  spec_accept_sampled takes caller
+ *     scratch; spec_accept ignores its scratch arguments.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns KDA_EINVAL and enqueues nothing.  The reason is kept
  *     per thread for kda_last_error().
