@@ -839,8 +839,9 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         for i in range(3):
             col_step(i, evc[Kc + i])
         barrier()
-        for i in range(Kc):
-            col_step(i, evc[i])
+        with nvtx_range("col_stash"):
+            for i in range(Kc):
+                col_step(i, evc[i])
         barrier()
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the column-stash steps")
@@ -936,8 +937,9 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         for i in range(3):
             var_step(i % R, evv[Kv + i])
         barrier()
-        for i in range(Kv):
-            var_step(i % R, evv[i])
+        with nvtx_range("var_t"):
+            for i in range(Kv):
+                var_step(i % R, evv[i])
         barrier()
         if int(status.item()):
             raise RuntimeError(f"device status {int(status.item()):#x} after the variable-T steps")
