@@ -26,7 +26,9 @@
 // Two launches.  Every reduction and scan runs in a fixed order (or on integers), so
 // the results are reproducible bit for bit.
 //   1. row_stats_kernel, one CTA per (session, row) of the 2T-1 target and draft
-//      rows: max, S, an exact radix select of the k-th largest logit (four 8-bit
+//      rows (or, when the rows' clusters fit on the GPU at once, a cluster of 8 CTAs a
+//      row, each over a slice, merging its integer bins and sums across the cluster
+//      so that every CTA takes the same decisions): max, S, an exact radix select of the k-th largest logit (four 8-bit
 //      count passes over order-preserving keys), the top-p threshold by four 8-bit
 //      passes of e-mass histograms (fixed-point integer sums, per-warp bins) that
 //      find the key at which the descending running sum reaches top_p * S, then
@@ -34,6 +36,7 @@
 //      which read 16-byte vectors.
 //   2. walk_kernel, one CTA per session: the accept tests from the row statistics,
 //      then one pass for the total weight of the final draw and one scan for it.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -84,6 +87,10 @@ struct RowShared {
     int kk, done;
     unsigned long long above;
     RowStats rs;
+    // a row shared by a cluster: each CTA's part of a reduction, read by every CTA
+    float cmax;
+    int cnan;
+    unsigned long long csum;
 };
 
 struct WalkShared {
@@ -207,14 +214,33 @@ __device__ float block_max(float *red, float x)
     return t;
 }
 
-// f(v, x) for every element of the row; each thread takes whole 16-byte vectors
-// (8 bf16 or 4 f32 logits) in a fixed order where the row allows it.
-template <class F>
+__device__ __forceinline__ int row_chunks(const SampArgs &a);
+
+// The chunks of a row that CTA `rank` of a cluster of CL takes (all of them when CL = 1).
+template <int CL>
+__device__ __forceinline__ void slice_of(const SampArgs &a, int &c0, int &c1)
+{
+    const int nc = row_chunks(a);
+    if (CL == 1) {
+        c0 = 0;
+        c1 = nc;
+        return;
+    }
+    const int rank = static_cast<int>(cooperative_groups::this_cluster().block_rank());
+    c0 = static_cast<int>(static_cast<long long>(nc) * rank / CL);
+    c1 = static_cast<int>(static_cast<long long>(nc) * (rank + 1) / CL);
+}
+
+// f(v, x) for every element of the CTA's slice of the row; each thread takes whole
+// 16-byte vectors (8 bf16 or 4 f32 logits) in a fixed order where the row allows it.
+template <int CL, class F>
 __device__ __forceinline__ void for_row(const SampArgs &a, const void *row, F f)
 {
+    int c0, c1;
+    slice_of<CL>(a, c0, c1);
     if (a.vec && a.bf16) {
         const uint4 *r = static_cast<const uint4 *>(row);
-        for (int c = threadIdx.x; c < a.V / 8; c += SNT) {
+        for (int c = c0 + threadIdx.x; c < c1; c += SNT) {
             const uint4 u = __ldg(r + c);
             const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -225,7 +251,7 @@ __device__ __forceinline__ void for_row(const SampArgs &a, const void *row, F f)
         }
     } else if (a.vec) {
         const float4 *r = static_cast<const float4 *>(row);
-        for (int c = threadIdx.x; c < a.V / 4; c += SNT) {
+        for (int c = c0 + threadIdx.x; c < c1; c += SNT) {
             const float4 u = __ldg(r + c);
             f(4 * c, u.x);
             f(4 * c + 1, u.y);
@@ -233,9 +259,86 @@ __device__ __forceinline__ void for_row(const SampArgs &a, const void *row, F f)
             f(4 * c + 3, u.w);
         }
     } else {
-        for (int v = threadIdx.x; v < a.V; v += SNT)
+        for (int v = c0 + threadIdx.x; v < c1; v += SNT)
             f(v, load_x(row, a.bf16, v));
     }
+}
+
+// ---- reductions over the CTAs of a cluster that share a row ------------------------
+// Each CTA publishes its part in its own shared memory; after a cluster barrier every CTA
+// reads all parts in rank order, so every CTA holds the same (exact or order-fixed)
+// result; a second barrier keeps the parts until all have been read.
+template <int CL>
+__device__ __forceinline__ void cluster_barrier()
+{
+    if (CL > 1)
+        cooperative_groups::this_cluster().sync();
+}
+
+template <int CL>
+__device__ float cluster_max(RowShared &sh, float x)
+{
+    if (CL == 1)
+        return x;
+    auto cl = cooperative_groups::this_cluster();
+    if (threadIdx.x == 0)
+        sh.cmax = x;
+    cl.sync();
+    float m = -INFINITY;
+    for (int r = 0; r < CL; ++r)
+        m = fmaxf(m, *cl.map_shared_rank(&sh.cmax, r));
+    cl.sync();
+    return m;
+}
+
+template <int CL>
+__device__ int cluster_or(RowShared &sh, int x)
+{
+    if (CL == 1)
+        return x;
+    auto cl = cooperative_groups::this_cluster();
+    if (threadIdx.x == 0)
+        sh.cnan = x;
+    cl.sync();
+    int o = 0;
+    for (int r = 0; r < CL; ++r)
+        o |= *cl.map_shared_rank(&sh.cnan, r);
+    cl.sync();
+    return o;
+}
+
+template <int CL>
+__device__ unsigned long long cluster_sum(RowShared &sh, unsigned long long x)
+{
+    if (CL == 1)
+        return x;
+    auto cl = cooperative_groups::this_cluster();
+    if (threadIdx.x == 0)
+        sh.csum = x;
+    cl.sync();
+    unsigned long long t = 0;
+    for (int r = 0; r < CL; ++r)
+        t += *cl.map_shared_rank(&sh.csum, r);
+    cl.sync();
+    return t;
+}
+
+// bins[0..256) of every CTA of the cluster summed into out[0..256) of each (integer sums);
+// the caller's bins are complete (a barrier of this CTA precedes the call)
+template <int CL, class U>
+__device__ void cluster_bins(U *bins, U *out)
+{
+    if (CL == 1)
+        return;
+    auto cl = cooperative_groups::this_cluster();
+    cl.sync();
+    for (int i = threadIdx.x; i < 256; i += SNT) {
+        U t = 0;
+        for (int r = 0; r < CL; ++r)
+            t += cl.map_shared_rank(bins, r)[i];
+        out[i] = t;
+    }
+    cl.sync();
 }
 
 // The same traversal as for_row, chunk by chunk: chunk c of the row into xs[0..n), the
@@ -270,6 +373,7 @@ __device__ __forceinline__ int load_chunk(const SampArgs &a, const void *row, in
 }
 
 // The key of the k-th largest logit of the row (k >= 1, k <= V), by four 8-bit count passes.
+template <int CL>
 __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void *row, int k)
 {
     if (threadIdx.x == 0) {
@@ -287,8 +391,9 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
         // bin in a register and add each run once
         int cur = -1;
         unsigned run = 0;
-        const int nc = row_chunks(a);
-        for (int c = threadIdx.x; c < nc; c += SNT) {
+        int c0, c1;
+        slice_of<CL>(a, c0, c1);
+        for (int c = c0 + threadIdx.x; c < c1; c += SNT) {
             float xs[8];
             const int n = load_chunk(a, row, c, xs);
             for (int i = 0; i < n; ++i) {
@@ -308,12 +413,18 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
         if (cur >= 0)
             atomicAdd(&sh.hist[cur], run);
         __syncthreads();
+        // a cluster's row: the counts of every slice (into the spare e-mass bins)
+        if (CL > 1) {
+            cluster_bins<CL>(sh.hist, reinterpret_cast<unsigned *>(&sh.tot[0]));
+            __syncthreads();
+        }
         if (threadIdx.x < 32) {  // warp 0: the bin holding the kk-th largest, from the top
             const int lane = threadIdx.x;
             unsigned c[8], tot = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                c[i] = sh.hist[255 - (8 * lane + i)];
+                c[i] = CL > 1 ? reinterpret_cast<const unsigned *>(&sh.tot[0])[255 - (8 * lane + i)]
+                              : sh.hist[255 - (8 * lane + i)];
                 tot += c[i];
             }
             unsigned incl = tot;  // inclusive prefix over lanes (bins counted from the top)
@@ -354,6 +465,7 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
 // already passed).  Only keys >= floor take part (the k-th largest key under top_k):
 // when their whole mass stays below the target, the top-p threshold lies under the
 // top-k one and floor is returned.
+template <int CL>
 __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, float m, double target,
                              unsigned floor)
 {
@@ -373,8 +485,9 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
         // runs of one bin summed in a register (integer sums: the order does not matter)
         int cur = -1;
         unsigned long long run = 0;
-        const int nc = row_chunks(a);
-        for (int c = threadIdx.x; c < nc; c += SNT) {
+        int c0, c1;
+        slice_of<CL>(a, c0, c1);
+        for (int c = c0 + threadIdx.x; c < c1; c += SNT) {
             float xs[8];
             const int n = load_chunk(a, row, c, xs);
             for (int i = 0; i < n; ++i) {
@@ -401,6 +514,13 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
             sh.tot[d] = t;
         }
         __syncthreads();
+        if (CL > 1) {  // a cluster's row: the mass of every slice (into warp 0's bins)
+            cluster_bins<CL>(sh.tot, &sh.hw[0][0]);
+            __syncthreads();
+            for (int d = threadIdx.x; d < 256; d += SNT)
+                sh.tot[d] = sh.hw[0][d];
+            __syncthreads();
+        }
         if (threadIdx.x < 32) {
             const int lane = threadIdx.x;
             const unsigned long long above = sh.above;
@@ -461,18 +581,20 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
     return sh.prefix;
 }
 
-// Filter statistics of one row into sh.rs.
+// Filter statistics of one row into sh.rs (CL > 1: the row shared by the CTAs of a
+// cluster, each taking a slice; every CTA ends with the same statistics).
+template <int CL>
 __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
 {
     float mx = -INFINITY;
     int nan = 0;
-    for_row(a, row, [&](int, float x) {
+    for_row<CL>(a, row, [&](int, float x) {
         const float z = __fdiv_rn(x, a.temperature);
         nan |= z != z;
         mx = fmaxf(mx, z);
     });
-    nan = __syncthreads_or(nan);
-    const float m = block_max(sh.red, mx);
+    nan = cluster_or<CL>(sh, __syncthreads_or(nan));
+    const float m = cluster_max<CL>(sh, block_max(sh.red, mx));
     if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
         if (threadIdx.x == 0)
             sh.rs = RowStats{m, 0.f, 0.0, 1, {0, 0, 0}};
@@ -482,25 +604,25 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
     float th = 0.f;
     unsigned floor = 0;  // the k-th largest key: top-p looks no lower
     if (a.top_k > 0 && a.top_k < a.V) {
-        floor = kth_largest_key(sh, a, row, a.top_k);
+        floor = kth_largest_key<CL>(sh, a, row, a.top_k);
         th = e_of(unkey(floor), m, a.temperature);
     }
     if (a.top_p < 1.0f) {
         unsigned long long s = 0;
-        for_row(a, row, [&](int, float x) { s += fx(e_of(x, m, a.temperature)); });
-        const unsigned long long S = block_sum_u64(sh.ured, s);
+        for_row<CL>(a, row, [&](int, float x) { s += fx(e_of(x, m, a.temperature)); });
+        const unsigned long long S = cluster_sum<CL>(sh, block_sum_u64(sh.ured, s));
         const double target = static_cast<double>(a.top_p) * static_cast<double>(S);
-        th = fmaxf(th, e_of(unkey(topp_key(sh, a, row, m, target, floor)), m, a.temperature));
+        th = fmaxf(th, e_of(unkey(topp_key<CL>(sh, a, row, m, target, floor)), m, a.temperature));
     }
     if (a.min_p > 0.f)
         th = fmaxf(th, a.min_p);
     unsigned long long z = 0;
-    for_row(a, row, [&](int, float x) {
+    for_row<CL>(a, row, [&](int, float x) {
         const float e = e_of(x, m, a.temperature);
         if (e >= th)
             z += fx(e);
     });
-    const double Z = static_cast<double>(block_sum_u64(sh.ured, z)) * FX_UNIT;
+    const double Z = static_cast<double>(cluster_sum<CL>(sh, block_sum_u64(sh.ured, z))) * FX_UNIT;
     if (threadIdx.x == 0)
         sh.rs = RowStats{m, th, Z, 0, {0, 0, 0}};
     __syncthreads();
@@ -514,20 +636,37 @@ __device__ __forceinline__ float prob32(const RowStats &r, float x, float temper
 }
 
 // Row ri of session b: target row ri (ri < T) or draft row ri - T.
+__device__ __forceinline__ const void *stats_row(const SampArgs &a, int rowi)
+{
+    const int nr = 2 * a.T - 1;
+    const int b = rowi / nr, ri = rowi % nr;
+    const int K = a.T - 1;
+    const size_t es = a.bf16 ? 2 : 4;
+    return ri < a.T ? static_cast<const unsigned char *>(a.logits) + (static_cast<size_t>(b) * a.T + ri) * a.V * es
+                    : static_cast<const unsigned char *>(a.draft_logits) +
+                          (static_cast<size_t>(b) * K + (ri - a.T)) * a.V * es;
+}
+
+// One CTA a row (many rows: the GPU is full).
 __global__ void __launch_bounds__(SNT) row_stats_kernel(const SampArgs a, RowStats *__restrict__ stats)
 {
     __shared__ RowShared sh;
-    const int nr = 2 * a.T - 1;
-    const int b = blockIdx.x / nr, ri = blockIdx.x % nr;
-    const int K = a.T - 1;
-    const size_t es = a.bf16 ? 2 : 4;
-    const unsigned char *row =
-        ri < a.T ? static_cast<const unsigned char *>(a.logits) + (static_cast<size_t>(b) * a.T + ri) * a.V * es
-                 : static_cast<const unsigned char *>(a.draft_logits) +
-                       (static_cast<size_t>(b) * K + (ri - a.T)) * a.V * es;
-    row_stats(sh, a, row);
+    row_stats<1>(sh, a, stats_row(a, blockIdx.x));
     if (threadIdx.x == 0)
         stats[blockIdx.x] = sh.rs;
+}
+
+// A cluster of SCL CTAs a row, each over a slice of it (few rows: one CTA a row would
+// leave most SMs idle and run every pass of the row on one).
+constexpr int SCL = 8;
+__global__ void __cluster_dims__(SCL, 1, 1) __launch_bounds__(SNT, 1)
+    row_stats_cluster_kernel(const SampArgs a, RowStats *__restrict__ stats)
+{
+    __shared__ RowShared sh;
+    const int rowi = blockIdx.x / SCL;
+    row_stats<SCL>(sh, a, stats_row(a, rowi));
+    if (threadIdx.x == 0 && cooperative_groups::this_cluster().block_rank() == 0)
+        stats[rowi] = sh.rs;
 }
 
 __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowStats *__restrict__ stats)
@@ -776,9 +915,24 @@ int sampled_common(const void *logits, const void *draft_logits, int logit_dtype
     const size_t row_bytes = static_cast<size_t>(V) * (a.bf16 ? 2 : 4);
     a.vec = aligned16(logits) && (T == 1 || aligned16(draft_logits)) && row_bytes % 16 == 0;
     RowStats *stats = static_cast<RowStats *>(scratch);
-    row_stats_kernel<<<static_cast<unsigned>(B * (2 * T - 1)), SNT, 0, stream>>>(a, stats);
-    if ((rc = check_launch("row_stats_kernel")))
-        return rc;
+    const long long rows = static_cast<long long>(B) * (2 * T - 1);
+    int sms = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        return fail(KDA_ECUDA, "cudaDeviceGetAttribute(cudaDevAttrMultiProcessorCount) failed");
+    // few rows (every cluster resident at once): a cluster of CTAs a row; measured on
+    // GB300 at V = 32768, 15 rows 84.5 -> 62.1 us, while 60 rows (3 waves of clusters)
+    // ran 94.8 -> 140 us, so more rows keep one CTA a row
+    if (rows * SCL <= sms) {
+        row_stats_cluster_kernel<<<static_cast<unsigned>(rows * SCL), SNT, 0, stream>>>(a, stats);
+        if ((rc = check_launch("row_stats_cluster_kernel")))
+            return rc;
+    } else {
+        row_stats_kernel<<<static_cast<unsigned>(rows), SNT, 0, stream>>>(a, stats);
+        if ((rc = check_launch("row_stats_kernel")))
+            return rc;
+    }
     walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
     return check_launch("walk_kernel");
 }

@@ -98,6 +98,34 @@ def test_sampled_accept_against_oracle(orc, fi, V, bf16, ties):
     assert len(seen_j) >= 3, "the case should exercise several accept lengths"
 
 
+@pytest.mark.parametrize("fi", range(len(FILTERS)))
+@pytest.mark.parametrize("V,bf16,ties", [(300, False, False), (32768, True, False), (32768, True, True)])
+def test_sampled_accept_few_rows_against_oracle(orc, fi, V, bf16, ties):
+    """One session of T = 8 (15 rows): each row's statistics come from a cluster of CTAs
+    sharing the row (few rows leave the GPU room for them); the result must equal the
+    oracle's exactly, as with one CTA a row."""
+    filt = FILTERS[fi]
+    seen_j = set()
+    for case in range(8):
+        rng = np.random.default_rng(5000 + 97 * fi + 13 * case + V % 5 + ties)
+        P, Q, d, ua, us = _case(rng, 1, 8, V, orc, filt, bf16, ties)
+        if case % 2:
+            # the draft rows equal the target rows: every draft passes, the bonus comes
+            # from the target's last row
+            Q = P[:, :7].copy()
+            for r in range(7):
+                pt = orc.filtered(P[0, r], **f32(filt))
+                d[0, r] = rng.choice(V, p=pt / pt.sum())
+        j, tok, keep = kb.spec_accept_sampled(to_dev(P, bf16), to_dev(Q, bf16), to_dev(d), to_dev(ua), to_dev(us),
+                                              **filt)
+        torch.cuda.synchronize()
+        want = orc.sampled_accept(P[0], Q[0], d[0], ua[0], float(us[0]), **f32(filt))
+        assert (int(j[0]), int(tok[0])) == want, (case, (int(j[0]), int(tok[0])), want)
+        assert int(keep[0]) == int(j[0]) + 1
+        seen_j.add(want[0])
+    assert len(seen_j) >= 2, "the cases should exercise several accept lengths"
+
+
 def test_top_p_with_thousands_of_ties(orc):
     """Rows whose top-p boundary falls inside a tie group of more than 1024 tokens: the
     kept set takes the whole group, on the device as in the oracle."""
