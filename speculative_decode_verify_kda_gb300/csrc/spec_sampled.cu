@@ -80,17 +80,21 @@ static_assert(sizeof(RowStats) == 32, "row statistics are 32 bytes in scratch");
 struct RowShared {
     float red[SNW];
     unsigned long long ured[SNW];
-    unsigned hist[256];
+    unsigned hist[2][256];            // counts of one radix pass (alternate passes alternate)
     unsigned long long hw[SNW][256];  // per-warp e-mass bins of one radix pass
     unsigned long long tot[256];
     unsigned prefix;
     int kk, done;
     unsigned long long above;
     RowStats rs;
-    // a row shared by a cluster: each CTA's part of a reduction, read by every CTA
+    // a row shared by a cluster: each CTA's part of a reduction, read by every CTA.  Each
+    // scalar slot is written once; the bins alternate between two slots, so a slot is
+    // written again only after a later cluster barrier, which every CTA reaches after its
+    // reads of the slot: no second barrier per reduction.
     float cmax;
     int cnan;
-    unsigned long long csum;
+    unsigned long long csum[2];
+    unsigned long long pub[2][256];
 };
 
 struct WalkShared {
@@ -267,66 +271,51 @@ __device__ __forceinline__ void for_row(const SampArgs &a, const void *row, F f)
 // ---- reductions over the CTAs of a cluster that share a row ------------------------
 // Each CTA publishes its part in its own shared memory; after a cluster barrier every CTA
 // reads all parts in rank order, so every CTA holds the same (exact or order-fixed)
-// result; a second barrier keeps the parts until all have been read.
-template <int CL>
-__device__ __forceinline__ void cluster_barrier()
-{
-    if (CL > 1)
-        cooperative_groups::this_cluster().sync();
-}
+// result.  A published slot is not written again before a later barrier (see RowShared),
+// and the kernel ends with a barrier, so no CTA leaves while another reads its parts.
 
+// the NaN flag and the maximum of the row, in one exchange
 template <int CL>
-__device__ float cluster_max(RowShared &sh, float x)
+__device__ void cluster_or_max(RowShared &sh, int &nan, float &m)
 {
     if (CL == 1)
-        return x;
+        return;
     auto cl = cooperative_groups::this_cluster();
-    if (threadIdx.x == 0)
-        sh.cmax = x;
-    cl.sync();
-    float m = -INFINITY;
-    for (int r = 0; r < CL; ++r)
-        m = fmaxf(m, *cl.map_shared_rank(&sh.cmax, r));
-    cl.sync();
-    return m;
-}
-
-template <int CL>
-__device__ int cluster_or(RowShared &sh, int x)
-{
-    if (CL == 1)
-        return x;
-    auto cl = cooperative_groups::this_cluster();
-    if (threadIdx.x == 0)
-        sh.cnan = x;
+    if (threadIdx.x == 0) {
+        sh.cnan = nan;
+        sh.cmax = m;
+    }
     cl.sync();
     int o = 0;
-    for (int r = 0; r < CL; ++r)
+    float x = -INFINITY;
+    for (int r = 0; r < CL; ++r) {
         o |= *cl.map_shared_rank(&sh.cnan, r);
-    cl.sync();
-    return o;
+        x = fmaxf(x, *cl.map_shared_rank(&sh.cmax, r));
+    }
+    nan = o;
+    m = x;
 }
 
+// slot: 0 or 1, each used once per row
 template <int CL>
-__device__ unsigned long long cluster_sum(RowShared &sh, unsigned long long x)
+__device__ unsigned long long cluster_sum(RowShared &sh, unsigned long long x, int slot)
 {
     if (CL == 1)
         return x;
     auto cl = cooperative_groups::this_cluster();
     if (threadIdx.x == 0)
-        sh.csum = x;
+        sh.csum[slot] = x;
     cl.sync();
     unsigned long long t = 0;
     for (int r = 0; r < CL; ++r)
-        t += *cl.map_shared_rank(&sh.csum, r);
-    cl.sync();
+        t += *cl.map_shared_rank(&sh.csum[slot], r);
     return t;
 }
 
-// bins[0..256) of every CTA of the cluster summed into out[0..256) of each (integer sums);
-// the caller's bins are complete (a barrier of this CTA precedes the call)
+// bins[0..256) of every CTA of the cluster summed into out[0..256) of each (integer
+// sums); the caller's bins are complete, and stay unwritten until the next barrier
 template <int CL, class U>
-__device__ void cluster_bins(U *bins, U *out)
+__device__ void cluster_bins(const U *bins, U *out)
 {
     if (CL == 1)
         return;
@@ -338,7 +327,14 @@ __device__ void cluster_bins(U *bins, U *out)
             t += cl.map_shared_rank(bins, r)[i];
         out[i] = t;
     }
-    cl.sync();
+}
+
+// The low 16 bits of the keys of bf16 logits: zero for a positive value, all ones for a
+// negative one (the key complements a negative float).  Keys that share their top 16 bits
+// are then the same key, so the two low radix passes of a bf16 row are skipped.
+__device__ __forceinline__ unsigned bf16_key_low(unsigned prefix)
+{
+    return (prefix & 0x80000000u) ? 0u : 0xffffu;
 }
 
 // The same traversal as for_row, chunk by chunk: chunk c of the row into xs[0..n), the
@@ -381,10 +377,12 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
         sh.kk = k;
     }
     unsigned mask = 0;
-    for (int pass = 0; pass < 4; ++pass) {
+    const int passes = a.bf16 ? 2 : 4;
+    for (int pass = 0; pass < passes; ++pass) {
         const int shift = 24 - 8 * pass;
+        unsigned *hist = sh.hist[pass & 1];
         for (int i = threadIdx.x; i < 256; i += SNT)
-            sh.hist[i] = 0;
+            hist[i] = 0;
         __syncthreads();
         const unsigned prefix = sh.prefix;
         // a thread's consecutive elements mostly share the top bytes: count runs of one
@@ -403,7 +401,7 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
                 const int bin = static_cast<int>((key >> shift) & 255u);
                 if (bin != cur) {
                     if (cur >= 0)
-                        atomicAdd(&sh.hist[cur], run);
+                        atomicAdd(&hist[cur], run);
                     cur = bin;
                     run = 0;
                 }
@@ -411,11 +409,11 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
             }
         }
         if (cur >= 0)
-            atomicAdd(&sh.hist[cur], run);
+            atomicAdd(&hist[cur], run);
         __syncthreads();
         // a cluster's row: the counts of every slice (into the spare e-mass bins)
         if (CL > 1) {
-            cluster_bins<CL>(sh.hist, reinterpret_cast<unsigned *>(&sh.tot[0]));
+            cluster_bins<CL>(static_cast<const unsigned *>(hist), reinterpret_cast<unsigned *>(&sh.tot[0]));
             __syncthreads();
         }
         if (threadIdx.x < 32) {  // warp 0: the bin holding the kk-th largest, from the top
@@ -424,7 +422,7 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 c[i] = CL > 1 ? reinterpret_cast<const unsigned *>(&sh.tot[0])[255 - (8 * lane + i)]
-                              : sh.hist[255 - (8 * lane + i)];
+                              : hist[255 - (8 * lane + i)];
                 tot += c[i];
             }
             unsigned incl = tot;  // inclusive prefix over lanes (bins counted from the top)
@@ -453,7 +451,7 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
         mask |= 255u << shift;
         __syncthreads();
     }
-    return sh.prefix;
+    return a.bf16 ? sh.prefix | bf16_key_low(sh.prefix) : sh.prefix;
 }
 
 // The key of the top-p boundary: the largest key kappa whose mass F(kappa) = sum of e
@@ -476,7 +474,8 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
         sh.done = 0;
     }
     unsigned mask = 0;
-    for (int pass = 0; pass < 4; ++pass) {
+    const int passes = a.bf16 ? 2 : 4;
+    for (int pass = 0; pass < passes; ++pass) {
         const int shift = 24 - 8 * pass;
         for (int i = threadIdx.x; i < SNW * 256; i += SNT)
             (&sh.hw[0][0])[i] = 0;
@@ -507,18 +506,17 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
         if (cur >= 0)
             atomicAdd(&sh.hw[w][cur], run);
         __syncthreads();
+        // the CTA's bins (a cluster's row: published, then the bins of every slice summed)
+        unsigned long long *mine = CL > 1 ? sh.pub[pass & 1] : sh.tot;
         for (int d = threadIdx.x; d < 256; d += SNT) {
             unsigned long long t = 0;
             for (int i = 0; i < SNW; ++i)
                 t += sh.hw[i][d];
-            sh.tot[d] = t;
+            mine[d] = t;
         }
         __syncthreads();
-        if (CL > 1) {  // a cluster's row: the mass of every slice (into warp 0's bins)
-            cluster_bins<CL>(sh.tot, &sh.hw[0][0]);
-            __syncthreads();
-            for (int d = threadIdx.x; d < 256; d += SNT)
-                sh.tot[d] = sh.hw[0][d];
+        if (CL > 1) {
+            cluster_bins<CL>(static_cast<const unsigned long long *>(mine), sh.tot);
             __syncthreads();
         }
         if (threadIdx.x < 32) {
@@ -576,9 +574,10 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
         mask |= 255u << shift;
         __syncthreads();
         if (sh.done)
-            break;
+            return sh.prefix;
     }
-    return sh.prefix;
+    // (a chosen group always holds mass, so a bf16 row's low passes would pick its one key)
+    return a.bf16 ? sh.prefix | bf16_key_low(sh.prefix) : sh.prefix;
 }
 
 // Filter statistics of one row into sh.rs (CL > 1: the row shared by the CTAs of a
@@ -593,8 +592,9 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
         nan |= z != z;
         mx = fmaxf(mx, z);
     });
-    nan = cluster_or<CL>(sh, __syncthreads_or(nan));
-    const float m = cluster_max<CL>(sh, block_max(sh.red, mx));
+    nan = __syncthreads_or(nan);
+    float m = block_max(sh.red, mx);
+    cluster_or_max<CL>(sh, nan, m);
     if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
         if (threadIdx.x == 0)
             sh.rs = RowStats{m, 0.f, 0.0, 1, {0, 0, 0}};
@@ -610,7 +610,7 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
     if (a.top_p < 1.0f) {
         unsigned long long s = 0;
         for_row<CL>(a, row, [&](int, float x) { s += fx(e_of(x, m, a.temperature)); });
-        const unsigned long long S = cluster_sum<CL>(sh, block_sum_u64(sh.ured, s));
+        const unsigned long long S = cluster_sum<CL>(sh, block_sum_u64(sh.ured, s), 0);
         const double target = static_cast<double>(a.top_p) * static_cast<double>(S);
         th = fmaxf(th, e_of(unkey(topp_key<CL>(sh, a, row, m, target, floor)), m, a.temperature));
     }
@@ -622,7 +622,7 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
         if (e >= th)
             z += fx(e);
     });
-    const double Z = static_cast<double>(cluster_sum<CL>(sh, block_sum_u64(sh.ured, z))) * FX_UNIT;
+    const double Z = static_cast<double>(cluster_sum<CL>(sh, block_sum_u64(sh.ured, z), 1)) * FX_UNIT;
     if (threadIdx.x == 0)
         sh.rs = RowStats{m, th, Z, 0, {0, 0, 0}};
     __syncthreads();
@@ -665,8 +665,10 @@ __global__ void __cluster_dims__(SCL, 1, 1) __launch_bounds__(SNT, 1)
     __shared__ RowShared sh;
     const int rowi = blockIdx.x / SCL;
     row_stats<SCL>(sh, a, stats_row(a, rowi));
-    if (threadIdx.x == 0 && cooperative_groups::this_cluster().block_rank() == 0)
+    auto cl = cooperative_groups::this_cluster();
+    if (threadIdx.x == 0 && cl.block_rank() == 0)
         stats[rowi] = sh.rs;
+    cl.sync();  // the CTA's published parts stay until every CTA has read them
 }
 
 __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowStats *__restrict__ stats)

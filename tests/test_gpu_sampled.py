@@ -126,6 +126,31 @@ def test_sampled_accept_few_rows_against_oracle(orc, fi, V, bf16, ties):
     assert len(seen_j) >= 2, "the cases should exercise several accept lengths"
 
 
+@pytest.mark.parametrize("B", [1, 12])
+@pytest.mark.parametrize("fi", [1, 2, 5, 6])
+@pytest.mark.parametrize("V,bf16", [(300, False), (32768, True)])
+def test_negative_logits_against_oracle(orc, B, fi, V, bf16):
+    """Every logit below zero: the top-k and top-p boundaries fall on negative values,
+    whose order keys are complemented bit patterns (B = 1: a cluster of CTAs a row;
+    B = 12: one CTA a row)."""
+    filt = FILTERS[fi]
+    rng = np.random.default_rng(7000 + 31 * fi + B + bf16)
+    P, Q, d, ua, us = _case(rng, B, 5, V, orc, filt, False)
+    P, Q = P - 40.0, Q - 40.0
+    if bf16:
+        P, Q = synth.to_bf16_bits(P), synth.to_bf16_bits(Q)
+    for b in range(B):  # drafts drawn again from the shifted draft rows
+        for r in range(4):
+            qt = orc.filtered(Q[b, r], **f32(filt))
+            d[b, r] = rng.choice(V, p=qt / qt.sum())
+    j, tok, _ = kb.spec_accept_sampled(to_dev(P, bf16), to_dev(Q, bf16), to_dev(d), to_dev(ua), to_dev(us),
+                                       **filt)
+    torch.cuda.synchronize()
+    for b in range(B):
+        want = orc.sampled_accept(P[b], Q[b], d[b], ua[b], float(us[b]), **f32(filt))
+        assert (int(j[b]), int(tok[b])) == want, (b, (int(j[b]), int(tok[b])), want)
+
+
 def test_top_p_with_thousands_of_ties(orc):
     """Rows whose top-p boundary falls inside a tie group of more than 1024 tokens: the
     kept set takes the whole group, on the device as in the oracle."""
