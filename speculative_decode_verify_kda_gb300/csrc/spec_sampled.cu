@@ -26,16 +26,19 @@
 // Two launches.  Every reduction and scan runs in a fixed order (or on integers), so
 // the results are reproducible bit for bit.
 //   1. row_stats_kernel, one CTA per (session, row) of the 2T-1 target and draft
-//      rows (or, when the rows' clusters fit on the GPU at once, a cluster of 8 CTAs a
-//      row, each over a slice, merging its integer bins and sums across the cluster
-//      so that every CTA takes the same decisions): max, S, an exact radix select of the k-th largest logit (four 8-bit
-//      count passes over order-preserving keys), the top-p threshold by four 8-bit
-//      passes of e-mass histograms (fixed-point integer sums, per-warp bins) that
-//      find the key at which the descending running sum reaches top_p * S, then
-//      the kept mass Z, into scratch.  The row stays in L1 between its passes,
-//      which read 16-byte vectors.
-//   2. walk_kernel, one CTA per session: the accept tests from the row statistics,
-//      then one pass for the total weight of the final draw and one scan for it.
+//      rows (or, when the rows' clusters fit on the GPU at once, a cluster of 8, 4 or
+//      2 CTAs a row, each over a slice, merging its integer bins and sums across the
+//      cluster so that every CTA takes the same decisions): max, S, an exact radix
+//      select of the k-th largest logit (8-bit count passes over order-preserving
+//      keys: four for f32 rows, two for bf16 rows, whose keys end in 16 fixed bits),
+//      the top-p threshold by as many 8-bit passes of e-mass histograms (fixed-point
+//      integer sums, per-warp bins) that find the key at which the descending running
+//      sum reaches top_p * S, then the kept mass Z, into scratch.  The row stays in
+//      L1 between its passes, which read 16-byte vectors.
+//   2. walk_kernel, one CTA per session (or, for at most a cluster per SM's worth of
+//      sessions, a cluster of 8 CTAs a session, each weighting a slice of the draw's
+//      row): the accept tests from the row statistics, then one pass for the total
+//      weight of the final draw and one scan for it.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -104,6 +107,7 @@ struct WalkShared {
     float u_sample;
     float tu[KDA_TMAX], tp[KDA_TMAX], tq[KDA_TMAX];  // accept test r: its uniform, p~ and q~
     int tcode[KDA_TMAX];                             // 0 ok, 1 a NaN row, 2 draft id outside the vocabulary
+    unsigned long long cw[2];                        // a cluster's session: this slice's residual and p~ weights
 };
 
 // ---- Philox4x32-10 and the session uniforms ---------------------------------------
@@ -656,25 +660,40 @@ __global__ void __launch_bounds__(SNT) row_stats_kernel(const SampArgs a, RowSta
         stats[blockIdx.x] = sh.rs;
 }
 
-// A cluster of SCL CTAs a row, each over a slice of it (few rows: one CTA a row would
+// A cluster of CL CTAs a row, each over a slice of it (few rows: one CTA a row would
 // leave most SMs idle and run every pass of the row on one).
-constexpr int SCL = 8;
-__global__ void __cluster_dims__(SCL, 1, 1) __launch_bounds__(SNT, 1)
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(SNT, 1)
     row_stats_cluster_kernel(const SampArgs a, RowStats *__restrict__ stats)
 {
     __shared__ RowShared sh;
-    const int rowi = blockIdx.x / SCL;
-    row_stats<SCL>(sh, a, stats_row(a, rowi));
+    const int rowi = blockIdx.x / CL;
+    row_stats<CL>(sh, a, stats_row(a, rowi));
     auto cl = cooperative_groups::this_cluster();
     if (threadIdx.x == 0 && cl.block_rank() == 0)
         stats[rowi] = sh.rs;
     cl.sync();  // the CTA's published parts stay until every CTA has read them
 }
 
-__global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowStats *__restrict__ stats)
+// the two halves of a cluster barrier: arrive (release) and wait (acquire)
+__device__ __forceinline__ void cluster_arrive()
 {
-    __shared__ WalkShared sh;
-    const int b = blockIdx.x;
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The walk of session b.  CL > 1: the draw's row shared by a cluster of CL CTAs, each
+// weighting a slice of it.  Every CTA runs the accept tests (the same inputs give the
+// same j), the slices' weight sums are exchanged, and the CTA whose slice holds the
+// draw's target (or, for a target rounded up to the total, the last slice with weight)
+// walks its slice and writes the results.
+template <int CL>
+__device__ void walk_session(WalkShared &sh, const SampArgs &a, const RowStats *__restrict__ stats, int b)
+{
     const int K = a.T - 1, nr = 2 * a.T - 1;
     const size_t es = a.bf16 ? 2 : 4;
     const RowStats *st = stats + static_cast<size_t>(b) * nr;
@@ -683,6 +702,7 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
     const bool session = a.seeds != nullptr;
     const unsigned long long seed = session ? a.seeds[b] : 0ull;
     const uint32_t uctr = session ? a.counters[2 * b] : 0u, sctr = session ? a.counters[2 * b + 1] : 0u;
+    const int rank = CL > 1 ? static_cast<int>(cooperative_groups::this_cluster().block_rank()) : 0;
     // every accept test's inputs at once (thread r: test r), then the walk in order
     if (threadIdx.x < K) {
         const int r = threadIdx.x;
@@ -714,19 +734,27 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
         sh.jsh = j;
         sh.flag = bad;
         sh.u_sample = session ? session_u01(seed, sctr, TAG_DRAW) : a.u_sample[b];
-        if (session) {  // the tests run (j + 1 on a rejection, K when every draft passed), one draw
-            a.counters[2 * b] = uctr + static_cast<uint32_t>(j < K ? j + 1 : K);
-            a.counters[2 * b + 1] = sctr + 1u;
-        }
     }
     __syncthreads();
     const int j = sh.jsh;
+    // the results, by thread 0 of the one CTA that writes them; the counters advance by
+    // the tests run (j + 1 on a rejection, K when every draft passed) and one draw (a
+    // cluster's CTAs have all read them: a cluster barrier precedes every write)
+    auto finish = [&](int token) {
+        a.j_out[b] = j;
+        a.token_out[b] = token;
+        if (a.keep_out)
+            a.keep_out[b] = j + 1;
+        if (session) {
+            a.counters[2 * b] = uctr + static_cast<uint32_t>(j < K ? j + 1 : K);
+            a.counters[2 * b + 1] = sctr + 1u;
+        }
+    };
     if (sh.flag) {
-        if (threadIdx.x == 0) {
-            a.j_out[b] = j;
-            a.token_out[b] = -1;
-            if (a.keep_out)
-                a.keep_out[b] = j + 1;
+        if (CL > 1)
+            cooperative_groups::this_cluster().sync();
+        if (threadIdx.x == 0 && rank == 0) {
+            finish(-1);
             if (a.status)
                 atomicOr(a.status, KDA_ST_NAN);
         }
@@ -748,12 +776,14 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
         const float r = __fsub_rn(ep >= rp.th ? __fmul_rn(ep, ip) : 0.f, eq >= rq.th ? __fmul_rn(eq, iq) : 0.f);
         return r > 0.f ? fx(r) : 0ull;
     };
-    // thread t owns a contiguous run of the row's 16-byte chunks (the for_row chunks):
+    // thread t owns a contiguous run of the slice's 16-byte chunks (the for_row chunks):
     // one pass sums both weight kinds per run; the block's exclusive scan of the run sums
     // finds the run holding the target, and its thread walks it
-    const int nc = row_chunks(a), per = a.vec ? (a.bf16 ? 8 : 4) : 1;
-    const int cs = (nc + SNT - 1) / SNT;
-    const int c0 = threadIdx.x * cs, c1 = min(nc, c0 + cs);
+    const int per = a.vec ? (a.bf16 ? 8 : 4) : 1;
+    int s0, s1;
+    slice_of<CL>(a, s0, s1);
+    const int cs = (s1 - s0 + SNT - 1) / SNT;
+    const int c0 = s0 + threadIdx.x * cs, c1 = min(s1, c0 + cs);
     unsigned long long sr = 0, sp = 0;
     for (int c = c0; c < c1; ++c) {
         float xp[8], xq[8];
@@ -768,80 +798,126 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
                     sr += wr_of(xp[i], xq[i]);
             }
     }
-    const unsigned long long Wr = block_sum_u64(sh.ured, sr);
-    const unsigned long long Wp = block_sum_u64(sh.ured, sp);
+    unsigned long long Wr = block_sum_u64(sh.ured, sr);
+    unsigned long long Wp = block_sum_u64(sh.ured, sp);
+    // the slice's weights, the weight of the slices before it, the last slice with weight
+    unsigned long long cr = Wr, cp = Wp, br = 0, bp = 0;
+    int lr = 0, lp = 0;
+    if (CL > 1) {
+        auto cl = cooperative_groups::this_cluster();
+        if (threadIdx.x == 0) {
+            sh.cw[0] = Wr;
+            sh.cw[1] = Wp;
+        }
+        cl.sync();
+        Wr = Wp = 0;
+        lr = lp = -1;
+        for (int r = 0; r < CL; ++r) {
+            const unsigned long long *o = cl.map_shared_rank(sh.cw, r);
+            const unsigned long long xr = o[0], xq = o[1];
+            if (r < rank) {
+                br += xr;
+                bp += xq;
+            }
+            if (xr)
+                lr = r;
+            if (xq)
+                lp = r;
+            Wr += xr;
+            Wp += xq;
+        }
+        cluster_arrive();  // this CTA has read the parts (the matching wait ends the kernel)
+    }
     const bool use_resid = qrow && Wr > 0;
     const unsigned long long W = use_resid ? Wr : Wp, own = use_resid ? sr : sp;
     // run > u W  <=>  run > floor(u W) for the integer running weights
     const unsigned long long target =
         static_cast<unsigned long long>(static_cast<double>(sh.u_sample) * static_cast<double>(W));
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    unsigned long long incl = own;
+    const unsigned long long base = use_resid ? br : bp, mine = use_resid ? cr : cp;
+    const bool draws = (base <= target && target < base + mine) || (target >= W && rank == (use_resid ? lr : lp));
+    if (draws) {
+        const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        unsigned long long incl = own;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off)
-            incl += y;
-    }
-    __syncthreads();
-    if (lane == 31)
-        sh.ured[wid] = incl;
-    __syncthreads();
-    unsigned long long wbase = 0;
-    for (int i = 0; i < wid; ++i)
-        wbase += sh.ured[i];
-    const unsigned long long excl = wbase + incl - own;
-    if (threadIdx.x == 0)
-        sh.ired[0] = -1;
-    __syncthreads();
-    if (excl <= target && target < excl + own) {  // exactly one thread: the run of the draw
-        unsigned long long run = excl;
-        for (int c = c0, found = 0; c < c1 && !found; ++c) {
-            float xp[8], xq[8];
-            const int n = load_chunk(a, prow, c, xp);
-            if (use_resid)
-                load_chunk(a, qrow, c, xq);
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off)
+                incl += y;
+        }
+        __syncthreads();
+        if (lane == 31)
+            sh.ured[wid] = incl;
+        __syncthreads();
+        unsigned long long wbase = base;
+        for (int i = 0; i < wid; ++i)
+            wbase += sh.ured[i];
+        const unsigned long long excl = wbase + incl - own;
+        if (threadIdx.x == 0)
+            sh.ired[0] = -1;
+        __syncthreads();
+        if (excl <= target && target < excl + own) {  // exactly one thread: the run of the draw
+            unsigned long long run = excl;
+            for (int c = c0, found = 0; c < c1 && !found; ++c) {
+                float xp[8], xq[8];
+                const int n = load_chunk(a, prow, c, xp);
+                if (use_resid)
+                    load_chunk(a, qrow, c, xq);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i < n && !found) {
-                    run += use_resid ? wr_of(xp[i], xq[i]) : wp_of(xp[i]);
-                    if (run > target) {
-                        sh.ired[0] = c * per + i;
-                        found = 1;
+                for (int i = 0; i < 8; ++i)
+                    if (i < n && !found) {
+                        run += use_resid ? wr_of(xp[i], xq[i]) : wp_of(xp[i]);
+                        if (run > target) {
+                            sh.ired[0] = c * per + i;
+                            found = 1;
+                        }
                     }
+            }
+        }
+        __syncthreads();
+        int token = sh.ired[0];
+        if (token < 0) {  // target rounded up to the total: the last token with weight
+            int haswt = -1;
+            if (own > 0)
+                for (int c = c1 - 1; c >= c0 && haswt < 0; --c) {
+                    float xp[8], xq[8];
+                    const int n = load_chunk(a, prow, c, xp);
+                    if (use_resid)
+                        load_chunk(a, qrow, c, xq);
+#pragma unroll
+                    for (int i = 7; i >= 0; --i)
+                        if (i < n && haswt < 0 && (use_resid ? wr_of(xp[i], xq[i]) : wp_of(xp[i])) > 0)
+                            haswt = c * per + i;
                 }
-        }
-    }
-    // the last token with weight, for a target rounded up to the total
-    int haswt = -1;
-    if (own > 0)
-        for (int c = c1 - 1; c >= c0 && haswt < 0; --c) {
-            float xp[8], xq[8];
-            const int n = load_chunk(a, prow, c, xp);
-            if (use_resid)
-                load_chunk(a, qrow, c, xq);
 #pragma unroll
-            for (int i = 7; i >= 0; --i)
-                if (i < n && haswt < 0 && (use_resid ? wr_of(xp[i], xq[i]) : wp_of(xp[i])) > 0)
-                    haswt = c * per + i;
+            for (int off = 16; off > 0; off >>= 1)
+                haswt = max(haswt, __shfl_xor_sync(0xffffffffu, haswt, off));
+            if (lane == 0)
+                sh.ired2[wid] = haswt;
+            __syncthreads();
+            for (int i = 0; i < SNW; ++i)
+                token = max(token, sh.ired2[i]);
         }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        haswt = max(haswt, __shfl_xor_sync(0xffffffffu, haswt, off));
-    if (lane == 0)
-        sh.ired2[wid] = haswt;
-    __syncthreads();
-    int token = sh.ired[0], last = -1;
-    for (int i = 0; i < SNW; ++i)
-        last = max(last, sh.ired2[i]);
-    if (token < 0)
-        token = last;  // target rounded up to the total: the last token with weight
-    if (threadIdx.x == 0) {
-        a.j_out[b] = j;
-        a.token_out[b] = token;
-        if (a.keep_out)
-            a.keep_out[b] = j + 1;
+        if (threadIdx.x == 0)
+            finish(token);
     }
+    if (CL > 1)
+        cluster_wait();  // no CTA leaves while another may still read its parts
+}
+
+// One CTA a session.
+__global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowStats *__restrict__ stats)
+{
+    __shared__ WalkShared sh;
+    walk_session<1>(sh, a, stats, blockIdx.x);
+}
+
+// A cluster of CL CTAs a session (few sessions: one CTA would weight the whole row).
+template <int CL>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(SNT)
+    walk_cluster_kernel(const SampArgs a, const RowStats *__restrict__ stats)
+{
+    __shared__ WalkShared sh;
+    walk_session<CL>(sh, a, stats, blockIdx.x / CL);
 }
 
 int check_sampling(const kda_sampling *sp)
@@ -923,20 +999,25 @@ int sampled_common(const void *logits, const void *draft_logits, int logit_dtype
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
                                                   cudaSuccess)
         return fail(KDA_ECUDA, "cudaDeviceGetAttribute(cudaDevAttrMultiProcessorCount) failed");
-    // few rows (every cluster resident at once): a cluster of CTAs a row; measured on
-    // GB300 at V = 32768, 15 rows 84.5 -> 62.1 us, while 60 rows (3 waves of clusters)
-    // ran 94.8 -> 140 us, so more rows keep one CTA a row
-    if (rows * SCL <= sms) {
-        row_stats_cluster_kernel<<<static_cast<unsigned>(rows * SCL), SNT, 0, stream>>>(a, stats);
-        if ((rc = check_launch("row_stats_cluster_kernel")))
-            return rc;
-    } else {
-        row_stats_kernel<<<static_cast<unsigned>(rows), SNT, 0, stream>>>(a, stats);
-        if ((rc = check_launch("row_stats_kernel")))
-            return rc;
-    }
-    walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
-    return check_launch("walk_kernel");
+    // few rows: a cluster of CTAs a row, as many as keep every cluster resident at once
+    // (one CTA an SM); more rows than that keep one CTA a row (measured on GB300 at
+    // V = 32768: 60 rows in three waves of 8-CTA clusters ran 94.8 -> 140 us)
+    const unsigned gr = static_cast<unsigned>(rows);
+    if (rows * 8 <= sms)
+        row_stats_cluster_kernel<8><<<gr * 8, SNT, 0, stream>>>(a, stats);
+    else if (rows * 4 <= sms)
+        row_stats_cluster_kernel<4><<<gr * 4, SNT, 0, stream>>>(a, stats);
+    else if (rows * 2 <= sms)
+        row_stats_cluster_kernel<2><<<gr * 2, SNT, 0, stream>>>(a, stats);
+    else
+        row_stats_kernel<<<gr, SNT, 0, stream>>>(a, stats);
+    if ((rc = check_launch("row statistics")))
+        return rc;
+    if (static_cast<long long>(B) * 8 <= sms)
+        walk_cluster_kernel<8><<<static_cast<unsigned>(B) * 8, SNT, 0, stream>>>(a, stats);
+    else
+        walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
+    return check_launch("walk");
 }
 
 }  // namespace
