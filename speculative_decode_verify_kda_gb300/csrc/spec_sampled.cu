@@ -72,11 +72,13 @@ struct SampArgs {
 };
 
 struct RowStats {
-    float m;   // max z
-    float th;  // kept iff e >= th
-    double Z;  // kept mass (its exact fixed-point sum, as a double)
-    int bad;   // the row holds a NaN or no finite maximum
-    int pad[3];
+    float m;     // max z
+    float th;    // kept iff e >= th
+    double Z;    // kept mass (its exact fixed-point sum, as a double)
+    int bad;     // the row holds a NaN or no finite maximum
+    float lo;    // every logit below lo has e < max(th, 2^-46): dropped, or of weight 0
+    float lo_f;  // every logit below lo_f has e < th: dropped
+    int pad;
 };
 static_assert(sizeof(RowStats) == 32, "row statistics are 32 bytes in scratch");
 
@@ -584,6 +586,28 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
     return a.bf16 ? sh.prefix | bf16_key_low(sh.prefix) : sh.prefix;
 }
 
+// A logit below which every e lies under te (> 0): x -> RN(RN(x / t) - m) is
+// non-decreasing, exp is increasing and expf lies within 2 ulp (2^-22 relative) of exp,
+// so a logit c whose e lies below te (1 - 2^-20) bounds the e of every smaller logit
+// below te.  The candidates start near the logit whose e is te and step down; -inf when
+// none checks out (or te <= 0).  Every thread computes the same value.
+__device__ float skip_below(float m, float te, float temperature)
+{
+    if (!(te > 0.f))
+        return -INFINITY;
+    const float bound = te * (1.f - 0x1p-20f);
+    float c = __fmul_rn(temperature, __fadd_rn(m, logf(te)));
+    float step = fmaxf(fabsf(c), 1.f) * 0x1p-10f;
+    for (int i = 0; i < 6; ++i, step *= 8.f) {
+        if (!(c > -INFINITY) || !(c < INFINITY))
+            break;
+        if (e_of(c, m, temperature) < bound)
+            return c;
+        c = __fsub_rn(c, step);
+    }
+    return -INFINITY;
+}
+
 // Filter statistics of one row into sh.rs (CL > 1: the row shared by the CTAs of a
 // cluster, each taking a slice; every CTA ends with the same statistics).
 template <int CL>
@@ -592,16 +616,18 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
     float mx = -INFINITY;
     int nan = 0;
     for_row<CL>(a, row, [&](int, float x) {
-        const float z = __fdiv_rn(x, a.temperature);
-        nan |= z != z;
-        mx = fmaxf(mx, z);
+        nan |= x != x;
+        mx = fmaxf(mx, x);
     });
     nan = __syncthreads_or(nan);
     float m = block_max(sh.red, mx);
     cluster_or_max<CL>(sh, nan, m);
+    // x -> RN(x / t) is non-decreasing for t > 0, so the largest z is z of the largest
+    // logit (and z is NaN exactly where x is)
+    m = __fdiv_rn(m, a.temperature);
     if (nan || !(m > -INFINITY) || !(m < INFINITY)) {
         if (threadIdx.x == 0)
-            sh.rs = RowStats{m, 0.f, 0.0, 1, {0, 0, 0}};
+            sh.rs = RowStats{m, 0.f, 0.0, 1, -INFINITY, -INFINITY, 0};
         __syncthreads();
         return;
     }
@@ -620,15 +646,18 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
     }
     if (a.min_p > 0.f)
         th = fmaxf(th, a.min_p);
+    const float lo = skip_below(m, fmaxf(th, 0x1p-46f), a.temperature);
     unsigned long long z = 0;
     for_row<CL>(a, row, [&](int, float x) {
-        const float e = e_of(x, m, a.temperature);
-        if (e >= th)
-            z += fx(e);
+        if (x >= lo) {  // (a logit below lo is dropped or weighs 0)
+            const float e = e_of(x, m, a.temperature);
+            if (e >= th)
+                z += fx(e);
+        }
     });
     const double Z = static_cast<double>(cluster_sum<CL>(sh, block_sum_u64(sh.ured, z), 1)) * FX_UNIT;
     if (threadIdx.x == 0)
-        sh.rs = RowStats{m, th, Z, 0, {0, 0, 0}};
+        sh.rs = RowStats{m, th, Z, 0, lo, skip_below(m, th, a.temperature), 0};
     __syncthreads();
 }
 
@@ -765,15 +794,30 @@ __device__ void walk_session(WalkShared &sh, const SampArgs &a, const RowStats *
     const unsigned char *prow = P + static_cast<size_t>(j) * a.V * es;
     const unsigned char *qrow = j < K ? Q + static_cast<size_t>(j) * a.V * es : nullptr;
     const RowStats rp = st[j];
-    const RowStats rq = j < K ? st[a.T + j] : RowStats{0.f, 0.f, 1.0, 0, {0, 0, 0}};
+    const RowStats rq = j < K ? st[a.T + j] : RowStats{0.f, 0.f, 1.0, 0, -INFINITY, -INFINITY, 0};
     const float ip = __double2float_rn(1.0 / rp.Z), iq = __double2float_rn(1.0 / rq.Z);
+    // (below rp.lo a target logit is dropped or its p~ and residual weigh 0, p~ <= e
+    // as Z >= 1; below rq.lo_f a draft logit is dropped: the weights are those of the
+    // full evaluation)
     auto wp_of = [&](float x) -> unsigned long long {
+        if (!(x >= rp.lo))
+            return 0ull;
         const float e = e_of(x, rp.m, a.temperature);
         return e >= rp.th ? fx(e) : 0ull;
     };
     auto wr_of = [&](float x, float xq) -> unsigned long long {
-        const float ep = e_of(x, rp.m, a.temperature), eq = e_of(xq, rq.m, a.temperature);
-        const float r = __fsub_rn(ep >= rp.th ? __fmul_rn(ep, ip) : 0.f, eq >= rq.th ? __fmul_rn(eq, iq) : 0.f);
+        float pt = 0.f, qt = 0.f;
+        if (x >= rp.lo) {
+            const float ep = e_of(x, rp.m, a.temperature);
+            if (ep >= rp.th)
+                pt = __fmul_rn(ep, ip);
+        }
+        if (xq >= rq.lo_f) {
+            const float eq = e_of(xq, rq.m, a.temperature);
+            if (eq >= rq.th)
+                qt = __fmul_rn(eq, iq);
+        }
+        const float r = __fsub_rn(pt, qt);
         return r > 0.f ? fx(r) : 0ull;
     };
     // thread t owns a contiguous run of the slice's 16-byte chunks (the for_row chunks):
