@@ -43,7 +43,9 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <string>
 
 #include "kda_internal.h"
@@ -82,6 +84,8 @@ struct RowStats {
 };
 static_assert(sizeof(RowStats) == 32, "row statistics are 32 bytes in scratch");
 
+constexpr int SLIST = 4096;  // the candidate list of a row's top-k select, in logits
+
 struct RowShared {
     float red[SNW];
     unsigned long long ured[SNW];
@@ -89,7 +93,7 @@ struct RowShared {
     unsigned long long hw[SNW][256];  // per-warp e-mass bins of one radix pass
     unsigned long long tot[256];
     unsigned prefix;
-    int kk, done;
+    int kk, done, nlist;
     unsigned long long above;
     RowStats rs;
     // a row shared by a cluster: each CTA's part of a reduction, read by every CTA.  Each
@@ -374,90 +378,86 @@ __device__ __forceinline__ int load_chunk(const SampArgs &a, const void *row, in
     return 1;
 }
 
-// The key of the k-th largest logit of the row (k >= 1, k <= V), by four 8-bit count passes.
-template <int CL>
-__device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void *row, int k)
-{
-    if (threadIdx.x == 0) {
-        sh.prefix = 0;
-        sh.kk = k;
-    }
-    unsigned mask = 0;
-    const int passes = a.bf16 ? 2 : 4;
-    for (int pass = 0; pass < passes; ++pass) {
-        const int shift = 24 - 8 * pass;
-        unsigned *hist = sh.hist[pass & 1];
-        for (int i = threadIdx.x; i < 256; i += SNT)
-            hist[i] = 0;
-        __syncthreads();
-        const unsigned prefix = sh.prefix;
-        // a thread's consecutive elements mostly share the top bytes: count runs of one
-        // bin in a register and add each run once
-        int cur = -1;
-        unsigned run = 0;
-        int c0, c1;
-        slice_of<CL>(a, c0, c1);
-        for (int c = c0 + threadIdx.x; c < c1; c += SNT) {
-            float xs[8];
-            const int n = load_chunk(a, row, c, xs);
-            for (int i = 0; i < n; ++i) {
-                const unsigned key = okey(xs[i]);
-                if ((key & mask) != prefix)
-                    continue;
-                const int bin = static_cast<int>((key >> shift) & 255u);
-                if (bin != cur) {
-                    if (cur >= 0)
-                        atomicAdd(&hist[cur], run);
-                    cur = bin;
-                    run = 0;
-                }
-                ++run;
-            }
+// Runs of one bin counted in a register and added to the bins once per run (a thread's
+// consecutive logits mostly share the top bytes of their keys).
+struct BinRun {
+    int cur = -1;
+    unsigned run = 0;
+    __device__ __forceinline__ void add(unsigned *hist, int bin)
+    {
+        if (bin != cur) {
+            if (cur >= 0)
+                atomicAdd(&hist[cur], run);
+            cur = bin;
+            run = 0;
         }
+        ++run;
+    }
+    __device__ __forceinline__ void flush(unsigned *hist)
+    {
         if (cur >= 0)
             atomicAdd(&hist[cur], run);
-        __syncthreads();
-        // a cluster's row: the counts of every slice (into the spare e-mass bins)
-        if (CL > 1) {
-            cluster_bins<CL>(static_cast<const unsigned *>(hist), reinterpret_cast<unsigned *>(&sh.tot[0]));
-            __syncthreads();
-        }
-        if (threadIdx.x < 32) {  // warp 0: the bin holding the kk-th largest, from the top
-            const int lane = threadIdx.x;
-            unsigned c[8], tot = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                c[i] = CL > 1 ? reinterpret_cast<const unsigned *>(&sh.tot[0])[255 - (8 * lane + i)]
-                              : hist[255 - (8 * lane + i)];
-                tot += c[i];
-            }
-            unsigned incl = tot;  // inclusive prefix over lanes (bins counted from the top)
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
-                if (lane >= off)
-                    incl += y;
-            }
-            const unsigned excl = incl - tot;
-            const int kk = sh.kk;
-            if (excl < static_cast<unsigned>(kk) && static_cast<unsigned>(kk) <= incl) {
-                unsigned run = excl;
-                int bin = 255 - 8 * lane;
-                for (int i = 0; i < 8; ++i) {
-                    if (run + c[i] >= static_cast<unsigned>(kk)) {
-                        bin = 255 - (8 * lane + i);
-                        break;
-                    }
-                    run += c[i];
-                }
-                sh.prefix = prefix | (static_cast<unsigned>(bin) << shift);
-                sh.kk = kk - static_cast<int>(run);
-            }
-        }
-        mask |= 255u << shift;
-        __syncthreads();
     }
-    return a.bf16 ? sh.prefix | bf16_key_low(sh.prefix) : sh.prefix;
+};
+
+// The CTA's logits handed to f(x): the candidate list when it holds them (n >= 0), else
+// the CTA's slice of the row.
+template <int CL, class F>
+__device__ __forceinline__ void each_logit(const SampArgs &a, const void *row, const float *list, int n, F f)
+{
+    if (n >= 0) {
+        for (int i = threadIdx.x; i < n; i += SNT)
+            f(list[i]);
+    } else {
+        for_row<CL>(a, row, [&](int, float x) { f(x); });
+    }
+}
+
+// One step of the exact select of the k-th largest key: hist holds this CTA's counts of
+// the byte at `shift` of the keys under `prefix` (complete: a barrier of the CTA precedes
+// the call); warp 0 finds the bin holding the sh.kk-th largest, counting from the top,
+// and extends sh.prefix by it.
+template <int CL>
+__device__ void pick_kth_bin(RowShared &sh, const unsigned *hist, unsigned prefix, int shift)
+{
+    const unsigned *cnt = hist;
+    if (CL > 1) {  // a cluster's row: the counts of every slice (into the spare e-mass bins)
+        cluster_bins<CL>(hist, reinterpret_cast<unsigned *>(&sh.tot[0]));
+        __syncthreads();
+        cnt = reinterpret_cast<const unsigned *>(&sh.tot[0]);
+    }
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        unsigned c[8], tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            c[i] = cnt[255 - (8 * lane + i)];
+            tot += c[i];
+        }
+        unsigned incl = tot;  // inclusive prefix over lanes (bins counted from the top)
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off)
+                incl += y;
+        }
+        const unsigned excl = incl - tot;
+        const int kk = sh.kk;
+        if (excl < static_cast<unsigned>(kk) && static_cast<unsigned>(kk) <= incl) {
+            unsigned run = excl;
+            int bin = 255 - 8 * lane;
+            for (int i = 0; i < 8; ++i) {
+                if (run + c[i] >= static_cast<unsigned>(kk)) {
+                    bin = 255 - (8 * lane + i);
+                    break;
+                }
+                run += c[i];
+            }
+            sh.prefix = prefix | (static_cast<unsigned>(bin) << shift);
+            sh.kk = kk - static_cast<int>(run);
+        }
+    }
+    __syncthreads();
 }
 
 // The key of the top-p boundary: the largest key kappa whose mass F(kappa) = sum of e
@@ -468,10 +468,11 @@ __device__ unsigned kth_largest_key(RowShared &sh, const SampArgs &a, const void
 // current prefix, and warp 0 walks the bins from the top (above: the mass of the keys
 // already passed).  Only keys >= floor take part (the k-th largest key under top_k):
 // when their whole mass stays below the target, the top-p threshold lies under the
-// top-k one and floor is returned.
+// top-k one and floor is returned.  The passes read the candidate list when it holds
+// every key >= floor (nl >= 0), else the row.
 template <int CL>
-__device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, float m, double target,
-                             unsigned floor)
+__device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, const float *list, int nl, float m,
+                             double target, unsigned floor)
 {
     const int w = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
@@ -490,25 +491,19 @@ __device__ unsigned topp_key(RowShared &sh, const SampArgs &a, const void *row, 
         // runs of one bin summed in a register (integer sums: the order does not matter)
         int cur = -1;
         unsigned long long run = 0;
-        int c0, c1;
-        slice_of<CL>(a, c0, c1);
-        for (int c = c0 + threadIdx.x; c < c1; c += SNT) {
-            float xs[8];
-            const int n = load_chunk(a, row, c, xs);
-            for (int i = 0; i < n; ++i) {
-                const unsigned key = okey(xs[i]);
-                if ((key & mask) != prefix || key < floor)
-                    continue;
-                const int bin = static_cast<int>((key >> shift) & 255u);
-                if (bin != cur) {
-                    if (cur >= 0)
-                        atomicAdd(&sh.hw[w][cur], run);
-                    cur = bin;
-                    run = 0;
-                }
-                run += fx(e_of(xs[i], m, a.temperature));
+        each_logit<CL>(a, row, list, nl, [&](float x) {
+            const unsigned key = okey(x);
+            if ((key & mask) != prefix || key < floor)
+                return;
+            const int bin = static_cast<int>((key >> shift) & 255u);
+            if (bin != cur) {
+                if (cur >= 0)
+                    atomicAdd(&sh.hw[w][cur], run);
+                cur = bin;
+                run = 0;
             }
-        }
+            run += fx(e_of(x, m, a.temperature));
+        });
         if (cur >= 0)
             atomicAdd(&sh.hw[w][cur], run);
         __syncthreads();
@@ -609,16 +604,37 @@ __device__ float skip_below(float m, float te, float temperature)
 }
 
 // Filter statistics of one row into sh.rs (CL > 1: the row shared by the CTAs of a
-// cluster, each taking a slice; every CTA ends with the same statistics).
+// cluster, each taking a slice; every CTA ends with the same statistics).  Sweeps of the
+// CTA's logits: (1) the maximum, the NaN flag and the first count pass of the top-k
+// select; (2) S for top-p and, for top-k, the candidates: every logit whose key's top byte
+// is at or above the one holding the k-th largest, into `list` while it has room (every
+// later pass selects among them, so the later count passes and the top-p passes read the
+// list, or the row when the list overflowed); (3) the kept mass Z.  All sums and counts are
+// integers, so the order in which the list holds the candidates does not matter.
 template <int CL>
-__device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
+__device__ void row_stats(RowShared &sh, float *list, const SampArgs &a, const void *row)
 {
+    const bool topk = a.top_k > 0 && a.top_k < a.V, topp = a.top_p < 1.0f;
+    const int passes = a.bf16 ? 2 : 4;
+    if (topk)
+        for (int i = threadIdx.x; i < 256; i += SNT)
+            sh.hist[0][i] = 0;
+    if (threadIdx.x == 0) {
+        sh.prefix = 0;
+        sh.kk = a.top_k;
+        sh.nlist = 0;
+    }
+    __syncthreads();
     float mx = -INFINITY;
     int nan = 0;
+    BinRun br;
     for_row<CL>(a, row, [&](int, float x) {
         nan |= x != x;
         mx = fmaxf(mx, x);
+        if (topk)
+            br.add(sh.hist[0], static_cast<int>(okey(x) >> 24));
     });
+    br.flush(sh.hist[0]);
     nan = __syncthreads_or(nan);
     float m = block_max(sh.red, mx);
     cluster_or_max<CL>(sh, nan, m);
@@ -631,18 +647,51 @@ __device__ void row_stats(RowShared &sh, const SampArgs &a, const void *row)
         __syncthreads();
         return;
     }
+    if (topk)
+        pick_kth_bin<CL>(sh, sh.hist[0], 0u, 24);
+    const unsigned base = sh.prefix;
+    unsigned long long s = 0;
+    if (topp || topk)
+        for_row<CL>(a, row, [&](int, float x) {
+            if (topp)
+                s += fx(e_of(x, m, a.temperature));
+            if (topk && okey(x) >= base) {
+                const int i = atomicAdd(&sh.nlist, 1);
+                if (i < SLIST)
+                    list[i] = x;
+            }
+        });
+    __syncthreads();
+    const int nl = topk && sh.nlist <= SLIST ? sh.nlist : -1;
     float th = 0.f;
     unsigned floor = 0;  // the k-th largest key: top-p looks no lower
-    if (a.top_k > 0 && a.top_k < a.V) {
-        floor = kth_largest_key<CL>(sh, a, row, a.top_k);
+    if (topk) {
+        unsigned mask = 0xff000000u;
+        for (int pass = 1; pass < passes; ++pass) {  // (bf16 keys end in 16 fixed bits)
+            const int shift = 24 - 8 * pass;
+            unsigned *hist = sh.hist[pass & 1];
+            for (int i = threadIdx.x; i < 256; i += SNT)
+                hist[i] = 0;
+            __syncthreads();
+            const unsigned prefix = sh.prefix;
+            BinRun r;
+            each_logit<CL>(a, row, list, nl, [&](float x) {
+                const unsigned key = okey(x);
+                if ((key & mask) == prefix)
+                    r.add(hist, static_cast<int>((key >> shift) & 255u));
+            });
+            r.flush(hist);
+            __syncthreads();
+            pick_kth_bin<CL>(sh, hist, prefix, shift);
+            mask |= 255u << shift;
+        }
+        floor = a.bf16 ? sh.prefix | bf16_key_low(sh.prefix) : sh.prefix;
         th = e_of(unkey(floor), m, a.temperature);
     }
-    if (a.top_p < 1.0f) {
-        unsigned long long s = 0;
-        for_row<CL>(a, row, [&](int, float x) { s += fx(e_of(x, m, a.temperature)); });
+    if (topp) {
         const unsigned long long S = cluster_sum<CL>(sh, block_sum_u64(sh.ured, s), 0);
         const double target = static_cast<double>(a.top_p) * static_cast<double>(S);
-        th = fmaxf(th, e_of(unkey(topp_key<CL>(sh, a, row, m, target, floor)), m, a.temperature));
+        th = fmaxf(th, e_of(unkey(topp_key<CL>(sh, a, row, list, nl, m, target, floor)), m, a.temperature));
     }
     if (a.min_p > 0.f)
         th = fmaxf(th, a.min_p);
@@ -680,11 +729,15 @@ __device__ __forceinline__ const void *stats_row(const SampArgs &a, int rowi)
                           (static_cast<size_t>(b) * K + (ri - a.T)) * a.V * es;
 }
 
+// The launches' dynamic shared memory: the row's work space, then the candidate list.
+constexpr size_t ROW_SMEM = sizeof(RowShared) + SLIST * sizeof(float);
+
 // One CTA a row (many rows: the GPU is full).
 __global__ void __launch_bounds__(SNT) row_stats_kernel(const SampArgs a, RowStats *__restrict__ stats)
 {
-    __shared__ RowShared sh;
-    row_stats<1>(sh, a, stats_row(a, blockIdx.x));
+    extern __shared__ __align__(16) unsigned char smem[];
+    RowShared &sh = *reinterpret_cast<RowShared *>(smem);
+    row_stats<1>(sh, reinterpret_cast<float *>(smem + sizeof(RowShared)), a, stats_row(a, blockIdx.x));
     if (threadIdx.x == 0)
         stats[blockIdx.x] = sh.rs;
 }
@@ -695,9 +748,10 @@ template <int CL>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(SNT, 1)
     row_stats_cluster_kernel(const SampArgs a, RowStats *__restrict__ stats)
 {
-    __shared__ RowShared sh;
+    extern __shared__ __align__(16) unsigned char smem[];
+    RowShared &sh = *reinterpret_cast<RowShared *>(smem);
     const int rowi = blockIdx.x / CL;
-    row_stats<CL>(sh, a, stats_row(a, rowi));
+    row_stats<CL>(sh, reinterpret_cast<float *>(smem + sizeof(RowShared)), a, stats_row(a, rowi));
     auto cl = cooperative_groups::this_cluster();
     if (threadIdx.x == 0 && cl.block_rank() == 0)
         stats[rowi] = sh.rs;
@@ -979,6 +1033,46 @@ int check_sampling(const kda_sampling *sp)
     return KDA_OK;
 }
 
+// Once per device (under a lock): the SM count, and the row-statistics launches' dynamic
+// shared memory above the default 48 KiB.
+int device_setup(int &sms)
+{
+    struct Info {
+        std::atomic<int> ready{0};
+        int sms = 0;
+    };
+    static Info info[64];
+    static std::mutex init_mutex;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return fail(KDA_ECUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
+    if (dev < 0 || dev >= 64)
+        return fail(KDA_EINVAL, "device ordinal beyond the launch table");
+    Info &di = info[dev];
+    if (!di.ready.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(init_mutex);
+        if (!di.ready.load(std::memory_order_relaxed)) {
+            int n = 0;
+            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+            const void *kernels[4] = {reinterpret_cast<const void *>(row_stats_kernel),
+                                      reinterpret_cast<const void *>(row_stats_cluster_kernel<8>),
+                                      reinterpret_cast<const void *>(row_stats_cluster_kernel<4>),
+                                      reinterpret_cast<const void *>(row_stats_cluster_kernel<2>)};
+            for (const void *k : kernels)
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(ROW_SMEM));
+            if (e != cudaSuccess)
+                return fail(KDA_ECUDA, std::string("sampled accept set-up: ") + cudaGetErrorString(e));
+            di.sms = n;
+            di.ready.store(1, std::memory_order_release);
+        }
+    }
+    sms = di.sms;
+    return KDA_OK;
+}
+
 // Shared body of both entry points: u_accept/u_sample or seeds/counters.
 int sampled_common(const void *logits, const void *draft_logits, int logit_dtype, int B, int T, int V,
                    const int *drafts, const float *u_accept, const float *u_sample, const unsigned long long *seeds,
@@ -1039,22 +1133,20 @@ int sampled_common(const void *logits, const void *draft_logits, int logit_dtype
     RowStats *stats = static_cast<RowStats *>(scratch);
     const long long rows = static_cast<long long>(B) * (2 * T - 1);
     int sms = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
-                                                  cudaSuccess)
-        return fail(KDA_ECUDA, "cudaDeviceGetAttribute(cudaDevAttrMultiProcessorCount) failed");
+    if ((rc = device_setup(sms)))
+        return rc;
     // few rows: a cluster of CTAs a row, as many as keep every cluster resident at once
     // (one CTA an SM); more rows than that keep one CTA a row (measured on GB300 at
     // V = 32768: 60 rows in three waves of 8-CTA clusters ran 94.8 -> 140 us)
     const unsigned gr = static_cast<unsigned>(rows);
     if (rows * 8 <= sms)
-        row_stats_cluster_kernel<8><<<gr * 8, SNT, 0, stream>>>(a, stats);
+        row_stats_cluster_kernel<8><<<gr * 8, SNT, ROW_SMEM, stream>>>(a, stats);
     else if (rows * 4 <= sms)
-        row_stats_cluster_kernel<4><<<gr * 4, SNT, 0, stream>>>(a, stats);
+        row_stats_cluster_kernel<4><<<gr * 4, SNT, ROW_SMEM, stream>>>(a, stats);
     else if (rows * 2 <= sms)
-        row_stats_cluster_kernel<2><<<gr * 2, SNT, 0, stream>>>(a, stats);
+        row_stats_cluster_kernel<2><<<gr * 2, SNT, ROW_SMEM, stream>>>(a, stats);
     else
-        row_stats_kernel<<<gr, SNT, 0, stream>>>(a, stats);
+        row_stats_kernel<<<gr, SNT, ROW_SMEM, stream>>>(a, stats);
     if ((rc = check_launch("row statistics")))
         return rc;
     if (static_cast<long long>(B) * 8 <= sms)
