@@ -35,10 +35,10 @@
 //      integer sums, per-warp bins) that find the key at which the descending running
 //      sum reaches top_p * S, then the kept mass Z, into scratch.  The row stays in
 //      L1 between its passes, which read 16-byte vectors.
-//   2. walk_kernel, one CTA per session (or, for at most a cluster per SM's worth of
-//      sessions, a cluster of 8 CTAs a session, each weighting a slice of the draw's
-//      row): the accept tests from the row statistics, then one pass for the total
-//      weight of the final draw and one scan for it.
+//   2. walk_kernel, one CTA per session (or, when the clusters fit on the GPU at once,
+//      a cluster of 8, 4 or 2 CTAs a session, each weighting a slice of the draw's row):
+//      the accept tests from the row statistics, then one pass for the total weight of
+//      the final draw and one scan for it.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -1011,7 +1011,7 @@ __global__ void __launch_bounds__(SNT) walk_kernel(const SampArgs a, const RowSt
 
 // A cluster of CL CTAs a session (few sessions: one CTA would weight the whole row).
 template <int CL>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(SNT)
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(SNT, 1)
     walk_cluster_kernel(const SampArgs a, const RowStats *__restrict__ stats)
 {
     __shared__ WalkShared sh;
@@ -1149,8 +1149,16 @@ int sampled_common(const void *logits, const void *draft_logits, int logit_dtype
         row_stats_kernel<<<gr, SNT, ROW_SMEM, stream>>>(a, stats);
     if ((rc = check_launch("row statistics")))
         return rc;
-    if (static_cast<long long>(B) * 8 <= sms)
-        walk_cluster_kernel<8><<<static_cast<unsigned>(B) * 8, SNT, 0, stream>>>(a, stats);
+    // the walk: a cluster of 8, 4 or 2 CTAs a session while the clusters fit on the GPU at
+    // once, else one CTA a session
+    const long long bs = B;
+    const unsigned gb = static_cast<unsigned>(B);
+    if (bs * 8 <= sms)
+        walk_cluster_kernel<8><<<gb * 8, SNT, 0, stream>>>(a, stats);
+    else if (bs * 4 <= sms)
+        walk_cluster_kernel<4><<<gb * 4, SNT, 0, stream>>>(a, stats);
+    else if (bs * 2 <= sms)
+        walk_cluster_kernel<2><<<gb * 2, SNT, 0, stream>>>(a, stats);
     else
         walk_kernel<<<B, SNT, 0, stream>>>(a, stats);
     return check_launch("walk");

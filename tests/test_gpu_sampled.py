@@ -171,12 +171,12 @@ def test_top_p_with_thousands_of_ties(orc):
             assert (int(j[b]), int(tok[b])) == want, (filt, b)
 
 
-@pytest.mark.parametrize("B", [24, 3])
+@pytest.mark.parametrize("B", [24, 3, 50])
 def test_session_rounds_against_oracle(orc, B):
     """spec_accept_sampled_session over several rounds in a row: every round draws its
     uniforms from the session's counters and advances them on the device, exactly as the
-    oracle's session walk does (B = 3: each session's walk shared by a cluster of CTAs,
-    one of which writes the counters the others have read)."""
+    oracle's session walk does (B = 3, 24, 50: each session's walk shared by a cluster of
+    8, 4 or 2 CTAs, one of which writes the counters the others have read)."""
     rng = np.random.default_rng(71 + B)
     T, V = 6, 2000
     seeds = rng.integers(0, 2**63, B, dtype=np.int64)
