@@ -444,7 +444,9 @@ int spec_window(const float *scores, int B, int K, int policy, float param, int 
  *   whose running sum reaches top_p * S, ties kept), min_p (e >= min_p);
  *   p~ = e / Z over the kept tokens, Z their sum.  S, Z and every running sum are
  *   exact integer sums of the weights in units of 2^-46 (no sum depends on the order
- *   of its terms); top_p is exact for any top_k (0 included) and any number of ties.
+ *   of its terms; a 64-bit sum of V weights of at most 1 holds V up to KDA_SAMPLED_VMAX,
+ *   larger V is refused with KDA_EINVAL); top_p is exact for any top_k (0 included) and
+ *   any number of ties.
  * Draft r is accepted iff u_r * q~_r(x_r) < p~_r(x_r), compared in double on the f32
  * values of p~ and q~ (the page's (u as f64) * (qj as f64) < pj as f64); the walk
  * stops at the first rejection j.  j < K: the token is drawn from max(0, p~_j - q~_j)
@@ -453,6 +455,8 @@ int spec_window(const float *scores, int B, int K, int policy, float param, int 
  * u * (total weight).  Every result is reproducible bit for bit from the
  * inputs (and, for the session form, the counters).
  */
+#define KDA_SAMPLED_VMAX 262143 /* 2^18 - 1: V * 2^46 stays below 2^64 */
+
 typedef struct kda_sampling {
     float temperature; /* > 0                                                  */
     int top_k;         /* 0 off; >= 1 keeps the k largest (>= V: every token)  */

@@ -102,8 +102,10 @@ struct RowShared {
     // reads of the slot: no second barrier per reduction.
     float cmax;
     int cnan;
-    unsigned long long csum[2];
+    unsigned long long csum[4];
     unsigned long long pub[2][256];
+    unsigned fine[4096];  // top-k and top-p: counts of the keys' top 12 bits (first sweep)
+    int fstar;            // the fine bin holding the k-th largest
 };
 
 struct WalkShared {
@@ -306,7 +308,7 @@ __device__ void cluster_or_max(RowShared &sh, int &nan, float &m)
     m = x;
 }
 
-// slot: 0 or 1, each used once per row
+// slot: 0 to 3, each used once per row
 template <int CL>
 __device__ unsigned long long cluster_sum(RowShared &sh, unsigned long long x, int slot)
 {
@@ -606,17 +608,28 @@ __device__ float skip_below(float m, float te, float temperature)
 // Filter statistics of one row into sh.rs (CL > 1: the row shared by the CTAs of a
 // cluster, each taking a slice; every CTA ends with the same statistics).  Sweeps of the
 // CTA's logits: (1) the maximum, the NaN flag and the first count pass of the top-k
-// select; (2) S for top-p and, for top-k, the candidates: every logit whose key's top byte
-// is at or above the one holding the k-th largest, into `list` while it has room (every
-// later pass selects among them, so the later count passes and the top-p passes read the
-// list, or the row when the list overflowed); (3) the kept mass Z.  All sums and counts are
-// integers, so the order in which the list holds the candidates does not matter.
+// select; (2) with top-k, the candidates: every logit whose key's top byte is at or above
+// the one holding the k-th largest (every later pass selects among them), into `list`
+// when their count, known from the first pass, fits (else the later passes read the row
+// again), and S for top-p; (3) the kept mass Z.  All sums and counts are integers, so the
+// order in which the list holds the candidates does not matter.
+// Top-k and top-p together: the first pass counts the keys' top 12 bits (bins of an
+// eighth of a binade); from those counts, S is bounded from below (every logit of a bin
+// is at least the bin's smallest value) and the mass of the top-k set from above (every
+// key >= the k-th largest lies in its bin or a higher one, every logit of a bin is at
+// most the bin's largest value), the e of a bin's edge taken with a 2^-19 margin for
+// expf's 2-ulp error.  When the bound of the top-k mass stays below top_p times the
+// bound of S, top-k binds: top-p's threshold lies under the top-k one, and S is not formed.
 template <int CL>
 __device__ void row_stats(RowShared &sh, float *list, const SampArgs &a, const void *row)
 {
     const bool topk = a.top_k > 0 && a.top_k < a.V, topp = a.top_p < 1.0f;
+    const bool fine = topk && topp;
     const int passes = a.bf16 ? 2 : 4;
-    if (topk)
+    if (fine)
+        for (int i = threadIdx.x; i < 4096; i += SNT)
+            sh.fine[i] = 0;
+    else if (topk)
         for (int i = threadIdx.x; i < 256; i += SNT)
             sh.hist[0][i] = 0;
     if (threadIdx.x == 0) {
@@ -628,13 +641,15 @@ __device__ void row_stats(RowShared &sh, float *list, const SampArgs &a, const v
     float mx = -INFINITY;
     int nan = 0;
     BinRun br;
+    unsigned *const h0 = fine ? sh.fine : sh.hist[0];
+    const int hs = fine ? 20 : 24;
     for_row<CL>(a, row, [&](int, float x) {
         nan |= x != x;
         mx = fmaxf(mx, x);
         if (topk)
-            br.add(sh.hist[0], static_cast<int>(okey(x) >> 24));
+            br.add(h0, static_cast<int>(okey(x) >> hs));
     });
-    br.flush(sh.hist[0]);
+    br.flush(h0);
     nan = __syncthreads_or(nan);
     float m = block_max(sh.red, mx);
     cluster_or_max<CL>(sh, nan, m);
@@ -647,22 +662,85 @@ __device__ void row_stats(RowShared &sh, float *list, const SampArgs &a, const v
         __syncthreads();
         return;
     }
-    if (topk)
-        pick_kth_bin<CL>(sh, sh.hist[0], 0u, 24);
-    const unsigned base = sh.prefix;
-    unsigned long long s = 0;
-    if (topp || topk)
-        for_row<CL>(a, row, [&](int, float x) {
-            if (topp)
-                s += fx(e_of(x, m, a.temperature));
-            if (topk && okey(x) >= base) {
-                const int i = atomicAdd(&sh.nlist, 1);
-                if (i < SLIST)
-                    list[i] = x;
+    bool gather = false, skip_s = false;
+    if (topk) {
+        if (fine) {  // the top bytes' counts from the fine ones
+            for (int b = threadIdx.x; b < 256; b += SNT) {
+                unsigned c = 0;
+                for (int i = 0; i < 16; ++i)
+                    c += sh.fine[16 * b + i];
+                sh.hist[0][b] = c;
             }
+            __syncthreads();
+        }
+        pick_kth_bin<CL>(sh, sh.hist[0], 0u, 24);
+        const unsigned bin0 = sh.prefix >> 24;
+        unsigned long long n_part = 0;  // this CTA's candidates
+        for (int b = threadIdx.x; b < 256; b += SNT)
+            if (static_cast<unsigned>(b) >= bin0)
+                n_part += sh.hist[0][b];
+        gather = block_sum_u64(sh.ured, n_part) <= static_cast<unsigned long long>(SLIST);
+        if (fine) {
+            if (threadIdx.x < 32) {  // the fine bin of bin0 holding the kk-th largest (the row's counts)
+                const int lane = threadIdx.x;
+                unsigned c = 0;
+                if (lane < 16) {
+                    const int f = 16 * static_cast<int>(bin0) + 15 - lane;  // from the top
+                    if (CL > 1) {
+                        auto cl = cooperative_groups::this_cluster();
+                        for (int r = 0; r < CL; ++r)
+                            c += cl.map_shared_rank(sh.fine, r)[f];
+                    } else {
+                        c = sh.fine[f];
+                    }
+                }
+                unsigned incl = c;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+                    if (lane >= off)
+                        incl += y;
+                }
+                const unsigned kk = static_cast<unsigned>(sh.kk);
+                if (lane < 16 && incl - c < kk && kk <= incl)
+                    sh.fstar = 16 * static_cast<int>(bin0) + 15 - lane;
+            }
+            __syncthreads();
+            const int fs = sh.fstar;
+            unsigned long long lo_part = 0, hi_part = 0;
+            for (int f = threadIdx.x; f < 4096; f += SNT) {
+                const unsigned c = sh.fine[f];
+                if (!c)
+                    continue;
+                const unsigned fu = static_cast<unsigned>(f);
+                const float x0 = unkey(fu << 20), x1 = unkey(((fu + 1u) << 20) - 1u);  // the bin's edges
+                if (x0 > -INFINITY && x0 < INFINITY)
+                    lo_part += static_cast<unsigned long long>(c) *
+                               fx(__fmul_rn(e_of(x0, m, a.temperature), 1.f - 0x1p-19f));
+                if (f >= fs) {
+                    float e1 = 1.f;
+                    if (x1 > -INFINITY && x1 < INFINITY)
+                        e1 = fminf(e_of(x1, m, a.temperature), 1.f);
+                    hi_part += static_cast<unsigned long long>(c) * fx(__fmul_rn(e1, 1.f + 0x1p-19f));
+                }
+            }
+            const unsigned long long s_lo = cluster_sum<CL>(sh, block_sum_u64(sh.ured, lo_part), 2);
+            const unsigned long long mk_hi = cluster_sum<CL>(sh, block_sum_u64(sh.ured, hi_part), 3);
+            skip_s = static_cast<double>(mk_hi) < static_cast<double>(a.top_p) * static_cast<double>(s_lo);
+        }
+    }
+    const unsigned base = sh.prefix;
+    const bool need_s = topp && !skip_s;
+    unsigned long long s = 0;
+    if (gather || need_s)
+        for_row<CL>(a, row, [&](int, float x) {
+            if (need_s)
+                s += fx(e_of(x, m, a.temperature));
+            if (gather && okey(x) >= base)
+                list[atomicAdd(&sh.nlist, 1)] = x;  // (the count fits: see above)
         });
     __syncthreads();
-    const int nl = topk && sh.nlist <= SLIST ? sh.nlist : -1;
+    const int nl = gather ? sh.nlist : -1;
     float th = 0.f;
     unsigned floor = 0;  // the k-th largest key: top-p looks no lower
     if (topk) {
@@ -688,7 +766,7 @@ __device__ void row_stats(RowShared &sh, float *list, const SampArgs &a, const v
         floor = a.bf16 ? sh.prefix | bf16_key_low(sh.prefix) : sh.prefix;
         th = e_of(unkey(floor), m, a.temperature);
     }
-    if (topp) {
+    if (need_s) {
         const unsigned long long S = cluster_sum<CL>(sh, block_sum_u64(sh.ured, s), 0);
         const double target = static_cast<double>(a.top_p) * static_cast<double>(S);
         th = fmaxf(th, e_of(unkey(topp_key<CL>(sh, a, row, list, nl, m, target, floor)), m, a.temperature));
@@ -1083,8 +1161,9 @@ int sampled_common(const void *logits, const void *draft_logits, int logit_dtype
         return fail(KDA_EINVAL, "B must be >= 0");
     if (T < 1 || T > KDA_TMAX)
         return fail(KDA_EINVAL, "T must lie in 1..15, got " + std::to_string(T));
-    if (V < 1)
-        return fail(KDA_EINVAL, "V must be >= 1");
+    if (V < 1 || V > KDA_SAMPLED_VMAX)
+        return fail(KDA_EINVAL, "V must lie in 1.." + std::to_string(KDA_SAMPLED_VMAX) +
+                                    " (the fixed-point sums of the weights hold 2^64 / 2^46 of them)");
     if (logit_dtype != KDA_F32 && logit_dtype != KDA_BF16)
         return fail(KDA_EINVAL, "logit_dtype must be KDA_F32 or KDA_BF16");
     int rc = check_sampling(sp);

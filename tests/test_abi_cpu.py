@@ -187,6 +187,8 @@ def test_sampled_accept_rejects_bad_shapes_and_pointers(L):
                                              ctypes.byref(s), FAKE, FAKE, None, None, k.get("scr", FAKE),
                                              k.get("nb", 1 << 20), None)
     assert call(T=0) == kb.EINVAL and call(T=16) == kb.EINVAL and call(V=0) == kb.EINVAL
+    # the fixed-point sums of V weights of at most 1 (units of 2^-46) must fit 64 bits
+    assert call(V=2**18) == kb.EINVAL and call(V=2**18 - 1, B=0) == kb.OK
     assert call(dt=9) == kb.EINVAL and call(us=None) == kb.EINVAL and call(lg=FAKE + 1) == kb.EINVAL
     assert call(scr=None) == kb.EINVAL and call(scr=FAKE + 8) == kb.EINVAL
     assert L.spec_accept_sampled_scratch_bytes(2, 8) == 2 * 15 * 32

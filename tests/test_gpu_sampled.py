@@ -151,6 +151,35 @@ def test_negative_logits_against_oracle(orc, B, fi, V, bf16):
         assert (int(j[b]), int(tok[b])) == want, (b, (int(j[b]), int(tok[b])), want)
 
 
+@pytest.mark.parametrize("B", [1, 12])
+@pytest.mark.parametrize("fi", [1, 2, 5, 6])
+@pytest.mark.parametrize("V,bf16", [(4000, False), (32768, True)])
+def test_flat_logits_against_oracle(orc, B, fi, V, bf16):
+    """Logits N(0, 1), as in the verify workloads: a flat distribution on which top-k
+    binds far below top-p (the device then proves it from a lower bound of S and forms
+    no S), and nucleus sampling alone keeps about half the vocabulary."""
+    filt = FILTERS[fi]
+    rng = np.random.default_rng(8100 + 17 * fi + B + bf16)
+    T, K = 6, 5
+    P = rng.normal(0, 1.0, (B, T, V)).astype(np.float32)
+    Q = (P[:, :K] + rng.normal(0, 0.3, (B, K, V))).astype(np.float32)
+    if bf16:
+        P, Q = synth.to_bf16_bits(P), synth.to_bf16_bits(Q)
+    d = np.zeros((B, K), np.int32)
+    for b in range(B):
+        for r in range(K):
+            qt = orc.filtered(Q[b, r], **f32(filt))
+            d[b, r] = rng.choice(V, p=qt / qt.sum())
+    ua = rng.uniform(0, 1, (B, K)).astype(np.float32)
+    us = rng.uniform(0, 1, B).astype(np.float32)
+    j, tok, _ = kb.spec_accept_sampled(to_dev(P, bf16), to_dev(Q, bf16), to_dev(d), to_dev(ua), to_dev(us),
+                                       **filt)
+    torch.cuda.synchronize()
+    for b in range(B):
+        want = orc.sampled_accept(P[b], Q[b], d[b], ua[b], float(us[b]), **f32(filt))
+        assert (int(j[b]), int(tok[b])) == want, (b, (int(j[b]), int(tok[b])), want)
+
+
 def test_top_p_with_thousands_of_ties(orc):
     """Rows whose top-p boundary falls inside a tie group of more than 1024 tokens: the
     kept set takes the whole group, on the device as in the oracle."""
