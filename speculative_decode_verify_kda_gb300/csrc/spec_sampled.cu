@@ -33,8 +33,10 @@
 //      keys: four for f32 rows, two for bf16 rows, whose keys end in 16 fixed bits),
 //      the top-p threshold by as many 8-bit passes of e-mass histograms (fixed-point
 //      integer sums, per-warp bins) that find the key at which the descending running
-//      sum reaches top_p * S, then the kept mass Z, into scratch.  The row stays in
-//      L1 between its passes, which read 16-byte vectors.
+//      sum reaches top_p * S, then the kept mass Z, into scratch.  Three sweeps of the
+//      row (16-byte vectors, the row in L1 between them); the later select passes read
+//      a list of the top-k candidates gathered in the second, and S is not formed when
+//      bounds from the first sweep's counts prove that top-k binds (row_stats).
 //   2. walk_kernel, one CTA per session (or, when the clusters fit on the GPU at once,
 //      a cluster of 8, 4 or 2 CTAs a session, each weighting a slice of the draw's row):
 //      the accept tests from the row statistics, then one pass for the total weight of
