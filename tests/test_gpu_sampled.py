@@ -180,6 +180,23 @@ def test_flat_logits_against_oracle(orc, B, fi, V, bf16):
         assert (int(j[b]), int(tok[b])) == want, (b, (int(j[b]), int(tok[b])), want)
 
 
+@pytest.mark.parametrize("B", [1, 12])
+@pytest.mark.parametrize("V,bf16", [(1001, True), (37, False), (4099, False)])
+def test_unvectorised_rows_against_oracle(orc, B, V, bf16):
+    """Rows that are not whole 16-byte vectors are read one logit at a time, and a
+    cluster's CTAs then split the row by logits (B = 1) rather than by vectors."""
+    rng = np.random.default_rng(8300 + V + B)
+    for fi in (1, 2, 5, 6):
+        filt = FILTERS[fi]
+        P, Q, d, ua, us = _case(rng, B, 5, V, orc, filt, bf16)
+        j, tok, _ = kb.spec_accept_sampled(to_dev(P, bf16), to_dev(Q, bf16), to_dev(d), to_dev(ua), to_dev(us),
+                                           **filt)
+        torch.cuda.synchronize()
+        for b in range(B):
+            want = orc.sampled_accept(P[b], Q[b], d[b], ua[b], float(us[b]), **f32(filt))
+            assert (int(j[b]), int(tok[b])) == want, (fi, b, (int(j[b]), int(tok[b])), want)
+
+
 def test_top_p_with_thousands_of_ties(orc):
     """Rows whose top-p boundary falls inside a tie group of more than 1024 tokens: the
     kept set takes the whole group, on the device as in the oracle."""
