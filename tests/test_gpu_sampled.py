@@ -197,6 +197,30 @@ def test_unvectorised_rows_against_oracle(orc, B, V, bf16):
             assert (int(j[b]), int(tok[b])) == want, (fi, b, (int(j[b]), int(tok[b])), want)
 
 
+@pytest.mark.parametrize("sd", [1.0, 4.0])
+def test_largest_batch_against_oracle(orc, sd):
+    """64 sessions of T = 15 at V = 32768 (the largest seeded batch: 1856 rows, several
+    waves of one CTA a row), flat (top-k binds, S skipped) and peaked (top-p binds) rows;
+    six sessions across the batch against the oracle (its filter takes about 0.15 s a
+    row here), every session's result a valid walk length and token."""
+    filt = FILTERS[1]
+    rng = np.random.default_rng(8400 + int(sd))
+    B, T, K, V = 64, 15, 14, 32768
+    P = (rng.normal(0, sd, (B, T, V))).astype(np.float32)
+    Q = (P[:, :K] + rng.normal(0, 0.3 * sd, (B, K, V))).astype(np.float32)
+    P, Q = synth.to_bf16_bits(P), synth.to_bf16_bits(Q)
+    d = np.argmax(synth.bf16_bits_to_f32(Q), axis=-1).astype(np.int32)  # the draft rows' modes
+    ua = rng.uniform(0, 1, (B, K)).astype(np.float32)
+    us = rng.uniform(0, 1, B).astype(np.float32)
+    j, tok, _ = kb.spec_accept_sampled(to_dev(P, True), to_dev(Q, True), to_dev(d), to_dev(ua), to_dev(us), **filt)
+    torch.cuda.synchronize()
+    jg, tg = j.cpu().numpy(), tok.cpu().numpy()
+    assert ((jg >= 0) & (jg <= K)).all() and ((tg >= 0) & (tg < V)).all()
+    for b in (0, 13, 31, 40, 52, 63):
+        want = orc.sampled_accept(P[b], Q[b], d[b], ua[b], float(us[b]), **f32(filt))
+        assert (int(jg[b]), int(tg[b])) == want, (b, (int(jg[b]), int(tg[b])), want)
+
+
 def test_top_p_with_thousands_of_ties(orc):
     """Rows whose top-p boundary falls inside a tie group of more than 1024 tokens: the
     kept set takes the whole group, on the device as in the oracle."""
