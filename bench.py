@@ -491,6 +491,63 @@ def run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, 
     return res
 
 
+def run_sampled(args, w, logits, K, j_out, keep_out, status, stream, dev, barrier, accept_ms):
+    """The sampled acceptance of one workload's first round: the rejection walk with
+    filtered target and draft rows (the draft rows equal the target rows, so every draft
+    is accepted: the longest walk), from caller uniforms and from the sessions' Philox
+    streams."""
+    import torch
+
+    from speculative_decode_verify_kda_gb300 import binding as kb
+    filt = dict(temperature=0.7, top_k=50, top_p=0.9, min_p=0.0)
+    lg0 = logits[0]
+    dl = lg0[:, :w.K].contiguous()
+    dr = torch.argmax(lg0[:, :w.K].float(), dim=-1).to(torch.int32).contiguous()
+    g = torch.Generator(device=dev)
+    g.manual_seed(w.seed)
+    ua = torch.rand((w.B, w.K), generator=g, device=dev)
+    us = torch.rand((w.B,), generator=g, device=dev)
+    tok = torch.empty_like(j_out)
+    Ks = max(1, min(args.sampled_steps, K))
+    for _ in range(3):
+        kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
+                               dev_status=status, stream=stream, **filt)
+    barrier()
+    a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with nvtx_range("sampled"):
+        a_.record(stream)
+        for _ in range(Ks):
+            kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
+                                   dev_status=status, stream=stream, **filt)
+        b_.record(stream)
+    barrier()
+    if int(status.item()) or int(j_out.min().item()) != w.K:
+        raise RuntimeError("sampled accept: unexpected status or walk length")
+    s_ms = a_.elapsed_time(b_) / Ks
+    # the same walk drawing from the sessions' Philox streams (counters advanced on the device)
+    seeds = torch.arange(w.B, dtype=torch.int64, device=dev) + w.seed
+    counters = torch.zeros((w.B, 2), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok, keep_out=keep_out,
+                                       dev_status=status, stream=stream, **filt)
+    barrier()
+    with nvtx_range("sampled_session"):
+        a_.record(stream)
+        for _ in range(Ks):
+            kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok,
+                                           keep_out=keep_out, dev_status=status, stream=stream, **filt)
+        b_.record(stream)
+    barrier()
+    if int(status.item()) or int(j_out.min().item()) != w.K:
+        raise RuntimeError("sampled accept (session): unexpected status or walk length")
+    ss_ms = a_.elapsed_time(b_) / Ks
+    nbytes = w.B * (2 * w.K + 1) * w.V * lg0.element_size()
+    return {"filter": filt, "walk": "every draft accepted (draft rows = target rows)",
+            "ms": s_ms, "session_ms": ss_ms, "greedy_accept_ms": accept_ms,
+            "logit_rows_per_call": w.B * (2 * w.K + 1),
+            "logits_gbs": nbytes / (s_ms * 1e-3) / 1e9}
+
+
 def run_gpu(args, rank, world, local_rank, wname, full=True):
     """One workload on this rank's GPU.  full: every section; else the timed deferred
     rounds and the e2e rounds only."""
@@ -655,6 +712,9 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
         if not args.no_e2e:
             res["e2e"] = run_e2e(args, w, R, pp, rows, logits, drafts, out, status, scratch, stream, dev, world,
                                  args.e2e_chunks, use_w, in_place=args.e2e_rows == "in_place")
+        if not args.no_sampled:
+            res["sampled_accept"] = run_sampled(args, w, logits, K, j_out, keep_out, status, stream, dev, barrier,
+                                                res["accept_ms"])
         return res
 
     # the same rounds with the rollback as its own launch: ping-pong verify, accept,
@@ -862,56 +922,10 @@ def run_gpu(args, rank, world, local_rank, wname, full=True):
                                                 "round_ms": res["separate_rollback"]["ms_per_step"],
                                                 "stash_bytes": w.L * w.B * w.H * (128 * 128 + 9 * 128) * 4}}
 
-    # sampled acceptance: the rejection walk with filtered target and draft rows; the
-    # draft rows equal the target rows, so every draft is accepted (the longest walk)
+    # sampled acceptance (run_sampled)
     if not args.no_sampled:
-        filt = dict(temperature=0.7, top_k=50, top_p=0.9, min_p=0.0)
-        lg0 = logits[0]
-        dl = lg0[:, :w.K].contiguous()
-        dr = torch.argmax(lg0[:, :w.K].float(), dim=-1).to(torch.int32).contiguous()
-        g = torch.Generator(device=dev)
-        g.manual_seed(w.seed)
-        ua = torch.rand((w.B, w.K), generator=g, device=dev)
-        us = torch.rand((w.B,), generator=g, device=dev)
-        tok = torch.empty_like(j_out)
-        Ks = max(1, min(args.sampled_steps, K))
-        for _ in range(3):
-            kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
-                                   dev_status=status, stream=stream, **filt)
-        barrier()
-        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with nvtx_range("sampled"):
-            a_.record(stream)
-            for _ in range(Ks):
-                kb.spec_accept_sampled(lg0, dl, dr, ua, us, j_out=j_out, token_out=tok, keep_out=keep_out,
-                                       dev_status=status, stream=stream, **filt)
-            b_.record(stream)
-        barrier()
-        if int(status.item()) or int(j_out.min().item()) != w.K:
-            raise RuntimeError("sampled accept: unexpected status or walk length")
-        s_ms = a_.elapsed_time(b_) / Ks
-        # the same walk drawing from the sessions' Philox streams (counters advanced on the device)
-        seeds = torch.arange(w.B, dtype=torch.int64, device=dev) + w.seed
-        counters = torch.zeros((w.B, 2), dtype=torch.int32, device=dev)
-        for _ in range(3):
-            kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok, keep_out=keep_out,
-                                           dev_status=status, stream=stream, **filt)
-        barrier()
-        with nvtx_range("sampled_session"):
-            a_.record(stream)
-            for _ in range(Ks):
-                kb.spec_accept_sampled_session(lg0, dl, dr, seeds, counters, j_out=j_out, token_out=tok,
-                                               keep_out=keep_out, dev_status=status, stream=stream, **filt)
-            b_.record(stream)
-        barrier()
-        if int(status.item()) or int(j_out.min().item()) != w.K:
-            raise RuntimeError("sampled accept (session): unexpected status or walk length")
-        ss_ms = a_.elapsed_time(b_) / Ks
-        nbytes = w.B * (2 * w.K + 1) * w.V * lg0.element_size()
-        res["sampled_accept"] = {"filter": filt, "walk": "every draft accepted (draft rows = target rows)",
-                                 "ms": s_ms, "session_ms": ss_ms, "greedy_accept_ms": res["accept_ms"],
-                                 "logit_rows_per_call": w.B * (2 * w.K + 1),
-                                 "logits_gbs": nbytes / (s_ms * 1e-3) / 1e9}
+        res["sampled_accept"] = run_sampled(args, w, logits, K, j_out, keep_out, status, stream, dev, barrier,
+                                            res["accept_ms"])
 
     # variable T per session: the window of each session's round from seeded drafter
     # confidences (glm5_conf_keep, p_min 0.5), then verify / accept / rollback with
@@ -1147,6 +1161,7 @@ def main():
                          "unit": UNIT, "steps": args.steps, "ms_per_step": r["ms_per_step"],
                          "round_kernel_ms": r["round_kernel_ms"], "accept_ms": r["accept_ms"],
                          "roofline": roofline_of(wn, r, clocks), "e2e": r.get("e2e"),
+                         "sampled_accept": r.get("sampled_accept"),
                          "gpu_launches": r["launches_per_step"] * args.steps}
     line = {
         "metric": METRIC, "value": res["rows_per_s"], "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
